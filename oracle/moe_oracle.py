@@ -1,0 +1,293 @@
+"""Plain, slow, obviously-correct CPU oracle of the MoE layer forward hot path (float64).
+
+TEST INFRASTRUCTURE ONLY. Only tests/, __graft_entry__.smoke() and bench.py's CPU-baseline leg may import
+this module. The CUDA product path never calls it, and it shares no code with that path: it reads the
+same seeded inputs (moe_inputs) and nothing else.
+
+Page keys used in the citations below:
+  [MEG6]  "Megatron-LM 分布式训练（六）：MoE 专家并行 EP 与上下文并行 CP" (swordlidev blog)
+  [EP7]   "专家并行" (formulaic docs, distributed training / 7-expert-parallel)
+  [L7]    "v6 长序列和 MoE: Context Parallel 与 Expert Parallel" (ml-interview infra-l7)
+  [B10.5] "10.5 序列并行与专家并行" (llm-fullstack-book)
+
+Every step is the plain definition, in the pages' order: router -> top-k gates -> dispatch (with optional
+capacity) -> per-expert SwiGLU FFN -> combine ([MEG6] "MoE 层的数据流"; [L7] shape table under
+"NVIDIA 原题: Implement MoE and show the dimensions"). Library primitives used as steps: numpy matmul
+(float64), numpy stable argsort, exp. Readings of points the pages leave open are noted where they apply.
+
+Parity pins (tests/test_oracle_pins.py): shape table and C=1280 of [L7]; brute-force top-k by subset
+enumeration; sum of counts = k*T; brute-force loop dispatch; stable per-expert token order; identity
+experts giving y = sum gates*x (and y = x under renormalised gates); E=1,k=1 reducing to a dense SwiGLU
+FFN checked against scalar loops; aux = alpha exactly at a uniform split and >= alpha when f = P;
+FLOP and byte counts of [L7] "EP" (6.2 ms at 400 TFLOPS, 64 MiB per dispatch). No function is unpinned.
+"""
+from __future__ import annotations
+
+import math
+
+import numpy as np
+
+SOFTMAX = "softmax"
+SOFTMAX_RENORM = "softmax_renorm"
+SIGMOID_BIAS_RENORM = "sigmoid_bias_renorm"
+
+
+# ---------------------------------------------------------------------------------------------------------
+# capacity
+# ---------------------------------------------------------------------------------------------------------
+
+def capacity(cf: float, k: int, T: int, E: int) -> int:
+    """Per-expert slot limit C = cf * k * T / E ([L7] "Capacity" bullet under the shape table:
+    1.25 * 2 * 4096 / 8 = 1280). cf = 0 means dropless (Megatron's default, same bullet) and returns 0.
+    Reading: a non-integer product is rounded up, so that C >= the formula's value."""
+    if cf <= 0:
+        return 0
+    return int(math.ceil(cf * k * T / E - 1e-9))
+
+
+# ---------------------------------------------------------------------------------------------------------
+# router: gating GEMM, gates, top-k, aux-loss terms
+# ---------------------------------------------------------------------------------------------------------
+
+def router_logits(x: np.ndarray, w_r: np.ndarray, bias: np.ndarray | None, gating: str) -> np.ndarray:
+    """logits = hidden_states @ W_router ([MEG6] "Router" step 1; [L7] table row "router": x times
+    Wr [h, E]). In the softmax modes a per-expert bias (if given) is added to the logits; under sigmoid
+    gating the bias is only a selection term ([L7] "Load balancing loss", DeepSeek-V3 aux-loss-free bias)
+    and is applied in `route`, not here."""
+    L = np.asarray(x, np.float64) @ np.asarray(w_r, np.float64)
+    if bias is not None and gating != SIGMOID_BIAS_RENORM:
+        L = L + np.asarray(bias, np.float64)[None, :]
+    return L
+
+
+def softmax(L: np.ndarray) -> np.ndarray:
+    """Row softmax in float64, with the row max subtracted first."""
+    z = np.exp(L - L.max(axis=1, keepdims=True))
+    return z / z.sum(axis=1, keepdims=True)
+
+
+def sigmoid(L: np.ndarray) -> np.ndarray:
+    return 1.0 / (1.0 + np.exp(-L))
+
+
+def route(L: np.ndarray, k: int, gating: str, bias: np.ndarray | None = None, alpha: float = 0.01) -> dict:
+    """Top-k routing and the Switch aux-loss terms ([MEG6] "Router" step 2; [L7] table row "top-k" and
+    "Load balancing loss").
+
+    selection score: the logits (softmax modes; softmax is monotone so this is selection on the
+      probabilities), or sigmoid(L) + b (sigmoid mode, b used for selection only).
+    order: descending score; equal scores -> lower expert index first (reading: the pages are silent).
+    gates: softmax mode -> the full-softmax probability of each chosen expert, not renormalised (the table
+      takes the top-k of the softmax output); softmax_renorm -> p / sum over the k chosen p;
+      sigmoid -> s / sum over the k chosen s (bias excluded).
+    counts n_e: assignments per expert before any capacity limit (sum = k*T).
+    f_e = n_e / (k*T); P_e = mean over tokens of the router probability of e (softmax modes: the full
+      softmax; sigmoid mode, reading: s_e / sum_e' s_e'); aux = alpha * E * sum_e f_e P_e.
+    margins: per token, the gaps between consecutive entries of its top-(k+1) sorted scores (covering
+      the order inside the top-k and the k / k+1 boundary)."""
+    T, E = L.shape
+    assert 1 <= k <= E
+    if gating == SIGMOID_BIAS_RENORM:
+        s = sigmoid(L)
+        score = s + (np.asarray(bias, np.float64)[None, :] if bias is not None else 0.0)
+        prob = s / s.sum(axis=1, keepdims=True)
+    else:
+        prob = softmax(L)
+        score = L
+    order = np.argsort(-score, axis=1, kind="stable")
+    ids = order[:, :k]
+    rows = np.arange(T)[:, None]
+    if gating == SOFTMAX:
+        gates = prob[rows, ids]
+    elif gating == SOFTMAX_RENORM:
+        pk = prob[rows, ids]
+        gates = pk / pk.sum(axis=1, keepdims=True)
+    elif gating == SIGMOID_BIAS_RENORM:
+        sk = s[rows, ids]
+        gates = sk / sk.sum(axis=1, keepdims=True)
+    else:
+        raise ValueError(gating)
+    counts = np.bincount(ids.ravel(), minlength=E).astype(np.int64)
+    f = counts / float(k * T)
+    P = prob.mean(axis=0)
+    aux = alpha * E * float(np.sum(f * P))
+    top = np.take_along_axis(score, order[:, :min(k + 1, E)], axis=1)
+    gaps = top[:, :-1] - top[:, 1:]
+    return dict(logits=L, ids=ids.astype(np.int32), gates=gates, counts=counts, f=f, P=P, aux=aux,
+                prob=prob, score=score, gaps=gaps)
+
+
+def near_tie_rows(gaps: np.ndarray, thresh: float) -> np.ndarray:
+    """Tokens whose top-k selection or order has a score gap below `thresh`."""
+    if gaps.shape[1] == 0:
+        return np.zeros(0, np.int64)
+    return np.nonzero(gaps.min(axis=1) < thresh)[0]
+
+
+# ---------------------------------------------------------------------------------------------------------
+# dispatch: group by expert (stable, token order), capacity mask, EP-rank-major layout
+# ---------------------------------------------------------------------------------------------------------
+
+def dispatch(ids: np.ndarray, E: int, C: int, R: int) -> dict:
+    """Token dispatch into per-expert contiguous blocks ([L7] table row "dispatch": group by expert, at
+    most C tokens per group, pad the rest; [L7] "自测" answer: over-capacity tokens are dropped, unfilled
+    slots padded; [L7] follow-up: sort tokens by expert and run one grouped GEMM; [EP7] "All2All": the
+    (E, C, M) input pre-sorted into blocks by destination expert).
+
+    slot(t, j) = number of earlier assignments (in token order t, then j) to the same expert.
+    Reading: over-capacity drops go in token order (a token never picks one expert twice, so within an
+    expert the order is by t alone). keep iff dropless (C == 0) or slot < C.
+    dropless: offsets = exclusive prefix sum of n_e, rows = k*T. capacity: offsets[e] = e*C, rows = E*C.
+    dest_row = offsets[e] + slot for kept pairs, -1 for dropped ones; src_token/src_slot invert it (-1 on
+    pad rows). EP layout ([EP7] "All2All": experts on ranks in contiguous blocks, the all-to-all being a
+    block transpose; [MEG6] "专家并行 EP"): rank r owns experts [r*E/R, (r+1)*E/R), so the expert-major
+    buffer is already rank-major; rank_offsets[r] = offsets[r*E/R], rank_counts[r] = kept rows of r."""
+    T, k = ids.shape
+    assert E % R == 0
+    flat = ids.ravel().astype(np.int64)
+    A = flat.size
+    counts = np.bincount(flat, minlength=E).astype(np.int64)
+    order = np.argsort(flat, kind="stable")           # assignments grouped by expert, token order kept
+    starts = np.concatenate([[0], np.cumsum(counts)])
+    slot = np.empty(A, np.int64)
+    slot[order] = np.arange(A) - starts[flat[order]]
+    keep = np.ones(A, bool) if C == 0 else slot < C
+    kept_counts = counts if C == 0 else np.minimum(counts, C)
+    if C == 0:
+        offsets = starts.copy()
+        rows = A
+    else:
+        offsets = np.arange(E + 1, dtype=np.int64) * C
+        rows = E * C
+    dest = np.where(keep, offsets[flat] + slot, -1)
+    src_token = np.full(rows, -1, np.int64)
+    src_slot = np.full(rows, -1, np.int64)
+    kept_idx = np.nonzero(keep)[0]
+    src_token[dest[kept_idx]] = kept_idx // k
+    src_slot[dest[kept_idx]] = kept_idx % k
+    epr = E // R
+    rank_offsets = offsets[::epr].copy()
+    rank_counts = kept_counts.reshape(R, epr).sum(axis=1)
+    return dict(counts=counts, kept_counts=kept_counts, offsets=offsets, rows=rows,
+                slot=slot.reshape(T, k), dest_row=dest.reshape(T, k), drop_mask=(~keep).reshape(T, k),
+                src_token=src_token, src_slot=src_slot, rank_offsets=rank_offsets, rank_counts=rank_counts)
+
+
+def dispatch_payload(x: np.ndarray, d: dict) -> np.ndarray:
+    """buf[rows, h]: buf[dest_row(t, j)] = x[t] for kept pairs; pad rows are zero (reading of [L7] table
+    row "dispatch", which pads the unfilled slots of each expert)."""
+    buf = np.zeros((d["rows"], x.shape[1]), dtype=x.dtype)
+    live = d["src_token"] >= 0
+    buf[live] = x[d["src_token"][live]]
+    return buf
+
+
+# ---------------------------------------------------------------------------------------------------------
+# experts: SwiGLU FFN h -> F -> h (three matrices, [L7] "dense FFN ... 3 x 4096 x 12288")
+# ---------------------------------------------------------------------------------------------------------
+
+def silu(z: np.ndarray) -> np.ndarray:
+    return z / (1.0 + np.exp(-z))
+
+
+def swiglu_ffn(X: np.ndarray, w_gate: np.ndarray, w_up: np.ndarray, w_down: np.ndarray) -> np.ndarray:
+    """out = (silu(X W_gate^T) * (X W_up^T)) W_down^T, weights in nn.Linear layout ([F,h], [F,h], [h,F]).
+    Reading: the standard SwiGLU, no biases (the page gives only its three matrices)."""
+    X = np.asarray(X, np.float64)
+    a = silu(X @ w_gate.T) * (X @ w_up.T)
+    return a @ w_down.T
+
+
+def expert_outputs(buf: np.ndarray, d: dict, weights) -> np.ndarray:
+    """eout[rows, h] for every kept row: expert e's FFN on its block [offsets[e], offsets[e]+kept[e])
+    ([MEG6] "experts ... (GroupedGEMM)"; [L7] table row "expert"). `weights(e)` returns float64
+    (W_gate, W_up, W_down). Pad rows stay zero."""
+    eout = np.zeros((d["rows"], buf.shape[1]), np.float64)
+    for e in range(len(d["kept_counts"])):
+        n = int(d["kept_counts"][e])
+        if n == 0:
+            continue
+        o = int(d["offsets"][e])
+        eout[o:o + n] = swiglu_ffn(buf[o:o + n], *weights(e))
+    return eout
+
+
+# ---------------------------------------------------------------------------------------------------------
+# combine
+# ---------------------------------------------------------------------------------------------------------
+
+def combine(eout: np.ndarray, dest_row: np.ndarray, gates: np.ndarray, shared_out: np.ndarray | None = None):
+    """y[t] = sum over kept j of gate[t, j] * eout[dest_row[t, j]] (+ shared expert output, gate 1)
+    ([L7] table row "combine": back to the original position, the k outputs summed weighted by gate;
+    [EP7] forward pass: top-2 weighted; [MEG6] data flow: "+ shared_experts"). A dropped pair adds
+    nothing (it reaches the next layer only through the residual, [L7] "自测"), and gates are not
+    renormalised after a drop (reading). No residual is added here."""
+    T, k = dest_row.shape
+    y = np.zeros((T, eout.shape[1]), np.float64) if shared_out is None else np.array(shared_out, np.float64)
+    for j in range(k):
+        kept = dest_row[:, j] >= 0
+        y[kept] += gates[kept, j][:, None] * eout[dest_row[kept, j]]
+    return y
+
+
+# ---------------------------------------------------------------------------------------------------------
+# whole layer
+# ---------------------------------------------------------------------------------------------------------
+
+def moe_layer(x, w_r, bias, weights, *, k: int, gating: str, cf: float, R: int, alpha: float = 0.01,
+              shared=None, experts: str = "swiglu") -> dict:
+    """Full forward: router -> dispatch -> experts -> combine. Inputs are float64 arrays of the
+    dtype-rounded values. `weights(e)` gives expert e's matrices; `shared()` the shared expert's (or
+    None). experts="identity" replaces each expert by the identity (eout = buf) for the pins."""
+    x = np.asarray(x, np.float64)
+    T, h = x.shape
+    E = np.asarray(w_r).shape[1]
+    L = router_logits(x, w_r, bias, gating)
+    r = route(L, k, gating, bias, alpha)
+    C = capacity(cf, k, T, E)
+    d = dispatch(r["ids"], E, C, R)
+    buf = dispatch_payload(x, d)
+    eout = buf.copy() if experts == "identity" else expert_outputs(buf, d, weights)
+    sh = swiglu_ffn(x, *shared()) if shared is not None else None
+    y = combine(eout, d["dest_row"], r["gates"], sh)
+    return dict(router=r, dispatch=d, C=C, buf=buf, eout=eout, shared_out=sh, y=y)
+
+
+def moe_layer_tokens(tokens, x, route_out: dict, disp: dict, weights, shared=None) -> np.ndarray:
+    """y for a subset of tokens, from the full router and dispatch results: for each chosen token t,
+    y[t] = sum over kept j of gate[t, j] * FFN_{e(t, j)}(x[t]) (+ shared FFN(x[t])). Dispatch copies x[t]
+    to its row unchanged, so this is the layer's output for those tokens, computed one token at a time
+    instead of for the whole batch."""
+    tokens = np.asarray(tokens, np.int64)
+    x = np.asarray(x, np.float64)
+    ids, gates, dest = route_out["ids"], route_out["gates"], disp["dest_row"]
+    y = np.zeros((tokens.size, x.shape[1]), np.float64)
+    if shared is not None:
+        y += swiglu_ffn(x[tokens], *shared())
+    by_expert: dict[int, list[tuple[int, int]]] = {}
+    for i, t in enumerate(tokens):
+        for j in range(ids.shape[1]):
+            if dest[t, j] >= 0:
+                by_expert.setdefault(int(ids[t, j]), []).append((i, j))
+    for e, pairs in sorted(by_expert.items()):
+        ii = np.array([p[0] for p in pairs])
+        jj = np.array([p[1] for p in pairs])
+        out = swiglu_ffn(x[tokens[ii]], *weights(e))
+        y[ii] += gates[tokens[ii], jj][:, None] * out
+    return y
+
+
+# ---------------------------------------------------------------------------------------------------------
+# algorithmic work (the units the roofline numbers divide by)
+# ---------------------------------------------------------------------------------------------------------
+
+def ffn_flops(rows: int, h: int, F: int) -> int:
+    """Multiply-adds of three h x F matmuls per row, 2 flops each: 6 h F per row ([L7] "EP": 6.2 ms at
+    400 TFLOPS for T=4096, k=2, h=4096, F=12288)."""
+    return 6 * h * F * rows
+
+
+def dispatch_bytes(T: int, kept: int, h: int, el: int) -> int:
+    """Bytes the dispatch must move: read T token rows, write one row per kept assignment ([L7] "EP":
+    64 MiB for one dispatch at T=4096, k=2, h=4096 in bf16 counts the written rows)."""
+    return (T + kept) * h * el

@@ -1,0 +1,106 @@
+"""Plant plausible mistakes in the oracle (on the CPU) and check that the pins catch each one.
+
+Each mutant replaces one oracle function for the duration of a test; the pin tests of
+test_oracle_pins.py are then run against the mutant and at least one must fail."""
+import numpy as np
+import pytest
+
+from oracle import moe_oracle as O
+from tests import test_oracle_pins as P
+
+_route, _dispatch, _swiglu, _combine, _capacity = O.route, O.dispatch, O.swiglu_ffn, O.combine, O.capacity
+
+
+def mut_renormalise_softmax(L, k, gating, bias=None, alpha=0.01):
+    g = O.SOFTMAX_RENORM if gating == O.SOFTMAX else gating
+    return _route(L, k, g, bias, alpha)
+
+
+def mut_ascending_order(L, k, gating, bias=None, alpha=0.01):
+    r = _route(L, k, gating, bias, alpha)
+    r["ids"] = r["ids"][:, ::-1].copy()
+    r["gates"] = r["gates"][:, ::-1].copy()
+    return r
+
+
+def mut_bias_in_sigmoid_gates(L, k, gating, bias=None, alpha=0.01):
+    r = _route(L, k, gating, bias, alpha)
+    if gating == O.SIGMOID_BIAS_RENORM and bias is not None:
+        sc = np.take_along_axis(r["score"], r["ids"].astype(np.int64), axis=1)
+        r["gates"] = sc / sc.sum(axis=1, keepdims=True)
+    return r
+
+
+def mut_aux_denominator_T(L, k, gating, bias=None, alpha=0.01):
+    r = _route(L, k, gating, bias, alpha)
+    r["aux"] *= k              # f_e = n_e / T instead of n_e / (k T)
+    return r
+
+
+def mut_drop_latest_first(ids, E, C, R):
+    """Keeps the LAST C assignments of each expert instead of the first C."""
+    d = _dispatch(ids[::-1].copy(), E, C, R)
+    T = ids.shape[0]
+    out = _dispatch(ids, E, C, R)
+    keep_rev = ~d["drop_mask"][::-1]
+    if C:
+        out["drop_mask"] = ~keep_rev
+    return out
+
+
+def mut_dispatch_unstable(ids, E, C, R):
+    d = _dispatch(ids, E, C, R)
+    for e in range(E):
+        o, n = d["offsets"][e], d["kept_counts"][e]
+        if n > 1:
+            d["src_token"][o:o + n] = d["src_token"][o:o + n][::-1].copy()
+    return d
+
+
+def mut_swap_gate_up(X, w_gate, w_up, w_down):
+    return _swiglu(X, w_up, w_gate, w_down)
+
+
+def mut_transpose_down(X, w_gate, w_up, w_down):
+    """Reads the [h, F] down matrix with the wrong layout ([F, h] row-major)."""
+    X = np.asarray(X, np.float64)
+    a = O.silu(X @ w_gate.T) * (X @ w_up.T)
+    return a @ w_down.reshape(w_down.shape[1], w_down.shape[0])
+
+
+def mut_combine_no_gate(eout, dest_row, gates, shared_out=None):
+    return _combine(eout, dest_row, np.ones_like(gates), shared_out)
+
+
+def mut_capacity_floor_over_E(cf, k, T, E):
+    return 0 if cf <= 0 else int(cf * T / E)      # forgot the k
+
+
+MUTANTS = [
+    ("route", mut_renormalise_softmax), ("route", mut_ascending_order), ("route", mut_bias_in_sigmoid_gates),
+    ("route", mut_aux_denominator_T), ("dispatch", mut_drop_latest_first), ("dispatch", mut_dispatch_unstable),
+    ("swiglu_ffn", mut_swap_gate_up), ("swiglu_ffn", mut_transpose_down), ("combine", mut_combine_no_gate),
+    ("capacity", mut_capacity_floor_over_E),
+]
+
+PINS = [
+    P.test_page3_capacity_and_shapes, P.test_capacity_rounding, P.test_softmax_gate_closed_forms,
+    P.test_topk_exact_ties_take_lower_index, P.test_sigmoid_selection_uses_bias_but_gates_do_not,
+    P.test_aux_uniform_split_equals_alpha, P.test_aux_closed_form_skewed, P.test_capacity_drops_in_token_order,
+    P.test_dispatch_stable_and_bijective, P.test_single_expert_reduces_to_dense_swiglu, P.test_swiglu_closed_forms,
+    lambda: P.test_topk_brute_force(8, 2), lambda: P.test_dispatch_brute_force(64, 8, 2, 10, 4),
+    lambda: P.test_identity_experts(O.SOFTMAX, 0), lambda: P.test_identity_experts(O.SOFTMAX_RENORM, 0),
+    P.test_token_sampled_layer_matches_full_layer,
+]
+
+
+@pytest.mark.parametrize("name,fn", MUTANTS, ids=[m[1].__name__ for m in MUTANTS])
+def test_pins_catch_mutant(name, fn, monkeypatch):
+    monkeypatch.setattr(O, name, fn)
+    caught = []
+    for pin in PINS:
+        try:
+            pin()
+        except (AssertionError, ValueError, IndexError):
+            caught.append(getattr(pin, "__name__", "lambda"))
+    assert caught, f"no pin caught mutant {fn.__name__}"
