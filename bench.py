@@ -1,0 +1,395 @@
+"""MoE layer forward benchmark on GB300: tokens/s of router -> dispatch -> grouped SwiGLU FFN -> combine.
+
+python bench.py [--gpus N] [--steps K] [--warmup W] [--impl gb300|reference] [--workload NAME]
+
+One step = one full forward of the layer over one batch of synthetic tokens (all four stages, plus the
+shared expert where the workload has one). Default workload: the page-3 worked shape (T=4096, h=4096,
+E=8, k=2, cf=1.25 -> C=1280, SwiGLU 4096->12288->4096, bf16 with fp32 accumulation). Weights and x are
+resident in HBM before the timed region; L2 (129 MB) is flushed by a 512 MiB write between steps, outside
+the per-step CUDA events. Under torchrun each rank runs its own replica on its own GPU (weak scaling, no
+data-path collective); rank 0 prints one JSON line.
+
+--impl reference times the CPU oracle (float64, numpy) on the host cores instead: each step runs the
+oracle's router and dispatch over the whole batch and its FFN + combine on a bounded sample of tokens,
+and the per-token FFN cost is extrapolated to the batch.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import moe_inputs  # noqa: E402
+
+METRIC = "MoE-layer fwd tokens/s at 1 GB300; grouped-GEMM % bf16 peak; dispatch GB/s"
+
+
+def _workload_desc(cfg, C):
+    return (f"{cfg.name}: T={cfg.T} h={cfg.h} E={cfg.E} k={cfg.k} F={cfg.F} gating={cfg.gating} "
+            + (f"cf={cfg.cf} (C={C})" if cfg.cf else "dropless") + f" R={cfg.R} shared={cfg.n_shared} {cfg.dtype}")
+
+
+def _peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as fh:
+            p = json.load(fh)
+        return p["hbm_gbs"], p["bf16_tflops"], p.get("bf16_tflops_sustained"), "measured"
+    except Exception:
+        return 6800.0, 1900.0, 1700.0, "fallback"
+
+
+def _smi_id(local):
+    """nvidia-smi -i argument of this process's GPU (its UUID; nvidia-smi ignores CUDA_VISIBLE_DEVICES)."""
+    import torch
+    try:
+        u = str(torch.cuda.get_device_properties(local).uuid)
+        return u if u.startswith("GPU-") else "GPU-" + u
+    except Exception:
+        return str(local)
+
+
+class ClockSampler:
+    """nvidia-smi sampling of SM clocks and throttle reasons during the timed region."""
+
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,clocks_event_reasons.hw_slowdown,"
+              "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+              "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device_index: int):
+        self.idx = device_index
+        self.proc = None
+        self.lines: list[str] = []
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.idx), f"--query-gpu={self.FIELDS}",
+                                          "--format=csv,noheader,nounits", "-lms", "100"],
+                                         stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.t = threading.Thread(target=self._read, daemon=True)
+            self.t.start()
+        except Exception:
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def __exit__(self, *a):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+
+    def summary(self):
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in self.lines:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 8:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                mx.append(float(parts[1]))
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[4:8]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"], "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# ---------------------------------------------------------------------------------------------------------
+# host inputs
+# ---------------------------------------------------------------------------------------------------------
+
+def host_inputs(cfg, seed=0):
+    x = moe_inputs.make_x(cfg, seed)
+    w_r, bias = moe_inputs.make_router(cfg, seed)
+    wg, wu, wd = moe_inputs.all_expert_weights(cfg, seed)
+    shared = None
+    if cfg.n_shared:
+        shared = tuple(a[0] for a in moe_inputs.all_expert_weights(cfg, seed, shared=True))
+    return dict(x=x, w_r=w_r, bias=bias, wg=wg, wu=wu, wd=wd, shared=shared)
+
+
+# ---------------------------------------------------------------------------------------------------------
+# CPU oracle arm (reference arm and cpu_baseline)
+# ---------------------------------------------------------------------------------------------------------
+
+def oracle_step(cfg, inp, w64, sample_tokens):
+    """One bounded oracle step: router + dispatch over all T tokens, FFN + combine for `sample_tokens`.
+    Returns (seconds for router+dispatch, seconds for the sampled FFN)."""
+    from oracle import moe_oracle as O
+    t0 = time.perf_counter()
+    x64 = moe_inputs.to_f64(inp["x"], cfg.dtype)
+    L = O.router_logits(x64, moe_inputs.to_f64(inp["w_r"], cfg.dtype), inp["bias"], cfg.gating)
+    r = O.route(L, cfg.k, cfg.gating, inp["bias"], cfg.alpha)
+    d = O.dispatch(r["ids"], cfg.E, O.capacity(cfg.cf, cfg.k, cfg.T, cfg.E), cfg.R)
+    t1 = time.perf_counter()
+    O.moe_layer_tokens(sample_tokens, x64, r, d, lambda e: w64[e], shared=w64.get("shared"))
+    t2 = time.perf_counter()
+    return t1 - t0, t2 - t1
+
+
+def decode_weights(cfg, inp):
+    w64 = {e: (moe_inputs.to_f64(inp["wg"][e], cfg.dtype), moe_inputs.to_f64(inp["wu"][e], cfg.dtype),
+               moe_inputs.to_f64(inp["wd"][e], cfg.dtype)) for e in range(cfg.E)}
+    if inp["shared"] is not None:
+        sh = tuple(moe_inputs.to_f64(w, cfg.dtype) for w in inp["shared"])
+        w64["shared"] = lambda: sh
+    return w64
+
+
+def blas_threads():
+    try:
+        from threadpoolctl import threadpool_info
+        n = [i.get("num_threads") for i in threadpool_info() if i.get("user_api") == "blas"]
+        if n:
+            return int(max(n))
+    except Exception:
+        pass
+    return os.cpu_count() or 1
+
+
+def oracle_throughput(cfg, inp, w64, steps, n_sample, seed=1):
+    """Tokens/s of the oracle: T / (router+dispatch time + sampled FFN time scaled to T tokens)."""
+    rng = np.random.default_rng(seed)
+    vals = []
+    for _ in range(steps):
+        toks = np.sort(rng.choice(cfg.T, size=n_sample, replace=False))
+        t_rd, t_ffn = oracle_step(cfg, inp, w64, toks)
+        vals.append(cfg.T / (t_rd + t_ffn * cfg.T / n_sample))
+    return vals
+
+
+def run_reference(args, cfg, C):
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return
+    inp = host_inputs(cfg)
+    w64 = decode_weights(cfg, inp)
+    n_sample = args.sample_tokens
+    oracle_throughput(cfg, inp, w64, args.warmup, n_sample)
+    t0 = time.perf_counter()
+    vals = oracle_throughput(cfg, inp, w64, args.steps, n_sample)
+    wall = time.perf_counter() - t0
+    v = statistics.median(vals)
+    cores = blas_threads()
+    sample = (f"per step: oracle router+dispatch over all {cfg.T} tokens, FFN+combine on {n_sample} random tokens "
+              f"(float64 numpy), FFN cost scaled to {cfg.T} tokens; median of {args.steps} steps")
+    line = {"impl": "reference", "metric": METRIC, "value": v, "unit": "tokens/s", "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": wall / args.steps * 1e3,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": _workload_desc(cfg, C), "l2": "n/a (CPU)"},
+            "cpu_baseline": {"value": v, "unit": "tokens/s", "cores": cores, "kind": "oracle", "sample": sample},
+            "e2e": {"value": v, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+# ---------------------------------------------------------------------------------------------------------
+# GPU arm
+# ---------------------------------------------------------------------------------------------------------
+
+def run_gpu(args, cfg, C):
+    import torch
+    import torch.distributed as dist
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+
+    from top_routing_dispatch_moe_gb300 import moe
+    from top_routing_dispatch_moe_gb300.layer import MoELayer
+
+    inp = host_inputs(cfg)
+
+    def up(a):
+        if cfg.dtype == "bf16":
+            return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).to(dev).view(torch.bfloat16)
+        return torch.from_numpy(np.ascontiguousarray(a)).to(dev)
+
+    layer = MoELayer(T=cfg.T, h=cfg.h, E=cfg.E, k=cfg.k, F=cfg.F, gating=cfg.gating, cf=cfg.cf, R=cfg.R,
+                     alpha=cfg.alpha, w_r=up(inp["w_r"]),
+                     bias=torch.from_numpy(inp["bias"]).to(dev) if inp["bias"] is not None else None,
+                     w_gate=up(inp["wg"]), w_up=up(inp["wu"]), w_down=up(inp["wd"]),
+                     shared=tuple(up(w) for w in inp["shared"]) if inp["shared"] is not None else None, device=dev)
+    x = up(inp["x"])
+    flush = torch.empty(512 * 2**20, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream()
+
+    for _ in range(args.warmup):
+        layer.forward(x)
+        flush.zero_()
+    torch.cuda.synchronize()
+    assert moe.moe_check_device_error() == moe.MOE_OK, moe.moe_last_error_string()
+    kept = int(layer.d_out["kept_counts"].sum().item())
+
+    # ---- device-resident timed region
+    events: dict = {}
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    launches0 = moe.moe_launch_count()
+    with ClockSampler(_smi_id(local)) as clk:
+        t_wall0 = time.perf_counter()
+        for _ in range(args.steps):
+            layer.forward(x, events=events)
+            flush.zero_()
+        torch.cuda.synchronize()
+        t_wall = time.perf_counter() - t_wall0
+    if world > 1:
+        dist.barrier()
+    launches = moe.moe_launch_count() - launches0
+    assert moe.moe_check_device_error() == moe.MOE_OK, moe.moe_last_error_string()
+
+    stage_names = [s for s in MoELayer.STAGES if s in events]
+    order = ["start"] + stage_names
+    stage_ms = {s: [] for s in stage_names}
+    step_ms = []
+    for i in range(args.steps):
+        for a, b in zip(order[:-1], order[1:]):
+            stage_ms[b].append(events[a][i].elapsed_time(events[b][i]))
+        step_ms.append(events["start"][i].elapsed_time(events[order[-1]][i]))
+    ms = float(np.mean(step_ms))
+    if world > 1:
+        t = torch.tensor([ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms = float(t.item())
+    value = world * cfg.T / (ms * 1e-3)
+
+    # ---- end-to-end through the public API: pinned host x -> device, forward, y -> pinned host
+    x_host = torch.from_numpy(np.ascontiguousarray(inp["x"]).view(np.int16) if cfg.dtype == "bf16"
+                              else np.ascontiguousarray(inp["x"])).pin_memory()
+    y_host = torch.empty(x_host.shape, dtype=x_host.dtype).pin_memory()
+    x_dev = torch.empty(x_host.shape, dtype=x_host.dtype, device=dev)
+    e2e_ms = []
+    for i in range(args.warmup + args.steps):
+        flush.zero_()
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        x_dev.copy_(x_host, non_blocking=True)
+        y = layer.forward(x_dev.view(torch.bfloat16) if cfg.dtype == "bf16" else x_dev)
+        y_host.copy_(y.view(torch.int16) if cfg.dtype == "bf16" else y, non_blocking=True)
+        e1.record(stream)
+        e1.synchronize()
+        if i >= args.warmup:
+            e2e_ms.append(e0.elapsed_time(e1))
+    e2e = float(np.mean(e2e_ms))
+    if world > 1:
+        t = torch.tensor([e2e], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        e2e = float(t.item())
+    io_bytes = cfg.T * cfg.h * cfg.el
+
+    # ---- roofline of the dominant kernel (the up/gate grouped GEMM) and the bandwidth stages
+    hbm, bf16_burst, bf16_sus, peak_src = _peaks()
+    ug_ms = float(np.mean(stage_ms["up_gate"]))
+    dn_ms = float(np.mean(stage_ms["down"]))
+    ug_flops = 4.0 * kept * cfg.h * cfg.F
+    ffn_flops = 6.0 * kept * cfg.h * cfg.F + (6.0 * cfg.T * cfg.h * cfg.F if cfg.n_shared else 0.0)
+    ffn_ms = ug_ms + dn_ms + sum(float(np.mean(stage_ms[s])) for s in ("shared_up_gate", "shared_down") if s in stage_ms)
+    ug_tflops = ug_flops / (ug_ms * 1e-3) / 1e12
+    disp_bytes = (cfg.T + kept) * cfg.h * cfg.el
+    comb_bytes = (kept + cfg.T + (cfg.T if cfg.n_shared else 0)) * cfg.h * cfg.el
+    disp_gbs = disp_bytes / (float(np.mean(stage_ms["dispatch"])) * 1e-3) / 1e9
+    comb_gbs = comb_bytes / (float(np.mean(stage_ms["combine"])) * 1e-3) / 1e9
+    traffic = None
+    try:
+        with open(os.path.join(ROOT, "profiles", "traffic.json")) as fh:
+            tr = json.load(fh).get(cfg.name, {})
+        if tr.get("kernel_source_hash") == kernel_hash():
+            traffic = tr.get("up_gate_dram_bytes")
+    except Exception:
+        pass
+    roofline = {"bound": "tensor", "kernel": "up/gate grouped GEMM (SwiGLU epilogue)", "achieved": ug_tflops,
+                "peak": bf16_burst, "unit": "TFLOP/s", "frac": ug_tflops / bf16_burst, "traffic": traffic,
+                "peak_source": f"{peak_src} bf16 burst"}
+
+    line = {"metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "bf16" if cfg.dtype == "bf16" else "f32", "data": "synthetic",
+            "config": {"workload": _workload_desc(cfg, C), "global_batch": cfg.T * world, "tokens_per_gpu": cfg.T,
+                       "parallelism": f"replicas x{world}", "l2": "flushed between steps (512 MiB write)",
+                       "kept_assignments": kept},
+            "roofline": roofline,
+            "e2e": {"value": world * cfg.T / (e2e * 1e-3), "unit": "tokens/s", "h2d_bytes_per_step": io_bytes,
+                    "d2h_bytes_per_step": io_bytes, "ms_per_step": e2e},
+            "gpu_launches": int(launches),
+            "stages_ms": {s: float(np.mean(v)) for s, v in stage_ms.items()},
+            "expert_tflops": ffn_flops / (ffn_ms * 1e-3) / 1e12,
+            "grouped_gemm_pct_bf16_peak": 100.0 * ffn_flops / (ffn_ms * 1e-3) / 1e12 / bf16_burst,
+            "dispatch_gbs": disp_gbs, "dispatch_pct_hbm": 100.0 * disp_gbs / hbm,
+            "combine_gbs": comb_gbs, "combine_pct_hbm": 100.0 * comb_gbs / hbm,
+            "wall_s_timed_region": t_wall}
+    line["clocks"] = clk.summary()
+
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        w64 = decode_weights(cfg, inp)
+        vals = oracle_throughput(cfg, inp, w64, 1, args.baseline_tokens)
+        line["cpu_baseline"] = {"value": vals[0], "unit": "tokens/s", "cores": blas_threads(), "kind": "oracle",
+                                "sample": f"oracle router+dispatch over all {cfg.T} tokens, FFN+combine on "
+                                          f"{args.baseline_tokens} random tokens (float64 numpy), FFN cost scaled "
+                                          f"to {cfg.T} tokens"}
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+
+
+def kernel_hash():
+    import hashlib
+    h = hashlib.sha256()
+    d = os.path.join(ROOT, "top_routing_dispatch_moe_gb300", "csrc")
+    for f in sorted(os.listdir(d)):
+        if f.startswith("ffn"):
+            h.update(open(os.path.join(d, f), "rb").read())
+    return h.hexdigest()[:16]
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
+    ap.add_argument("--workload", default="page3_cf1.25", choices=moe_inputs.CONFIG_ORDER)
+    ap.add_argument("--sample-tokens", type=int, default=32, help="oracle tokens per reference-arm step")
+    ap.add_argument("--baseline-tokens", type=int, default=128, help="oracle tokens of the cpu_baseline sample")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    assert args.warmup >= 3, "at least 3 warm-up steps"
+    cfg = moe_inputs.get_config(args.workload)
+    C = 0
+    if cfg.cf:
+        import math
+        C = int(math.ceil(cfg.cf * cfg.k * cfg.T / cfg.E - 1e-9))
+    if args.impl == "reference":
+        run_reference(args, cfg, C)
+    else:
+        from top_routing_dispatch_moe_gb300 import build
+        build.build()
+        run_gpu(args, cfg, C)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,188 @@
+/*
+ * moe.h: C ABI of the GB300 (sm_103a) MoE layer forward hot path.
+ *
+ *   router -> dispatch -> grouped SwiGLU expert FFN -> combine
+ *
+ * The steps follow the MoE data flow of "Megatron-LM 分布式训练（六）：MoE 专家并行 EP 与上下文并行 CP"
+ * (section "MoE 层的数据流") and the shape table of "v6 长序列和 MoE: Context Parallel 与 Expert Parallel"
+ * (section "NVIDIA 原题: Implement MoE and show the dimensions"):
+ *   x [T,h] -> router logits [T,E] -> top-k [T,k] -> dispatch [E,C,h] (or dropless blocks) -> expert FFN
+ *   -> combine y [T,h].
+ *
+ * Conventions (every entry point):
+ *   - Tensor arguments are DEVICE pointers owned by the caller, row-major with the last dimension
+ *     contiguous. The library never allocates memory: calls that need scratch take a caller-provided
+ *     device workspace whose size the matching *_workspace_size() function returns.
+ *   - `stream` is a cudaStream_t passed as void* (NULL = the legacy default stream). Every call only
+ *     enqueues work on that stream; none synchronizes the host.
+ *   - Return value: MOE_OK, or an error code with a message retrievable by moe_last_error_string()
+ *     (per host thread). Argument checks happen before anything is enqueued, so a call that returns
+ *     MOE_ERR_INVALID_ARG / MOE_ERR_UNSUPPORTED / MOE_ERR_WORKSPACE has not touched device memory.
+ *     MOE_ERR_CUDA reports a failed launch. Errors detected on the device (a bounded wait that ran out)
+ *     are latched in a device word and reported by moe_check_device_error().
+ *   - dtype: MOE_F32 (fp32 in/out, fp32 arithmetic) or MOE_BF16 (bf16 tensors, fp32 accumulation).
+ *     Gates, logits, f, P and aux are always fp32.
+ *   - Sizes: T >= 0; 1 <= k <= min(E, 16); 1 <= E <= 1024; h % 8 == 0; F % 8 == 0. All tensor pointers
+ *     must be 16-byte aligned.
+ */
+#ifndef MOE_GB300_H
+#define MOE_GB300_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+enum moe_status {
+    MOE_OK = 0,
+    MOE_ERR_INVALID_ARG = 1,  /* null / misaligned pointer, size out of range */
+    MOE_ERR_UNSUPPORTED = 2,  /* dtype, gating mode or shape this build does not handle */
+    MOE_ERR_WORKSPACE = 3,    /* workspace smaller than *_workspace_size() */
+    MOE_ERR_CUDA = 4,         /* a CUDA launch or runtime call failed */
+    MOE_ERR_TIMEOUT = 5       /* a bounded device-side wait ran out (see moe_check_device_error) */
+};
+
+enum moe_dtype { MOE_F32 = 0, MOE_BF16 = 1 };
+
+/* Gating modes ("Megatron-LM ... （六）", section "Router": top-k on the logits with softmax or sigmoid
+ * weights; "v6 长序列和 MoE ...", "Load balancing loss" bullet: DeepSeek-V3 selection-only bias). */
+enum moe_gating {
+    MOE_GATING_SOFTMAX = 0,            /* gate = full-softmax probability of the chosen expert */
+    MOE_GATING_SOFTMAX_RENORM = 1,     /* gate = softmax probability / sum over the k chosen */
+    MOE_GATING_SIGMOID_BIAS_RENORM = 2 /* select on sigmoid(L)+bias; gate = s / sum_chosen s */
+};
+
+/* Rows per tile of the device tile schedule written by moe_dispatch and read by the expert FFN. */
+#define MOE_TILE_M 128
+
+/* ---------------------------------------------------------------------------------------------------
+ * moe_router: gating GEMM, top-k, gates, per-expert counts and Switch aux-loss terms.
+ *   "Megatron-LM ... （六）", section "Router" (logits = hidden_states @ W_router, then top-k with
+ *   softmax/sigmoid weights); "v6 长序列和 MoE ...", table rows "router" and "top-k", and the
+ *   "Load balancing loss" bullet (aux = alpha * E * sum_i f_i P_i).
+ *
+ *   x        [T,h]  dtype        tokens
+ *   w_r      [h,E]  dtype        router weight
+ *   bias     [E]    fp32 or NULL softmax modes: added to the logits; sigmoid mode: selection only
+ *   logits   [T,E]  fp32 or NULL x @ w_r (+ bias in softmax modes)
+ *   topk_ids [T,k]  int32        chosen experts, by descending selection score, ties -> lower index
+ *   gates    [T,k]  fp32         gate of each chosen expert (see enum moe_gating)
+ *   counts   [E]    int32        assignments per expert before any capacity limit (sum = k*T)
+ *   f        [E]    fp32         counts / (k*T)
+ *   P        [E]    fp32         mean over tokens of the router probability (softmax modes: the full
+ *                                softmax; sigmoid mode: s_e / sum_e' s_e')
+ *   aux      [1]    fp32         alpha * E * sum_e f_e * P_e
+ *   Deterministic: the same inputs give bitwise-identical outputs on every call.
+ * ------------------------------------------------------------------------------------------------- */
+size_t moe_router_workspace_size(int T, int h, int E, int k, int dtype);
+int moe_router(const void* x, const void* w_r, const float* bias, int T, int h, int E, int k, int dtype,
+               int gating, float alpha, float* logits, int32_t* topk_ids, float* gates, int32_t* counts,
+               float* f, float* P, float* aux, void* ws, size_t ws_bytes, void* stream);
+
+/* ---------------------------------------------------------------------------------------------------
+ * moe_dispatch: histogram, exclusive scan, stable scatter, capacity mask, permutation indices, EP send
+ * layout and the expert FFN's tile schedule.
+ *   "v6 长序列和 MoE ...", table row "dispatch" (group by expert, at most C per expert, pad) and the
+ *   "Capacity" bullet (C = cf*k*T/E; tokens over capacity are dropped); the follow-up note there (sort
+ *   tokens by expert, one grouped GEMM); "专家并行" (formulaic), section "All2All" (the (E,C,M) buffer
+ *   pre-sorted by destination expert; the all-to-all as a block transpose).
+ *
+ *   capacity  0 = dropless (rows = k*T, offsets = exclusive scan of counts), else C (rows = E*C,
+ *             offsets[e] = e*C, pad rows zero). moe_dispatch_rows() returns rows.
+ *   slot(t,j) = number of earlier assignments to the same expert in token order; kept iff dropless or
+ *             slot < C.
+ *   x           [T,h] dtype      tokens
+ *   topk_ids    [T,k] int32      from moe_router (values in [0,E); a token never repeats an expert)
+ *   buf         [rows,h] dtype   buf[dest_row[t,j]] = x[t]; pad rows zero
+ *   offsets     [E+1] int32      first row of each expert block (offsets[E] = rows)
+ *   kept_counts [E]   int32      rows used by each expert
+ *   dest_row    [T,k] int32      row of (t,j) in buf, -1 if dropped
+ *   drop_mask   [T,k] uint8      1 if (t,j) was dropped
+ *   src_token   [rows] int32     token of each row, -1 on pad rows
+ *   src_slot    [rows] int32     j of each row, -1 on pad rows
+ *   rank_counts [R]   int32      kept rows of each virtual EP rank (rank r owns experts
+ *                                [r*E/R, (r+1)*E/R); the expert-major buffer is already rank-major)
+ *   rank_offsets[R+1] int32      first row of each rank block (= offsets[r*E/R])
+ *   tile_sched  moe_tile_sched_bytes() bytes, opaque: per-expert MOE_TILE_M-row tiles for the FFN
+ *   Deterministic and stable (token order inside every expert block).
+ * ------------------------------------------------------------------------------------------------- */
+size_t moe_dispatch_rows(int T, int E, int k, int capacity);
+size_t moe_tile_sched_bytes(int T, int E, int k, int capacity);
+size_t moe_dispatch_workspace_size(int T, int E, int k, int capacity);
+int moe_dispatch(const void* x, const int32_t* topk_ids, int T, int h, int E, int k, int capacity,
+                 int num_ranks, int dtype, void* buf, int32_t* offsets, int32_t* kept_counts,
+                 int32_t* dest_row, uint8_t* drop_mask, int32_t* src_token, int32_t* src_slot,
+                 int32_t* rank_counts, int32_t* rank_offsets, int32_t* tile_sched, void* ws,
+                 size_t ws_bytes, void* stream);
+
+/* Writes a tile schedule for one dense group of `rows` rows (offsets {0, rows}): the shared expert of a
+ * DeepSeek-V3-shaped layer runs through the expert FFN with E = 1 and this schedule. */
+int moe_dense_tile_sched(int rows, int32_t* tile_sched, void* stream);
+
+/* ---------------------------------------------------------------------------------------------------
+ * moe_pack_expert_weights: one-time repack of the SwiGLU expert weights for the grouped GEMM.
+ *   "v6 长序列和 MoE ...", section "MoE" (a SwiGLU FFN has three h x F matrices).
+ *   w_gate [E,F,h], w_up [E,F,h], w_down [E,h,F] (nn.Linear layout, dtype) -> packed
+ *   (moe_packed_weights_bytes() bytes, opaque): gate and up rows interleaved in blocks of 128 so that one
+ *   GEMM tile computes both halves of the SwiGLU for the same 128 columns of F, and w_down.
+ * ------------------------------------------------------------------------------------------------- */
+size_t moe_packed_weights_bytes(int E, int h, int F, int dtype);
+int moe_pack_expert_weights(const void* w_gate, const void* w_up, const void* w_down, int E, int h, int F,
+                            int dtype, void* packed, void* stream);
+
+/* ---------------------------------------------------------------------------------------------------
+ * Grouped SwiGLU expert FFN ("Megatron-LM ... （六）", data flow: experts run as one GroupedGEMM;
+ * "v6 长序列和 MoE ...", table row "expert": each expert runs its own FFN h -> F -> h).
+ *   For every expert e and every kept row r in [offsets[e], offsets[e] + kept_counts[e]):
+ *     act[r]  = silu(buf[r] @ W_gate[e]^T) * (buf[r] @ W_up[e]^T)     [rows,F] dtype
+ *     eout[r] = act[r] @ W_down[e]^T                                    [rows,h] dtype
+ *   Rows outside the kept ranges are not written. bf16 runs on the tcgen05 tensor cores (bf16 operands,
+ *   fp32 accumulation in tensor memory; act is stored in bf16); fp32 runs on the CUDA cores.
+ *   moe_expert_up_gate and moe_expert_down are the two steps; moe_expert_ffn runs both with act in the
+ *   workspace.
+ * ------------------------------------------------------------------------------------------------- */
+int moe_expert_up_gate(const void* buf, const int32_t* tile_sched, const void* packed_w, int E, int h, int F,
+                       int rows, int dtype, void* act, void* stream);
+int moe_expert_down(const void* act, const int32_t* tile_sched, const void* packed_w, int E, int h, int F,
+                    int rows, int dtype, void* eout, void* stream);
+size_t moe_expert_ffn_workspace_size(int rows, int F, int dtype);
+int moe_expert_ffn(const void* buf, const int32_t* tile_sched, const void* packed_w, int E, int h, int F,
+                   int rows, int dtype, void* eout, void* ws, size_t ws_bytes, void* stream);
+
+/* ---------------------------------------------------------------------------------------------------
+ * moe_combine: un-permute and gate-weighted sum of the k expert outputs.
+ *   "v6 长序列和 MoE ...", table row "combine" (back to the original position, k outputs summed weighted
+ *   by gate); "专家并行" (formulaic), forward pass (top-2 weighted merge); "Megatron-LM ... （六）" data flow
+ *   (+ shared experts).
+ *   y[t] = shared_out[t] (if not NULL) + sum over j with dest_row[t,j] >= 0 of gates[t,j] * eout[dest_row[t,j]]
+ *   accumulated in fp32 in ascending j, rounded once to dtype. Dropped pairs add nothing; no residual.
+ *   eout [rows,h] dtype; dest_row [T,k] int32; gates [T,k] fp32; shared_out [T,h] dtype or NULL;
+ *   y [T,h] dtype. Deterministic (no atomics).
+ * ------------------------------------------------------------------------------------------------- */
+int moe_combine(const void* eout, const int32_t* dest_row, const float* gates, const void* shared_out, int T,
+                int h, int k, int dtype, void* y, void* stream);
+
+/* ---------------------------------------------------------------------------------------------------
+ * Errors and diagnostics.
+ * ------------------------------------------------------------------------------------------------- */
+/* Message of the last failing call on this host thread ("" if none). */
+const char* moe_last_error_string(void);
+/* Synchronizes `stream`, then reads and clears the device error word of the current device. Returns
+ * MOE_OK, MOE_ERR_TIMEOUT if a bounded device-side wait ran out since the last check, or MOE_ERR_CUDA. */
+int moe_check_device_error(void* stream);
+/* Sets the iteration limit of the bounded device-side waits (mbarrier polls) of later launches;
+ * spins <= 0 restores the default. A small limit makes those waits give up early, which exercises the
+ * error path: the kernel drains its copies in flight, frees its tensor memory, latches MOE_ERR_TIMEOUT
+ * and returns. */
+void moe_set_wait_limit(long long spins);
+/* Number of kernels this process has launched through the library (all devices, all threads). */
+unsigned long long moe_launch_count(void);
+/* Library version string. */
+const char* moe_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* MOE_GB300_H */

@@ -1,0 +1,86 @@
+"""CPU checks of the C-ABI library: it loads, exports every entry point include/moe.h declares, and its
+size functions and host-side argument checks behave as documented (no compute calls without a GPU)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def _declared():
+    src = open(os.path.join(ROOT, "include", "moe.h")).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"\b(moe_[a-z0-9_]+)\s*\(", src)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from top_routing_dispatch_moe_gb300 import build
+    build.build()
+    from top_routing_dispatch_moe_gb300 import moe
+    return moe
+
+
+def test_exports_every_declared_symbol(lib):
+    names = _declared()
+    assert len(names) >= 18
+    raw = lib.raw_lib()
+    for n in names:
+        assert hasattr(raw, n), n
+    assert sorted(lib.EXPORTED) == names
+    assert "sm_103a" in lib.moe_version()
+
+
+def test_size_functions(lib):
+    assert lib.moe_dispatch_rows(4096, 8, 2, 1280) == 8 * 1280
+    assert lib.moe_dispatch_rows(4096, 8, 2, 0) == 8192
+    # tile schedule: header + prefix (aligned to 4 words) + 4 words per tile, at most rows/128 + E tiles
+    E = 8
+    words = ((2 + E + 1 + 3) & ~3) + 4 * ((8 * 1280 + 127) // 128 + E)
+    assert lib.moe_tile_sched_bytes(4096, 8, 2, 1280) == 4 * words
+    Fp = 12288
+    assert lib.moe_packed_weights_bytes(8, 4096, 12288, lib.MOE_BF16) == 8 * 2 * Fp * 4096 * 2 + 8 * 4096 * 12288 * 2
+    assert lib.moe_packed_weights_bytes(1, 8, 8, lib.MOE_F32) == 2 * 128 * 8 * 4 + 8 * 8 * 4
+    assert lib.moe_expert_ffn_workspace_size(10240, 12288, lib.MOE_BF16) == 10240 * 12288 * 2
+    assert lib.moe_router_workspace_size(4096, 4096, 8, 2, lib.MOE_BF16) > 0
+    assert lib.moe_dispatch_workspace_size(4096, 8, 2, 0) >= 8 * 4 * (4096 // 512)
+
+
+def test_host_checks_reject_before_any_cuda_call(lib):
+    raw = lib.raw_lib()
+    P = ctypes.c_void_p
+    n = None
+    # bad dtype
+    assert raw.moe_router(n, n, n, 4, 16, 4, 2, 7, 0, 0.0, n, n, n, n, n, n, n, n, 0, n) == lib.MOE_ERR_UNSUPPORTED
+    assert "dtype" in lib.moe_last_error_string()
+    # bad gating
+    assert raw.moe_router(n, n, n, 4, 16, 4, 2, 1, 9, 0.0, n, n, n, n, n, n, n, n, 0, n) == lib.MOE_ERR_UNSUPPORTED
+    # h not a multiple of 8
+    assert raw.moe_router(n, n, n, 4, 12, 4, 2, 1, 0, 0.0, n, n, n, n, n, n, n, n, 0, n) == lib.MOE_ERR_INVALID_ARG
+    # k > E
+    assert raw.moe_router(n, n, n, 4, 16, 4, 5, 1, 0, 0.0, n, n, n, n, n, n, n, n, 0, n) == lib.MOE_ERR_INVALID_ARG
+    # null outputs
+    assert raw.moe_router(n, n, n, 4, 16, 4, 2, 1, 0, 0.0, n, n, n, n, n, n, n, n, 0, n) == lib.MOE_ERR_INVALID_ARG
+    # misaligned pointer
+    bad = P(0x1003)
+    ok = P(0x1000)
+    assert raw.moe_router(bad, ok, n, 4, 16, 4, 2, 1, 0, 0.0, n, ok, ok, ok, ok, ok, ok, n, 0,
+                          n) == lib.MOE_ERR_INVALID_ARG
+    # workspace too small (checked before launching)
+    assert raw.moe_router(ok, ok, n, 4, 16, 4, 2, 1, 0, 0.0, n, ok, ok, ok, ok, ok, ok, ok, 1,
+                          n) == lib.MOE_ERR_WORKSPACE
+    # dispatch: ranks must divide E; capacity >= 0
+    args = [ok, ok, 4, 16, 8, 2, 0, 3, 1] + [ok] * 10 + [ok, 1 << 20, n]
+    assert raw.moe_dispatch(*args) == lib.MOE_ERR_INVALID_ARG
+    args[6], args[7] = -1, 2
+    assert raw.moe_dispatch(*args) == lib.MOE_ERR_INVALID_ARG
+    # FFN: F % 8
+    assert raw.moe_expert_ffn(ok, ok, ok, 8, 16, 12, 4, 1, ok, ok, 1 << 20, n) == lib.MOE_ERR_INVALID_ARG
+    # FFN workspace
+    assert raw.moe_expert_ffn(ok, ok, ok, 8, 16, 16, 4, 1, ok, ok, 8, n) == lib.MOE_ERR_WORKSPACE
+    # combine: dtype
+    assert raw.moe_combine(ok, ok, ok, n, 4, 16, 2, 5, ok, n) == lib.MOE_ERR_UNSUPPORTED
+    # pack: F % 8
+    assert raw.moe_pack_expert_weights(ok, ok, ok, 2, 16, 12, 1, ok, n) == lib.MOE_ERR_INVALID_ARG

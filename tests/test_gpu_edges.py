@@ -1,0 +1,140 @@
+"""GPU edge cases of the C-ABI path against the oracle: empty input, single token, k = E, one expert,
+empty experts, minimum and ragged hidden sizes, everything dropped but the first C, and the device-side
+check of out-of-range expert ids."""
+import numpy as np
+import pytest
+
+import moe_inputs
+from oracle import moe_oracle as O
+from tests import cases
+
+pytestmark = pytest.mark.gpu
+
+
+def _run(cfg, bias=None):
+    import torch
+    inp = cases.router_inputs(cfg, bias=bias)
+    wg, wu, wd = moe_inputs.all_expert_weights(cfg)
+    shared = tuple(a[0] for a in moe_inputs.all_expert_weights(cfg, shared=True)) if cfg.n_shared else None
+    ref = cases.oracle_layer(cfg, inp, cases.weights_fn_from(cfg, wg, wu, wd),
+                             (lambda: tuple(moe_inputs.to_f64(w, cfg.dtype) for w in shared)) if shared else None)
+    layer = cases.build_gpu_layer(cfg, inp, wg, wu, wd, shared)
+    y = layer.forward(cases.to_device(inp["x"], cfg))
+    torch.cuda.synchronize()
+    return inp, ref, layer, cases.from_device(y, cfg)
+
+
+@pytest.mark.parametrize("over", [
+    dict(T=1, E=4, k=4, R=2),                 # single token, k = E
+    dict(T=3, E=1, k=1, R=1),                 # one expert: a dense SwiGLU layer
+    dict(T=10, E=64, k=2, R=8),               # most experts empty
+    dict(T=129, h=8, F=8),                    # minimum hidden size, F below one 128 block
+    dict(T=257, h=264, F=136),                # ragged vector tails in h and F
+])
+@pytest.mark.parametrize("base", ["tiny_fp32", "page3_cf1.25"])
+def test_small_shapes(base, over):
+    cfg = moe_inputs.get_config(base, **dict(dict(h=128, F=256, T=64), **over))
+    if cfg.E % cfg.R:
+        cfg = moe_inputs.get_config(base, **dict(dict(h=128, F=256, T=64), **over, R=1))
+    inp, ref, layer, y = _run(cfg)
+    np.testing.assert_array_equal(layer.r_out["topk_ids"].cpu().numpy(), ref["route"]["ids"])
+    np.testing.assert_array_equal(layer.d_out["dest_row"].cpu().numpy(), ref["disp"]["dest_row"])
+    np.testing.assert_array_equal(layer.d_out["offsets"].cpu().numpy(), ref["disp"]["offsets"])
+    fn, tol = cases.y_tolerance(cfg)
+    assert fn(y, ref["y"]) <= tol
+
+
+def test_empty_batch():
+    import torch
+    from top_routing_dispatch_moe_gb300 import moe
+    dev = "cuda"
+    x = torch.empty((0, 64), dtype=torch.bfloat16, device=dev)
+    w = torch.randn(64, 8, device=dev).to(torch.bfloat16)
+    r = moe.moe_router(x, w, None, 2)
+    torch.cuda.synchronize()
+    assert r["counts"].sum().item() == 0 and r["aux"].item() == 0.0
+    d = moe.moe_dispatch(x, r["ids"], 8, capacity=0, num_ranks=2)
+    torch.cuda.synchronize()
+    assert d["offsets"].cpu().tolist() == [0] * 9 and d["tile_sched"][0].item() == 0
+    d2 = moe.moe_dispatch(x, r["ids"], 8, capacity=4, num_ranks=2)
+    torch.cuda.synchronize()
+    assert d2["offsets"].cpu().tolist() == [4 * e for e in range(9)]
+    assert d2["src_token"].cpu().tolist() == [-1] * 32 and torch.count_nonzero(d2["buf"]).item() == 0
+    y = moe.moe_combine(torch.empty((0, 64), dtype=torch.bfloat16, device=dev),
+                        torch.empty((0, 2), dtype=torch.int32, device=dev),
+                        torch.empty((0, 2), dtype=torch.float32, device=dev))
+    assert y.shape == (0, 64)
+
+
+def test_capacity_keeps_first_tokens():
+    """Every token routed to experts (0, 1): with C = 5 only tokens 0..4 keep them; the rest are dropped and
+    their rows in y are zero."""
+    import torch
+    from top_routing_dispatch_moe_gb300 import moe
+    T, h, E = 40, 64, 4
+    ids = np.tile(np.array([[0, 1]], np.int32), (T, 1))
+    x = torch.randn(T, h, device="cuda").to(torch.bfloat16)
+    d = moe.moe_dispatch(x, torch.from_numpy(ids).cuda(), E, capacity=5, num_ranks=2)
+    torch.cuda.synchronize()
+    ref = O.dispatch(ids, E, 5, 2)
+    np.testing.assert_array_equal(d["dest_row"].cpu().numpy(), ref["dest_row"])
+    np.testing.assert_array_equal(d["src_token"].cpu().numpy(), ref["src_token"])
+    assert d["kept_counts"].cpu().tolist() == [5, 5, 0, 0]
+    gates = torch.full((T, 2), 0.5, device="cuda")
+    y = moe.moe_combine(d["buf"], d["dest_row"], gates)          # identity experts
+    torch.cuda.synchronize()
+    yn = y.float().cpu().numpy()
+    xn = x.float().cpu().numpy()
+    np.testing.assert_allclose(yn[:5], xn[:5], rtol=1e-2, atol=1e-2)
+    assert np.all(yn[5:] == 0)
+
+
+def test_out_of_range_id_is_flagged():
+    """An expert id >= E is caught by the dispatch kernel's own bounds check: the pair is dropped, nothing is
+    written out of bounds, and moe_check_device_error reports MOE_ERR_INVALID_ARG."""
+    import torch
+    from top_routing_dispatch_moe_gb300 import moe
+    T, h, E = 16, 32, 4
+    ids = np.tile(np.array([[0, 1]], np.int32), (T, 1))
+    ids[3, 1] = E + 5
+    x = torch.randn(T, h, device="cuda").to(torch.bfloat16)
+    d = moe.moe_dispatch(x, torch.from_numpy(ids).cuda(), E, capacity=0, num_ranks=1)
+    rc = moe.moe_check_device_error()
+    assert rc == moe.MOE_ERR_INVALID_ARG and "out of range" in moe.moe_last_error_string()
+    assert d["dest_row"][3, 1].item() == -1
+    assert moe.moe_check_device_error() == moe.MOE_OK          # the flag was cleared
+
+
+def test_identity_experts_end_to_end():
+    """Dispatch then combine with identity experts (eout = buf): y = sum over kept j of gate * x, and with
+    renormalised gates and no drops y = x up to bf16 rounding."""
+    import torch
+    from top_routing_dispatch_moe_gb300 import moe
+    cfg = moe_inputs.get_config("mixtral_zipf", T=512, h=256, F=128)
+    inp = cases.router_inputs(cfg, bias=np.zeros(8, np.float32))
+    x = cases.to_device(inp["x"], cfg)
+    r = moe.moe_router(x, cases.to_device(inp["w_r"], cfg), torch.zeros(8, device="cuda"), cfg.k, cfg.gating)
+    d = moe.moe_dispatch(x, r["ids"], cfg.E, 0, cfg.R)
+    y = moe.moe_combine(d["buf"], d["dest_row"], r["gates"])
+    torch.cuda.synchronize()
+    assert cases.rel_l2(cases.from_device(y, cfg), moe_inputs.to_f64(inp["x"], cfg.dtype)) < 4e-3
+
+
+def test_host_argument_errors():
+    import torch
+    from top_routing_dispatch_moe_gb300 import moe
+    x = torch.zeros((4, 12), dtype=torch.bfloat16, device="cuda")      # h % 8 != 0
+    with pytest.raises(moe.MoEError) as ei:
+        moe.moe_router(x, torch.zeros((12, 4), dtype=torch.bfloat16, device="cuda"), None, 2)
+    assert ei.value.code == moe.MOE_ERR_INVALID_ARG
+    x = torch.zeros((4, 16), dtype=torch.bfloat16, device="cuda")
+    with pytest.raises(moe.MoEError) as ei:
+        moe.moe_router(x, torch.zeros((16, 4), dtype=torch.bfloat16, device="cuda"), None, 5)   # k > E
+    assert ei.value.code == moe.MOE_ERR_INVALID_ARG
+    with pytest.raises(moe.MoEError) as ei:
+        moe.moe_router(x, torch.zeros((16, 4), dtype=torch.bfloat16, device="cuda"), None, 2,
+                       ws=torch.empty(1, dtype=torch.uint8, device="cuda"))
+    assert ei.value.code == moe.MOE_ERR_WORKSPACE
+    with pytest.raises(moe.MoEError) as ei:
+        moe.moe_router(x.half(), torch.zeros((16, 4), dtype=torch.half, device="cuda"), None, 2)
+    assert ei.value.code == moe.MOE_ERR_UNSUPPORTED

@@ -1,0 +1,77 @@
+// Combine: un-permute the expert outputs and sum the k of each token weighted by their gates.
+//
+// "v6 长序列和 MoE", table row "combine" (back to the original position, k outputs weighted by gate and
+// summed); "专家并行" (formulaic), forward pass (the top-2 weighted merge on the source GPU);
+// "Megatron-LM 分布式训练（六）", data flow ("+ shared_experts", every token, gate 1).
+//
+// A gather, not a scatter: one warp per token reads its (at most k) expert rows with 16-byte loads,
+// accumulates in fp32 in ascending j (after the shared expert's output), and writes y once. No atomics,
+// so the result is deterministic. HBM-bound: (kept assignments + T [+ T shared]) rows read, T rows written.
+#include "common.cuh"
+
+namespace moe {
+
+template <typename T>
+__global__ void __launch_bounds__(256)
+combine_kernel(const T* __restrict__ eout, const int32_t* __restrict__ dest_row, const float* __restrict__ gates,
+               const T* __restrict__ shared_out, int T_, int h, int k, T* __restrict__ y) {
+    constexpr int V = Vec16<T>::N;
+    const int lane = threadIdx.x & 31;
+    const int t = blockIdx.x * 8 + (threadIdx.x >> 5);
+    if (t >= T_) return;
+    const int myd = lane < k ? dest_row[(size_t)t * k + lane] : -1;
+    const float myg = lane < k ? gates[(size_t)t * k + lane] : 0.f;
+    int dj[16];
+    float gj[16];
+#pragma unroll
+    for (int j = 0; j < 16; ++j) {
+        dj[j] = __shfl_sync(0xffffffffu, myd, j);
+        gj[j] = __shfl_sync(0xffffffffu, myg, j);
+    }
+    for (int d0 = lane * V; d0 < h; d0 += 32 * V) {
+        float acc[V];
+        if (shared_out) {
+            Vec16<T> s = ld16_stream(shared_out + (size_t)t * h + d0);
+#pragma unroll
+            for (int i = 0; i < V; ++i) acc[i] = s.get(i);
+        } else {
+#pragma unroll
+            for (int i = 0; i < V; ++i) acc[i] = 0.f;
+        }
+#pragma unroll
+        for (int j = 0; j < 16; ++j) {
+            if (j < k && dj[j] >= 0) {
+                Vec16<T> v = ld16_stream(eout + (size_t)dj[j] * h + d0);
+#pragma unroll
+                for (int i = 0; i < V; ++i) acc[i] = fmaf(gj[j], v.get(i), acc[i]);
+            }
+        }
+        Vec16<T> o;
+#pragma unroll
+        for (int i = 0; i < V; ++i) o.set(i, acc[i]);
+        st16(y + (size_t)t * h + d0, o);
+    }
+}
+
+}  // namespace moe
+
+using namespace moe;
+
+extern "C" int moe_combine(const void* eout, const int32_t* dest_row, const float* gates, const void* shared_out,
+                           int T, int h, int k, int dtype, void* y, void* stream) {
+    MOE_REQUIRE(dtype == MOE_F32 || dtype == MOE_BF16, MOE_ERR_UNSUPPORTED, "moe_combine: dtype %d", dtype);
+    MOE_REQUIRE(T >= 0 && h > 0 && h % 8 == 0 && k >= 1 && k <= 16, MOE_ERR_INVALID_ARG,
+                "moe_combine: T=%d h=%d k=%d", T, h, k);
+    if (T == 0) return MOE_OK;
+    MOE_REQUIRE(eout && dest_row && gates && y, MOE_ERR_INVALID_ARG, "moe_combine: null pointer");
+    MOE_REQUIRE(aligned16(eout) && aligned16(shared_out) && aligned16(y), MOE_ERR_INVALID_ARG,
+                "moe_combine: eout, shared_out and y must be 16-byte aligned");
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (dtype == MOE_BF16)
+        combine_kernel<__nv_bfloat16><<<cdiv(T, 8), 256, 0, s>>>(static_cast<const __nv_bfloat16*>(eout), dest_row,
+            gates, static_cast<const __nv_bfloat16*>(shared_out), T, h, k, static_cast<__nv_bfloat16*>(y));
+    else
+        combine_kernel<float><<<cdiv(T, 8), 256, 0, s>>>(static_cast<const float*>(eout), dest_row, gates,
+            static_cast<const float*>(shared_out), T, h, k, static_cast<float*>(y));
+    return check_launch("combine_kernel");
+}

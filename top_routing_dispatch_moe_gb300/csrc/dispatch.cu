@@ -1,0 +1,297 @@
+// Dispatch: per-expert histogram, exclusive scan, stable scatter with capacity mask, payload permute,
+// EP-rank-major send layout and the expert FFN's tile schedule.
+//
+// "v6 长序列和 MoE", table row "dispatch" (group by expert, at most C per expert, pad the rest) and the
+// "Capacity" bullet (C = cf*k*T/E, over-capacity tokens dropped; dropless by default in Megatron); the
+// follow-up there (sort tokens by expert, run one grouped GEMM). "专家并行" (formulaic), section "All2All":
+// the (E, C, M) buffer is pre-sorted by destination expert so that the all-to-all is a block transpose.
+//
+// Stability and determinism come from a two-level count: the assignments (t, j) in token order are cut
+// into chunks of at most 1024; kernel 1 counts each chunk's assignments per expert, kernel 2 (one block)
+// scans those counts per expert over the chunks, then over the experts, and writes offsets, kept counts,
+// the rank layout and the tile schedule; kernel 3 ranks each assignment inside its chunk (warp match_any
+// + per-warp prefix over the chunk's 32 warps) and writes the indices; kernel 4 copies each token row to
+// its (at most k) destination rows with 16-byte loads and stores, reading x once. In capacity mode a
+// fifth kernel zero-fills the pad rows and marks them -1.
+#include <algorithm>
+#include "common.cuh"
+
+namespace moe {
+
+constexpr int kChunkA = 1024;          // assignments per chunk (one thread each)
+
+__device__ __forceinline__ int tokens_per_chunk(int k) { return kChunkA / k; }
+
+__global__ void __launch_bounds__(kChunkA)
+dispatch_count_kernel(const int32_t* __restrict__ ids, int T, int E, int k, int32_t* __restrict__ chunk_counts,
+                      unsigned* err) {
+    extern __shared__ int s_hist[];
+    for (int e = threadIdx.x; e < E; e += blockDim.x) s_hist[e] = 0;
+    __syncthreads();
+    const int tpc = tokens_per_chunk(k);
+    const int a = threadIdx.x;
+    const int t = blockIdx.x * tpc + a / k;
+    if (a < tpc * k && t < T) {
+        const int e = ids[(size_t)blockIdx.x * tpc * k + a];
+        if (e >= 0 && e < E) atomicAdd(&s_hist[e], 1);
+        else latch_device_error(err, kDevErrBadIndex, 0x100u);
+    }
+    __syncthreads();
+    for (int e = threadIdx.x; e < E; e += blockDim.x) chunk_counts[(size_t)blockIdx.x * E + e] = s_hist[e];
+}
+
+// Inclusive block scan of one int per thread (blockDim.x == 1024).
+__device__ int block_inclusive_scan(int v, int* s_tmp) {
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        int n = __shfl_up_sync(0xffffffffu, v, o);
+        if (lane >= o) v += n;
+    }
+    if (lane == 31) s_tmp[warp] = v;
+    __syncthreads();
+    if (warp == 0) {
+        int w = s_tmp[lane];
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            int n = __shfl_up_sync(0xffffffffu, w, o);
+            if (lane >= o) w += n;
+        }
+        s_tmp[lane] = w;
+    }
+    __syncthreads();
+    if (warp > 0) v += s_tmp[warp - 1];
+    __syncthreads();
+    return v;
+}
+
+__global__ void __launch_bounds__(1024)
+dispatch_scan_kernel(int32_t* __restrict__ chunk_counts /* in: counts, out: per-chunk base */, int nchunks, int E,
+                     int C, int R, int32_t* __restrict__ offsets, int32_t* __restrict__ kept_counts,
+                     int32_t* __restrict__ rank_counts, int32_t* __restrict__ rank_offsets, int32_t* __restrict__ sched) {
+    __shared__ int s_tmp[32];
+    __shared__ int s_kept[1024];
+    __shared__ int s_off[1025];
+    __shared__ int s_tp[1025];
+    const int e = threadIdx.x;
+    int n = 0;
+    if (e < E) {
+        for (int c = 0; c < nchunks; ++c) {
+            int v = chunk_counts[(size_t)c * E + e];
+            chunk_counts[(size_t)c * E + e] = n;
+            n += v;
+        }
+    }
+    const int kept = (e < E) ? (C > 0 ? min(n, C) : n) : 0;
+    const int incl = block_inclusive_scan(kept, s_tmp);
+    const int ntiles = (kept + MOE_TILE_M - 1) / MOE_TILE_M;
+    const int tincl = block_inclusive_scan(ntiles, s_tmp);
+    if (e < E) {
+        s_kept[e] = kept;
+        s_off[e] = C > 0 ? e * C : incl - kept;
+        s_tp[e] = tincl - ntiles;
+    }
+    if (e == E - 1) { s_off[E] = C > 0 ? E * C : incl; s_tp[E] = tincl; }
+    __syncthreads();
+    for (int i = e; i <= E; i += blockDim.x) {
+        offsets[i] = s_off[i];
+        sched[kSchedHeader + i] = s_tp[i];
+    }
+    if (e < E) kept_counts[e] = s_kept[e];
+    if (e == 0) { sched[0] = s_tp[E]; sched[1] = E; }
+    const int epr = E / R;
+    for (int r = e; r <= R; r += blockDim.x) rank_offsets[r] = s_off[r * epr];
+    if (e < R) {
+        int s = 0;
+        for (int i = e * epr; i < (e + 1) * epr; ++i) s += s_kept[i];
+        rank_counts[e] = s;
+    }
+    if (e < E) {
+        int4* tiles = reinterpret_cast<int4*>(sched + sched_tiles_offset(E));
+        const int row0 = s_off[e];
+        for (int m = 0; m < ntiles; ++m) {
+            const int rb = row0 + m * MOE_TILE_M;
+            tiles[s_tp[e] + m] = make_int4(e, rb, min(rb + MOE_TILE_M, row0 + kept), 0);
+        }
+    }
+}
+
+__global__ void __launch_bounds__(kChunkA)
+dispatch_scatter_kernel(const int32_t* __restrict__ ids, int T, int E, int k, int C,
+                        const int32_t* __restrict__ chunk_base, const int32_t* __restrict__ offsets,
+                        int32_t* __restrict__ dest_row, uint8_t* __restrict__ drop_mask,
+                        int32_t* __restrict__ src_token, int32_t* __restrict__ src_slot) {
+    extern __shared__ int s_wc[];                 // [32 warps][E] per-warp counts, then prefixes
+    for (int i = threadIdx.x; i < 32 * E; i += blockDim.x) s_wc[i] = 0;
+    __syncthreads();
+    const int tpc = tokens_per_chunk(k);
+    const int a = threadIdx.x, lane = a & 31, warp = a >> 5;
+    const int t = blockIdx.x * tpc + a / k, j = a % k;
+    const bool valid = a < tpc * k && t < T;
+    const size_t ga = (size_t)blockIdx.x * tpc * k + a;
+    int e = valid ? ids[ga] : -1;
+    if (e >= E) e = -1;                          // out-of-range id: treated as dropped (flagged by count)
+    const unsigned peers = __match_any_sync(0xffffffffu, e);
+    const int intra = __popc(peers & ((1u << lane) - 1u));
+    if (e >= 0 && lane == __ffs(peers) - 1) s_wc[warp * E + e] = __popc(peers);
+    __syncthreads();
+    for (int x = threadIdx.x; x < E; x += blockDim.x) {
+        int run = 0;
+        for (int w = 0; w < 32; ++w) { int v = s_wc[w * E + x]; s_wc[w * E + x] = run; run += v; }
+    }
+    __syncthreads();
+    if (valid) {
+        int d = -1;
+        if (e >= 0) {
+            const int slot = chunk_base[(size_t)blockIdx.x * E + e] + s_wc[warp * E + e] + intra;
+            if (C == 0 || slot < C) {
+                d = offsets[e] + slot;
+                src_token[d] = t;
+                src_slot[d] = j;
+            }
+        }
+        dest_row[ga] = d;
+        drop_mask[ga] = d < 0 ? 1 : 0;
+    }
+}
+
+// One warp per token: read x[t] once, write it to each kept destination row.
+template <typename T>
+__global__ void __launch_bounds__(256)
+dispatch_copy_kernel(const T* __restrict__ x, const int32_t* __restrict__ dest_row, int T_, int h, int k,
+                     T* __restrict__ buf) {
+    constexpr int V = Vec16<T>::N;
+    const int lane = threadIdx.x & 31;
+    const int t = blockIdx.x * 8 + (threadIdx.x >> 5);
+    if (t >= T_) return;
+    const int my = lane < k ? dest_row[(size_t)t * k + lane] : -1;
+    int dj[16];
+#pragma unroll
+    for (int j = 0; j < 16; ++j) dj[j] = __shfl_sync(0xffffffffu, my, j);   // all lanes, before any exit
+    const T* src = x + (size_t)t * h;
+    for (int d0 = lane * V; d0 < h; d0 += 32 * V) {
+        Vec16<T> v = ld16_stream(src + d0);
+#pragma unroll
+        for (int j = 0; j < 16; ++j)
+            if (j < k && dj[j] >= 0) st16(buf + (size_t)dj[j] * h + d0, v);
+    }
+}
+
+// Capacity mode: pad rows [offsets[e] + kept[e], offsets[e+1]) -> zero payload, src = -1.
+template <typename T>
+__global__ void __launch_bounds__(256)
+dispatch_pad_kernel(const int32_t* __restrict__ kept_counts, int E, int C, int h, T* __restrict__ buf,
+                    int32_t* __restrict__ src_token, int32_t* __restrict__ src_slot) {
+    constexpr int V = Vec16<T>::N;
+    const int lane = threadIdx.x & 31;
+    const long long rows = (long long)E * C;
+    for (long long r = (long long)blockIdx.x * 8 + (threadIdx.x >> 5); r < rows; r += (long long)gridDim.x * 8) {
+        const int e = (int)(r / C);
+        if (r - (long long)e * C < kept_counts[e]) continue;
+        if (lane == 0) { src_token[r] = -1; src_slot[r] = -1; }
+        Vec16<T> z;
+        z.v = {};
+        for (int d0 = lane * V; d0 < h; d0 += 32 * V) st16(buf + r * h + d0, z);
+    }
+}
+
+__global__ void dense_sched_kernel(int rows, int32_t* sched) {
+    const int ntiles = (rows + MOE_TILE_M - 1) / MOE_TILE_M;
+    if (blockIdx.x == 0 && threadIdx.x == 0) { sched[0] = ntiles; sched[1] = 1; sched[2] = 0; sched[3] = ntiles; }
+    int4* tiles = reinterpret_cast<int4*>(sched + sched_tiles_offset(1));
+    for (int m = blockIdx.x * blockDim.x + threadIdx.x; m < ntiles; m += gridDim.x * blockDim.x)
+        tiles[m] = make_int4(0, m * MOE_TILE_M, min(rows, (m + 1) * MOE_TILE_M), 0);
+}
+
+static int num_chunks(int T, int k) { return T <= 0 ? 0 : cdiv(T, kChunkA / k); }
+
+}  // namespace moe
+
+using namespace moe;
+
+extern "C" size_t moe_dispatch_rows(int T, int E, int k, int capacity) {
+    if (T < 0 || E <= 0 || k <= 0) return 0;
+    return capacity > 0 ? (size_t)E * capacity : (size_t)T * k;
+}
+
+extern "C" size_t moe_tile_sched_bytes(int T, int E, int k, int capacity) {
+    if (T < 0 || E <= 0 || k <= 0) return 0;
+    return sched_words((long long)moe_dispatch_rows(T, E, k, capacity), E) * sizeof(int32_t);
+}
+
+extern "C" size_t moe_dispatch_workspace_size(int T, int E, int k, int capacity) {
+    (void)capacity;
+    if (T < 0 || E <= 0 || k <= 0 || k > kChunkA) return 0;
+    return align_up((size_t)num_chunks(T, k) * E * sizeof(int32_t), 256);
+}
+
+extern "C" int moe_dispatch(const void* x, const int32_t* topk_ids, int T, int h, int E, int k, int capacity,
+                            int num_ranks, int dtype, void* buf, int32_t* offsets, int32_t* kept_counts,
+                            int32_t* dest_row, uint8_t* drop_mask, int32_t* src_token, int32_t* src_slot,
+                            int32_t* rank_counts, int32_t* rank_offsets, int32_t* tile_sched, void* ws,
+                            size_t ws_bytes, void* stream) {
+    MOE_REQUIRE(dtype == MOE_F32 || dtype == MOE_BF16, MOE_ERR_UNSUPPORTED, "moe_dispatch: dtype %d", dtype);
+    MOE_REQUIRE(T >= 0 && h > 0 && h % 8 == 0, MOE_ERR_INVALID_ARG, "moe_dispatch: T=%d h=%d", T, h);
+    MOE_REQUIRE(E >= 1 && E <= 1024 && k >= 1 && k <= E && k <= 16, MOE_ERR_INVALID_ARG,
+                "moe_dispatch: E=%d k=%d", E, k);
+    MOE_REQUIRE(capacity >= 0, MOE_ERR_INVALID_ARG, "moe_dispatch: capacity %d < 0", capacity);
+    MOE_REQUIRE(num_ranks >= 1 && num_ranks <= E && E % num_ranks == 0, MOE_ERR_INVALID_ARG,
+                "moe_dispatch: num_ranks %d must divide E=%d", num_ranks, E);
+    const long long rows = (long long)moe_dispatch_rows(T, E, k, capacity);
+    MOE_REQUIRE(rows < (1LL << 31), MOE_ERR_INVALID_ARG, "moe_dispatch: %lld rows overflow int32", rows);
+    MOE_REQUIRE(offsets && kept_counts && rank_counts && rank_offsets && tile_sched, MOE_ERR_INVALID_ARG,
+                "moe_dispatch: null pointer");
+    MOE_REQUIRE(T == 0 || (x && topk_ids && dest_row && drop_mask), MOE_ERR_INVALID_ARG, "moe_dispatch: null pointer");
+    MOE_REQUIRE(rows == 0 || (buf && src_token && src_slot), MOE_ERR_INVALID_ARG, "moe_dispatch: null pointer");
+    MOE_REQUIRE(aligned16(x) && aligned16(buf) && aligned16(tile_sched), MOE_ERR_INVALID_ARG,
+                "moe_dispatch: x, buf and tile_sched must be 16-byte aligned");
+    const size_t need = moe_dispatch_workspace_size(T, E, k, capacity);
+    MOE_REQUIRE(ws_bytes >= need && (need == 0 || ws), MOE_ERR_WORKSPACE, "moe_dispatch: workspace %zu < %zu",
+                ws_bytes, need);
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    unsigned* err = device_error_word();
+    MOE_REQUIRE(err, MOE_ERR_CUDA, "moe_dispatch: device error word unavailable");
+    const int nch = num_chunks(T, k);
+    int32_t* chunk = static_cast<int32_t*>(ws);
+    if (nch > 0) {
+        dispatch_count_kernel<<<nch, kChunkA, E * sizeof(int), s>>>(topk_ids, T, E, k, chunk, err);
+        if (int rc = check_launch("dispatch_count_kernel")) return rc;
+    }
+    dispatch_scan_kernel<<<1, 1024, 0, s>>>(chunk, nch, E, capacity, num_ranks, offsets, kept_counts, rank_counts,
+                                           rank_offsets, tile_sched);
+    if (int rc = check_launch("dispatch_scan_kernel")) return rc;
+    if (nch > 0) {
+        const size_t smem = (size_t)32 * E * sizeof(int);
+        cudaFuncSetAttribute(dispatch_scatter_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        dispatch_scatter_kernel<<<nch, kChunkA, smem, s>>>(topk_ids, T, E, k, capacity, chunk, offsets, dest_row,
+                                                          drop_mask, src_token, src_slot);
+        if (int rc = check_launch("dispatch_scatter_kernel")) return rc;
+        if (dtype == MOE_BF16)
+            dispatch_copy_kernel<__nv_bfloat16><<<cdiv(T, 8), 256, 0, s>>>(static_cast<const __nv_bfloat16*>(x),
+                dest_row, T, h, k, static_cast<__nv_bfloat16*>(buf));
+        else
+            dispatch_copy_kernel<float><<<cdiv(T, 8), 256, 0, s>>>(static_cast<const float*>(x), dest_row, T, h, k,
+                                                                  static_cast<float*>(buf));
+        if (int rc = check_launch("dispatch_copy_kernel")) return rc;
+    }
+    if (capacity > 0 && rows > 0) {
+        const int grid = std::min(cdiv(rows, 8), 8 * num_sms());
+        if (dtype == MOE_BF16)
+            dispatch_pad_kernel<__nv_bfloat16><<<grid, 256, 0, s>>>(kept_counts, E, capacity, h,
+                static_cast<__nv_bfloat16*>(buf), src_token, src_slot);
+        else
+            dispatch_pad_kernel<float><<<grid, 256, 0, s>>>(kept_counts, E, capacity, h, static_cast<float*>(buf),
+                                                           src_token, src_slot);
+        if (int rc = check_launch("dispatch_pad_kernel")) return rc;
+    }
+    return MOE_OK;
+}
+
+extern "C" int moe_dense_tile_sched(int rows, int32_t* tile_sched, void* stream) {
+    MOE_REQUIRE(rows >= 0 && tile_sched && aligned16(tile_sched), MOE_ERR_INVALID_ARG,
+                "moe_dense_tile_sched: rows=%d, tile_sched must be non-null and 16-byte aligned", rows);
+    const int ntiles = cdiv(rows, MOE_TILE_M);
+    dense_sched_kernel<<<std::max(1, std::min(cdiv(ntiles, 256), 64)), 256, 0, static_cast<cudaStream_t>(stream)>>>(
+        rows, tile_sched);
+    return check_launch("dense_sched_kernel");
+}

@@ -1,0 +1,51 @@
+// C-ABI entry points of the grouped SwiGLU expert FFN ("Megatron-LM 分布式训练（六）", data flow: the
+// experts run as one GroupedGEMM; "v6 长序列和 MoE", table row "expert": each expert's FFN h -> F -> h).
+// bf16 goes to the tcgen05 tensor-core kernels, fp32 to the CUDA-core kernels.
+#include "ffn.cuh"
+
+using namespace moe;
+
+static int ffn_check(const char* fn, const void* in, const int32_t* sched, const void* packed, int E, int h, int F,
+                     int rows, int dtype, const void* out) {
+    MOE_REQUIRE(dtype == MOE_F32 || dtype == MOE_BF16, MOE_ERR_UNSUPPORTED, "%s: dtype %d", fn, dtype);
+    MOE_REQUIRE(E >= 1 && E <= 1024 && h > 0 && F > 0 && h % 8 == 0 && F % 8 == 0 && rows >= 0, MOE_ERR_INVALID_ARG,
+                "%s: E=%d h=%d F=%d rows=%d (need h%%8==0, F%%8==0)", fn, E, h, F, rows);
+    MOE_REQUIRE(rows == 0 || (in && sched && packed && out), MOE_ERR_INVALID_ARG, "%s: null pointer", fn);
+    MOE_REQUIRE(aligned16(in) && aligned16(sched) && aligned16(packed) && aligned16(out), MOE_ERR_INVALID_ARG,
+                "%s: pointers must be 16-byte aligned", fn);
+    return MOE_OK;
+}
+
+extern "C" int moe_expert_up_gate(const void* buf, const int32_t* tile_sched, const void* packed_w, int E, int h, int F,
+                                  int rows, int dtype, void* act, void* stream) {
+    if (int rc = ffn_check("moe_expert_up_gate", buf, tile_sched, packed_w, E, h, F, rows, dtype, act)) return rc;
+    if (rows == 0) return MOE_OK;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (dtype == MOE_BF16) return ffn_tc_up_gate(buf, tile_sched, packed_w, E, h, F, rows, act, s);
+    return ffn_simt_up_gate(buf, tile_sched, packed_w, E, h, F, rows, dtype, act, s);
+}
+
+extern "C" int moe_expert_down(const void* act, const int32_t* tile_sched, const void* packed_w, int E, int h, int F,
+                               int rows, int dtype, void* eout, void* stream) {
+    if (int rc = ffn_check("moe_expert_down", act, tile_sched, packed_w, E, h, F, rows, dtype, eout)) return rc;
+    if (rows == 0) return MOE_OK;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (dtype == MOE_BF16) return ffn_tc_down(act, tile_sched, packed_w, E, h, F, rows, eout, s);
+    return ffn_simt_down(act, tile_sched, packed_w, E, h, F, rows, dtype, eout, s);
+}
+
+extern "C" size_t moe_expert_ffn_workspace_size(int rows, int F, int dtype) {
+    if (rows < 0 || F <= 0) return 0;
+    return align_up((size_t)rows * F * (dtype == MOE_F32 ? 4 : 2), 256);
+}
+
+extern "C" int moe_expert_ffn(const void* buf, const int32_t* tile_sched, const void* packed_w, int E, int h, int F,
+                              int rows, int dtype, void* eout, void* ws, size_t ws_bytes, void* stream) {
+    if (int rc = ffn_check("moe_expert_ffn", buf, tile_sched, packed_w, E, h, F, rows, dtype, eout)) return rc;
+    const size_t need = moe_expert_ffn_workspace_size(rows, F, dtype);
+    MOE_REQUIRE(ws_bytes >= need && (need == 0 || ws), MOE_ERR_WORKSPACE, "moe_expert_ffn: workspace %zu < %zu",
+                ws_bytes, need);
+    MOE_REQUIRE(aligned16(ws), MOE_ERR_INVALID_ARG, "moe_expert_ffn: workspace must be 16-byte aligned");
+    if (int rc = moe_expert_up_gate(buf, tile_sched, packed_w, E, h, F, rows, dtype, ws, stream)) return rc;
+    return moe_expert_down(ws, tile_sched, packed_w, E, h, F, rows, dtype, eout, stream);
+}

@@ -1,0 +1,35 @@
+// Grouped SwiGLU expert FFN: shared declarations.
+#pragma once
+#include "common.cuh"
+
+namespace moe {
+
+struct PackedLayout {
+    int Fp;                 // F rounded up to 128
+    size_t up_gate_off;     // bytes: [E][Fp/128][256][h]
+    size_t down_off;        // bytes: [E][h][F]
+    size_t total_bytes;
+};
+
+inline PackedLayout packed_layout(int E, int h, int F, int el) {
+    PackedLayout L;
+    L.Fp = (F + 127) / 128 * 128;
+    L.up_gate_off = 0;
+    L.down_off = align_up((size_t)E * 2 * L.Fp * h * el, 256);
+    L.total_bytes = L.down_off + (size_t)E * h * F * el;
+    return L;
+}
+
+// CUDA-core path (fp32; the reference-precision path of the library).
+int ffn_simt_up_gate(const void* buf, const int32_t* sched, const void* packed, int E, int h, int F, int rows, int dtype,
+                     void* act, cudaStream_t s);
+int ffn_simt_down(const void* act, const int32_t* sched, const void* packed, int E, int h, int F, int rows, int dtype,
+                  void* eout, cudaStream_t s);
+
+// tcgen05 tensor-core path (bf16 operands, fp32 accumulation in tensor memory).
+int ffn_tc_up_gate(const void* buf, const int32_t* sched, const void* packed, int E, int h, int F, int rows, void* act,
+                   cudaStream_t s);
+int ffn_tc_down(const void* act, const int32_t* sched, const void* packed, int E, int h, int F, int rows, void* eout,
+                cudaStream_t s);
+
+}  // namespace moe

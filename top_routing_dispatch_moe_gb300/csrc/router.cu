@@ -1,0 +1,405 @@
+// Router: gating GEMM, top-k, gates, counts and the Switch aux-loss terms.
+//
+// "Megatron-LM 分布式训练（六）", section "Router": logits = hidden_states @ W_router, then top-k with
+// softmax / sigmoid weights. "v6 长序列和 MoE", table rows "router" / "top-k" and the "Load balancing
+// loss" bullet: aux = alpha * E * sum_i f_i P_i; DeepSeek-V3's bias is a selection-only term.
+//
+// Two ways to the logits, one gating epilogue:
+//   E <= 32: fused kernel, one warp per token, W_r^T staged in shared memory (the whole router weight is
+//            at most a few hundred KB and is read from L2 once per block), x streamed with 16-byte loads.
+//   E  > 32: logits GEMM [T,h] x [h,E] into fp32, then the gating kernel reads them back (L2-resident).
+// The gating epilogue keeps the E logits of a token spread over the 32 lanes of a warp (lane l holds
+// experts l, l+32, ...), takes k warp-wide argmax rounds (ties -> lower index), and accumulates per-block
+// partial sums of P and per-block counts; a one-block finalize kernel adds the partials in a fixed order,
+// so every output is deterministic.
+#include <math.h>
+#include <algorithm>
+#include "common.cuh"
+
+namespace moe {
+
+constexpr int kRouterWarps = 8;
+constexpr int kRouterMaxBlocks = 1024;
+constexpr int kMaxK = 16;
+
+struct GateOut {
+    int32_t* ids;
+    float* gates;
+    float* logits;      // may be null
+    float* partial_P;   // [grid][E]
+    int32_t* partial_C; // [grid][E]
+};
+
+// Gating of one token whose NPL-per-lane logits are in L (expert of slot i = lane + 32 i).
+// Accumulates the token's router probabilities into Pacc and its choices into the shared histogram.
+template <int NPL>
+__device__ __forceinline__ void gate_token(float (&L)[NPL], int t, int E, int k, int gating, const float* bias,
+                                           const GateOut& o, float (&Pacc)[NPL], int* s_hist) {
+    const int lane = threadIdx.x & 31;
+    float score[NPL], prob[NPL];
+    bool live[NPL];
+#pragma unroll
+    for (int i = 0; i < NPL; ++i) live[i] = (lane + 32 * i) < E;
+
+    if (gating == MOE_GATING_SIGMOID_BIAS_RENORM) {
+        float s_sum = 0.f;
+#pragma unroll
+        for (int i = 0; i < NPL; ++i) {
+            float s = live[i] ? 1.f / (1.f + expf(-L[i])) : 0.f;
+            prob[i] = s;                                   // sigmoid value, normalised below
+            score[i] = live[i] ? s + (bias ? bias[lane + 32 * i] : 0.f) : -INFINITY;
+            s_sum += s;
+        }
+        s_sum = warp_sum(s_sum);
+        float inv = 1.f / s_sum;
+#pragma unroll
+        for (int i = 0; i < NPL; ++i) Pacc[i] += prob[i] * inv;
+    } else {
+        float m = -INFINITY;
+#pragma unroll
+        for (int i = 0; i < NPL; ++i) if (live[i]) m = fmaxf(m, L[i]);
+        m = warp_max(m);
+        float z = 0.f;
+#pragma unroll
+        for (int i = 0; i < NPL; ++i) {
+            prob[i] = live[i] ? expf(L[i] - m) : 0.f;
+            z += prob[i];
+            score[i] = live[i] ? L[i] : -INFINITY;
+        }
+        z = warp_sum(z);
+        float inv = 1.f / z;
+#pragma unroll
+        for (int i = 0; i < NPL; ++i) { prob[i] *= inv; Pacc[i] += prob[i]; }
+    }
+
+    // k rounds of warp argmax on the selection score
+    int sel_id[kMaxK];
+    float sel_p[kMaxK];
+    float psum = 0.f;
+#pragma unroll
+    for (int j = 0; j < kMaxK; ++j) {
+        if (j < k) {
+            float bv = -INFINITY;
+            int bi = 0x7fffffff;
+#pragma unroll
+            for (int i = 0; i < NPL; ++i)
+                if (score[i] > bv) { bv = score[i]; bi = lane + 32 * i; }   // strict: lower index on ties
+            warp_argmax(bv, bi);
+            const int owner = bi & 31, slot = bi >> 5;
+            float pv = 0.f;
+#pragma unroll
+            for (int i = 0; i < NPL; ++i) {
+                if (i == slot) pv = prob[i];
+                if (i == slot && lane == owner) score[i] = -INFINITY;      // taken
+            }
+            pv = __shfl_sync(0xffffffffu, pv, owner);
+            sel_id[j] = bi;
+            sel_p[j] = pv;
+            psum += pv;
+        }
+    }
+    const float norm = (gating == MOE_GATING_SOFTMAX) ? 1.f : 1.f / psum;
+#pragma unroll
+    for (int j = 0; j < kMaxK; ++j) {
+        if (j < k && lane == j) {
+            o.ids[(size_t)t * k + j] = sel_id[j];
+            o.gates[(size_t)t * k + j] = sel_p[j] * norm;
+            atomicAdd(&s_hist[sel_id[j]], 1);
+        }
+    }
+}
+
+// Per-block partial sums of P and counts (fixed order over the block's warps).
+template <int NPL>
+__device__ __forceinline__ void flush_partials(float (&Pacc)[NPL], int E, float* s_P, int* s_hist,
+                                               const GateOut& o) {
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+#pragma unroll
+    for (int i = 0; i < NPL; ++i) {
+        int e = lane + 32 * i;
+        if (e < E) s_P[warp * E + e] = Pacc[i];
+    }
+    __syncthreads();
+    for (int e = threadIdx.x; e < E; e += blockDim.x) {
+        float s = 0.f;
+        for (int w = 0; w < kRouterWarps; ++w) s += s_P[w * E + e];
+        o.partial_P[(size_t)blockIdx.x * E + e] = s;
+        o.partial_C[(size_t)blockIdx.x * E + e] = s_hist[e];
+    }
+}
+
+// ---------------------------------------------------------------------------------------------------
+// E <= 32: fused logits + gating, W_r^T in shared memory
+// ---------------------------------------------------------------------------------------------------
+template <typename T, int EMAX>
+__global__ void __launch_bounds__(kRouterWarps * 32)
+router_small_kernel(const T* __restrict__ x, const T* __restrict__ w_r, const float* __restrict__ bias, int T_,
+                    int h, int E, int k, int gating, GateOut o) {
+    extern __shared__ __align__(16) unsigned char smem_raw[];
+    T* wT = reinterpret_cast<T*>(smem_raw);                                     // [E][h]
+    float* s_P = reinterpret_cast<float*>(smem_raw + (((size_t)E * h * sizeof(T) + 15) & ~(size_t)15));
+    int* s_hist = reinterpret_cast<int*>(s_P + kRouterWarps * E);
+
+    for (int i = threadIdx.x; i < E * h; i += blockDim.x) {
+        const int d = i / E, e = i - d * E;
+        wT[(size_t)e * h + d] = w_r[i];
+    }
+    for (int e = threadIdx.x; e < E; e += blockDim.x) s_hist[e] = 0;
+    __syncthreads();
+
+    constexpr int V = Vec16<T>::N;
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    float Pacc[1] = {0.f};
+    const bool use_bias_in_logits = bias && gating != MOE_GATING_SIGMOID_BIAS_RENORM;
+    for (int t = blockIdx.x * kRouterWarps + warp; t < T_; t += gridDim.x * kRouterWarps) {
+        float acc[EMAX];
+#pragma unroll
+        for (int e = 0; e < EMAX; ++e) acc[e] = 0.f;
+        const T* xr = x + (size_t)t * h;
+        for (int d0 = lane * V; d0 < h; d0 += 32 * V) {
+            Vec16<T> xv = ld16_stream(xr + d0);
+#pragma unroll
+            for (int e = 0; e < EMAX; ++e) {
+                if (e < E) {
+                    Vec16<T> wv = *reinterpret_cast<const Vec16<T>*>(wT + (size_t)e * h + d0);
+                    float s = acc[e];
+#pragma unroll
+                    for (int i = 0; i < V; ++i) s = fmaf(xv.get(i), wv.get(i), s);
+                    acc[e] = s;
+                }
+            }
+        }
+        float L[1] = {-INFINITY};
+#pragma unroll
+        for (int e = 0; e < EMAX; ++e) {
+            if (e < E) {
+                float s = warp_sum(acc[e]);
+                if (lane == e) L[0] = s;
+            }
+        }
+        if (lane < E) {
+            if (use_bias_in_logits) L[0] += bias[lane];
+            if (o.logits) o.logits[(size_t)t * E + lane] = L[0];
+        }
+        gate_token<1>(L, t, E, k, gating, bias, o, Pacc, s_hist);
+    }
+    __syncthreads();
+    flush_partials<1>(Pacc, E, s_P, s_hist, o);
+}
+
+// ---------------------------------------------------------------------------------------------------
+// E > 32: logits GEMM (fp32 accumulation, CUDA cores), then the gating kernel
+// ---------------------------------------------------------------------------------------------------
+// C[T,E] = x[T,h] @ W[h,E] (+ bias in softmax modes). 64x64 tiles, 16-deep K steps, 4x4 per thread.
+template <typename T>
+__global__ void __launch_bounds__(256)
+router_logits_gemm(const T* __restrict__ x, const T* __restrict__ w, const float* __restrict__ bias, int T_, int h,
+                   int E, float* __restrict__ out) {
+    __shared__ float As[16][64 + 4];
+    __shared__ float Bs[16][64 + 4];
+    const int tx = threadIdx.x & 15, ty = threadIdx.x >> 4;
+    const int m0 = blockIdx.y * 64, n0 = blockIdx.x * 64;
+    float acc[4][4] = {};
+    for (int k0 = 0; k0 < h; k0 += 16) {
+        for (int i = threadIdx.x; i < 64 * 16; i += 256) {
+            int r = i / 16, c = i % 16;                     // A: row r, k c
+            int gm = m0 + r, gk = k0 + c;
+            As[c][r] = (gm < T_ && gk < h) ? to_f32(x[(size_t)gm * h + gk]) : 0.f;
+            int kr = i / 64, nc = i % 64;                   // B: k kr, col nc
+            int bk = k0 + kr, bn = n0 + nc;
+            Bs[kr][nc] = (bk < h && bn < E) ? to_f32(w[(size_t)bk * E + bn]) : 0.f;
+        }
+        __syncthreads();
+#pragma unroll
+        for (int kk = 0; kk < 16; ++kk) {
+            float a[4], b[4];
+#pragma unroll
+            for (int i = 0; i < 4; ++i) { a[i] = As[kk][ty * 4 + i]; b[i] = Bs[kk][tx * 4 + i]; }
+#pragma unroll
+            for (int i = 0; i < 4; ++i)
+#pragma unroll
+                for (int j = 0; j < 4; ++j) acc[i][j] = fmaf(a[i], b[j], acc[i][j]);
+        }
+        __syncthreads();
+    }
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        int gm = m0 + ty * 4 + i;
+        if (gm >= T_) continue;
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            int gn = n0 + tx * 4 + j;
+            if (gn < E) out[(size_t)gm * E + gn] = acc[i][j] + (bias ? bias[gn] : 0.f);
+        }
+    }
+}
+
+template <int NPL>
+__global__ void __launch_bounds__(kRouterWarps * 32)
+router_gate_kernel(const float* __restrict__ logits, const float* __restrict__ bias, int T_, int E, int k, int gating,
+                   GateOut o) {
+    extern __shared__ __align__(16) unsigned char smem_raw[];
+    float* s_P = reinterpret_cast<float*>(smem_raw);
+    int* s_hist = reinterpret_cast<int*>(s_P + kRouterWarps * E);
+    for (int e = threadIdx.x; e < E; e += blockDim.x) s_hist[e] = 0;
+    __syncthreads();
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    float Pacc[NPL];
+#pragma unroll
+    for (int i = 0; i < NPL; ++i) Pacc[i] = 0.f;
+    for (int t = blockIdx.x * kRouterWarps + warp; t < T_; t += gridDim.x * kRouterWarps) {
+        float L[NPL];
+#pragma unroll
+        for (int i = 0; i < NPL; ++i) {
+            int e = lane + 32 * i;
+            L[i] = e < E ? logits[(size_t)t * E + e] : -INFINITY;
+        }
+        gate_token<NPL>(L, t, E, k, gating, bias, o, Pacc, s_hist);
+    }
+    __syncthreads();
+    flush_partials<NPL>(Pacc, E, s_P, s_hist, o);
+}
+
+// One block: counts, f, P and aux from the per-block partials, in a fixed order.
+__global__ void __launch_bounds__(1024)
+router_finalize(const float* __restrict__ partial_P, const int32_t* __restrict__ partial_C, int grid, int T_, int E,
+                int k, float alpha, int32_t* counts, float* f, float* P, float* aux) {
+    __shared__ float s_red[1024];
+    float term = 0.f;
+    for (int e = threadIdx.x; e < E; e += blockDim.x) {
+        float ps = 0.f;
+        int c = 0;
+        for (int b = 0; b < grid; ++b) { ps += partial_P[(size_t)b * E + e]; c += partial_C[(size_t)b * E + e]; }
+        const float Pe = T_ > 0 ? ps / (float)T_ : 0.f;
+        const float fe = T_ > 0 ? (float)c / ((float)k * (float)T_) : 0.f;
+        counts[e] = c;
+        f[e] = fe;
+        P[e] = Pe;
+        term += fe * Pe;
+    }
+    s_red[threadIdx.x] = term;
+    __syncthreads();
+    for (int s = blockDim.x / 2; s > 0; s >>= 1) {
+        if ((int)threadIdx.x < s) s_red[threadIdx.x] += s_red[threadIdx.x + s];
+        __syncthreads();
+    }
+    if (threadIdx.x == 0) aux[0] = alpha * (float)E * s_red[0];
+}
+
+// ---------------------------------------------------------------------------------------------------
+// host
+// ---------------------------------------------------------------------------------------------------
+static int router_grid(int T) { return std::max(1, std::min(cdiv(T, kRouterWarps), kRouterMaxBlocks)); }
+
+static size_t small_smem_bytes(int h, int E, int el) {
+    return align_up((size_t)E * h * el, 16) + (size_t)kRouterWarps * E * sizeof(float) + (size_t)E * sizeof(int);
+}
+static bool use_small_path(int h, int E, int el) { return E <= 32 && small_smem_bytes(h, E, el) <= 200 * 1024; }
+
+struct RouterWs { float* partial_P; int32_t* partial_C; float* logits; size_t bytes; };
+
+static RouterWs router_ws_layout(void* ws, int T, int h, int E, int el, bool need_logits) {
+    RouterWs w{};
+    const int G = router_grid(T);
+    size_t off = 0;
+    char* base = static_cast<char*>(ws);
+    w.partial_P = reinterpret_cast<float*>(base + off); off = align_up(off + (size_t)G * E * 4, 256);
+    w.partial_C = reinterpret_cast<int32_t*>(base + off); off = align_up(off + (size_t)G * E * 4, 256);
+    w.logits = nullptr;
+    if (need_logits) { w.logits = reinterpret_cast<float*>(base + off); off = align_up(off + (size_t)T * E * 4, 256); }
+    w.bytes = off;
+    return w;
+}
+
+}  // namespace moe
+
+using namespace moe;
+
+extern "C" size_t moe_router_workspace_size(int T, int h, int E, int k, int dtype) {
+    (void)k;
+    if (T < 0 || h <= 0 || E <= 0) return 0;
+    const int el = dtype == MOE_F32 ? 4 : 2;
+    return router_ws_layout(nullptr, T, h, E, el, !use_small_path(h, E, el)).bytes;
+}
+
+extern "C" int moe_router(const void* x, const void* w_r, const float* bias, int T, int h, int E, int k, int dtype,
+                          int gating, float alpha, float* logits, int32_t* topk_ids, float* gates, int32_t* counts,
+                          float* f, float* P, float* aux, void* ws, size_t ws_bytes, void* stream) {
+    MOE_REQUIRE(dtype == MOE_F32 || dtype == MOE_BF16, MOE_ERR_UNSUPPORTED, "moe_router: dtype %d", dtype);
+    MOE_REQUIRE(gating >= MOE_GATING_SOFTMAX && gating <= MOE_GATING_SIGMOID_BIAS_RENORM, MOE_ERR_UNSUPPORTED,
+                "moe_router: gating mode %d", gating);
+    MOE_REQUIRE(T >= 0 && h > 0 && h % 8 == 0, MOE_ERR_INVALID_ARG, "moe_router: T=%d h=%d (need T>=0, h%%8==0)", T, h);
+    MOE_REQUIRE(E >= 1 && E <= 1024 && k >= 1 && k <= E && k <= kMaxK, MOE_ERR_INVALID_ARG,
+                "moe_router: E=%d k=%d (need 1<=k<=min(E,16), E<=1024)", E, k);
+    MOE_REQUIRE(w_r && topk_ids && gates && counts && f && P && aux && (T == 0 || x), MOE_ERR_INVALID_ARG,
+                "moe_router: null pointer");
+    MOE_REQUIRE(aligned16(x) && aligned16(w_r) && aligned16(logits), MOE_ERR_INVALID_ARG,
+                "moe_router: x, w_r and logits must be 16-byte aligned");
+    const int el = dtype == MOE_F32 ? 4 : 2;
+    const bool small = use_small_path(h, E, el);
+    RouterWs w = router_ws_layout(ws, T, h, E, el, !small && logits == nullptr);
+    MOE_REQUIRE(ws_bytes >= w.bytes && (w.bytes == 0 || ws), MOE_ERR_WORKSPACE,
+                "moe_router: workspace %zu < %zu bytes", ws_bytes, w.bytes);
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    const int G = router_grid(T);
+    GateOut o{topk_ids, gates, logits, w.partial_P, w.partial_C};
+    if (T > 0) {
+        if (small) {
+            const size_t smem = small_smem_bytes(h, E, el);
+            if (dtype == MOE_BF16) {
+                const __nv_bfloat16* xb = static_cast<const __nv_bfloat16*>(x);
+                const __nv_bfloat16* wb = static_cast<const __nv_bfloat16*>(w_r);
+                if (E <= 8) {
+                    cudaFuncSetAttribute(router_small_kernel<__nv_bfloat16, 8>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+                    router_small_kernel<__nv_bfloat16, 8><<<G, kRouterWarps * 32, smem, s>>>(xb, wb, bias, T, h, E, k, gating, o);
+                } else if (E <= 16) {
+                    cudaFuncSetAttribute(router_small_kernel<__nv_bfloat16, 16>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+                    router_small_kernel<__nv_bfloat16, 16><<<G, kRouterWarps * 32, smem, s>>>(xb, wb, bias, T, h, E, k, gating, o);
+                } else {
+                    cudaFuncSetAttribute(router_small_kernel<__nv_bfloat16, 32>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+                    router_small_kernel<__nv_bfloat16, 32><<<G, kRouterWarps * 32, smem, s>>>(xb, wb, bias, T, h, E, k, gating, o);
+                }
+            } else {
+                const float* xf = static_cast<const float*>(x);
+                const float* wf = static_cast<const float*>(w_r);
+                if (E <= 8) {
+                    cudaFuncSetAttribute(router_small_kernel<float, 8>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+                    router_small_kernel<float, 8><<<G, kRouterWarps * 32, smem, s>>>(xf, wf, bias, T, h, E, k, gating, o);
+                } else if (E <= 16) {
+                    cudaFuncSetAttribute(router_small_kernel<float, 16>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+                    router_small_kernel<float, 16><<<G, kRouterWarps * 32, smem, s>>>(xf, wf, bias, T, h, E, k, gating, o);
+                } else {
+                    cudaFuncSetAttribute(router_small_kernel<float, 32>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+                    router_small_kernel<float, 32><<<G, kRouterWarps * 32, smem, s>>>(xf, wf, bias, T, h, E, k, gating, o);
+                }
+            }
+            if (int rc = check_launch("router_small_kernel")) return rc;
+        } else {
+            float* lg = logits ? logits : w.logits;
+            const float* lbias = (gating != MOE_GATING_SIGMOID_BIAS_RENORM) ? bias : nullptr;
+            dim3 grid(cdiv(E, 64), cdiv(T, 64));
+            if (dtype == MOE_BF16)
+                router_logits_gemm<__nv_bfloat16><<<grid, 256, 0, s>>>(static_cast<const __nv_bfloat16*>(x),
+                    static_cast<const __nv_bfloat16*>(w_r), lbias, T, h, E, lg);
+            else
+                router_logits_gemm<float><<<grid, 256, 0, s>>>(static_cast<const float*>(x),
+                    static_cast<const float*>(w_r), lbias, T, h, E, lg);
+            if (int rc = check_launch("router_logits_gemm")) return rc;
+            const size_t smem = (size_t)kRouterWarps * E * sizeof(float) + (size_t)E * sizeof(int);
+            const int npl = cdiv(E, 32);
+            o.logits = nullptr;
+#define MOE_GATE_LAUNCH(N)                                                                              \
+            cudaFuncSetAttribute(router_gate_kernel<N>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem); \
+            router_gate_kernel<N><<<G, kRouterWarps * 32, smem, s>>>(lg, bias, T, E, k, gating, o);
+            if (npl <= 2) { MOE_GATE_LAUNCH(2) }
+            else if (npl <= 4) { MOE_GATE_LAUNCH(4) }
+            else if (npl <= 8) { MOE_GATE_LAUNCH(8) }
+            else if (npl <= 16) { MOE_GATE_LAUNCH(16) }
+            else { MOE_GATE_LAUNCH(32) }
+#undef MOE_GATE_LAUNCH
+            if (int rc = check_launch("router_gate_kernel")) return rc;
+        }
+    }
+    router_finalize<<<1, 1024, 0, s>>>(w.partial_P, w.partial_C, T > 0 ? G : 0, T, E, k, alpha, counts, f, P, aux);
+    return check_launch("router_finalize");
+}

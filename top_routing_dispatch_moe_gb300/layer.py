@@ -1,0 +1,104 @@
+"""One MoE layer forward over preallocated device buffers, chaining the four C-ABI calls.
+
+router ("Megatron-LM 分布式训练（六）", section "Router") -> dispatch ("v6 长序列和 MoE", table row
+"dispatch") -> grouped SwiGLU expert FFN (table row "expert"; shared expert per the data flow of the
+Megatron page) -> combine (table row "combine"). All work is enqueued on one stream with no host sync.
+"""
+from __future__ import annotations
+
+import math
+
+import torch
+
+from . import moe
+
+
+def capacity_slots(cf: float, k: int, T: int, E: int) -> int:
+    """Per-expert capacity C = cf * k * T / E rounded up ("v6 长序列和 MoE", "Capacity" bullet); 0 = dropless."""
+    if cf <= 0:
+        return 0
+    return int(math.ceil(cf * k * T / E - 1e-9))
+
+
+class MoELayer:
+    """Holds the packed expert weights, the router weight and every intermediate buffer of one layer.
+
+    Stages (in order): "router", "dispatch", "up_gate", "down", ["shared_up_gate", "shared_down"], "combine".
+    forward(x, events=...) records one CUDA event before the first stage and after each stage when given
+    a dict of lists, so callers can time the stages on the launching stream."""
+
+    STAGES = ("router", "dispatch", "up_gate", "down", "shared_up_gate", "shared_down", "combine")
+
+    def __init__(self, *, T, h, E, k, F, gating, cf, R, alpha, w_r, bias, w_gate, w_up, w_down,
+                 shared=None, device="cuda"):
+        self.T, self.h, self.E, self.k, self.F = T, h, E, k, F
+        self.gating, self.R, self.alpha = gating, R, alpha
+        self.C = capacity_slots(cf, k, T, E)
+        self.dtype = w_r.dtype
+        dt = self.dtype
+        dev = torch.device(device)
+        self.device = dev
+        self.w_r = w_r
+        self.bias = bias
+        self.packed = moe.moe_pack_expert_weights(w_gate, w_up, w_down)
+        self.shared_packed = moe.moe_pack_expert_weights(*shared) if shared is not None else None
+        i32, f32 = torch.int32, torch.float32
+        code = moe.dtype_code(dt)
+        self.rows = moe.moe_dispatch_rows(T, E, k, self.C)
+        self.r_out = dict(logits=torch.empty((T, E), dtype=f32, device=dev),
+                          topk_ids=torch.empty((T, k), dtype=i32, device=dev),
+                          gates=torch.empty((T, k), dtype=f32, device=dev),
+                          counts=torch.empty(E, dtype=i32, device=dev), f=torch.empty(E, dtype=f32, device=dev),
+                          P=torch.empty(E, dtype=f32, device=dev), aux=torch.empty(1, dtype=f32, device=dev))
+        self.r_ws = moe._bytes_tensor(moe.moe_router_workspace_size(T, h, E, k, code), dev)
+        self.d_out = dict(buf=torch.empty((self.rows, h), dtype=dt, device=dev),
+                          offsets=torch.empty(E + 1, dtype=i32, device=dev),
+                          kept_counts=torch.empty(E, dtype=i32, device=dev),
+                          dest_row=torch.empty((T, k), dtype=i32, device=dev),
+                          drop_mask=torch.empty((T, k), dtype=torch.uint8, device=dev),
+                          src_token=torch.empty(self.rows, dtype=i32, device=dev),
+                          src_slot=torch.empty(self.rows, dtype=i32, device=dev),
+                          rank_counts=torch.empty(R, dtype=i32, device=dev),
+                          rank_offsets=torch.empty(R + 1, dtype=i32, device=dev),
+                          tile_sched=torch.empty(moe.moe_tile_sched_bytes(T, E, k, self.C) // 4, dtype=i32,
+                                                 device=dev))
+        self.d_ws = moe._bytes_tensor(moe.moe_dispatch_workspace_size(T, E, k, self.C), dev)
+        self.act = torch.empty((self.rows, F), dtype=dt, device=dev)
+        self.eout = torch.empty((self.rows, h), dtype=dt, device=dev)
+        if self.shared_packed is not None:
+            self.sh_sched = moe.moe_dense_tile_sched(T, device=dev)
+            self.sh_act = torch.empty((T, F), dtype=dt, device=dev)
+            self.sh_out = torch.empty((T, h), dtype=dt, device=dev)
+        self.y = torch.empty((T, h), dtype=dt, device=dev)
+
+    def forward(self, x, stream=None, events=None):
+        def mark(stage):
+            if events is not None:
+                ev = torch.cuda.Event(enable_timing=True)
+                ev.record(stream if stream is not None else torch.cuda.current_stream())
+                events.setdefault(stage, []).append(ev)
+
+        mark("start")
+        r = self.r_out
+        moe.moe_router(x, self.w_r, self.bias, self.k, self.gating, self.alpha, logits=r["logits"],
+                       topk_ids=r["topk_ids"], gates=r["gates"], counts=r["counts"], f=r["f"], P=r["P"], aux=r["aux"],
+                       ws=self.r_ws, stream=stream)
+        mark("router")
+        moe.moe_dispatch(x, r["topk_ids"], self.E, self.C, self.R, out=self.d_out, ws=self.d_ws, stream=stream)
+        mark("dispatch")
+        sched = self.d_out["tile_sched"]
+        moe.moe_expert_up_gate(self.d_out["buf"], sched, self.packed, self.E, self.F, act=self.act, stream=stream)
+        mark("up_gate")
+        moe.moe_expert_down(self.act, sched, self.packed, self.E, self.h, eout=self.eout, stream=stream)
+        mark("down")
+        shared_out = None
+        if self.shared_packed is not None:
+            moe.moe_expert_up_gate(x, self.sh_sched, self.shared_packed, 1, self.F, act=self.sh_act, stream=stream)
+            mark("shared_up_gate")
+            moe.moe_expert_down(self.sh_act, self.sh_sched, self.shared_packed, 1, self.h, eout=self.sh_out,
+                                stream=stream)
+            mark("shared_down")
+            shared_out = self.sh_out
+        moe.moe_combine(self.eout, self.d_out["dest_row"], r["gates"], shared_out, y=self.y, stream=stream)
+        mark("combine")
+        return self.y

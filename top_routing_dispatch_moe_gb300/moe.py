@@ -1,0 +1,254 @@
+"""Python binding of the C-ABI library libmoe_gb300.so (argument marshalling only).
+
+Every function has the name of the C entry point it calls and takes torch tensors for the device buffers;
+all computation happens in the library's CUDA kernels. Torch provides device memory and the stream.
+Importing this module fails loudly if the library has not been built (there is no fallback path).
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import torch
+
+_LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libmoe_gb300.so")
+if not os.path.exists(_LIB_PATH):
+    raise ImportError(f"{_LIB_PATH} is missing: build it first (python -m top_routing_dispatch_moe_gb300.build)")
+_lib = ctypes.CDLL(_LIB_PATH)
+
+MOE_OK, MOE_ERR_INVALID_ARG, MOE_ERR_UNSUPPORTED, MOE_ERR_WORKSPACE, MOE_ERR_CUDA, MOE_ERR_TIMEOUT = range(6)
+MOE_F32, MOE_BF16 = 0, 1
+GATING = {"softmax": 0, "softmax_renorm": 1, "sigmoid_bias_renorm": 2}
+TILE_M = 128
+
+_P, _I, _Z, _F, _LL = ctypes.c_void_p, ctypes.c_int, ctypes.c_size_t, ctypes.c_float, ctypes.c_longlong
+_SIGS = {
+    "moe_router_workspace_size": (_Z, [_I, _I, _I, _I, _I]),
+    "moe_router": (_I, [_P, _P, _P, _I, _I, _I, _I, _I, _I, _F, _P, _P, _P, _P, _P, _P, _P, _P, _Z, _P]),
+    "moe_dispatch_rows": (_Z, [_I, _I, _I, _I]),
+    "moe_tile_sched_bytes": (_Z, [_I, _I, _I, _I]),
+    "moe_dispatch_workspace_size": (_Z, [_I, _I, _I, _I]),
+    "moe_dispatch": (_I, [_P, _P, _I, _I, _I, _I, _I, _I, _I, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _Z, _P]),
+    "moe_dense_tile_sched": (_I, [_I, _P, _P]),
+    "moe_packed_weights_bytes": (_Z, [_I, _I, _I, _I]),
+    "moe_pack_expert_weights": (_I, [_P, _P, _P, _I, _I, _I, _I, _P, _P]),
+    "moe_expert_up_gate": (_I, [_P, _P, _P, _I, _I, _I, _I, _I, _P, _P]),
+    "moe_expert_down": (_I, [_P, _P, _P, _I, _I, _I, _I, _I, _P, _P]),
+    "moe_expert_ffn_workspace_size": (_Z, [_I, _I, _I]),
+    "moe_expert_ffn": (_I, [_P, _P, _P, _I, _I, _I, _I, _I, _P, _P, _Z, _P]),
+    "moe_combine": (_I, [_P, _P, _P, _P, _I, _I, _I, _I, _P, _P]),
+    "moe_last_error_string": (ctypes.c_char_p, []),
+    "moe_check_device_error": (_I, [_P]),
+    "moe_set_wait_limit": (None, [_LL]),
+    "moe_version": (ctypes.c_char_p, []),
+    "moe_launch_count": (ctypes.c_ulonglong, []),
+}
+for _name, (_res, _args) in _SIGS.items():
+    _fn = getattr(_lib, _name)
+    _fn.restype = _res
+    _fn.argtypes = _args
+
+EXPORTED = sorted(_SIGS)
+LIB_PATH = _LIB_PATH
+
+
+class MoEError(RuntimeError):
+    def __init__(self, code: int, msg: str):
+        super().__init__(f"[moe status {code}] {msg}")
+        self.code = code
+
+
+def _check(rc: int):
+    if rc != MOE_OK:
+        raise MoEError(rc, _lib.moe_last_error_string().decode(errors="replace"))
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream):
+    s = torch.cuda.current_stream() if stream is None else stream
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def dtype_code(dt: torch.dtype) -> int:
+    if dt == torch.float32:
+        return MOE_F32
+    if dt == torch.bfloat16:
+        return MOE_BF16
+    raise MoEError(MOE_ERR_UNSUPPORTED, f"dtype {dt}")
+
+
+def _bytes_tensor(nbytes: int, device) -> torch.Tensor:
+    return torch.empty(max(int(nbytes), 16), dtype=torch.uint8, device=device)
+
+
+# ------------------------------------------------------------------------------------------------ router
+
+def moe_router_workspace_size(T, h, E, k, dtype) -> int:
+    return _lib.moe_router_workspace_size(T, h, E, k, dtype)
+
+
+def moe_router(x, w_r, bias, k: int, gating: str | int = "softmax", alpha: float = 0.01, *, logits=None,
+               topk_ids=None, gates=None, counts=None, f=None, P=None, aux=None, ws=None, stream=None,
+               want_logits=True):
+    T, h = x.shape
+    E = w_r.shape[1]
+    dev = x.device
+    dt = dtype_code(x.dtype)
+    g = GATING[gating] if isinstance(gating, str) else int(gating)
+    if logits is None and want_logits:
+        logits = torch.empty((T, E), dtype=torch.float32, device=dev)
+    topk_ids = torch.empty((T, k), dtype=torch.int32, device=dev) if topk_ids is None else topk_ids
+    gates = torch.empty((T, k), dtype=torch.float32, device=dev) if gates is None else gates
+    counts = torch.empty(E, dtype=torch.int32, device=dev) if counts is None else counts
+    f = torch.empty(E, dtype=torch.float32, device=dev) if f is None else f
+    P = torch.empty(E, dtype=torch.float32, device=dev) if P is None else P
+    aux = torch.empty(1, dtype=torch.float32, device=dev) if aux is None else aux
+    need = moe_router_workspace_size(T, h, E, k, dt)
+    ws = _bytes_tensor(need, dev) if ws is None else ws
+    _check(_lib.moe_router(_ptr(x), _ptr(w_r), _ptr(bias), T, h, E, k, dt, g, alpha, _ptr(logits), _ptr(topk_ids),
+                           _ptr(gates), _ptr(counts), _ptr(f), _ptr(P), _ptr(aux), _ptr(ws), ws.numel(),
+                           _stream(stream)))
+    return dict(logits=logits, ids=topk_ids, gates=gates, counts=counts, f=f, P=P, aux=aux)
+
+
+# ---------------------------------------------------------------------------------------------- dispatch
+
+def moe_dispatch_rows(T, E, k, capacity) -> int:
+    return _lib.moe_dispatch_rows(T, E, k, capacity)
+
+
+def moe_tile_sched_bytes(T, E, k, capacity) -> int:
+    return _lib.moe_tile_sched_bytes(T, E, k, capacity)
+
+
+def moe_dispatch_workspace_size(T, E, k, capacity) -> int:
+    return _lib.moe_dispatch_workspace_size(T, E, k, capacity)
+
+
+def moe_dispatch(x, topk_ids, E: int, capacity: int = 0, num_ranks: int = 1, *, out=None, ws=None, stream=None):
+    """Returns dict(buf, offsets, kept_counts, dest_row, drop_mask, src_token, src_slot, rank_counts,
+    rank_offsets, tile_sched). `out` may hold preallocated tensors under those names."""
+    T, h = x.shape
+    k = topk_ids.shape[1]
+    dev = x.device
+    dt = dtype_code(x.dtype)
+    rows = moe_dispatch_rows(T, E, k, capacity)
+    o = dict(out or {})
+    o.setdefault("buf", torch.empty((rows, h), dtype=x.dtype, device=dev))
+    o.setdefault("offsets", torch.empty(E + 1, dtype=torch.int32, device=dev))
+    o.setdefault("kept_counts", torch.empty(E, dtype=torch.int32, device=dev))
+    o.setdefault("dest_row", torch.empty((T, k), dtype=torch.int32, device=dev))
+    o.setdefault("drop_mask", torch.empty((T, k), dtype=torch.uint8, device=dev))
+    o.setdefault("src_token", torch.empty(rows, dtype=torch.int32, device=dev))
+    o.setdefault("src_slot", torch.empty(rows, dtype=torch.int32, device=dev))
+    o.setdefault("rank_counts", torch.empty(num_ranks, dtype=torch.int32, device=dev))
+    o.setdefault("rank_offsets", torch.empty(num_ranks + 1, dtype=torch.int32, device=dev))
+    o.setdefault("tile_sched", torch.empty(moe_tile_sched_bytes(T, E, k, capacity) // 4, dtype=torch.int32,
+                                           device=dev))
+    need = moe_dispatch_workspace_size(T, E, k, capacity)
+    ws = _bytes_tensor(need, dev) if ws is None else ws
+    _check(_lib.moe_dispatch(_ptr(x), _ptr(topk_ids), T, h, E, k, capacity, num_ranks, dt, _ptr(o["buf"]),
+                             _ptr(o["offsets"]), _ptr(o["kept_counts"]), _ptr(o["dest_row"]), _ptr(o["drop_mask"]),
+                             _ptr(o["src_token"]), _ptr(o["src_slot"]), _ptr(o["rank_counts"]),
+                             _ptr(o["rank_offsets"]), _ptr(o["tile_sched"]), _ptr(ws), ws.numel(), _stream(stream)))
+    o["rows"] = rows
+    return o
+
+
+def moe_dense_tile_sched(rows: int, tile_sched=None, device="cuda", stream=None):
+    if tile_sched is None:
+        tile_sched = torch.empty(moe_tile_sched_bytes(rows, 1, 1, 0) // 4, dtype=torch.int32, device=device)
+    _check(_lib.moe_dense_tile_sched(rows, _ptr(tile_sched), _stream(stream)))
+    return tile_sched
+
+
+# ------------------------------------------------------------------------------------------------ experts
+
+def moe_packed_weights_bytes(E, h, F, dtype) -> int:
+    return _lib.moe_packed_weights_bytes(E, h, F, dtype)
+
+
+def moe_pack_expert_weights(w_gate, w_up, w_down, packed=None, stream=None):
+    E, F, h = w_gate.shape
+    dt = dtype_code(w_gate.dtype)
+    if packed is None:
+        packed = _bytes_tensor(moe_packed_weights_bytes(E, h, F, dt), w_gate.device)
+    _check(_lib.moe_pack_expert_weights(_ptr(w_gate), _ptr(w_up), _ptr(w_down), E, h, F, dt, _ptr(packed),
+                                        _stream(stream)))
+    return packed
+
+
+def moe_expert_up_gate(buf, tile_sched, packed_w, E: int, F: int, act=None, stream=None):
+    rows, h = buf.shape
+    if act is None:
+        act = torch.empty((rows, F), dtype=buf.dtype, device=buf.device)
+    _check(_lib.moe_expert_up_gate(_ptr(buf), _ptr(tile_sched), _ptr(packed_w), E, h, F, rows, dtype_code(buf.dtype),
+                                   _ptr(act), _stream(stream)))
+    return act
+
+
+def moe_expert_down(act, tile_sched, packed_w, E: int, h: int, eout=None, stream=None):
+    rows, F = act.shape
+    if eout is None:
+        eout = torch.empty((rows, h), dtype=act.dtype, device=act.device)
+    _check(_lib.moe_expert_down(_ptr(act), _ptr(tile_sched), _ptr(packed_w), E, h, F, rows, dtype_code(act.dtype),
+                                _ptr(eout), _stream(stream)))
+    return eout
+
+
+def moe_expert_ffn_workspace_size(rows, F, dtype) -> int:
+    return _lib.moe_expert_ffn_workspace_size(rows, F, dtype)
+
+
+def moe_expert_ffn(buf, tile_sched, packed_w, E: int, F: int, eout=None, ws=None, stream=None):
+    rows, h = buf.shape
+    dt = dtype_code(buf.dtype)
+    if eout is None:
+        eout = torch.empty((rows, h), dtype=buf.dtype, device=buf.device)
+    need = moe_expert_ffn_workspace_size(rows, F, dt)
+    ws = _bytes_tensor(need, buf.device) if ws is None else ws
+    _check(_lib.moe_expert_ffn(_ptr(buf), _ptr(tile_sched), _ptr(packed_w), E, h, F, rows, dt, _ptr(eout), _ptr(ws),
+                               ws.numel(), _stream(stream)))
+    return eout
+
+
+# ------------------------------------------------------------------------------------------------ combine
+
+def moe_combine(eout, dest_row, gates, shared_out=None, y=None, stream=None):
+    T, k = dest_row.shape
+    h = eout.shape[1]
+    if y is None:
+        y = torch.empty((T, h), dtype=eout.dtype, device=eout.device)
+    _check(_lib.moe_combine(_ptr(eout), _ptr(dest_row), _ptr(gates), _ptr(shared_out), T, h, k,
+                            dtype_code(eout.dtype), _ptr(y), _stream(stream)))
+    return y
+
+
+# ------------------------------------------------------------------------------------------------ errors
+
+def moe_last_error_string() -> str:
+    return _lib.moe_last_error_string().decode(errors="replace")
+
+
+def moe_check_device_error(stream=None) -> int:
+    return _lib.moe_check_device_error(_stream(stream))
+
+
+def moe_set_wait_limit(spins: int):
+    _lib.moe_set_wait_limit(int(spins))
+
+
+def moe_launch_count() -> int:
+    return int(_lib.moe_launch_count())
+
+
+def moe_version() -> str:
+    return _lib.moe_version().decode()
+
+
+def raw_lib():
+    """The ctypes handle (tests call entry points with raw pointers through it)."""
+    return _lib
