@@ -85,6 +85,7 @@ __device__ __forceinline__ void gate_token(float (&L)[NPL], int t, int E, int k,
             for (int i = 0; i < NPL; ++i)
                 if (score[i] > bv) { bv = score[i]; bi = lane + 32 * i; }   // strict: lower index on ties
             warp_argmax(bv, bi);
+            if (bi >= E) bi = E - 1;          // only reachable with NaN scores: keeps every index in bounds
             const int owner = bi & 31, slot = bi >> 5;
             float pv = 0.f;
 #pragma unroll
