@@ -231,7 +231,8 @@ def run_gpu(args, cfg, C):
                      alpha=cfg.alpha, w_r=up(inp["w_r"]),
                      bias=torch.from_numpy(inp["bias"]).to(dev) if inp["bias"] is not None else None,
                      w_gate=up(inp["wg"]), w_up=up(inp["wu"]), w_down=up(inp["wd"]),
-                     shared=tuple(up(w) for w in inp["shared"]) if inp["shared"] is not None else None, device=dev)
+                     shared=tuple(up(np.ascontiguousarray(w)[None]) for w in inp["shared"])
+                     if inp["shared"] is not None else None, device=dev)
     x = up(inp["x"])
     flush = torch.empty(512 * 2**20, dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream()

@@ -106,7 +106,7 @@ def build_gpu_layer(cfg, inp, wg, wu, wd, shared=None, device="cuda"):
     b = torch.from_numpy(inp["bias"]).to(dev) if inp["bias"] is not None else None
     sh = None
     if shared is not None:
-        sh = tuple(to_device(w, cfg, dev) for w in shared)
+        sh = tuple(to_device(np.ascontiguousarray(w)[None], cfg, dev) for w in shared)   # one expert: [1, ...]
     layer = MoELayer(T=cfg.T, h=cfg.h, E=cfg.E, k=cfg.k, F=cfg.F, gating=cfg.gating, cf=cfg.cf, R=cfg.R,
                      alpha=cfg.alpha, w_r=to_device(inp["w_r"], cfg, dev), bias=b, w_gate=to_device(wg, cfg, dev),
                      w_up=to_device(wu, cfg, dev), w_down=to_device(wd, cfg, dev), shared=sh, device=dev)

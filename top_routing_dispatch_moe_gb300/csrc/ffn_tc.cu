@@ -1,12 +1,431 @@
-// placeholder: tcgen05 grouped GEMM (bf16) -- temporarily routed to the CUDA-core kernels
+// Grouped SwiGLU expert FFN on the 5th-generation tensor cores (tcgen05, sm_103a), bf16 operands with
+// fp32 accumulation in tensor memory.
+//
+// "Megatron-LM 分布式训练（六）", data flow: the local experts run as one GroupedGEMM; "v6 长序列和 MoE",
+// table row "expert" (each expert's FFN h -> F -> h) and the follow-up note (sort tokens by expert, one
+// grouped GEMM instead of E small launches).
+//
+// One persistent kernel per GEMM, one CTA per SM, 6 warps with fixed roles:
+//   warp 0  TMA producer: 128x64 A tiles (token rows of one expert) and 256x64 B tiles (weight rows) into a
+//           4-stage shared-memory ring, 128-byte swizzled, completion counted on one mbarrier per stage;
+//   warp 1  allocates all 512 tensor-memory columns (two 128x256 fp32 accumulators) and issues the
+//           tcgen05.mma (M=128, N=256, K=16) from one thread; tcgen05.commit frees a stage once the MMAs
+//           that read it are done and signals a full accumulator after the last K step;
+//   warps 2-5  epilogue: tcgen05.ld of the accumulator rows (one TMEM lane = one output row per thread),
+//           then either silu(gate) * up -> bf16 act (up/gate GEMM; the packed B tile holds 128 gate and the
+//           matching 128 up rows) or a plain bf16 conversion (down GEMM), masked to the expert's rows.
+// The two accumulators let the epilogue of tile i overlap the MMAs of tile i+1.
+//
+// Work items are (m-tile, n-tile) pairs over the device tile schedule written by dispatch, ordered expert by
+// expert, n-tile by n-tile, m-tile fastest: CTAs running at the same time share one expert's token rows and
+// one 256-row weight tile, so weights are read from HBM about once. Nothing about the routing is known on
+// the host: the kernel reads the tile count and per-expert tile prefix from device memory.
+//
+// Every mbarrier wait is bounded. A wait that runs out latches MOE_ERR_TIMEOUT into the device error word
+// and raises a CTA-wide abort flag; every role then leaves its loop, the producer waits (bounded) for its
+// TMA copies in flight, the MMA thread waits (bounded) for its MMAs, and the tensor memory is freed before
+// the CTA exits.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+#include <math.h>
+#include <mutex>
 #include "ffn.cuh"
+
 namespace moe {
+namespace tc {
+
+constexpr int BM = 128;                      // rows per tile (UMMA M, one TMEM lane per row)
+constexpr int BN = 256;                      // columns per tile (UMMA N)
+constexpr int BK = 64;                       // K per stage: 64 bf16 = one 128-byte swizzle row
+constexpr int UK = 16;                       // K per tcgen05.mma (kind::f16)
+constexpr int STAGES = 4;
+constexpr int A_BYTES = BM * BK * 2;         // 16 KB
+constexpr int B_BYTES = BN * BK * 2;         // 32 KB
+constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
+constexpr int TMEM_COLS = 512;               // 2 accumulators x 256 fp32 columns
+constexpr int NUM_THREADS = 192;
+constexpr int SMEM_BYTES = 1024 /* alignment slack */ + STAGES * STAGE_BYTES + 256 /* barriers, flags */;
+constexpr long long kDrainLimit = 1LL << 24;
+
+// ---------------------------------------------------------------------------------------------------
+// PTX wrappers
+// ---------------------------------------------------------------------------------------------------
+__device__ __forceinline__ uint32_t smem_u32(const void* p) { return (uint32_t)__cvta_generic_to_shared(p); }
+
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
+}
+__device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes) : "memory");
+}
+__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
+// Bounded wait: true when the phase completed; false when another role aborted or the limit ran out
+// (then the abort flag is raised and the timeout latched).
+__device__ __forceinline__ bool wait_phase(uint32_t bar, uint32_t parity, long long limit, volatile int* abort_flag,
+                                           unsigned* err, unsigned site) {
+    for (long long i = 0; i < limit; ++i) {
+        if (mbar_try_wait(bar, parity)) return true;
+        if (*abort_flag) return false;
+    }
+    *abort_flag = 1;
+    latch_device_error(err, kDevErrTimeout, site);
+    return false;
+}
+// Drain wait at exit: no abort check, fixed limit.
+__device__ __forceinline__ void drain_phase(uint32_t bar, uint32_t parity, unsigned* err, unsigned site) {
+    for (long long i = 0; i < kDrainLimit; ++i)
+        if (mbar_try_wait(bar, parity)) return;
+    latch_device_error(err, kDevErrTimeout, site);
+}
+
+__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map, int x, int y, uint32_t bar) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];"
+        ::"r"(dst), "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(bar)
+        : "memory");
+}
+__device__ __forceinline__ void prefetch_tmap(const CUtensorMap* map) {
+    asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
+}
+
+__device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
+__device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
+
+__device__ __forceinline__ void tmem_alloc(uint32_t slot_smem, uint32_t ncols) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(slot_smem), "r"(ncols)
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols) : "memory");
+}
+
+// D[tmem] (+)= A[smem] * B[smem]^T, A: M x K (K-major), B: N x K (K-major), bf16 in, fp32 accumulate.
+__device__ __forceinline__ void umma_bf16(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
+                                          uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}"
+        ::"r"(d_tmem), "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+// Arrive on an mbarrier once every tcgen05 operation this thread issued before has completed.
+__device__ __forceinline__ void umma_commit(uint32_t bar) {
+    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
+                 : "memory");
+}
+
+// 32 consecutive fp32 columns of this warp's 32 TMEM lanes (one row per thread).
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, float (&v)[32]) {
+    uint32_t r[32];
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
+        "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
+        "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+          "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]),
+          "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]),
+          "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+        : "r"(taddr)
+        : "memory");
+    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+#pragma unroll
+    for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
+}
+
+// Shared-memory matrix descriptor of a K-major tile written by TMA with 128-byte swizzling: rows of 128
+// bytes, 8-row core groups 1024 bytes apart (stride byte offset), leading byte offset unused for this
+// layout (set to 16 bytes), descriptor version 1 (bits 46-48), swizzle mode 2 = 128B (bits 61-63).
+__device__ __forceinline__ uint64_t sw128_desc(uint32_t saddr) {
+    uint64_t d = 0;
+    d |= (uint64_t)((saddr & 0x3FFFFu) >> 4);          // start address
+    d |= (uint64_t)(16u >> 4) << 16;                     // leading byte offset
+    d |= (uint64_t)(1024u >> 4) << 32;                   // stride byte offset
+    d |= (uint64_t)1 << 46;                              // version
+    d |= (uint64_t)2 << 61;                              // 128B swizzle
+    return d;
+}
+
+// Instruction descriptor, kind::f16: D fp32 (bits 4-5 = 1), A and B bf16 (bits 7-9, 10-12 = 1), both
+// K-major (bits 15, 16 = 0), N >> 3 at bits 17-22, M >> 4 at bits 24-28.
+constexpr uint32_t kIdesc = (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(BN >> 3) << 17) | ((uint32_t)(BM >> 4) << 24);
+
+struct Params {
+    const int32_t* sched;
+    int K;              // reduction length
+    int NT;             // n-tiles per expert
+    int b_rows;         // B rows per expert in the B tensor map (2 Fp for up/gate, h for down)
+    int n_valid;        // valid output columns (F for up/gate, h for down)
+    int ldo;            // output leading dimension
+    __nv_bfloat16* out;
+    unsigned* err;
+    long long wait_limit;
+};
+
+struct Work { int e, row0, row1, n; };
+
+// Work item w -> (expert, rows, n-tile), expert-major, n-tile next, m-tile fastest.
+__device__ __forceinline__ Work map_work(const int32_t* sched, int E, int NT, int w) {
+    const int32_t* prefix = sched + kSchedHeader;
+    int lo = 0, hi = E;                      // find last e with prefix[e] * NT <= w
+    while (lo < hi) {
+        const int mid = (lo + hi + 1) >> 1;
+        if ((long long)__ldg(prefix + mid) * NT <= w) lo = mid; else hi = mid - 1;
+    }
+    const int e = lo;
+    const int p0 = __ldg(prefix + e), mt = __ldg(prefix + e + 1) - p0;
+    const int local = w - p0 * NT;
+    const int n = local / mt, m = p0 + local % mt;
+    const int4 ent = __ldg(reinterpret_cast<const int4*>(sched + sched_tiles_offset(E)) + m);
+    return Work{ent.x, ent.y, ent.z, n};
+}
+
+template <bool SWIGLU>
+__global__ void __launch_bounds__(NUM_THREADS, 1)
+grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB, Params p) {
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t raw_addr = smem_u32(smem_raw);
+    uint8_t* smem = smem_raw + ((1024u - (raw_addr & 1023u)) & 1023u);
+    const uint32_t sbase = smem_u32(smem);
+    const uint32_t sA = sbase, sB = sbase + STAGES * A_BYTES;
+    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + STAGES * STAGE_BYTES);
+    const uint32_t bar0 = smem_u32(bars);
+    auto full = [&](int s) { return bar0 + 8u * s; };
+    auto empty = [&](int s) { return bar0 + 8u * (STAGES + s); };
+    auto tfull = [&](int a) { return bar0 + 8u * (2 * STAGES + a); };
+    auto tempty = [&](int a) { return bar0 + 8u * (2 * STAGES + 2 + a); };
+    const uint32_t mma_done = bar0 + 8u * (2 * STAGES + 4);
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * STAGES + 5);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < STAGES; ++s) { mbar_init(full(s), 1); mbar_init(empty(s), 1); }
+        for (int a = 0; a < 2; ++a) { mbar_init(tfull(a), 1); mbar_init(tempty(a), 4); }
+        mbar_init(mma_done, 1);
+        *abort_flag = 0;
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+        prefetch_tmap(&tmA);
+        prefetch_tmap(&tmB);
+    }
+    if (warp == 1) tmem_alloc(smem_u32(tmem_slot), TMEM_COLS);
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+
+    const int E = __ldg(p.sched + 1);
+    const int total = __ldg(p.sched) * p.NT;
+    const int KB = (p.K + BK - 1) / BK;
+
+    if (warp == 0) {
+        if (lane == 0) {
+            // ------------------------------------------------------------------ TMA producer
+            int stage = 0;
+            uint32_t phase = 0, issued = 0, last_par = 0;
+            for (int w = blockIdx.x; w < total && !*abort_flag; w += gridDim.x) {
+                const Work wk = map_work(p.sched, E, p.NT, w);
+                const int brow = wk.e * p.b_rows + wk.n * BN;
+                bool ok = true;
+                for (int kb = 0; kb < KB; ++kb) {
+                    if (!wait_phase(empty(stage), phase ^ 1u, p.wait_limit, abort_flag, p.err, 0x10u)) { ok = false; break; }
+                    mbar_expect_tx(full(stage), STAGE_BYTES);
+                    tma_load_2d(sA + stage * A_BYTES, &tmA, kb * BK, wk.row0, full(stage));
+                    tma_load_2d(sB + stage * B_BYTES, &tmB, kb * BK, brow, full(stage));
+                    issued |= 1u << stage;
+                    last_par = (last_par & ~(1u << stage)) | (phase << stage);
+                    if (++stage == STAGES) { stage = 0; phase ^= 1u; }
+                }
+                if (!ok) break;
+            }
+            for (int s = 0; s < STAGES; ++s)        // every issued copy has landed before the CTA exits
+                if (issued & (1u << s)) drain_phase(full(s), (last_par >> s) & 1u, p.err, 0x11u);
+        }
+    } else if (warp == 1) {
+        if (lane == 0) {
+            // ------------------------------------------------------------------ MMA issuer
+            int stage = 0;
+            uint32_t phase = 0;
+            int iter = 0;
+            for (int w = blockIdx.x; w < total && !*abort_flag; w += gridDim.x, ++iter) {
+                const int a = iter & 1;
+                const uint32_t aph = (iter >> 1) & 1;
+                if (!wait_phase(tempty(a), aph ^ 1u, p.wait_limit, abort_flag, p.err, 0x20u)) break;
+                tc_fence_after();
+                const uint32_t d_tmem = tmem + (uint32_t)(a * BN);
+                bool ok = true;
+                for (int kb = 0; kb < KB; ++kb) {
+                    if (!wait_phase(full(stage), phase, p.wait_limit, abort_flag, p.err, 0x21u)) { ok = false; break; }
+                    tc_fence_after();
+                    const uint32_t a_s = sA + stage * A_BYTES, b_s = sB + stage * B_BYTES;
+#pragma unroll
+                    for (int k = 0; k < BK / UK; ++k)
+                        umma_bf16(d_tmem, sw128_desc(a_s + k * UK * 2), sw128_desc(b_s + k * UK * 2), kIdesc,
+                                  (kb | k) != 0);
+                    umma_commit(empty(stage));
+                    if (++stage == STAGES) { stage = 0; phase ^= 1u; }
+                }
+                if (!ok) break;
+                umma_commit(tfull(a));
+            }
+            umma_commit(mma_done);                  // all MMAs finished before the columns are freed
+            drain_phase(mma_done, 0, p.err, 0x22u);
+        }
+    } else {
+        // ---------------------------------------------------------------------- epilogue (warps 2..5)
+        const int lane_base = 32 * (warp & 3);
+        int iter = 0;
+        for (int w = blockIdx.x; w < total; w += gridDim.x, ++iter) {
+            const int a = iter & 1;
+            const uint32_t aph = (iter >> 1) & 1;
+            if (!wait_phase(tfull(a), aph, p.wait_limit, abort_flag, p.err, 0x30u)) break;
+            tc_fence_after();
+            const Work wk = map_work(p.sched, E, p.NT, w);
+            const int row = wk.row0 + lane_base + lane;
+            const bool live = row < wk.row1;
+            const uint32_t tbase = tmem + (uint32_t)(a * BN) + ((uint32_t)lane_base << 16);
+            if constexpr (SWIGLU) {
+#pragma unroll 1
+                for (int j = 0; j < 4; ++j) {
+                    float g[32], u[32];
+                    tmem_ld32(tbase + 32 * j, g);
+                    tmem_ld32(tbase + 128 + 32 * j, u);
+                    const int f0 = wk.n * 128 + 32 * j;
+                    if (live) {
+                        __nv_bfloat16* dst = p.out + (size_t)row * p.ldo + f0;
+#pragma unroll
+                        for (int c = 0; c < 32; c += 8) {
+                            if (f0 + c < p.n_valid) {
+                                Vec16<__nv_bfloat16> o;
+#pragma unroll
+                                for (int i = 0; i < 8; ++i) {
+                                    const float gv = g[c + i];
+                                    o.set(i, gv / (1.f + expf(-gv)) * u[c + i]);
+                                }
+                                st16(dst + c, o);
+                            }
+                        }
+                    }
+                }
+            } else {
+#pragma unroll 1
+                for (int j = 0; j < 8; ++j) {
+                    float v[32];
+                    tmem_ld32(tbase + 32 * j, v);
+                    const int n0 = wk.n * BN + 32 * j;
+                    if (live) {
+                        __nv_bfloat16* dst = p.out + (size_t)row * p.ldo + n0;
+#pragma unroll
+                        for (int c = 0; c < 32; c += 8) {
+                            if (n0 + c < p.n_valid) {
+                                Vec16<__nv_bfloat16> o;
+#pragma unroll
+                                for (int i = 0; i < 8; ++i) o.set(i, v[c + i]);
+                                st16(dst + c, o);
+                            }
+                        }
+                    }
+                }
+            }
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(tempty(a));
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc(tmem, TMEM_COLS);
+    }
+}
+
+// ---------------------------------------------------------------------------------------------------
+// host: tensor maps and launch
+// ---------------------------------------------------------------------------------------------------
+static PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+    });
+    return fn;
+}
+
+// 2-D bf16 tensor [rows, cols] row-major, box [box_rows, 64 columns], 128-byte swizzle, zero fill.
+static int make_map(CUtensorMap* m, const void* base, long long rows, long long cols, int box_rows) {
+    auto fn = encode_fn();
+    MOE_REQUIRE(fn, MOE_ERR_CUDA, "cuTensorMapEncodeTiled unavailable from the driver");
+    cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
+    cuuint64_t strides[1] = {(cuuint64_t)cols * 2};
+    cuuint32_t box[2] = {(cuuint32_t)BK, (cuuint32_t)box_rows};
+    cuuint32_t estr[2] = {1, 1};
+    CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, estr,
+                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    MOE_REQUIRE(r == CUDA_SUCCESS, MOE_ERR_CUDA, "cuTensorMapEncodeTiled failed (%d) rows=%lld cols=%lld", (int)r,
+                rows, cols);
+    return MOE_OK;
+}
+
+template <bool SWIGLU>
+static int launch(const CUtensorMap& a, const CUtensorMap& b, const Params& p, cudaStream_t s) {
+    static bool attr_set[2] = {false, false};
+    if (!attr_set[SWIGLU]) {
+        cudaError_t e = cudaFuncSetAttribute(grouped_gemm_kernel<SWIGLU>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             SMEM_BYTES);
+        if (e != cudaSuccess) return set_error(MOE_ERR_CUDA, "grouped_gemm smem attribute: %s", cudaGetErrorString(e));
+        attr_set[SWIGLU] = true;
+    }
+    grouped_gemm_kernel<SWIGLU><<<num_sms(), NUM_THREADS, SMEM_BYTES, s>>>(a, b, p);
+    return check_launch(SWIGLU ? "grouped_gemm_kernel<up_gate>" : "grouped_gemm_kernel<down>");
+}
+
+}  // namespace tc
+
 int ffn_tc_up_gate(const void* buf, const int32_t* sched, const void* packed, int E, int h, int F, int rows, void* act,
                    cudaStream_t s) {
-    return ffn_simt_up_gate(buf, sched, packed, E, h, F, rows, MOE_BF16, act, s);
+    const PackedLayout L = packed_layout(E, h, F, 2);
+    CUtensorMap ma, mb;
+    if (int rc = tc::make_map(&ma, buf, rows, h, tc::BM)) return rc;
+    if (int rc = tc::make_map(&mb, static_cast<const char*>(packed) + L.up_gate_off, (long long)E * 2 * L.Fp, h, tc::BN))
+        return rc;
+    unsigned* err = device_error_word();
+    MOE_REQUIRE(err, MOE_ERR_CUDA, "device error word unavailable");
+    tc::Params p{sched, h, L.Fp / 128, 2 * L.Fp, F, F, static_cast<__nv_bfloat16*>(act), err, wait_limit()};
+    return tc::launch<true>(ma, mb, p, s);
 }
+
 int ffn_tc_down(const void* act, const int32_t* sched, const void* packed, int E, int h, int F, int rows, void* eout,
                 cudaStream_t s) {
-    return ffn_simt_down(act, sched, packed, E, h, F, rows, MOE_BF16, eout, s);
+    const PackedLayout L = packed_layout(E, h, F, 2);
+    CUtensorMap ma, mb;
+    if (int rc = tc::make_map(&ma, act, rows, F, tc::BM)) return rc;
+    if (int rc = tc::make_map(&mb, static_cast<const char*>(packed) + L.down_off, (long long)E * h, F, tc::BN))
+        return rc;
+    unsigned* err = device_error_word();
+    MOE_REQUIRE(err, MOE_ERR_CUDA, "device error word unavailable");
+    tc::Params p{sched, F, cdiv(h, tc::BN), h, h, h, static_cast<__nv_bfloat16*>(eout), err, wait_limit()};
+    return tc::launch<false>(ma, mb, p, s);
 }
+
 }  // namespace moe

@@ -141,10 +141,8 @@ router_small_kernel(const T* __restrict__ x, const T* __restrict__ w_r, const fl
     float* s_P = reinterpret_cast<float*>(smem_raw + (((size_t)E * h * sizeof(T) + 15) & ~(size_t)15));
     int* s_hist = reinterpret_cast<int*>(s_P + kRouterWarps * E);
 
-    for (int i = threadIdx.x; i < E * h; i += blockDim.x) {
-        const int d = i / E, e = i - d * E;
-        wT[(size_t)e * h + d] = w_r[i];
-    }
+    for (int d = threadIdx.x; d < h; d += blockDim.x)      // one router-weight row per thread: conflict-free
+        for (int e = 0; e < E; ++e) wT[(size_t)e * h + d] = w_r[(size_t)d * E + e];
     for (int e = threadIdx.x; e < E; e += blockDim.x) s_hist[e] = 0;
     __syncthreads();
 
@@ -290,7 +288,10 @@ router_finalize(const float* __restrict__ partial_P, const int32_t* __restrict__
 // ---------------------------------------------------------------------------------------------------
 // host
 // ---------------------------------------------------------------------------------------------------
+// Upper bound of the blocks of any router launch (sizes the partial-sum workspace).
 static int router_grid(int T) { return std::max(1, std::min(cdiv(T, kRouterWarps), kRouterMaxBlocks)); }
+// The fused small-E kernel stages the router weight in every block: two blocks per SM amortise it.
+static int router_small_grid(int T) { return std::max(1, std::min(router_grid(T), 2 * num_sms())); }
 
 static size_t small_smem_bytes(int h, int E, int el) {
     return align_up((size_t)E * h * el, 16) + (size_t)kRouterWarps * E * sizeof(float) + (size_t)E * sizeof(int);
@@ -332,7 +333,7 @@ extern "C" int moe_router(const void* x, const void* w_r, const float* bias, int
     MOE_REQUIRE(T >= 0 && h > 0 && h % 8 == 0, MOE_ERR_INVALID_ARG, "moe_router: T=%d h=%d (need T>=0, h%%8==0)", T, h);
     MOE_REQUIRE(E >= 1 && E <= 1024 && k >= 1 && k <= E && k <= kMaxK, MOE_ERR_INVALID_ARG,
                 "moe_router: E=%d k=%d (need 1<=k<=min(E,16), E<=1024)", E, k);
-    MOE_REQUIRE(w_r && topk_ids && gates && counts && f && P && aux && (T == 0 || x), MOE_ERR_INVALID_ARG,
+    MOE_REQUIRE(w_r && counts && f && P && aux && (T == 0 || (x && topk_ids && gates)), MOE_ERR_INVALID_ARG,
                 "moe_router: null pointer");
     MOE_REQUIRE(aligned16(x) && aligned16(w_r) && aligned16(logits), MOE_ERR_INVALID_ARG,
                 "moe_router: x, w_r and logits must be 16-byte aligned");
@@ -342,7 +343,7 @@ extern "C" int moe_router(const void* x, const void* w_r, const float* bias, int
     MOE_REQUIRE(ws_bytes >= w.bytes && (w.bytes == 0 || ws), MOE_ERR_WORKSPACE,
                 "moe_router: workspace %zu < %zu bytes", ws_bytes, w.bytes);
     cudaStream_t s = static_cast<cudaStream_t>(stream);
-    const int G = router_grid(T);
+    const int G = small ? router_small_grid(T) : router_grid(T);
     GateOut o{topk_ids, gates, logits, w.partial_P, w.partial_C};
     if (T > 0) {
         if (small) {
