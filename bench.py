@@ -373,7 +373,7 @@ def main():
     ap.add_argument("--steps", type=int, default=20)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
-    ap.add_argument("--workload", default="page3_cf1.25", choices=moe_inputs.CONFIG_ORDER)
+    ap.add_argument("--workload", default="page3_cf1.25", choices=list(moe_inputs.CONFIGS))
     ap.add_argument("--sample-tokens", type=int, default=32, help="oracle tokens per reference-arm step")
     ap.add_argument("--baseline-tokens", type=int, default=128, help="oracle tokens of the cpu_baseline sample")
     ap.add_argument("--no-cpu-baseline", action="store_true")

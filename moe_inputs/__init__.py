@@ -70,6 +70,10 @@ CONFIGS = {
     # Qwen3-MoE-shaped, uniform routing, Switch aux with alpha = 0.01, 8 virtual EP ranks
     "qwen3_moe": MoEConfig("qwen3_moe", T=16384, h=2048, E=128, k=8, F=768, gating=GATING_SOFTMAX,
                            cf=0.0, R=8, n_shared=0, dtype="bf16", alpha=0.01, bias="none"),
+    # profiling stand-in for the page-3 shape: identical GEMM tiles (K=4096, 128x256 tiles, same routing and
+    # capacity) with F=1536, so that a full ncu capture of the grouped GEMM holds well under 1 GB on the device
+    "page3_profile": MoEConfig("page3_profile", T=4096, h=4096, E=8, k=2, F=1536, gating=GATING_SOFTMAX, cf=1.25,
+                               R=8, n_shared=0, dtype="bf16", alpha=0.01, bias="none"),
 }
 CONFIG_ORDER = ["tiny_fp32", "page3_cf1.25", "mixtral_zipf", "deepseek_v3", "qwen3_moe"]
 
