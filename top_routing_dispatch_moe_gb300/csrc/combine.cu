@@ -28,28 +28,54 @@ combine_kernel(const T* __restrict__ eout, const int32_t* __restrict__ dest_row,
         dj[j] = __shfl_sync(0xffffffffu, myd, j);
         gj[j] = __shfl_sync(0xffffffffu, myg, j);
     }
-    for (int d0 = lane * V; d0 < h; d0 += 32 * V) {
-        float acc[V];
-        if (shared_out) {
-            Vec16<T> s = ld16_stream(shared_out + (size_t)t * h + d0);
+    constexpr int U = 2;                          // 16-byte column chunks per lane per pass
+    for (int d0 = lane * V; d0 < h; d0 += U * 32 * V) {
+        float acc[U][V];
 #pragma unroll
-            for (int i = 0; i < V; ++i) acc[i] = s.get(i);
-        } else {
+        for (int u = 0; u < U; ++u) {
+            const int d = d0 + u * 32 * V;
+            if (shared_out && d < h) {
+                Vec16<T> s = ld16_stream(shared_out + (size_t)t * h + d);
 #pragma unroll
-            for (int i = 0; i < V; ++i) acc[i] = 0.f;
-        }
+                for (int i = 0; i < V; ++i) acc[u][i] = s.get(i);
+            } else {
 #pragma unroll
-        for (int j = 0; j < 16; ++j) {
-            if (j < k && dj[j] >= 0) {
-                Vec16<T> v = ld16_stream(eout + (size_t)dj[j] * h + d0);
-#pragma unroll
-                for (int i = 0; i < V; ++i) acc[i] = fmaf(gj[j], v.get(i), acc[i]);
+                for (int i = 0; i < V; ++i) acc[u][i] = 0.f;
             }
         }
-        Vec16<T> o;
+        // issue every load of this pass before the first use: k rows x U chunks in flight per lane
 #pragma unroll
-        for (int i = 0; i < V; ++i) o.set(i, acc[i]);
-        st16(y + (size_t)t * h + d0, o);
+        for (int j0 = 0; j0 < 16; j0 += 4) {
+            if (j0 >= k) break;
+            Vec16<T> v[4][U];
+#pragma unroll
+            for (int jj = 0; jj < 4; ++jj)
+#pragma unroll
+                for (int u = 0; u < U; ++u) {
+                    const int j = j0 + jj, d = d0 + u * 32 * V;
+                    if (j < k && dj[j] >= 0 && d < h) v[jj][u] = ld16_stream(eout + (size_t)dj[j] * h + d);
+                }
+#pragma unroll
+            for (int jj = 0; jj < 4; ++jj)
+#pragma unroll
+                for (int u = 0; u < U; ++u) {
+                    const int j = j0 + jj, d = d0 + u * 32 * V;
+                    if (j < k && dj[j] >= 0 && d < h) {
+#pragma unroll
+                        for (int i = 0; i < V; ++i) acc[u][i] = fmaf(gj[j], v[jj][u].get(i), acc[u][i]);
+                    }
+                }
+        }
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+            const int d = d0 + u * 32 * V;
+            if (d < h) {
+                Vec16<T> o;
+#pragma unroll
+                for (int i = 0; i < V; ++i) o.set(i, acc[u][i]);
+                st16(y + (size_t)t * h + d, o);
+            }
+        }
     }
 }
 

@@ -169,11 +169,19 @@ dispatch_copy_kernel(const T* __restrict__ x, const int32_t* __restrict__ dest_r
 #pragma unroll
     for (int j = 0; j < 16; ++j) dj[j] = __shfl_sync(0xffffffffu, my, j);   // all lanes, before any exit
     const T* src = x + (size_t)t * h;
-    for (int d0 = lane * V; d0 < h; d0 += 32 * V) {
-        Vec16<T> v = ld16_stream(src + d0);
+    constexpr int U = 4;                          // 16-byte loads in flight per lane
+    for (int d0 = lane * V; d0 < h; d0 += U * 32 * V) {
+        Vec16<T> v[U];
+#pragma unroll
+        for (int u = 0; u < U; ++u)
+            if (d0 + u * 32 * V < h) v[u] = ld16_stream(src + d0 + u * 32 * V);
 #pragma unroll
         for (int j = 0; j < 16; ++j)
-            if (j < k && dj[j] >= 0) st16(buf + (size_t)dj[j] * h + d0, v);
+            if (j < k && dj[j] >= 0) {
+#pragma unroll
+                for (int u = 0; u < U; ++u)
+                    if (d0 + u * 32 * V < h) st16(buf + (size_t)dj[j] * h + d0 + u * 32 * V, v[u]);
+            }
     }
 }
 
@@ -295,3 +303,4 @@ extern "C" int moe_dense_tile_sched(int rows, int32_t* tile_sched, void* stream)
         rows, tile_sched);
     return check_launch("dense_sched_kernel");
 }
+

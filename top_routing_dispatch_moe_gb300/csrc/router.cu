@@ -141,12 +141,32 @@ router_small_kernel(const T* __restrict__ x, const T* __restrict__ w_r, const fl
     float* s_P = reinterpret_cast<float*>(smem_raw + (((size_t)E * h * sizeof(T) + 15) & ~(size_t)15));
     int* s_hist = reinterpret_cast<int*>(s_P + kRouterWarps * E);
 
-    for (int d = threadIdx.x; d < h; d += blockDim.x)      // one router-weight row per thread: conflict-free
-        for (int e = 0; e < E; ++e) wT[(size_t)e * h + d] = w_r[(size_t)d * E + e];
+    constexpr int V = Vec16<T>::N;
+    {   // stage W_r^T: 16-byte loads of the row-major [h][E] weight, transposed into shared memory
+        const int nvec = h * E / V;
+        for (int v0 = threadIdx.x; v0 < nvec; v0 += 4 * blockDim.x) {
+            Vec16<T> wv[4];
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                const int v = v0 + u * blockDim.x;
+                if (v < nvec) wv[u] = ld16(w_r + (size_t)v * V);
+            }
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                const int v = v0 + u * blockDim.x;
+                if (v < nvec) {
+#pragma unroll
+                    for (int q = 0; q < V; ++q) {
+                        const int i = v * V + q, d = i / E, e = i - d * E;
+                        wT[(size_t)e * h + d] = from_f32<T>(wv[u].get(q));
+                    }
+                }
+            }
+        }
+    }
     for (int e = threadIdx.x; e < E; e += blockDim.x) s_hist[e] = 0;
     __syncthreads();
 
-    constexpr int V = Vec16<T>::N;
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     float Pacc[1] = {0.f};
     const bool use_bias_in_logits = bias && gating != MOE_GATING_SIGMOID_BIAS_RENORM;
@@ -155,16 +175,26 @@ router_small_kernel(const T* __restrict__ x, const T* __restrict__ w_r, const fl
 #pragma unroll
         for (int e = 0; e < EMAX; ++e) acc[e] = 0.f;
         const T* xr = x + (size_t)t * h;
-        for (int d0 = lane * V; d0 < h; d0 += 32 * V) {
-            Vec16<T> xv = ld16_stream(xr + d0);
+        constexpr int U = 4;                      // 16-byte loads in flight per lane
+        for (int d0 = lane * V; d0 < h; d0 += U * 32 * V) {
+            Vec16<T> xv[U];
 #pragma unroll
-            for (int e = 0; e < EMAX; ++e) {
-                if (e < E) {
-                    Vec16<T> wv = *reinterpret_cast<const Vec16<T>*>(wT + (size_t)e * h + d0);
-                    float s = acc[e];
+            for (int u = 0; u < U; ++u)
+                if (d0 + u * 32 * V < h) xv[u] = ld16_stream(xr + d0 + u * 32 * V);
 #pragma unroll
-                    for (int i = 0; i < V; ++i) s = fmaf(xv.get(i), wv.get(i), s);
-                    acc[e] = s;
+            for (int u = 0; u < U; ++u) {
+                const int d = d0 + u * 32 * V;
+                if (d < h) {
+#pragma unroll
+                    for (int e = 0; e < EMAX; ++e) {
+                        if (e < E) {
+                            Vec16<T> wv = *reinterpret_cast<const Vec16<T>*>(wT + (size_t)e * h + d);
+                            float s = acc[e];
+#pragma unroll
+                            for (int i = 0; i < V; ++i) s = fmaf(xv[u].get(i), wv.get(i), s);
+                            acc[e] = s;
+                        }
+                    }
                 }
             }
         }
@@ -259,27 +289,49 @@ router_gate_kernel(const float* __restrict__ logits, const float* __restrict__ b
     flush_partials<NPL>(Pacc, E, s_P, s_hist, o);
 }
 
-// One block: counts, f, P and aux from the per-block partials, in a fixed order.
+// One block: counts, f, P and aux from the per-block partials. Thread (s, e) of an [S][E] arrangement sums
+// the partials of blocks s, s + S, s + 2S, ... of expert e; the S partial sums of each expert are then added
+// in a fixed tree order, so the result does not depend on timing.
 __global__ void __launch_bounds__(1024)
 router_finalize(const float* __restrict__ partial_P, const int32_t* __restrict__ partial_C, int grid, int T_, int E,
                 int k, float alpha, int32_t* counts, float* f, float* P, float* aux) {
+    __shared__ float s_p[1024];
+    __shared__ int s_c[1024];
     __shared__ float s_red[1024];
+    const int S = max(1, (int)blockDim.x / E);          // slices per expert (power of two not required)
     float term = 0.f;
-    for (int e = threadIdx.x; e < E; e += blockDim.x) {
+    for (int e0 = 0; e0 < E; e0 += blockDim.x) {        // E <= 1024: one pass when E * S <= blockDim
+        const int tid = threadIdx.x;
+        const int e = e0 + tid % min(E - e0, (int)blockDim.x);
+        const int s = tid / min(E - e0, (int)blockDim.x);
+        const int Se = (int)blockDim.x / min(E - e0, (int)blockDim.x);
         float ps = 0.f;
         int c = 0;
-        for (int b = 0; b < grid; ++b) { ps += partial_P[(size_t)b * E + e]; c += partial_C[(size_t)b * E + e]; }
-        const float Pe = T_ > 0 ? ps / (float)T_ : 0.f;
-        const float fe = T_ > 0 ? (float)c / ((float)k * (float)T_) : 0.f;
-        counts[e] = c;
-        f[e] = fe;
-        P[e] = Pe;
-        term += fe * Pe;
+        if (s < Se && e < E)
+            for (int b = s; b < grid; b += Se) { ps += partial_P[(size_t)b * E + e]; c += partial_C[(size_t)b * E + e]; }
+        s_p[tid] = ps;
+        s_c[tid] = c;
+        __syncthreads();
+        const int ew = min(E - e0, (int)blockDim.x);
+        if (tid < ew) {
+            float tp = 0.f;
+            int tc = 0;
+            for (int q = 0; q < Se; ++q) { tp += s_p[q * ew + tid]; tc += s_c[q * ew + tid]; }
+            const int ee = e0 + tid;
+            const float Pe = T_ > 0 ? tp / (float)T_ : 0.f;
+            const float fe = T_ > 0 ? (float)tc / ((float)k * (float)T_) : 0.f;
+            counts[ee] = tc;
+            f[ee] = fe;
+            P[ee] = Pe;
+            term += fe * Pe;
+        }
+        __syncthreads();
     }
+    (void)S;
     s_red[threadIdx.x] = term;
     __syncthreads();
-    for (int s = blockDim.x / 2; s > 0; s >>= 1) {
-        if ((int)threadIdx.x < s) s_red[threadIdx.x] += s_red[threadIdx.x + s];
+    for (int st = blockDim.x / 2; st > 0; st >>= 1) {
+        if ((int)threadIdx.x < st) s_red[threadIdx.x] += s_red[threadIdx.x + st];
         __syncthreads();
     }
     if (threadIdx.x == 0) aux[0] = alpha * (float)E * s_red[0];
