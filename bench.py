@@ -65,15 +65,16 @@ class ClockSampler:
               "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
               "clocks_event_reasons.sw_power_cap")
 
-    def __init__(self, device_index: int):
+    def __init__(self, device_index):
         self.idx = device_index
         self.proc = None
-        self.lines: list[str] = []
+        self.lines: list[tuple[float, str]] = []
+        self.window = (0.0, float("inf"))
 
-    def __enter__(self):
+    def start(self):
         try:
             self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.idx), f"--query-gpu={self.FIELDS}",
-                                          "--format=csv,noheader,nounits", "-lms", "100"],
+                                          "--format=csv,noheader,nounits", "-lms", "20"],
                                          stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
             self.t = threading.Thread(target=self._read, daemon=True)
             self.t.start()
@@ -83,7 +84,14 @@ class ClockSampler:
 
     def _read(self):
         for line in self.proc.stdout:
-            self.lines.append(line.strip())
+            self.lines.append((time.time(), line.strip()))
+
+    def mark(self, t0, t1):
+        """Keep only the samples that arrived inside the timed region [t0, t1]."""
+        self.window = (t0, t1)
+
+    def stop(self):
+        self.__exit__()
 
     def __exit__(self, *a):
         if self.proc is not None:
@@ -96,7 +104,9 @@ class ClockSampler:
     def summary(self):
         sm, mx, reasons = [], [], set()
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        for line in self.lines:
+        for ts, line in self.lines:
+            if not (self.window[0] <= ts <= self.window[1] + 0.03):
+                continue
             parts = [p.strip() for p in line.split(",")]
             if len(parts) < 8:
                 continue
@@ -237,10 +247,16 @@ def run_gpu(args, cfg, C):
     flush = torch.empty(512 * 2**20, dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream()
 
+    clk = ClockSampler(_smi_id(local)).start()
     for _ in range(args.warmup):
         layer.forward(x)
         flush.zero_()
     torch.cuda.synchronize()
+    t_start = time.time()
+    while time.time() - t_start < 0.3:                  # let the sampler start; keep the GPU busy meanwhile
+        layer.forward(x)
+        flush.zero_()
+        torch.cuda.synchronize()
     assert moe.moe_check_device_error() == moe.MOE_OK, moe.moe_last_error_string()
     kept = int(layer.d_out["kept_counts"].sum().item())
 
@@ -250,13 +266,16 @@ def run_gpu(args, cfg, C):
         dist.barrier()
     torch.cuda.synchronize()
     launches0 = moe.moe_launch_count()
-    with ClockSampler(_smi_id(local)) as clk:
-        t_wall0 = time.perf_counter()
-        for _ in range(args.steps):
-            layer.forward(x, events=events)
-            flush.zero_()
-        torch.cuda.synchronize()
-        t_wall = time.perf_counter() - t_wall0
+    t_clk0 = time.time()
+    t_wall0 = time.perf_counter()
+    for _ in range(args.steps):
+        layer.forward(x, events=events)
+        flush.zero_()
+    torch.cuda.synchronize()
+    t_wall = time.perf_counter() - t_wall0
+    clk.mark(t_clk0, time.time())
+    time.sleep(0.05)
+    clk.stop()
     if world > 1:
         dist.barrier()
     launches = moe.moe_launch_count() - launches0
@@ -370,7 +389,7 @@ def kernel_hash():
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--steps", type=int, default=100)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
     ap.add_argument("--workload", default="page3_cf1.25", choices=list(moe_inputs.CONFIGS))
