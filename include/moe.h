@@ -117,6 +117,21 @@ int moe_dispatch(const void* x, const int32_t* topk_ids, int T, int h, int E, in
                  int32_t* rank_counts, int32_t* rank_offsets, int32_t* tile_sched, void* ws,
                  size_t ws_bytes, void* stream);
 
+/* moe_dispatch_static: moe_dispatch for callers that cannot allocate device memory, such as a plugin whose
+ * host framework owns all device memory, a latency-critical thread that may not allocate, or a program that
+ * reserves all its memory at start-up. The paper has no counterpart: this is a library-usage variant.
+ * Arguments and outputs are those of moe_dispatch minus the workspace: the scratch lives in a fixed 1 MiB
+ * (1048576-byte) array of the library's own device memory, held by every GPU that loads the library until
+ * the process exits. A size whose scratch (moe_dispatch_workspace_size) exceeds 1 MiB is rejected with
+ * MOE_ERR_INVALID_ARG before anything is enqueued. The first call on a device (with that device current)
+ * looks up the array's device address; make that call before any stream capture on the device. All calls
+ * share the array and each overwrites it: calls that may overlap on the GPU race and must be serialised by
+ * the caller. No call allocates memory. */
+int moe_dispatch_static(const void* x, const int32_t* topk_ids, int T, int h, int E, int k, int capacity,
+                        int num_ranks, int dtype, void* buf, int32_t* offsets, int32_t* kept_counts,
+                        int32_t* dest_row, uint8_t* drop_mask, int32_t* src_token, int32_t* src_slot,
+                        int32_t* rank_counts, int32_t* rank_offsets, int32_t* tile_sched, void* stream);
+
 /* Writes a tile schedule for one dense group of `rows` rows (offsets {0, rows}): the shared expert of a
  * DeepSeek-V3-shaped layer runs through the expert FFN with E = 1 and this schedule. */
 int moe_dense_tile_sched(int rows, int32_t* tile_sched, void* stream);

@@ -14,6 +14,7 @@
 // its (at most k) destination rows with 16-byte loads and stores, reading x once. In capacity mode a
 // fifth kernel zero-fills the pad rows and marks them -1.
 #include <algorithm>
+#include <mutex>
 #include "common.cuh"
 
 namespace moe {
@@ -304,3 +305,59 @@ extern "C" int moe_dense_tile_sched(int rows, int32_t* tile_sched, void* stream)
     return check_launch("dense_sched_kernel");
 }
 
+
+// ---------------------------------------------------------------------------------------------------
+// moe_dispatch_static: the same dispatch for callers that cannot allocate device memory.
+//
+// Some callers cannot call cudaMalloc, or any allocator, at the point where they dispatch tokens: code that
+// runs inside a host framework which owns all device memory and hands plugins only the tensors of a call,
+// real-time or latency-critical threads where an allocation (and the device synchronisation it may imply)
+// is not allowed, and programs that must reserve every byte of device memory once at start-up. For them
+// this entry point keeps its scratch (the per-chunk expert counts) in a fixed array in the library's own
+// device memory instead of a caller-provided workspace; the caller still passes every input and output.
+//
+// The array is a file-scope __device__ variable: every GPU that loads the library holds it until the process
+// exits. Its host-side name is only a stand-in for the symbol, never a device address, so the first call on
+// each device, with that device current, looks its address up with cudaGetSymbolAddress and caches it; make
+// that first call on a device before capturing a stream on it. All calls share the one array: calls whose
+// kernels may overlap on the GPU (different streams, no ordering between them) race on it and must be
+// serialised by the caller. Nothing in the array has to start at zero: every call writes each word before it
+// reads it, so the contents left by the previous call do not matter.
+// ---------------------------------------------------------------------------------------------------
+namespace moe {
+constexpr size_t kStaticScratchBytes = (size_t)1 << 20;     // 1 MiB: ceil(T / (1024/k)) chunks x E x 4 B
+static __device__ __align__(256) int32_t g_dispatch_scratch[kStaticScratchBytes / sizeof(int32_t)];
+static std::mutex g_static_mu;
+static void* g_static_ptr[64];
+}  // namespace moe
+
+extern "C" int moe_dispatch_static(const void* x, const int32_t* topk_ids, int T, int h, int E, int k, int capacity,
+                                   int num_ranks, int dtype, void* buf, int32_t* offsets, int32_t* kept_counts,
+                                   int32_t* dest_row, uint8_t* drop_mask, int32_t* src_token, int32_t* src_slot,
+                                   int32_t* rank_counts, int32_t* rank_offsets, int32_t* tile_sched, void* stream) {
+    MOE_REQUIRE(T >= 0 && E >= 1 && E <= 1024 && k >= 1 && k <= 16, MOE_ERR_INVALID_ARG,
+                "moe_dispatch_static: T=%d E=%d k=%d", T, E, k);
+    const size_t need = moe_dispatch_workspace_size(T, E, k, capacity);
+    MOE_REQUIRE(need <= moe::kStaticScratchBytes, MOE_ERR_INVALID_ARG,
+                "moe_dispatch_static: T=%d, E=%d, k=%d needs %zu scratch bytes, more than the static %zu; "
+                "use moe_dispatch with a workspace instead", T, E, k, need, moe::kStaticScratchBytes);
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    MOE_REQUIRE(e == cudaSuccess && dev >= 0 && dev < 64, MOE_ERR_CUDA, "moe_dispatch_static: no current device (%s)",
+                cudaGetErrorString(e));
+    void* scratch = nullptr;
+    {
+        std::lock_guard<std::mutex> lk(moe::g_static_mu);
+        if (!moe::g_static_ptr[dev]) {
+            void* p = nullptr;
+            e = cudaGetSymbolAddress(&p, moe::g_dispatch_scratch);
+            MOE_REQUIRE(e == cudaSuccess && p, MOE_ERR_CUDA, "moe_dispatch_static: cudaGetSymbolAddress failed: %s",
+                        cudaGetErrorString(e));
+            moe::g_static_ptr[dev] = p;
+        }
+        scratch = moe::g_static_ptr[dev];
+    }
+    return moe_dispatch(x, topk_ids, T, h, E, k, capacity, num_ranks, dtype, buf, offsets, kept_counts, dest_row,
+                        drop_mask, src_token, src_slot, rank_counts, rank_offsets, tile_sched, scratch,
+                        moe::kStaticScratchBytes, stream);
+}

@@ -29,6 +29,7 @@ _SIGS = {
     "moe_tile_sched_bytes": (_Z, [_I, _I, _I, _I]),
     "moe_dispatch_workspace_size": (_Z, [_I, _I, _I, _I]),
     "moe_dispatch": (_I, [_P, _P, _I, _I, _I, _I, _I, _I, _I, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _Z, _P]),
+    "moe_dispatch_static": (_I, [_P, _P, _I, _I, _I, _I, _I, _I, _I, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P]),
     "moe_dense_tile_sched": (_I, [_I, _P, _P]),
     "moe_packed_weights_bytes": (_Z, [_I, _I, _I, _I]),
     "moe_pack_expert_weights": (_I, [_P, _P, _P, _I, _I, _I, _I, _P, _P]),
@@ -154,6 +155,34 @@ def moe_dispatch(x, topk_ids, E: int, capacity: int = 0, num_ranks: int = 1, *, 
                              _ptr(o["offsets"]), _ptr(o["kept_counts"]), _ptr(o["dest_row"]), _ptr(o["drop_mask"]),
                              _ptr(o["src_token"]), _ptr(o["src_slot"]), _ptr(o["rank_counts"]),
                              _ptr(o["rank_offsets"]), _ptr(o["tile_sched"]), _ptr(ws), ws.numel(), _stream(stream)))
+    o["rows"] = rows
+    return o
+
+
+def moe_dispatch_static(x, topk_ids, E: int, capacity: int = 0, num_ranks: int = 1, *, out=None, stream=None):
+    """moe_dispatch without a workspace: the library's fixed device scratch is used (for callers that cannot
+    allocate device memory). Outputs as moe_dispatch; `out` may hold preallocated output tensors."""
+    T, h = x.shape
+    k = topk_ids.shape[1]
+    dev = x.device
+    rows = moe_dispatch_rows(T, E, k, capacity)
+    o = dict(out or {})
+    o.setdefault("buf", torch.empty((rows, h), dtype=x.dtype, device=dev))
+    o.setdefault("offsets", torch.empty(E + 1, dtype=torch.int32, device=dev))
+    o.setdefault("kept_counts", torch.empty(E, dtype=torch.int32, device=dev))
+    o.setdefault("dest_row", torch.empty((T, k), dtype=torch.int32, device=dev))
+    o.setdefault("drop_mask", torch.empty((T, k), dtype=torch.uint8, device=dev))
+    o.setdefault("src_token", torch.empty(rows, dtype=torch.int32, device=dev))
+    o.setdefault("src_slot", torch.empty(rows, dtype=torch.int32, device=dev))
+    o.setdefault("rank_counts", torch.empty(num_ranks, dtype=torch.int32, device=dev))
+    o.setdefault("rank_offsets", torch.empty(num_ranks + 1, dtype=torch.int32, device=dev))
+    o.setdefault("tile_sched", torch.empty(moe_tile_sched_bytes(T, E, k, capacity) // 4, dtype=torch.int32,
+                                           device=dev))
+    _check(_lib.moe_dispatch_static(_ptr(x), _ptr(topk_ids), T, h, E, k, capacity, num_ranks, dtype_code(x.dtype),
+                                    _ptr(o["buf"]), _ptr(o["offsets"]), _ptr(o["kept_counts"]), _ptr(o["dest_row"]),
+                                    _ptr(o["drop_mask"]), _ptr(o["src_token"]), _ptr(o["src_slot"]),
+                                    _ptr(o["rank_counts"]), _ptr(o["rank_offsets"]), _ptr(o["tile_sched"]),
+                                    _stream(stream)))
     o["rows"] = rows
     return o
 
