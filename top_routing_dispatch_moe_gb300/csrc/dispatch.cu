@@ -296,13 +296,18 @@ extern "C" int moe_dispatch(const void* x, const int32_t* topk_ids, int T, int h
     return MOE_OK;
 }
 
+namespace moe {
+int launch_dense_sched(int rows, int32_t* sched, cudaStream_t s) {
+    const int ntiles = cdiv(rows, MOE_TILE_M);
+    dense_sched_kernel<<<std::max(1, std::min(cdiv(ntiles, 256), 64)), 256, 0, s>>>(rows, sched);
+    return check_launch("dense_sched_kernel");
+}
+}  // namespace moe
+
 extern "C" int moe_dense_tile_sched(int rows, int32_t* tile_sched, void* stream) {
     MOE_REQUIRE(rows >= 0 && tile_sched && aligned16(tile_sched), MOE_ERR_INVALID_ARG,
                 "moe_dense_tile_sched: rows=%d, tile_sched must be non-null and 16-byte aligned", rows);
-    const int ntiles = cdiv(rows, MOE_TILE_M);
-    dense_sched_kernel<<<std::max(1, std::min(cdiv(ntiles, 256), 64)), 256, 0, static_cast<cudaStream_t>(stream)>>>(
-        rows, tile_sched);
-    return check_launch("dense_sched_kernel");
+    return launch_dense_sched(rows, tile_sched, static_cast<cudaStream_t>(stream));
 }
 
 

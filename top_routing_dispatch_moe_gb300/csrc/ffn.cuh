@@ -32,4 +32,10 @@ int ffn_tc_up_gate(const void* buf, const int32_t* sched, const void* packed, in
 int ffn_tc_down(const void* act, const int32_t* sched, const void* packed, int E, int h, int F, int rows, void* eout,
                 cudaStream_t s);
 
+// Router logits on the tensor cores (bf16 x and transposed router weight, fp32 logits + bias).
+int tc_router_logits(const void* x, const void* w_rT, const float* bias, int T, int h, int E, const int32_t* sched,
+                     float* logits, cudaStream_t s);
+// Dense tile schedule of `rows` rows (one group), launched on `s`.
+int launch_dense_sched(int rows, int32_t* sched, cudaStream_t s);
+
 }  // namespace moe

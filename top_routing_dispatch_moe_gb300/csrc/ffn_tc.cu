@@ -165,14 +165,20 @@ __device__ __forceinline__ uint64_t sw128_desc(uint32_t saddr) {
 // K-major (bits 15, 16 = 0), N >> 3 at bits 17-22, M >> 4 at bits 24-28.
 constexpr uint32_t kIdesc = (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(BN >> 3) << 17) | ((uint32_t)(BM >> 4) << 24);
 
+// Epilogues: SwiGLU of the packed gate/up tile -> bf16 act; plain bf16 conversion; fp32 (+ per-column bias),
+// used for the router logits.
+enum Epi : int { EPI_SWIGLU = 0, EPI_BF16 = 1, EPI_F32 = 2 };
+
 struct Params {
     const int32_t* sched;
     int K;              // reduction length
     int NT;             // n-tiles per expert
-    int b_rows;         // B rows per expert in the B tensor map (2 Fp for up/gate, h for down)
-    int n_valid;        // valid output columns (F for up/gate, h for down)
+    int b_rows;         // B rows per expert in the B tensor map (2 Fp for up/gate, h for down, E for the router)
+    int n_valid;        // valid output columns (F for up/gate, h for down, E for the router)
     int ldo;            // output leading dimension
     __nv_bfloat16* out;
+    float* out_f32;     // EPI_F32 output
+    const float* bias;  // EPI_F32: per-column bias or null
     unsigned* err;
     long long wait_limit;
 };
@@ -195,7 +201,7 @@ __device__ __forceinline__ Work map_work(const int32_t* sched, int E, int NT, in
     return Work{ent.x, ent.y, ent.z, n};
 }
 
-template <bool SWIGLU>
+template <int EPI>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
 grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB, Params p) {
     extern __shared__ uint8_t smem_raw[];
@@ -299,7 +305,7 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
             const int row = wk.row0 + lane_base + lane;
             const bool live = row < wk.row1;
             const uint32_t tbase = tmem + (uint32_t)(a * BN) + ((uint32_t)lane_base << 16);
-            if constexpr (SWIGLU) {
+            if constexpr (EPI == EPI_SWIGLU) {
 #pragma unroll 1
                 for (int j = 0; j < 4; ++j) {
                     float g[32], u[32];
@@ -318,6 +324,27 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
                                     o.set(i, gv / (1.f + expf(-gv)) * u[c + i]);
                                 }
                                 st16(dst + c, o);
+                            }
+                        }
+                    }
+                }
+            } else if constexpr (EPI == EPI_F32) {
+#pragma unroll 1
+                for (int j = 0; j < 8; ++j) {
+                    float v[32];
+                    tmem_ld32(tbase + 32 * j, v);
+                    const int n0 = wk.n * BN + 32 * j;
+                    if (live) {
+                        float* dst = p.out_f32 + (size_t)row * p.ldo + n0;
+#pragma unroll
+                        for (int c = 0; c < 32; c += 4) {
+                            if (n0 + c < p.n_valid) {
+                                float4 o;
+                                o.x = v[c] + (p.bias ? __ldg(p.bias + n0 + c) : 0.f);
+                                o.y = v[c + 1] + (p.bias ? __ldg(p.bias + n0 + c + 1) : 0.f);
+                                o.z = v[c + 2] + (p.bias ? __ldg(p.bias + n0 + c + 2) : 0.f);
+                                o.w = v[c + 3] + (p.bias ? __ldg(p.bias + n0 + c + 3) : 0.f);
+                                *reinterpret_cast<float4*>(dst + c) = o;
                             }
                         }
                     }
@@ -387,17 +414,25 @@ static int make_map(CUtensorMap* m, const void* base, long long rows, long long 
     return MOE_OK;
 }
 
-template <bool SWIGLU>
-static int launch(const CUtensorMap& a, const CUtensorMap& b, const Params& p, cudaStream_t s) {
-    static bool attr_set[2] = {false, false};
-    if (!attr_set[SWIGLU]) {
-        cudaError_t e = cudaFuncSetAttribute(grouped_gemm_kernel<SWIGLU>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+template <int EPI>
+static int gemm(const void* a, long long a_rows, const void* b, long long b_rows_total, const Params& p,
+                cudaStream_t s) {
+    static bool attr_set[64][3];             // the attribute belongs to the kernel in each device's context
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64)
+        return set_error(MOE_ERR_CUDA, "grouped_gemm: no usable current device");
+    if (!attr_set[dev][EPI]) {
+        cudaError_t e = cudaFuncSetAttribute(grouped_gemm_kernel<EPI>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                              SMEM_BYTES);
         if (e != cudaSuccess) return set_error(MOE_ERR_CUDA, "grouped_gemm smem attribute: %s", cudaGetErrorString(e));
-        attr_set[SWIGLU] = true;
+        attr_set[dev][EPI] = true;
     }
-    grouped_gemm_kernel<SWIGLU><<<num_sms(), NUM_THREADS, SMEM_BYTES, s>>>(a, b, p);
-    return check_launch(SWIGLU ? "grouped_gemm_kernel<up_gate>" : "grouped_gemm_kernel<down>");
+    CUtensorMap ma, mb;
+    if (int rc = make_map(&ma, a, a_rows, p.K, BM)) return rc;
+    if (int rc = make_map(&mb, b, b_rows_total, p.K, BN)) return rc;
+    grouped_gemm_kernel<EPI><<<num_sms(), NUM_THREADS, SMEM_BYTES, s>>>(ma, mb, p);
+    return check_launch(EPI == EPI_SWIGLU ? "grouped_gemm_kernel<up_gate>"
+                        : EPI == EPI_BF16 ? "grouped_gemm_kernel<down>" : "grouped_gemm_kernel<router>");
 }
 
 }  // namespace tc
@@ -405,27 +440,32 @@ static int launch(const CUtensorMap& a, const CUtensorMap& b, const Params& p, c
 int ffn_tc_up_gate(const void* buf, const int32_t* sched, const void* packed, int E, int h, int F, int rows, void* act,
                    cudaStream_t s) {
     const PackedLayout L = packed_layout(E, h, F, 2);
-    CUtensorMap ma, mb;
-    if (int rc = tc::make_map(&ma, buf, rows, h, tc::BM)) return rc;
-    if (int rc = tc::make_map(&mb, static_cast<const char*>(packed) + L.up_gate_off, (long long)E * 2 * L.Fp, h, tc::BN))
-        return rc;
     unsigned* err = device_error_word();
     MOE_REQUIRE(err, MOE_ERR_CUDA, "device error word unavailable");
-    tc::Params p{sched, h, L.Fp / 128, 2 * L.Fp, F, F, static_cast<__nv_bfloat16*>(act), err, wait_limit()};
-    return tc::launch<true>(ma, mb, p, s);
+    tc::Params p{sched, h, L.Fp / 128, 2 * L.Fp, F, F, static_cast<__nv_bfloat16*>(act), nullptr, nullptr, err,
+                 wait_limit()};
+    return tc::gemm<tc::EPI_SWIGLU>(buf, rows, static_cast<const char*>(packed) + L.up_gate_off,
+                                    (long long)E * 2 * L.Fp, p, s);
 }
 
 int ffn_tc_down(const void* act, const int32_t* sched, const void* packed, int E, int h, int F, int rows, void* eout,
                 cudaStream_t s) {
     const PackedLayout L = packed_layout(E, h, F, 2);
-    CUtensorMap ma, mb;
-    if (int rc = tc::make_map(&ma, act, rows, F, tc::BM)) return rc;
-    if (int rc = tc::make_map(&mb, static_cast<const char*>(packed) + L.down_off, (long long)E * h, F, tc::BN))
-        return rc;
     unsigned* err = device_error_word();
     MOE_REQUIRE(err, MOE_ERR_CUDA, "device error word unavailable");
-    tc::Params p{sched, F, cdiv(h, tc::BN), h, h, h, static_cast<__nv_bfloat16*>(eout), err, wait_limit()};
-    return tc::launch<false>(ma, mb, p, s);
+    tc::Params p{sched, F, cdiv(h, tc::BN), h, h, h, static_cast<__nv_bfloat16*>(eout), nullptr, nullptr, err,
+                 wait_limit()};
+    return tc::gemm<tc::EPI_BF16>(act, rows, static_cast<const char*>(packed) + L.down_off, (long long)E * h, p, s);
+}
+
+// Router logits [T, E] fp32 = x [T, h] @ w_rT^T (+ bias), w_rT the K-major [E, h] copy of the router weight,
+// `sched` a dense schedule of T rows.
+int tc_router_logits(const void* x, const void* w_rT, const float* bias, int T, int h, int E, const int32_t* sched,
+                     float* logits, cudaStream_t s) {
+    unsigned* err = device_error_word();
+    MOE_REQUIRE(err, MOE_ERR_CUDA, "device error word unavailable");
+    tc::Params p{sched, h, cdiv(E, tc::BN), E, E, E, nullptr, logits, bias, err, wait_limit()};
+    return tc::gemm<tc::EPI_F32>(x, T, w_rT, E, p, s);
 }
 
 }  // namespace moe

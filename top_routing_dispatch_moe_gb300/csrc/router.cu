@@ -15,6 +15,7 @@
 #include <math.h>
 #include <algorithm>
 #include "common.cuh"
+#include "ffn.cuh"
 
 namespace moe {
 
@@ -129,6 +130,19 @@ __device__ __forceinline__ void flush_partials(float (&Pacc)[NPL], int E, float*
     }
 }
 
+// 16 bytes of elements -> fp32 (bf16: the value's bits are the high half of an fp32 word).
+__device__ __forceinline__ void unpack16(const Vec16<float>& v, float (&f)[4]) {
+    f[0] = v.v.x; f[1] = v.v.y; f[2] = v.v.z; f[3] = v.v.w;
+}
+__device__ __forceinline__ void unpack16(const Vec16<__nv_bfloat16>& v, float (&f)[8]) {
+    const uint32_t w[4] = {v.v.x, v.v.y, v.v.z, v.v.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        f[2 * i] = __uint_as_float(w[i] << 16);
+        f[2 * i + 1] = __uint_as_float(w[i] & 0xffff0000u);
+    }
+}
+
 // ---------------------------------------------------------------------------------------------------
 // E <= 32: fused logits + gating, W_r^T in shared memory
 // ---------------------------------------------------------------------------------------------------
@@ -175,7 +189,7 @@ router_small_kernel(const T* __restrict__ x, const T* __restrict__ w_r, const fl
 #pragma unroll
         for (int e = 0; e < EMAX; ++e) acc[e] = 0.f;
         const T* xr = x + (size_t)t * h;
-        constexpr int U = 4;                      // 16-byte loads in flight per lane
+        constexpr int U = 8;                      // 16-byte loads in flight per lane
         for (int d0 = lane * V; d0 < h; d0 += U * 32 * V) {
             Vec16<T> xv[U];
 #pragma unroll
@@ -185,13 +199,16 @@ router_small_kernel(const T* __restrict__ x, const T* __restrict__ w_r, const fl
             for (int u = 0; u < U; ++u) {
                 const int d = d0 + u * 32 * V;
                 if (d < h) {
+                    float xf[V];
+                    unpack16(xv[u], xf);              // once per element, not once per expert
 #pragma unroll
                     for (int e = 0; e < EMAX; ++e) {
                         if (e < E) {
-                            Vec16<T> wv = *reinterpret_cast<const Vec16<T>*>(wT + (size_t)e * h + d);
+                            float wf[V];
+                            unpack16(*reinterpret_cast<const Vec16<T>*>(wT + (size_t)e * h + d), wf);
                             float s = acc[e];
 #pragma unroll
-                            for (int i = 0; i < V; ++i) s = fmaf(xv[u].get(i), wv.get(i), s);
+                            for (int i = 0; i < V; ++i) s = fmaf(xf[i], wf[i], s);
                             acc[e] = s;
                         }
                     }
@@ -337,22 +354,42 @@ router_finalize(const float* __restrict__ partial_P, const int32_t* __restrict__
     if (threadIdx.x == 0) aux[0] = alpha * (float)E * s_red[0];
 }
 
+// W_r [h, E] -> W_rT [E, h] (K-major operand of the tensor-core logits GEMM), 32 x 32 shared-memory tiles.
+__global__ void __launch_bounds__(256)
+router_transpose_kernel(const __nv_bfloat16* __restrict__ w, int h, int E, __nv_bfloat16* __restrict__ wT) {
+    __shared__ __nv_bfloat16 tile[32][33];
+    const int e0 = blockIdx.x * 32, d0 = blockIdx.y * 32;
+    for (int r = threadIdx.y; r < 32; r += 8) {
+        const int d = d0 + r, e = e0 + threadIdx.x;
+        if (d < h && e < E) tile[r][threadIdx.x] = w[(size_t)d * E + e];
+    }
+    __syncthreads();
+    for (int r = threadIdx.y; r < 32; r += 8) {
+        const int e = e0 + r, d = d0 + threadIdx.x;
+        if (e < E && d < h) wT[(size_t)e * h + d] = tile[threadIdx.x][r];
+    }
+}
+
 // ---------------------------------------------------------------------------------------------------
 // host
 // ---------------------------------------------------------------------------------------------------
 // Upper bound of the blocks of any router launch (sizes the partial-sum workspace).
 static int router_grid(int T) { return std::max(1, std::min(cdiv(T, kRouterWarps), kRouterMaxBlocks)); }
-// The fused small-E kernel stages the router weight in every block: two blocks per SM amortise it.
-static int router_small_grid(int T) { return std::max(1, std::min(router_grid(T), 2 * num_sms())); }
+// The fused small-E kernel stages the router weight in every block: three blocks per SM amortise it.
+static int router_small_grid(int T) { return std::max(1, std::min(router_grid(T), 3 * num_sms())); }
 
 static size_t small_smem_bytes(int h, int E, int el) {
     return align_up((size_t)E * h * el, 16) + (size_t)kRouterWarps * E * sizeof(float) + (size_t)E * sizeof(int);
 }
 static bool use_small_path(int h, int E, int el) { return E <= 32 && small_smem_bytes(h, E, el) <= 200 * 1024; }
 
-struct RouterWs { float* partial_P; int32_t* partial_C; float* logits; size_t bytes; };
+// The logits GEMM runs on the tcgen05 tensor cores for bf16 with E > 32 (E % 4 == 0 keeps the fp32 row
+// stores 16-byte aligned); otherwise on the CUDA cores.
+static bool use_tc_logits(int E, int dtype, bool small) { return !small && dtype == MOE_BF16 && E % 4 == 0; }
 
-static RouterWs router_ws_layout(void* ws, int T, int h, int E, int el, bool need_logits) {
+struct RouterWs { float* partial_P; int32_t* partial_C; float* logits; void* w_rT; int32_t* sched; size_t bytes; };
+
+static RouterWs router_ws_layout(void* ws, int T, int h, int E, int el, bool need_logits, bool tc) {
     RouterWs w{};
     const int G = router_grid(T);
     size_t off = 0;
@@ -361,6 +398,12 @@ static RouterWs router_ws_layout(void* ws, int T, int h, int E, int el, bool nee
     w.partial_C = reinterpret_cast<int32_t*>(base + off); off = align_up(off + (size_t)G * E * 4, 256);
     w.logits = nullptr;
     if (need_logits) { w.logits = reinterpret_cast<float*>(base + off); off = align_up(off + (size_t)T * E * 4, 256); }
+    w.w_rT = nullptr;
+    w.sched = nullptr;
+    if (tc) {
+        w.w_rT = base + off; off = align_up(off + (size_t)E * h * el, 256);
+        w.sched = reinterpret_cast<int32_t*>(base + off); off = align_up(off + sched_words(T, 1) * 4, 256);
+    }
     w.bytes = off;
     return w;
 }
@@ -373,7 +416,8 @@ extern "C" size_t moe_router_workspace_size(int T, int h, int E, int k, int dtyp
     (void)k;
     if (T < 0 || h <= 0 || E <= 0) return 0;
     const int el = dtype == MOE_F32 ? 4 : 2;
-    return router_ws_layout(nullptr, T, h, E, el, !use_small_path(h, E, el)).bytes;
+    const bool small = use_small_path(h, E, el);
+    return router_ws_layout(nullptr, T, h, E, el, !small, use_tc_logits(E, dtype, small)).bytes;
 }
 
 extern "C" int moe_router(const void* x, const void* w_r, const float* bias, int T, int h, int E, int k, int dtype,
@@ -391,7 +435,8 @@ extern "C" int moe_router(const void* x, const void* w_r, const float* bias, int
                 "moe_router: x, w_r and logits must be 16-byte aligned");
     const int el = dtype == MOE_F32 ? 4 : 2;
     const bool small = use_small_path(h, E, el);
-    RouterWs w = router_ws_layout(ws, T, h, E, el, !small && logits == nullptr);
+    const bool tc = use_tc_logits(E, dtype, small);
+    RouterWs w = router_ws_layout(ws, T, h, E, el, !small && logits == nullptr, tc);
     MOE_REQUIRE(ws_bytes >= w.bytes && (w.bytes == 0 || ws), MOE_ERR_WORKSPACE,
                 "moe_router: workspace %zu < %zu bytes", ws_bytes, w.bytes);
     cudaStream_t s = static_cast<cudaStream_t>(stream);
@@ -431,14 +476,22 @@ extern "C" int moe_router(const void* x, const void* w_r, const float* bias, int
         } else {
             float* lg = logits ? logits : w.logits;
             const float* lbias = (gating != MOE_GATING_SIGMOID_BIAS_RENORM) ? bias : nullptr;
-            dim3 grid(cdiv(E, 64), cdiv(T, 64));
-            if (dtype == MOE_BF16)
-                router_logits_gemm<__nv_bfloat16><<<grid, 256, 0, s>>>(static_cast<const __nv_bfloat16*>(x),
-                    static_cast<const __nv_bfloat16*>(w_r), lbias, T, h, E, lg);
-            else
-                router_logits_gemm<float><<<grid, 256, 0, s>>>(static_cast<const float*>(x),
-                    static_cast<const float*>(w_r), lbias, T, h, E, lg);
-            if (int rc = check_launch("router_logits_gemm")) return rc;
+            if (tc) {
+                router_transpose_kernel<<<dim3(cdiv(E, 32), cdiv(h, 32)), dim3(32, 8), 0, s>>>(
+                    static_cast<const __nv_bfloat16*>(w_r), h, E, static_cast<__nv_bfloat16*>(w.w_rT));
+                if (int rc = check_launch("router_transpose_kernel")) return rc;
+                if (int rc = launch_dense_sched(T, w.sched, s)) return rc;
+                if (int rc = tc_router_logits(x, w.w_rT, lbias, T, h, E, w.sched, lg, s)) return rc;
+            } else {
+                dim3 grid(cdiv(E, 64), cdiv(T, 64));
+                if (dtype == MOE_BF16)
+                    router_logits_gemm<__nv_bfloat16><<<grid, 256, 0, s>>>(static_cast<const __nv_bfloat16*>(x),
+                        static_cast<const __nv_bfloat16*>(w_r), lbias, T, h, E, lg);
+                else
+                    router_logits_gemm<float><<<grid, 256, 0, s>>>(static_cast<const float*>(x),
+                        static_cast<const float*>(w_r), lbias, T, h, E, lg);
+                if (int rc = check_launch("router_logits_gemm")) return rc;
+            }
             const size_t smem = (size_t)kRouterWarps * E * sizeof(float) + (size_t)E * sizeof(int);
             const int npl = cdiv(E, 32);
             o.logits = nullptr;
