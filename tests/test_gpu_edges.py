@@ -138,3 +138,27 @@ def test_host_argument_errors():
     with pytest.raises(moe.MoEError) as ei:
         moe.moe_router(x.half(), torch.zeros((16, 4), dtype=torch.half, device="cuda"), None, 2)
     assert ei.value.code == moe.MOE_ERR_UNSUPPORTED
+
+
+@pytest.mark.parametrize("C", [0, 50])
+def test_dispatch_large_count_table_path(C):
+    """T=70000 tokens, E=1024 experts, k=1: the per-chunk count table (69 chunks x 1024 experts) is too large
+    for the single-launch scan+scatter, so dispatch takes its three-launch path; both must agree with the
+    oracle."""
+    import torch
+    from top_routing_dispatch_moe_gb300 import moe
+    T, h, E = 70000, 8, 1024
+    rng = np.random.default_rng(C)
+    ids = rng.integers(0, E, size=(T, 1)).astype(np.int32)
+    x = torch.randn(T, h, device="cuda").to(torch.bfloat16)
+    d = moe.moe_dispatch(x, torch.from_numpy(ids).cuda(), E, capacity=C, num_ranks=8)
+    torch.cuda.synchronize()
+    ref = O.dispatch(ids, E, C, 8)
+    for key in ["offsets", "kept_counts", "dest_row", "src_token", "src_slot", "rank_counts", "rank_offsets"]:
+        np.testing.assert_array_equal(d[key].cpu().numpy(), ref[key], err_msg=key)
+    live = ref["src_token"] >= 0
+    got = d["buf"].view(torch.int16).cpu().numpy()
+    want = x.view(torch.int16).cpu().numpy()[ref["src_token"][live]]
+    np.testing.assert_array_equal(got[live], want)
+    if C:
+        assert np.all(got[~live] == 0)

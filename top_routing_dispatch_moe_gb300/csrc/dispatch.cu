@@ -66,6 +66,53 @@ __device__ int block_inclusive_scan(int v, int* s_tmp) {
     return v;
 }
 
+// Per-expert kept counts -> offsets, tile prefix (block scans; every thread of the 1024-thread block calls
+// it). Thread e < E passes its expert's assignment count n; s_off / s_tp / s_kept receive E + 1 / E + 1 / E
+// entries.
+__device__ void layout_from_counts(int n, int E, int C, int* s_tmp, int* s_kept, int* s_off, int* s_tp) {
+    const int e = threadIdx.x;
+    const int kept = (e < E) ? (C > 0 ? min(n, C) : n) : 0;
+    const int incl = block_inclusive_scan(kept, s_tmp);
+    const int ntiles = (kept + MOE_TILE_M - 1) / MOE_TILE_M;
+    const int tincl = block_inclusive_scan(ntiles, s_tmp);
+    if (e < E) {
+        s_kept[e] = kept;
+        s_off[e] = C > 0 ? e * C : incl - kept;
+        s_tp[e] = tincl - ntiles;
+    }
+    if (e == E - 1) { s_off[E] = C > 0 ? E * C : incl; s_tp[E] = tincl; }
+    __syncthreads();
+}
+
+// Writes offsets, kept counts, the EP rank layout and the tile schedule from the shared layout.
+__device__ void publish_layout(int E, int R, const int* s_kept, const int* s_off, const int* s_tp,
+                               int32_t* __restrict__ offsets, int32_t* __restrict__ kept_counts,
+                               int32_t* __restrict__ rank_counts, int32_t* __restrict__ rank_offsets,
+                               int32_t* __restrict__ sched) {
+    const int e = threadIdx.x;
+    for (int i = e; i <= E; i += blockDim.x) {
+        offsets[i] = s_off[i];
+        sched[kSchedHeader + i] = s_tp[i];
+    }
+    if (e < E) kept_counts[e] = s_kept[e];
+    if (e == 0) { sched[0] = s_tp[E]; sched[1] = E; }
+    const int epr = E / R;
+    for (int r = e; r <= R; r += blockDim.x) rank_offsets[r] = s_off[r * epr];
+    if (e < R) {
+        int sum = 0;
+        for (int i = e * epr; i < (e + 1) * epr; ++i) sum += s_kept[i];
+        rank_counts[e] = sum;
+    }
+    if (e < E) {
+        int4* tiles = reinterpret_cast<int4*>(sched + sched_tiles_offset(E));
+        const int row0 = s_off[e], ntiles = s_tp[e + 1] - s_tp[e];
+        for (int m = 0; m < ntiles; ++m) {
+            const int rb = row0 + m * MOE_TILE_M;
+            tiles[s_tp[e] + m] = make_int4(e, rb, min(rb + MOE_TILE_M, row0 + s_kept[e]), 0);
+        }
+    }
+}
+
 __global__ void __launch_bounds__(1024)
 dispatch_scan_kernel(int32_t* __restrict__ chunk_counts /* in: counts, out: per-chunk base */, int nchunks, int E,
                      int C, int R, int32_t* __restrict__ offsets, int32_t* __restrict__ kept_counts,
@@ -83,46 +130,17 @@ dispatch_scan_kernel(int32_t* __restrict__ chunk_counts /* in: counts, out: per-
             n += v;
         }
     }
-    const int kept = (e < E) ? (C > 0 ? min(n, C) : n) : 0;
-    const int incl = block_inclusive_scan(kept, s_tmp);
-    const int ntiles = (kept + MOE_TILE_M - 1) / MOE_TILE_M;
-    const int tincl = block_inclusive_scan(ntiles, s_tmp);
-    if (e < E) {
-        s_kept[e] = kept;
-        s_off[e] = C > 0 ? e * C : incl - kept;
-        s_tp[e] = tincl - ntiles;
-    }
-    if (e == E - 1) { s_off[E] = C > 0 ? E * C : incl; s_tp[E] = tincl; }
-    __syncthreads();
-    for (int i = e; i <= E; i += blockDim.x) {
-        offsets[i] = s_off[i];
-        sched[kSchedHeader + i] = s_tp[i];
-    }
-    if (e < E) kept_counts[e] = s_kept[e];
-    if (e == 0) { sched[0] = s_tp[E]; sched[1] = E; }
-    const int epr = E / R;
-    for (int r = e; r <= R; r += blockDim.x) rank_offsets[r] = s_off[r * epr];
-    if (e < R) {
-        int s = 0;
-        for (int i = e * epr; i < (e + 1) * epr; ++i) s += s_kept[i];
-        rank_counts[e] = s;
-    }
-    if (e < E) {
-        int4* tiles = reinterpret_cast<int4*>(sched + sched_tiles_offset(E));
-        const int row0 = s_off[e];
-        for (int m = 0; m < ntiles; ++m) {
-            const int rb = row0 + m * MOE_TILE_M;
-            tiles[s_tp[e] + m] = make_int4(e, rb, min(rb + MOE_TILE_M, row0 + kept), 0);
-        }
-    }
+    layout_from_counts(n, E, C, s_tmp, s_kept, s_off, s_tp);
+    publish_layout(E, R, s_kept, s_off, s_tp, offsets, kept_counts, rank_counts, rank_offsets, sched);
 }
 
-__global__ void __launch_bounds__(kChunkA)
-dispatch_scatter_kernel(const int32_t* __restrict__ ids, int T, int E, int k, int C,
-                        const int32_t* __restrict__ chunk_base, const int32_t* __restrict__ offsets,
-                        int32_t* __restrict__ dest_row, uint8_t* __restrict__ drop_mask,
-                        int32_t* __restrict__ src_token, int32_t* __restrict__ src_slot) {
-    extern __shared__ int s_wc[];                 // [32 warps][E] per-warp counts, then prefixes
+// Ranks the chunk's assignments in token order and writes dest_row, drop_mask, src_token, src_slot.
+// s_wc: [32][E] shared scratch; chunk_base(e) = assignments to e in earlier chunks; off = expert offsets.
+template <typename Base, typename Off>
+__device__ __forceinline__ void rank_chunk(const int32_t* __restrict__ ids, int T, int E, int k, int C, int* s_wc,
+                                           Base chunk_base, Off off, int32_t* __restrict__ dest_row,
+                                           uint8_t* __restrict__ drop_mask, int32_t* __restrict__ src_token,
+                                           int32_t* __restrict__ src_slot) {
     for (int i = threadIdx.x; i < 32 * E; i += blockDim.x) s_wc[i] = 0;
     __syncthreads();
     const int tpc = tokens_per_chunk(k);
@@ -144,9 +162,9 @@ dispatch_scatter_kernel(const int32_t* __restrict__ ids, int T, int E, int k, in
     if (valid) {
         int d = -1;
         if (e >= 0) {
-            const int slot = chunk_base[(size_t)blockIdx.x * E + e] + s_wc[warp * E + e] + intra;
+            const int slot = chunk_base(e) + s_wc[warp * E + e] + intra;
             if (C == 0 || slot < C) {
-                d = offsets[e] + slot;
+                d = off(e) + slot;
                 src_token[d] = t;
                 src_slot[d] = j;
             }
@@ -156,45 +174,99 @@ dispatch_scatter_kernel(const int32_t* __restrict__ ids, int T, int E, int k, in
     }
 }
 
-// One warp per token: read x[t] once, write it to each kept destination row.
-template <typename T>
-__global__ void __launch_bounds__(256)
-dispatch_copy_kernel(const T* __restrict__ x, const int32_t* __restrict__ dest_row, int T_, int h, int k,
-                     T* __restrict__ buf) {
-    constexpr int V = Vec16<T>::N;
-    const int lane = threadIdx.x & 31;
-    const int t = blockIdx.x * 8 + (threadIdx.x >> 5);
-    if (t >= T_) return;
-    const int my = lane < k ? dest_row[(size_t)t * k + lane] : -1;
-    int dj[16];
-#pragma unroll
-    for (int j = 0; j < 16; ++j) dj[j] = __shfl_sync(0xffffffffu, my, j);   // all lanes, before any exit
-    const T* src = x + (size_t)t * h;
-    constexpr int U = 4;                          // 16-byte loads in flight per lane
-    for (int d0 = lane * V; d0 < h; d0 += U * 32 * V) {
-        Vec16<T> v[U];
-#pragma unroll
-        for (int u = 0; u < U; ++u)
-            if (d0 + u * 32 * V < h) v[u] = ld16_stream(src + d0 + u * 32 * V);
-#pragma unroll
-        for (int j = 0; j < 16; ++j)
-            if (j < k && dj[j] >= 0) {
-#pragma unroll
-                for (int u = 0; u < U; ++u)
-                    if (d0 + u * 32 * V < h) st16(buf + (size_t)dj[j] * h + d0 + u * 32 * V, v[u]);
-            }
-    }
+__global__ void __launch_bounds__(kChunkA)
+dispatch_scatter_kernel(const int32_t* __restrict__ ids, int T, int E, int k, int C,
+                        const int32_t* __restrict__ chunk_base, const int32_t* __restrict__ offsets,
+                        int32_t* __restrict__ dest_row, uint8_t* __restrict__ drop_mask,
+                        int32_t* __restrict__ src_token, int32_t* __restrict__ src_slot) {
+    extern __shared__ int s_wc[];
+    rank_chunk(ids, T, E, k, C, s_wc, [&](int e) { return chunk_base[(size_t)blockIdx.x * E + e]; },
+               [&](int e) { return offsets[e]; }, dest_row, drop_mask, src_token, src_slot);
 }
 
-// Capacity mode: pad rows [offsets[e] + kept[e], offsets[e+1]) -> zero payload, src = -1.
+// Scan and scatter in one launch, for count tables of at most kFusedScanEntries entries: every block adds up
+// the count table itself (its own chunk base and the per-expert totals, in a fixed order) and derives the
+// same offsets; block 0 also publishes offsets, kept counts, the rank layout and the tile schedule.
+constexpr int kFusedScanEntries = 1 << 16;
+
+// Shared-memory layout of dispatch_scan_scatter_kernel, in ints: s_wc [32 E], s_base [E], s_kept [E],
+// s_off [E + 1], s_tp [E + 1]. The kernel's pointers and the launch's allocation both come from here.
+__host__ __device__ constexpr int fused_wc(int) { return 0; }
+__host__ __device__ constexpr int fused_base(int E) { return 32 * E; }
+__host__ __device__ constexpr int fused_kept(int E) { return fused_base(E) + E; }
+__host__ __device__ constexpr int fused_off(int E) { return fused_kept(E) + E; }
+__host__ __device__ constexpr int fused_tp(int E) { return fused_off(E) + E + 1; }
+__host__ __device__ constexpr int fused_smem_ints(int E) { return fused_tp(E) + E + 1; }
+
+__global__ void __launch_bounds__(kChunkA)
+dispatch_scan_scatter_kernel(const int32_t* __restrict__ ids, int T, int E, int k, int C, int R,
+                             const int32_t* __restrict__ chunk_counts, int nchunks, int32_t* __restrict__ offsets,
+                             int32_t* __restrict__ kept_counts, int32_t* __restrict__ rank_counts,
+                             int32_t* __restrict__ rank_offsets, int32_t* __restrict__ sched,
+                             int32_t* __restrict__ dest_row, uint8_t* __restrict__ drop_mask,
+                             int32_t* __restrict__ src_token, int32_t* __restrict__ src_slot) {
+    extern __shared__ int sm[];
+    int* s_wc = sm + fused_wc(E);                // [32][E]
+    int* s_base = sm + fused_base(E);            // [E]
+    int* s_kept = sm + fused_kept(E);            // [E]
+    int* s_off = sm + fused_off(E);              // [E + 1]
+    int* s_tp = sm + fused_tp(E);                // [E + 1]
+    __shared__ int s_tmp[32];
+    const int e = threadIdx.x;
+    int base = 0, total = 0;
+    if (e < E) {
+#pragma unroll 4
+        for (int c = 0; c < nchunks; ++c) {
+            const int v = __ldg(chunk_counts + (size_t)c * E + e);
+            total += v;
+            base += c < (int)blockIdx.x ? v : 0;
+        }
+        s_base[e] = base;
+    }
+    layout_from_counts(total, E, C, s_tmp, s_kept, s_off, s_tp);
+    if (blockIdx.x == 0)
+        publish_layout(E, R, s_kept, s_off, s_tp, offsets, kept_counts, rank_counts, rank_offsets, sched);
+    rank_chunk(ids, T, E, k, C, s_wc, [&](int ee) { return s_base[ee]; }, [&](int ee) { return s_off[ee]; },
+               dest_row, drop_mask, src_token, src_slot);
+}
+
+// Blocks [0, tok_blocks): one warp per token, read x[t] once and write it to each kept destination row.
+// Blocks [tok_blocks, grid) (capacity mode): pad rows [offsets[e] + kept[e], offsets[e + 1]) get a zero
+// payload and src = -1.
 template <typename T>
 __global__ void __launch_bounds__(256)
-dispatch_pad_kernel(const int32_t* __restrict__ kept_counts, int E, int C, int h, T* __restrict__ buf,
-                    int32_t* __restrict__ src_token, int32_t* __restrict__ src_slot) {
+dispatch_copy_pad_kernel(const T* __restrict__ x, const int32_t* __restrict__ dest_row, int T_, int h, int k,
+                         T* __restrict__ buf, int tok_blocks, const int32_t* __restrict__ kept_counts, int E, int C,
+                         int32_t* __restrict__ src_token, int32_t* __restrict__ src_slot) {
     constexpr int V = Vec16<T>::N;
     const int lane = threadIdx.x & 31;
+    if ((int)blockIdx.x < tok_blocks) {
+        const int t = blockIdx.x * 8 + (threadIdx.x >> 5);
+        if (t >= T_) return;
+        const int my = lane < k ? dest_row[(size_t)t * k + lane] : -1;
+        int dj[16];
+#pragma unroll
+        for (int j = 0; j < 16; ++j) dj[j] = __shfl_sync(0xffffffffu, my, j);   // all lanes, before any exit
+        const T* src = x + (size_t)t * h;
+        constexpr int U = 4;                      // 16-byte loads in flight per lane
+        for (int d0 = lane * V; d0 < h; d0 += U * 32 * V) {
+            Vec16<T> v[U];
+#pragma unroll
+            for (int u = 0; u < U; ++u)
+                if (d0 + u * 32 * V < h) v[u] = ld16_stream(src + d0 + u * 32 * V);
+#pragma unroll
+            for (int j = 0; j < 16; ++j)
+                if (j < k && dj[j] >= 0) {
+#pragma unroll
+                    for (int u = 0; u < U; ++u)
+                        if (d0 + u * 32 * V < h) st16(buf + (size_t)dj[j] * h + d0 + u * 32 * V, v[u]);
+                }
+        }
+        return;
+    }
     const long long rows = (long long)E * C;
-    for (long long r = (long long)blockIdx.x * 8 + (threadIdx.x >> 5); r < rows; r += (long long)gridDim.x * 8) {
+    const int nb = gridDim.x - tok_blocks;
+    for (long long r = (long long)(blockIdx.x - tok_blocks) * 8 + (threadIdx.x >> 5); r < rows; r += (long long)nb * 8) {
         const int e = (int)(r / C);
         if (r - (long long)e * C < kept_counts[e]) continue;
         if (lane == 0) { src_token[r] = -1; src_slot[r] = -1; }
@@ -266,32 +338,36 @@ extern "C" int moe_dispatch(const void* x, const int32_t* topk_ids, int T, int h
         dispatch_count_kernel<<<nch, kChunkA, E * sizeof(int), s>>>(topk_ids, T, E, k, chunk, err);
         if (int rc = check_launch("dispatch_count_kernel")) return rc;
     }
-    dispatch_scan_kernel<<<1, 1024, 0, s>>>(chunk, nch, E, capacity, num_ranks, offsets, kept_counts, rank_counts,
-                                           rank_offsets, tile_sched);
-    if (int rc = check_launch("dispatch_scan_kernel")) return rc;
-    if (nch > 0) {
-        const size_t smem = (size_t)32 * E * sizeof(int);
-        cudaFuncSetAttribute(dispatch_scatter_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-        dispatch_scatter_kernel<<<nch, kChunkA, smem, s>>>(topk_ids, T, E, k, capacity, chunk, offsets, dest_row,
-                                                          drop_mask, src_token, src_slot);
-        if (int rc = check_launch("dispatch_scatter_kernel")) return rc;
-        if (dtype == MOE_BF16)
-            dispatch_copy_kernel<__nv_bfloat16><<<cdiv(T, 8), 256, 0, s>>>(static_cast<const __nv_bfloat16*>(x),
-                dest_row, T, h, k, static_cast<__nv_bfloat16*>(buf));
-        else
-            dispatch_copy_kernel<float><<<cdiv(T, 8), 256, 0, s>>>(static_cast<const float*>(x), dest_row, T, h, k,
-                                                                  static_cast<float*>(buf));
-        if (int rc = check_launch("dispatch_copy_kernel")) return rc;
+    if (nch > 0 && (long long)nch * E <= kFusedScanEntries) {
+        const size_t smem = (size_t)fused_smem_ints(E) * sizeof(int);
+        cudaFuncSetAttribute(dispatch_scan_scatter_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        dispatch_scan_scatter_kernel<<<nch, kChunkA, smem, s>>>(topk_ids, T, E, k, capacity, num_ranks, chunk, nch,
+            offsets, kept_counts, rank_counts, rank_offsets, tile_sched, dest_row, drop_mask, src_token, src_slot);
+        if (int rc = check_launch("dispatch_scan_scatter_kernel")) return rc;
+    } else {
+        dispatch_scan_kernel<<<1, 1024, 0, s>>>(chunk, nch, E, capacity, num_ranks, offsets, kept_counts, rank_counts,
+                                               rank_offsets, tile_sched);
+        if (int rc = check_launch("dispatch_scan_kernel")) return rc;
+        if (nch > 0) {
+            const size_t smem = (size_t)32 * E * sizeof(int);
+            cudaFuncSetAttribute(dispatch_scatter_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+            dispatch_scatter_kernel<<<nch, kChunkA, smem, s>>>(topk_ids, T, E, k, capacity, chunk, offsets, dest_row,
+                                                              drop_mask, src_token, src_slot);
+            if (int rc = check_launch("dispatch_scatter_kernel")) return rc;
+        }
     }
-    if (capacity > 0 && rows > 0) {
-        const int grid = std::min(cdiv(rows, 8), 8 * num_sms());
+    const int tok_blocks = cdiv(T, 8);
+    const int pad_blocks = (capacity > 0 && rows > 0) ? std::min(cdiv(rows, 8), 2 * num_sms()) : 0;
+    if (tok_blocks + pad_blocks > 0) {
         if (dtype == MOE_BF16)
-            dispatch_pad_kernel<__nv_bfloat16><<<grid, 256, 0, s>>>(kept_counts, E, capacity, h,
-                static_cast<__nv_bfloat16*>(buf), src_token, src_slot);
+            dispatch_copy_pad_kernel<__nv_bfloat16><<<tok_blocks + pad_blocks, 256, 0, s>>>(
+                static_cast<const __nv_bfloat16*>(x), dest_row, T, h, k, static_cast<__nv_bfloat16*>(buf), tok_blocks,
+                kept_counts, E, capacity, src_token, src_slot);
         else
-            dispatch_pad_kernel<float><<<grid, 256, 0, s>>>(kept_counts, E, capacity, h, static_cast<float*>(buf),
-                                                           src_token, src_slot);
-        if (int rc = check_launch("dispatch_pad_kernel")) return rc;
+            dispatch_copy_pad_kernel<float><<<tok_blocks + pad_blocks, 256, 0, s>>>(
+                static_cast<const float*>(x), dest_row, T, h, k, static_cast<float*>(buf), tok_blocks, kept_counts, E,
+                capacity, src_token, src_slot);
+        if (int rc = check_launch("dispatch_copy_pad_kernel")) return rc;
     }
     return MOE_OK;
 }

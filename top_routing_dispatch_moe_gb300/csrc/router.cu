@@ -144,11 +144,11 @@ __device__ __forceinline__ void unpack16(const Vec16<__nv_bfloat16>& v, float (&
 }
 
 // ---------------------------------------------------------------------------------------------------
-// E <= 32: fused logits + gating, W_r^T in shared memory
+// E <= 32: fused logits + gating, W_r^T in shared memory (copied from the per-call transposed weight)
 // ---------------------------------------------------------------------------------------------------
 template <typename T, int EMAX>
 __global__ void __launch_bounds__(kRouterWarps * 32)
-router_small_kernel(const T* __restrict__ x, const T* __restrict__ w_r, const float* __restrict__ bias, int T_,
+router_small_kernel(const T* __restrict__ x, const T* __restrict__ w_rT, const float* __restrict__ bias, int T_,
                     int h, int E, int k, int gating, GateOut o) {
     extern __shared__ __align__(16) unsigned char smem_raw[];
     T* wT = reinterpret_cast<T*>(smem_raw);                                     // [E][h]
@@ -156,27 +156,10 @@ router_small_kernel(const T* __restrict__ x, const T* __restrict__ w_r, const fl
     int* s_hist = reinterpret_cast<int*>(s_P + kRouterWarps * E);
 
     constexpr int V = Vec16<T>::N;
-    {   // stage W_r^T: 16-byte loads of the row-major [h][E] weight, transposed into shared memory
-        const int nvec = h * E / V;
-        for (int v0 = threadIdx.x; v0 < nvec; v0 += 4 * blockDim.x) {
-            Vec16<T> wv[4];
-#pragma unroll
-            for (int u = 0; u < 4; ++u) {
-                const int v = v0 + u * blockDim.x;
-                if (v < nvec) wv[u] = ld16(w_r + (size_t)v * V);
-            }
-#pragma unroll
-            for (int u = 0; u < 4; ++u) {
-                const int v = v0 + u * blockDim.x;
-                if (v < nvec) {
-#pragma unroll
-                    for (int q = 0; q < V; ++q) {
-                        const int i = v * V + q, d = i / E, e = i - d * E;
-                        wT[(size_t)e * h + d] = from_f32<T>(wv[u].get(q));
-                    }
-                }
-            }
-        }
+    {   // stage W_r^T [E][h] (transposed once per call) into shared memory with 16-byte copies
+        const int nvec = E * h / V;
+        for (int v = threadIdx.x; v < nvec; v += blockDim.x)
+            *reinterpret_cast<Vec16<T>*>(wT + (size_t)v * V) = ld16(w_rT + (size_t)v * V);
     }
     for (int e = threadIdx.x; e < E; e += blockDim.x) s_hist[e] = 0;
     __syncthreads();
@@ -354,10 +337,12 @@ router_finalize(const float* __restrict__ partial_P, const int32_t* __restrict__
     if (threadIdx.x == 0) aux[0] = alpha * (float)E * s_red[0];
 }
 
-// W_r [h, E] -> W_rT [E, h] (K-major operand of the tensor-core logits GEMM), 32 x 32 shared-memory tiles.
+// W_r [h, E] -> W_rT [E, h]: the K-major operand of the tensor-core logits GEMM and the per-expert rows the
+// fused small-E kernel streams. 32 x 32 shared-memory tiles.
+template <typename T>
 __global__ void __launch_bounds__(256)
-router_transpose_kernel(const __nv_bfloat16* __restrict__ w, int h, int E, __nv_bfloat16* __restrict__ wT) {
-    __shared__ __nv_bfloat16 tile[32][33];
+router_transpose_kernel(const T* __restrict__ w, int h, int E, T* __restrict__ wT) {
+    __shared__ T tile[32][33];
     const int e0 = blockIdx.x * 32, d0 = blockIdx.y * 32;
     for (int r = threadIdx.y; r < 32; r += 8) {
         const int d = d0 + r, e = e0 + threadIdx.x;
@@ -375,8 +360,9 @@ router_transpose_kernel(const __nv_bfloat16* __restrict__ w, int h, int E, __nv_
 // ---------------------------------------------------------------------------------------------------
 // Upper bound of the blocks of any router launch (sizes the partial-sum workspace).
 static int router_grid(int T) { return std::max(1, std::min(cdiv(T, kRouterWarps), kRouterMaxBlocks)); }
-// The fused small-E kernel stages the router weight in every block: three blocks per SM amortise it.
-static int router_small_grid(int T) { return std::max(1, std::min(router_grid(T), 3 * num_sms())); }
+// The fused small-E kernel copies the transposed router weight into every block; its register budget allows
+// two blocks per SM.
+static int router_small_grid(int T) { return std::max(1, std::min(router_grid(T), 2 * num_sms())); }
 
 static size_t small_smem_bytes(int h, int E, int el) {
     return align_up((size_t)E * h * el, 16) + (size_t)kRouterWarps * E * sizeof(float) + (size_t)E * sizeof(int);
@@ -389,7 +375,7 @@ static bool use_tc_logits(int E, int dtype, bool small) { return !small && dtype
 
 struct RouterWs { float* partial_P; int32_t* partial_C; float* logits; void* w_rT; int32_t* sched; size_t bytes; };
 
-static RouterWs router_ws_layout(void* ws, int T, int h, int E, int el, bool need_logits, bool tc) {
+static RouterWs router_ws_layout(void* ws, int T, int h, int E, int el, bool small, bool need_logits, bool tc) {
     RouterWs w{};
     const int G = router_grid(T);
     size_t off = 0;
@@ -400,10 +386,10 @@ static RouterWs router_ws_layout(void* ws, int T, int h, int E, int el, bool nee
     if (need_logits) { w.logits = reinterpret_cast<float*>(base + off); off = align_up(off + (size_t)T * E * 4, 256); }
     w.w_rT = nullptr;
     w.sched = nullptr;
-    if (tc) {
+    if (tc || small) {                       // transposed weight: tensor-core GEMM and fused small-E kernel
         w.w_rT = base + off; off = align_up(off + (size_t)E * h * el, 256);
-        w.sched = reinterpret_cast<int32_t*>(base + off); off = align_up(off + sched_words(T, 1) * 4, 256);
     }
+    if (tc) { w.sched = reinterpret_cast<int32_t*>(base + off); off = align_up(off + sched_words(T, 1) * 4, 256); }
     w.bytes = off;
     return w;
 }
@@ -417,7 +403,7 @@ extern "C" size_t moe_router_workspace_size(int T, int h, int E, int k, int dtyp
     if (T < 0 || h <= 0 || E <= 0) return 0;
     const int el = dtype == MOE_F32 ? 4 : 2;
     const bool small = use_small_path(h, E, el);
-    return router_ws_layout(nullptr, T, h, E, el, !small, use_tc_logits(E, dtype, small)).bytes;
+    return router_ws_layout(nullptr, T, h, E, el, small, !small, use_tc_logits(E, dtype, small)).bytes;
 }
 
 extern "C" int moe_router(const void* x, const void* w_r, const float* bias, int T, int h, int E, int k, int dtype,
@@ -436,7 +422,7 @@ extern "C" int moe_router(const void* x, const void* w_r, const float* bias, int
     const int el = dtype == MOE_F32 ? 4 : 2;
     const bool small = use_small_path(h, E, el);
     const bool tc = use_tc_logits(E, dtype, small);
-    RouterWs w = router_ws_layout(ws, T, h, E, el, !small && logits == nullptr, tc);
+    RouterWs w = router_ws_layout(ws, T, h, E, el, small, !small && logits == nullptr, tc);
     MOE_REQUIRE(ws_bytes >= w.bytes && (w.bytes == 0 || ws), MOE_ERR_WORKSPACE,
                 "moe_router: workspace %zu < %zu bytes", ws_bytes, w.bytes);
     cudaStream_t s = static_cast<cudaStream_t>(stream);
@@ -445,9 +431,13 @@ extern "C" int moe_router(const void* x, const void* w_r, const float* bias, int
     if (T > 0) {
         if (small) {
             const size_t smem = small_smem_bytes(h, E, el);
+            const dim3 tgrid(cdiv(E, 32), cdiv(h, 32)), tblock(32, 8);
             if (dtype == MOE_BF16) {
                 const __nv_bfloat16* xb = static_cast<const __nv_bfloat16*>(x);
-                const __nv_bfloat16* wb = static_cast<const __nv_bfloat16*>(w_r);
+                const __nv_bfloat16* wb = static_cast<const __nv_bfloat16*>(w.w_rT);
+                router_transpose_kernel<__nv_bfloat16><<<tgrid, tblock, 0, s>>>(
+                    static_cast<const __nv_bfloat16*>(w_r), h, E, static_cast<__nv_bfloat16*>(w.w_rT));
+                if (int rc = check_launch("router_transpose_kernel")) return rc;
                 if (E <= 8) {
                     cudaFuncSetAttribute(router_small_kernel<__nv_bfloat16, 8>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
                     router_small_kernel<__nv_bfloat16, 8><<<G, kRouterWarps * 32, smem, s>>>(xb, wb, bias, T, h, E, k, gating, o);
@@ -460,7 +450,10 @@ extern "C" int moe_router(const void* x, const void* w_r, const float* bias, int
                 }
             } else {
                 const float* xf = static_cast<const float*>(x);
-                const float* wf = static_cast<const float*>(w_r);
+                const float* wf = static_cast<const float*>(w.w_rT);
+                router_transpose_kernel<float><<<tgrid, tblock, 0, s>>>(static_cast<const float*>(w_r), h, E,
+                                                                        static_cast<float*>(w.w_rT));
+                if (int rc = check_launch("router_transpose_kernel")) return rc;
                 if (E <= 8) {
                     cudaFuncSetAttribute(router_small_kernel<float, 8>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
                     router_small_kernel<float, 8><<<G, kRouterWarps * 32, smem, s>>>(xf, wf, bias, T, h, E, k, gating, o);
@@ -477,7 +470,7 @@ extern "C" int moe_router(const void* x, const void* w_r, const float* bias, int
             float* lg = logits ? logits : w.logits;
             const float* lbias = (gating != MOE_GATING_SIGMOID_BIAS_RENORM) ? bias : nullptr;
             if (tc) {
-                router_transpose_kernel<<<dim3(cdiv(E, 32), cdiv(h, 32)), dim3(32, 8), 0, s>>>(
+                router_transpose_kernel<__nv_bfloat16><<<dim3(cdiv(E, 32), cdiv(h, 32)), dim3(32, 8), 0, s>>>(
                     static_cast<const __nv_bfloat16*>(w_r), h, E, static_cast<__nv_bfloat16*>(w.w_rT));
                 if (int rc = check_launch("router_transpose_kernel")) return rc;
                 if (int rc = launch_dense_sched(T, w.sched, s)) return rc;
