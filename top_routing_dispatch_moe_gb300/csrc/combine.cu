@@ -11,7 +11,7 @@
 
 namespace moe {
 
-template <typename T>
+template <typename T, int KMAX>
 __global__ void __launch_bounds__(256)
 combine_kernel(const T* __restrict__ eout, const int32_t* __restrict__ dest_row, const float* __restrict__ gates,
                const T* __restrict__ shared_out, int T_, int h, int k, T* __restrict__ y) {
@@ -21,10 +21,10 @@ combine_kernel(const T* __restrict__ eout, const int32_t* __restrict__ dest_row,
     if (t >= T_) return;
     const int myd = lane < k ? dest_row[(size_t)t * k + lane] : -1;
     const float myg = lane < k ? gates[(size_t)t * k + lane] : 0.f;
-    int dj[16];
-    float gj[16];
+    int dj[KMAX];
+    float gj[KMAX];
 #pragma unroll
-    for (int j = 0; j < 16; ++j) {
+    for (int j = 0; j < KMAX; ++j) {
         dj[j] = __shfl_sync(0xffffffffu, myd, j);
         gj[j] = __shfl_sync(0xffffffffu, myg, j);
     }
@@ -45,7 +45,7 @@ combine_kernel(const T* __restrict__ eout, const int32_t* __restrict__ dest_row,
         }
         // issue every load of this pass before the first use: k rows x U chunks in flight per lane
 #pragma unroll
-        for (int j0 = 0; j0 < 16; j0 += 4) {
+        for (int j0 = 0; j0 < KMAX; j0 += 4) {
             if (j0 >= k) break;
             Vec16<T> v[4][U];
 #pragma unroll
@@ -53,14 +53,14 @@ combine_kernel(const T* __restrict__ eout, const int32_t* __restrict__ dest_row,
 #pragma unroll
                 for (int u = 0; u < U; ++u) {
                     const int j = j0 + jj, d = d0 + u * 32 * V;
-                    if (j < k && dj[j] >= 0 && d < h) v[jj][u] = ld16_stream(eout + (size_t)dj[j] * h + d);
+                    if (j < KMAX && j < k && dj[j] >= 0 && d < h) v[jj][u] = ld16_stream(eout + (size_t)dj[j] * h + d);
                 }
 #pragma unroll
             for (int jj = 0; jj < 4; ++jj)
 #pragma unroll
                 for (int u = 0; u < U; ++u) {
                     const int j = j0 + jj, d = d0 + u * 32 * V;
-                    if (j < k && dj[j] >= 0 && d < h) {
+                    if (j < KMAX && j < k && dj[j] >= 0 && d < h) {
 #pragma unroll
                         for (int i = 0; i < V; ++i) acc[u][i] = fmaf(gj[j], v[jj][u].get(i), acc[u][i]);
                     }
@@ -93,11 +93,20 @@ extern "C" int moe_combine(const void* eout, const int32_t* dest_row, const floa
     MOE_REQUIRE(aligned16(eout) && aligned16(shared_out) && aligned16(y), MOE_ERR_INVALID_ARG,
                 "moe_combine: eout, shared_out and y must be 16-byte aligned");
     cudaStream_t s = static_cast<cudaStream_t>(stream);
-    if (dtype == MOE_BF16)
-        combine_kernel<__nv_bfloat16><<<cdiv(T, 8), 256, 0, s>>>(static_cast<const __nv_bfloat16*>(eout), dest_row,
-            gates, static_cast<const __nv_bfloat16*>(shared_out), T, h, k, static_cast<__nv_bfloat16*>(y));
-    else
-        combine_kernel<float><<<cdiv(T, 8), 256, 0, s>>>(static_cast<const float*>(eout), dest_row, gates,
-            static_cast<const float*>(shared_out), T, h, k, static_cast<float*>(y));
+    const int grid = cdiv(T, 8);
+    const __nv_bfloat16* eb = static_cast<const __nv_bfloat16*>(eout);
+    const __nv_bfloat16* sb = static_cast<const __nv_bfloat16*>(shared_out);
+    __nv_bfloat16* yb = static_cast<__nv_bfloat16*>(y);
+    const float* ef = static_cast<const float*>(eout);
+    const float* sf = static_cast<const float*>(shared_out);
+    float* yf = static_cast<float*>(y);
+#define MOE_COMBINE(KM)                                                                                         \
+    if (dtype == MOE_BF16) combine_kernel<__nv_bfloat16, KM><<<grid, 256, 0, s>>>(eb, dest_row, gates, sb, T, h, k, yb); \
+    else combine_kernel<float, KM><<<grid, 256, 0, s>>>(ef, dest_row, gates, sf, T, h, k, yf);
+    if (k <= 2) { MOE_COMBINE(2) }
+    else if (k <= 4) { MOE_COMBINE(4) }
+    else if (k <= 8) { MOE_COMBINE(8) }
+    else { MOE_COMBINE(16) }
+#undef MOE_COMBINE
     return check_launch("combine_kernel");
 }

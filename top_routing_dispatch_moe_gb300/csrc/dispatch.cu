@@ -21,15 +21,13 @@ namespace moe {
 
 constexpr int kChunkA = 1024;          // assignments per chunk (one thread each)
 
-__device__ __forceinline__ int tokens_per_chunk(int k) { return kChunkA / k; }
-
+// Chunk c covers tokens [c * tpc, (c + 1) * tpc), i.e. assignments [c * tpc * k, ...): tpc * k <= kChunkA.
 __global__ void __launch_bounds__(kChunkA)
-dispatch_count_kernel(const int32_t* __restrict__ ids, int T, int E, int k, int32_t* __restrict__ chunk_counts,
+dispatch_count_kernel(const int32_t* __restrict__ ids, int T, int E, int k, int tpc, int32_t* __restrict__ chunk_counts,
                       unsigned* err) {
     extern __shared__ int s_hist[];
     for (int e = threadIdx.x; e < E; e += blockDim.x) s_hist[e] = 0;
     __syncthreads();
-    const int tpc = tokens_per_chunk(k);
     const int a = threadIdx.x;
     const int t = blockIdx.x * tpc + a / k;
     if (a < tpc * k && t < T) {
@@ -136,14 +134,14 @@ dispatch_scan_kernel(int32_t* __restrict__ chunk_counts /* in: counts, out: per-
 
 // Ranks the chunk's assignments in token order and writes dest_row, drop_mask, src_token, src_slot.
 // s_wc: [32][E] shared scratch; chunk_base(e) = assignments to e in earlier chunks; off = expert offsets.
+// Returns the destination row of this thread's assignment (-1: dropped or no assignment).
 template <typename Base, typename Off>
-__device__ __forceinline__ void rank_chunk(const int32_t* __restrict__ ids, int T, int E, int k, int C, int* s_wc,
-                                           Base chunk_base, Off off, int32_t* __restrict__ dest_row,
-                                           uint8_t* __restrict__ drop_mask, int32_t* __restrict__ src_token,
-                                           int32_t* __restrict__ src_slot) {
+__device__ __forceinline__ int rank_chunk(const int32_t* __restrict__ ids, int T, int E, int k, int tpc, int C,
+                                          int* s_wc, Base chunk_base, Off off, int32_t* __restrict__ dest_row,
+                                          uint8_t* __restrict__ drop_mask, int32_t* __restrict__ src_token,
+                                          int32_t* __restrict__ src_slot) {
     for (int i = threadIdx.x; i < 32 * E; i += blockDim.x) s_wc[i] = 0;
     __syncthreads();
-    const int tpc = tokens_per_chunk(k);
     const int a = threadIdx.x, lane = a & 31, warp = a >> 5;
     const int t = blockIdx.x * tpc + a / k, j = a % k;
     const bool valid = a < tpc * k && t < T;
@@ -171,7 +169,9 @@ __device__ __forceinline__ void rank_chunk(const int32_t* __restrict__ ids, int 
         }
         dest_row[ga] = d;
         drop_mask[ga] = d < 0 ? 1 : 0;
+        return d;
     }
+    return -1;
 }
 
 __global__ void __launch_bounds__(kChunkA)
@@ -180,54 +180,130 @@ dispatch_scatter_kernel(const int32_t* __restrict__ ids, int T, int E, int k, in
                         int32_t* __restrict__ dest_row, uint8_t* __restrict__ drop_mask,
                         int32_t* __restrict__ src_token, int32_t* __restrict__ src_slot) {
     extern __shared__ int s_wc[];
-    rank_chunk(ids, T, E, k, C, s_wc, [&](int e) { return chunk_base[(size_t)blockIdx.x * E + e]; },
+    rank_chunk(ids, T, E, k, kChunkA / k, C, s_wc, [&](int e) { return chunk_base[(size_t)blockIdx.x * E + e]; },
                [&](int e) { return offsets[e]; }, dest_row, drop_mask, src_token, src_slot);
 }
 
-// Scan and scatter in one launch, for count tables of at most kFusedScanEntries entries: every block adds up
-// the count table itself (its own chunk base and the per-expert totals, in a fixed order) and derives the
-// same offsets; block 0 also publishes offsets, kept counts, the rank layout and the tile schedule.
-constexpr int kFusedScanEntries = 1 << 16;
+// Scan, scatter and payload copy in one launch, for small count tables (at most kFusedScanEntries
+// entries, chunks of tpc tokens): every block adds up the count table itself (its own chunk base and the
+// per-expert totals, in a fixed order) and derives the same offsets; block 0 also publishes offsets, kept
+// counts, the rank layout and the tile schedule. Each block then ranks its chunk, copies its tokens' rows
+// (one warp per token, x read once) and, in capacity mode, fills its share of the pad rows.
+constexpr int kFusedScanEntries = 1 << 15;
 
-// Shared-memory layout of dispatch_scan_scatter_kernel, in ints: s_wc [32 E], s_base [E], s_kept [E],
-// s_off [E + 1], s_tp [E + 1]. The kernel's pointers and the launch's allocation both come from here.
+// Shared-memory layout of dispatch_fused_kernel, in ints: s_wc [32 E], s_base [E], s_kept [E],
+// s_off [E + 1], s_tp [E + 1], s_dest [kChunkA], s_red [2 kChunkA]. The kernel's pointers and the launch's
+// allocation both come from here.
 __host__ __device__ constexpr int fused_wc(int) { return 0; }
 __host__ __device__ constexpr int fused_base(int E) { return 32 * E; }
 __host__ __device__ constexpr int fused_kept(int E) { return fused_base(E) + E; }
 __host__ __device__ constexpr int fused_off(int E) { return fused_kept(E) + E; }
 __host__ __device__ constexpr int fused_tp(int E) { return fused_off(E) + E + 1; }
-__host__ __device__ constexpr int fused_smem_ints(int E) { return fused_tp(E) + E + 1; }
+__host__ __device__ constexpr int fused_dest(int E) { return fused_tp(E) + E + 1; }
+__host__ __device__ constexpr int fused_red(int E) { return fused_dest(E) + kChunkA; }          // 2 x kChunkA
+__host__ __device__ constexpr int fused_smem_ints(int E) { return fused_red(E) + 2 * kChunkA; }
 
+// Tokens per chunk of the fused path (0: the count table would be too large; use the three-launch path).
+// At most max_chunks chunks (the launch uses one chunk per SM so that every block is resident at once; the
+// workspace is sized for the bound of 256) and at most kFusedScanEntries table entries.
+constexpr int kFusedMaxChunks = 256;
+inline int fused_tokens_per_chunk(int T, int E, int k, int max_chunks) {
+    if (T <= 0) return 0;
+    const int target = std::max(1, std::min(max_chunks, kFusedScanEntries / E));
+    const int tpc = std::max(1, cdiv(T, target));
+    return tpc * k <= kChunkA ? tpc : 0;
+}
+
+template <typename T>
 __global__ void __launch_bounds__(kChunkA)
-dispatch_scan_scatter_kernel(const int32_t* __restrict__ ids, int T, int E, int k, int C, int R,
-                             const int32_t* __restrict__ chunk_counts, int nchunks, int32_t* __restrict__ offsets,
-                             int32_t* __restrict__ kept_counts, int32_t* __restrict__ rank_counts,
-                             int32_t* __restrict__ rank_offsets, int32_t* __restrict__ sched,
-                             int32_t* __restrict__ dest_row, uint8_t* __restrict__ drop_mask,
-                             int32_t* __restrict__ src_token, int32_t* __restrict__ src_slot) {
+dispatch_fused_kernel(const T* __restrict__ x, const int32_t* __restrict__ ids, int T_, int h, int E, int k, int tpc,
+                      int C, int R, const int32_t* __restrict__ chunk_counts, int nchunks, T* __restrict__ buf,
+                      int32_t* __restrict__ offsets, int32_t* __restrict__ kept_counts,
+                      int32_t* __restrict__ rank_counts, int32_t* __restrict__ rank_offsets,
+                      int32_t* __restrict__ sched, int32_t* __restrict__ dest_row, uint8_t* __restrict__ drop_mask,
+                      int32_t* __restrict__ src_token, int32_t* __restrict__ src_slot) {
     extern __shared__ int sm[];
-    int* s_wc = sm + fused_wc(E);                // [32][E]
-    int* s_base = sm + fused_base(E);            // [E]
-    int* s_kept = sm + fused_kept(E);            // [E]
-    int* s_off = sm + fused_off(E);              // [E + 1]
-    int* s_tp = sm + fused_tp(E);                // [E + 1]
+    int* s_wc = sm + fused_wc(E);
+    int* s_base = sm + fused_base(E);
+    int* s_kept = sm + fused_kept(E);
+    int* s_off = sm + fused_off(E);
+    int* s_tp = sm + fused_tp(E);
+    int* s_dest = sm + fused_dest(E);
+    int* s_rb = sm + fused_red(E);
+    int* s_rt = s_rb + kChunkA;
     __shared__ int s_tmp[32];
-    const int e = threadIdx.x;
-    int base = 0, total = 0;
-    if (e < E) {
-#pragma unroll 4
-        for (int c = 0; c < nchunks; ++c) {
-            const int v = __ldg(chunk_counts + (size_t)c * E + e);
-            total += v;
-            base += c < (int)blockIdx.x ? v : 0;
+    {   // count table -> this chunk's base and the per-expert totals: S slices of chunks per expert in
+        // parallel, then a tree over the slices (S = largest power of two with S * E <= kChunkA)
+        int S = 1;
+        while (S * 2 * E <= kChunkA) S *= 2;
+        const int tid = threadIdx.x, sl = tid / E, ex = tid - sl * E;
+        if (sl < S) {
+            int pb = 0, pt = 0;
+            for (int c = sl; c < nchunks; c += S) {
+                const int v = __ldg(chunk_counts + (size_t)c * E + ex);
+                pt += v;
+                pb += c < (int)blockIdx.x ? v : 0;
+            }
+            s_rb[tid] = pb;
+            s_rt[tid] = pt;
         }
-        s_base[e] = base;
+        for (int st = S / 2; st > 0; st >>= 1) {
+            __syncthreads();
+            if (sl < st) { s_rb[tid] += s_rb[tid + st * E]; s_rt[tid] += s_rt[tid + st * E]; }
+        }
+        __syncthreads();
     }
+    const int e = threadIdx.x;
+    int total = 0;
+    if (e < E) { s_base[e] = s_rb[e]; total = s_rt[e]; }
     layout_from_counts(total, E, C, s_tmp, s_kept, s_off, s_tp);
     if (blockIdx.x == 0)
         publish_layout(E, R, s_kept, s_off, s_tp, offsets, kept_counts, rank_counts, rank_offsets, sched);
-    rank_chunk(ids, T, E, k, C, s_wc, [&](int ee) { return s_base[ee]; }, [&](int ee) { return s_off[ee]; },
-               dest_row, drop_mask, src_token, src_slot);
+    const int d = rank_chunk(ids, T_, E, k, tpc, C, s_wc, [&](int ee) { return s_base[ee]; },
+                             [&](int ee) { return s_off[ee]; }, dest_row, drop_mask, src_token, src_slot);
+    s_dest[threadIdx.x] = d;
+    __syncthreads();
+
+    constexpr int V = Vec16<T>::N;
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int t0 = blockIdx.x * tpc;
+    const int ntok = min(tpc, T_ - t0);
+    for (int tl = warp; tl < ntok; tl += kChunkA / 32) {
+        const T* src = x + (size_t)(t0 + tl) * h;
+        constexpr int U = 4;
+        for (int d0 = lane * V; d0 < h; d0 += U * 32 * V) {
+            Vec16<T> v[U];
+#pragma unroll
+            for (int u = 0; u < U; ++u)
+                if (d0 + u * 32 * V < h) v[u] = ld16_stream(src + d0 + u * 32 * V);
+            for (int j = 0; j < k; ++j) {
+                const int dj = s_dest[tl * k + j];
+                if (dj >= 0) {
+#pragma unroll
+                    for (int u = 0; u < U; ++u)
+                        if (d0 + u * 32 * V < h) st16(buf + (size_t)dj * h + d0 + u * 32 * V, v[u]);
+                }
+            }
+        }
+    }
+    if (C > 0) {
+        // Pad rows, numbered in expert order, go round-robin to all warps of the grid: pad row number q
+        // (q = pads of earlier experts + p) belongs to warp q mod W.
+        const long long W = (long long)gridDim.x * (kChunkA / 32), g = (long long)blockIdx.x * (kChunkA / 32) + warp;
+        long long run = 0;
+        for (int ee = 0; ee < E; ++ee) {
+            const int npad = C - s_kept[ee];
+            long long p = ((g - run) % W + W) % W;
+            for (; p < npad; p += W) {
+                const long long r = (long long)ee * C + s_kept[ee] + p;
+                if (lane == 0) { src_token[r] = -1; src_slot[r] = -1; }
+                Vec16<T> z;
+                z.v = {};
+                for (int d0 = lane * V; d0 < h; d0 += 32 * V) st16(buf + r * h + d0, z);
+            }
+            run += npad;
+        }
+    }
 }
 
 // Blocks [0, tok_blocks): one warp per token, read x[t] once and write it to each kept destination row.
@@ -285,6 +361,10 @@ __global__ void dense_sched_kernel(int rows, int32_t* sched) {
 }
 
 static int num_chunks(int T, int k) { return T <= 0 ? 0 : cdiv(T, kChunkA / k); }
+static int num_fused_chunks(int T, int E, int k) {
+    const int tpc = fused_tokens_per_chunk(T, E, k, kFusedMaxChunks);
+    return tpc ? cdiv(T, tpc) : 0;
+}
 
 }  // namespace moe
 
@@ -303,7 +383,8 @@ extern "C" size_t moe_tile_sched_bytes(int T, int E, int k, int capacity) {
 extern "C" size_t moe_dispatch_workspace_size(int T, int E, int k, int capacity) {
     (void)capacity;
     if (T < 0 || E <= 0 || k <= 0 || k > kChunkA) return 0;
-    return align_up((size_t)num_chunks(T, k) * E * sizeof(int32_t), 256);
+    const int nch = std::max(num_chunks(T, k), num_fused_chunks(T, E, k));
+    return align_up((size_t)nch * E * sizeof(int32_t), 256);
 }
 
 extern "C" int moe_dispatch(const void* x, const int32_t* topk_ids, int T, int h, int E, int k, int capacity,
@@ -332,29 +413,42 @@ extern "C" int moe_dispatch(const void* x, const int32_t* topk_ids, int T, int h
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     unsigned* err = device_error_word();
     MOE_REQUIRE(err, MOE_ERR_CUDA, "moe_dispatch: device error word unavailable");
-    const int nch = num_chunks(T, k);
     int32_t* chunk = static_cast<int32_t*>(ws);
+    const int tpc_f = fused_tokens_per_chunk(T, E, k, std::min(kFusedMaxChunks, num_sms()));
+    if (tpc_f > 0) {
+        const int nch = cdiv(T, tpc_f);
+        dispatch_count_kernel<<<nch, kChunkA, E * sizeof(int), s>>>(topk_ids, T, E, k, tpc_f, chunk, err);
+        if (int rc = check_launch("dispatch_count_kernel")) return rc;
+        const size_t smem = (size_t)fused_smem_ints(E) * sizeof(int);
+        if (dtype == MOE_BF16) {
+            cudaFuncSetAttribute(dispatch_fused_kernel<__nv_bfloat16>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 (int)smem);
+            dispatch_fused_kernel<__nv_bfloat16><<<nch, kChunkA, smem, s>>>(static_cast<const __nv_bfloat16*>(x),
+                topk_ids, T, h, E, k, tpc_f, capacity, num_ranks, chunk, nch, static_cast<__nv_bfloat16*>(buf),
+                offsets, kept_counts, rank_counts, rank_offsets, tile_sched, dest_row, drop_mask, src_token, src_slot);
+        } else {
+            cudaFuncSetAttribute(dispatch_fused_kernel<float>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+            dispatch_fused_kernel<float><<<nch, kChunkA, smem, s>>>(static_cast<const float*>(x), topk_ids, T, h, E, k,
+                tpc_f, capacity, num_ranks, chunk, nch, static_cast<float*>(buf), offsets, kept_counts, rank_counts,
+                rank_offsets, tile_sched, dest_row, drop_mask, src_token, src_slot);
+        }
+        return check_launch("dispatch_fused_kernel");
+    }
+    // large count tables (or no tokens): count, scan, scatter, then copy and pad fill
+    const int nch = num_chunks(T, k);
     if (nch > 0) {
-        dispatch_count_kernel<<<nch, kChunkA, E * sizeof(int), s>>>(topk_ids, T, E, k, chunk, err);
+        dispatch_count_kernel<<<nch, kChunkA, E * sizeof(int), s>>>(topk_ids, T, E, k, kChunkA / k, chunk, err);
         if (int rc = check_launch("dispatch_count_kernel")) return rc;
     }
-    if (nch > 0 && (long long)nch * E <= kFusedScanEntries) {
-        const size_t smem = (size_t)fused_smem_ints(E) * sizeof(int);
-        cudaFuncSetAttribute(dispatch_scan_scatter_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-        dispatch_scan_scatter_kernel<<<nch, kChunkA, smem, s>>>(topk_ids, T, E, k, capacity, num_ranks, chunk, nch,
-            offsets, kept_counts, rank_counts, rank_offsets, tile_sched, dest_row, drop_mask, src_token, src_slot);
-        if (int rc = check_launch("dispatch_scan_scatter_kernel")) return rc;
-    } else {
-        dispatch_scan_kernel<<<1, 1024, 0, s>>>(chunk, nch, E, capacity, num_ranks, offsets, kept_counts, rank_counts,
-                                               rank_offsets, tile_sched);
-        if (int rc = check_launch("dispatch_scan_kernel")) return rc;
-        if (nch > 0) {
-            const size_t smem = (size_t)32 * E * sizeof(int);
-            cudaFuncSetAttribute(dispatch_scatter_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-            dispatch_scatter_kernel<<<nch, kChunkA, smem, s>>>(topk_ids, T, E, k, capacity, chunk, offsets, dest_row,
-                                                              drop_mask, src_token, src_slot);
-            if (int rc = check_launch("dispatch_scatter_kernel")) return rc;
-        }
+    dispatch_scan_kernel<<<1, 1024, 0, s>>>(chunk, nch, E, capacity, num_ranks, offsets, kept_counts, rank_counts,
+                                           rank_offsets, tile_sched);
+    if (int rc = check_launch("dispatch_scan_kernel")) return rc;
+    if (nch > 0) {
+        const size_t smem = (size_t)32 * E * sizeof(int);
+        cudaFuncSetAttribute(dispatch_scatter_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        dispatch_scatter_kernel<<<nch, kChunkA, smem, s>>>(topk_ids, T, E, k, capacity, chunk, offsets, dest_row,
+                                                          drop_mask, src_token, src_slot);
+        if (int rc = check_launch("dispatch_scatter_kernel")) return rc;
     }
     const int tok_blocks = cdiv(T, 8);
     const int pad_blocks = (capacity > 0 && rows > 0) ? std::min(cdiv(rows, 8), 2 * num_sms()) : 0;

@@ -143,6 +143,25 @@ __device__ __forceinline__ void unpack16(const Vec16<__nv_bfloat16>& v, float (&
     }
 }
 
+// Packed fp32 pairs: element 2i in the low word, 2i + 1 in the high word.
+__device__ __forceinline__ unsigned long long fma2(unsigned long long a, unsigned long long b, unsigned long long c) {
+    asm("fma.rn.f32x2 %0, %1, %2, %0;" : "+l"(c) : "l"(a), "l"(b));
+    return c;
+}
+__device__ __forceinline__ float pair_sum(unsigned long long p) {
+    return __uint_as_float((uint32_t)p) + __uint_as_float((uint32_t)(p >> 32));
+}
+__device__ __forceinline__ void unpack_pairs(const Vec16<float>& v, unsigned long long (&p)[2]) {
+    p[0] = ((unsigned long long)__float_as_uint(v.v.y) << 32) | __float_as_uint(v.v.x);
+    p[1] = ((unsigned long long)__float_as_uint(v.v.w) << 32) | __float_as_uint(v.v.z);
+}
+__device__ __forceinline__ void unpack_pairs(const Vec16<__nv_bfloat16>& v, unsigned long long (&p)[4]) {
+    const uint32_t w[4] = {v.v.x, v.v.y, v.v.z, v.v.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+        p[i] = ((unsigned long long)(w[i] & 0xffff0000u) << 32) | (unsigned long long)(w[i] << 16);
+}
+
 // ---------------------------------------------------------------------------------------------------
 // E <= 32: fused logits + gating, W_r^T in shared memory (copied from the per-call transposed weight)
 // ---------------------------------------------------------------------------------------------------
@@ -167,50 +186,61 @@ router_small_kernel(const T* __restrict__ x, const T* __restrict__ w_rT, const f
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     float Pacc[1] = {0.f};
     const bool use_bias_in_logits = bias && gating != MOE_GATING_SIGMOID_BIAS_RENORM;
-    for (int t = blockIdx.x * kRouterWarps + warp; t < T_; t += gridDim.x * kRouterWarps) {
-        float acc[EMAX];
+    const int nwarps = gridDim.x * kRouterWarps;
+    // Two tokens per warp: every unpacked weight pair feeds both; accumulation in packed fp32 pairs
+    // (even / odd element partial sums, added at the end).
+    for (int t0 = 2 * (blockIdx.x * kRouterWarps + warp); t0 < T_; t0 += 2 * nwarps) {
+        const bool has1 = t0 + 1 < T_;
+        unsigned long long acc0[EMAX], acc1[EMAX];
 #pragma unroll
-        for (int e = 0; e < EMAX; ++e) acc[e] = 0.f;
-        const T* xr = x + (size_t)t * h;
-        constexpr int U = 8;                      // 16-byte loads in flight per lane
+        for (int e = 0; e < EMAX; ++e) { acc0[e] = 0ull; acc1[e] = 0ull; }
+        const T* x0 = x + (size_t)t0 * h;
+        const T* x1 = x + (size_t)(has1 ? t0 + 1 : t0) * h;
+        constexpr int U = 2;                      // 16-byte loads in flight per token and lane
         for (int d0 = lane * V; d0 < h; d0 += U * 32 * V) {
-            Vec16<T> xv[U];
+            Vec16<T> va[U], vb[U];
 #pragma unroll
-            for (int u = 0; u < U; ++u)
-                if (d0 + u * 32 * V < h) xv[u] = ld16_stream(xr + d0 + u * 32 * V);
+            for (int u = 0; u < U; ++u) {
+                const int d = d0 + u * 32 * V;
+                if (d < h) { va[u] = ld16_stream(x0 + d); vb[u] = ld16_stream(x1 + d); }
+            }
 #pragma unroll
             for (int u = 0; u < U; ++u) {
                 const int d = d0 + u * 32 * V;
                 if (d < h) {
-                    float xf[V];
-                    unpack16(xv[u], xf);              // once per element, not once per expert
+                    unsigned long long xa[V / 2], xb[V / 2];
+                    unpack_pairs(va[u], xa);
+                    unpack_pairs(vb[u], xb);
 #pragma unroll
                     for (int e = 0; e < EMAX; ++e) {
                         if (e < E) {
-                            float wf[V];
-                            unpack16(*reinterpret_cast<const Vec16<T>*>(wT + (size_t)e * h + d), wf);
-                            float s = acc[e];
+                            unsigned long long wp[V / 2];
+                            unpack_pairs(*reinterpret_cast<const Vec16<T>*>(wT + (size_t)e * h + d), wp);
 #pragma unroll
-                            for (int i = 0; i < V; ++i) s = fmaf(xf[i], wf[i], s);
-                            acc[e] = s;
+                            for (int i = 0; i < V / 2; ++i) {
+                                acc0[e] = fma2(xa[i], wp[i], acc0[e]);
+                                acc1[e] = fma2(xb[i], wp[i], acc1[e]);
+                            }
                         }
                     }
                 }
             }
         }
-        float L[1] = {-INFINITY};
+        float L0[1] = {-INFINITY}, L1[1] = {-INFINITY};
 #pragma unroll
         for (int e = 0; e < EMAX; ++e) {
             if (e < E) {
-                float s = warp_sum(acc[e]);
-                if (lane == e) L[0] = s;
+                const float a = warp_sum(pair_sum(acc0[e])), b = warp_sum(pair_sum(acc1[e]));
+                if (lane == e) { L0[0] = a; L1[0] = b; }
             }
         }
-        if (lane < E) {
-            if (use_bias_in_logits) L[0] += bias[lane];
-            if (o.logits) o.logits[(size_t)t * E + lane] = L[0];
+        if (lane < E && use_bias_in_logits) { L0[0] += bias[lane]; L1[0] += bias[lane]; }
+        if (lane < E && o.logits) {
+            o.logits[(size_t)t0 * E + lane] = L0[0];
+            if (has1) o.logits[(size_t)(t0 + 1) * E + lane] = L1[0];
         }
-        gate_token<1>(L, t, E, k, gating, bias, o, Pacc, s_hist);
+        gate_token<1>(L0, t0, E, k, gating, bias, o, Pacc, s_hist);
+        if (has1) gate_token<1>(L1, t0 + 1, E, k, gating, bias, o, Pacc, s_hist);
     }
     __syncthreads();
     flush_partials<1>(Pacc, E, s_P, s_hist, o);
@@ -360,9 +390,9 @@ router_transpose_kernel(const T* __restrict__ w, int h, int E, T* __restrict__ w
 // ---------------------------------------------------------------------------------------------------
 // Upper bound of the blocks of any router launch (sizes the partial-sum workspace).
 static int router_grid(int T) { return std::max(1, std::min(cdiv(T, kRouterWarps), kRouterMaxBlocks)); }
-// The fused small-E kernel copies the transposed router weight into every block; its register budget allows
-// two blocks per SM.
-static int router_small_grid(int T) { return std::max(1, std::min(router_grid(T), 2 * num_sms())); }
+// The fused small-E kernel copies the transposed router weight into every block, takes two tokens per
+// warp, and its register budget allows two blocks per SM.
+static int router_small_grid(int T) { return std::max(1, std::min(cdiv(T, 2 * kRouterWarps), 2 * num_sms())); }
 
 static size_t small_smem_bytes(int h, int E, int el) {
     return align_up((size_t)E * h * el, 16) + (size_t)kRouterWarps * E * sizeof(float) + (size_t)E * sizeof(int);
