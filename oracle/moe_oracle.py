@@ -291,3 +291,52 @@ def dispatch_bytes(T: int, kept: int, h: int, el: int) -> int:
     """Bytes the dispatch must move: read T token rows, write one row per kept assignment ([L7] "EP":
     64 MiB for one dispatch at T=4096, k=2, h=4096 in bf16 counts the written rows)."""
     return (T + kept) * h * el
+
+
+# ---------------------------------------------------------------------------------------------------------
+# expert-choice routing ([B10.5] 10.5.6 "负载均衡问题", the expert-choice bullet: the routing direction is
+# reversed, each expert takes the fixed number of highest-scoring tokens among all tokens)
+# ---------------------------------------------------------------------------------------------------------
+
+def expert_choice(L: np.ndarray, C: int) -> dict:
+    """Each expert e selects the C tokens with the highest router probability p[t, e] (the full softmax over
+    experts of token t's logits: the token-choice router's probability, reading).
+
+    Readings (the page gives one sentence): equal scores -> lower token index first; the selected tokens of
+    expert e occupy rows e*C .. e*C + C - 1 in ascending token order; the gate of a selected pair is p[t, e];
+    a token no expert selects contributes nothing (y = 0 for it, the residual being outside the layer).
+    Returns tokens [E, C], gates [E, C], slot [T, E] (j or -1) and gaps [E] (score gap between the C-th
+    and the (C+1)-th selected candidate, for the near-tie policy)."""
+    T, E = L.shape
+    assert 1 <= C <= T
+    p = softmax(L)
+    tokens = np.empty((E, C), np.int64)
+    gates = np.empty((E, C), np.float64)
+    slot = np.full((T, E), -1, np.int64)
+    gaps = np.full(E, np.inf)
+    for e in range(E):
+        order = np.argsort(-p[:, e], kind="stable")      # descending score, ties -> lower token index
+        chosen = np.sort(order[:C])
+        tokens[e] = chosen
+        gates[e] = p[chosen, e]
+        slot[chosen, e] = np.arange(C)
+        if C < T:
+            gaps[e] = p[order[C - 1], e] - p[order[C], e]
+    return dict(prob=p, tokens=tokens, gates=gates, slot=slot, gaps=gaps)
+
+
+def expert_choice_layer(x, w_r, weights, C: int, shared=None) -> dict:
+    """Expert-choice layer forward: logits, selection, buf[e*C + j] = x[tokens[e, j]], expert FFN,
+    y[t] = sum over the experts e that selected t (ascending e) of gate * FFN_e(x[t]) (+ shared FFN)."""
+    x = np.asarray(x, np.float64)
+    L = router_logits(x, w_r, None, SOFTMAX)
+    ec = expert_choice(L, C)
+    E = L.shape[1]
+    buf = x[ec["tokens"].reshape(-1)]
+    eout = np.empty_like(buf)
+    for e in range(E):
+        eout[e * C:(e + 1) * C] = swiglu_ffn(buf[e * C:(e + 1) * C], *weights(e))
+    y = np.zeros_like(x) if shared is None else swiglu_ffn(x, *shared())
+    for e in range(E):
+        y[ec["tokens"][e]] += ec["gates"][e][:, None] * eout[e * C:(e + 1) * C]
+    return dict(logits=L, ec=ec, buf=buf, eout=eout, y=y)

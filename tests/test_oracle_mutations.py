@@ -9,6 +9,7 @@ from oracle import moe_oracle as O
 from tests import test_oracle_pins as P
 
 _route, _dispatch, _swiglu, _combine, _capacity = O.route, O.dispatch, O.swiglu_ffn, O.combine, O.capacity
+_ec = O.expert_choice
 
 
 def mut_renormalise_softmax(L, k, gating, bias=None, alpha=0.01):
@@ -76,11 +77,32 @@ def mut_capacity_floor_over_E(cf, k, T, E):
     return 0 if cf <= 0 else int(cf * T / E)      # forgot the k
 
 
+def mut_ec_select_on_logits(L, C):
+    """Selects each expert's tokens on the raw logits instead of the per-token softmax probability."""
+    out = _ec(L, C)
+    E = L.shape[1]
+    for e in range(E):
+        chosen = np.sort(np.argsort(-L[:, e], kind="stable")[:C])
+        out["tokens"][e] = chosen
+        out["gates"][e] = out["prob"][chosen, e]
+    return out
+
+
+def mut_ec_ties_higher_token(L, C):
+    out = _ec(L[::-1].copy(), C)
+    T = L.shape[0]
+    out["tokens"] = np.sort(T - 1 - out["tokens"], axis=1)
+    out["prob"] = out["prob"][::-1]
+    out["gates"] = np.take_along_axis(out["prob"].T, out["tokens"], axis=1)
+    return out
+
+
 MUTANTS = [
     ("route", mut_renormalise_softmax), ("route", mut_ascending_order), ("route", mut_bias_in_sigmoid_gates),
     ("route", mut_aux_denominator_T), ("dispatch", mut_drop_latest_first), ("dispatch", mut_dispatch_unstable),
     ("swiglu_ffn", mut_swap_gate_up), ("swiglu_ffn", mut_transpose_down), ("combine", mut_combine_no_gate),
-    ("capacity", mut_capacity_floor_over_E),
+    ("capacity", mut_capacity_floor_over_E), ("expert_choice", mut_ec_select_on_logits),
+    ("expert_choice", mut_ec_ties_higher_token),
 ]
 
 PINS = [
@@ -90,7 +112,8 @@ PINS = [
     P.test_dispatch_stable_and_bijective, P.test_single_expert_reduces_to_dense_swiglu, P.test_swiglu_closed_forms,
     lambda: P.test_topk_brute_force(8, 2), lambda: P.test_dispatch_brute_force(64, 8, 2, 10, 4),
     lambda: P.test_identity_experts(O.SOFTMAX, 0), lambda: P.test_identity_experts(O.SOFTMAX_RENORM, 0),
-    P.test_token_sampled_layer_matches_full_layer,
+    P.test_token_sampled_layer_matches_full_layer, lambda: P.test_expert_choice_brute_force(9, 4, 4),
+    P.test_expert_choice_ties_take_lower_token, P.test_expert_choice_full_capacity_is_dense,
 ]
 
 

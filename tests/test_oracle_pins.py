@@ -379,3 +379,69 @@ def test_zipf_bias_gives_zipf_load():
     p = 1.0 / np.arange(1, 9)
     p /= p.sum()
     assert np.max(np.abs(r["counts"] / (cfg.k * cfg.T) / p - 1)) < 0.02
+
+
+# -------------------------------------------------------------------------------------- expert choice
+
+def _brute_expert_choice(col, C):
+    """Max-sum C-subset of tokens; among equal sums the lexicographically smallest index set."""
+    best, best_set = None, None
+    for sub in itertools.combinations(range(len(col)), C):
+        s = sum(col[i] for i in sub)
+        if best is None or s > best:
+            best, best_set = s, sub
+    return list(best_set)
+
+
+@pytest.mark.parametrize("T,E,C", [(7, 3, 2), (9, 4, 4), (8, 2, 8), (6, 5, 1)])
+def test_expert_choice_brute_force(T, E, C):
+    rng = np.random.default_rng(T * 100 + E * 10 + C)
+    L = rng.standard_normal((T, E))
+    ec = O.expert_choice(L, C)
+    p = O.softmax(L)
+    for e in range(E):
+        assert ec["tokens"][e].tolist() == _brute_expert_choice(list(p[:, e]), C)
+        assert np.allclose(ec["gates"][e], p[ec["tokens"][e], e], rtol=1e-15)
+    assert (ec["slot"] >= 0).sum() == E * C                 # every expert takes exactly C tokens
+    for t in range(T):
+        for e in range(E):
+            j = ec["slot"][t, e]
+            assert (j < 0) == (t not in ec["tokens"][e]) and (j < 0 or ec["tokens"][e][j] == t)
+
+
+def test_expert_choice_ties_take_lower_token():
+    L = np.zeros((6, 2))                                   # all scores equal
+    ec = O.expert_choice(L, 3)
+    assert ec["tokens"].tolist() == [[0, 1, 2], [0, 1, 2]]
+    assert np.allclose(ec["gates"], 0.5)
+
+
+def test_expert_choice_full_capacity_is_dense():
+    """C = T: every expert takes every token, the gates of a token sum to 1, and with identical experts the
+    layer is one dense SwiGLU FFN."""
+    rng = np.random.default_rng(12)
+    T, h, E, F = 10, 6, 3, 8
+    x = rng.standard_normal((T, h))
+    wr = rng.standard_normal((h, E))
+    W = tuple(rng.standard_normal(s) for s in [(F, h), (F, h), (h, F)])
+    out = O.expert_choice_layer(x, wr, lambda e: W, C=T)
+    assert np.allclose(out["ec"]["gates"].sum(axis=0), 1.0)
+    ref = np.array([_scalar_swiglu(list(x[t]), *[w.tolist() for w in W]) for t in range(T)])
+    assert np.allclose(out["y"], ref, rtol=1e-12, atol=1e-12)
+
+
+def test_expert_choice_layer_against_scalar_loops():
+    rng = np.random.default_rng(13)
+    T, h, E, F, C = 12, 5, 3, 7, 4
+    x = rng.standard_normal((T, h))
+    wr = rng.standard_normal((h, E))
+    W = [tuple(rng.standard_normal(s) for s in [(F, h), (F, h), (h, F)]) for _ in range(E)]
+    out = O.expert_choice_layer(x, wr, lambda e: W[e], C=C)
+    p = O.softmax(x @ wr)
+    for t in range(T):
+        want = np.zeros(h)
+        for e in range(E):
+            col = sorted(range(T), key=lambda i: (-p[i, e], i))[:C]
+            if t in col:
+                want += p[t, e] * np.array(_scalar_swiglu(list(x[t]), *[w.tolist() for w in W[e]]))
+        assert np.allclose(out["y"][t], want, rtol=1e-12, atol=1e-12)
