@@ -242,7 +242,7 @@ def run_gpu(args, cfg, C):
                      bias=torch.from_numpy(inp["bias"]).to(dev) if inp["bias"] is not None else None,
                      w_gate=up(inp["wg"]), w_up=up(inp["wu"]), w_down=up(inp["wd"]),
                      shared=tuple(up(np.ascontiguousarray(w)[None]) for w in inp["shared"])
-                     if inp["shared"] is not None else None, device=dev)
+                     if inp["shared"] is not None else None, device=dev, routing=cfg.routing)
     x = up(inp["x"])
     flush = torch.empty(512 * 2**20, dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream()
@@ -258,7 +258,10 @@ def run_gpu(args, cfg, C):
         flush.zero_()
         torch.cuda.synchronize()
     assert moe.moe_check_device_error() == moe.MOE_OK, moe.moe_last_error_string()
-    kept = int(layer.d_out["kept_counts"].sum().item())
+    if cfg.routing == "expert_choice":
+        kept = cfg.E * layer.C                        # every expert takes exactly C tokens
+    else:
+        kept = int(layer.d_out["kept_counts"].sum().item())
 
     # ---- device-resident timed region
     events: dict = {}

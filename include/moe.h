@@ -137,6 +137,29 @@ int moe_dispatch_static(const void* x, const int32_t* topk_ids, int T, int h, in
 int moe_dense_tile_sched(int rows, int32_t* tile_sched, void* stream);
 
 /* ---------------------------------------------------------------------------------------------------
+ * Expert-choice routing ("10.5 序列并行与专家并行", section 10.5.6, expert-choice bullet: the routing
+ * direction is reversed and every expert takes a fixed number C of the highest-scoring tokens among all
+ * tokens, which balances the expert load by construction).
+ *   score[t,e] = softmax over experts of logits[t,:] (the logits of moe_router); expert e takes the C tokens
+ *   with the highest score[:,e] (equal scores -> lower token index) and lays them out in rows e*C .. e*C+C-1
+ *   in ascending token order; gate = score. A token chosen by no expert gets y = 0 (plus shared_out).
+ *   moe_expert_choice_route:   logits [T,E] fp32 -> tokens [E,C] int32, gates [E,C] fp32, slot [T,E] int32
+ *                              (row of (t,e) inside expert e's block, -1 if e did not choose t).
+ *                              Workspace: moe_expert_choice_workspace_size(T, E) bytes. 1 <= C <= T, E <= 256.
+ *   moe_expert_choice_dispatch: buf [E*C,h] dtype, buf[e*C+j] = x[tokens[e][j]]; tile_sched for the expert
+ *                              FFN (moe_tile_sched_bytes(T, E, 1, C) bytes).
+ *   moe_expert_choice_combine: y[t] = shared_out[t] + sum over experts e with slot[t][e] >= 0, ascending e, of
+ *                              gates[e][slot] * eout[e*C + slot[t][e]]; fp32 accumulation, deterministic.
+ * ------------------------------------------------------------------------------------------------- */
+size_t moe_expert_choice_workspace_size(int T, int E);
+int moe_expert_choice_route(const float* logits, int T, int E, int C, int32_t* tokens, float* gates, int32_t* slot,
+                            void* ws, size_t ws_bytes, void* stream);
+int moe_expert_choice_dispatch(const void* x, const int32_t* tokens, int T, int h, int E, int C, int dtype,
+                               void* buf, int32_t* tile_sched, void* stream);
+int moe_expert_choice_combine(const void* eout, const int32_t* slot, const float* gates, const void* shared_out,
+                              int T, int h, int E, int C, int dtype, void* y, void* stream);
+
+/* ---------------------------------------------------------------------------------------------------
  * moe_pack_expert_weights: one-time repack of the SwiGLU expert weights for the grouped GEMM.
  *   "v6 长序列和 MoE ...", section "MoE" (a SwiGLU FFN has three h x F matrices).
  *   w_gate [E,F,h], w_up [E,F,h], w_down [E,h,F] (nn.Linear layout, dtype) -> packed

@@ -46,6 +46,7 @@ class MoEConfig:
     dtype: str        # "f32" or "bf16"
     alpha: float      # Switch aux-loss coefficient
     bias: str         # "none" | "zipf" (added to logits) | "normal" (selection only, std 0.1)
+    routing: str = "token"   # "token": each token picks k experts; "expert_choice": each expert picks C tokens
 
     @property
     def el(self) -> int:
@@ -70,6 +71,10 @@ CONFIGS = {
     # Qwen3-MoE-shaped, uniform routing, Switch aux with alpha = 0.01, 8 virtual EP ranks
     "qwen3_moe": MoEConfig("qwen3_moe", T=16384, h=2048, E=128, k=8, F=768, gating=GATING_SOFTMAX,
                            cf=0.0, R=8, n_shared=0, dtype="bf16", alpha=0.01, bias="none"),
+    # page-3 shape with expert-choice routing: each of the 8 experts takes C = cf * k * T / E = 1024 tokens
+    "page3_expert_choice": MoEConfig("page3_expert_choice", T=4096, h=4096, E=8, k=2, F=12288,
+                                     gating=GATING_SOFTMAX, cf=1.0, R=8, n_shared=0, dtype="bf16", alpha=0.01,
+                                     bias="none", routing="expert_choice"),
     # profiling stand-in for the page-3 shape: identical GEMM tiles (K=4096, 128x256 tiles, same routing and
     # capacity) with F=1536, so that a full ncu capture of the grouped GEMM holds well under 1 GB on the device
     "page3_profile": MoEConfig("page3_profile", T=4096, h=4096, E=8, k=2, F=1536, gating=GATING_SOFTMAX, cf=1.25,

@@ -109,5 +109,32 @@ def build_gpu_layer(cfg, inp, wg, wu, wd, shared=None, device="cuda"):
         sh = tuple(to_device(np.ascontiguousarray(w)[None], cfg, dev) for w in shared)   # one expert: [1, ...]
     layer = MoELayer(T=cfg.T, h=cfg.h, E=cfg.E, k=cfg.k, F=cfg.F, gating=cfg.gating, cf=cfg.cf, R=cfg.R,
                      alpha=cfg.alpha, w_r=to_device(inp["w_r"], cfg, dev), bias=b, w_gate=to_device(wg, cfg, dev),
-                     w_up=to_device(wu, cfg, dev), w_down=to_device(wd, cfg, dev), shared=sh, device=dev)
+                     w_up=to_device(wu, cfg, dev), w_down=to_device(wd, cfg, dev), shared=sh, device=dev,
+                     routing=cfg.routing)
     return layer
+
+
+def ec_inputs(cfg, seed=0):
+    """Inputs of an expert-choice workload. For every expert whose C-th and (C+1)-th best scores differ by
+    less than 1e-5 (the oracle's float64 scores), the two boundary tokens are redrawn from their own
+    substreams, until no expert's choice is that close."""
+    w_r, _ = moe_inputs.make_router(cfg, seed)
+    w64 = moe_inputs.to_f64(w_r, cfg.dtype)
+    C = O.capacity(cfg.cf, cfg.k, cfg.T, cfg.E)
+    redraw: dict[int, int] = {}
+    x = moe_inputs.make_x(cfg, seed)
+    for _ in range(8):
+        L = O.router_logits(moe_inputs.to_f64(x, cfg.dtype), w64, None, O.SOFTMAX)
+        ec = O.expert_choice(L, C)
+        close = np.nonzero(ec["gaps"] < REDRAW_GAP)[0]
+        if close.size == 0:
+            break
+        for e in close.tolist():
+            order = np.argsort(-ec["prob"][:, e], kind="stable")
+            for t in (int(order[C - 1]), int(order[C])):
+                redraw[t] = redraw.get(t, 0) + 1
+        x = moe_inputs.make_x(cfg, seed, redraw=redraw)
+    else:
+        raise RuntimeError("expert-choice near ties persist after 8 redraw rounds")
+    return dict(x=x, w_r=w_r, bias=None, C=C, logits=L, ec=ec, redrawn=len(redraw),
+                near_ties=int((ec["gaps"] < REPORT_GAP).sum()))

@@ -115,4 +115,29 @@ __device__ __forceinline__ void warp_argmax(float& v, int& i) {
     }
 }
 
+// Inclusive block scan of one int per thread (blockDim.x == 1024).
+__device__ __forceinline__ int block_inclusive_scan(int v, int* s_tmp) {
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        int n = __shfl_up_sync(0xffffffffu, v, o);
+        if (lane >= o) v += n;
+    }
+    if (lane == 31) s_tmp[warp] = v;
+    __syncthreads();
+    if (warp == 0) {
+        int w = s_tmp[lane];
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            int n = __shfl_up_sync(0xffffffffu, w, o);
+            if (lane >= o) w += n;
+        }
+        s_tmp[lane] = w;
+    }
+    __syncthreads();
+    if (warp > 0) v += s_tmp[warp - 1];
+    __syncthreads();
+    return v;
+}
+
 }  // namespace moe

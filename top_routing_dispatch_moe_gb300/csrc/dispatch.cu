@@ -39,31 +39,6 @@ dispatch_count_kernel(const int32_t* __restrict__ ids, int T, int E, int k, int 
     for (int e = threadIdx.x; e < E; e += blockDim.x) chunk_counts[(size_t)blockIdx.x * E + e] = s_hist[e];
 }
 
-// Inclusive block scan of one int per thread (blockDim.x == 1024).
-__device__ int block_inclusive_scan(int v, int* s_tmp) {
-    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-        int n = __shfl_up_sync(0xffffffffu, v, o);
-        if (lane >= o) v += n;
-    }
-    if (lane == 31) s_tmp[warp] = v;
-    __syncthreads();
-    if (warp == 0) {
-        int w = s_tmp[lane];
-#pragma unroll
-        for (int o = 1; o < 32; o <<= 1) {
-            int n = __shfl_up_sync(0xffffffffu, w, o);
-            if (lane >= o) w += n;
-        }
-        s_tmp[lane] = w;
-    }
-    __syncthreads();
-    if (warp > 0) v += s_tmp[warp - 1];
-    __syncthreads();
-    return v;
-}
-
 // Per-expert kept counts -> offsets, tile prefix (block scans; every thread of the 1024-thread block calls
 // it). Thread e < E passes its expert's assignment count n; s_off / s_tp / s_kept receive E + 1 / E + 1 / E
 // entries.

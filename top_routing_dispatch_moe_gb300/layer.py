@@ -30,7 +30,7 @@ class MoELayer:
     STAGES = ("router", "dispatch", "up_gate", "down", "shared_up_gate", "shared_down", "combine")
 
     def __init__(self, *, T, h, E, k, F, gating, cf, R, alpha, w_r, bias, w_gate, w_up, w_down,
-                 shared=None, device="cuda"):
+                 shared=None, device="cuda", routing="token"):
         self.T, self.h, self.E, self.k, self.F = T, h, E, k, F
         self.gating, self.R, self.alpha = gating, R, alpha
         self.C = capacity_slots(cf, k, T, E)
@@ -44,7 +44,16 @@ class MoELayer:
         self.shared_packed = moe.moe_pack_expert_weights(*shared) if shared is not None else None
         i32, f32 = torch.int32, torch.float32
         code = moe.dtype_code(dt)
-        self.rows = moe.moe_dispatch_rows(T, E, k, self.C)
+        self.routing = routing
+        if routing == "expert_choice":
+            # every expert takes C = cf * k * T / E tokens (k: the average number of experts per token)
+            self.rows = E * self.C
+            self.ec = dict(tokens=torch.empty((E, self.C), dtype=i32, device=dev),
+                           gates=torch.empty((E, self.C), dtype=f32, device=dev),
+                           slot=torch.empty((T, E), dtype=i32, device=dev))
+            self.ec_ws = moe._bytes_tensor(moe.moe_expert_choice_workspace_size(T, E), dev)
+        else:
+            self.rows = moe.moe_dispatch_rows(T, E, k, self.C)
         self.r_out = dict(logits=torch.empty((T, E), dtype=f32, device=dev),
                           topk_ids=torch.empty((T, k), dtype=i32, device=dev),
                           gates=torch.empty((T, k), dtype=f32, device=dev),
@@ -83,8 +92,15 @@ class MoELayer:
         moe.moe_router(x, self.w_r, self.bias, self.k, self.gating, self.alpha, logits=r["logits"],
                        topk_ids=r["topk_ids"], gates=r["gates"], counts=r["counts"], f=r["f"], P=r["P"], aux=r["aux"],
                        ws=self.r_ws, stream=stream)
+        if self.routing == "expert_choice":
+            moe.moe_expert_choice_route(r["logits"], self.C, tokens=self.ec["tokens"], gates=self.ec["gates"],
+                                        slot=self.ec["slot"], ws=self.ec_ws, stream=stream)
         mark("router")
-        moe.moe_dispatch(x, r["topk_ids"], self.E, self.C, self.R, out=self.d_out, ws=self.d_ws, stream=stream)
+        if self.routing == "expert_choice":
+            moe.moe_expert_choice_dispatch(x, self.ec["tokens"], buf=self.d_out["buf"],
+                                           tile_sched=self.d_out["tile_sched"], stream=stream)
+        else:
+            moe.moe_dispatch(x, r["topk_ids"], self.E, self.C, self.R, out=self.d_out, ws=self.d_ws, stream=stream)
         mark("dispatch")
         sched = self.d_out["tile_sched"]
         moe.moe_expert_up_gate(self.d_out["buf"], sched, self.packed, self.E, self.F, act=self.act, stream=stream)
@@ -99,6 +115,10 @@ class MoELayer:
                                 stream=stream)
             mark("shared_down")
             shared_out = self.sh_out
-        moe.moe_combine(self.eout, self.d_out["dest_row"], r["gates"], shared_out, y=self.y, stream=stream)
+        if self.routing == "expert_choice":
+            moe.moe_expert_choice_combine(self.eout, self.ec["slot"], self.ec["gates"], shared_out, y=self.y,
+                                          stream=stream)
+        else:
+            moe.moe_combine(self.eout, self.d_out["dest_row"], r["gates"], shared_out, y=self.y, stream=stream)
         mark("combine")
         return self.y

@@ -31,6 +31,10 @@ _SIGS = {
     "moe_dispatch": (_I, [_P, _P, _I, _I, _I, _I, _I, _I, _I, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _Z, _P]),
     "moe_dispatch_static": (_I, [_P, _P, _I, _I, _I, _I, _I, _I, _I, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P]),
     "moe_dense_tile_sched": (_I, [_I, _P, _P]),
+    "moe_expert_choice_workspace_size": (_Z, [_I, _I]),
+    "moe_expert_choice_route": (_I, [_P, _I, _I, _I, _P, _P, _P, _P, _Z, _P]),
+    "moe_expert_choice_dispatch": (_I, [_P, _P, _I, _I, _I, _I, _I, _P, _P, _P]),
+    "moe_expert_choice_combine": (_I, [_P, _P, _P, _P, _I, _I, _I, _I, _I, _P, _P]),
     "moe_packed_weights_bytes": (_Z, [_I, _I, _I, _I]),
     "moe_pack_expert_weights": (_I, [_P, _P, _P, _I, _I, _I, _I, _P, _P]),
     "moe_expert_up_gate": (_I, [_P, _P, _P, _I, _I, _I, _I, _I, _P, _P]),
@@ -192,6 +196,47 @@ def moe_dense_tile_sched(rows: int, tile_sched=None, device="cuda", stream=None)
         tile_sched = torch.empty(moe_tile_sched_bytes(rows, 1, 1, 0) // 4, dtype=torch.int32, device=device)
     _check(_lib.moe_dense_tile_sched(rows, _ptr(tile_sched), _stream(stream)))
     return tile_sched
+
+
+# ---------------------------------------------------------------------------------------- expert choice
+
+def moe_expert_choice_workspace_size(T, E) -> int:
+    return _lib.moe_expert_choice_workspace_size(T, E)
+
+
+def moe_expert_choice_route(logits, C: int, *, tokens=None, gates=None, slot=None, ws=None, stream=None):
+    T, E = logits.shape
+    dev = logits.device
+    tokens = torch.empty((E, C), dtype=torch.int32, device=dev) if tokens is None else tokens
+    gates = torch.empty((E, C), dtype=torch.float32, device=dev) if gates is None else gates
+    slot = torch.empty((T, E), dtype=torch.int32, device=dev) if slot is None else slot
+    ws = _bytes_tensor(moe_expert_choice_workspace_size(T, E), dev) if ws is None else ws
+    _check(_lib.moe_expert_choice_route(_ptr(logits), T, E, C, _ptr(tokens), _ptr(gates), _ptr(slot), _ptr(ws),
+                                        ws.numel(), _stream(stream)))
+    return dict(tokens=tokens, gates=gates, slot=slot)
+
+
+def moe_expert_choice_dispatch(x, tokens, *, buf=None, tile_sched=None, stream=None):
+    T, h = x.shape
+    E, C = tokens.shape
+    if buf is None:
+        buf = torch.empty((E * C, h), dtype=x.dtype, device=x.device)
+    if tile_sched is None:
+        tile_sched = torch.empty(moe_tile_sched_bytes(T, E, 1, C) // 4, dtype=torch.int32, device=x.device)
+    _check(_lib.moe_expert_choice_dispatch(_ptr(x), _ptr(tokens), T, h, E, C, dtype_code(x.dtype), _ptr(buf),
+                                           _ptr(tile_sched), _stream(stream)))
+    return dict(buf=buf, tile_sched=tile_sched)
+
+
+def moe_expert_choice_combine(eout, slot, gates, shared_out=None, y=None, stream=None):
+    T, E = slot.shape
+    C = gates.shape[1]
+    h = eout.shape[1]
+    if y is None:
+        y = torch.empty((T, h), dtype=eout.dtype, device=eout.device)
+    _check(_lib.moe_expert_choice_combine(_ptr(eout), _ptr(slot), _ptr(gates), _ptr(shared_out), T, h, E, C,
+                                          dtype_code(eout.dtype), _ptr(y), _stream(stream)))
+    return y
 
 
 # ------------------------------------------------------------------------------------------------ experts
