@@ -216,6 +216,17 @@ def run_reference(args, cfg, C):
 # GPU arm
 # ---------------------------------------------------------------------------------------------------------
 
+def max_over_ranks(v: float, world: int, device) -> float:
+    """The slowest rank's value (the whole job ends when its slowest replica does)."""
+    if world <= 1:
+        return v
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([v], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
 def run_gpu(args, cfg, C):
     import torch
     import torch.distributed as dist
@@ -292,11 +303,7 @@ def run_gpu(args, cfg, C):
         for a, b in zip(order[:-1], order[1:]):
             stage_ms[b].append(events[a][i].elapsed_time(events[b][i]))
         step_ms.append(events["start"][i].elapsed_time(events[order[-1]][i]))
-    ms = float(np.mean(step_ms))
-    if world > 1:
-        t = torch.tensor([ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms = float(t.item())
+    ms = max_over_ranks(float(np.mean(step_ms)), world, dev)
     value = world * cfg.T / (ms * 1e-3)
 
     # ---- end-to-end through the public API: pinned host x -> device, forward, y -> pinned host
@@ -317,11 +324,7 @@ def run_gpu(args, cfg, C):
         e1.synchronize()
         if i >= args.warmup:
             e2e_ms.append(e0.elapsed_time(e1))
-    e2e = float(np.mean(e2e_ms))
-    if world > 1:
-        t = torch.tensor([e2e], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        e2e = float(t.item())
+    e2e = max_over_ranks(float(np.mean(e2e_ms)), world, dev)
     io_bytes = cfg.T * cfg.h * cfg.el
 
     # ---- roofline of the dominant kernel (the up/gate grouped GEMM) and the bandwidth stages

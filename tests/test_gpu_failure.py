@@ -1,0 +1,42 @@
+"""Failure detection on the GPU without a fault: the tensor-core GEMM's mbarrier waits are bounded. With the
+limit forced down to one poll the kernel gives up, latches MOE_ERR_TIMEOUT in the library's device error word,
+drains its copies and MMAs, frees its tensor memory and returns; the context stays usable and the next call,
+at the default limit, is correct."""
+import pytest
+
+pytestmark = pytest.mark.gpu
+
+
+def _problem():
+    import torch
+    from top_routing_dispatch_moe_gb300 import moe
+    torch.manual_seed(3)
+    rows, h, F = 512, 256, 256
+    x = torch.randn(rows, h, device="cuda").to(torch.bfloat16)
+    wg = (torch.randn(1, F, h, device="cuda") / h ** 0.5).to(torch.bfloat16)
+    wu = (torch.randn(1, F, h, device="cuda") / h ** 0.5).to(torch.bfloat16)
+    wd = (torch.randn(1, h, F, device="cuda") / F ** 0.5).to(torch.bfloat16)
+    return x, wg, wu, moe.moe_pack_expert_weights(wg, wu, wd), moe.moe_dense_tile_sched(rows), F
+
+
+def test_gemm_wait_timeout_reported_and_recoverable():
+    import torch
+    from top_routing_dispatch_moe_gb300 import moe
+    x, wg, wu, packed, sched, F = _problem()
+    torch.cuda.synchronize()
+    assert moe.moe_check_device_error() == moe.MOE_OK
+    try:
+        moe.moe_set_wait_limit(1)
+        moe.moe_expert_up_gate(x, sched, packed, 1, F)
+        rc = moe.moe_check_device_error()
+        msg = moe.moe_last_error_string()
+    finally:
+        moe.moe_set_wait_limit(0)
+    assert rc == moe.MOE_ERR_TIMEOUT, (rc, msg)
+    assert "wait ran out" in msg
+    act = moe.moe_expert_up_gate(x, sched, packed, 1, F)
+    torch.cuda.synchronize()
+    assert moe.moe_check_device_error() == moe.MOE_OK
+    g = x.float() @ wg[0].float().T
+    ref = g * torch.sigmoid(g) * (x.float() @ wu[0].float().T)
+    assert ((act.float() - ref).norm() / ref.norm()).item() < 1e-2

@@ -189,39 +189,98 @@ ec_combine_kernel(const T* __restrict__ eout, const int32_t* __restrict__ slot, 
         gl[g] = jl[g] >= 0 ? gates[(size_t)e_l * C + jl[g]] : 0.f;
         ml[g] = __ballot_sync(0xffffffffu, jl[g] >= 0);
     }
-    for (int d0b = 0; d0b < h; d0b += 32 * V) {     // warp-uniform trip count: shuffles below use all lanes
-        const int d0 = d0b + lane * V;
-        const bool in = d0 < h;
-        float acc[V];
-        if (shared_out && in) {
-            Vec16<T> sv = ld16_stream(shared_out + (size_t)t * h + d0);
+    // (row, gate) of the first kSel experts that chose t, ascending expert order, held by every lane
+    constexpr int kSel = 16;
+    int srow[kSel];
+    float sg[kSel];
+    int nsel = 0;
 #pragma unroll
-            for (int i = 0; i < V; ++i) acc[i] = sv.get(i);
-        } else {
+    for (int g = 0; g < G; ++g) {
+        unsigned m = ml[g];
+        while (m) {
+            const int src = __ffs(m) - 1;
+            m &= m - 1;
+            const int jj = __shfl_sync(0xffffffffu, jl[g], src);
+            const float gg = __shfl_sync(0xffffffffu, gl[g], src);
+            if (nsel < kSel) {
 #pragma unroll
-            for (int i = 0; i < V; ++i) acc[i] = 0.f;
+                for (int q = 0; q < kSel; ++q)
+                    if (q == nsel) { srow[q] = (32 * g + src) * C + jj; sg[q] = gg; }
+            }
+            ++nsel;
         }
+    }
+    constexpr int U = 2;                            // column chunks per pass
+    for (int d0b = 0; d0b < h; d0b += U * 32 * V) {  // warp-uniform trip count: shuffles below use all lanes
+        float acc[U][V];
 #pragma unroll
-        for (int g = 0; g < G; ++g) {
-            unsigned m = ml[g];
-            while (m) {
-                const int src = __ffs(m) - 1;
-                m &= m - 1;
-                const int ee = 32 * g + src;
-                const int jj = __shfl_sync(0xffffffffu, jl[g], src);
-                const float gg = __shfl_sync(0xffffffffu, gl[g], src);
-                if (in) {
-                    Vec16<T> v = ld16_stream(eout + ((size_t)ee * C + jj) * h + d0);
+        for (int u = 0; u < U; ++u) {
+            const int d0 = d0b + u * 32 * V + lane * V;
+            if (shared_out && d0 < h) {
+                Vec16<T> sv = ld16_stream(shared_out + (size_t)t * h + d0);
 #pragma unroll
-                    for (int i = 0; i < V; ++i) acc[i] = fmaf(gg, v.get(i), acc[i]);
+                for (int i = 0; i < V; ++i) acc[u][i] = sv.get(i);
+            } else {
+#pragma unroll
+                for (int i = 0; i < V; ++i) acc[u][i] = 0.f;
+            }
+        }
+        // up to kSel rows from registers, four rows x U chunks in flight, in ascending expert order
+#pragma unroll
+        for (int q0 = 0; q0 < kSel; q0 += 4) {
+            if (q0 >= nsel) break;
+            Vec16<T> v[4][U];
+#pragma unroll
+            for (int qq = 0; qq < 4; ++qq)
+#pragma unroll
+                for (int u = 0; u < U; ++u) {
+                    const int d0 = d0b + u * 32 * V + lane * V;
+                    if (d0 < h && q0 + qq < nsel) v[qq][u] = ld16_stream(eout + (size_t)srow[q0 + qq] * h + d0);
+                }
+#pragma unroll
+            for (int qq = 0; qq < 4; ++qq)
+#pragma unroll
+                for (int u = 0; u < U; ++u) {
+                    const int d0 = d0b + u * 32 * V + lane * V;
+                    if (d0 < h && q0 + qq < nsel) {
+#pragma unroll
+                        for (int i = 0; i < V; ++i) acc[u][i] = fmaf(sg[q0 + qq], v[qq][u].get(i), acc[u][i]);
+                    }
+                }
+        }
+        if (nsel > kSel) {                          // rare: more than kSel experts chose t; the rest in order
+            int seen = 0;
+#pragma unroll
+            for (int g = 0; g < G; ++g) {
+                unsigned m = ml[g];
+                while (m) {
+                    const int src = __ffs(m) - 1;
+                    m &= m - 1;
+                    const int jj = __shfl_sync(0xffffffffu, jl[g], src);
+                    const float gg = __shfl_sync(0xffffffffu, gl[g], src);
+                    if (seen++ >= kSel) {
+#pragma unroll
+                        for (int u = 0; u < U; ++u) {
+                            const int d0 = d0b + u * 32 * V + lane * V;
+                            if (d0 < h) {
+                                Vec16<T> v = ld16_stream(eout + ((size_t)(32 * g + src) * C + jj) * h + d0);
+#pragma unroll
+                                for (int i = 0; i < V; ++i) acc[u][i] = fmaf(gg, v.get(i), acc[u][i]);
+                            }
+                        }
+                    }
                 }
             }
         }
-        if (in) {
-            Vec16<T> o;
 #pragma unroll
-            for (int i = 0; i < V; ++i) o.set(i, acc[i]);
-            st16(y + (size_t)t * h + d0, o);
+        for (int u = 0; u < U; ++u) {
+            const int d0 = d0b + u * 32 * V + lane * V;
+            if (d0 < h) {
+                Vec16<T> o;
+#pragma unroll
+                for (int i = 0; i < V; ++i) o.set(i, acc[u][i]);
+                st16(y + (size_t)t * h + d0, o);
+            }
         }
     }
 }
