@@ -80,7 +80,7 @@ class MoELayer:
             self.sh_out = torch.empty((T, h), dtype=dt, device=dev)
         self.y = torch.empty((T, h), dtype=dt, device=dev)
 
-    def forward(self, x, stream=None, events=None):
+    def forward(self, x, stream=None, events=None, y=None):
         def mark(stage):
             if events is not None:
                 ev = torch.cuda.Event(enable_timing=True)
@@ -115,10 +115,56 @@ class MoELayer:
                                 stream=stream)
             mark("shared_down")
             shared_out = self.sh_out
+        out = self.y if y is None else y
         if self.routing == "expert_choice":
-            moe.moe_expert_choice_combine(self.eout, self.ec["slot"], self.ec["gates"], shared_out, y=self.y,
+            moe.moe_expert_choice_combine(self.eout, self.ec["slot"], self.ec["gates"], shared_out, y=out,
                                           stream=stream)
         else:
-            moe.moe_combine(self.eout, self.d_out["dest_row"], r["gates"], shared_out, y=self.y, stream=stream)
+            moe.moe_combine(self.eout, self.d_out["dest_row"], r["gates"], shared_out, y=out, stream=stream)
         mark("combine")
-        return self.y
+        return out
+
+    def forward_host_batches(self, x_hosts, y_hosts):
+        """Runs the layer over a sequence of batches that live in pinned host memory: x_hosts[i] -> y_hosts[i].
+
+        Every batch's tokens are copied host -> device and its output device -> host, on two copy streams,
+        while the layer works on another batch on the current stream (two device buffers for x and for y,
+        each reused only after the copy or the layer that last used it has finished). Returns after the last
+        output has reached host memory. The host tensors must be pinned and have the layer's dtype and
+        shape (bf16 may be given as int16 bit patterns)."""
+        dev = self.device
+        compute = torch.cuda.current_stream(dev)
+        h2d = torch.cuda.Stream(dev)
+        d2h = torch.cuda.Stream(dev)
+        dt = self.dtype
+        xd = [torch.empty((self.T, self.h), dtype=dt, device=dev) for _ in range(2)]
+        yd = [torch.empty((self.T, self.h), dtype=dt, device=dev) for _ in range(2)]
+        x_free = [None, None]          # layer done reading xd[b]
+        y_free = [None, None]          # d2h done reading yd[b]
+
+        def as_dt(t):
+            return t.view(dt) if t.dtype != dt else t
+
+        for i, (xh, yh) in enumerate(zip(x_hosts, y_hosts)):
+            b = i & 1
+            with torch.cuda.stream(h2d):
+                if x_free[b] is not None:
+                    h2d.wait_event(x_free[b])
+                xd[b].copy_(as_dt(xh), non_blocking=True)
+                x_in = torch.cuda.Event()
+                x_in.record(h2d)
+            compute.wait_event(x_in)
+            if y_free[b] is not None:
+                compute.wait_event(y_free[b])
+            self.forward(xd[b], y=yd[b])
+            done = torch.cuda.Event()
+            done.record(compute)
+            x_free[b] = done
+            with torch.cuda.stream(d2h):
+                d2h.wait_event(done)
+                as_dt(yh).copy_(yd[b], non_blocking=True)
+                out = torch.cuda.Event()
+                out.record(d2h)
+            y_free[b] = out
+        torch.cuda.synchronize(dev)
+        return y_hosts
