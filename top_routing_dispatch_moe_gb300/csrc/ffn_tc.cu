@@ -35,16 +35,26 @@ namespace moe {
 namespace tc {
 
 constexpr int BM = 128;                      // rows per tile (UMMA M, one TMEM lane per row)
-constexpr int BN = 256;                      // columns per tile (UMMA N)
 constexpr int BK = 64;                       // K per stage: 64 bf16 = one 128-byte swizzle row
 constexpr int UK = 16;                       // K per tcgen05.mma (kind::f16)
-constexpr int STAGES = 4;
 constexpr int A_BYTES = BM * BK * 2;         // 16 KB
-constexpr int B_BYTES = BN * BK * 2;         // 32 KB
-constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
-constexpr int TMEM_COLS = 512;               // 2 accumulators x 256 fp32 columns
+constexpr int TMEM_COLS = 512;               // 2 accumulators x up to 256 fp32 columns
 constexpr int NUM_THREADS = 192;
-constexpr int SMEM_BYTES = 1024 /* alignment slack */ + STAGES * STAGE_BYTES + 256 /* barriers, flags */;
+
+// Tile width (UMMA N) and ring depth: 256 columns x 4 stages of 48 KB. (A 192-column tile with 5 stages of
+// 40 KB was measured for the down GEMM: 2 % faster on the page-3 shape, where it shortens the last wave,
+// 6-17 % slower on the others, which pay for the extra operand bytes per flop.)
+template <int BN_, int STAGES_>
+struct TileCfg {
+    static constexpr int BN = BN_;
+    static constexpr int STAGES = STAGES_;
+    static constexpr int B_BYTES = BN * BK * 2;
+    static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
+    static constexpr int SMEM_BYTES = 1024 /* alignment slack */ + STAGES * STAGE_BYTES + 256 /* barriers, flags */;
+    static_assert(BN % 32 == 0 && BN >= 32 && BN <= 256, "UMMA N for M = 128");
+    static_assert(SMEM_BYTES <= 227 * 1024, "shared memory per CTA");
+};
+using Wide = TileCfg<256, 4>;
 constexpr long long kDrainLimit = 1LL << 24;
 
 // ---------------------------------------------------------------------------------------------------
@@ -163,7 +173,10 @@ __device__ __forceinline__ uint64_t sw128_desc(uint32_t saddr) {
 
 // Instruction descriptor, kind::f16: D fp32 (bits 4-5 = 1), A and B bf16 (bits 7-9, 10-12 = 1), both
 // K-major (bits 15, 16 = 0), N >> 3 at bits 17-22, M >> 4 at bits 24-28.
-constexpr uint32_t kIdesc = (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(BN >> 3) << 17) | ((uint32_t)(BM >> 4) << 24);
+template <int N>
+__host__ __device__ constexpr uint32_t idesc_bf16() {
+    return (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(N >> 3) << 17) | ((uint32_t)(BM >> 4) << 24);
+}
 
 // Epilogues: SwiGLU of the packed gate/up tile -> bf16 act; plain bf16 conversion; fp32 (+ per-column bias),
 // used for the router logits.
@@ -201,9 +214,12 @@ __device__ __forceinline__ Work map_work(const int32_t* sched, int E, int NT, in
     return Work{ent.x, ent.y, ent.z, n};
 }
 
-template <int EPI>
+template <int EPI, class CF>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
 grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB, Params p) {
+    constexpr int BN = CF::BN, STAGES = CF::STAGES, B_BYTES = CF::B_BYTES, STAGE_BYTES = CF::STAGE_BYTES;
+    constexpr uint32_t kIdesc = idesc_bf16<BN>();
+    static_assert(EPI != EPI_SWIGLU || BN == 256, "the SwiGLU epilogue pairs 128 gate with 128 up columns");
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw_addr = smem_u32(smem_raw);
     uint8_t* smem = smem_raw + ((1024u - (raw_addr & 1023u)) & 1023u);
@@ -330,7 +346,7 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
                 }
             } else if constexpr (EPI == EPI_F32) {
 #pragma unroll 1
-                for (int j = 0; j < 8; ++j) {
+                for (int j = 0; j < BN / 32; ++j) {
                     float v[32];
                     tmem_ld32(tbase + 32 * j, v);
                     const int n0 = wk.n * BN + 32 * j;
@@ -351,7 +367,7 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
                 }
             } else {
 #pragma unroll 1
-                for (int j = 0; j < 8; ++j) {
+                for (int j = 0; j < BN / 32; ++j) {
                     float v[32];
                     tmem_ld32(tbase + 32 * j, v);
                     const int n0 = wk.n * BN + 32 * j;
@@ -414,23 +430,23 @@ static int make_map(CUtensorMap* m, const void* base, long long rows, long long 
     return MOE_OK;
 }
 
-template <int EPI>
+template <int EPI, class CF>
 static int gemm(const void* a, long long a_rows, const void* b, long long b_rows_total, const Params& p,
                 cudaStream_t s) {
-    static bool attr_set[64][3];             // the attribute belongs to the kernel in each device's context
+    static bool attr_set[64];                // the attribute belongs to the kernel in each device's context
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64)
         return set_error(MOE_ERR_CUDA, "grouped_gemm: no usable current device");
-    if (!attr_set[dev][EPI]) {
-        cudaError_t e = cudaFuncSetAttribute(grouped_gemm_kernel<EPI>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             SMEM_BYTES);
+    if (!attr_set[dev]) {
+        cudaError_t e = cudaFuncSetAttribute(grouped_gemm_kernel<EPI, CF>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             CF::SMEM_BYTES);
         if (e != cudaSuccess) return set_error(MOE_ERR_CUDA, "grouped_gemm smem attribute: %s", cudaGetErrorString(e));
-        attr_set[dev][EPI] = true;
+        attr_set[dev] = true;
     }
     CUtensorMap ma, mb;
     if (int rc = make_map(&ma, a, a_rows, p.K, BM)) return rc;
-    if (int rc = make_map(&mb, b, b_rows_total, p.K, BN)) return rc;
-    grouped_gemm_kernel<EPI><<<num_sms(), NUM_THREADS, SMEM_BYTES, s>>>(ma, mb, p);
+    if (int rc = make_map(&mb, b, b_rows_total, p.K, CF::BN)) return rc;
+    grouped_gemm_kernel<EPI, CF><<<num_sms(), NUM_THREADS, CF::SMEM_BYTES, s>>>(ma, mb, p);
     return check_launch(EPI == EPI_SWIGLU ? "grouped_gemm_kernel<up_gate>"
                         : EPI == EPI_BF16 ? "grouped_gemm_kernel<down>" : "grouped_gemm_kernel<router>");
 }
@@ -444,7 +460,7 @@ int ffn_tc_up_gate(const void* buf, const int32_t* sched, const void* packed, in
     MOE_REQUIRE(err, MOE_ERR_CUDA, "device error word unavailable");
     tc::Params p{sched, h, L.Fp / 128, 2 * L.Fp, F, F, static_cast<__nv_bfloat16*>(act), nullptr, nullptr, err,
                  wait_limit()};
-    return tc::gemm<tc::EPI_SWIGLU>(buf, rows, static_cast<const char*>(packed) + L.up_gate_off,
+    return tc::gemm<tc::EPI_SWIGLU, tc::Wide>(buf, rows, static_cast<const char*>(packed) + L.up_gate_off,
                                     (long long)E * 2 * L.Fp, p, s);
 }
 
@@ -453,9 +469,10 @@ int ffn_tc_down(const void* act, const int32_t* sched, const void* packed, int E
     const PackedLayout L = packed_layout(E, h, F, 2);
     unsigned* err = device_error_word();
     MOE_REQUIRE(err, MOE_ERR_CUDA, "device error word unavailable");
-    tc::Params p{sched, F, cdiv(h, tc::BN), h, h, h, static_cast<__nv_bfloat16*>(eout), nullptr, nullptr, err,
+    using CF = tc::Wide;
+    tc::Params p{sched, F, cdiv(h, CF::BN), h, h, h, static_cast<__nv_bfloat16*>(eout), nullptr, nullptr, err,
                  wait_limit()};
-    return tc::gemm<tc::EPI_BF16>(act, rows, static_cast<const char*>(packed) + L.down_off, (long long)E * h, p, s);
+    return tc::gemm<tc::EPI_BF16, CF>(act, rows, static_cast<const char*>(packed) + L.down_off, (long long)E * h, p, s);
 }
 
 // Router logits [T, E] fp32 = x [T, h] @ w_rT^T (+ bias), w_rT the K-major [E, h] copy of the router weight,
@@ -464,8 +481,8 @@ int tc_router_logits(const void* x, const void* w_rT, const float* bias, int T, 
                      float* logits, cudaStream_t s) {
     unsigned* err = device_error_word();
     MOE_REQUIRE(err, MOE_ERR_CUDA, "device error word unavailable");
-    tc::Params p{sched, h, cdiv(E, tc::BN), E, E, E, nullptr, logits, bias, err, wait_limit()};
-    return tc::gemm<tc::EPI_F32>(x, T, w_rT, E, p, s);
+    tc::Params p{sched, h, cdiv(E, tc::Wide::BN), E, E, E, nullptr, logits, bias, err, wait_limit()};
+    return tc::gemm<tc::EPI_F32, tc::Wide>(x, T, w_rT, E, p, s);
 }
 
 }  // namespace moe
