@@ -340,3 +340,53 @@ def expert_choice_layer(x, w_r, weights, C: int, shared=None) -> dict:
     for e in range(E):
         y[ec["tokens"][e]] += ec["gates"][e][:, None] * eout[e * C:(e + 1) * C]
     return dict(logits=L, ec=ec, buf=buf, eout=eout, y=y)
+
+
+# ---------------------------------------------------------------------------------------------------------
+# Sinkhorn routing ([MEG6] "Router": Sinkhorn iterations normalise the routing matrix to a doubly stochastic
+# one, which balances the experts without an aux loss)
+# ---------------------------------------------------------------------------------------------------------
+
+SINKHORN_ITERS = 16
+SOFTMAX_SELBIAS = "softmax_selbias"      # select on logits + bias, gate = the softmax probability
+
+
+def sinkhorn_scaling(L: np.ndarray, n_iter: int = SINKHORN_ITERS):
+    """Sinkhorn-Knopp on K = exp(L - rowmax) [T, E]: starting from r = 1, n_iter times set the column scalings
+    c_e = (T / E) / sum_t K[t,e] r_t (columns sum to T / E), then the row scalings r_t = 1 / sum_e K[t,e] c_e
+    (rows sum to 1). Readings (the page names the method only): a fixed number of iterations (16), column
+    targets T / E. Returns (c, r)."""
+    T, E = L.shape
+    K = np.exp(L - L.max(axis=1, keepdims=True))
+    r = np.ones(T)
+    c = np.ones(E)
+    for _ in range(n_iter):
+        c = (T / E) / (K * r[:, None]).sum(axis=0)
+        r = 1.0 / (K * c[None, :]).sum(axis=1)
+    return c, r
+
+
+def route_sinkhorn(L: np.ndarray, k: int, n_iter: int = SINKHORN_ITERS, alpha: float = 0.01) -> dict:
+    """Top-k of the Sinkhorn-balanced matrix M = diag(r) K diag(c): a row scaling does not change a row's
+    order, so this is the top-k of L[t,e] + log c_e. Reading: the gates stay the router's softmax
+    probabilities of the chosen experts (not renormalised); counts, f, P and aux as in `route`."""
+    c, _ = sinkhorn_scaling(L, n_iter)
+    return route_selbias(L, k, np.log(c), alpha)
+
+
+def route_selbias(L: np.ndarray, k: int, sel_bias: np.ndarray, alpha: float = 0.01) -> dict:
+    """Select the top-k of L + sel_bias (descending, ties -> lower index); gates = softmax(L) of the chosen
+    (not renormalised); counts, f, P = mean softmax, aux = alpha E sum f P; gaps on the selection score."""
+    T, E = L.shape
+    prob = softmax(L)
+    score = L + np.asarray(sel_bias, np.float64)[None, :]
+    order = np.argsort(-score, axis=1, kind="stable")
+    ids = order[:, :k]
+    gates = prob[np.arange(T)[:, None], ids]
+    counts = np.bincount(ids.ravel(), minlength=E).astype(np.int64)
+    f = counts / float(k * T)
+    P = prob.mean(axis=0)
+    top = np.take_along_axis(score, order[:, :min(k + 1, E)], axis=1)
+    return dict(logits=L, ids=ids.astype(np.int32), gates=gates, counts=counts, f=f, P=P,
+                aux=alpha * E * float(np.sum(f * P)), prob=prob, score=score, gaps=top[:, :-1] - top[:, 1:],
+                sel_bias=np.asarray(sel_bias, np.float64))

@@ -10,6 +10,7 @@ from tests import test_oracle_pins as P
 
 _route, _dispatch, _swiglu, _combine, _capacity = O.route, O.dispatch, O.swiglu_ffn, O.combine, O.capacity
 _ec = O.expert_choice
+_sk = O.sinkhorn_scaling
 
 
 def mut_renormalise_softmax(L, k, gating, bias=None, alpha=0.01):
@@ -97,12 +98,32 @@ def mut_ec_ties_higher_token(L, C):
     return out
 
 
+def mut_sinkhorn_columns_only(L, n_iter=O.SINKHORN_ITERS):
+    """Normalises the columns once and never rescales the rows."""
+    T, E = L.shape
+    K = np.exp(L - L.max(axis=1, keepdims=True))
+    c = (T / E) / K.sum(axis=0)
+    return c, np.ones(T)
+
+
+def mut_sinkhorn_rows_first(L, n_iter=O.SINKHORN_ITERS):
+    """Swaps the targets: columns to 1, rows to T / E."""
+    T, E = L.shape
+    K = np.exp(L - L.max(axis=1, keepdims=True))
+    r = np.ones(T)
+    for _ in range(n_iter):
+        c = 1.0 / (K * r[:, None]).sum(axis=0)
+        r = (T / E) / (K * c[None, :]).sum(axis=1)
+    return c, r
+
+
 MUTANTS = [
     ("route", mut_renormalise_softmax), ("route", mut_ascending_order), ("route", mut_bias_in_sigmoid_gates),
     ("route", mut_aux_denominator_T), ("dispatch", mut_drop_latest_first), ("dispatch", mut_dispatch_unstable),
     ("swiglu_ffn", mut_swap_gate_up), ("swiglu_ffn", mut_transpose_down), ("combine", mut_combine_no_gate),
     ("capacity", mut_capacity_floor_over_E), ("expert_choice", mut_ec_select_on_logits),
-    ("expert_choice", mut_ec_ties_higher_token),
+    ("expert_choice", mut_ec_ties_higher_token), ("sinkhorn_scaling", mut_sinkhorn_columns_only),
+    ("sinkhorn_scaling", mut_sinkhorn_rows_first),
 ]
 
 PINS = [
@@ -114,6 +135,7 @@ PINS = [
     lambda: P.test_identity_experts(O.SOFTMAX, 0), lambda: P.test_identity_experts(O.SOFTMAX_RENORM, 0),
     P.test_token_sampled_layer_matches_full_layer, lambda: P.test_expert_choice_brute_force(9, 4, 4),
     P.test_expert_choice_ties_take_lower_token, P.test_expert_choice_full_capacity_is_dense,
+    P.test_sinkhorn_converges_to_doubly_stochastic, P.test_sinkhorn_closed_forms_and_balance,
 ]
 
 

@@ -445,3 +445,45 @@ def test_expert_choice_layer_against_scalar_loops():
             if t in col:
                 want += p[t, e] * np.array(_scalar_swiglu(list(x[t]), *[w.tolist() for w in W[e]]))
         assert np.allclose(out["y"][t], want, rtol=1e-12, atol=1e-12)
+
+
+# ------------------------------------------------------------------------------------------------ sinkhorn
+
+def test_sinkhorn_converges_to_doubly_stochastic():
+    """With many iterations the scaled matrix has rows summing to 1 and columns to T/E."""
+    rng = np.random.default_rng(21)
+    T, E = 64, 8
+    L = rng.standard_normal((T, E)) + np.linspace(0, 2, E)[None, :]
+    c, r = O.sinkhorn_scaling(L, n_iter=300)
+    K = np.exp(L - L.max(axis=1, keepdims=True))
+    M = r[:, None] * K * c[None, :]
+    assert np.allclose(M.sum(axis=1), 1.0, atol=1e-12)
+    assert np.allclose(M.sum(axis=0), T / E, rtol=1e-9)
+
+
+def test_sinkhorn_selection_equals_topk_of_balanced_matrix():
+    """Top-k of L + log c equals the top-k of diag(r) K diag(c) itself (brute force on the matrix)."""
+    rng = np.random.default_rng(22)
+    T, E, k = 40, 6, 2
+    L = rng.standard_normal((T, E)) * 2
+    c, r = O.sinkhorn_scaling(L)
+    M = r[:, None] * np.exp(L - L.max(axis=1, keepdims=True)) * c[None, :]
+    out = O.route_sinkhorn(L, k)
+    for t in range(T):
+        assert list(out["ids"][t]) == _brute_topk(list(M[t]), k)
+        assert np.allclose(out["gates"][t], O.softmax(L)[t, out["ids"][t]], rtol=1e-14)
+
+
+def test_sinkhorn_closed_forms_and_balance():
+    # uniform logits: K is constant, c uniform, the selection is plain top-k (ties -> lowest experts)
+    out = O.route_sinkhorn(np.zeros((12, 4)), 2)
+    assert out["ids"].tolist() == [[0, 1]] * 12
+    # a constant per-expert logit offset is exactly undone by the column scaling
+    rng = np.random.default_rng(23)
+    L = rng.standard_normal((200, 8))
+    shifted = O.route_sinkhorn(L + np.arange(8)[None, :] * 3.0, 1)
+    plain = O.route_sinkhorn(L, 1)
+    assert np.array_equal(shifted["ids"], plain["ids"])
+    # and the loads are far more even than plain top-1 on the shifted logits
+    raw = O.route(L + np.arange(8)[None, :] * 3.0, 1, O.SOFTMAX)
+    assert raw["counts"].max() > 150 and shifted["counts"].max() < 60
