@@ -51,7 +51,9 @@ enum moe_dtype { MOE_F32 = 0, MOE_BF16 = 1 };
 enum moe_gating {
     MOE_GATING_SOFTMAX = 0,            /* gate = full-softmax probability of the chosen expert */
     MOE_GATING_SOFTMAX_RENORM = 1,     /* gate = softmax probability / sum over the k chosen */
-    MOE_GATING_SIGMOID_BIAS_RENORM = 2 /* select on sigmoid(L)+bias; gate = s / sum_chosen s */
+    MOE_GATING_SIGMOID_BIAS_RENORM = 2, /* select on sigmoid(L)+bias; gate = s / sum_chosen s */
+    MOE_GATING_SOFTMAX_SELBIAS = 3      /* select on L+bias (bias: selection only, e.g. the Sinkhorn log column
+                                           scalings of moe_sinkhorn_bias); gate = full-softmax probability */
 };
 
 /* Rows per tile of the device tile schedule written by moe_dispatch and read by the expert FFN. */
@@ -80,6 +82,24 @@ size_t moe_router_workspace_size(int T, int h, int E, int k, int dtype);
 int moe_router(const void* x, const void* w_r, const float* bias, int T, int h, int E, int k, int dtype,
                int gating, float alpha, float* logits, int32_t* topk_ids, float* gates, int32_t* counts,
                float* f, float* P, float* aux, void* ws, size_t ws_bytes, void* stream);
+
+/* moe_router_from_logits: the gating part of moe_router (top-k, gates, counts, f, P, aux) on given fp32
+ * logits [T,E] (as moe_router writes them: bias already added in the two plain softmax modes; in the sigmoid
+ * and selection-bias modes `bias` is the selection-only term). Workspace: moe_router_from_logits_workspace_size. */
+size_t moe_router_from_logits_workspace_size(int T, int E);
+int moe_router_from_logits(const float* logits, const float* bias, int T, int E, int k, int gating, float alpha,
+                           int32_t* topk_ids, float* gates, int32_t* counts, float* f, float* P, float* aux,
+                           void* ws, size_t ws_bytes, void* stream);
+
+/* moe_sinkhorn_bias: Sinkhorn routing ("Megatron-LM ... （六）", section "Router": Sinkhorn iterations make the
+ * routing matrix doubly stochastic, balancing the experts without an aux loss). On K = exp(L - rowmax) [T,E]
+ * and starting from row scalings r = 1, n_iter times: c_e = (T/E) / sum_t K[t,e] r_t, then
+ * r_t = 1 / sum_e K[t,e] c_e. Writes sel_bias[e] = log c_e; the top-k of the balanced matrix
+ * diag(r) K diag(c) is the top-k of L + sel_bias (moe_router_from_logits with MOE_GATING_SOFTMAX_SELBIAS).
+ * fp32 with fixed-order sums (deterministic). Workspace: moe_sinkhorn_workspace_size(T, E). */
+size_t moe_sinkhorn_workspace_size(int T, int E);
+int moe_sinkhorn_bias(const float* logits, int T, int E, int n_iter, float* sel_bias, void* ws, size_t ws_bytes,
+                      void* stream);
 
 /* ---------------------------------------------------------------------------------------------------
  * moe_dispatch: histogram, exclusive scan, stable scatter, capacity mask, permutation indices, EP send

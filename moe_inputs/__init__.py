@@ -75,6 +75,11 @@ CONFIGS = {
     "page3_expert_choice": MoEConfig("page3_expert_choice", T=4096, h=4096, E=8, k=2, F=12288,
                                      gating=GATING_SOFTMAX, cf=1.0, R=8, n_shared=0, dtype="bf16", alpha=0.01,
                                      bias="none", routing="expert_choice"),
+    # Mixtral-shaped layer with the Zipf-skewed logits routed by Sinkhorn balancing (top-2 of the balanced
+    # matrix, softmax gates); the per-expert Zipf bias is a logit shift that Sinkhorn undoes exactly
+    "mixtral_sinkhorn": MoEConfig("mixtral_sinkhorn", T=8192, h=4096, E=8, k=2, F=14336,
+                                  gating="softmax_selbias", cf=0.0, R=8, n_shared=0, dtype="bf16", alpha=0.01,
+                                  bias="zipf", routing="sinkhorn"),
     # profiling stand-in for the page-3 shape: identical GEMM tiles (K=4096, 128x256 tiles, same routing and
     # capacity) with F=1536, so that a full ncu capture of the grouped GEMM holds well under 1 GB on the device
     "page3_profile": MoEConfig("page3_profile", T=4096, h=4096, E=8, k=2, F=1536, gating=GATING_SOFTMAX, cf=1.25,
@@ -134,6 +139,8 @@ ZIPF_BIAS_FILE = os.path.join(os.path.dirname(__file__), "mixtral_zipf_router_bi
 
 
 def load_zipf_bias(cfg: MoEConfig, seed: int = 0) -> np.ndarray:
+    if cfg.name == "mixtral_sinkhorn":                  # same inputs as the Mixtral-shaped workload
+        cfg = dataclasses.replace(cfg, name="mixtral_zipf")
     """Per-expert logit bias that makes the Mixtral-shaped workload's expert load follow Zipf(1).
 
     The values were found by a fixed-point calibration against the oracle's router and stored by

@@ -16,14 +16,33 @@ REPORT_GAP = 1e-6
 
 
 def router_inputs(cfg, seed=0, bias=None):
-    """x (with near-tie rows redrawn), w_r, bias, the oracle's routing, and the redraw record."""
+    """x (with near-tie rows redrawn), w_r, bias, the oracle's routing, and the redraw record.
+
+    Sinkhorn routing couples all tokens through the column scalings (redrawing one row moves every score by
+    ~1e-4), so for it the whole input is redrawn instead: the first seed >= `seed` whose balanced scores have
+    no gap below 1e-5."""
+    if cfg.routing == "sinkhorn":
+        w_r, b = moe_inputs.make_router(cfg, seed, bias=bias)
+        w64 = moe_inputs.to_f64(w_r, cfg.dtype)
+        for s in range(seed, seed + 200):
+            x = moe_inputs.make_x(cfg, s)
+            L = O.router_logits(moe_inputs.to_f64(x, cfg.dtype), w64, b, O.SOFTMAX)
+            r = O.route_sinkhorn(L, cfg.k, alpha=cfg.alpha)
+            if O.near_tie_rows(r["gaps"], REDRAW_GAP).size == 0:
+                return dict(x=x, w_r=w_r, bias=b, route=r, redrawn=0, x_seed=s,
+                            near_ties=int((r["gaps"] < REPORT_GAP).sum()))
+        raise RuntimeError("no near-tie-free input among 200 seeds")
     w_r, b = moe_inputs.make_router(cfg, seed, bias=bias)
     w64 = moe_inputs.to_f64(w_r, cfg.dtype)
     redraw: dict[int, int] = {}
     x = moe_inputs.make_x(cfg, seed)
     for _ in range(8):
-        L = O.router_logits(moe_inputs.to_f64(x, cfg.dtype), w64, b, cfg.gating)
-        r = O.route(L, cfg.k, cfg.gating, b, cfg.alpha)
+        if cfg.routing == "sinkhorn":           # logits with the bias added, then Sinkhorn-balanced top-k
+            L = O.router_logits(moe_inputs.to_f64(x, cfg.dtype), w64, b, O.SOFTMAX)
+            r = O.route_sinkhorn(L, cfg.k, alpha=cfg.alpha)
+        else:
+            L = O.router_logits(moe_inputs.to_f64(x, cfg.dtype), w64, b, cfg.gating)
+            r = O.route(L, cfg.k, cfg.gating, b, cfg.alpha)
         close = O.near_tie_rows(r["gaps"], REDRAW_GAP)
         if close.size == 0:
             break

@@ -31,6 +31,12 @@ struct GateOut {
     int32_t* partial_C; // [grid][E]
 };
 
+// The bias enters the logits in the plain and renormalised softmax modes; it is a selection-only term in the
+// sigmoid mode and in the softmax mode with selection bias.
+__host__ __device__ inline bool bias_in_logits(int gating) {
+    return gating == MOE_GATING_SOFTMAX || gating == MOE_GATING_SOFTMAX_RENORM;
+}
+
 // Gating of one token whose NPL-per-lane logits are in L (expert of slot i = lane + 32 i).
 // Accumulates the token's router probabilities into Pacc and its choices into the shared histogram.
 template <int NPL>
@@ -61,11 +67,12 @@ __device__ __forceinline__ void gate_token(float (&L)[NPL], int t, int E, int k,
         for (int i = 0; i < NPL; ++i) if (live[i]) m = fmaxf(m, L[i]);
         m = warp_max(m);
         float z = 0.f;
+        const bool selbias = gating == MOE_GATING_SOFTMAX_SELBIAS && bias;
 #pragma unroll
         for (int i = 0; i < NPL; ++i) {
             prob[i] = live[i] ? expf(L[i] - m) : 0.f;
             z += prob[i];
-            score[i] = live[i] ? L[i] : -INFINITY;
+            score[i] = live[i] ? L[i] + (selbias ? bias[lane + 32 * i] : 0.f) : -INFINITY;
         }
         z = warp_sum(z);
         float inv = 1.f / z;
@@ -100,7 +107,7 @@ __device__ __forceinline__ void gate_token(float (&L)[NPL], int t, int E, int k,
             psum += pv;
         }
     }
-    const float norm = (gating == MOE_GATING_SOFTMAX) ? 1.f : 1.f / psum;
+    const float norm = (gating == MOE_GATING_SOFTMAX || gating == MOE_GATING_SOFTMAX_SELBIAS) ? 1.f : 1.f / psum;
 #pragma unroll
     for (int j = 0; j < kMaxK; ++j) {
         if (j < k && lane == j) {
@@ -185,7 +192,7 @@ router_small_kernel(const T* __restrict__ x, const T* __restrict__ w_rT, const f
 
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     float Pacc[1] = {0.f};
-    const bool use_bias_in_logits = bias && gating != MOE_GATING_SIGMOID_BIAS_RENORM;
+    const bool use_bias_in_logits = bias && bias_in_logits(gating);
     const int nwarps = gridDim.x * kRouterWarps;
     // Two tokens per warp: every unpacked weight pair feeds both; accumulation in packed fp32 pairs
     // (even / odd element partial sums, added at the end).
@@ -440,7 +447,7 @@ extern "C" int moe_router(const void* x, const void* w_r, const float* bias, int
                           int gating, float alpha, float* logits, int32_t* topk_ids, float* gates, int32_t* counts,
                           float* f, float* P, float* aux, void* ws, size_t ws_bytes, void* stream) {
     MOE_REQUIRE(dtype == MOE_F32 || dtype == MOE_BF16, MOE_ERR_UNSUPPORTED, "moe_router: dtype %d", dtype);
-    MOE_REQUIRE(gating >= MOE_GATING_SOFTMAX && gating <= MOE_GATING_SIGMOID_BIAS_RENORM, MOE_ERR_UNSUPPORTED,
+    MOE_REQUIRE(gating >= MOE_GATING_SOFTMAX && gating <= MOE_GATING_SOFTMAX_SELBIAS, MOE_ERR_UNSUPPORTED,
                 "moe_router: gating mode %d", gating);
     MOE_REQUIRE(T >= 0 && h > 0 && h % 8 == 0, MOE_ERR_INVALID_ARG, "moe_router: T=%d h=%d (need T>=0, h%%8==0)", T, h);
     MOE_REQUIRE(E >= 1 && E <= 1024 && k >= 1 && k <= E && k <= kMaxK, MOE_ERR_INVALID_ARG,
@@ -498,7 +505,7 @@ extern "C" int moe_router(const void* x, const void* w_r, const float* bias, int
             if (int rc = check_launch("router_small_kernel")) return rc;
         } else {
             float* lg = logits ? logits : w.logits;
-            const float* lbias = (gating != MOE_GATING_SIGMOID_BIAS_RENORM) ? bias : nullptr;
+            const float* lbias = bias_in_logits(gating) ? bias : nullptr;
             if (tc) {
                 router_transpose_kernel<__nv_bfloat16><<<dim3(cdiv(E, 32), cdiv(h, 32)), dim3(32, 8), 0, s>>>(
                     static_cast<const __nv_bfloat16*>(w_r), h, E, static_cast<__nv_bfloat16*>(w.w_rT));
@@ -531,5 +538,46 @@ extern "C" int moe_router(const void* x, const void* w_r, const float* bias, int
         }
     }
     router_finalize<<<1, 1024, 0, s>>>(w.partial_P, w.partial_C, T > 0 ? G : 0, T, E, k, alpha, counts, f, P, aux);
+    return check_launch("router_finalize");
+}
+
+extern "C" size_t moe_router_from_logits_workspace_size(int T, int E) {
+    if (T < 0 || E <= 0) return 0;
+    const int G = router_grid(T);
+    return 2 * align_up((size_t)G * E * 4, 256);
+}
+
+extern "C" int moe_router_from_logits(const float* logits, const float* bias, int T, int E, int k, int gating,
+                                      float alpha, int32_t* topk_ids, float* gates, int32_t* counts, float* f,
+                                      float* P, float* aux, void* ws, size_t ws_bytes, void* stream) {
+    MOE_REQUIRE(gating >= MOE_GATING_SOFTMAX && gating <= MOE_GATING_SOFTMAX_SELBIAS, MOE_ERR_UNSUPPORTED,
+                "moe_router_from_logits: gating mode %d", gating);
+    MOE_REQUIRE(T >= 0 && E >= 1 && E <= 1024 && k >= 1 && k <= E && k <= kMaxK, MOE_ERR_INVALID_ARG,
+                "moe_router_from_logits: T=%d E=%d k=%d", T, E, k);
+    MOE_REQUIRE(counts && f && P && aux && (T == 0 || (logits && topk_ids && gates)), MOE_ERR_INVALID_ARG,
+                "moe_router_from_logits: null pointer");
+    const size_t need = moe_router_from_logits_workspace_size(T, E);
+    MOE_REQUIRE(ws && ws_bytes >= need, MOE_ERR_WORKSPACE, "moe_router_from_logits: workspace %zu < %zu", ws_bytes,
+                need);
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    const int G = router_grid(T);
+    char* base = static_cast<char*>(ws);
+    GateOut o{topk_ids, gates, nullptr, reinterpret_cast<float*>(base),
+              reinterpret_cast<int32_t*>(base + align_up((size_t)G * E * 4, 256))};
+    if (T > 0) {
+        const size_t smem = (size_t)kRouterWarps * E * sizeof(float) + (size_t)E * sizeof(int);
+        const int npl = cdiv(E, 32);
+#define MOE_GATE_LAUNCH2(N)                                                                             \
+        cudaFuncSetAttribute(router_gate_kernel<N>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem); \
+        router_gate_kernel<N><<<G, kRouterWarps * 32, smem, s>>>(logits, bias, T, E, k, gating, o);
+        if (npl <= 2) { MOE_GATE_LAUNCH2(2) }
+        else if (npl <= 4) { MOE_GATE_LAUNCH2(4) }
+        else if (npl <= 8) { MOE_GATE_LAUNCH2(8) }
+        else if (npl <= 16) { MOE_GATE_LAUNCH2(16) }
+        else { MOE_GATE_LAUNCH2(32) }
+#undef MOE_GATE_LAUNCH2
+        if (int rc = check_launch("router_gate_kernel")) return rc;
+    }
+    router_finalize<<<1, 1024, 0, s>>>(o.partial_P, o.partial_C, T > 0 ? G : 0, T, E, k, alpha, counts, f, P, aux);
     return check_launch("router_finalize");
 }

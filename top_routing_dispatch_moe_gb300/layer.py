@@ -54,6 +54,10 @@ class MoELayer:
             self.ec_ws = moe._bytes_tensor(moe.moe_expert_choice_workspace_size(T, E), dev)
         else:
             self.rows = moe.moe_dispatch_rows(T, E, k, self.C)
+        if routing == "sinkhorn":
+            self.sk_bias = torch.empty(E, dtype=f32, device=dev)
+            self.sk_ws = moe._bytes_tensor(moe._lib.moe_sinkhorn_workspace_size(T, E), dev)
+            self.rl_ws = moe._bytes_tensor(moe._lib.moe_router_from_logits_workspace_size(T, E), dev)
         self.r_out = dict(logits=torch.empty((T, E), dtype=f32, device=dev),
                           topk_ids=torch.empty((T, k), dtype=i32, device=dev),
                           gates=torch.empty((T, k), dtype=f32, device=dev),
@@ -89,12 +93,19 @@ class MoELayer:
 
         mark("start")
         r = self.r_out
-        moe.moe_router(x, self.w_r, self.bias, self.k, self.gating, self.alpha, logits=r["logits"],
+        moe.moe_router(x, self.w_r, self.bias, self.k, "softmax" if self.routing == "sinkhorn" else self.gating,
+                       self.alpha, logits=r["logits"],
                        topk_ids=r["topk_ids"], gates=r["gates"], counts=r["counts"], f=r["f"], P=r["P"], aux=r["aux"],
                        ws=self.r_ws, stream=stream)
         if self.routing == "expert_choice":
             moe.moe_expert_choice_route(r["logits"], self.C, tokens=self.ec["tokens"], gates=self.ec["gates"],
                                         slot=self.ec["slot"], ws=self.ec_ws, stream=stream)
+        elif self.routing == "sinkhorn":
+            # balanced selection: Sinkhorn column scalings as a selection-only bias, softmax gates
+            moe.moe_sinkhorn_bias(r["logits"], sel_bias=self.sk_bias, ws=self.sk_ws, stream=stream)
+            moe.moe_router_from_logits(r["logits"], self.sk_bias, self.k, "softmax_selbias", self.alpha,
+                                       topk_ids=r["topk_ids"], gates=r["gates"], counts=r["counts"], f=r["f"],
+                                       P=r["P"], aux=r["aux"], ws=self.rl_ws, stream=stream)
         mark("router")
         if self.routing == "expert_choice":
             moe.moe_expert_choice_dispatch(x, self.ec["tokens"], buf=self.d_out["buf"],

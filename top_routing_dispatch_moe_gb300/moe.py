@@ -18,13 +18,17 @@ _lib = ctypes.CDLL(_LIB_PATH)
 
 MOE_OK, MOE_ERR_INVALID_ARG, MOE_ERR_UNSUPPORTED, MOE_ERR_WORKSPACE, MOE_ERR_CUDA, MOE_ERR_TIMEOUT = range(6)
 MOE_F32, MOE_BF16 = 0, 1
-GATING = {"softmax": 0, "softmax_renorm": 1, "sigmoid_bias_renorm": 2}
+GATING = {"softmax": 0, "softmax_renorm": 1, "sigmoid_bias_renorm": 2, "softmax_selbias": 3}
 TILE_M = 128
 
 _P, _I, _Z, _F, _LL = ctypes.c_void_p, ctypes.c_int, ctypes.c_size_t, ctypes.c_float, ctypes.c_longlong
 _SIGS = {
     "moe_router_workspace_size": (_Z, [_I, _I, _I, _I, _I]),
     "moe_router": (_I, [_P, _P, _P, _I, _I, _I, _I, _I, _I, _F, _P, _P, _P, _P, _P, _P, _P, _P, _Z, _P]),
+    "moe_router_from_logits_workspace_size": (_Z, [_I, _I]),
+    "moe_router_from_logits": (_I, [_P, _P, _I, _I, _I, _I, _F, _P, _P, _P, _P, _P, _P, _P, _Z, _P]),
+    "moe_sinkhorn_workspace_size": (_Z, [_I, _I]),
+    "moe_sinkhorn_bias": (_I, [_P, _I, _I, _I, _P, _P, _Z, _P]),
     "moe_dispatch_rows": (_Z, [_I, _I, _I, _I]),
     "moe_tile_sched_bytes": (_Z, [_I, _I, _I, _I]),
     "moe_dispatch_workspace_size": (_Z, [_I, _I, _I, _I]),
@@ -117,6 +121,33 @@ def moe_router(x, w_r, bias, k: int, gating: str | int = "softmax", alpha: float
                            _ptr(gates), _ptr(counts), _ptr(f), _ptr(P), _ptr(aux), _ptr(ws), ws.numel(),
                            _stream(stream)))
     return dict(logits=logits, ids=topk_ids, gates=gates, counts=counts, f=f, P=P, aux=aux)
+
+
+def moe_router_from_logits(logits, bias, k: int, gating: str | int = "softmax", alpha: float = 0.01, *,
+                           topk_ids=None, gates=None, counts=None, f=None, P=None, aux=None, ws=None, stream=None):
+    T, E = logits.shape
+    dev = logits.device
+    g = GATING[gating] if isinstance(gating, str) else int(gating)
+    topk_ids = torch.empty((T, k), dtype=torch.int32, device=dev) if topk_ids is None else topk_ids
+    gates = torch.empty((T, k), dtype=torch.float32, device=dev) if gates is None else gates
+    counts = torch.empty(E, dtype=torch.int32, device=dev) if counts is None else counts
+    f = torch.empty(E, dtype=torch.float32, device=dev) if f is None else f
+    P = torch.empty(E, dtype=torch.float32, device=dev) if P is None else P
+    aux = torch.empty(1, dtype=torch.float32, device=dev) if aux is None else aux
+    ws = _bytes_tensor(_lib.moe_router_from_logits_workspace_size(T, E), dev) if ws is None else ws
+    _check(_lib.moe_router_from_logits(_ptr(logits), _ptr(bias), T, E, k, g, alpha, _ptr(topk_ids), _ptr(gates),
+                                       _ptr(counts), _ptr(f), _ptr(P), _ptr(aux), _ptr(ws), ws.numel(),
+                                       _stream(stream)))
+    return dict(ids=topk_ids, gates=gates, counts=counts, f=f, P=P, aux=aux)
+
+
+def moe_sinkhorn_bias(logits, n_iter: int = 16, *, sel_bias=None, ws=None, stream=None):
+    T, E = logits.shape
+    dev = logits.device
+    sel_bias = torch.empty(E, dtype=torch.float32, device=dev) if sel_bias is None else sel_bias
+    ws = _bytes_tensor(_lib.moe_sinkhorn_workspace_size(T, E), dev) if ws is None else ws
+    _check(_lib.moe_sinkhorn_bias(_ptr(logits), T, E, n_iter, _ptr(sel_bias), _ptr(ws), ws.numel(), _stream(stream)))
+    return sel_bias
 
 
 # ---------------------------------------------------------------------------------------------- dispatch
