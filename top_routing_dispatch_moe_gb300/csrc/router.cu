@@ -5,7 +5,7 @@
 // loss" bullet: aux = alpha * E * sum_i f_i P_i; DeepSeek-V3's bias is a selection-only term.
 //
 // Two ways to the logits, one gating epilogue:
-//   E <= 32: fused kernel, one warp per token, W_r^T staged in shared memory (the whole router weight is
+//   E <= 32: fused kernel, two tokens per warp, W_r^T staged in shared memory (the whole router weight is
 //            at most a few hundred KB and is read from L2 once per block), x streamed with 16-byte loads.
 //   E  > 32: logits GEMM [T,h] x [h,E] into fp32, then the gating kernel reads them back (L2-resident).
 // The gating epilogue keeps the E logits of a token spread over the 32 lanes of a warp (lane l holds
@@ -170,11 +170,48 @@ __device__ __forceinline__ void unpack_pairs(const Vec16<__nv_bfloat16>& v, unsi
 }
 
 // ---------------------------------------------------------------------------------------------------
-// E <= 32: fused logits + gating, W_r^T in shared memory (copied from the per-call transposed weight)
+// E <= 32: fused logits + gating, W_r^T in shared memory (transposed while it is staged)
 // ---------------------------------------------------------------------------------------------------
-template <typename T, int EMAX>
-__global__ void __launch_bounds__(kRouterWarps * 32)
-router_small_kernel(const T* __restrict__ x, const T* __restrict__ w_rT, const float* __restrict__ bias, int T_,
+// W_r [h][E] (global) -> wT [E][h] (shared), so that a lane's 16-byte x chunk meets each expert's weights
+// as one conflict-free 16-byte shared load. When an h-row of W_r is a whole number of 16-byte vectors, every
+// thread keeps 8 vector loads in flight and scatters their elements; otherwise element by element.
+template <typename T>
+__device__ __forceinline__ void stage_router_weight(const T* __restrict__ w_r, int h, int E, T* __restrict__ wT) {
+    constexpr int V = Vec16<T>::N;
+    if ((E * (int)sizeof(T)) % 16 == 0) {
+        const int RV = E / V;                                  // 16-byte vectors per h-row
+        const int nvec = h * RV;
+        constexpr int B = 4;
+        for (int v0 = threadIdx.x; v0 < nvec; v0 += B * blockDim.x) {
+            Vec16<T> r[B];
+#pragma unroll
+            for (int b = 0; b < B; ++b) {
+                const int v = v0 + b * blockDim.x;
+                if (v < nvec) r[b] = ld16(w_r + (size_t)v * V);
+            }
+#pragma unroll
+            for (int b = 0; b < B; ++b) {
+                const int v = v0 + b * blockDim.x;
+                if (v < nvec) {
+                    const int d = v / RV, e0 = (v - d * RV) * V;
+                    const T* el = reinterpret_cast<const T*>(&r[b].v);
+#pragma unroll
+                    for (int i = 0; i < V; ++i) wT[(size_t)(e0 + i) * h + d] = el[i];
+                }
+            }
+        }
+    } else {
+        for (int f = threadIdx.x; f < E * h; f += blockDim.x) {
+            const int d = f / E;
+            wT[(size_t)(f - d * E) * h + d] = w_r[f];
+        }
+    }
+}
+
+// U = 16-byte x chunks per token and lane in flight: 4 while the accumulators are small (E <= 8), else 2.
+template <typename T, int EMAX, int U>
+__global__ void __launch_bounds__(kRouterWarps * 32, 2)
+router_small_kernel(const T* __restrict__ x, const T* __restrict__ w_r, const float* __restrict__ bias, int T_,
                     int h, int E, int k, int gating, GateOut o) {
     extern __shared__ __align__(16) unsigned char smem_raw[];
     T* wT = reinterpret_cast<T*>(smem_raw);                                     // [E][h]
@@ -182,11 +219,7 @@ router_small_kernel(const T* __restrict__ x, const T* __restrict__ w_rT, const f
     int* s_hist = reinterpret_cast<int*>(s_P + kRouterWarps * E);
 
     constexpr int V = Vec16<T>::N;
-    {   // stage W_r^T [E][h] (transposed once per call) into shared memory with 16-byte copies
-        const int nvec = E * h / V;
-        for (int v = threadIdx.x; v < nvec; v += blockDim.x)
-            *reinterpret_cast<Vec16<T>*>(wT + (size_t)v * V) = ld16(w_rT + (size_t)v * V);
-    }
+    stage_router_weight(w_r, h, E, wT);
     for (int e = threadIdx.x; e < E; e += blockDim.x) s_hist[e] = 0;
     __syncthreads();
 
@@ -203,7 +236,6 @@ router_small_kernel(const T* __restrict__ x, const T* __restrict__ w_rT, const f
         for (int e = 0; e < EMAX; ++e) { acc0[e] = 0ull; acc1[e] = 0ull; }
         const T* x0 = x + (size_t)t0 * h;
         const T* x1 = x + (size_t)(has1 ? t0 + 1 : t0) * h;
-        constexpr int U = 2;                      // 16-byte loads in flight per token and lane
         for (int d0 = lane * V; d0 < h; d0 += U * 32 * V) {
             Vec16<T> va[U], vb[U];
 #pragma unroll
@@ -374,8 +406,7 @@ router_finalize(const float* __restrict__ partial_P, const int32_t* __restrict__
     if (threadIdx.x == 0) aux[0] = alpha * (float)E * s_red[0];
 }
 
-// W_r [h, E] -> W_rT [E, h]: the K-major operand of the tensor-core logits GEMM and the per-expert rows the
-// fused small-E kernel streams. 32 x 32 shared-memory tiles.
+// W_r [h, E] -> W_rT [E, h]: the K-major operand of the tensor-core logits GEMM. 32 x 32 shared-memory tiles.
 template <typename T>
 __global__ void __launch_bounds__(256)
 router_transpose_kernel(const T* __restrict__ w, int h, int E, T* __restrict__ wT) {
@@ -397,8 +428,8 @@ router_transpose_kernel(const T* __restrict__ w, int h, int E, T* __restrict__ w
 // ---------------------------------------------------------------------------------------------------
 // Upper bound of the blocks of any router launch (sizes the partial-sum workspace).
 static int router_grid(int T) { return std::max(1, std::min(cdiv(T, kRouterWarps), kRouterMaxBlocks)); }
-// The fused small-E kernel copies the transposed router weight into every block, takes two tokens per
-// warp, and its register budget allows two blocks per SM.
+// The fused small-E kernel stages the router weight into every block, takes two tokens per warp, and its
+// register budget allows two blocks per SM.
 static int router_small_grid(int T) { return std::max(1, std::min(cdiv(T, 2 * kRouterWarps), 2 * num_sms())); }
 
 static size_t small_smem_bytes(int h, int E, int el) {
@@ -423,7 +454,7 @@ static RouterWs router_ws_layout(void* ws, int T, int h, int E, int el, bool sma
     if (need_logits) { w.logits = reinterpret_cast<float*>(base + off); off = align_up(off + (size_t)T * E * 4, 256); }
     w.w_rT = nullptr;
     w.sched = nullptr;
-    if (tc || small) {                       // transposed weight: tensor-core GEMM and fused small-E kernel
+    if (tc) {                                // transposed weight: the tensor-core GEMM's K-major operand
         w.w_rT = base + off; off = align_up(off + (size_t)E * h * el, 256);
     }
     if (tc) { w.sched = reinterpret_cast<int32_t*>(base + off); off = align_up(off + sched_words(T, 1) * 4, 256); }
@@ -468,40 +499,21 @@ extern "C" int moe_router(const void* x, const void* w_r, const float* bias, int
     if (T > 0) {
         if (small) {
             const size_t smem = small_smem_bytes(h, E, el);
-            const dim3 tgrid(cdiv(E, 32), cdiv(h, 32)), tblock(32, 8);
+#define MOE_SMALL_LAUNCH(TY, EM, UU, XP, WP)                                                                  \
+            cudaFuncSetAttribute(router_small_kernel<TY, EM, UU>, cudaFuncAttributeMaxDynamicSharedMemorySize, \
+                                 (int)smem);                                                                  \
+            router_small_kernel<TY, EM, UU><<<G, kRouterWarps * 32, smem, s>>>(static_cast<const TY*>(XP),     \
+                static_cast<const TY*>(WP), bias, T, h, E, k, gating, o);
             if (dtype == MOE_BF16) {
-                const __nv_bfloat16* xb = static_cast<const __nv_bfloat16*>(x);
-                const __nv_bfloat16* wb = static_cast<const __nv_bfloat16*>(w.w_rT);
-                router_transpose_kernel<__nv_bfloat16><<<tgrid, tblock, 0, s>>>(
-                    static_cast<const __nv_bfloat16*>(w_r), h, E, static_cast<__nv_bfloat16*>(w.w_rT));
-                if (int rc = check_launch("router_transpose_kernel")) return rc;
-                if (E <= 8) {
-                    cudaFuncSetAttribute(router_small_kernel<__nv_bfloat16, 8>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-                    router_small_kernel<__nv_bfloat16, 8><<<G, kRouterWarps * 32, smem, s>>>(xb, wb, bias, T, h, E, k, gating, o);
-                } else if (E <= 16) {
-                    cudaFuncSetAttribute(router_small_kernel<__nv_bfloat16, 16>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-                    router_small_kernel<__nv_bfloat16, 16><<<G, kRouterWarps * 32, smem, s>>>(xb, wb, bias, T, h, E, k, gating, o);
-                } else {
-                    cudaFuncSetAttribute(router_small_kernel<__nv_bfloat16, 32>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-                    router_small_kernel<__nv_bfloat16, 32><<<G, kRouterWarps * 32, smem, s>>>(xb, wb, bias, T, h, E, k, gating, o);
-                }
+                if (E <= 8) { MOE_SMALL_LAUNCH(__nv_bfloat16, 8, 2, x, w_r) }
+                else if (E <= 16) { MOE_SMALL_LAUNCH(__nv_bfloat16, 16, 2, x, w_r) }
+                else { MOE_SMALL_LAUNCH(__nv_bfloat16, 32, 2, x, w_r) }
             } else {
-                const float* xf = static_cast<const float*>(x);
-                const float* wf = static_cast<const float*>(w.w_rT);
-                router_transpose_kernel<float><<<tgrid, tblock, 0, s>>>(static_cast<const float*>(w_r), h, E,
-                                                                        static_cast<float*>(w.w_rT));
-                if (int rc = check_launch("router_transpose_kernel")) return rc;
-                if (E <= 8) {
-                    cudaFuncSetAttribute(router_small_kernel<float, 8>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-                    router_small_kernel<float, 8><<<G, kRouterWarps * 32, smem, s>>>(xf, wf, bias, T, h, E, k, gating, o);
-                } else if (E <= 16) {
-                    cudaFuncSetAttribute(router_small_kernel<float, 16>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-                    router_small_kernel<float, 16><<<G, kRouterWarps * 32, smem, s>>>(xf, wf, bias, T, h, E, k, gating, o);
-                } else {
-                    cudaFuncSetAttribute(router_small_kernel<float, 32>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-                    router_small_kernel<float, 32><<<G, kRouterWarps * 32, smem, s>>>(xf, wf, bias, T, h, E, k, gating, o);
-                }
+                if (E <= 8) { MOE_SMALL_LAUNCH(float, 8, 2, x, w_r) }
+                else if (E <= 16) { MOE_SMALL_LAUNCH(float, 16, 2, x, w_r) }
+                else { MOE_SMALL_LAUNCH(float, 32, 2, x, w_r) }
             }
+#undef MOE_SMALL_LAUNCH
             if (int rc = check_launch("router_small_kernel")) return rc;
         } else {
             float* lg = logits ? logits : w.logits;
