@@ -7,11 +7,11 @@ import pytest
 pytestmark = pytest.mark.gpu
 
 
-def _problem():
+def _problem(rows):
     import torch
     from top_routing_dispatch_moe_gb300 import moe
     torch.manual_seed(3)
-    rows, h, F = 512, 256, 256
+    h, F = 256, 256
     x = torch.randn(rows, h, device="cuda").to(torch.bfloat16)
     wg = (torch.randn(1, F, h, device="cuda") / h ** 0.5).to(torch.bfloat16)
     wu = (torch.randn(1, F, h, device="cuda") / h ** 0.5).to(torch.bfloat16)
@@ -19,10 +19,11 @@ def _problem():
     return x, wg, wu, moe.moe_pack_expert_weights(wg, wu, wd), moe.moe_dense_tile_sched(rows), F
 
 
-def test_gemm_wait_timeout_reported_and_recoverable():
+@pytest.mark.parametrize("rows", [256, 512])      # the one-SM kernel (rows < 512 * E), the 2-SM kernel
+def test_gemm_wait_timeout_reported_and_recoverable(rows):
     import torch
     from top_routing_dispatch_moe_gb300 import moe
-    x, wg, wu, packed, sched, F = _problem()
+    x, wg, wu, packed, sched, F = _problem(rows)
     torch.cuda.synchronize()
     assert moe.moe_check_device_error() == moe.MOE_OK
     try:

@@ -1,6 +1,10 @@
 """The grouped SwiGLU GEMMs alone, on one dense group, against the same products computed by torch in fp32
 from the same bf16 operands (a localising check: on failure it reports which 128-row / 32-column blocks
-disagree), plus the tile-schedule corner cases: empty experts, one-row experts, ragged tails."""
+disagree), plus the tile-schedule corner cases: empty experts, one-row experts, ragged tails.
+
+The library runs the 2-SM kernel (pairs of 128-row tiles on a two-CTA cluster) when rows >= 512 * E and the
+one-SM kernel otherwise; the cases below cover both, including odd tile counts (a phantom half tile) and
+output widths that end inside the second CTA's half of a 256-column tile."""
 import numpy as np
 import pytest
 
@@ -28,7 +32,8 @@ def _blocks(err, rb=128, cb=32):
     return bad[:12]
 
 
-@pytest.mark.parametrize("rows,h,F", [(128, 128, 128), (300, 256, 384), (77, 512, 256), (1000, 1024, 640)])
+@pytest.mark.parametrize("rows,h,F", [(128, 128, 128), (300, 256, 384), (77, 512, 256), (1000, 1024, 640),
+                                      (640, 384, 256), (1100, 512, 384), (512, 256, 128)])
 def test_dense_group_up_gate_and_down(rows, h, F):
     import torch
     from top_routing_dispatch_moe_gb300 import moe
@@ -77,6 +82,40 @@ def test_grouped_schedule_with_empty_and_tiny_experts():
     assert moe.moe_check_device_error() == moe.MOE_OK, moe.moe_last_error_string()
     off = d["offsets"].cpu().tolist()
     assert off == list(np.concatenate([[0], np.cumsum(sizes)]))
+    for e in range(E):
+        if sizes[e] == 0:
+            continue
+        xb = d["buf"][off[e]:off[e + 1]]
+        a = _ref_act(xb, wg[e], wu[e]).to(torch.bfloat16).float()
+        ref = a @ wd[e].float().T
+        got = eout[off[e]:off[e + 1]].float()
+        rel = ((got - ref).norm() / ref.norm()).item()
+        assert rel < 1e-2, f"expert {e} ({sizes[e]} rows): rel err {rel:.3e}"
+
+
+def test_grouped_schedule_on_the_pair_kernel():
+    """Experts with 0, 1, 257 and 1900 rows (0, 1, 3 and 15 tiles: three odd counts) with rows >= 512 * E, so the
+    2-SM kernel runs, its phantom half tiles included."""
+    import torch
+    from top_routing_dispatch_moe_gb300 import moe
+    torch.manual_seed(1)
+    dev = "cuda"
+    sizes = [0, 1, 257, 1900]
+    E, h, F = len(sizes), 512, 384
+    assert sum(sizes) >= 512 * E
+    ids = np.concatenate([np.full(n, e, np.int32) for e, n in enumerate(sizes)])
+    np.random.default_rng(1).shuffle(ids)
+    T = ids.size
+    x = torch.randn(T, h, device=dev).to(torch.bfloat16)
+    d = moe.moe_dispatch(x, torch.from_numpy(ids[:, None]).to(dev), E, 0, 1)
+    wg = (torch.randn(E, F, h, device=dev) / h ** 0.5).to(torch.bfloat16)
+    wu = (torch.randn(E, F, h, device=dev) / h ** 0.5).to(torch.bfloat16)
+    wd = (torch.randn(E, h, F, device=dev) / F ** 0.5).to(torch.bfloat16)
+    packed = moe.moe_pack_expert_weights(wg, wu, wd)
+    eout = moe.moe_expert_ffn(d["buf"], d["tile_sched"], packed, E, F)
+    torch.cuda.synchronize()
+    assert moe.moe_check_device_error() == moe.MOE_OK, moe.moe_last_error_string()
+    off = d["offsets"].cpu().tolist()
     for e in range(E):
         if sizes[e] == 0:
             continue

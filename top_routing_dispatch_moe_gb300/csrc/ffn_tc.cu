@@ -28,6 +28,7 @@
 #include <cuda.h>
 #include <cudaTypedefs.h>
 #include <math.h>
+#include <algorithm>
 #include <mutex>
 #include "ffn.cuh"
 
@@ -173,9 +174,9 @@ __device__ __forceinline__ uint64_t sw128_desc(uint32_t saddr) {
 
 // Instruction descriptor, kind::f16: D fp32 (bits 4-5 = 1), A and B bf16 (bits 7-9, 10-12 = 1), both
 // K-major (bits 15, 16 = 0), N >> 3 at bits 17-22, M >> 4 at bits 24-28.
-template <int N>
+template <int N, int M = BM>
 __host__ __device__ constexpr uint32_t idesc_bf16() {
-    return (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(N >> 3) << 17) | ((uint32_t)(BM >> 4) << 24);
+    return (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
 }
 
 // Epilogues: SwiGLU of the packed gate/up tile -> bf16 act; plain bf16 conversion; fp32 (+ per-column bias),
@@ -212,6 +213,77 @@ __device__ __forceinline__ Work map_work(const int32_t* sched, int E, int NT, in
     const int n = local / mt, m = p0 + local % mt;
     const int4 ent = __ldg(reinterpret_cast<const int4*>(sched + sched_tiles_offset(E)) + m);
     return Work{ent.x, ent.y, ent.z, n};
+}
+
+// Epilogue of one accumulator: this thread's TMEM lane (one output row) -> SwiGLU of the packed gate/up
+// columns into bf16 act, a plain bf16 row, or an fp32 row (+ per-column bias), masked to the valid rows
+// and columns.
+template <int EPI, int BN>
+__device__ __forceinline__ void store_tile(const Params& p, uint32_t tbase, int row, bool live, int n) {
+    if constexpr (EPI == EPI_SWIGLU) {
+#pragma unroll 1
+        for (int j = 0; j < 4; ++j) {
+            float g[32], u[32];
+            tmem_ld32(tbase + 32 * j, g);
+            tmem_ld32(tbase + 128 + 32 * j, u);
+            const int f0 = n * 128 + 32 * j;
+            if (live) {
+                __nv_bfloat16* dst = p.out + (size_t)row * p.ldo + f0;
+#pragma unroll
+                for (int c = 0; c < 32; c += 8) {
+                    if (f0 + c < p.n_valid) {
+                        Vec16<__nv_bfloat16> o;
+#pragma unroll
+                        for (int i = 0; i < 8; ++i) {
+                            const float gv = g[c + i];
+                            o.set(i, gv / (1.f + expf(-gv)) * u[c + i]);
+                        }
+                        st16(dst + c, o);
+                    }
+                }
+            }
+        }
+    } else if constexpr (EPI == EPI_F32) {
+#pragma unroll 1
+        for (int j = 0; j < BN / 32; ++j) {
+            float v[32];
+            tmem_ld32(tbase + 32 * j, v);
+            const int n0 = n * BN + 32 * j;
+            if (live) {
+                float* dst = p.out_f32 + (size_t)row * p.ldo + n0;
+#pragma unroll
+                for (int c = 0; c < 32; c += 4) {
+                    if (n0 + c < p.n_valid) {
+                        float4 o;
+                        o.x = v[c] + (p.bias ? __ldg(p.bias + n0 + c) : 0.f);
+                        o.y = v[c + 1] + (p.bias ? __ldg(p.bias + n0 + c + 1) : 0.f);
+                        o.z = v[c + 2] + (p.bias ? __ldg(p.bias + n0 + c + 2) : 0.f);
+                        o.w = v[c + 3] + (p.bias ? __ldg(p.bias + n0 + c + 3) : 0.f);
+                        *reinterpret_cast<float4*>(dst + c) = o;
+                    }
+                }
+            }
+        }
+    } else {
+#pragma unroll 1
+        for (int j = 0; j < BN / 32; ++j) {
+            float v[32];
+            tmem_ld32(tbase + 32 * j, v);
+            const int n0 = n * BN + 32 * j;
+            if (live) {
+                __nv_bfloat16* dst = p.out + (size_t)row * p.ldo + n0;
+#pragma unroll
+                for (int c = 0; c < 32; c += 8) {
+                    if (n0 + c < p.n_valid) {
+                        Vec16<__nv_bfloat16> o;
+#pragma unroll
+                        for (int i = 0; i < 8; ++i) o.set(i, v[c + i]);
+                        st16(dst + c, o);
+                    }
+                }
+            }
+        }
+    }
 }
 
 template <int EPI, class CF>
@@ -321,70 +393,7 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
             const int row = wk.row0 + lane_base + lane;
             const bool live = row < wk.row1;
             const uint32_t tbase = tmem + (uint32_t)(a * BN) + ((uint32_t)lane_base << 16);
-            if constexpr (EPI == EPI_SWIGLU) {
-#pragma unroll 1
-                for (int j = 0; j < 4; ++j) {
-                    float g[32], u[32];
-                    tmem_ld32(tbase + 32 * j, g);
-                    tmem_ld32(tbase + 128 + 32 * j, u);
-                    const int f0 = wk.n * 128 + 32 * j;
-                    if (live) {
-                        __nv_bfloat16* dst = p.out + (size_t)row * p.ldo + f0;
-#pragma unroll
-                        for (int c = 0; c < 32; c += 8) {
-                            if (f0 + c < p.n_valid) {
-                                Vec16<__nv_bfloat16> o;
-#pragma unroll
-                                for (int i = 0; i < 8; ++i) {
-                                    const float gv = g[c + i];
-                                    o.set(i, gv / (1.f + expf(-gv)) * u[c + i]);
-                                }
-                                st16(dst + c, o);
-                            }
-                        }
-                    }
-                }
-            } else if constexpr (EPI == EPI_F32) {
-#pragma unroll 1
-                for (int j = 0; j < BN / 32; ++j) {
-                    float v[32];
-                    tmem_ld32(tbase + 32 * j, v);
-                    const int n0 = wk.n * BN + 32 * j;
-                    if (live) {
-                        float* dst = p.out_f32 + (size_t)row * p.ldo + n0;
-#pragma unroll
-                        for (int c = 0; c < 32; c += 4) {
-                            if (n0 + c < p.n_valid) {
-                                float4 o;
-                                o.x = v[c] + (p.bias ? __ldg(p.bias + n0 + c) : 0.f);
-                                o.y = v[c + 1] + (p.bias ? __ldg(p.bias + n0 + c + 1) : 0.f);
-                                o.z = v[c + 2] + (p.bias ? __ldg(p.bias + n0 + c + 2) : 0.f);
-                                o.w = v[c + 3] + (p.bias ? __ldg(p.bias + n0 + c + 3) : 0.f);
-                                *reinterpret_cast<float4*>(dst + c) = o;
-                            }
-                        }
-                    }
-                }
-            } else {
-#pragma unroll 1
-                for (int j = 0; j < BN / 32; ++j) {
-                    float v[32];
-                    tmem_ld32(tbase + 32 * j, v);
-                    const int n0 = wk.n * BN + 32 * j;
-                    if (live) {
-                        __nv_bfloat16* dst = p.out + (size_t)row * p.ldo + n0;
-#pragma unroll
-                        for (int c = 0; c < 32; c += 8) {
-                            if (n0 + c < p.n_valid) {
-                                Vec16<__nv_bfloat16> o;
-#pragma unroll
-                                for (int i = 0; i < 8; ++i) o.set(i, v[c + i]);
-                                st16(dst + c, o);
-                            }
-                        }
-                    }
-                }
-            }
+            store_tile<EPI, BN>(p, tbase, row, live, wk.n);
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(tempty(a));
@@ -395,6 +404,292 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
     if (warp == 1) {
         tc_fence_after();
         tmem_dealloc(tmem, TMEM_COLS);
+    }
+}
+
+// ---------------------------------------------------------------------------------------------------
+// 2-SM variant: a cluster of two CTAs computes a 256 x 256 tile with tcgen05.mma.cta_group::2 (M = 256)
+// ---------------------------------------------------------------------------------------------------
+// The even CTA of the pair (rank 0) issues the MMAs; each CTA holds its own 128 token rows (A) and one half of
+// the 256 weight rows (B: rows 0-127 in rank 0, 128-255 in rank 1), so per MMA an SM stages half the weight
+// bytes of the one-SM kernel. Every CTA's accumulator holds its 128 rows x all 256 columns, so the epilogue is
+// the same. Both CTAs' copies of a stage complete on rank 0's full barrier (TMA .cta_group::2); the MMA commits
+// are multicast to both CTAs' barriers; both epilogues arrive on rank 0's accumulator-empty barrier.
+// A pair covers two consecutive 128-row tiles of one expert; an odd last tile leaves rank 1 a phantom tile
+// whose rows it loads (the partner's, any valid rows) but never stores.
+constexpr int PAIR_STAGES = 6;
+constexpr int B_HALF_BYTES = 128 * BK * 2;                     // 16 KB
+constexpr int PAIR_STAGE_BYTES = A_BYTES + B_HALF_BYTES;       // 32 KB per CTA and stage
+constexpr int PAIR_MAX_E = 1024;
+constexpr int PAIR_SMEM_BYTES = 1024 + PAIR_STAGES * PAIR_STAGE_BYTES + 256 + (PAIR_MAX_E + 1) * 4;
+static_assert(PAIR_SMEM_BYTES <= 227 * 1024, "shared memory per CTA");
+
+__device__ __forceinline__ uint32_t cluster_rank() {
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+    return r;
+}
+// Shared-memory address `addr` of this CTA -> the same offset in CTA `rank` of the cluster.
+__device__ __forceinline__ uint32_t map_rank(uint32_t addr, uint32_t rank) {
+    uint32_t r;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(addr), "r"(rank));
+    return r;
+}
+__device__ __forceinline__ void cluster_sync_all() {
+    __syncwarp();
+    asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void st_cluster(uint32_t addr, uint32_t v) {
+    asm volatile("st.shared::cluster.u32 [%0], %1;" ::"r"(addr), "r"(v) : "memory");
+}
+__device__ __forceinline__ void mbar_arrive_cluster(uint32_t cluster_addr) {
+    asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr) : "memory");
+}
+__device__ __forceinline__ void mbar_complete_tx(uint32_t bar, uint32_t bytes) {
+    asm volatile("mbarrier.complete_tx.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(bytes) : "memory");
+}
+__device__ __forceinline__ bool mbar_try_wait_acq_cluster(uint32_t bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+// Bounded wait of the pair kernel: a timeout raises the abort flag of both CTAs.
+template <bool ACQ_CLUSTER = false>
+__device__ __forceinline__ bool wait_phase_pair(uint32_t bar, uint32_t parity, long long limit,
+                                                volatile int* abort_flag, uint32_t peer_abort, unsigned* err,
+                                                unsigned site) {
+    for (long long i = 0; i < limit; ++i) {
+        if (ACQ_CLUSTER ? mbar_try_wait_acq_cluster(bar, parity) : mbar_try_wait(bar, parity)) return true;
+        if (*abort_flag) return false;
+    }
+    *abort_flag = 1;
+    st_cluster(peer_abort, 1u);
+    latch_device_error(err, kDevErrTimeout, site);
+    return false;
+}
+// TMA load into this CTA's shared memory whose completion is counted on an mbarrier of either CTA of the pair.
+__device__ __forceinline__ void tma_load_2d_pair(uint32_t dst, const CUtensorMap* map, int x, int y,
+                                                 uint32_t bar_cluster) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.cta_group::2"
+        " [%0], [%1, {%2, %3}], [%4];"
+        ::"r"(dst), "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(bar_cluster)
+        : "memory");
+}
+__device__ __forceinline__ void tmem_alloc_pair(uint32_t slot_smem, uint32_t ncols) {
+    asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(slot_smem), "r"(ncols)
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void tmem_dealloc_pair(uint32_t taddr, uint32_t ncols) {
+    asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols) : "memory");
+}
+__device__ __forceinline__ void umma_bf16_pair(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
+                                               uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, p;\n\t}"
+        ::"r"(d_tmem), "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+// Arrive on the mbarrier at offset `bar` in both CTAs of the pair once the issued MMAs have completed.
+__device__ __forceinline__ void umma_commit_pair(uint32_t bar) {
+    asm volatile("tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;"
+                 ::"r"(bar), "h"((uint16_t)3)
+                 : "memory");
+}
+
+struct PairWork { int e, arow, row0, row1, n; };   // arow: first row this CTA loads; [row0, row1): rows it stores
+
+// Work item w -> (expert, n-tile, pair of 128-row tiles), expert-major, n-tile next, pair fastest; this CTA
+// (rank 0 or 1) takes the first or second tile of the pair. pp: per-expert prefix of pair counts.
+__device__ __forceinline__ PairWork map_pair(const int32_t* sched, const int* pp, int E, int NT, int w, int rank) {
+    int lo = 0, hi = E;                      // find last e with pp[e] * NT <= w
+    while (lo < hi) {
+        const int mid = (lo + hi + 1) >> 1;
+        if ((long long)pp[mid] * NT <= w) lo = mid; else hi = mid - 1;
+    }
+    const int e = lo;
+    const int np = pp[e + 1] - pp[e];
+    const int local = w - pp[e] * NT;
+    const int n = local / np, q = local % np;
+    const int32_t* prefix = sched + kSchedHeader;
+    const int t0 = __ldg(prefix + e), mt = __ldg(prefix + e + 1) - t0;
+    const bool has = 2 * q + rank < mt;
+    const int4 ent = __ldg(reinterpret_cast<const int4*>(sched + sched_tiles_offset(E)) + t0 + 2 * q + (has ? rank : 0));
+    return PairWork{ent.x, ent.y, has ? ent.y : 0, has ? ent.z : 0, n};
+}
+
+template <int EPI>
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
+grouped_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB, Params p) {
+    constexpr int BN = 256, STAGES = PAIR_STAGES;
+    constexpr uint32_t kIdesc = idesc_bf16<BN, 2 * BM>();
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t raw_addr = smem_u32(smem_raw);
+    uint8_t* smem = smem_raw + ((1024u - (raw_addr & 1023u)) & 1023u);
+    const uint32_t sbase = smem_u32(smem);
+    const uint32_t sA = sbase, sB = sbase + STAGES * A_BYTES;
+    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + STAGES * PAIR_STAGE_BYTES);
+    const uint32_t bar0 = smem_u32(bars);
+    auto full = [&](int s) { return bar0 + 8u * s; };
+    auto empty = [&](int s) { return bar0 + 8u * (STAGES + s); };
+    auto tfull = [&](int a) { return bar0 + 8u * (2 * STAGES + a); };
+    auto tempty = [&](int a) { return bar0 + 8u * (2 * STAGES + 2 + a); };
+    const uint32_t mma_done = bar0 + 8u * (2 * STAGES + 4);
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * STAGES + 5);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+    volatile int* peer_rounds = reinterpret_cast<volatile int*>(tmem_slot + 2);   // rank 1's copy rounds, in rank 0
+    int* s_pp = reinterpret_cast<int*>(smem + STAGES * PAIR_STAGE_BYTES + 256);
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const uint32_t rank = cluster_rank();
+    const bool leader = rank == 0;
+    const int E = __ldg(p.sched + 1);
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < STAGES; ++s) { mbar_init(full(s), 1); mbar_init(empty(s), 1); }
+        for (int a = 0; a < 2; ++a) { mbar_init(tfull(a), 1); mbar_init(tempty(a), 8); }
+        mbar_init(mma_done, 1);
+        *abort_flag = 0;
+        *peer_rounds = 0;
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+        prefetch_tmap(&tmA);
+        prefetch_tmap(&tmB);
+    }
+    if (warp == 2) {                         // pair prefix: pp[e + 1] = sum over e' <= e of ceil(tiles_e' / 2)
+        const int32_t* prefix = p.sched + kSchedHeader;
+        int carry = 0;
+        if (lane == 0) s_pp[0] = 0;
+        for (int base = 0; base < E; base += 32) {
+            const int e = base + lane;
+            int v = e < E ? (__ldg(prefix + e + 1) - __ldg(prefix + e) + 1) >> 1 : 0;
+#pragma unroll
+            for (int off = 1; off < 32; off <<= 1) {
+                const int t = __shfl_up_sync(0xffffffffu, v, off);
+                if (lane >= off) v += t;
+            }
+            if (e < E) s_pp[e + 1] = carry + v;
+            carry += __shfl_sync(0xffffffffu, v, 31);
+        }
+    }
+    if (warp == 1) tmem_alloc_pair(smem_u32(tmem_slot), TMEM_COLS);
+    tc_fence_before();
+    cluster_sync_all();                      // barriers initialised and both CTAs' tensor memory allocated
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+    const uint32_t peer_abort = map_rank(smem_u32(const_cast<int*>(abort_flag)), rank ^ 1u);
+
+    const int NC = gridDim.x >> 1, cid = blockIdx.x >> 1;
+    const int total = s_pp[E] * p.NT;
+    const int KB = (p.K + BK - 1) / BK;
+    int my_rounds = 0;
+
+    if (warp == 0) {
+        if (lane == 0) {
+            // ------------------------------------------------------------------ TMA producer (both CTAs)
+            int stage = 0;
+            uint32_t phase = 0;
+            for (int w = cid; w < total && !*abort_flag; w += NC) {
+                const PairWork wk = map_pair(p.sched, s_pp, E, p.NT, w, rank);
+                const int brow = wk.e * p.b_rows + wk.n * BN + (int)rank * 128;
+                bool ok = true;
+                for (int kb = 0; kb < KB; ++kb) {
+                    if (!wait_phase_pair(empty(stage), phase ^ 1u, p.wait_limit, abort_flag, peer_abort, p.err, 0x40u)) {
+                        ok = false;
+                        break;
+                    }
+                    if (leader) mbar_expect_tx(full(stage), 2 * PAIR_STAGE_BYTES);
+                    const uint32_t fb = map_rank(full(stage), 0);
+                    tma_load_2d_pair(sA + stage * A_BYTES, &tmA, kb * BK, wk.arow, fb);
+                    tma_load_2d_pair(sB + stage * B_HALF_BYTES, &tmB, kb * BK, brow, fb);
+                    ++my_rounds;
+                    if (++stage == STAGES) { stage = 0; phase ^= 1u; }
+                }
+                if (!ok) break;
+            }
+            if (!leader) st_cluster(map_rank(smem_u32(const_cast<int*>(peer_rounds)), 0), (uint32_t)my_rounds);
+        }
+    } else if (warp == 1) {
+        if (lane == 0 && leader) {
+            // ------------------------------------------------------------------ MMA issuer (rank 0)
+            int stage = 0;
+            uint32_t phase = 0;
+            int iter = 0;
+            for (int w = cid; w < total && !*abort_flag; w += NC, ++iter) {
+                const int a = iter & 1;
+                const uint32_t aph = (iter >> 1) & 1;
+                if (!wait_phase_pair<true>(tempty(a), aph ^ 1u, p.wait_limit, abort_flag, peer_abort, p.err, 0x50u))
+                    break;
+                tc_fence_after();
+                const uint32_t d_tmem = tmem + (uint32_t)(a * BN);
+                bool ok = true;
+                for (int kb = 0; kb < KB; ++kb) {
+                    if (!wait_phase_pair(full(stage), phase, p.wait_limit, abort_flag, peer_abort, p.err, 0x51u)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint32_t a_s = sA + stage * A_BYTES, b_s = sB + stage * B_HALF_BYTES;
+#pragma unroll
+                    for (int k = 0; k < BK / UK; ++k)
+                        umma_bf16_pair(d_tmem, sw128_desc(a_s + k * UK * 2), sw128_desc(b_s + k * UK * 2), kIdesc,
+                                       (kb | k) != 0);
+                    umma_commit_pair(empty(stage));
+                    if (++stage == STAGES) { stage = 0; phase ^= 1u; }
+                }
+                if (!ok) break;
+                umma_commit_pair(tfull(a));
+            }
+            umma_commit_pair(mma_done);             // both CTAs learn when every MMA has finished
+        }
+    } else {
+        // ---------------------------------------------------------------------- epilogue (warps 2..5)
+        const int lane_base = 32 * (warp & 3);
+        const uint32_t tempty_leader = map_rank(tempty(0), 0);
+        int iter = 0;
+        for (int w = cid; w < total; w += NC, ++iter) {
+            const int a = iter & 1;
+            const uint32_t aph = (iter >> 1) & 1;
+            if (!wait_phase_pair(tfull(a), aph, p.wait_limit, abort_flag, peer_abort, p.err, 0x60u)) break;
+            tc_fence_after();
+            const PairWork wk = map_pair(p.sched, s_pp, E, p.NT, w, rank);
+            const int row = wk.row0 + lane_base + lane;
+            const bool live = row < wk.row1;
+            const uint32_t tbase = tmem + (uint32_t)(a * BN) + ((uint32_t)lane_base << 16);
+            store_tile<EPI, BN>(p, tbase, row, live, wk.n);
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive_cluster(tempty_leader + 8u * a);
+        }
+    }
+    cluster_sync_all();                      // every role has left its loop; rank 1's round count is in rank 0
+    if (warp == 0 && lane == 0 && leader) {
+        // Settle the rounds only one CTA issued (possible after an abort), then wait until every copy of both
+        // CTAs has landed: rank 1 must not exit while its copies still count on rank 0's barriers.
+        const int rl = my_rounds, rp = *peer_rounds;
+        for (int n = min(rl, rp); n < max(rl, rp); ++n) {
+            if (n < rl) mbar_complete_tx(full(n % STAGES), PAIR_STAGE_BYTES);   // rank 1 never issued round n
+            else mbar_expect_tx(full(n % STAGES), PAIR_STAGE_BYTES);            // only rank 1 issued round n
+        }
+        const int rmax = max(rl, rp);
+        for (int s = 0; s < STAGES && s < rmax; ++s) {
+            const int last = s + ((rmax - 1 - s) / STAGES) * STAGES;          // last round on stage s
+            drain_phase(full(s), (uint32_t)(last / STAGES) & 1u, p.err, 0x41u);
+        }
+    }
+    if (warp == 1 && lane == 0) drain_phase(mma_done, 0, p.err, 0x52u);
+    tc_fence_before();
+    cluster_sync_all();                      // copies landed, MMAs done, both epilogues finished
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc_pair(tmem, TMEM_COLS);
     }
 }
 
@@ -451,6 +746,39 @@ static int gemm(const void* a, long long a_rows, const void* b, long long b_rows
                         : EPI == EPI_BF16 ? "grouped_gemm_kernel<down>" : "grouped_gemm_kernel<router>");
 }
 
+// 2-SM kernel: as many pairs as can be resident at once (one CTA per SM), each looping over work items.
+template <int EPI>
+static int gemm_pair(const void* a, long long a_rows, const void* b, long long b_rows_total, const Params& p,
+                     cudaStream_t s) {
+    static int clusters[64];                 // resident pairs per device, 0 = not yet queried
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64)
+        return set_error(MOE_ERR_CUDA, "grouped_gemm_pair: no usable current device");
+    if (!clusters[dev]) {
+        cudaError_t e = cudaFuncSetAttribute(grouped_gemm_pair_kernel<EPI>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             PAIR_SMEM_BYTES);
+        if (e != cudaSuccess) return set_error(MOE_ERR_CUDA, "grouped_gemm_pair smem attribute: %s", cudaGetErrorString(e));
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3(2 * (num_sms() / 2));
+        cfg.blockDim = dim3(NUM_THREADS);
+        cfg.dynamicSmemBytes = PAIR_SMEM_BYTES;
+        int n = 0;
+        e = cudaOccupancyMaxActiveClusters(&n, grouped_gemm_pair_kernel<EPI>, &cfg);
+        if (e != cudaSuccess || n <= 0)
+            return set_error(MOE_ERR_CUDA, "grouped_gemm_pair: no resident cluster of two CTAs (%s)", cudaGetErrorString(e));
+        clusters[dev] = std::min(n, num_sms() / 2);
+    }
+    CUtensorMap ma, mb;
+    if (int rc = make_map(&ma, a, a_rows, p.K, BM)) return rc;
+    if (int rc = make_map(&mb, b, b_rows_total, p.K, 128)) return rc;
+    grouped_gemm_pair_kernel<EPI><<<2 * clusters[dev], NUM_THREADS, PAIR_SMEM_BYTES, s>>>(ma, mb, p);
+    return check_launch(EPI == EPI_SWIGLU ? "grouped_gemm_pair_kernel<up_gate>" : "grouped_gemm_pair_kernel<down>");
+}
+
+// The 2-SM kernel when the average expert has at least four 128-row tiles (an odd tile count costs a
+// phantom half tile per expert), otherwise the one-SM kernel.
+static bool use_pair(int E, long long rows) { return E <= PAIR_MAX_E && rows >= 4LL * BM * E; }
+
 }  // namespace tc
 
 int ffn_tc_up_gate(const void* buf, const int32_t* sched, const void* packed, int E, int h, int F, int rows, void* act,
@@ -460,8 +788,9 @@ int ffn_tc_up_gate(const void* buf, const int32_t* sched, const void* packed, in
     MOE_REQUIRE(err, MOE_ERR_CUDA, "device error word unavailable");
     tc::Params p{sched, h, L.Fp / 128, 2 * L.Fp, F, F, static_cast<__nv_bfloat16*>(act), nullptr, nullptr, err,
                  wait_limit()};
-    return tc::gemm<tc::EPI_SWIGLU, tc::Wide>(buf, rows, static_cast<const char*>(packed) + L.up_gate_off,
-                                    (long long)E * 2 * L.Fp, p, s);
+    const char* b = static_cast<const char*>(packed) + L.up_gate_off;
+    if (tc::use_pair(E, rows)) return tc::gemm_pair<tc::EPI_SWIGLU>(buf, rows, b, (long long)E * 2 * L.Fp, p, s);
+    return tc::gemm<tc::EPI_SWIGLU, tc::Wide>(buf, rows, b, (long long)E * 2 * L.Fp, p, s);
 }
 
 int ffn_tc_down(const void* act, const int32_t* sched, const void* packed, int E, int h, int F, int rows, void* eout,
@@ -472,7 +801,9 @@ int ffn_tc_down(const void* act, const int32_t* sched, const void* packed, int E
     using CF = tc::Wide;
     tc::Params p{sched, F, cdiv(h, CF::BN), h, h, h, static_cast<__nv_bfloat16*>(eout), nullptr, nullptr, err,
                  wait_limit()};
-    return tc::gemm<tc::EPI_BF16, CF>(act, rows, static_cast<const char*>(packed) + L.down_off, (long long)E * h, p, s);
+    const char* b = static_cast<const char*>(packed) + L.down_off;
+    if (tc::use_pair(E, rows)) return tc::gemm_pair<tc::EPI_BF16>(act, rows, b, (long long)E * h, p, s);
+    return tc::gemm<tc::EPI_BF16, CF>(act, rows, b, (long long)E * h, p, s);
 }
 
 // Router logits [T, E] fp32 = x [T, h] @ w_rT^T (+ bias), w_rT the K-major [E, h] copy of the router weight,
