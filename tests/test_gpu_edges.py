@@ -182,3 +182,27 @@ def test_forward_host_batches_matches_device_forward():
     layer.forward_host_batches(x_hosts, y_hosts)
     for yh, w in zip(y_hosts, want):
         assert torch.equal(yh, w.view(torch.int16).cpu())
+
+
+@pytest.mark.parametrize("E,k", [(4, 2), (8, 2), (12, 3), (16, 4), (24, 2), (32, 8)])
+@pytest.mark.parametrize("T,h", [(1, 1024), (17, 264), (1000, 1024), (300, 8)])
+def test_router_small_expert_counts(E, k, T, h):
+    """The fused bf16 router for E <= 32 (tensor-core logits, 16 tokens per block, h split over 8 warps):
+    expert counts that fill 8-expert blocks partly or fully, a single token, a ragged last 16-token tile,
+    h with a partial 32-column chunk (264) and h below one chunk (8), against the oracle's routing."""
+    import torch
+    from top_routing_dispatch_moe_gb300 import moe
+    cfg = moe_inputs.get_config("page3_cf1.25", T=T, h=h, E=E, k=k, F=128, R=1)
+    inp = cases.router_inputs(cfg)
+    assert inp["near_ties"] == 0
+    x = cases.to_device(inp["x"], cfg)
+    w = cases.to_device(inp["w_r"], cfg)
+    r = moe.moe_router(x, w, None, k, cfg.gating, cfg.alpha)
+    torch.cuda.synchronize()
+    assert moe.moe_check_device_error() == moe.MOE_OK, moe.moe_last_error_string()
+    ref = inp["route"]
+    np.testing.assert_array_equal(r["ids"].cpu().numpy(), ref["ids"])
+    np.testing.assert_array_equal(r["counts"].cpu().numpy(), ref["counts"])
+    assert cases.rel_max(r["logits"].cpu().numpy(), ref["logits"]) <= 1e-5
+    assert cases.rel_max(r["gates"].cpu().numpy(), ref["gates"]) <= 1e-5
+    assert cases.rel_max(r["P"].cpu().numpy(), ref["P"]) <= 1e-5

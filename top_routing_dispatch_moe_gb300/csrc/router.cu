@@ -5,8 +5,9 @@
 // loss" bullet: aux = alpha * E * sum_i f_i P_i; DeepSeek-V3's bias is a selection-only term.
 //
 // Two ways to the logits, one gating epilogue:
-//   E <= 32: fused kernel, two tokens per warp, W_r^T staged in shared memory (the whole router weight is
-//            at most a few hundred KB and is read from L2 once per block), x streamed with 16-byte loads.
+//   E <= 32: fused kernel, W_r^T staged in shared memory (the whole router weight is at most a few hundred KB
+//            and is read from L2 once per block), x streamed with 16-byte loads; bf16 on mma.sync tensor-core
+//            instructions (16 tokens per block), fp32 on the CUDA cores (two tokens per warp).
 //   E  > 32: logits GEMM [T,h] x [h,E] into fp32, then the gating kernel reads them back (L2-resident).
 // The gating epilogue keeps the E logits of a token spread over the 32 lanes of a warp (lane l holds
 // experts l, l+32, ...), takes k warp-wide argmax rounds (ties -> lower index), and accumulates per-block
@@ -286,6 +287,149 @@ router_small_kernel(const T* __restrict__ x, const T* __restrict__ w_r, const fl
 }
 
 // ---------------------------------------------------------------------------------------------------
+// E <= 32, bf16: logits on mma.sync m16n8k16 (bf16 in, fp32 accumulate), fused with the gating
+// ---------------------------------------------------------------------------------------------------
+// The logits GEMM is HBM-bound (x is read once, 2 h E flop per 2 h bytes), so what matters is the number of
+// instructions per byte: one mma.sync does 16 tokens x 8 experts x 16 of h. A block takes 16 tokens; its 8
+// warps split h into contiguous slices of 32-column chunks, each warp accumulating its slice's partial
+// logits, which are then added in a fixed warp order (deterministic).
+// Within a 32-column chunk, lane (g = lane / 4, t = lane % 4) loads 16 contiguous bytes (columns 8t .. 8t+7)
+// of token rows g and g + 8 and of W_r^T row g. The two k16 steps of the chunk take those columns in the order
+// {8t, 8t+1 | 8t+2, 8t+3} and {8t+4, 8t+5 | 8t+6, 8t+7} as the fragment's {2t, 2t+1 | 2t+8, 2t+9}: A and B use
+// the same permutation of k, so every column of the chunk is summed exactly once.
+constexpr int kMmaTokens = 16;
+
+__device__ __forceinline__ void mma_bf16_16816(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
+                                               uint32_t b0, uint32_t b1) {
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+        "{%0,%1,%2,%3};"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+// W_r^T row stride in shared memory (elements): h rounded up to whole 32-column chunks, plus 64 bytes so that
+// the 8 lanes of a 16-byte load phase (two W rows, four column groups) hit distinct banks.
+__host__ __device__ inline int mma_wt_stride(int h) { return ((h + 31) / 32 * 32 * 2 + 127) / 128 * 64 + 32; }
+
+template <int NB, int U>   // NB blocks of 8 experts (E <= 8 NB); U chunks of 32 columns in flight per warp
+__global__ void __launch_bounds__(kRouterWarps * 32, 2)
+router_mma_kernel(const __nv_bfloat16* __restrict__ x, const __nv_bfloat16* __restrict__ w_r,
+                  const float* __restrict__ bias, int T_, int h, int E, int k, int gating, GateOut o) {
+    constexpr int EP = 8 * NB;
+    extern __shared__ __align__(16) unsigned char smem_raw[];
+    const int stride = mma_wt_stride(h);
+    __nv_bfloat16* wT = reinterpret_cast<__nv_bfloat16*>(smem_raw);                          // [EP][stride]
+    float* red = reinterpret_cast<float*>(smem_raw + (size_t)EP * stride * 2);                // [warps][16][EP]
+    float* s_P = red + kRouterWarps * kMmaTokens * EP;
+    int* s_hist = reinterpret_cast<int*>(s_P + kRouterWarps * E);
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, g = lane >> 2, t = lane & 3;
+    const int nchunks = (h + 31) / 32, cpw = (nchunks + kRouterWarps - 1) / kRouterWarps;
+    const int c_begin = min(nchunks, warp * cpw), c_end = min(nchunks, c_begin + cpw);
+
+    // This warp's slice of W_r [h][E] (rows d0 .. d1, one contiguous run of memory), transposed; rows e >= E
+    // and columns d1 .. dz past h are zero. With E = EP every 16-byte vector lies in one W_r row, and each lane
+    // keeps 8 vector loads in flight.
+    const int d0 = c_begin * 32, d1 = min(h, c_end * 32), dz = c_end * 32;
+    const __nv_bfloat16 zero = __float2bfloat16_rn(0.f);
+    if (E == EP) {
+        const int nvec = (d1 - d0) * EP / 8;
+        const uint4* src = reinterpret_cast<const uint4*>(w_r + (size_t)d0 * EP);
+        constexpr int B = 8;
+        for (int v0 = lane; v0 < nvec; v0 += 32 * B) {
+            uint4 r[B];
+#pragma unroll
+            for (int b = 0; b < B; ++b)
+                if (v0 + 32 * b < nvec) r[b] = __ldg(src + v0 + 32 * b);
+#pragma unroll
+            for (int b = 0; b < B; ++b) {
+                const int v = v0 + 32 * b;
+                if (v < nvec) {
+                    const int d = d0 + (8 * v) / EP, e0 = (8 * v) % EP;
+                    const __nv_bfloat16* el = reinterpret_cast<const __nv_bfloat16*>(&r[b]);
+#pragma unroll
+                    for (int i = 0; i < 8; ++i) wT[(size_t)(e0 + i) * stride + d] = el[i];
+                }
+            }
+        }
+    } else {
+        for (int f = lane; f < (d1 - d0) * EP; f += 32) {
+            const int d = d0 + f / EP, e = f % EP;
+            wT[(size_t)e * stride + d] = e < E ? w_r[(size_t)d * E + e] : zero;
+        }
+    }
+    for (int f = lane; f < (dz - d1) * EP; f += 32) wT[(size_t)(f % EP) * stride + d1 + f / EP] = zero;
+    for (int e = threadIdx.x; e < E; e += blockDim.x) s_hist[e] = 0;
+    __syncthreads();
+
+    float Pacc[1] = {0.f};
+    const bool use_bias_in_logits = bias && bias_in_logits(gating);
+    const int ntiles = (T_ + kMmaTokens - 1) / kMmaTokens;
+    for (int tile = blockIdx.x; tile < ntiles; tile += gridDim.x) {
+        const int tok0 = tile * kMmaTokens;
+        const __nv_bfloat16* x0 = x + (size_t)min(tok0 + g, T_ - 1) * h;          // rows past T: any valid row,
+        const __nv_bfloat16* x1 = x + (size_t)min(tok0 + g + 8, T_ - 1) * h;      // their logits are not used
+        float acc[NB][4];
+#pragma unroll
+        for (int nb = 0; nb < NB; ++nb) acc[nb][0] = acc[nb][1] = acc[nb][2] = acc[nb][3] = 0.f;
+        for (int c0 = c_begin; c0 < c_end; c0 += U) {
+            uint4 xa[U], xb[U];
+#pragma unroll
+            for (int u = 0; u < U; ++u) {
+                const int d = (c0 + u) * 32 + 8 * t;
+                if (c0 + u < c_end && d < h) {
+                    xa[u] = __ldcs(reinterpret_cast<const uint4*>(x0 + d));
+                    xb[u] = __ldcs(reinterpret_cast<const uint4*>(x1 + d));
+                } else {
+                    xa[u] = make_uint4(0, 0, 0, 0);
+                    xb[u] = make_uint4(0, 0, 0, 0);
+                }
+            }
+#pragma unroll
+            for (int u = 0; u < U; ++u) {
+                if (c0 + u < c_end) {
+#pragma unroll
+                    for (int nb = 0; nb < NB; ++nb) {
+                        const uint4 wv = *reinterpret_cast<const uint4*>(wT + (size_t)(8 * nb + g) * stride +
+                                                                        (c0 + u) * 32 + 8 * t);
+                        mma_bf16_16816(acc[nb], xa[u].x, xb[u].x, xa[u].y, xb[u].y, wv.x, wv.y);
+                        mma_bf16_16816(acc[nb], xa[u].z, xb[u].z, xa[u].w, xb[u].w, wv.z, wv.w);
+                    }
+                }
+            }
+        }
+        // D fragment: rows g and g + 8 (tokens), columns 2t, 2t + 1 of each 8-expert block
+#pragma unroll
+        for (int nb = 0; nb < NB; ++nb) {
+            float* r = red + (size_t)warp * kMmaTokens * EP + 8 * nb + 2 * t;
+            r[g * EP] = acc[nb][0];
+            r[g * EP + 1] = acc[nb][1];
+            r[(g + 8) * EP] = acc[nb][2];
+            r[(g + 8) * EP + 1] = acc[nb][3];
+        }
+        __syncthreads();
+        // gating: warp w takes tokens 2w and 2w + 1 of the tile; its lane e sums expert e over the 8 slices
+#pragma unroll
+        for (int j = 2 * warp; j < 2 * warp + 2; ++j) {
+            const int tok = tok0 + j;
+            if (tok >= T_) break;
+            float L[1] = {-INFINITY};
+            if (lane < E) {
+                float v = 0.f;
+#pragma unroll
+                for (int w = 0; w < kRouterWarps; ++w) v += red[((size_t)w * kMmaTokens + j) * EP + lane];
+                L[0] = v + (use_bias_in_logits ? bias[lane] : 0.f);
+                if (o.logits) o.logits[(size_t)tok * E + lane] = L[0];
+            }
+            gate_token<1>(L, tok, E, k, gating, bias, o, Pacc, s_hist);
+        }
+        __syncthreads();                      // red is rewritten by the next tile
+    }
+    flush_partials<1>(Pacc, E, s_P, s_hist, o);
+}
+
+// ---------------------------------------------------------------------------------------------------
 // E > 32: logits GEMM (fp32 accumulation, CUDA cores), then the gating kernel
 // ---------------------------------------------------------------------------------------------------
 // C[T,E] = x[T,h] @ W[h,E] (+ bias in softmax modes). 64x64 tiles, 16-deep K steps, 4x4 per thread.
@@ -435,7 +579,19 @@ static int router_small_grid(int T) { return std::max(1, std::min(cdiv(T, 2 * kR
 static size_t small_smem_bytes(int h, int E, int el) {
     return align_up((size_t)E * h * el, 16) + (size_t)kRouterWarps * E * sizeof(float) + (size_t)E * sizeof(int);
 }
-static bool use_small_path(int h, int E, int el) { return E <= 32 && small_smem_bytes(h, E, el) <= 200 * 1024; }
+// 8-expert blocks of the bf16 fused kernel instantiated for E (1, 2 or 4): sizes its shared memory and picks
+// the launch, so the two always agree.
+static int mma_blocks(int E) { return E <= 8 ? 1 : E <= 16 ? 2 : 4; }
+// The bf16 fused kernel on mma.sync: W_r^T padded to 8-expert blocks, the per-warp partial logits, P, counts.
+static size_t mma_smem_bytes(int h, int E) {
+    const int EP = 8 * mma_blocks(E);
+    return (size_t)EP * mma_wt_stride(h) * 2 + (size_t)kRouterWarps * kMmaTokens * EP * sizeof(float) +
+           (size_t)kRouterWarps * E * sizeof(float) + (size_t)E * sizeof(int);
+}
+static int router_mma_grid(int T) { return std::max(1, std::min(cdiv(T, kMmaTokens), 2 * num_sms())); }
+static bool use_small_path(int h, int E, int el) {
+    return E <= 32 && (el == 2 ? mma_smem_bytes(h, E) : small_smem_bytes(h, E, el)) <= 200 * 1024;
+}
 
 // The logits GEMM runs on the tcgen05 tensor cores for bf16 with E > 32 (E % 4 == 0 keeps the fp32 row
 // stores 16-byte aligned); otherwise on the CUDA cores.
@@ -494,25 +650,33 @@ extern "C" int moe_router(const void* x, const void* w_r, const float* bias, int
     MOE_REQUIRE(ws_bytes >= w.bytes && (w.bytes == 0 || ws), MOE_ERR_WORKSPACE,
                 "moe_router: workspace %zu < %zu bytes", ws_bytes, w.bytes);
     cudaStream_t s = static_cast<cudaStream_t>(stream);
-    const int G = small ? router_small_grid(T) : router_grid(T);
+    const int G = !small ? router_grid(T) : dtype == MOE_BF16 ? router_mma_grid(T) : router_small_grid(T);
     GateOut o{topk_ids, gates, logits, w.partial_P, w.partial_C};
     if (T > 0) {
-        if (small) {
-            const size_t smem = small_smem_bytes(h, E, el);
-#define MOE_SMALL_LAUNCH(TY, EM, UU, XP, WP)                                                                  \
-            cudaFuncSetAttribute(router_small_kernel<TY, EM, UU>, cudaFuncAttributeMaxDynamicSharedMemorySize, \
-                                 (int)smem);                                                                  \
-            router_small_kernel<TY, EM, UU><<<G, kRouterWarps * 32, smem, s>>>(static_cast<const TY*>(XP),     \
-                static_cast<const TY*>(WP), bias, T, h, E, k, gating, o);
-            if (dtype == MOE_BF16) {
-                if (E <= 8) { MOE_SMALL_LAUNCH(__nv_bfloat16, 8, 2, x, w_r) }
-                else if (E <= 16) { MOE_SMALL_LAUNCH(__nv_bfloat16, 16, 2, x, w_r) }
-                else { MOE_SMALL_LAUNCH(__nv_bfloat16, 32, 2, x, w_r) }
-            } else {
-                if (E <= 8) { MOE_SMALL_LAUNCH(float, 8, 2, x, w_r) }
-                else if (E <= 16) { MOE_SMALL_LAUNCH(float, 16, 2, x, w_r) }
-                else { MOE_SMALL_LAUNCH(float, 32, 2, x, w_r) }
+        if (small && dtype == MOE_BF16) {
+            const size_t smem = mma_smem_bytes(h, E);
+            const __nv_bfloat16* xb = static_cast<const __nv_bfloat16*>(x);
+            const __nv_bfloat16* wb = static_cast<const __nv_bfloat16*>(w_r);
+#define MOE_MMA_LAUNCH(NB, UU)                                                                                \
+            cudaFuncSetAttribute(router_mma_kernel<NB, UU>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem); \
+            router_mma_kernel<NB, UU><<<G, kRouterWarps * 32, smem, s>>>(xb, wb, bias, T, h, E, k, gating, o);
+            switch (mma_blocks(E)) {
+                case 1: { MOE_MMA_LAUNCH(1, 8) } break;
+                case 2: { MOE_MMA_LAUNCH(2, 8) } break;
+                default: { MOE_MMA_LAUNCH(4, 4) } break;
             }
+#undef MOE_MMA_LAUNCH
+            if (int rc = check_launch("router_mma_kernel")) return rc;
+        } else if (small) {
+            const size_t smem = small_smem_bytes(h, E, el);
+#define MOE_SMALL_LAUNCH(EM, UU)                                                                              \
+            cudaFuncSetAttribute(router_small_kernel<float, EM, UU>, cudaFuncAttributeMaxDynamicSharedMemorySize, \
+                                 (int)smem);                                                                  \
+            router_small_kernel<float, EM, UU><<<G, kRouterWarps * 32, smem, s>>>(static_cast<const float*>(x), \
+                static_cast<const float*>(w_r), bias, T, h, E, k, gating, o);
+            if (E <= 8) { MOE_SMALL_LAUNCH(8, 2) }
+            else if (E <= 16) { MOE_SMALL_LAUNCH(16, 2) }
+            else { MOE_SMALL_LAUNCH(32, 2) }
 #undef MOE_SMALL_LAUNCH
             if (int rc = check_launch("router_small_kernel")) return rc;
         } else {
