@@ -330,7 +330,9 @@ def run_gpu(args, cfg, C):
     hbm, bf16_burst, bf16_sus, peak_src = _peaks()
     ug_ms = float(np.mean(stage_ms["up_gate"]))
     dn_ms = float(np.mean(stage_ms["down"]))
-    ug_flops = 4.0 * kept * cfg.h * cfg.F
+    # with bf16 the shared expert's tiles run inside the up/gate and down launches
+    fused_shared = bool(cfg.n_shared) and "shared_up_gate" not in stage_ms
+    ug_flops = 4.0 * (kept + (cfg.T if fused_shared else 0)) * cfg.h * cfg.F
     ffn_flops = 6.0 * kept * cfg.h * cfg.F + (6.0 * cfg.T * cfg.h * cfg.F if cfg.n_shared else 0.0)
     ffn_ms = ug_ms + dn_ms + sum(float(np.mean(stage_ms[s])) for s in ("shared_up_gate", "shared_down") if s in stage_ms)
     ug_tflops = ug_flops / (ug_ms * 1e-3) / 1e12

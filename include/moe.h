@@ -205,6 +205,23 @@ int moe_expert_up_gate(const void* buf, const int32_t* tile_sched, const void* p
                        int rows, int dtype, void* act, void* stream);
 int moe_expert_down(const void* act, const int32_t* tile_sched, const void* packed_w, int E, int h, int F,
                     int rows, int dtype, void* eout, void* stream);
+/* Routed experts and one shared expert in the same launch per GEMM ("Megatron-LM ... （六）", data flow:
+ * the shared experts see every token and their output is added in the combine; the page's overlap
+ * guidance is realised by appending the shared expert's tiles to the routed experts' work list of one
+ * persistent tensor-core kernel, so they fill the routed GEMM's last partial wave instead of starting a
+ * launch of their own).
+ *   Routed part exactly as moe_expert_up_gate / moe_expert_down. Shared part, one dense group of T rows:
+ *     act_shared[t] = silu(x[t] @ Ws_gate^T) * (x[t] @ Ws_up^T)          [T,F]
+ *     out_shared[t] = act_shared[t] @ Ws_down^T                          [T,h]
+ *   packed_shared: the shared expert packed by moe_pack_expert_weights with E = 1 (same h, F).
+ *   bf16 only (MOE_ERR_UNSUPPORTED otherwise: fp32 callers make one call per group). tile_sched must be
+ *   valid even when rows == 0. All pointers 16-byte aligned; rows == 0 and T == 0 is a no-op. */
+int moe_expert_up_gate_shared(const void* buf, const int32_t* tile_sched, const void* packed_w, int E, int h, int F,
+                              int rows, const void* x, int T, const void* packed_shared, void* act_shared,
+                              int dtype, void* act, void* stream);
+int moe_expert_down_shared(const void* act, const int32_t* tile_sched, const void* packed_w, int E, int h, int F,
+                           int rows, const void* act_shared, int T, const void* packed_shared, void* out_shared,
+                           int dtype, void* eout, void* stream);
 size_t moe_expert_ffn_workspace_size(int rows, int F, int dtype);
 int moe_expert_ffn(const void* buf, const int32_t* tile_sched, const void* packed_w, int E, int h, int F,
                    int rows, int dtype, void* eout, void* ws, size_t ws_bytes, void* stream);

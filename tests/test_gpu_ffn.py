@@ -125,3 +125,49 @@ def test_grouped_schedule_on_the_pair_kernel():
         got = eout[off[e]:off[e + 1]].float()
         rel = ((got - ref).norm() / ref.norm()).item()
         assert rel < 1e-2, f"expert {e} ({sizes[e]} rows): rel err {rel:.3e}"
+
+
+@pytest.mark.parametrize("sizes,T", [
+    ([0, 1, 257, 1900], 300),      # 2-SM kernel (rows >= 512 E); 3 shared tiles: a phantom pair half
+    ([5, 130, 0, 77], 1000),       # one-SM kernel; ragged last shared tile
+    ([0, 0, 0, 0], 640),           # no routed rows: the launch runs the shared expert alone
+    ([40, 300, 2, 700], 0),        # no shared rows
+])
+def test_shared_expert_fused_into_routed_launch(sizes, T):
+    """moe_expert_up_gate_shared / moe_expert_down_shared: the shared expert's dense tiles appended to the routed
+    experts' work list of one launch per GEMM give bit-identical results to the separate calls (each tile's
+    arithmetic is the same)."""
+    import torch
+    from top_routing_dispatch_moe_gb300 import moe
+    torch.manual_seed(5)
+    dev = "cuda"
+    E, h, F = len(sizes), 256, 384
+    ids = np.concatenate([np.full(n, e, np.int32) for e, n in enumerate(sizes)]) if sum(sizes) else np.zeros(0, np.int32)
+    np.random.default_rng(2).shuffle(ids)
+    xr = torch.randn(max(ids.size, 1), h, device=dev).to(torch.bfloat16)[:ids.size]
+    d = moe.moe_dispatch(xr, torch.from_numpy(ids[:, None]).to(dev), E, 0, 1)
+    mk = lambda *s: (torch.randn(*s, device=dev) / s[-1] ** 0.5).to(torch.bfloat16)
+    packed = moe.moe_pack_expert_weights(mk(E, F, h), mk(E, F, h), mk(E, h, F))
+    packed_sh = moe.moe_pack_expert_weights(mk(1, F, h), mk(1, F, h), mk(1, h, F))
+    x = torch.randn(T, h, device=dev).to(torch.bfloat16)
+    buf = d["buf"]
+    act, act_sh = moe.moe_expert_up_gate_shared(buf, d["tile_sched"], packed, E, F, x, packed_sh)
+    eout, out_sh = moe.moe_expert_down_shared(act, d["tile_sched"], packed, E, h, act_sh, packed_sh)
+    torch.cuda.synchronize()
+    assert moe.moe_check_device_error() == moe.MOE_OK, moe.moe_last_error_string()
+    off = d["offsets"].cpu().tolist()
+    if buf.shape[0]:
+        act_ref = moe.moe_expert_up_gate(buf, d["tile_sched"], packed, E, F)
+        eout_ref = moe.moe_expert_down(act_ref, d["tile_sched"], packed, E, h)
+        torch.cuda.synchronize()
+        for e in range(E):
+            a, b = off[e], off[e + 1]
+            assert torch.equal(act[a:b], act_ref[a:b]), f"routed act, expert {e}"
+            assert torch.equal(eout[a:b], eout_ref[a:b]), f"routed eout, expert {e}"
+    if T:
+        sched = moe.moe_dense_tile_sched(T)
+        act_sh_ref = moe.moe_expert_up_gate(x, sched, packed_sh, 1, F)
+        out_sh_ref = moe.moe_expert_down(act_sh_ref, sched, packed_sh, 1, h)
+        torch.cuda.synchronize()
+        assert torch.equal(act_sh, act_sh_ref)
+        assert torch.equal(out_sh, out_sh_ref)

@@ -34,6 +34,37 @@ extern "C" int moe_expert_down(const void* act, const int32_t* tile_sched, const
     return ffn_simt_down(act, tile_sched, packed_w, E, h, F, rows, dtype, eout, s);
 }
 
+static int shared_check(const char* fn, const int32_t* sched, const void* in_sh, int T, const void* packed_sh,
+                        const void* out_sh, int dtype) {
+    MOE_REQUIRE(dtype == MOE_BF16, MOE_ERR_UNSUPPORTED, "%s: bf16 only (fp32: one call per group)", fn);
+    MOE_REQUIRE(T >= 0, MOE_ERR_INVALID_ARG, "%s: T=%d", fn, T);
+    MOE_REQUIRE(sched && (T == 0 || (in_sh && packed_sh && out_sh)), MOE_ERR_INVALID_ARG, "%s: null pointer", fn);
+    MOE_REQUIRE(aligned16(in_sh) && aligned16(packed_sh) && aligned16(out_sh), MOE_ERR_INVALID_ARG,
+                "%s: pointers must be 16-byte aligned", fn);
+    return MOE_OK;
+}
+
+extern "C" int moe_expert_up_gate_shared(const void* buf, const int32_t* tile_sched, const void* packed_w, int E, int h,
+                                         int F, int rows, const void* x, int T, const void* packed_shared,
+                                         void* act_shared, int dtype, void* act, void* stream) {
+    if (int rc = ffn_check("moe_expert_up_gate_shared", buf, tile_sched, packed_w, E, h, F, rows, dtype, act)) return rc;
+    if (int rc = shared_check("moe_expert_up_gate_shared", tile_sched, x, T, packed_shared, act_shared, dtype)) return rc;
+    if (rows == 0 && T == 0) return MOE_OK;
+    return ffn_tc_up_gate(buf, tile_sched, packed_w, E, h, F, rows, act, static_cast<cudaStream_t>(stream), x, T,
+                          packed_shared, act_shared);
+}
+
+extern "C" int moe_expert_down_shared(const void* act, const int32_t* tile_sched, const void* packed_w, int E, int h,
+                                      int F, int rows, const void* act_shared, int T, const void* packed_shared,
+                                      void* out_shared, int dtype, void* eout, void* stream) {
+    if (int rc = ffn_check("moe_expert_down_shared", act, tile_sched, packed_w, E, h, F, rows, dtype, eout)) return rc;
+    if (int rc = shared_check("moe_expert_down_shared", tile_sched, act_shared, T, packed_shared, out_shared, dtype))
+        return rc;
+    if (rows == 0 && T == 0) return MOE_OK;
+    return ffn_tc_down(act, tile_sched, packed_w, E, h, F, rows, eout, static_cast<cudaStream_t>(stream), act_shared, T,
+                       packed_shared, out_shared);
+}
+
 extern "C" size_t moe_expert_ffn_workspace_size(int rows, int F, int dtype) {
     if (rows < 0 || F <= 0) return 0;
     return align_up((size_t)rows * F * (dtype == MOE_F32 ? 4 : 2), 256);

@@ -26,11 +26,14 @@ int ffn_simt_up_gate(const void* buf, const int32_t* sched, const void* packed, 
 int ffn_simt_down(const void* act, const int32_t* sched, const void* packed, int E, int h, int F, int rows, int dtype,
                   void* eout, cudaStream_t s);
 
-// tcgen05 tensor-core path (bf16 operands, fp32 accumulation in tensor memory).
+// tcgen05 tensor-core path (bf16 operands, fp32 accumulation in tensor memory). With T_sh > 0 the same launch
+// also runs the shared expert (packed_sh, one expert) on its T_sh dense rows: x_sh -> act_sh, act_sh -> out_sh.
 int ffn_tc_up_gate(const void* buf, const int32_t* sched, const void* packed, int E, int h, int F, int rows, void* act,
-                   cudaStream_t s);
+                   cudaStream_t s, const void* x_sh = nullptr, int T_sh = 0, const void* packed_sh = nullptr,
+                   void* act_sh = nullptr);
 int ffn_tc_down(const void* act, const int32_t* sched, const void* packed, int E, int h, int F, int rows, void* eout,
-                cudaStream_t s);
+                cudaStream_t s, const void* act_sh = nullptr, int T_sh = 0, const void* packed_sh = nullptr,
+                void* out_sh = nullptr);
 
 // Router logits on the tensor cores (bf16 x and transposed router weight, fp32 logits + bias).
 int tc_router_logits(const void* x, const void* w_rT, const float* bias, int T, int h, int E, const int32_t* sched,

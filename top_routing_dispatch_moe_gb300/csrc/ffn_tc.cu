@@ -195,9 +195,21 @@ struct Params {
     const float* bias;  // EPI_F32: per-column bias or null
     unsigned* err;
     long long wait_limit;
+    int sh_rows;              // rows of the shared expert's dense group in the same launch (0: none)
+    __nv_bfloat16* sh_out;    // its output ([sh_rows, ldo])
 };
 
-struct Work { int e, row0, row1, n; };
+struct Work { int e, row0, row1, n, sh; };   // sh: the item belongs to the shared expert
+
+// Item w of the merged work list: the nr routed items first, then the ns shared-expert items. With the static
+// round-robin assignment of items to CTAs, the shorter shared items then fill the routed items' last partial
+// wave, and the shared tiles keep their L2 reuse (x rows across n-tiles, a weight tile across m-tiles), which
+// spreading them through the list loses. Returns the index within its own list in idx.
+__device__ __forceinline__ bool split_item(int w, int nr, int& idx) {
+    if (w < nr) { idx = w; return false; }
+    idx = w - nr;
+    return true;
+}
 
 // Work item w -> (expert, rows, n-tile), expert-major, n-tile next, m-tile fastest.
 __device__ __forceinline__ Work map_work(const int32_t* sched, int E, int NT, int w) {
@@ -212,14 +224,25 @@ __device__ __forceinline__ Work map_work(const int32_t* sched, int E, int NT, in
     const int local = w - p0 * NT;
     const int n = local / mt, m = p0 + local % mt;
     const int4 ent = __ldg(reinterpret_cast<const int4*>(sched + sched_tiles_offset(E)) + m);
-    return Work{ent.x, ent.y, ent.z, n};
+    return Work{ent.x, ent.y, ent.z, n, 0};
+}
+
+// Merged list of the one-SM kernel: routed items (map_work) and the shared expert's dense 128-row tiles,
+// n-tile major, m-tile fastest.
+__device__ __forceinline__ Work map_item(const Params& p, int E, int w, int nr) {
+    int idx;
+    if (!split_item(w, nr, idx)) return map_work(p.sched, E, p.NT, idx);
+    const int mt = (p.sh_rows + BM - 1) / BM;
+    const int n = idx / mt, row0 = (idx % mt) * BM;
+    return Work{0, row0, min(row0 + BM, p.sh_rows), n, 1};
 }
 
 // Epilogue of one accumulator: this thread's TMEM lane (one output row) -> SwiGLU of the packed gate/up
 // columns into bf16 act, a plain bf16 row, or an fp32 row (+ per-column bias), masked to the valid rows
 // and columns.
 template <int EPI, int BN>
-__device__ __forceinline__ void store_tile(const Params& p, uint32_t tbase, int row, bool live, int n) {
+__device__ __forceinline__ void store_tile(const Params& p, __nv_bfloat16* out, uint32_t tbase, int row, bool live,
+                                           int n) {
     if constexpr (EPI == EPI_SWIGLU) {
 #pragma unroll 1
         for (int j = 0; j < 4; ++j) {
@@ -228,7 +251,7 @@ __device__ __forceinline__ void store_tile(const Params& p, uint32_t tbase, int 
             tmem_ld32(tbase + 128 + 32 * j, u);
             const int f0 = n * 128 + 32 * j;
             if (live) {
-                __nv_bfloat16* dst = p.out + (size_t)row * p.ldo + f0;
+                __nv_bfloat16* dst = out + (size_t)row * p.ldo + f0;
 #pragma unroll
                 for (int c = 0; c < 32; c += 8) {
                     if (f0 + c < p.n_valid) {
@@ -271,7 +294,7 @@ __device__ __forceinline__ void store_tile(const Params& p, uint32_t tbase, int 
             tmem_ld32(tbase + 32 * j, v);
             const int n0 = n * BN + 32 * j;
             if (live) {
-                __nv_bfloat16* dst = p.out + (size_t)row * p.ldo + n0;
+                __nv_bfloat16* dst = out + (size_t)row * p.ldo + n0;
 #pragma unroll
                 for (int c = 0; c < 32; c += 8) {
                     if (n0 + c < p.n_valid) {
@@ -288,7 +311,8 @@ __device__ __forceinline__ void store_tile(const Params& p, uint32_t tbase, int 
 
 template <int EPI, class CF>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
-grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB, Params p) {
+grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                    const __grid_constant__ CUtensorMap tmA2, const __grid_constant__ CUtensorMap tmB2, Params p) {
     constexpr int BN = CF::BN, STAGES = CF::STAGES, B_BYTES = CF::B_BYTES, STAGE_BYTES = CF::STAGE_BYTES;
     constexpr uint32_t kIdesc = idesc_bf16<BN>();
     static_assert(EPI != EPI_SWIGLU || BN == 256, "the SwiGLU epilogue pairs 128 gate with 128 up columns");
@@ -316,6 +340,7 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
         prefetch_tmap(&tmA);
         prefetch_tmap(&tmB);
+        if (p.sh_rows) { prefetch_tmap(&tmA2); prefetch_tmap(&tmB2); }
     }
     if (warp == 1) tmem_alloc(smem_u32(tmem_slot), TMEM_COLS);
     tc_fence_before();
@@ -324,7 +349,9 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
     const uint32_t tmem = *tmem_slot;
 
     const int E = __ldg(p.sched + 1);
-    const int total = __ldg(p.sched) * p.NT;
+    const int nr = __ldg(p.sched) * p.NT;                        // routed items
+    const int ns = (p.sh_rows + BM - 1) / BM * p.NT;             // shared-expert items
+    const int total = nr + ns;
     const int KB = (p.K + BK - 1) / BK;
 
     if (warp == 0) {
@@ -333,14 +360,16 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
             int stage = 0;
             uint32_t phase = 0, issued = 0, last_par = 0;
             for (int w = blockIdx.x; w < total && !*abort_flag; w += gridDim.x) {
-                const Work wk = map_work(p.sched, E, p.NT, w);
+                const Work wk = map_item(p, E, w, nr);
                 const int brow = wk.e * p.b_rows + wk.n * BN;
+                const CUtensorMap* ma = wk.sh ? &tmA2 : &tmA;
+                const CUtensorMap* mb = wk.sh ? &tmB2 : &tmB;
                 bool ok = true;
                 for (int kb = 0; kb < KB; ++kb) {
                     if (!wait_phase(empty(stage), phase ^ 1u, p.wait_limit, abort_flag, p.err, 0x10u)) { ok = false; break; }
                     mbar_expect_tx(full(stage), STAGE_BYTES);
-                    tma_load_2d(sA + stage * A_BYTES, &tmA, kb * BK, wk.row0, full(stage));
-                    tma_load_2d(sB + stage * B_BYTES, &tmB, kb * BK, brow, full(stage));
+                    tma_load_2d(sA + stage * A_BYTES, ma, kb * BK, wk.row0, full(stage));
+                    tma_load_2d(sB + stage * B_BYTES, mb, kb * BK, brow, full(stage));
                     issued |= 1u << stage;
                     last_par = (last_par & ~(1u << stage)) | (phase << stage);
                     if (++stage == STAGES) { stage = 0; phase ^= 1u; }
@@ -389,11 +418,11 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
             const uint32_t aph = (iter >> 1) & 1;
             if (!wait_phase(tfull(a), aph, p.wait_limit, abort_flag, p.err, 0x30u)) break;
             tc_fence_after();
-            const Work wk = map_work(p.sched, E, p.NT, w);
+            const Work wk = map_item(p, E, w, nr);
             const int row = wk.row0 + lane_base + lane;
             const bool live = row < wk.row1;
             const uint32_t tbase = tmem + (uint32_t)(a * BN) + ((uint32_t)lane_base << 16);
-            store_tile<EPI, BN>(p, tbase, row, live, wk.n);
+            store_tile<EPI, BN>(p, wk.sh ? p.sh_out : p.out, tbase, row, live, wk.n);
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(tempty(a));
@@ -506,7 +535,7 @@ __device__ __forceinline__ void umma_commit_pair(uint32_t bar) {
                  : "memory");
 }
 
-struct PairWork { int e, arow, row0, row1, n; };   // arow: first row this CTA loads; [row0, row1): rows it stores
+struct PairWork { int e, arow, row0, row1, n, sh; };   // arow: first row this CTA loads; [row0, row1): rows it stores
 
 // Work item w -> (expert, n-tile, pair of 128-row tiles), expert-major, n-tile next, pair fastest; this CTA
 // (rank 0 or 1) takes the first or second tile of the pair. pp: per-expert prefix of pair counts.
@@ -524,12 +553,25 @@ __device__ __forceinline__ PairWork map_pair(const int32_t* sched, const int* pp
     const int t0 = __ldg(prefix + e), mt = __ldg(prefix + e + 1) - t0;
     const bool has = 2 * q + rank < mt;
     const int4 ent = __ldg(reinterpret_cast<const int4*>(sched + sched_tiles_offset(E)) + t0 + 2 * q + (has ? rank : 0));
-    return PairWork{ent.x, ent.y, has ? ent.y : 0, has ? ent.z : 0, n};
+    return PairWork{ent.x, ent.y, has ? ent.y : 0, has ? ent.z : 0, n, 0};
+}
+
+// Merged list of the 2-SM kernel: routed pair items and the shared expert's dense 256-row pairs (n-tile
+// major, pair fastest); a pair whose second tile starts past the shared rows is a phantom for rank 1.
+__device__ __forceinline__ PairWork map_pair_item(const Params& p, const int* pp, int E, int w, int nr, int rank) {
+    int idx;
+    if (!split_item(w, nr, idx)) return map_pair(p.sched, pp, E, p.NT, idx, rank);
+    const int np = (p.sh_rows + 2 * BM - 1) / (2 * BM);
+    const int n = idx / np, q = idx % np;
+    const int row0 = 2 * BM * q + BM * rank;
+    const bool has = row0 < p.sh_rows;
+    return PairWork{0, has ? row0 : 2 * BM * q, has ? row0 : 0, has ? min(row0 + BM, p.sh_rows) : 0, n, 1};
 }
 
 template <int EPI>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
-grouped_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB, Params p) {
+grouped_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                         const __grid_constant__ CUtensorMap tmA2, const __grid_constant__ CUtensorMap tmB2, Params p) {
     constexpr int BN = 256, STAGES = PAIR_STAGES;
     constexpr uint32_t kIdesc = idesc_bf16<BN, 2 * BM>();
     extern __shared__ uint8_t smem_raw[];
@@ -562,6 +604,7 @@ grouped_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_c
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
         prefetch_tmap(&tmA);
         prefetch_tmap(&tmB);
+        if (p.sh_rows) { prefetch_tmap(&tmA2); prefetch_tmap(&tmB2); }
     }
     if (warp == 2) {                         // pair prefix: pp[e + 1] = sum over e' <= e of ceil(tiles_e' / 2)
         const int32_t* prefix = p.sched + kSchedHeader;
@@ -587,7 +630,9 @@ grouped_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_c
     const uint32_t peer_abort = map_rank(smem_u32(const_cast<int*>(abort_flag)), rank ^ 1u);
 
     const int NC = gridDim.x >> 1, cid = blockIdx.x >> 1;
-    const int total = s_pp[E] * p.NT;
+    const int nr = s_pp[E] * p.NT;                                      // routed items
+    const int ns = (p.sh_rows + 2 * BM - 1) / (2 * BM) * p.NT;         // shared-expert items
+    const int total = nr + ns;
     const int KB = (p.K + BK - 1) / BK;
     int my_rounds = 0;
 
@@ -597,8 +642,10 @@ grouped_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_c
             int stage = 0;
             uint32_t phase = 0;
             for (int w = cid; w < total && !*abort_flag; w += NC) {
-                const PairWork wk = map_pair(p.sched, s_pp, E, p.NT, w, rank);
+                const PairWork wk = map_pair_item(p, s_pp, E, w, nr, rank);
                 const int brow = wk.e * p.b_rows + wk.n * BN + (int)rank * 128;
+                const CUtensorMap* ma = wk.sh ? &tmA2 : &tmA;
+                const CUtensorMap* mb = wk.sh ? &tmB2 : &tmB;
                 bool ok = true;
                 for (int kb = 0; kb < KB; ++kb) {
                     if (!wait_phase_pair(empty(stage), phase ^ 1u, p.wait_limit, abort_flag, peer_abort, p.err, 0x40u)) {
@@ -607,8 +654,8 @@ grouped_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_c
                     }
                     if (leader) mbar_expect_tx(full(stage), 2 * PAIR_STAGE_BYTES);
                     const uint32_t fb = map_rank(full(stage), 0);
-                    tma_load_2d_pair(sA + stage * A_BYTES, &tmA, kb * BK, wk.arow, fb);
-                    tma_load_2d_pair(sB + stage * B_HALF_BYTES, &tmB, kb * BK, brow, fb);
+                    tma_load_2d_pair(sA + stage * A_BYTES, ma, kb * BK, wk.arow, fb);
+                    tma_load_2d_pair(sB + stage * B_HALF_BYTES, mb, kb * BK, brow, fb);
                     ++my_rounds;
                     if (++stage == STAGES) { stage = 0; phase ^= 1u; }
                 }
@@ -659,11 +706,11 @@ grouped_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_c
             const uint32_t aph = (iter >> 1) & 1;
             if (!wait_phase_pair(tfull(a), aph, p.wait_limit, abort_flag, peer_abort, p.err, 0x60u)) break;
             tc_fence_after();
-            const PairWork wk = map_pair(p.sched, s_pp, E, p.NT, w, rank);
+            const PairWork wk = map_pair_item(p, s_pp, E, w, nr, rank);
             const int row = wk.row0 + lane_base + lane;
             const bool live = row < wk.row1;
             const uint32_t tbase = tmem + (uint32_t)(a * BN) + ((uint32_t)lane_base << 16);
-            store_tile<EPI, BN>(p, tbase, row, live, wk.n);
+            store_tile<EPI, BN>(p, wk.sh ? p.sh_out : p.out, tbase, row, live, wk.n);
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive_cluster(tempty_leader + 8u * a);
@@ -725,9 +772,13 @@ static int make_map(CUtensorMap* m, const void* base, long long rows, long long 
     return MOE_OK;
 }
 
+// A second operand set for the same launch: the shared expert's input rows and its packed weights
+// (p.sh_rows > 0); otherwise the routed maps are passed twice and never read through the second pair.
+struct SharedOperands { const void* a; const void* b; long long b_rows; };
+
 template <int EPI, class CF>
 static int gemm(const void* a, long long a_rows, const void* b, long long b_rows_total, const Params& p,
-                cudaStream_t s) {
+                cudaStream_t s, const SharedOperands& sh = SharedOperands{}) {
     static bool attr_set[64];                // the attribute belongs to the kernel in each device's context
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64)
@@ -738,10 +789,17 @@ static int gemm(const void* a, long long a_rows, const void* b, long long b_rows
         if (e != cudaSuccess) return set_error(MOE_ERR_CUDA, "grouped_gemm smem attribute: %s", cudaGetErrorString(e));
         attr_set[dev] = true;
     }
-    CUtensorMap ma, mb;
+    if (a_rows == 0) { a = sh.a; a_rows = p.sh_rows; b = sh.b; b_rows_total = sh.b_rows; }   // no routed items
+    CUtensorMap ma, mb, ma2, mb2;
     if (int rc = make_map(&ma, a, a_rows, p.K, BM)) return rc;
     if (int rc = make_map(&mb, b, b_rows_total, p.K, CF::BN)) return rc;
-    grouped_gemm_kernel<EPI, CF><<<num_sms(), NUM_THREADS, CF::SMEM_BYTES, s>>>(ma, mb, p);
+    ma2 = ma;
+    mb2 = mb;
+    if (p.sh_rows > 0) {
+        if (int rc = make_map(&ma2, sh.a, p.sh_rows, p.K, BM)) return rc;
+        if (int rc = make_map(&mb2, sh.b, sh.b_rows, p.K, CF::BN)) return rc;
+    }
+    grouped_gemm_kernel<EPI, CF><<<num_sms(), NUM_THREADS, CF::SMEM_BYTES, s>>>(ma, mb, ma2, mb2, p);
     return check_launch(EPI == EPI_SWIGLU ? "grouped_gemm_kernel<up_gate>"
                         : EPI == EPI_BF16 ? "grouped_gemm_kernel<down>" : "grouped_gemm_kernel<router>");
 }
@@ -749,7 +807,7 @@ static int gemm(const void* a, long long a_rows, const void* b, long long b_rows
 // 2-SM kernel: as many pairs as can be resident at once (one CTA per SM), each looping over work items.
 template <int EPI>
 static int gemm_pair(const void* a, long long a_rows, const void* b, long long b_rows_total, const Params& p,
-                     cudaStream_t s) {
+                     cudaStream_t s, const SharedOperands& sh = SharedOperands{}) {
     static int clusters[64];                 // resident pairs per device, 0 = not yet queried
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64)
@@ -768,10 +826,17 @@ static int gemm_pair(const void* a, long long a_rows, const void* b, long long b
             return set_error(MOE_ERR_CUDA, "grouped_gemm_pair: no resident cluster of two CTAs (%s)", cudaGetErrorString(e));
         clusters[dev] = std::min(n, num_sms() / 2);
     }
-    CUtensorMap ma, mb;
+    if (a_rows == 0) { a = sh.a; a_rows = p.sh_rows; b = sh.b; b_rows_total = sh.b_rows; }   // no routed items
+    CUtensorMap ma, mb, ma2, mb2;
     if (int rc = make_map(&ma, a, a_rows, p.K, BM)) return rc;
     if (int rc = make_map(&mb, b, b_rows_total, p.K, 128)) return rc;
-    grouped_gemm_pair_kernel<EPI><<<2 * clusters[dev], NUM_THREADS, PAIR_SMEM_BYTES, s>>>(ma, mb, p);
+    ma2 = ma;
+    mb2 = mb;
+    if (p.sh_rows > 0) {
+        if (int rc = make_map(&ma2, sh.a, p.sh_rows, p.K, BM)) return rc;
+        if (int rc = make_map(&mb2, sh.b, sh.b_rows, p.K, 128)) return rc;
+    }
+    grouped_gemm_pair_kernel<EPI><<<2 * clusters[dev], NUM_THREADS, PAIR_SMEM_BYTES, s>>>(ma, mb, ma2, mb2, p);
     return check_launch(EPI == EPI_SWIGLU ? "grouped_gemm_pair_kernel<up_gate>" : "grouped_gemm_pair_kernel<down>");
 }
 
@@ -782,28 +847,34 @@ static bool use_pair(int E, long long rows) { return E <= PAIR_MAX_E && rows >= 
 }  // namespace tc
 
 int ffn_tc_up_gate(const void* buf, const int32_t* sched, const void* packed, int E, int h, int F, int rows, void* act,
-                   cudaStream_t s) {
+                   cudaStream_t s, const void* x_sh, int T_sh, const void* packed_sh, void* act_sh) {
     const PackedLayout L = packed_layout(E, h, F, 2);
+    const PackedLayout Ls = packed_layout(1, h, F, 2);
     unsigned* err = device_error_word();
     MOE_REQUIRE(err, MOE_ERR_CUDA, "device error word unavailable");
     tc::Params p{sched, h, L.Fp / 128, 2 * L.Fp, F, F, static_cast<__nv_bfloat16*>(act), nullptr, nullptr, err,
-                 wait_limit()};
+                 wait_limit(), T_sh, static_cast<__nv_bfloat16*>(act_sh)};
     const char* b = static_cast<const char*>(packed) + L.up_gate_off;
-    if (tc::use_pair(E, rows)) return tc::gemm_pair<tc::EPI_SWIGLU>(buf, rows, b, (long long)E * 2 * L.Fp, p, s);
-    return tc::gemm<tc::EPI_SWIGLU, tc::Wide>(buf, rows, b, (long long)E * 2 * L.Fp, p, s);
+    const tc::SharedOperands sh{x_sh, packed_sh ? static_cast<const char*>(packed_sh) + Ls.up_gate_off : nullptr,
+                                2LL * Ls.Fp};
+    if (tc::use_pair(E, rows)) return tc::gemm_pair<tc::EPI_SWIGLU>(buf, rows, b, (long long)E * 2 * L.Fp, p, s, sh);
+    return tc::gemm<tc::EPI_SWIGLU, tc::Wide>(buf, rows, b, (long long)E * 2 * L.Fp, p, s, sh);
 }
 
 int ffn_tc_down(const void* act, const int32_t* sched, const void* packed, int E, int h, int F, int rows, void* eout,
-                cudaStream_t s) {
+                cudaStream_t s, const void* act_sh, int T_sh, const void* packed_sh, void* out_sh) {
     const PackedLayout L = packed_layout(E, h, F, 2);
+    const PackedLayout Ls = packed_layout(1, h, F, 2);
     unsigned* err = device_error_word();
     MOE_REQUIRE(err, MOE_ERR_CUDA, "device error word unavailable");
     using CF = tc::Wide;
     tc::Params p{sched, F, cdiv(h, CF::BN), h, h, h, static_cast<__nv_bfloat16*>(eout), nullptr, nullptr, err,
-                 wait_limit()};
+                 wait_limit(), T_sh, static_cast<__nv_bfloat16*>(out_sh)};
     const char* b = static_cast<const char*>(packed) + L.down_off;
-    if (tc::use_pair(E, rows)) return tc::gemm_pair<tc::EPI_BF16>(act, rows, b, (long long)E * h, p, s);
-    return tc::gemm<tc::EPI_BF16, CF>(act, rows, b, (long long)E * h, p, s);
+    const tc::SharedOperands sh{act_sh, packed_sh ? static_cast<const char*>(packed_sh) + Ls.down_off : nullptr,
+                                (long long)h};
+    if (tc::use_pair(E, rows)) return tc::gemm_pair<tc::EPI_BF16>(act, rows, b, (long long)E * h, p, s, sh);
+    return tc::gemm<tc::EPI_BF16, CF>(act, rows, b, (long long)E * h, p, s, sh);
 }
 
 // Router logits [T, E] fp32 = x [T, h] @ w_rT^T (+ bias), w_rT the K-major [E, h] copy of the router weight,
@@ -812,7 +883,7 @@ int tc_router_logits(const void* x, const void* w_rT, const float* bias, int T, 
                      float* logits, cudaStream_t s) {
     unsigned* err = device_error_word();
     MOE_REQUIRE(err, MOE_ERR_CUDA, "device error word unavailable");
-    tc::Params p{sched, h, cdiv(E, tc::Wide::BN), E, E, E, nullptr, logits, bias, err, wait_limit()};
+    tc::Params p{sched, h, cdiv(E, tc::Wide::BN), E, E, E, nullptr, logits, bias, err, wait_limit(), 0, nullptr};
     return tc::gemm<tc::EPI_F32, tc::Wide>(x, T, w_rT, E, p, s);
 }
 

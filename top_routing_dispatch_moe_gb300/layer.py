@@ -23,7 +23,8 @@ def capacity_slots(cf: float, k: int, T: int, E: int) -> int:
 class MoELayer:
     """Holds the packed expert weights, the router weight and every intermediate buffer of one layer.
 
-    Stages (in order): "router", "dispatch", "up_gate", "down", ["shared_up_gate", "shared_down"], "combine".
+    Stages (in order): "router", "dispatch", "up_gate", "down", ["shared_up_gate", "shared_down"], "combine". With
+    bf16 the shared expert runs inside the "up_gate" and "down" launches; the two shared stages exist for fp32.
     forward(x, events=...) records one CUDA event before the first stage and after each stage when given
     a dict of lists, so callers can time the stages on the launching stream."""
 
@@ -114,12 +115,22 @@ class MoELayer:
             moe.moe_dispatch(x, r["topk_ids"], self.E, self.C, self.R, out=self.d_out, ws=self.d_ws, stream=stream)
         mark("dispatch")
         sched = self.d_out["tile_sched"]
-        moe.moe_expert_up_gate(self.d_out["buf"], sched, self.packed, self.E, self.F, act=self.act, stream=stream)
-        mark("up_gate")
-        moe.moe_expert_down(self.act, sched, self.packed, self.E, self.h, eout=self.eout, stream=stream)
-        mark("down")
         shared_out = None
-        if self.shared_packed is not None:
+        if self.shared_packed is not None and self.dtype == torch.bfloat16:
+            # the shared expert's tiles run inside the routed experts' launches
+            moe.moe_expert_up_gate_shared(self.d_out["buf"], sched, self.packed, self.E, self.F, x, self.shared_packed,
+                                          act=self.act, act_shared=self.sh_act, stream=stream)
+            mark("up_gate")
+            moe.moe_expert_down_shared(self.act, sched, self.packed, self.E, self.h, self.sh_act, self.shared_packed,
+                                       eout=self.eout, out_shared=self.sh_out, stream=stream)
+            mark("down")
+            shared_out = self.sh_out
+        else:
+            moe.moe_expert_up_gate(self.d_out["buf"], sched, self.packed, self.E, self.F, act=self.act, stream=stream)
+            mark("up_gate")
+            moe.moe_expert_down(self.act, sched, self.packed, self.E, self.h, eout=self.eout, stream=stream)
+            mark("down")
+        if self.shared_packed is not None and shared_out is None:
             moe.moe_expert_up_gate(x, self.sh_sched, self.shared_packed, 1, self.F, act=self.sh_act, stream=stream)
             mark("shared_up_gate")
             moe.moe_expert_down(self.sh_act, self.sh_sched, self.shared_packed, 1, self.h, eout=self.sh_out,

@@ -43,6 +43,8 @@ _SIGS = {
     "moe_pack_expert_weights": (_I, [_P, _P, _P, _I, _I, _I, _I, _P, _P]),
     "moe_expert_up_gate": (_I, [_P, _P, _P, _I, _I, _I, _I, _I, _P, _P]),
     "moe_expert_down": (_I, [_P, _P, _P, _I, _I, _I, _I, _I, _P, _P]),
+    "moe_expert_up_gate_shared": (_I, [_P, _P, _P, _I, _I, _I, _I, _P, _I, _P, _P, _I, _P, _P]),
+    "moe_expert_down_shared": (_I, [_P, _P, _P, _I, _I, _I, _I, _P, _I, _P, _P, _I, _P, _P]),
     "moe_expert_ffn_workspace_size": (_Z, [_I, _I, _I]),
     "moe_expert_ffn": (_I, [_P, _P, _P, _I, _I, _I, _I, _I, _P, _P, _Z, _P]),
     "moe_combine": (_I, [_P, _P, _P, _P, _I, _I, _I, _I, _P, _P]),
@@ -293,6 +295,36 @@ def moe_expert_up_gate(buf, tile_sched, packed_w, E: int, F: int, act=None, stre
     _check(_lib.moe_expert_up_gate(_ptr(buf), _ptr(tile_sched), _ptr(packed_w), E, h, F, rows, dtype_code(buf.dtype),
                                    _ptr(act), _stream(stream)))
     return act
+
+
+def moe_expert_up_gate_shared(buf, tile_sched, packed_w, E: int, F: int, x, packed_shared, act=None, act_shared=None,
+                              stream=None):
+    """Routed up/gate GEMM and the shared expert's (x -> act_shared) in one launch (bf16)."""
+    rows, h = buf.shape
+    T = x.shape[0]
+    if act is None:
+        act = torch.empty((rows, F), dtype=buf.dtype, device=buf.device)
+    if act_shared is None:
+        act_shared = torch.empty((T, F), dtype=buf.dtype, device=buf.device)
+    _check(_lib.moe_expert_up_gate_shared(_ptr(buf), _ptr(tile_sched), _ptr(packed_w), E, h, F, rows, _ptr(x), T,
+                                          _ptr(packed_shared), _ptr(act_shared), dtype_code(buf.dtype), _ptr(act),
+                                          _stream(stream)))
+    return act, act_shared
+
+
+def moe_expert_down_shared(act, tile_sched, packed_w, E: int, h: int, act_shared, packed_shared, eout=None,
+                           out_shared=None, stream=None):
+    """Routed down GEMM and the shared expert's (act_shared -> out_shared) in one launch (bf16)."""
+    rows, F = act.shape
+    T = act_shared.shape[0]
+    if eout is None:
+        eout = torch.empty((rows, h), dtype=act.dtype, device=act.device)
+    if out_shared is None:
+        out_shared = torch.empty((T, h), dtype=act.dtype, device=act.device)
+    _check(_lib.moe_expert_down_shared(_ptr(act), _ptr(tile_sched), _ptr(packed_w), E, h, F, rows, _ptr(act_shared),
+                                       T, _ptr(packed_shared), _ptr(out_shared), dtype_code(act.dtype), _ptr(eout),
+                                       _stream(stream)))
+    return eout, out_shared
 
 
 def moe_expert_down(act, tile_sched, packed_w, E: int, h: int, eout=None, stream=None):
