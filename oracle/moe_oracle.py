@@ -19,7 +19,10 @@ Parity pins (tests/test_oracle_pins.py): shape table and C=1280 of [L7]; brute-f
 enumeration; sum of counts = k*T; brute-force loop dispatch; stable per-expert token order; identity
 experts giving y = sum gates*x (and y = x under renormalised gates); E=1,k=1 reducing to a dense SwiGLU
 FFN checked against scalar loops; aux = alpha exactly at a uniform split and >= alpha when f = P;
-FLOP and byte counts of [L7] "EP" (6.2 ms at 400 TFLOPS, 64 MiB per dispatch). No function is unpinned.
+FLOP and byte counts of [L7] "EP" (6.2 ms at 400 TFLOPS, 64 MiB per dispatch). The backward
+(combine_backward, swiglu_ffn_backward, route_backward, moe_layer_backward) is pinned by central differences
+of the forward in every gating mode with and without drops, a hand-derived 1 x 1 SwiGLU derivative, and zero
+gradients on dropped pairs and pad rows. No function is unpinned.
 """
 from __future__ import annotations
 
@@ -390,3 +393,114 @@ def route_selbias(L: np.ndarray, k: int, sel_bias: np.ndarray, alpha: float = 0.
     return dict(logits=L, ids=ids.astype(np.int32), gates=gates, counts=counts, f=f, P=P,
                 aux=alpha * E * float(np.sum(f * P)), prob=prob, score=score, gaps=top[:, :-1] - top[:, 1:],
                 sel_bias=np.asarray(sel_bias, np.float64))
+
+
+# ---------------------------------------------------------------------------------------------------------
+# backward of the layer ([EP7] "BWD（反向传播）": each expert computes its own weight gradients, and in the
+# overlap notes the gradients return to the experts along the routing path). The pages give no formulas;
+# reading: the chain rule through the forward above, with the top-k selection, the counts (hence f) and the
+# capacity drops held constant (piecewise constant in the inputs). Upstream gradients: dy for y and d_aux
+# for the aux loss, i.e. the gradient of <dy, y> + d_aux * aux.
+# ---------------------------------------------------------------------------------------------------------
+
+def combine_backward(dy: np.ndarray, eout: np.ndarray, dest_row: np.ndarray, gates: np.ndarray, rows: int):
+    """Through y[t] = sum_kept gate[t,j] eout[dest_row[t,j]]: d_eout[r] = gate[t,j] dy[t] on kept rows (zero on
+    pad rows); d_gates[t,j] = <dy[t], eout[dest_row[t,j]]> for kept pairs, 0 for dropped ones."""
+    T, k = dest_row.shape
+    d_eout = np.zeros((rows, dy.shape[1]), np.float64)
+    d_gates = np.zeros((T, k), np.float64)
+    for j in range(k):
+        kept = dest_row[:, j] >= 0
+        r = dest_row[kept, j]
+        d_eout[r] = gates[kept, j][:, None] * dy[kept]
+        d_gates[kept, j] = np.sum(dy[kept] * eout[r], axis=1)
+    return d_eout, d_gates
+
+
+def swiglu_ffn_backward(X: np.ndarray, w_gate, w_up, w_down, d_out: np.ndarray):
+    """Backward of out = (silu(G) * U) W_down^T with G = X W_gate^T, U = X W_up^T:
+    d_a = d_out W_down; dW_down = d_out^T a; dG = d_a * U * silu'(G) with silu'(z) = s(z) (1 + z (1 - s(z))),
+    s the logistic function; dU = d_a * silu(G); dX = dG W_gate + dU W_up; dW_gate = dG^T X; dW_up = dU^T X."""
+    X = np.asarray(X, np.float64)
+    G = X @ w_gate.T
+    U = X @ w_up.T
+    s = sigmoid(G)
+    a = G * s * U
+    d_a = d_out @ w_down
+    dG = d_a * U * s * (1.0 + G * (1.0 - s))
+    dU = d_a * G * s
+    return dict(dX=dG @ w_gate + dU @ w_up, dW_gate=dG.T @ X, dW_up=dU.T @ X, dW_down=d_out.T @ a,
+                d_a=d_a, dG=dG, dU=dU)
+
+
+def route_backward(L: np.ndarray, r: dict, d_gates: np.ndarray, gating: str, alpha: float, d_aux: float):
+    """d_logits from the gate gradients and the aux loss.
+    Gates (see `route`): softmax g_j = p[ids_j]; softmax_renorm g_j = p[ids_j] / S; sigmoid g_j = s[ids_j] / S
+    (S the sum over the k chosen). aux = alpha E sum_e f_e P_e with P_e = mean_t q[t, e], q = p (softmax modes)
+    or s / sum_e s (sigmoid mode), so d aux / d q[t, e] = alpha E f_e / T.
+    Softmax modes: dq -> dL by the softmax Jacobian dL = p * (dp - <dp, p>). Sigmoid mode: dq -> ds by the
+    Jacobian of s / sum(s), then dL = ds * s (1 - s)."""
+    T, E = L.shape
+    ids, gates, f = r["ids"], r["gates"], r["f"]
+    k = ids.shape[1]
+    rows = np.arange(T)[:, None]
+    c = d_aux * alpha * E * np.asarray(f, np.float64) / T          # d aux / d q[t, e], the same for every t
+    if gating == SIGMOID_BIAS_RENORM:
+        s = sigmoid(L)
+        ds = np.zeros((T, E))
+        Sk = s[rows, ids].sum(axis=1, keepdims=True)
+        dsk = (d_gates - np.sum(d_gates * gates, axis=1, keepdims=True)) / Sk
+        np.add.at(ds, (np.repeat(np.arange(T), k), ids.ravel()), dsk.ravel())
+        Ssum = s.sum(axis=1, keepdims=True)
+        q = s / Ssum
+        dq = np.broadcast_to(c[None, :], (T, E))
+        ds += (dq - np.sum(dq * q, axis=1, keepdims=True)) / Ssum
+        return ds * s * (1.0 - s)
+    p = softmax(L)
+    dp = np.zeros((T, E))
+    if gating == SOFTMAX:
+        np.add.at(dp, (np.repeat(np.arange(T), k), ids.ravel()), d_gates.ravel())
+    elif gating == SOFTMAX_RENORM:
+        Sk = p[rows, ids].sum(axis=1, keepdims=True)
+        dpk = (d_gates - np.sum(d_gates * gates, axis=1, keepdims=True)) / Sk
+        np.add.at(dp, (np.repeat(np.arange(T), k), ids.ravel()), dpk.ravel())
+    else:
+        raise ValueError(gating)
+    dp = dp + c[None, :]
+    return p * (dp - np.sum(dp * p, axis=1, keepdims=True))
+
+
+def moe_layer_backward(x, w_r, bias, weights, fwd: dict, dy, *, gating: str, alpha: float = 0.01,
+                       d_aux: float = 1.0, shared=None) -> dict:
+    """Gradients of <dy, y> + d_aux * aux for the forward `fwd` = moe_layer(...): dx, dW_r, d_bias (softmax
+    modes; the sigmoid-mode bias only selects and gets none), per-expert dW_gate / dW_up / dW_down, the shared
+    expert's, and the intermediate gradients (d_eout, d_gates, d_buf, d_logits)."""
+    x = np.asarray(x, np.float64)
+    dy = np.asarray(dy, np.float64)
+    r, d = fwd["router"], fwd["dispatch"]
+    E = np.asarray(w_r).shape[1]
+    d_eout, d_gates = combine_backward(dy, fwd["eout"], d["dest_row"], r["gates"], d["rows"])
+    d_buf = np.zeros_like(fwd["buf"], dtype=np.float64)
+    dW = []
+    for e in range(E):
+        n, o = int(d["kept_counts"][e]), int(d["offsets"][e])
+        wg, wu, wd = weights(e)
+        if n == 0:
+            dW.append((np.zeros_like(wg), np.zeros_like(wu), np.zeros_like(wd)))
+            continue
+        g = swiglu_ffn_backward(fwd["buf"][o:o + n], wg, wu, wd, d_eout[o:o + n])
+        d_buf[o:o + n] = g["dX"]
+        dW.append((g["dW_gate"], g["dW_up"], g["dW_down"]))
+    dx = np.zeros_like(x)
+    live = d["src_token"] >= 0
+    np.add.at(dx, d["src_token"][live], d_buf[live])                 # dispatch copied x[t] to each kept row
+    sh = None
+    if shared is not None:
+        sh = swiglu_ffn_backward(x, *shared(), dy)
+        dx += sh["dX"]
+    d_logits = route_backward(fwd["router"]["logits"], r, d_gates, gating, alpha, d_aux)
+    dx += d_logits @ np.asarray(w_r, np.float64).T
+    dW_r = x.T @ d_logits
+    d_bias = d_logits.sum(axis=0) if (bias is not None and gating != SIGMOID_BIAS_RENORM) else None
+    return dict(dx=dx, dW_r=dW_r, d_bias=d_bias, dW=dW, shared=sh, d_eout=d_eout, d_gates=d_gates, d_buf=d_buf,
+                d_logits=d_logits)

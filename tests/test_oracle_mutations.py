@@ -11,6 +11,7 @@ from tests import test_oracle_pins as P
 _route, _dispatch, _swiglu, _combine, _capacity = O.route, O.dispatch, O.swiglu_ffn, O.combine, O.capacity
 _ec = O.expert_choice
 _sk = O.sinkhorn_scaling
+_cbwd, _swbwd, _rbwd = O.combine_backward, O.swiglu_ffn_backward, O.route_backward
 
 
 def mut_renormalise_softmax(L, k, gating, bias=None, alpha=0.01):
@@ -117,13 +118,39 @@ def mut_sinkhorn_rows_first(L, n_iter=O.SINKHORN_ITERS):
     return c, r
 
 
+def mut_silu_prime_plain_sigmoid(X, w_gate, w_up, w_down, d_out):
+    """Takes silu'(z) = s(z), dropping the z s (1 - s) term."""
+    g = _swbwd(X, w_gate, w_up, w_down, d_out)
+    X = np.asarray(X, np.float64)
+    G, U = X @ w_gate.T, X @ w_up.T
+    s = O.sigmoid(G)
+    dG = g["d_a"] * U * s
+    g["dX"] = dG @ w_gate + g["dU"] @ w_up
+    g["dW_gate"] = dG.T @ X
+    return g
+
+
+def mut_route_backward_no_aux(L, r, d_gates, gating, alpha, d_aux):
+    return _rbwd(L, r, d_gates, gating, alpha, 0.0)
+
+
+def mut_route_backward_renorm_as_plain(L, r, d_gates, gating, alpha, d_aux):
+    return _rbwd(L, r, d_gates, O.SOFTMAX if gating == O.SOFTMAX_RENORM else gating, alpha, d_aux)
+
+
+def mut_combine_backward_no_gate(dy, eout, dest_row, gates, rows):
+    return _cbwd(dy, eout, dest_row, np.ones_like(gates), rows)
+
+
 MUTANTS = [
     ("route", mut_renormalise_softmax), ("route", mut_ascending_order), ("route", mut_bias_in_sigmoid_gates),
     ("route", mut_aux_denominator_T), ("dispatch", mut_drop_latest_first), ("dispatch", mut_dispatch_unstable),
     ("swiglu_ffn", mut_swap_gate_up), ("swiglu_ffn", mut_transpose_down), ("combine", mut_combine_no_gate),
     ("capacity", mut_capacity_floor_over_E), ("expert_choice", mut_ec_select_on_logits),
     ("expert_choice", mut_ec_ties_higher_token), ("sinkhorn_scaling", mut_sinkhorn_columns_only),
-    ("sinkhorn_scaling", mut_sinkhorn_rows_first),
+    ("sinkhorn_scaling", mut_sinkhorn_rows_first), ("swiglu_ffn_backward", mut_silu_prime_plain_sigmoid),
+    ("route_backward", mut_route_backward_no_aux), ("route_backward", mut_route_backward_renorm_as_plain),
+    ("combine_backward", mut_combine_backward_no_gate),
 ]
 
 PINS = [
@@ -136,6 +163,10 @@ PINS = [
     P.test_token_sampled_layer_matches_full_layer, lambda: P.test_expert_choice_brute_force(9, 4, 4),
     P.test_expert_choice_ties_take_lower_token, P.test_expert_choice_full_capacity_is_dense,
     P.test_sinkhorn_converges_to_doubly_stochastic, P.test_sinkhorn_closed_forms_and_balance,
+    lambda: P.test_backward_matches_finite_differences(O.SOFTMAX, 0.0),
+    lambda: P.test_backward_matches_finite_differences(O.SOFTMAX_RENORM, 0.6),
+    lambda: P.test_backward_matches_finite_differences(O.SIGMOID_BIAS_RENORM, 0.0),
+    P.test_swiglu_backward_scalar_closed_form, P.test_backward_dropped_pairs_and_pad_rows_get_zero,
 ]
 
 

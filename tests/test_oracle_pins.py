@@ -487,3 +487,95 @@ def test_sinkhorn_closed_forms_and_balance():
     # and the loads are far more even than plain top-1 on the shifted logits
     raw = O.route(L + np.arange(8)[None, :] * 3.0, 1, O.SOFTMAX)
     assert raw["counts"].max() > 150 and shifted["counts"].max() < 60
+
+
+# ------------------------------------------------------------------------------------------------ backward
+
+def _bwd_problem(gating, cf, seed=0, T=7, h=5, E=4, k=2, F=3):
+    rng = np.random.default_rng(seed)
+    x = rng.normal(size=(T, h))
+    w_r = rng.normal(size=(h, E))
+    bias = rng.normal(size=E) * 0.3
+    W = [(rng.normal(size=(F, h)), rng.normal(size=(F, h)), rng.normal(size=(h, F))) for _ in range(E)]
+    Ws = (rng.normal(size=(F, h)), rng.normal(size=(F, h)), rng.normal(size=(h, F)))
+    dy = rng.normal(size=(T, h))
+    return x, w_r, bias, W, Ws, dy, k
+
+
+@pytest.mark.parametrize("gating", [O.SOFTMAX, O.SOFTMAX_RENORM, O.SIGMOID_BIAS_RENORM])
+@pytest.mark.parametrize("cf", [0.0, 0.6])
+def test_backward_matches_finite_differences(gating, cf):
+    """Every gradient of <dy, y> + d_aux * aux (dx, dW_r, d_bias, each expert's three matrices, the shared
+    expert's) against central differences of the forward, which is pinned on its own (selection, counts and
+    drops do not move under a 1e-6 step at these random inputs)."""
+    x, w_r, bias, W, Ws, dy, k = _bwd_problem(gating, cf, seed=int(cf * 10) + len(gating))
+    alpha, d_aux = 0.3, 0.7
+
+    def loss(x, w_r, bias, W, Ws):
+        f = O.moe_layer(x, w_r, bias, lambda e: W[e], k=k, gating=gating, cf=cf, R=1, alpha=alpha,
+                        shared=lambda: Ws)
+        return float(np.sum(dy * f["y"]) + d_aux * f["router"]["aux"]), f
+
+    _, fwd = loss(x, w_r, bias, W, Ws)
+    g = O.moe_layer_backward(x, w_r, bias, lambda e: W[e], fwd, dy, gating=gating, alpha=alpha, d_aux=d_aux,
+                             shared=lambda: Ws)
+    eps = 1e-6
+
+    def check(got, perturb):
+        num = (loss(*perturb(eps))[0] - loss(*perturb(-eps))[0]) / (2 * eps)
+        assert abs(num - got) <= 1e-6 * max(1.0, abs(num)), (num, got)
+
+    def bump(a, idx, e):
+        b = a.copy()
+        b[idx] += e
+        return b
+
+    for idx in [(0, 0), (3, 2), (6, 4)]:
+        check(g["dx"][idx], lambda e: (bump(x, idx, e), w_r, bias, W, Ws))
+    for idx in [(0, 1), (4, 3), (2, 0)]:
+        check(g["dW_r"][idx], lambda e: (x, bump(w_r, idx, e), bias, W, Ws))
+    if gating != O.SIGMOID_BIAS_RENORM:
+        check(g["d_bias"][2], lambda e: (x, w_r, bump(bias, 2, e), W, Ws))
+    else:
+        assert g["d_bias"] is None
+    for ex in range(len(W)):
+        for m, idx in [(0, (1, 2)), (1, (2, 4)), (2, (3, 1))]:
+            def pert(e, ex=ex, m=m, idx=idx):
+                W2 = [list(w) for w in W]
+                W2[ex][m] = bump(W2[ex][m], idx, e)
+                return x, w_r, bias, [tuple(w) for w in W2], Ws
+            check(g["dW"][ex][m][idx], pert)
+    for m, idx in [(0, (0, 1)), (1, (2, 3)), (2, (4, 2))]:
+        def pert_s(e, m=m, idx=idx):
+            Ws2 = list(Ws)
+            Ws2[m] = bump(Ws2[m], idx, e)
+            return x, w_r, bias, W, tuple(Ws2)
+        check({0: g["shared"]["dW_gate"], 1: g["shared"]["dW_up"], 2: g["shared"]["dW_down"]}[m][idx], pert_s)
+
+
+def test_swiglu_backward_scalar_closed_form():
+    """h = F = 1: out = wd * silu(wg x) * (wu x), so d out / dx = wd (silu'(wg x) wg (wu x) + silu(wg x) wu)
+    with silu'(z) = s(z) + z s(z) (1 - s(z)), written out by hand."""
+    x, wg, wu, wd = 0.7, -1.3, 0.9, 2.1
+    z = wg * x
+    s = 1 / (1 + math.exp(-z))
+    silu_z, dsilu = z * s, s + z * s * (1 - s)
+    g = O.swiglu_ffn_backward(np.array([[x]]), np.array([[wg]]), np.array([[wu]]), np.array([[wd]]),
+                              np.array([[1.0]]))
+    assert g["dX"][0, 0] == pytest.approx(wd * (dsilu * wg * wu * x + silu_z * wu), rel=1e-12)
+    assert g["dW_gate"][0, 0] == pytest.approx(wd * dsilu * x * wu * x, rel=1e-12)
+    assert g["dW_up"][0, 0] == pytest.approx(wd * silu_z * x, rel=1e-12)
+    assert g["dW_down"][0, 0] == pytest.approx(silu_z * wu * x, rel=1e-12)
+
+
+def test_backward_dropped_pairs_and_pad_rows_get_zero():
+    """A dropped pair contributes nothing to y, so its gate gradient is 0; pad rows carry no gradient."""
+    x, w_r, _, W, Ws, dy, k = _bwd_problem(O.SOFTMAX, 1.0, seed=3, T=12, E=4)
+    bias = np.array([4.0, 0.0, 0.0, 0.0])            # every token picks expert 0: it overflows, the others pad
+    fwd = O.moe_layer(x, w_r, bias, lambda e: W[e], k=k, gating=O.SOFTMAX, cf=1.0, R=1)
+    d = fwd["dispatch"]
+    assert d["drop_mask"].any()
+    g = O.moe_layer_backward(x, w_r, bias, lambda e: W[e], fwd, dy, gating=O.SOFTMAX)
+    assert np.all(g["d_gates"][d["drop_mask"]] == 0)
+    pad = d["src_token"] < 0
+    assert pad.any() and np.all(g["d_eout"][pad] == 0) and np.all(g["d_buf"][pad] == 0)
