@@ -240,6 +240,55 @@ int moe_combine(const void* eout, const int32_t* dest_row, const float* gates, c
                 int h, int k, int dtype, void* y, void* stream);
 
 /* ---------------------------------------------------------------------------------------------------
+ * Backward of the layer ("专家并行" (formulaic), section "BWD（反向传播）" and the overlap notes: the
+ * gradients return to the experts along the routing path; each expert computes its own weight gradients).
+ * The pages give no formulas: these are the chain rule through the forward calls above with the top-k
+ * selection, the counts and the capacity drops held constant. Upstream gradients: dy for y and d_aux for the
+ * aux loss. Every reduction runs in a fixed order; all outputs are deterministic.
+ *
+ * moe_combine_backward: through moe_combine.
+ *   d_eout[r] = gates[t,j] * dy[t] for every kept row r (t = src_token[r], j = src_slot[r]), 0 on pad rows;
+ *   d_gates[t,j] = sum_d dy[t,d] * eout[dest_row[t,j], d] (fp32) for kept pairs, 0 for dropped ones.
+ *   dy [T,h], eout [rows,h], d_eout [rows,h] dtype; src_token/src_slot [rows], dest_row [T,k] from
+ *   moe_dispatch; gates [T,k] and d_gates [T,k] fp32. The shared expert's output gradient is dy itself.
+ * ------------------------------------------------------------------------------------------------- */
+int moe_combine_backward(const void* dy, const void* eout, const int32_t* src_token, const int32_t* src_slot,
+                         const int32_t* dest_row, const float* gates, int T, int h, int k, int rows, int dtype,
+                         void* d_eout, float* d_gates, void* stream);
+
+/* moe_router_backward: d_logits [T,E] fp32 from d_gates [T,k] and the aux loss, for the forward's logits,
+ *   topk_ids, gates and f (all as moe_router wrote them) and its gating mode and alpha.
+ *   With c_e = d_aux * alpha * E * f_e / T:
+ *     softmax / softmax_selbias: dp_e = sum_j [ids_j = e] d_g_j + c_e, d_logits = p * (dp - <dp, p>)
+ *     softmax_renorm: dp_e = sum_j [ids_j = e] (d_g_j - sum_i d_g_i g_i) / S + c_e (S = sum_j p[ids_j]), same
+ *     sigmoid_bias_renorm: ds_e = sum_j [ids_j = e] (d_g_j - sum_i d_g_i g_i) / S + (c_e - <c, q>) / sum(s),
+ *       q = s / sum(s), S = sum_j s[ids_j]; d_logits = ds * s * (1 - s)   (the selection bias gets none).
+ *   d_bias [E] fp32 (may be NULL) = sum over t of d_logits: the gradient of the bias the softmax modes add to
+ *   the logits. Workspace: moe_router_backward_workspace_size(T, E) bytes when d_bias is given. */
+size_t moe_router_backward_workspace_size(int T, int E);
+int moe_router_backward(const float* logits, const int32_t* topk_ids, const float* gates, const float* d_gates,
+                        const float* f, int T, int E, int k, int gating, float alpha, float d_aux, float* d_logits,
+                        float* d_bias, void* ws, size_t ws_bytes, void* stream);
+
+/* moe_router_weight_grad: dW_r [h,E] fp32 = x^T d_logits (x [T,h] dtype, d_logits [T,E] fp32), fp32
+ *   accumulation: per token slice, then the slices in order. Workspace:
+ *   moe_router_weight_grad_workspace_size(T, h, E) bytes. */
+size_t moe_router_weight_grad_workspace_size(int T, int h, int E);
+int moe_router_weight_grad(const void* x, const float* d_logits, int T, int h, int E, int dtype, float* dW_r,
+                           void* ws, size_t ws_bytes, void* stream);
+
+/* moe_dispatch_backward: through moe_dispatch and the router's x W_r.
+ *   dx[t] = dx_extra[t] + sum over kept j of d_buf[dest_row[t,j]] + sum_e d_logits[t,e] * W_r[:, e]
+ *   accumulated in fp32 in that order (j ascending, e ascending), rounded once to dtype. dx_extra [T,h] dtype
+ *   (e.g. the shared expert's input gradient) and d_logits may be NULL (their terms are then absent; w_r
+ *   is only read with d_logits). d_buf [rows,h], dx [T,h], w_r [h,E] dtype. Workspace (with d_logits):
+ *   moe_dispatch_backward_workspace_size(h, E, dtype) bytes, 16-byte aligned (W_r transposed). */
+size_t moe_dispatch_backward_workspace_size(int h, int E, int dtype);
+int moe_dispatch_backward(const void* d_buf, const int32_t* dest_row, const float* d_logits, const void* w_r,
+                          const void* dx_extra, int T, int h, int k, int E, int dtype, void* dx, void* ws,
+                          size_t ws_bytes, void* stream);
+
+/* ---------------------------------------------------------------------------------------------------
  * Errors and diagnostics.
  * ------------------------------------------------------------------------------------------------- */
 /* Message of the last failing call on this host thread ("" if none). */

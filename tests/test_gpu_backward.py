@@ -1,0 +1,119 @@
+"""GPU backward against the oracle's backward, element by element, on the same inputs.
+
+The forward runs on the GPU (router, dispatch, experts, combine); each backward call is then given the GPU's
+own forward results and checked against the oracle's backward function fed the same values (converted to
+float64): combine (d_eout, d_gates), router (d_logits, d_bias, through every gating mode, with the aux term),
+router weight (dW_r), dispatch (dx with the router term and an extra input gradient).
+
+Tolerances: fp32 results max-rel 1e-5 (fp32 sums against float64); outputs rounded to bf16 within half a bf16
+ulp of the reference's own value (rtol 2^-8) where they are one product, and normwise 4e-3 / max-rel 1e-2 where
+they are sums rounded once.
+"""
+import numpy as np
+import pytest
+
+import moe_inputs
+from oracle import moe_oracle as O
+from tests import cases
+
+pytestmark = pytest.mark.gpu
+
+CASES = {
+    "tiny_fp32": ("tiny_fp32", dict(T=300, cf=0.75), None),                       # softmax, capacity drops
+    "page3_small": ("page3_cf1.25", dict(T=300, h=256, F=128), None),             # softmax, capacity
+    "mixtral_small": ("mixtral_zipf", dict(T=400, h=256, F=128), "zipf"),         # renormalised, logit bias
+    "deepseek_small": ("deepseek_v3", dict(T=200, h=256, F=128, E=64, k=6, n_shared=0), None),   # sigmoid + bias
+}
+_cache = {}
+
+
+def _forward(name):
+    if name in _cache:
+        return _cache[name]
+    import torch
+    base, over, bias_kind = CASES[name]
+    cfg = moe_inputs.get_config(base, **over)
+    bias = moe_inputs.load_zipf_bias(moe_inputs.get_config("mixtral_zipf")) if bias_kind == "zipf" else None
+    inp = cases.router_inputs(cfg, bias=bias)
+    wg, wu, wd = moe_inputs.all_expert_weights(cfg)
+    layer = cases.build_gpu_layer(cfg, inp, wg, wu, wd)
+    x = cases.to_device(inp["x"], cfg)
+    layer.forward(x)
+    rng = np.random.default_rng(11)
+    dt = x.dtype
+    dy = torch.from_numpy(rng.normal(size=(cfg.T, cfg.h)).astype(np.float32)).to("cuda").to(dt)
+    torch.cuda.synchronize()
+    _cache[name] = (cfg, inp, layer, x, dy)
+    return _cache[name]
+
+
+def _np(t):
+    return t.detach().float().cpu().numpy().astype(np.float64)
+
+
+def _combine(name):
+    from top_routing_dispatch_moe_gb300 import moe
+    cfg, inp, layer, x, dy = _forward(name)
+    r, d = layer.r_out, layer.d_out
+    d_eout, d_gates = moe.moe_combine_backward(dy, layer.eout, d["src_token"], d["src_slot"], d["dest_row"], r["gates"])
+    ref_eout, ref_gates = O.combine_backward(_np(dy), _np(layer.eout), d["dest_row"].cpu().numpy(), _np(r["gates"]),
+                                             layer.rows)
+    return cfg, d_eout, d_gates, ref_eout, ref_gates
+
+
+@pytest.mark.parametrize("name", list(CASES))
+def test_combine_backward(name):
+    import torch
+    cfg, d_eout, d_gates, ref_eout, ref_gates = _combine(name)
+    torch.cuda.synchronize()
+    rtol = 2.0 ** -8 if cfg.dtype == "bf16" else 1e-6
+    np.testing.assert_allclose(_np(d_eout), ref_eout, rtol=rtol, atol=1e-30)
+    assert cases.rel_max(_np(d_gates), ref_gates) <= 1e-5
+
+
+@pytest.mark.parametrize("name", list(CASES))
+def test_router_backward_and_weight_grad(name):
+    import torch
+    from top_routing_dispatch_moe_gb300 import moe
+    cfg, inp, layer, x, dy = _forward(name)
+    _, _, d_gates, _, _ = _combine(name)
+    r = layer.r_out
+    alpha, d_aux = cfg.alpha, 0.7
+    d_logits, d_bias = moe.moe_router_backward(r["logits"], r["topk_ids"], r["gates"], d_gates, r["f"], cfg.gating,
+                                               alpha, d_aux)
+    dW_r = moe.moe_router_weight_grad(x, d_logits)
+    torch.cuda.synchronize()
+    rr = dict(ids=r["topk_ids"].cpu().numpy().astype(np.int64), gates=_np(r["gates"]), f=_np(r["f"]))
+    ref = O.route_backward(_np(r["logits"]), rr, _np(d_gates), cfg.gating, alpha, d_aux)
+    assert cases.rel_max(_np(d_logits), ref) <= 1e-5
+    assert cases.rel_max(_np(d_bias), ref.sum(axis=0)) <= 1e-5
+    ref_w = moe_inputs.to_f64(inp["x"], cfg.dtype).T @ _np(d_logits)
+    assert cases.rel_max(_np(dW_r), ref_w) <= 1e-5
+
+
+@pytest.mark.parametrize("name", list(CASES))
+def test_dispatch_backward(name):
+    import torch
+    from top_routing_dispatch_moe_gb300 import moe
+    cfg, inp, layer, x, dy = _forward(name)
+    d = layer.d_out
+    rng = np.random.default_rng(12)
+    dt = x.dtype
+    d_buf = torch.from_numpy(rng.normal(size=(layer.rows, cfg.h)).astype(np.float32)).to("cuda").to(dt)
+    extra = torch.from_numpy(rng.normal(size=(cfg.T, cfg.h)).astype(np.float32)).to("cuda").to(dt)
+    d_logits = torch.from_numpy(rng.normal(size=(cfg.T, cfg.E)).astype(np.float32)).to("cuda")
+    dx = moe.moe_dispatch_backward(d_buf, d["dest_row"], d_logits, layer.w_r, dx_extra=extra)
+    dx_plain = moe.moe_dispatch_backward(d_buf, d["dest_row"], None, layer.w_r)
+    torch.cuda.synchronize()
+    dest = d["dest_row"].cpu().numpy()
+    db = _np(d_buf)
+    plain = np.zeros((cfg.T, cfg.h))
+    for j in range(cfg.k):
+        kept = dest[:, j] >= 0
+        plain[kept] += db[dest[kept, j]]
+    ref = _np(extra) + plain + _np(d_logits) @ moe_inputs.to_f64(inp["w_r"], cfg.dtype).T
+    if cfg.dtype == "bf16":
+        assert cases.rel_l2(_np(dx), ref) <= 4e-3 and cases.rel_max(_np(dx), ref) <= 1e-2
+        assert cases.rel_l2(_np(dx_plain), plain) <= 4e-3
+    else:
+        assert cases.rel_max(_np(dx), ref) <= 1e-5 and cases.rel_max(_np(dx_plain), plain) <= 1e-5

@@ -44,6 +44,13 @@ _SIGS = {
     "moe_expert_up_gate": (_I, [_P, _P, _P, _I, _I, _I, _I, _I, _P, _P]),
     "moe_expert_down": (_I, [_P, _P, _P, _I, _I, _I, _I, _I, _P, _P]),
     "moe_expert_up_gate_shared": (_I, [_P, _P, _P, _I, _I, _I, _I, _P, _I, _P, _P, _I, _P, _P]),
+    "moe_combine_backward": (_I, [_P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _P, _P, _P]),
+    "moe_router_backward_workspace_size": (_Z, [_I, _I]),
+    "moe_router_backward": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _F, _F, _P, _P, _P, _Z, _P]),
+    "moe_router_weight_grad_workspace_size": (_Z, [_I, _I, _I]),
+    "moe_router_weight_grad": (_I, [_P, _P, _I, _I, _I, _I, _P, _P, _Z, _P]),
+    "moe_dispatch_backward_workspace_size": (_Z, [_I, _I, _I]),
+    "moe_dispatch_backward": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _P, _P, _Z, _P]),
     "moe_expert_down_shared": (_I, [_P, _P, _P, _I, _I, _I, _I, _P, _I, _P, _P, _I, _P, _P]),
     "moe_expert_ffn_workspace_size": (_Z, [_I, _I, _I]),
     "moe_expert_ffn": (_I, [_P, _P, _P, _I, _I, _I, _I, _I, _P, _P, _Z, _P]),
@@ -389,3 +396,62 @@ def moe_version() -> str:
 def raw_lib():
     """The ctypes handle (tests call entry points with raw pointers through it)."""
     return _lib
+
+
+# ------------------------------------------------------------------------------------------------ backward
+
+def moe_combine_backward(dy, eout, src_token, src_slot, dest_row, gates, d_eout=None, d_gates=None, stream=None):
+    T, h = dy.shape
+    rows = eout.shape[0]
+    k = dest_row.shape[1]
+    if d_eout is None:
+        d_eout = torch.empty((rows, h), dtype=dy.dtype, device=dy.device)
+    if d_gates is None:
+        d_gates = torch.empty((T, k), dtype=torch.float32, device=dy.device)
+    _check(_lib.moe_combine_backward(_ptr(dy), _ptr(eout), _ptr(src_token), _ptr(src_slot), _ptr(dest_row),
+                                     _ptr(gates), T, h, k, rows, dtype_code(dy.dtype), _ptr(d_eout), _ptr(d_gates),
+                                     _stream(stream)))
+    return d_eout, d_gates
+
+
+def moe_router_backward(logits, topk_ids, gates, d_gates, f, gating, alpha: float = 0.01, d_aux: float = 1.0, *,
+                        d_logits=None, want_bias_grad=True, ws=None, stream=None):
+    T, E = logits.shape
+    k = topk_ids.shape[1]
+    g = GATING[gating] if isinstance(gating, str) else int(gating)
+    if d_logits is None:
+        d_logits = torch.empty((T, E), dtype=torch.float32, device=logits.device)
+    d_bias = torch.empty(E, dtype=torch.float32, device=logits.device) if want_bias_grad else None
+    if ws is None:
+        ws = _bytes_tensor(_lib.moe_router_backward_workspace_size(T, E), logits.device)
+    _check(_lib.moe_router_backward(_ptr(logits), _ptr(topk_ids), _ptr(gates), _ptr(d_gates), _ptr(f), T, E, k, g,
+                                    alpha, d_aux, _ptr(d_logits), _ptr(d_bias), _ptr(ws), ws.numel(),
+                                    _stream(stream)))
+    return d_logits, d_bias
+
+
+def moe_router_weight_grad(x, d_logits, dW_r=None, ws=None, stream=None):
+    T, h = x.shape
+    E = d_logits.shape[1]
+    if dW_r is None:
+        dW_r = torch.empty((h, E), dtype=torch.float32, device=x.device)
+    if ws is None:
+        ws = _bytes_tensor(_lib.moe_router_weight_grad_workspace_size(T, h, E), x.device)
+    _check(_lib.moe_router_weight_grad(_ptr(x), _ptr(d_logits), T, h, E, dtype_code(x.dtype), _ptr(dW_r), _ptr(ws),
+                                       ws.numel(), _stream(stream)))
+    return dW_r
+
+
+def moe_dispatch_backward(d_buf, dest_row, d_logits, w_r, dx_extra=None, dx=None, ws=None, stream=None):
+    T, k = dest_row.shape
+    h = d_buf.shape[1]
+    E = w_r.shape[1]
+    if dx is None:
+        dx = torch.empty((T, h), dtype=d_buf.dtype, device=d_buf.device)
+    if ws is None and d_logits is not None:
+        ws = _bytes_tensor(_lib.moe_dispatch_backward_workspace_size(h, E, dtype_code(d_buf.dtype)), d_buf.device)
+    _check(_lib.moe_dispatch_backward(_ptr(d_buf), _ptr(dest_row), _ptr(d_logits), _ptr(w_r), _ptr(dx_extra), T, h, k,
+                                      E, dtype_code(d_buf.dtype), _ptr(dx), _ptr(ws),
+                                      ws.numel() if ws is not None else 0, _stream(stream)))
+    return dx
+
