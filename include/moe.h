@@ -1,5 +1,5 @@
 /*
- * moe.h: C ABI of the GB300 (sm_103a) MoE layer forward hot path.
+ * moe.h: C ABI of the GB300 (sm_103a) MoE layer forward hot path and its backward.
  *
  *   router -> dispatch -> grouped SwiGLU expert FFN -> combine
  *
@@ -287,6 +287,34 @@ size_t moe_dispatch_backward_workspace_size(int h, int E, int dtype);
 int moe_dispatch_backward(const void* d_buf, const int32_t* dest_row, const float* d_logits, const void* w_r,
                           const void* dx_extra, int T, int h, int k, int E, int dtype, void* dx, void* ws,
                           size_t ws_bytes, void* stream);
+
+/* Expert FFN backward (bf16, tcgen05 tensor cores; MOE_ERR_UNSUPPORTED for fp32). With g = buf W_gate^T,
+ * u = buf W_up^T, s the logistic of g and act = silu(g) u as in moe_expert_up_gate:
+ *   moe_pack_expert_weights_backward: one-time repack of the same three matrices as the dgrad GEMMs'
+ *     operands (moe_packed_weights_backward_bytes() bytes, opaque).
+ *   moe_expert_down_backward:    d_act [rows,F] = d_eout [rows,h] @ W_down[e]          for the kept rows
+ *   moe_expert_up_gate_backward: recomputes g and u, then
+ *     d_gu [rows, 2*Fp] (Fp = F rounded up to 128; columns in blocks of 256: 128 of d_g then the d_u of the same
+ *       f, f >= F zero): d_g = d_act * u * s * (1 + g (1 - s)), d_u = d_act * silu(g)
+ *     d_buf [rows,h] = d_g @ W_gate[e] + d_u @ W_up[e]
+ *   moe_expert_weight_grads: fp32 [E,F,h] dW_gate = d_g^T buf, dW_up = d_u^T buf, [E,h,F] dW_down = d_eout^T act
+ *     over each expert's kept rows [offsets[e], offsets[e] + kept_counts[e]) (zero for an expert without rows),
+ *     from buf, act (the forward's), d_gu and d_eout. Workspace: moe_expert_weight_grads_workspace_size()
+ *     bytes (each expert's rows transposed into a 64-aligned column segment).
+ *   Rows outside the kept ranges are not read (weight gradients) or not written (d_act, d_gu, d_buf). */
+size_t moe_packed_weights_backward_bytes(int E, int h, int F, int dtype);
+int moe_pack_expert_weights_backward(const void* w_gate, const void* w_up, const void* w_down, int E, int h, int F,
+                                     int dtype, void* packed_bwd, void* stream);
+int moe_expert_down_backward(const void* d_eout, const int32_t* tile_sched, const void* packed_bwd, int E, int h,
+                             int F, int rows, int dtype, void* d_act, void* stream);
+int moe_expert_up_gate_backward(const void* buf, const void* d_act, const int32_t* tile_sched, const void* packed_w,
+                                const void* packed_bwd, int E, int h, int F, int rows, int dtype, void* d_gu,
+                                void* d_buf, void* stream);
+size_t moe_expert_weight_grads_workspace_size(int E, int h, int F, int rows, int dtype);
+int moe_expert_weight_grads(const void* buf, const void* act, const void* d_gu, const void* d_eout,
+                            const int32_t* offsets, const int32_t* kept_counts, int E, int h, int F, int rows,
+                            int dtype, float* dW_gate, float* dW_up, float* dW_down, void* ws, size_t ws_bytes,
+                            void* stream);
 
 /* ---------------------------------------------------------------------------------------------------
  * Errors and diagnostics.

@@ -3,11 +3,13 @@
 The forward runs on the GPU (router, dispatch, experts, combine); each backward call is then given the GPU's
 own forward results and checked against the oracle's backward function fed the same values (converted to
 float64): combine (d_eout, d_gates), router (d_logits, d_bias, through every gating mode, with the aux term),
-router weight (dW_r), dispatch (dx with the router term and an extra input gradient).
+router weight (dW_r), dispatch (dx with the router term and an extra input gradient), and the expert FFN
+(d_act, d_g / d_u, d_buf, fp32 weight gradients) per expert against the oracle's SwiGLU backward.
 
 Tolerances: fp32 results max-rel 1e-5 (fp32 sums against float64); outputs rounded to bf16 within half a bf16
 ulp of the reference's own value (rtol 2^-8) where they are one product, and normwise 4e-3 / max-rel 1e-2 where
-they are sums rounded once.
+they are sums rounded once; the expert backward, whose intermediates (act, d_act, d_g / d_u) are bf16, normwise
+2e-2 like the layer output.
 """
 import numpy as np
 import pytest
@@ -117,3 +119,50 @@ def test_dispatch_backward(name):
         assert cases.rel_l2(_np(dx_plain), plain) <= 4e-3
     else:
         assert cases.rel_max(_np(dx), ref) <= 1e-5 and cases.rel_max(_np(dx_plain), plain) <= 1e-5
+
+
+@pytest.mark.parametrize("sizes", [[0, 1, 127, 129, 300], [0, 257, 1900, 40]])
+def test_expert_backward(sizes):
+    """Expert FFN backward per expert against the oracle's SwiGLU backward on the same bf16 operands: d_act,
+    the packed d_g / d_u, d_buf and the fp32 weight gradients (zero for an expert without rows). F = 320 leaves a
+    zero-padded part of the last 128-column block. The second size list has rows >= 512 E, so the dgrad GEMMs run
+    on the 2-SM kernel; the weight gradients always run on the one-SM kernel."""
+    import torch
+    from top_routing_dispatch_moe_gb300 import moe
+    torch.manual_seed(7)
+    dev = "cuda"
+    E, h, F = len(sizes), 256, 320
+    Fp = (F + 127) // 128 * 128
+    ids = np.concatenate([np.full(n, e, np.int32) for e, n in enumerate(sizes)])
+    np.random.default_rng(3).shuffle(ids)
+    x = torch.randn(ids.size, h, device=dev).to(torch.bfloat16)
+    d = moe.moe_dispatch(x, torch.from_numpy(ids[:, None]).to(dev), E, 0, 1)
+    mk = lambda *s: (torch.randn(*s, device=dev) / s[-1] ** 0.5).to(torch.bfloat16)
+    wg, wu, wd = mk(E, F, h), mk(E, F, h), mk(E, h, F)
+    packed = moe.moe_pack_expert_weights(wg, wu, wd)
+    packed_bwd = moe.moe_pack_expert_weights_backward(wg, wu, wd)
+    buf, sched = d["buf"], d["tile_sched"]
+    act = moe.moe_expert_up_gate(buf, sched, packed, E, F)
+    d_eout = torch.randn(buf.shape[0], h, device=dev).to(torch.bfloat16)
+    d_act = moe.moe_expert_down_backward(d_eout, sched, packed_bwd, E, F)
+    d_gu, d_buf = moe.moe_expert_up_gate_backward(buf, d_act, sched, packed, packed_bwd, E)
+    dWg, dWu, dWd = moe.moe_expert_weight_grads(buf, act, d_gu, d_eout, d["offsets"], d["kept_counts"], E)
+    torch.cuda.synchronize()
+    assert moe.moe_check_device_error() == moe.MOE_OK, moe.moe_last_error_string()
+    off = d["offsets"].cpu().tolist()
+    f64 = lambda t: t.double().cpu().numpy()
+    for e in range(E):
+        a, b = off[e], off[e + 1]
+        if a == b:
+            assert not dWg[e].any() and not dWu[e].any() and not dWd[e].any()
+            continue
+        g = O.swiglu_ffn_backward(f64(buf[a:b]), f64(wg[e]), f64(wu[e]), f64(wd[e]), f64(d_eout[a:b]))
+        gu = f64(d_gu[a:b]).reshape(b - a, Fp // 128, 2, 128)
+        dG = gu[:, :, 0, :].reshape(b - a, Fp)
+        dU = gu[:, :, 1, :].reshape(b - a, Fp)
+        assert np.all(dG[:, F:] == 0) and np.all(dU[:, F:] == 0)
+        for got, ref, what in [(f64(d_act[a:b]), g["d_a"], "d_act"), (dG[:, :F], g["dG"], "d_g"),
+                               (dU[:, :F], g["dU"], "d_u"), (f64(d_buf[a:b]), g["dX"], "d_buf"),
+                               (f64(dWg[e]), g["dW_gate"], "dW_gate"), (f64(dWu[e]), g["dW_up"], "dW_up"),
+                               (f64(dWd[e]), g["dW_down"], "dW_down")]:
+            assert cases.rel_l2(got, ref) <= 2e-2, f"expert {e} ({b - a} rows): {what} rel err {cases.rel_l2(got, ref):.3e}"

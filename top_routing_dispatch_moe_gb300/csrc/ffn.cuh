@@ -20,6 +20,24 @@ inline PackedLayout packed_layout(int E, int h, int F, int el) {
     return L;
 }
 
+// Backward packing: W_down^T [E][F][h], then W_gu^T [E][h][2Fp] (columns in the forward's packed order) from the
+// next 256-byte boundary.
+struct PackedBwdLayout {
+    int Fp;
+    size_t down_t_off;
+    size_t gu_t_off;
+    size_t total_bytes;
+};
+
+inline PackedBwdLayout packed_bwd_layout(int E, int h, int F, int el) {
+    PackedBwdLayout L;
+    L.Fp = (F + 127) / 128 * 128;
+    L.down_t_off = 0;
+    L.gu_t_off = align_up((size_t)E * F * h * el, 256);
+    L.total_bytes = L.gu_t_off + (size_t)E * h * 2 * L.Fp * el;
+    return L;
+}
+
 // CUDA-core path (fp32; the reference-precision path of the library).
 int ffn_simt_up_gate(const void* buf, const int32_t* sched, const void* packed, int E, int h, int F, int rows, int dtype,
                      void* act, cudaStream_t s);
@@ -34,6 +52,16 @@ int ffn_tc_up_gate(const void* buf, const int32_t* sched, const void* packed, in
 int ffn_tc_down(const void* act, const int32_t* sched, const void* packed, int E, int h, int F, int rows, void* eout,
                 cudaStream_t s, const void* act_sh = nullptr, int T_sh = 0, const void* packed_sh = nullptr,
                 void* out_sh = nullptr);
+
+// Backward on the tensor cores (bf16): down dgrad; up/gate recompute with the SwiGLU backward epilogue, then
+// the up/gate dgrad; the experts' weight gradients from K-major transposed operands.
+int ffn_tc_down_backward(const void* d_eout, const int32_t* sched, const void* packed_bwd, int E, int h, int F,
+                         int rows, void* d_act, cudaStream_t s);
+int ffn_tc_up_gate_backward(const void* buf, const void* d_act, const int32_t* sched, const void* packed,
+                            const void* packed_bwd, int E, int h, int F, int rows, void* d_gu, void* d_buf,
+                            cudaStream_t s);
+int ffn_tc_weight_grad(const void* At, const void* Bt, long long ktot, const int32_t* seg, int E, int M, int N, int gu,
+                       int F, float* out, float* out2, cudaStream_t s);
 
 // Router logits on the tensor cores (bf16 x and transposed router weight, fp32 logits + bias).
 int tc_router_logits(const void* x, const void* w_rT, const float* bias, int T, int h, int E, const int32_t* sched,

@@ -1,0 +1,154 @@
+// Backward of the grouped SwiGLU expert FFN: C-ABI entry points, the weight-gradient operand transposes.
+//
+// "专家并行" (formulaic), section "BWD（反向传播）": each GPU first computes the gradients of its own experts'
+// weights. The chain rule through the forward (ffn_tc.cu) with g = x W_gate^T, u = x W_up^T, a = silu(g) u:
+//   d_act = d_eout W_down;  d_g = d_act u s (1 + g (1 - s)), d_u = d_act silu(g)  (s the logistic of g);
+//   d_buf = d_g W_gate + d_u W_up;  dW_down = d_eout^T act;  dW_gate = d_g^T buf;  dW_up = d_u^T buf.
+// All GEMMs run on the tcgen05 grouped kernels. The weight gradients contract over each expert's rows: those
+// rows are transposed into K-major column segments, one per expert, each padded with zeros to a multiple of 64
+// columns, so the GEMM's K loop of expert e covers exactly its rows.
+#include <algorithm>
+#include "ffn.cuh"
+
+namespace moe {
+
+constexpr int kSegAlign = 64;
+
+// seg[0] = 0, seg[e + 1] = seg[e] + kept[e] rounded up to 64 (one warp, 32 experts per step).
+__global__ void seg_offsets_kernel(const int32_t* __restrict__ kept, int E, int32_t* __restrict__ seg) {
+    const int lane = threadIdx.x;
+    int carry = 0;
+    if (lane == 0) seg[0] = 0;
+    for (int base = 0; base < E; base += 32) {
+        const int e = base + lane;
+        int v = e < E ? (kept[e] + kSegAlign - 1) / kSegAlign * kSegAlign : 0;
+#pragma unroll
+        for (int off = 1; off < 32; off <<= 1) {
+            const int t = __shfl_up_sync(0xffffffffu, v, off);
+            if (lane >= off) v += t;
+        }
+        if (e < E) seg[e + 1] = carry + v;
+        carry += __shfl_sync(0xffffffffu, v, 31);
+    }
+}
+
+// dst [C][ktot]: column k of expert e's segment [seg[e], seg[e+1]) holds row offsets[e] + (k - seg[e]) of
+// src [rows][C] while k - seg[e] < kept[e], zero after it. 64 x 64 tiles through shared memory; a 64-column
+// tile of dst lies in one expert's segment (segments are 64-aligned).
+template <typename T>
+__global__ void __launch_bounds__(256)
+segment_transpose_kernel(const T* __restrict__ src, int C, const int32_t* __restrict__ offsets,
+                         const int32_t* __restrict__ kept, const int32_t* __restrict__ seg, int E, long long ktot,
+                         T* __restrict__ dst) {
+    __shared__ T tile[64][65];
+    const int k0 = blockIdx.x * 64;
+    if (k0 >= seg[E]) return;                 // the grid covers the largest possible ktot
+    int lo = 0, hi = E - 1;                   // last e with seg[e] <= k0
+    while (lo < hi) {
+        const int mid = (lo + hi + 1) >> 1;
+        if (seg[mid] <= k0) lo = mid; else hi = mid - 1;
+    }
+    const int e = lo, local0 = k0 - seg[e], n = kept[e], r0 = offsets[e];
+    const int c0 = blockIdx.y * 64;
+    for (int i = threadIdx.y; i < 64; i += blockDim.y) {
+        const int local = local0 + i, c = c0 + threadIdx.x;
+        tile[i][threadIdx.x] = (local < n && c < C) ? src[(size_t)(r0 + local) * C + c] : T(0.f);
+    }
+    __syncthreads();
+    for (int c = threadIdx.y; c < 64; c += blockDim.y)
+        if (c0 + c < C) dst[(size_t)(c0 + c) * ktot + k0 + threadIdx.x] = tile[threadIdx.x][c];
+}
+
+// Column extent of the transposed operands: every expert's rows rounded up to 64, at most rows + 63 E.
+static long long grads_ktot(int rows, int E) {
+    return ((long long)rows + (long long)(kSegAlign - 1) * E + kSegAlign - 1) / kSegAlign * kSegAlign;
+}
+
+struct GradsWs { int32_t* seg; void* d_eout_t; void* act_t; void* d_gu_t; void* buf_t; long long ktot; size_t bytes; };
+
+static GradsWs grads_ws_layout(void* ws, int E, int h, int F, int rows) {
+    GradsWs w{};
+    const int Fp = (F + 127) / 128 * 128;
+    w.ktot = grads_ktot(rows, E);
+    char* base = static_cast<char*>(ws);
+    size_t off = 0;
+    w.seg = reinterpret_cast<int32_t*>(base + off); off = align_up(off + (size_t)(E + 1) * 4, 256);
+    w.d_eout_t = base + off; off = align_up(off + (size_t)h * w.ktot * 2, 256);
+    w.act_t = base + off;    off = align_up(off + (size_t)F * w.ktot * 2, 256);
+    w.d_gu_t = base + off;   off = align_up(off + (size_t)2 * Fp * w.ktot * 2, 256);
+    w.buf_t = base + off;    off = align_up(off + (size_t)h * w.ktot * 2, 256);
+    w.bytes = off;
+    return w;
+}
+
+static int bwd_ffn_check(const char* fn, int E, int h, int F, int rows, int dtype) {
+    MOE_REQUIRE(dtype == MOE_BF16, MOE_ERR_UNSUPPORTED, "%s: bf16 only (the tensor-core path)", fn);
+    MOE_REQUIRE(E >= 1 && E <= 1024 && h > 0 && F > 0 && h % 8 == 0 && F % 8 == 0 && rows >= 0, MOE_ERR_INVALID_ARG,
+                "%s: E=%d h=%d F=%d rows=%d (need h%%8==0, F%%8==0)", fn, E, h, F, rows);
+    return MOE_OK;
+}
+
+}  // namespace moe
+
+using namespace moe;
+
+extern "C" int moe_expert_down_backward(const void* d_eout, const int32_t* tile_sched, const void* packed_bwd, int E,
+                                        int h, int F, int rows, int dtype, void* d_act, void* stream) {
+    if (int rc = bwd_ffn_check("moe_expert_down_backward", E, h, F, rows, dtype)) return rc;
+    if (rows == 0) return MOE_OK;
+    MOE_REQUIRE(d_eout && tile_sched && packed_bwd && d_act, MOE_ERR_INVALID_ARG, "moe_expert_down_backward: null pointer");
+    MOE_REQUIRE(aligned16(d_eout) && aligned16(tile_sched) && aligned16(packed_bwd) && aligned16(d_act),
+                MOE_ERR_INVALID_ARG, "moe_expert_down_backward: pointers must be 16-byte aligned");
+    return ffn_tc_down_backward(d_eout, tile_sched, packed_bwd, E, h, F, rows, d_act, static_cast<cudaStream_t>(stream));
+}
+
+extern "C" int moe_expert_up_gate_backward(const void* buf, const void* d_act, const int32_t* tile_sched,
+                                           const void* packed_w, const void* packed_bwd, int E, int h, int F, int rows,
+                                           int dtype, void* d_gu, void* d_buf, void* stream) {
+    if (int rc = bwd_ffn_check("moe_expert_up_gate_backward", E, h, F, rows, dtype)) return rc;
+    if (rows == 0) return MOE_OK;
+    MOE_REQUIRE(buf && d_act && tile_sched && packed_w && packed_bwd && d_gu && d_buf, MOE_ERR_INVALID_ARG,
+                "moe_expert_up_gate_backward: null pointer");
+    MOE_REQUIRE(aligned16(buf) && aligned16(d_act) && aligned16(tile_sched) && aligned16(packed_w) &&
+                    aligned16(packed_bwd) && aligned16(d_gu) && aligned16(d_buf),
+                MOE_ERR_INVALID_ARG, "moe_expert_up_gate_backward: pointers must be 16-byte aligned");
+    return ffn_tc_up_gate_backward(buf, d_act, tile_sched, packed_w, packed_bwd, E, h, F, rows, d_gu, d_buf,
+                                   static_cast<cudaStream_t>(stream));
+}
+
+extern "C" size_t moe_expert_weight_grads_workspace_size(int E, int h, int F, int rows, int dtype) {
+    if (E <= 0 || h <= 0 || F <= 0 || rows < 0 || dtype != MOE_BF16) return 0;
+    return grads_ws_layout(nullptr, E, h, F, rows).bytes;
+}
+
+extern "C" int moe_expert_weight_grads(const void* buf, const void* act, const void* d_gu, const void* d_eout,
+                                       const int32_t* offsets, const int32_t* kept_counts, int E, int h, int F, int rows,
+                                       int dtype, float* dW_gate, float* dW_up, float* dW_down, void* ws,
+                                       size_t ws_bytes, void* stream) {
+    if (int rc = bwd_ffn_check("moe_expert_weight_grads", E, h, F, rows, dtype)) return rc;
+    MOE_REQUIRE(offsets && kept_counts && dW_gate && dW_up && dW_down &&
+                    (rows == 0 || (buf && act && d_gu && d_eout)),
+                MOE_ERR_INVALID_ARG, "moe_expert_weight_grads: null pointer");
+    MOE_REQUIRE(aligned16(dW_gate) && aligned16(dW_up) && aligned16(dW_down) && aligned16(ws), MOE_ERR_INVALID_ARG,
+                "moe_expert_weight_grads: pointers must be 16-byte aligned");
+    const GradsWs w = grads_ws_layout(ws, E, h, F, rows);
+    MOE_REQUIRE(ws && ws_bytes >= w.bytes, MOE_ERR_WORKSPACE, "moe_expert_weight_grads: workspace %zu < %zu", ws_bytes,
+                w.bytes);
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    const int Fp = (F + 127) / 128 * 128;
+    seg_offsets_kernel<<<1, 32, 0, s>>>(kept_counts, E, w.seg);
+    if (int rc = check_launch("seg_offsets_kernel")) return rc;
+    using B = __nv_bfloat16;
+    const dim3 block(64, 4);
+    const int kt = (int)(w.ktot / 64);
+    struct { const void* src; int C; void* dst; } tr[4] = {
+        {d_eout, h, w.d_eout_t}, {act, F, w.act_t}, {d_gu, 2 * Fp, w.d_gu_t}, {buf, h, w.buf_t}};
+    for (auto& t : tr) {
+        segment_transpose_kernel<B><<<dim3(kt, cdiv(t.C, 64)), block, 0, s>>>(
+            static_cast<const B*>(t.src), t.C, offsets, kept_counts, w.seg, E, w.ktot, static_cast<B*>(t.dst));
+        if (int rc = check_launch("segment_transpose_kernel")) return rc;
+    }
+    // dW_down[e] [h][F] = d_eout_e^T act_e ; dW_gate / dW_up [E][F][h] from d_gu_e^T buf_e (packed rows)
+    if (int rc = ffn_tc_weight_grad(w.d_eout_t, w.act_t, w.ktot, w.seg, E, h, F, 0, F, dW_down, nullptr, s)) return rc;
+    return ffn_tc_weight_grad(w.d_gu_t, w.buf_t, w.ktot, w.seg, E, 2 * Fp, h, 1, F, dW_gate, dW_up, s);
+}

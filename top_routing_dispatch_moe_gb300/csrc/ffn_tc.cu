@@ -180,8 +180,9 @@ __host__ __device__ constexpr uint32_t idesc_bf16() {
 }
 
 // Epilogues: SwiGLU of the packed gate/up tile -> bf16 act; plain bf16 conversion; fp32 (+ per-column bias),
-// used for the router logits.
-enum Epi : int { EPI_SWIGLU = 0, EPI_BF16 = 1, EPI_F32 = 2 };
+// used for the router logits and the weight gradients; SwiGLU backward of the packed gate/up tile (reads the
+// act gradient, writes the gate and up pre-activation gradients in the packed column order).
+enum Epi : int { EPI_SWIGLU = 0, EPI_BF16 = 1, EPI_F32 = 2, EPI_SWIGLU_BWD = 3 };
 
 struct Params {
     const int32_t* sched;
@@ -197,9 +198,19 @@ struct Params {
     long long wait_limit;
     int sh_rows;              // rows of the shared expert's dense group in the same launch (0: none)
     __nv_bfloat16* sh_out;    // its output ([sh_rows, ldo])
+    const __nv_bfloat16* d_act;   // EPI_SWIGLU_BWD: act gradient [rows, n_valid]
+    // weight-gradient mapping (wg_E > 0, one-SM kernel): item = (expert e, n-tile, m-tile), A rows m-tile of
+    // wg_M rows, B rows n-tile, K = expert e's segment [seg[e], seg[e + 1]) of the transposed operands.
+    int wg_E, wg_MT, wg_M;
+    const int32_t* seg;
+    int wg_gu;                // rows are the packed gate/up order: block b of 128 rows -> out_f32 (gate, b even)
+                              // or out2 (up, b odd), row (b / 2) * 128 + i of expert e's [F][ldo] matrix
+    int wg_F;                 // wg_gu: valid rows F of each de-interleaved matrix
+    float* out2;
 };
 
-struct Work { int e, row0, row1, n, sh; };   // sh: the item belongs to the shared expert
+// sh: the item belongs to the shared expert; K steps kb0 .. kb0 + nkb of BK columns starting at column kx0
+struct Work { int e, row0, row1, n, sh, kx0, nkb; };
 
 // Item w of the merged work list: the nr routed items first, then the ns shared-expert items. With the static
 // round-robin assignment of items to CTAs, the shorter shared items then fill the routed items' last partial
@@ -224,17 +235,28 @@ __device__ __forceinline__ Work map_work(const int32_t* sched, int E, int NT, in
     const int local = w - p0 * NT;
     const int n = local / mt, m = p0 + local % mt;
     const int4 ent = __ldg(reinterpret_cast<const int4*>(sched + sched_tiles_offset(E)) + m);
-    return Work{ent.x, ent.y, ent.z, n, 0};
+    return Work{ent.x, ent.y, ent.z, n, 0, 0, 0};
 }
 
 // Merged list of the one-SM kernel: routed items (map_work) and the shared expert's dense 128-row tiles,
 // n-tile major, m-tile fastest.
-__device__ __forceinline__ Work map_item(const Params& p, int E, int w, int nr) {
+__device__ __forceinline__ Work map_item(const Params& p, int E, int w, int nr, int KB) {
     int idx;
-    if (!split_item(w, nr, idx)) return map_work(p.sched, E, p.NT, idx);
+    if (p.wg_E > 0) {                        // weight gradient: expert-major, n-tile next, m-tile fastest
+        const int per_e = p.wg_MT * p.NT;
+        const int e = w / per_e, rem = w - e * per_e;
+        const int n = rem / p.wg_MT, m = rem - n * p.wg_MT;
+        const int k0 = __ldg(p.seg + e), k1 = __ldg(p.seg + e + 1);
+        return Work{e, m * BM, min(m * BM + BM, p.wg_M), n, 0, k0, (k1 - k0) / BK};
+    }
+    if (!split_item(w, nr, idx)) {
+        Work wk = map_work(p.sched, E, p.NT, idx);
+        wk.nkb = KB;
+        return wk;
+    }
     const int mt = (p.sh_rows + BM - 1) / BM;
     const int n = idx / mt, row0 = (idx % mt) * BM;
-    return Work{0, row0, min(row0 + BM, p.sh_rows), n, 1};
+    return Work{0, row0, min(row0 + BM, p.sh_rows), n, 1, 0, KB};
 }
 
 // Epilogue of one accumulator: this thread's TMEM lane (one output row) -> SwiGLU of the packed gate/up
@@ -242,8 +264,36 @@ __device__ __forceinline__ Work map_item(const Params& p, int E, int w, int nr) 
 // and columns.
 template <int EPI, int BN>
 __device__ __forceinline__ void store_tile(const Params& p, __nv_bfloat16* out, uint32_t tbase, int row, bool live,
-                                           int n) {
-    if constexpr (EPI == EPI_SWIGLU) {
+                                           int n, float* outf = nullptr, bool zero = false) {
+    if constexpr (EPI == EPI_SWIGLU_BWD) {
+        // g, u from the accumulator; da = act gradient (0 past F): s = sigmoid(g),
+        // d_g = da u s (1 + g (1 - s)), d_u = da g s, written to columns n*256 + c and n*256 + 128 + c.
+#pragma unroll 1
+        for (int j = 0; j < 4; ++j) {
+            float g[32], u[32];
+            tmem_ld32(tbase + 32 * j, g);
+            tmem_ld32(tbase + 128 + 32 * j, u);
+            const int f0 = n * 128 + 32 * j;
+            if (live) {
+                __nv_bfloat16* dst = out + (size_t)row * p.ldo + (size_t)n * 256 + 32 * j;
+#pragma unroll
+                for (int c = 0; c < 32; c += 8) {
+                    Vec16<__nv_bfloat16> da, og, ou;
+                    if (f0 + c < p.n_valid) da = ld16(p.d_act + (size_t)row * p.n_valid + f0 + c);
+                    else da.v = make_uint4(0, 0, 0, 0);
+#pragma unroll
+                    for (int i = 0; i < 8; ++i) {
+                        const float gv = g[c + i], uv = u[c + i], a = da.get(i);
+                        const float sg = 1.f / (1.f + expf(-gv));
+                        og.set(i, a * uv * sg * (1.f + gv * (1.f - sg)));
+                        ou.set(i, a * gv * sg);
+                    }
+                    st16(dst + c, og);
+                    st16(dst + 128 + c, ou);
+                }
+            }
+        }
+    } else if constexpr (EPI == EPI_SWIGLU) {
 #pragma unroll 1
         for (int j = 0; j < 4; ++j) {
             float g[32], u[32];
@@ -270,10 +320,15 @@ __device__ __forceinline__ void store_tile(const Params& p, __nv_bfloat16* out, 
 #pragma unroll 1
         for (int j = 0; j < BN / 32; ++j) {
             float v[32];
-            tmem_ld32(tbase + 32 * j, v);
+            if (zero) {                      // no K steps (an expert without rows): the result is zero
+#pragma unroll
+                for (int i = 0; i < 32; ++i) v[i] = 0.f;
+            } else {
+                tmem_ld32(tbase + 32 * j, v);
+            }
             const int n0 = n * BN + 32 * j;
             if (live) {
-                float* dst = p.out_f32 + (size_t)row * p.ldo + n0;
+                float* dst = (outf ? outf : p.out_f32) + (size_t)row * p.ldo + n0;
 #pragma unroll
                 for (int c = 0; c < 32; c += 4) {
                     if (n0 + c < p.n_valid) {
@@ -315,7 +370,8 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
                     const __grid_constant__ CUtensorMap tmA2, const __grid_constant__ CUtensorMap tmB2, Params p) {
     constexpr int BN = CF::BN, STAGES = CF::STAGES, B_BYTES = CF::B_BYTES, STAGE_BYTES = CF::STAGE_BYTES;
     constexpr uint32_t kIdesc = idesc_bf16<BN>();
-    static_assert(EPI != EPI_SWIGLU || BN == 256, "the SwiGLU epilogue pairs 128 gate with 128 up columns");
+    static_assert((EPI != EPI_SWIGLU && EPI != EPI_SWIGLU_BWD) || BN == 256,
+                  "the SwiGLU epilogues pair 128 gate with 128 up columns");
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw_addr = smem_u32(smem_raw);
     uint8_t* smem = smem_raw + ((1024u - (raw_addr & 1023u)) & 1023u);
@@ -349,10 +405,16 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
     const uint32_t tmem = *tmem_slot;
 
     const int E = __ldg(p.sched + 1);
-    const int nr = __ldg(p.sched) * p.NT;                        // routed items
-    const int ns = (p.sh_rows + BM - 1) / BM * p.NT;             // shared-expert items
-    const int total = nr + ns;
     const int KB = (p.K + BK - 1) / BK;
+    int nr, ns;
+    if (p.wg_E > 0) {                                            // weight gradient: every expert's tiles
+        nr = p.wg_E * p.wg_MT * p.NT;
+        ns = 0;
+    } else {
+        nr = __ldg(p.sched) * p.NT;                              // routed items
+        ns = (p.sh_rows + BM - 1) / BM * p.NT;                   // shared-expert items
+    }
+    const int total = nr + ns;
 
     if (warp == 0) {
         if (lane == 0) {
@@ -360,16 +422,16 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
             int stage = 0;
             uint32_t phase = 0, issued = 0, last_par = 0;
             for (int w = blockIdx.x; w < total && !*abort_flag; w += gridDim.x) {
-                const Work wk = map_item(p, E, w, nr);
+                const Work wk = map_item(p, E, w, nr, KB);
                 const int brow = wk.e * p.b_rows + wk.n * BN;
                 const CUtensorMap* ma = wk.sh ? &tmA2 : &tmA;
                 const CUtensorMap* mb = wk.sh ? &tmB2 : &tmB;
                 bool ok = true;
-                for (int kb = 0; kb < KB; ++kb) {
+                for (int kb = 0; kb < wk.nkb; ++kb) {
                     if (!wait_phase(empty(stage), phase ^ 1u, p.wait_limit, abort_flag, p.err, 0x10u)) { ok = false; break; }
                     mbar_expect_tx(full(stage), STAGE_BYTES);
-                    tma_load_2d(sA + stage * A_BYTES, ma, kb * BK, wk.row0, full(stage));
-                    tma_load_2d(sB + stage * B_BYTES, mb, kb * BK, brow, full(stage));
+                    tma_load_2d(sA + stage * A_BYTES, ma, wk.kx0 + kb * BK, wk.row0, full(stage));
+                    tma_load_2d(sB + stage * B_BYTES, mb, wk.kx0 + kb * BK, brow, full(stage));
                     issued |= 1u << stage;
                     last_par = (last_par & ~(1u << stage)) | (phase << stage);
                     if (++stage == STAGES) { stage = 0; phase ^= 1u; }
@@ -391,8 +453,9 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
                 if (!wait_phase(tempty(a), aph ^ 1u, p.wait_limit, abort_flag, p.err, 0x20u)) break;
                 tc_fence_after();
                 const uint32_t d_tmem = tmem + (uint32_t)(a * BN);
+                const int nkb = map_item(p, E, w, nr, KB).nkb;
                 bool ok = true;
-                for (int kb = 0; kb < KB; ++kb) {
+                for (int kb = 0; kb < nkb; ++kb) {
                     if (!wait_phase(full(stage), phase, p.wait_limit, abort_flag, p.err, 0x21u)) { ok = false; break; }
                     tc_fence_after();
                     const uint32_t a_s = sA + stage * A_BYTES, b_s = sB + stage * B_BYTES;
@@ -418,11 +481,22 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
             const uint32_t aph = (iter >> 1) & 1;
             if (!wait_phase(tfull(a), aph, p.wait_limit, abort_flag, p.err, 0x30u)) break;
             tc_fence_after();
-            const Work wk = map_item(p, E, w, nr);
-            const int row = wk.row0 + lane_base + lane;
-            const bool live = row < wk.row1;
+            const Work wk = map_item(p, E, w, nr, KB);
+            int row = wk.row0 + lane_base + lane;
+            bool live = row < wk.row1;
+            float* outf = nullptr;
+            if (p.wg_E > 0) {
+                if (p.wg_gu) {                       // de-interleave the packed gate/up rows of expert e
+                    const int b = wk.row0 / BM, f = (b >> 1) * BM + lane_base + lane;
+                    outf = ((b & 1) ? p.out2 : p.out_f32) + ((size_t)wk.e * p.wg_F + (b >> 1) * BM) * p.ldo;
+                    row = lane_base + lane;
+                    live = f < p.wg_F;
+                } else {
+                    outf = p.out_f32 + (size_t)wk.e * p.wg_M * p.ldo;
+                }
+            }
             const uint32_t tbase = tmem + (uint32_t)(a * BN) + ((uint32_t)lane_base << 16);
-            store_tile<EPI, BN>(p, wk.sh ? p.sh_out : p.out, tbase, row, live, wk.n);
+            store_tile<EPI, BN>(p, wk.sh ? p.sh_out : p.out, tbase, row, live, wk.n, outf, wk.nkb == 0);
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(tempty(a));
@@ -801,7 +875,8 @@ static int gemm(const void* a, long long a_rows, const void* b, long long b_rows
     }
     grouped_gemm_kernel<EPI, CF><<<num_sms(), NUM_THREADS, CF::SMEM_BYTES, s>>>(ma, mb, ma2, mb2, p);
     return check_launch(EPI == EPI_SWIGLU ? "grouped_gemm_kernel<up_gate>"
-                        : EPI == EPI_BF16 ? "grouped_gemm_kernel<down>" : "grouped_gemm_kernel<router>");
+                        : EPI == EPI_BF16 ? "grouped_gemm_kernel<bf16>"
+                        : EPI == EPI_SWIGLU_BWD ? "grouped_gemm_kernel<swiglu_bwd>" : "grouped_gemm_kernel<f32>");
 }
 
 // 2-SM kernel: as many pairs as can be resident at once (one CTA per SM), each looping over work items.
@@ -837,7 +912,8 @@ static int gemm_pair(const void* a, long long a_rows, const void* b, long long b
         if (int rc = make_map(&mb2, sh.b, sh.b_rows, p.K, 128)) return rc;
     }
     grouped_gemm_pair_kernel<EPI><<<2 * clusters[dev], NUM_THREADS, PAIR_SMEM_BYTES, s>>>(ma, mb, ma2, mb2, p);
-    return check_launch(EPI == EPI_SWIGLU ? "grouped_gemm_pair_kernel<up_gate>" : "grouped_gemm_pair_kernel<down>");
+    return check_launch(EPI == EPI_SWIGLU ? "grouped_gemm_pair_kernel<up_gate>"
+                        : EPI == EPI_SWIGLU_BWD ? "grouped_gemm_pair_kernel<swiglu_bwd>" : "grouped_gemm_pair_kernel<bf16>");
 }
 
 // The 2-SM kernel when the average expert has at least four 128-row tiles (an odd tile count costs a
@@ -875,6 +951,59 @@ int ffn_tc_down(const void* act, const int32_t* sched, const void* packed, int E
                                 (long long)h};
     if (tc::use_pair(E, rows)) return tc::gemm_pair<tc::EPI_BF16>(act, rows, b, (long long)E * h, p, s, sh);
     return tc::gemm<tc::EPI_BF16, CF>(act, rows, b, (long long)E * h, p, s, sh);
+}
+
+// d_act [rows, F] = d_eout [rows, h] @ W_down[e] per expert, with W_down^T [E][F][h] (backward packing) as
+// the K-major operand.
+int ffn_tc_down_backward(const void* d_eout, const int32_t* sched, const void* packed_bwd, int E, int h, int F,
+                         int rows, void* d_act, cudaStream_t s) {
+    const PackedBwdLayout L = packed_bwd_layout(E, h, F, 2);
+    unsigned* err = device_error_word();
+    MOE_REQUIRE(err, MOE_ERR_CUDA, "device error word unavailable");
+    tc::Params p{sched, h, cdiv(F, 256), F, F, F, static_cast<__nv_bfloat16*>(d_act), nullptr, nullptr, err,
+                 wait_limit(), 0, nullptr};
+    const char* b = static_cast<const char*>(packed_bwd) + L.down_t_off;
+    if (tc::use_pair(E, rows)) return tc::gemm_pair<tc::EPI_BF16>(d_eout, rows, b, (long long)E * F, p, s);
+    return tc::gemm<tc::EPI_BF16, tc::Wide>(d_eout, rows, b, (long long)E * F, p, s);
+}
+
+// The up/gate GEMM again (g and u are not stored by the forward), its epilogue turning the act gradient into
+// the gate and up gradients d_gu [rows, 2 Fp] (packed column order); then d_buf [rows, h] = d_gu @ W_gu[e] with
+// W_gu^T [E][h][2Fp] (backward packing) as the K-major operand.
+int ffn_tc_up_gate_backward(const void* buf, const void* d_act, const int32_t* sched, const void* packed,
+                            const void* packed_bwd, int E, int h, int F, int rows, void* d_gu, void* d_buf,
+                            cudaStream_t s) {
+    const PackedLayout L = packed_layout(E, h, F, 2);
+    const PackedBwdLayout Lb = packed_bwd_layout(E, h, F, 2);
+    unsigned* err = device_error_word();
+    MOE_REQUIRE(err, MOE_ERR_CUDA, "device error word unavailable");
+    tc::Params p1{sched, h, L.Fp / 128, 2 * L.Fp, F, 2 * L.Fp, static_cast<__nv_bfloat16*>(d_gu), nullptr, nullptr,
+                  err, wait_limit(), 0, nullptr, static_cast<const __nv_bfloat16*>(d_act)};
+    const char* b1 = static_cast<const char*>(packed) + L.up_gate_off;
+    int rc = tc::use_pair(E, rows)
+                 ? tc::gemm_pair<tc::EPI_SWIGLU_BWD>(buf, rows, b1, (long long)E * 2 * L.Fp, p1, s)
+                 : tc::gemm<tc::EPI_SWIGLU_BWD, tc::Wide>(buf, rows, b1, (long long)E * 2 * L.Fp, p1, s);
+    if (rc) return rc;
+    tc::Params p2{sched, 2 * L.Fp, cdiv(h, 256), h, h, h, static_cast<__nv_bfloat16*>(d_buf), nullptr, nullptr, err,
+                  wait_limit(), 0, nullptr};
+    const char* b2 = static_cast<const char*>(packed_bwd) + Lb.gu_t_off;
+    if (tc::use_pair(E, rows)) return tc::gemm_pair<tc::EPI_BF16>(d_gu, rows, b2, (long long)E * h, p2, s);
+    return tc::gemm<tc::EPI_BF16, tc::Wide>(d_gu, rows, b2, (long long)E * h, p2, s);
+}
+
+// Weight gradient of every expert: out[e] [M][N] fp32 = At[:, seg[e] .. seg[e+1]) @ Bt[:, seg[e] .. seg[e+1])^T,
+// At [M][ktot] and Bt [N][ktot] bf16 K-major (the experts' rows transposed into 64-aligned column segments).
+// gu: At's rows are the packed gate/up order and are written de-interleaved to out (gate) and out2 (up), each
+// [E][F][N].
+int ffn_tc_weight_grad(const void* At, const void* Bt, long long ktot, const int32_t* seg, int E, int M, int N, int gu,
+                       int F, float* out, float* out2, cudaStream_t s) {
+    unsigned* err = device_error_word();
+    MOE_REQUIRE(err, MOE_ERR_CUDA, "device error word unavailable");
+    MOE_REQUIRE(ktot > 0 && ktot % tc::BK == 0 && ktot < (1LL << 31), MOE_ERR_INVALID_ARG,
+                "weight gradient: K extent %lld", ktot);
+    tc::Params p{seg, (int)ktot, cdiv(N, 256), 0, N, N, nullptr, out, nullptr, err, wait_limit(), 0, nullptr, nullptr,
+                 E, cdiv(M, tc::BM), M, seg, gu, F, out2};
+    return tc::gemm<tc::EPI_F32, tc::Wide>(At, M, Bt, N, p, s);
 }
 
 // Router logits [T, E] fp32 = x [T, h] @ w_rT^T (+ bias), w_rT the K-major [E, h] copy of the router weight,

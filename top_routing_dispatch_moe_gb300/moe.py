@@ -51,6 +51,12 @@ _SIGS = {
     "moe_router_weight_grad": (_I, [_P, _P, _I, _I, _I, _I, _P, _P, _Z, _P]),
     "moe_dispatch_backward_workspace_size": (_Z, [_I, _I, _I]),
     "moe_dispatch_backward": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _P, _P, _Z, _P]),
+    "moe_packed_weights_backward_bytes": (_Z, [_I, _I, _I, _I]),
+    "moe_pack_expert_weights_backward": (_I, [_P, _P, _P, _I, _I, _I, _I, _P, _P]),
+    "moe_expert_down_backward": (_I, [_P, _P, _P, _I, _I, _I, _I, _I, _P, _P]),
+    "moe_expert_up_gate_backward": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _P, _P, _P]),
+    "moe_expert_weight_grads_workspace_size": (_Z, [_I, _I, _I, _I, _I]),
+    "moe_expert_weight_grads": (_I, [_P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _P, _P, _P, _P, _Z, _P]),
     "moe_expert_down_shared": (_I, [_P, _P, _P, _I, _I, _I, _I, _P, _I, _P, _P, _I, _P, _P]),
     "moe_expert_ffn_workspace_size": (_Z, [_I, _I, _I]),
     "moe_expert_ffn": (_I, [_P, _P, _P, _I, _I, _I, _I, _I, _P, _P, _Z, _P]),
@@ -454,4 +460,59 @@ def moe_dispatch_backward(d_buf, dest_row, d_logits, w_r, dx_extra=None, dx=None
                                       E, dtype_code(d_buf.dtype), _ptr(dx), _ptr(ws),
                                       ws.numel() if ws is not None else 0, _stream(stream)))
     return dx
+
+
+def moe_pack_expert_weights_backward(w_gate, w_up, w_down, packed_bwd=None, stream=None):
+    E, F, h = w_gate.shape
+    dt = dtype_code(w_gate.dtype)
+    if packed_bwd is None:
+        packed_bwd = _bytes_tensor(_lib.moe_packed_weights_backward_bytes(E, h, F, dt), w_gate.device)
+    _check(_lib.moe_pack_expert_weights_backward(_ptr(w_gate), _ptr(w_up), _ptr(w_down), E, h, F, dt, _ptr(packed_bwd),
+                                                 _stream(stream)))
+    return packed_bwd
+
+
+def gu_cols(F: int) -> int:
+    """Columns of d_gu: 2 * (F rounded up to 128)."""
+    return 2 * ((F + 127) // 128 * 128)
+
+
+def moe_expert_down_backward(d_eout, tile_sched, packed_bwd, E: int, F: int, d_act=None, stream=None):
+    rows, h = d_eout.shape
+    if d_act is None:
+        d_act = torch.empty((rows, F), dtype=d_eout.dtype, device=d_eout.device)
+    _check(_lib.moe_expert_down_backward(_ptr(d_eout), _ptr(tile_sched), _ptr(packed_bwd), E, h, F, rows,
+                                         dtype_code(d_eout.dtype), _ptr(d_act), _stream(stream)))
+    return d_act
+
+
+def moe_expert_up_gate_backward(buf, d_act, tile_sched, packed_w, packed_bwd, E: int, d_gu=None, d_buf=None,
+                                stream=None):
+    rows, h = buf.shape
+    F = d_act.shape[1]
+    if d_gu is None:
+        d_gu = torch.empty((rows, gu_cols(F)), dtype=buf.dtype, device=buf.device)
+    if d_buf is None:
+        d_buf = torch.empty((rows, h), dtype=buf.dtype, device=buf.device)
+    _check(_lib.moe_expert_up_gate_backward(_ptr(buf), _ptr(d_act), _ptr(tile_sched), _ptr(packed_w), _ptr(packed_bwd),
+                                            E, h, F, rows, dtype_code(buf.dtype), _ptr(d_gu), _ptr(d_buf),
+                                            _stream(stream)))
+    return d_gu, d_buf
+
+
+def moe_expert_weight_grads(buf, act, d_gu, d_eout, offsets, kept_counts, E: int, dW_gate=None, dW_up=None,
+                            dW_down=None, ws=None, stream=None):
+    rows, h = buf.shape
+    F = act.shape[1]
+    dev = buf.device
+    f32 = torch.float32
+    dW_gate = torch.empty((E, F, h), dtype=f32, device=dev) if dW_gate is None else dW_gate
+    dW_up = torch.empty((E, F, h), dtype=f32, device=dev) if dW_up is None else dW_up
+    dW_down = torch.empty((E, h, F), dtype=f32, device=dev) if dW_down is None else dW_down
+    if ws is None:
+        ws = _bytes_tensor(_lib.moe_expert_weight_grads_workspace_size(E, h, F, rows, dtype_code(buf.dtype)), dev)
+    _check(_lib.moe_expert_weight_grads(_ptr(buf), _ptr(act), _ptr(d_gu), _ptr(d_eout), _ptr(offsets),
+                                        _ptr(kept_counts), E, h, F, rows, dtype_code(buf.dtype), _ptr(dW_gate),
+                                        _ptr(dW_up), _ptr(dW_down), _ptr(ws), ws.numel(), _stream(stream)))
+    return dW_gate, dW_up, dW_down
 
