@@ -253,7 +253,8 @@ def run_gpu(args, cfg, C):
                      bias=torch.from_numpy(inp["bias"]).to(dev) if inp["bias"] is not None else None,
                      w_gate=up(inp["wg"]), w_up=up(inp["wu"]), w_down=up(inp["wd"]),
                      shared=tuple(up(np.ascontiguousarray(w)[None]) for w in inp["shared"])
-                     if inp["shared"] is not None else None, device=dev, routing=cfg.routing)
+                     if inp["shared"] is not None else None, device=dev, routing=cfg.routing,
+                     backward=want_backward(args, cfg))
     x = up(inp["x"])
     flush = torch.empty(512 * 2**20, dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream()
@@ -326,6 +327,15 @@ def run_gpu(args, cfg, C):
     e2e = max_over_ranks(e0.elapsed_time(e1) / args.steps, world, dev)
     io_bytes = cfg.T * cfg.h * cfg.el
 
+    # ---- backward of the layer (a separate timed loop; the headline value above is the forward): K backward
+    # passes over the saved state of one forward of x, L2 flushed between them
+    backward = None
+    if want_backward(args, cfg):
+        try:
+            backward = time_backward(args, cfg, layer, x, flush, stream, kept)
+        except Exception as exc:                      # reported in the line; the forward figures stand
+            backward = {"error": f"{type(exc).__name__}: {exc}"}
+
     # ---- roofline of the dominant kernel (the up/gate grouped GEMM) and the bandwidth stages
     hbm, bf16_burst, bf16_sus, peak_src = _peaks()
     ug_ms = float(np.mean(stage_ms["up_gate"]))
@@ -359,6 +369,7 @@ def run_gpu(args, cfg, C):
                        "parallelism": f"replicas x{world}", "l2": "flushed between steps (512 MiB write)",
                        "kept_assignments": kept},
             "roofline": roofline,
+            **({"backward": backward} if backward is not None else {}),
             "e2e": {"value": world * cfg.T / (e2e * 1e-3), "unit": "tokens/s", "h2d_bytes_per_step": io_bytes,
                     "d2h_bytes_per_step": io_bytes, "ms_per_step": e2e},
             "gpu_launches": int(launches),
@@ -383,6 +394,43 @@ def run_gpu(args, cfg, C):
         dist.destroy_process_group()
 
 
+def want_backward(args, cfg) -> bool:
+    return args.backward and cfg.dtype == "bf16" and cfg.routing == "token"
+
+
+def time_backward(args, cfg, layer, x, flush, stream, kept):
+    """Gradients of <dy, y> + aux for one forward of x, timed over K passes with CUDA events per stage."""
+    import torch
+    from top_routing_dispatch_moe_gb300 import moe
+    dy = torch.randn(x.shape, generator=torch.Generator(device=x.device).manual_seed(5), device=x.device,
+                     dtype=torch.float32).to(x.dtype)
+    layer.forward(x)
+    for _ in range(max(1, args.warmup)):
+        layer.backward(x, dy)
+        flush.zero_()
+    torch.cuda.synchronize()
+    events: dict = {}
+    for _ in range(args.steps):
+        layer.backward(x, dy, events=events)
+        flush.zero_()
+    torch.cuda.synchronize()
+    assert moe.moe_check_device_error() == moe.MOE_OK, moe.moe_last_error_string()
+    names = [s for s in ("combine_bwd", "expert_dgrad", "expert_wgrad", "shared_bwd", "router_bwd", "dispatch_bwd")
+             if s in events]
+    order = ["start"] + names
+    st = {b: float(np.mean([events[a][i].elapsed_time(events[b][i]) for i in range(args.steps)]))
+          for a, b in zip(order[:-1], order[1:])}
+    ms = float(np.mean([events["start"][i].elapsed_time(events[order[-1]][i]) for i in range(args.steps)]))
+    # expert GEMM work: dgrad 10 h F (down 2, up/gate recompute 4, up/gate dgrad 4) + wgrad 6 h F per row
+    rows = kept + (cfg.T if cfg.n_shared else 0)
+    gemm_flops = 16.0 * rows * cfg.h * cfg.F
+    gemm_ms = st["expert_dgrad"] + st["expert_wgrad"] + st.get("shared_bwd", 0.0)
+    return {"ms_per_step": ms, "tokens_per_s": cfg.T / (ms * 1e-3), "unit": "tokens/s", "stages_ms": st,
+            "expert_gemm_tflops": gemm_flops / (gemm_ms * 1e-3) / 1e12,
+            "what": "dx, dW_r, d_bias, every expert's and the shared expert's fp32 weight gradients for "
+                    "<dy, y> + aux; L2 flushed between passes"}
+
+
 def kernel_hash():
     import hashlib
     h = hashlib.sha256()
@@ -400,6 +448,8 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
     ap.add_argument("--workload", default="page3_cf1.25", choices=list(moe_inputs.CONFIGS))
+    ap.add_argument("--backward", action=argparse.BooleanOptionalAction, default=True,
+                    help="also time the layer's backward (bf16 token-choice workloads), reported under 'backward'")
     ap.add_argument("--sample-tokens", type=int, default=32, help="oracle tokens per reference-arm step")
     ap.add_argument("--baseline-tokens", type=int, default=128, help="oracle tokens of the cpu_baseline sample")
     ap.add_argument("--no-cpu-baseline", action="store_true")

@@ -166,3 +166,60 @@ def test_expert_backward(sizes):
                                (f64(dWg[e]), g["dW_gate"], "dW_gate"), (f64(dWu[e]), g["dW_up"], "dW_up"),
                                (f64(dWd[e]), g["dW_down"], "dW_down")]:
             assert cases.rel_l2(got, ref) <= 2e-2, f"expert {e} ({b - a} rows): {what} rel err {cases.rel_l2(got, ref):.3e}"
+
+
+LAYER_CASES = {
+    "page3_small": ("page3_cf1.25", dict(T=300, h=256, F=128), None),             # softmax, capacity drops
+    "mixtral_small": ("mixtral_zipf", dict(T=400, h=256, F=128), "zipf"),         # renormalised, bias gradient
+    "deepseek_small": ("deepseek_v3", dict(T=200, h=256, F=128, E=64, k=6), None),  # sigmoid + its shared expert
+}
+
+
+@pytest.mark.parametrize("name", list(LAYER_CASES))
+def test_layer_backward(name):
+    """MoELayer.backward (every backward call in sequence) against the oracle's moe_layer_backward of its own
+    float64 forward, for <dy, y> + d_aux * aux: dx, dW_r, d_bias, every expert's and the shared expert's weight
+    gradients. The GPU's intermediates (eout, act, d_act, d_g / d_u, d_buf) are bf16: normwise 2e-2."""
+    import torch
+    base, over, bias_kind = LAYER_CASES[name]
+    cfg = moe_inputs.get_config(base, **over)
+    bias = moe_inputs.load_zipf_bias(moe_inputs.get_config("mixtral_zipf")) if bias_kind == "zipf" else None
+    inp = cases.router_inputs(cfg, bias=bias)
+    assert inp["near_ties"] == 0
+    wg, wu, wd = moe_inputs.all_expert_weights(cfg)
+    shared = tuple(a[0] for a in moe_inputs.all_expert_weights(cfg, shared=True)) if cfg.n_shared else None
+    layer = cases.build_gpu_layer(cfg, inp, wg, wu, wd, shared, backward=True)
+    x = cases.to_device(inp["x"], cfg)
+    layer.forward(x)
+    rng = np.random.default_rng(13)
+    dy = torch.from_numpy(rng.normal(size=(cfg.T, cfg.h)).astype(np.float32)).to("cuda").to(x.dtype)
+    d_aux = 0.7
+    g = layer.backward(x, dy, d_aux=d_aux)
+    torch.cuda.synchronize()
+    from top_routing_dispatch_moe_gb300 import moe
+    assert moe.moe_check_device_error() == moe.MOE_OK, moe.moe_last_error_string()
+
+    x64 = moe_inputs.to_f64(inp["x"], cfg.dtype)
+    w_r64 = moe_inputs.to_f64(inp["w_r"], cfg.dtype)
+    wfn = cases.weights_fn_from(cfg, wg, wu, wd)
+    sfn = (lambda: tuple(moe_inputs.to_f64(w, cfg.dtype) for w in shared)) if shared else None
+    fwd = O.moe_layer(x64, w_r64, inp["bias"], wfn, k=cfg.k, gating=cfg.gating, cf=cfg.cf, R=cfg.R, alpha=cfg.alpha,
+                      shared=sfn)
+    np.testing.assert_array_equal(layer.r_out["topk_ids"].cpu().numpy(), fwd["router"]["ids"])
+    ref = O.moe_layer_backward(x64, w_r64, inp["bias"], wfn, fwd, _np(dy), gating=cfg.gating, alpha=cfg.alpha,
+                               d_aux=d_aux, shared=sfn)
+    checks = [("dx", _np(g["dx"]), ref["dx"]), ("dW_r", _np(g["dW_r"]), ref["dW_r"]),
+              ("dW_gate", _np(g["dW_gate"]), np.stack([w[0] for w in ref["dW"]])),
+              ("dW_up", _np(g["dW_up"]), np.stack([w[1] for w in ref["dW"]])),
+              ("dW_down", _np(g["dW_down"]), np.stack([w[2] for w in ref["dW"]]))]
+    if ref["d_bias"] is not None:
+        checks.append(("d_bias", _np(g["d_bias"]), ref["d_bias"]))
+    else:
+        assert g["d_bias"] is None
+    if shared:
+        checks += [("shared_dW_gate", _np(g["shared_dW_gate"]), ref["shared"]["dW_gate"]),
+                   ("shared_dW_up", _np(g["shared_dW_up"]), ref["shared"]["dW_up"]),
+                   ("shared_dW_down", _np(g["shared_dW_down"]), ref["shared"]["dW_down"])]
+    for what, got, want in checks:
+        err = cases.rel_l2(got, want)
+        assert err <= 2e-2, f"{what}: rel err {err:.3e}"

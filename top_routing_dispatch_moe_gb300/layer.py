@@ -31,7 +31,7 @@ class MoELayer:
     STAGES = ("router", "dispatch", "up_gate", "down", "shared_up_gate", "shared_down", "combine")
 
     def __init__(self, *, T, h, E, k, F, gating, cf, R, alpha, w_r, bias, w_gate, w_up, w_down,
-                 shared=None, device="cuda", routing="token"):
+                 shared=None, device="cuda", routing="token", backward=False):
         self.T, self.h, self.E, self.k, self.F = T, h, E, k, F
         self.gating, self.R, self.alpha = gating, R, alpha
         self.C = capacity_slots(cf, k, T, E)
@@ -43,6 +43,11 @@ class MoELayer:
         self.bias = bias
         self.packed = moe.moe_pack_expert_weights(w_gate, w_up, w_down)
         self.shared_packed = moe.moe_pack_expert_weights(*shared) if shared is not None else None
+        # the dgrad GEMMs' weight operands (only when the layer will run backward: twice the weight memory)
+        self.packed_bwd = moe.moe_pack_expert_weights_backward(w_gate, w_up, w_down) if backward else None
+        self.shared_packed_bwd = (moe.moe_pack_expert_weights_backward(*shared)
+                                  if backward and shared is not None else None)
+        self._bwd = None
         i32, f32 = torch.int32, torch.float32
         code = moe.dtype_code(dt)
         self.routing = routing
@@ -144,6 +149,98 @@ class MoELayer:
         else:
             moe.moe_combine(self.eout, self.d_out["dest_row"], r["gates"], shared_out, y=out, stream=stream)
         mark("combine")
+        return out
+
+    def backward(self, x, dy, d_aux=1.0, stream=None, events=None):
+        """Gradients of <dy, y> + d_aux * aux for the last forward(x): returns dict(dx, dW_r, d_bias, dW_gate,
+        dW_up, dW_down[, shared_dW_gate, shared_dW_up, shared_dW_down]); weight gradients fp32, dx in the
+        layer's dtype. Token-choice routing, bf16, and a layer built with backward=True. Order of the calls:
+        combine, expert down / up-gate dgrad, expert weight gradients, [shared expert], router, router weight,
+        dispatch (+ the router and shared terms of dx). `events` as in forward (stages "combine_bwd",
+        "expert_dgrad", "expert_wgrad", ["shared_bwd"], "router_bwd", "dispatch_bwd")."""
+        if self.packed_bwd is None:
+            raise RuntimeError("MoELayer.backward: build the layer with backward=True")
+        if self.routing != "token" or self.dtype != torch.bfloat16:
+            raise NotImplementedError("MoELayer.backward: token-choice routing in bf16")
+
+        def mark(stage):
+            if events is not None:
+                ev = torch.cuda.Event(enable_timing=True)
+                ev.record(stream if stream is not None else torch.cuda.current_stream())
+                events.setdefault(stage, []).append(ev)
+
+        dev, dt, f32 = self.device, self.dtype, torch.float32
+        T, h, E, k, F, rows = self.T, self.h, self.E, self.k, self.F, self.rows
+        if self._bwd is None:
+            b = dict(d_eout=torch.empty((rows, h), dtype=dt, device=dev),
+                     d_gates=torch.empty((T, k), dtype=f32, device=dev),
+                     d_act=torch.empty((rows, F), dtype=dt, device=dev),
+                     d_gu=torch.empty((rows, moe.gu_cols(F)), dtype=dt, device=dev),
+                     d_buf=torch.empty((rows, h), dtype=dt, device=dev),
+                     d_logits=torch.empty((T, E), dtype=f32, device=dev),
+                     dx=torch.empty((T, h), dtype=dt, device=dev),
+                     dW_r=torch.empty((h, E), dtype=f32, device=dev),
+                     dW_gate=torch.empty((E, F, h), dtype=f32, device=dev),
+                     dW_up=torch.empty((E, F, h), dtype=f32, device=dev),
+                     dW_down=torch.empty((E, h, F), dtype=f32, device=dev),
+                     ws_wg=moe._bytes_tensor(moe._lib.moe_expert_weight_grads_workspace_size(
+                         E, h, F, rows, moe.dtype_code(dt)), dev),
+                     ws_rb=moe._bytes_tensor(moe._lib.moe_router_backward_workspace_size(T, E), dev),
+                     ws_rw=moe._bytes_tensor(moe._lib.moe_router_weight_grad_workspace_size(T, h, E), dev),
+                     ws_db=moe._bytes_tensor(moe._lib.moe_dispatch_backward_workspace_size(h, E, moe.dtype_code(dt)),
+                                             dev))
+            if self.shared_packed is not None:
+                b.update(sh_d_act=torch.empty((T, F), dtype=dt, device=dev),
+                         sh_d_gu=torch.empty((T, moe.gu_cols(F)), dtype=dt, device=dev),
+                         sh_dx=torch.empty((T, h), dtype=dt, device=dev),
+                         sh_dW_gate=torch.empty((1, F, h), dtype=f32, device=dev),
+                         sh_dW_up=torch.empty((1, F, h), dtype=f32, device=dev),
+                         sh_dW_down=torch.empty((1, h, F), dtype=f32, device=dev),
+                         sh_off=torch.tensor([0, T], dtype=torch.int32, device=dev),
+                         sh_kept=torch.tensor([T], dtype=torch.int32, device=dev),
+                         ws_sh=moe._bytes_tensor(moe._lib.moe_expert_weight_grads_workspace_size(
+                             1, h, F, T, moe.dtype_code(dt)), dev))
+            self._bwd = b
+        b = self._bwd
+        r, d = self.r_out, self.d_out
+        sched = d["tile_sched"]
+        mark("start")
+        moe.moe_combine_backward(dy, self.eout, d["src_token"], d["src_slot"], d["dest_row"], r["gates"],
+                                 d_eout=b["d_eout"], d_gates=b["d_gates"], stream=stream)
+        mark("combine_bwd")
+        moe.moe_expert_down_backward(b["d_eout"], sched, self.packed_bwd, E, F, d_act=b["d_act"], stream=stream)
+        moe.moe_expert_up_gate_backward(d["buf"], b["d_act"], sched, self.packed, self.packed_bwd, E, d_gu=b["d_gu"],
+                                        d_buf=b["d_buf"], stream=stream)
+        mark("expert_dgrad")
+        moe.moe_expert_weight_grads(d["buf"], self.act, b["d_gu"], b["d_eout"], d["offsets"], d["kept_counts"], E,
+                                    dW_gate=b["dW_gate"], dW_up=b["dW_up"], dW_down=b["dW_down"], ws=b["ws_wg"],
+                                    stream=stream)
+        mark("expert_wgrad")
+        sh_dx = None
+        if self.shared_packed is not None:
+            moe.moe_expert_down_backward(dy, self.sh_sched, self.shared_packed_bwd, 1, F, d_act=b["sh_d_act"],
+                                         stream=stream)
+            moe.moe_expert_up_gate_backward(x, b["sh_d_act"], self.sh_sched, self.shared_packed, self.shared_packed_bwd,
+                                            1, d_gu=b["sh_d_gu"], d_buf=b["sh_dx"], stream=stream)
+            moe.moe_expert_weight_grads(x, self.sh_act, b["sh_d_gu"], dy, b["sh_off"], b["sh_kept"], 1,
+                                        dW_gate=b["sh_dW_gate"], dW_up=b["sh_dW_up"], dW_down=b["sh_dW_down"],
+                                        ws=b["ws_sh"], stream=stream)
+            sh_dx = b["sh_dx"]
+            mark("shared_bwd")
+        want_bias = self.bias is not None and self.gating in ("softmax", "softmax_renorm")
+        d_logits, d_bias = moe.moe_router_backward(r["logits"], r["topk_ids"], r["gates"], b["d_gates"], r["f"],
+                                                   self.gating, self.alpha, d_aux, d_logits=b["d_logits"],
+                                                   want_bias_grad=want_bias, ws=b["ws_rb"], stream=stream)
+        moe.moe_router_weight_grad(x, d_logits, dW_r=b["dW_r"], ws=b["ws_rw"], stream=stream)
+        mark("router_bwd")
+        moe.moe_dispatch_backward(b["d_buf"], d["dest_row"], d_logits, self.w_r, dx_extra=sh_dx,
+                                  dx=b["dx"], ws=b["ws_db"], stream=stream)
+        mark("dispatch_bwd")
+        out = dict(dx=b["dx"], dW_r=b["dW_r"], d_bias=d_bias, dW_gate=b["dW_gate"], dW_up=b["dW_up"],
+                   dW_down=b["dW_down"])
+        if self.shared_packed is not None:
+            out.update(shared_dW_gate=b["sh_dW_gate"][0], shared_dW_up=b["sh_dW_up"][0],
+                       shared_dW_down=b["sh_dW_down"][0])
         return out
 
     def forward_host_batches(self, x_hosts, y_hosts):
