@@ -22,7 +22,10 @@ FFN checked against scalar loops; aux = alpha exactly at a uniform split and >= 
 FLOP and byte counts of [L7] "EP" (6.2 ms at 400 TFLOPS, 64 MiB per dispatch). The backward
 (combine_backward, swiglu_ffn_backward, route_backward, moe_layer_backward) is pinned by central differences
 of the forward in every gating mode with and without drops, a hand-derived 1 x 1 SwiGLU derivative, and zero
-gradients on dropped pairs and pad rows. No function is unpinned.
+gradients on dropped pairs and pad rows. The FP8 payload (e4m3_value, e4m3_encode, fp8_quantize_rows,
+fp8_dequantize_rows, dispatch_payload_fp8) is pinned by hand-written code values, a brute-force nearest
+search with the tie rule, exact midpoints, saturation, the amax -> 448 scale and the half-ulp error bound. No
+function is unpinned.
 """
 from __future__ import annotations
 
@@ -504,3 +507,91 @@ def moe_layer_backward(x, w_r, bias, weights, fwd: dict, dy, *, gating: str, alp
     d_bias = d_logits.sum(axis=0) if (bias is not None and gating != SIGMOID_BIAS_RENORM) else None
     return dict(dx=dx, dW_r=dW_r, d_bias=d_bias, dW=dW, shared=sh, d_eout=d_eout, d_gates=d_gates, d_buf=d_buf,
                 d_logits=d_logits)
+
+
+# ---------------------------------------------------------------------------------------------------------
+# FP8 dispatch payload ([B10.5] 10.5.7 "低精度传输与压缩": activations crossing nodes can use a low-precision
+# format such as FP8, halving the bytes with negligible effect on model quality). The page fixes neither the
+# format nor the scaling; readings: e4m3 in its finite-only variant (1 sign, 4 exponent bits with bias 7, 3
+# mantissa bits, subnormals, largest magnitude 448, no infinities), one fp32 scale per token and per 128 columns
+# s = amax / 448 (s = 1 for an all-zero block), code = round-to-nearest-even of fp32(x) / s on the e4m3 grid
+# with saturation to +-448; dequantisation as the GEMM prologue does it: bf16(fp32(value(code)) * s).
+# ---------------------------------------------------------------------------------------------------------
+
+E4M3_MAX = 448.0
+FP8_BLOCK = 128
+
+
+def e4m3_value(code: int) -> float:
+    """Value of an e4m3 byte: exponent field 0 -> subnormal m/8 * 2^-6; else (1 + m/8) * 2^(e - 7);
+    code 0x7f / 0xff (exponent and mantissa all ones) is NaN."""
+    s = -1.0 if code & 0x80 else 1.0
+    e = (code >> 3) & 0xF
+    m = code & 0x7
+    if e == 0xF and m == 0x7:
+        return math.nan
+    if e == 0:
+        return s * (m / 8.0) * 2.0 ** -6
+    return s * (1.0 + m / 8.0) * 2.0 ** (e - 7)
+
+
+def e4m3_table() -> np.ndarray:
+    return np.array([e4m3_value(c) for c in range(256)])
+
+
+def e4m3_encode(v: np.ndarray) -> np.ndarray:
+    """Nearest finite e4m3 code of each float (ties to the code with an even mantissa), saturating beyond 448.
+    Zero maps to +0 (code 0) and -0 to code 0x80."""
+    v = np.asarray(v, np.float64)
+    tab = e4m3_table()
+    pos = np.array([c for c in range(0x7F)])                 # +0 .. 448, increasing values
+    pv = tab[pos]
+    a = np.minimum(np.abs(v), E4M3_MAX)
+    idx = np.searchsorted(pv, a)                              # pv[idx-1] < a <= pv[idx]
+    idx = np.clip(idx, 1, len(pv) - 1)
+    lo, hi = pos[idx - 1], pos[idx]
+    dlo, dhi = a - tab[lo], tab[hi] - a
+    pick_hi = (dhi < dlo) | ((dhi == dlo) & ((hi & 1) == 0))
+    code = np.where(pick_hi, hi, lo)
+    code = np.where(a == 0, 0, code)
+    neg = np.signbit(v)
+    return (code | np.where(neg, 0x80, 0)).astype(np.uint8)
+
+
+def fp8_quantize_rows(X: np.ndarray):
+    """Per row and per 128 columns: s = fp32(amax) / 448 in fp32 (1 for an all-zero block); codes =
+    e4m3_encode(fp32(x) / s in fp32). Returns (codes uint8 [rows, h], scales float32 [rows, h / 128])."""
+    X = np.asarray(X, np.float32)
+    n, h = X.shape
+    assert h % FP8_BLOCK == 0
+    blocks = X.reshape(n, h // FP8_BLOCK, FP8_BLOCK)
+    amax = np.abs(blocks).max(axis=2)
+    scales = np.where(amax > 0, amax / np.float32(E4M3_MAX), np.float32(1.0)).astype(np.float32)
+    q = (blocks / scales[:, :, None]).astype(np.float32)
+    return e4m3_encode(q).reshape(n, h), scales
+
+
+def bf16_round(v: np.ndarray) -> np.ndarray:
+    """Round float32 values to bfloat16 (nearest, ties to even) and return them as float64."""
+    b = np.asarray(v, np.float32).view(np.uint32).astype(np.uint64)
+    b = (b + 0x7FFF + ((b >> 16) & 1)) >> 16
+    return (b.astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+
+
+def fp8_dequantize_rows(codes: np.ndarray, scales: np.ndarray) -> np.ndarray:
+    """bf16(fp32(value(code)) * s) per element, as float64."""
+    n, h = codes.shape
+    vals = e4m3_table()[codes].astype(np.float32).reshape(n, h // FP8_BLOCK, FP8_BLOCK)
+    return bf16_round((vals * np.asarray(scales, np.float32)[:, :, None]).reshape(n, h))
+
+
+def dispatch_payload_fp8(x: np.ndarray, d: dict):
+    """The dispatch send buffer in FP8: every kept row holds its token's codes and scales (each token quantised
+    once); pad rows hold code 0 and scale 0."""
+    codes_t, scales_t = fp8_quantize_rows(x)
+    codes = np.zeros((d["rows"], x.shape[1]), np.uint8)
+    scales = np.zeros((d["rows"], x.shape[1] // FP8_BLOCK), np.float32)
+    live = d["src_token"] >= 0
+    codes[live] = codes_t[d["src_token"][live]]
+    scales[live] = scales_t[d["src_token"][live]]
+    return codes, scales

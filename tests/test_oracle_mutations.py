@@ -12,6 +12,7 @@ _route, _dispatch, _swiglu, _combine, _capacity = O.route, O.dispatch, O.swiglu_
 _ec = O.expert_choice
 _sk = O.sinkhorn_scaling
 _cbwd, _swbwd, _rbwd = O.combine_backward, O.swiglu_ffn_backward, O.route_backward
+_enc, _q8, _dq8 = O.e4m3_encode, O.fp8_quantize_rows, O.fp8_dequantize_rows
 
 
 def mut_renormalise_softmax(L, k, gating, bias=None, alpha=0.01):
@@ -142,6 +143,33 @@ def mut_combine_backward_no_gate(dy, eout, dest_row, gates, rows):
     return _cbwd(dy, eout, dest_row, np.ones_like(gates), rows)
 
 
+def mut_e4m3_ties_away(v):
+    """Rounds ties away from zero instead of to the even mantissa."""
+    v = np.asarray(v, np.float64)
+    code = _enc(v)
+    t = O.e4m3_table()
+    a = np.abs(v)
+    c = code & 0x7F
+    up = np.minimum(c + 1, 0x7E)
+    tie = (np.abs(t[up] - a) == np.abs(a - t[c])) & (t[up] > t[c])
+    return np.where(tie, up | (code & 0x80), code).astype(np.uint8)
+
+
+def mut_fp8_scale_240(X):
+    """Takes the scale for a largest value of 240 (another fp8 variant's)."""
+    codes, scales = _q8(X)
+    X = np.asarray(X, np.float32)
+    n, h = X.shape
+    amax = np.abs(X.reshape(n, h // 128, 128)).max(axis=2)
+    sc = np.where(amax > 0, amax / np.float32(240.0), np.float32(1.0)).astype(np.float32)
+    q = (X.reshape(n, h // 128, 128) / sc[:, :, None]).astype(np.float32)
+    return _enc(q).reshape(n, h), sc
+
+
+def mut_fp8_dequant_no_scale(codes, scales):
+    return _dq8(codes, np.ones_like(scales))
+
+
 MUTANTS = [
     ("route", mut_renormalise_softmax), ("route", mut_ascending_order), ("route", mut_bias_in_sigmoid_gates),
     ("route", mut_aux_denominator_T), ("dispatch", mut_drop_latest_first), ("dispatch", mut_dispatch_unstable),
@@ -150,7 +178,8 @@ MUTANTS = [
     ("expert_choice", mut_ec_ties_higher_token), ("sinkhorn_scaling", mut_sinkhorn_columns_only),
     ("sinkhorn_scaling", mut_sinkhorn_rows_first), ("swiglu_ffn_backward", mut_silu_prime_plain_sigmoid),
     ("route_backward", mut_route_backward_no_aux), ("route_backward", mut_route_backward_renorm_as_plain),
-    ("combine_backward", mut_combine_backward_no_gate),
+    ("combine_backward", mut_combine_backward_no_gate), ("e4m3_encode", mut_e4m3_ties_away),
+    ("fp8_quantize_rows", mut_fp8_scale_240), ("fp8_dequantize_rows", mut_fp8_dequant_no_scale),
 ]
 
 PINS = [
@@ -167,6 +196,8 @@ PINS = [
     lambda: P.test_backward_matches_finite_differences(O.SOFTMAX_RENORM, 0.6),
     lambda: P.test_backward_matches_finite_differences(O.SIGMOID_BIAS_RENORM, 0.0),
     P.test_swiglu_backward_scalar_closed_form, P.test_backward_dropped_pairs_and_pad_rows_get_zero,
+    P.test_e4m3_table_closed_form, P.test_e4m3_encode_brute_force_and_ties,
+    P.test_fp8_quantize_rows_scale_and_error_bound, P.test_fp8_payload_rows_and_pads,
 ]
 
 

@@ -579,3 +579,81 @@ def test_backward_dropped_pairs_and_pad_rows_get_zero():
     assert np.all(g["d_gates"][d["drop_mask"]] == 0)
     pad = d["src_token"] < 0
     assert pad.any() and np.all(g["d_eout"][pad] == 0) and np.all(g["d_buf"][pad] == 0)
+
+
+# ------------------------------------------------------------------------------------------------ fp8 payload
+
+def test_e4m3_table_closed_form():
+    """Values written out by hand from the e4m3 definition (bias 7, 3 mantissa bits, no infinities)."""
+    t = O.e4m3_table()
+    hand = {0x00: 0.0, 0x01: 2.0 ** -9, 0x07: 7 / 8 * 2.0 ** -6, 0x08: 2.0 ** -6, 0x38: 1.0, 0x3C: 1.5, 0x40: 2.0,
+            0x7E: 448.0, 0x78: 256.0, 0xB8: -1.0, 0xFE: -448.0, 0x30: 0.5}
+    for c, v in hand.items():
+        assert t[c] == v, (hex(c), t[c], v)
+    assert np.isnan(t[0x7F]) and np.isnan(t[0xFF]) and np.isfinite(t).sum() == 254
+    assert np.all(np.diff(t[:0x7F]) > 0)                      # codes 0 .. 0x7e increase
+    assert np.array_equal(t[0x80:0xFF], -t[0x00:0x7F])        # sign bit mirrors
+
+
+def test_e4m3_encode_brute_force_and_ties():
+    """Nearest finite code by exhaustive search (ties -> even mantissa), midpoints, saturation."""
+    t = O.e4m3_table()
+    fin = np.array([c for c in range(256) if np.isfinite(t[c])])
+    rng = np.random.default_rng(0)
+    v = np.concatenate([rng.normal(size=2000) * 50, rng.normal(size=500) * 0.01, [0.0, 447.0, 448.0]])
+    got = O.e4m3_encode(v)
+    for x, c in zip(v, got):
+        d = np.abs(t[fin] - x)
+        best = fin[d == d.min()]
+        if len(best) > 1:                                     # a tie (or +-0): prefer the even mantissa, same sign
+            best = [b for b in best if (b & 1) == 0 and (np.signbit(t[b]) == np.signbit(x) or t[b] != 0)] or best
+        assert c in best, (x, hex(c), [hex(b) for b in best])
+    pos = np.arange(0x7F)
+    mids = (t[pos[:-1]] + t[pos[1:]]) / 2                     # exact midpoints between neighbours
+    m = O.e4m3_encode(mids)
+    assert np.all((m & 1) == 0) and np.all((m == pos[:-1]) | (m == pos[1:]))
+    assert np.all(O.e4m3_encode(np.array([449.0, 500.0, 1e30])) == 0x7E)
+    assert np.all(O.e4m3_encode(np.array([-449.0, -1e30])) == 0xFE)
+
+
+def test_fp8_quantize_rows_scale_and_error_bound():
+    """The block's largest magnitude maps to +-448 exactly; an all-zero block gets scale 1 and code 0; the
+    dequantised value is within half an e4m3 ulp (relative 2^-4 for normals, 2^-10 s for subnormals) plus the
+    bf16 rounding of x itself."""
+    rng = np.random.default_rng(1)
+    X = rng.normal(size=(6, 384)).astype(np.float32)
+    X[2, 128:256] = 0.0
+    X[3, :128] *= 1e-3
+    codes, scales = O.fp8_quantize_rows(X)
+    assert codes.shape == X.shape and scales.shape == (6, 3) and scales.dtype == np.float32
+    t = O.e4m3_table()
+    for r in range(6):
+        for b in range(3):
+            blk = X[r, 128 * b:128 * (b + 1)]
+            if not blk.any():
+                assert scales[r, b] == 1.0 and not codes[r, 128 * b:128 * (b + 1)].any()
+                continue
+            i = int(np.argmax(np.abs(blk)))
+            assert abs(t[codes[r, 128 * b + i]]) == 448.0
+            assert scales[r, b] == np.float32(np.abs(blk).max()) / np.float32(448.0)
+    Xd = O.fp8_dequantize_rows(codes, scales)
+    s = np.repeat(scales, 128, axis=1).astype(np.float64)
+    bound = 2.0 ** -4 * np.abs(X) + 2.0 ** -10 * s + 2.0 ** -8 * np.abs(Xd)
+    assert np.all(np.abs(Xd - X) <= bound)
+
+
+def test_fp8_payload_rows_and_pads():
+    """Every kept row of the FP8 send buffer is its token's quantisation; pad rows are code 0, scale 0."""
+    rng = np.random.default_rng(2)
+    T, h, E, k = 20, 256, 4, 2
+    ids = np.stack([rng.permutation(E)[:k] for _ in range(T)]).astype(np.int32)
+    d = O.dispatch(ids, E, 8, 1)
+    x = rng.normal(size=(T, h)).astype(np.float32)
+    codes, scales = O.dispatch_payload_fp8(x, d)
+    ct, st = O.fp8_quantize_rows(x)
+    for r in range(d["rows"]):
+        t = d["src_token"][r]
+        if t < 0:
+            assert not codes[r].any() and not scales[r].any()
+        else:
+            assert np.array_equal(codes[r], ct[t]) and np.array_equal(scales[r], st[t])
