@@ -36,7 +36,8 @@ METRIC = "MoE-layer fwd tokens/s at 1 GB300; grouped-GEMM % bf16 peak; dispatch 
 
 def _workload_desc(cfg, C):
     return (f"{cfg.name}: T={cfg.T} h={cfg.h} E={cfg.E} k={cfg.k} F={cfg.F} gating={cfg.gating} "
-            + (f"cf={cfg.cf} (C={C})" if cfg.cf else "dropless") + f" R={cfg.R} shared={cfg.n_shared} {cfg.dtype}")
+            + (f"cf={cfg.cf} (C={C})" if cfg.cf else "dropless") + f" R={cfg.R} shared={cfg.n_shared} {cfg.dtype}"
+            + (" payload=fp8 (e4m3, per-128 scales)" if cfg.payload == "fp8" else ""))
 
 
 def _peaks():
@@ -254,7 +255,7 @@ def run_gpu(args, cfg, C):
                      w_gate=up(inp["wg"]), w_up=up(inp["wu"]), w_down=up(inp["wd"]),
                      shared=tuple(up(np.ascontiguousarray(w)[None]) for w in inp["shared"])
                      if inp["shared"] is not None else None, device=dev, routing=cfg.routing,
-                     backward=want_backward(args, cfg))
+                     backward=want_backward(args, cfg), payload=cfg.payload)
     x = up(inp["x"])
     flush = torch.empty(512 * 2**20, dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream()
@@ -346,7 +347,10 @@ def run_gpu(args, cfg, C):
     ffn_flops = 6.0 * kept * cfg.h * cfg.F + (6.0 * cfg.T * cfg.h * cfg.F if cfg.n_shared else 0.0)
     ffn_ms = ug_ms + dn_ms + sum(float(np.mean(stage_ms[s])) for s in ("shared_up_gate", "shared_down") if s in stage_ms)
     ug_tflops = ug_flops / (ug_ms * 1e-3) / 1e12
-    disp_bytes = (cfg.T + kept) * cfg.h * cfg.el
+    if cfg.payload == "fp8":                         # read x once, write one byte per element + a scale per 128
+        disp_bytes = cfg.T * cfg.h * cfg.el + kept * (cfg.h + cfg.h // 128 * 4)
+    else:
+        disp_bytes = (cfg.T + kept) * cfg.h * cfg.el
     comb_bytes = (kept + cfg.T + (cfg.T if cfg.n_shared else 0)) * cfg.h * cfg.el
     disp_gbs = disp_bytes / (float(np.mean(stage_ms["dispatch"])) * 1e-3) / 1e9
     comb_gbs = comb_bytes / (float(np.mean(stage_ms["combine"])) * 1e-3) / 1e9
@@ -395,7 +399,7 @@ def run_gpu(args, cfg, C):
 
 
 def want_backward(args, cfg) -> bool:
-    return args.backward and cfg.dtype == "bf16" and cfg.routing == "token"
+    return args.backward and cfg.dtype == "bf16" and cfg.routing == "token" and cfg.payload == "bf16"
 
 
 def time_backward(args, cfg, layer, x, flush, stream, kept):

@@ -240,6 +240,26 @@ int moe_combine(const void* eout, const int32_t* dest_row, const float* gates, c
                 int h, int k, int dtype, void* y, void* stream);
 
 /* ---------------------------------------------------------------------------------------------------
+ * FP8 dispatch payload ("10.5 序列并行与专家并行", section 10.5.7: activations that cross nodes can travel in
+ * a low-precision format such as FP8, halving the bytes with negligible effect on model quality).
+ * moe_dispatch_fp8: moe_dispatch with the send buffer in e4m3 (finite-only variant: bias 7, 3 mantissa bits,
+ *   largest magnitude 448). bf16 x, h % 128 == 0. For every kept row r of token t and every block b of 128
+ *   columns: scales[r, b] = max |x[t, block b]| / 448 in fp32 (1 for an all-zero block) and
+ *   buf8[r, col] = e4m3(x[t, col] / scales[r, b]) rounded to nearest, ties to even, saturating at +-448;
+ *   pad rows: codes 0, scale 0. buf8 [rows,h] uint8, scales [rows,h/128] fp32; every other output and the
+ *   workspace as moe_dispatch.
+ * moe_expert_up_gate_fp8: moe_expert_up_gate reading that buffer: each code is dequantised to
+ *   bf16(fp32(value) * scale) inside the GEMM (converter warps turn each staged e4m3 tile into the bf16
+ *   operand tile in shared memory), so the bf16 buffer never exists in memory. act [rows,F] bf16.
+ * ------------------------------------------------------------------------------------------------- */
+int moe_dispatch_fp8(const void* x, const int32_t* topk_ids, int T, int h, int E, int k, int capacity, int num_ranks,
+                     uint8_t* buf8, float* scales, int32_t* offsets, int32_t* kept_counts, int32_t* dest_row,
+                     uint8_t* drop_mask, int32_t* src_token, int32_t* src_slot, int32_t* rank_counts,
+                     int32_t* rank_offsets, int32_t* tile_sched, void* ws, size_t ws_bytes, void* stream);
+int moe_expert_up_gate_fp8(const uint8_t* buf8, const float* scales, const int32_t* tile_sched, const void* packed_w,
+                           int E, int h, int F, int rows, void* act, void* stream);
+
+/* ---------------------------------------------------------------------------------------------------
  * Backward of the layer ("专家并行" (formulaic), section "BWD（反向传播）" and the overlap notes: the
  * gradients return to the experts along the routing path; each expert computes its own weight gradients).
  * The pages give no formulas: these are the chain rule through the forward calls above with the top-k

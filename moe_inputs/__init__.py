@@ -47,6 +47,7 @@ class MoEConfig:
     alpha: float      # Switch aux-loss coefficient
     bias: str         # "none" | "zipf" (added to logits) | "normal" (selection only, std 0.1)
     routing: str = "token"   # "token": each token picks k experts; "expert_choice": each expert picks C tokens
+    payload: str = "bf16"    # dispatch send buffer: "bf16" (the working dtype) or "fp8" (e4m3 + per-128 scales)
 
     @property
     def el(self) -> int:
@@ -84,6 +85,9 @@ CONFIGS = {
     # capacity) with F=1536, so that a full ncu capture of the grouped GEMM holds well under 1 GB on the device
     "page3_profile": MoEConfig("page3_profile", T=4096, h=4096, E=8, k=2, F=1536, gating=GATING_SOFTMAX, cf=1.25,
                                R=8, n_shared=0, dtype="bf16", alpha=0.01, bias="none"),
+    # page-3 worked shape with the dispatch send buffer in FP8 (e4m3, one scale per token and 128 columns)
+    "page3_fp8": MoEConfig("page3_fp8", T=4096, h=4096, E=8, k=2, F=12288, gating=GATING_SOFTMAX, cf=1.25, R=8,
+                           n_shared=0, dtype="bf16", alpha=0.01, bias="none", payload="fp8"),
 }
 CONFIG_ORDER = ["tiny_fp32", "page3_cf1.25", "mixtral_zipf", "deepseek_v3", "qwen3_moe"]
 

@@ -241,10 +241,12 @@ def combine(eout: np.ndarray, dest_row: np.ndarray, gates: np.ndarray, shared_ou
 # ---------------------------------------------------------------------------------------------------------
 
 def moe_layer(x, w_r, bias, weights, *, k: int, gating: str, cf: float, R: int, alpha: float = 0.01,
-              shared=None, experts: str = "swiglu") -> dict:
+              shared=None, experts: str = "swiglu", payload: str = "bf16") -> dict:
     """Full forward: router -> dispatch -> experts -> combine. Inputs are float64 arrays of the
     dtype-rounded values. `weights(e)` gives expert e's matrices; `shared()` the shared expert's (or
-    None). experts="identity" replaces each expert by the identity (eout = buf) for the pins."""
+    None). experts="identity" replaces each expert by the identity (eout = buf) for the pins.
+    payload="fp8": the routed experts read the dequantised FP8 send buffer (dispatch_payload_fp8); the shared
+    expert reads x itself (it is not dispatched)."""
     x = np.asarray(x, np.float64)
     T, h = x.shape
     E = np.asarray(w_r).shape[1]
@@ -252,7 +254,10 @@ def moe_layer(x, w_r, bias, weights, *, k: int, gating: str, cf: float, R: int, 
     r = route(L, k, gating, bias, alpha)
     C = capacity(cf, k, T, E)
     d = dispatch(r["ids"], E, C, R)
-    buf = dispatch_payload(x, d)
+    if payload == "fp8":
+        buf = fp8_dequantize_rows(*dispatch_payload_fp8(x, d))
+    else:
+        buf = dispatch_payload(x, d)
     eout = buf.copy() if experts == "identity" else expert_outputs(buf, d, weights)
     sh = swiglu_ffn(x, *shared()) if shared is not None else None
     y = combine(eout, d["dest_row"], r["gates"], sh)

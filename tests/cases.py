@@ -129,7 +129,7 @@ def build_gpu_layer(cfg, inp, wg, wu, wd, shared=None, device="cuda", backward=F
     layer = MoELayer(T=cfg.T, h=cfg.h, E=cfg.E, k=cfg.k, F=cfg.F, gating=cfg.gating, cf=cfg.cf, R=cfg.R,
                      alpha=cfg.alpha, w_r=to_device(inp["w_r"], cfg, dev), bias=b, w_gate=to_device(wg, cfg, dev),
                      w_up=to_device(wu, cfg, dev), w_down=to_device(wd, cfg, dev), shared=sh, device=dev,
-                     routing=cfg.routing, backward=backward)
+                     routing=cfg.routing, backward=backward, payload=cfg.payload)
     return layer
 
 

@@ -15,6 +15,7 @@
 // fifth kernel zero-fills the pad rows and marks them -1.
 #include <algorithm>
 #include <mutex>
+#include <cuda_fp8.h>
 #include "common.cuh"
 
 namespace moe {
@@ -327,6 +328,84 @@ dispatch_copy_pad_kernel(const T* __restrict__ x, const int32_t* __restrict__ de
     }
 }
 
+// FP8 send buffer ("10.5 序列并行与专家并行", section 10.5.7: activations cross nodes in a low-precision
+// format such as FP8, halving the bytes). Blocks [0, tok_blocks): one warp per token, quantised once: each
+// half-warp covers one 128-column block with 8 columns per lane; amax over the half-warp, s = amax / 448 (1 for
+// an all-zero block), codes = e4m3(x / s) rounded to nearest even with saturation; the 8 code bytes of a lane
+// and (first lane of the half) the scale go to every kept destination row. Blocks [tok_blocks, grid): pad rows
+// (capacity mode) get codes 0, scale 0 and src = -1.
+__global__ void __launch_bounds__(256)
+dispatch_copy_fp8_kernel(const __nv_bfloat16* __restrict__ x, const int32_t* __restrict__ dest_row, int T_, int h,
+                         int k, uint8_t* __restrict__ buf8, float* __restrict__ scales, int tok_blocks,
+                         const int32_t* __restrict__ kept_counts, int E, int C, int32_t* __restrict__ src_token,
+                         int32_t* __restrict__ src_slot) {
+    const int lane = threadIdx.x & 31, half = lane >> 4, hl = lane & 15;
+    const int nblk = h / 128;
+    if ((int)blockIdx.x < tok_blocks) {
+        const int t = blockIdx.x * 8 + (threadIdx.x >> 5);
+        if (t >= T_) return;
+        const int my = lane < k ? dest_row[(size_t)t * k + lane] : -1;
+        int dj[16];
+#pragma unroll
+        for (int j = 0; j < 16; ++j) dj[j] = __shfl_sync(0xffffffffu, my, j);
+        const __nv_bfloat16* src = x + (size_t)t * h;
+        constexpr int U = 2;                          // 2 x 2 blocks of 128 columns per iteration
+        for (int b0 = 0; b0 < nblk; b0 += 2 * U) {
+            Vec16<__nv_bfloat16> v[U];
+#pragma unroll
+            for (int u = 0; u < U; ++u) {
+                const int b = b0 + 2 * u + half;
+                if (b < nblk) v[u] = ld16_stream(src + (size_t)b * 128 + hl * 8);
+                else v[u].v = make_uint4(0, 0, 0, 0);
+            }
+#pragma unroll
+            for (int u = 0; u < U; ++u) {
+                const int b = b0 + 2 * u + half;
+                float f[8];
+                float amax = 0.f;
+#pragma unroll
+                for (int i = 0; i < 8; ++i) {
+                    f[i] = v[u].get(i);
+                    amax = fmaxf(amax, fabsf(f[i]));
+                }
+#pragma unroll
+                for (int off = 8; off > 0; off >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, off));
+                const float sc = amax > 0.f ? amax / 448.f : 1.f;
+                uint32_t w[2];
+#pragma unroll
+                for (int i = 0; i < 2; ++i) {
+                    const __nv_fp8x2_storage_t lo = __nv_cvt_float2_to_fp8x2(make_float2(f[4 * i] / sc, f[4 * i + 1] / sc),
+                                                                             __NV_SATFINITE, __NV_E4M3);
+                    const __nv_fp8x2_storage_t hi = __nv_cvt_float2_to_fp8x2(make_float2(f[4 * i + 2] / sc,
+                                                                                         f[4 * i + 3] / sc),
+                                                                             __NV_SATFINITE, __NV_E4M3);
+                    w[i] = (uint32_t)lo | ((uint32_t)hi << 16);
+                }
+                if (b < nblk) {
+#pragma unroll
+                    for (int j = 0; j < 16; ++j)
+                        if (j < k && dj[j] >= 0) {
+                            *reinterpret_cast<uint2*>(buf8 + (size_t)dj[j] * h + (size_t)b * 128 + hl * 8) =
+                                make_uint2(w[0], w[1]);
+                            if (hl == 0) scales[(size_t)dj[j] * nblk + b] = sc;
+                        }
+                }
+            }
+        }
+        return;
+    }
+    const long long rows = (long long)E * C;
+    const int nb = gridDim.x - tok_blocks;
+    for (long long r = (long long)(blockIdx.x - tok_blocks) * 8 + (threadIdx.x >> 5); r < rows; r += (long long)nb * 8) {
+        const int e = (int)(r / C);
+        if (r - (long long)e * C < kept_counts[e]) continue;
+        if (lane == 0) { src_token[r] = -1; src_slot[r] = -1; }
+        for (int d0 = lane * 16; d0 < h; d0 += 32 * 16)
+            *reinterpret_cast<uint4*>(buf8 + r * h + d0) = make_uint4(0, 0, 0, 0);
+        for (int b = lane; b < nblk; b += 32) scales[r * nblk + b] = 0.f;
+    }
+}
+
 __global__ void dense_sched_kernel(int rows, int32_t* sched) {
     const int ntiles = (rows + MOE_TILE_M - 1) / MOE_TILE_M;
     if (blockIdx.x == 0 && threadIdx.x == 0) { sched[0] = ntiles; sched[1] = 1; sched[2] = 0; sched[3] = ntiles; }
@@ -510,4 +589,58 @@ extern "C" int moe_dispatch_static(const void* x, const int32_t* topk_ids, int T
     return moe_dispatch(x, topk_ids, T, h, E, k, capacity, num_ranks, dtype, buf, offsets, kept_counts, dest_row,
                         drop_mask, src_token, src_slot, rank_counts, rank_offsets, tile_sched, scratch,
                         moe::kStaticScratchBytes, stream);
+}
+
+extern "C" int moe_dispatch_fp8(const void* x, const int32_t* topk_ids, int T, int h, int E, int k, int capacity,
+                                int num_ranks, uint8_t* buf8, float* scales, int32_t* offsets, int32_t* kept_counts,
+                                int32_t* dest_row, uint8_t* drop_mask, int32_t* src_token, int32_t* src_slot,
+                                int32_t* rank_counts, int32_t* rank_offsets, int32_t* tile_sched, void* ws,
+                                size_t ws_bytes, void* stream) {
+    MOE_REQUIRE(T >= 0 && h > 0 && h % 128 == 0, MOE_ERR_INVALID_ARG, "moe_dispatch_fp8: T=%d h=%d (need h%%128==0)",
+                T, h);
+    MOE_REQUIRE(E >= 1 && E <= 1024 && k >= 1 && k <= E && k <= 16, MOE_ERR_INVALID_ARG,
+                "moe_dispatch_fp8: E=%d k=%d", E, k);
+    MOE_REQUIRE(capacity >= 0, MOE_ERR_INVALID_ARG, "moe_dispatch_fp8: capacity %d < 0", capacity);
+    MOE_REQUIRE(num_ranks >= 1 && num_ranks <= E && E % num_ranks == 0, MOE_ERR_INVALID_ARG,
+                "moe_dispatch_fp8: num_ranks %d must divide E=%d", num_ranks, E);
+    const long long rows = (long long)moe_dispatch_rows(T, E, k, capacity);
+    MOE_REQUIRE(rows < (1LL << 31), MOE_ERR_INVALID_ARG, "moe_dispatch_fp8: %lld rows overflow int32", rows);
+    MOE_REQUIRE(offsets && kept_counts && rank_counts && rank_offsets && tile_sched, MOE_ERR_INVALID_ARG,
+                "moe_dispatch_fp8: null pointer");
+    MOE_REQUIRE(T == 0 || (x && topk_ids && dest_row && drop_mask), MOE_ERR_INVALID_ARG,
+                "moe_dispatch_fp8: null pointer");
+    MOE_REQUIRE(rows == 0 || (buf8 && scales && src_token && src_slot), MOE_ERR_INVALID_ARG,
+                "moe_dispatch_fp8: null pointer");
+    MOE_REQUIRE(aligned16(x) && aligned16(buf8) && aligned16(tile_sched), MOE_ERR_INVALID_ARG,
+                "moe_dispatch_fp8: x, buf8 and tile_sched must be 16-byte aligned");
+    const size_t need = moe_dispatch_workspace_size(T, E, k, capacity);
+    MOE_REQUIRE(ws_bytes >= need && (need == 0 || ws), MOE_ERR_WORKSPACE, "moe_dispatch_fp8: workspace %zu < %zu",
+                ws_bytes, need);
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    unsigned* err = device_error_word();
+    MOE_REQUIRE(err, MOE_ERR_CUDA, "moe_dispatch_fp8: device error word unavailable");
+    int32_t* chunk = static_cast<int32_t*>(ws);
+    const int nch = num_chunks(T, k);
+    if (nch > 0) {
+        dispatch_count_kernel<<<nch, kChunkA, E * sizeof(int), s>>>(topk_ids, T, E, k, kChunkA / k, chunk, err);
+        if (int rc = check_launch("dispatch_count_kernel")) return rc;
+    }
+    dispatch_scan_kernel<<<1, 1024, 0, s>>>(chunk, nch, E, capacity, num_ranks, offsets, kept_counts, rank_counts,
+                                           rank_offsets, tile_sched);
+    if (int rc = check_launch("dispatch_scan_kernel")) return rc;
+    if (nch > 0) {
+        const size_t smem = (size_t)32 * E * sizeof(int);
+        cudaFuncSetAttribute(dispatch_scatter_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        dispatch_scatter_kernel<<<nch, kChunkA, smem, s>>>(topk_ids, T, E, k, capacity, chunk, offsets, dest_row,
+                                                          drop_mask, src_token, src_slot);
+        if (int rc = check_launch("dispatch_scatter_kernel")) return rc;
+    }
+    const int tok_blocks = cdiv(T, 8);
+    const int pad_blocks = (capacity > 0 && rows > 0) ? std::min(cdiv(rows, 8), 2 * num_sms()) : 0;
+    if (tok_blocks + pad_blocks > 0) {
+        dispatch_copy_fp8_kernel<<<tok_blocks + pad_blocks, 256, 0, s>>>(static_cast<const __nv_bfloat16*>(x), dest_row,
+            T, h, k, buf8, scales, tok_blocks, kept_counts, E, capacity, src_token, src_slot);
+        if (int rc = check_launch("dispatch_copy_fp8_kernel")) return rc;
+    }
+    return MOE_OK;
 }

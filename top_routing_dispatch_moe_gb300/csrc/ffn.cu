@@ -65,6 +65,17 @@ extern "C" int moe_expert_down_shared(const void* act, const int32_t* tile_sched
                        packed_shared, out_shared);
 }
 
+extern "C" int moe_expert_up_gate_fp8(const uint8_t* buf8, const float* scales, const int32_t* tile_sched,
+                                      const void* packed_w, int E, int h, int F, int rows, void* act, void* stream) {
+    MOE_REQUIRE(E >= 1 && E <= 1024 && h > 0 && h % 128 == 0 && F > 0 && F % 8 == 0 && rows >= 0, MOE_ERR_INVALID_ARG,
+                "moe_expert_up_gate_fp8: E=%d h=%d F=%d rows=%d (need h%%128==0, F%%8==0)", E, h, F, rows);
+    if (rows == 0) return MOE_OK;
+    MOE_REQUIRE(buf8 && scales && tile_sched && packed_w && act, MOE_ERR_INVALID_ARG, "moe_expert_up_gate_fp8: null pointer");
+    MOE_REQUIRE(aligned16(buf8) && aligned16(tile_sched) && aligned16(packed_w) && aligned16(act), MOE_ERR_INVALID_ARG,
+                "moe_expert_up_gate_fp8: pointers must be 16-byte aligned");
+    return ffn_tc_up_gate_fp8(buf8, scales, tile_sched, packed_w, E, h, F, rows, act, static_cast<cudaStream_t>(stream));
+}
+
 extern "C" size_t moe_expert_ffn_workspace_size(int rows, int F, int dtype) {
     if (rows < 0 || F <= 0) return 0;
     return align_up((size_t)rows * F * (dtype == MOE_F32 ? 4 : 2), 256);

@@ -53,6 +53,9 @@ int ffn_tc_down(const void* act, const int32_t* sched, const void* packed, int E
                 cudaStream_t s, const void* act_sh = nullptr, int T_sh = 0, const void* packed_sh = nullptr,
                 void* out_sh = nullptr);
 
+// Up/gate GEMM on the FP8 send buffer (e4m3 codes + per-row, per-128-column scales), dequantised in the prologue.
+int ffn_tc_up_gate_fp8(const uint8_t* buf8, const float* scales, const int32_t* sched, const void* packed, int E, int h,
+                       int F, int rows, void* act, cudaStream_t s);
 // Backward on the tensor cores (bf16): down dgrad; up/gate recompute with the SwiGLU backward epilogue, then
 // the up/gate dgrad; the experts' weight gradients from K-major transposed operands.
 int ffn_tc_down_backward(const void* d_eout, const int32_t* sched, const void* packed_bwd, int E, int h, int F,

@@ -28,6 +28,7 @@
 #include <cuda.h>
 #include <cudaTypedefs.h>
 #include <math.h>
+#include <cuda_fp8.h>
 #include <algorithm>
 #include <mutex>
 #include "ffn.cuh"
@@ -41,6 +42,9 @@ constexpr int UK = 16;                       // K per tcgen05.mma (kind::f16)
 constexpr int A_BYTES = BM * BK * 2;         // 16 KB
 constexpr int TMEM_COLS = 512;               // 2 accumulators x up to 256 fp32 columns
 constexpr int NUM_THREADS = 192;
+constexpr int NUM_THREADS_A8 = 448;          // + 8 warps that dequantise an e4m3 A operand into the bf16 stage
+constexpr int A8_CONVERTER_WARPS = 8;
+constexpr int A8_BYTES = BM * BK;            // 8 KB: a 128 x 64 e4m3 tile
 
 // Tile width (UMMA N) and ring depth: 256 columns x 4 stages of 48 KB. (A 192-column tile with 5 stages of
 // 40 KB was measured for the down GEMM: 2 % faster on the page-3 shape, where it shortens the last wave,
@@ -52,8 +56,10 @@ struct TileCfg {
     static constexpr int B_BYTES = BN * BK * 2;
     static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
     static constexpr int SMEM_BYTES = 1024 /* alignment slack */ + STAGES * STAGE_BYTES + 256 /* barriers, flags */;
+    static constexpr int SMEM_BYTES_A8 = SMEM_BYTES + STAGES * A8_BYTES;   // + the e4m3 staging tiles
     static_assert(BN % 32 == 0 && BN >= 32 && BN <= 256, "UMMA N for M = 128");
     static_assert(SMEM_BYTES <= 227 * 1024, "shared memory per CTA");
+    static_assert(SMEM_BYTES_A8 <= 227 * 1024, "shared memory per CTA (e4m3 operand)");
 };
 using Wide = TileCfg<256, 4>;
 constexpr long long kDrainLimit = 1LL << 24;
@@ -207,6 +213,9 @@ struct Params {
                               // or out2 (up, b odd), row (b / 2) * 128 + i of expert e's [F][ldo] matrix
     int wg_F;                 // wg_gu: valid rows F of each de-interleaved matrix
     float* out2;
+    // e4m3 A operand (A8 kernels): value = bf16(fp32(e4m3) * a_scales[row * a_nblk + column / 128]), rows < a_rows
+    const float* a_scales;
+    int a_nblk, a_rows;
 };
 
 // sh: the item belongs to the shared expert; K steps kb0 .. kb0 + nkb of BK columns starting at column kx0
@@ -364,8 +373,8 @@ __device__ __forceinline__ void store_tile(const Params& p, __nv_bfloat16* out, 
     }
 }
 
-template <int EPI, class CF>
-__global__ void __launch_bounds__(NUM_THREADS, 1)
+template <int EPI, class CF, bool A8 = false>
+__global__ void __launch_bounds__(A8 ? NUM_THREADS_A8 : NUM_THREADS, 1)
 grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                     const __grid_constant__ CUtensorMap tmA2, const __grid_constant__ CUtensorMap tmB2, Params p) {
     constexpr int BN = CF::BN, STAGES = CF::STAGES, B_BYTES = CF::B_BYTES, STAGE_BYTES = CF::STAGE_BYTES;
@@ -377,19 +386,27 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
     uint8_t* smem = smem_raw + ((1024u - (raw_addr & 1023u)) & 1023u);
     const uint32_t sbase = smem_u32(smem);
     const uint32_t sA = sbase, sB = sbase + STAGES * A_BYTES;
-    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + STAGES * STAGE_BYTES);
+    const uint32_t s8 = sB + STAGES * B_BYTES;                   // A8: e4m3 staging tiles
+    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + STAGES * STAGE_BYTES + (A8 ? STAGES * A8_BYTES : 0));
     const uint32_t bar0 = smem_u32(bars);
     auto full = [&](int s) { return bar0 + 8u * s; };
     auto empty = [&](int s) { return bar0 + 8u * (STAGES + s); };
     auto tfull = [&](int a) { return bar0 + 8u * (2 * STAGES + a); };
     auto tempty = [&](int a) { return bar0 + 8u * (2 * STAGES + 2 + a); };
     const uint32_t mma_done = bar0 + 8u * (2 * STAGES + 4);
-    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * STAGES + 5);
+    auto raw = [&](int s) { return bar0 + 8u * (2 * STAGES + 5 + s); };   // A8: the TMA copies of a stage landed
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 3 * STAGES + 5);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+    // with A8 the MMA waits for the converter warps instead of the copies
+    auto landed = [&](int s) { return A8 ? raw(s) : full(s); };
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     if (threadIdx.x == 0) {
-        for (int s = 0; s < STAGES; ++s) { mbar_init(full(s), 1); mbar_init(empty(s), 1); }
+        for (int s = 0; s < STAGES; ++s) {
+            mbar_init(full(s), A8 ? A8_CONVERTER_WARPS : 1);
+            mbar_init(empty(s), 1);
+            mbar_init(raw(s), 1);
+        }
         for (int a = 0; a < 2; ++a) { mbar_init(tfull(a), 1); mbar_init(tempty(a), 4); }
         mbar_init(mma_done, 1);
         *abort_flag = 0;
@@ -429,9 +446,15 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
                 bool ok = true;
                 for (int kb = 0; kb < wk.nkb; ++kb) {
                     if (!wait_phase(empty(stage), phase ^ 1u, p.wait_limit, abort_flag, p.err, 0x10u)) { ok = false; break; }
-                    mbar_expect_tx(full(stage), STAGE_BYTES);
-                    tma_load_2d(sA + stage * A_BYTES, ma, wk.kx0 + kb * BK, wk.row0, full(stage));
-                    tma_load_2d(sB + stage * B_BYTES, mb, wk.kx0 + kb * BK, brow, full(stage));
+                    if constexpr (A8) {
+                        mbar_expect_tx(raw(stage), A8_BYTES + B_BYTES);
+                        tma_load_2d(s8 + stage * A8_BYTES, ma, wk.kx0 + kb * BK, wk.row0, raw(stage));
+                        tma_load_2d(sB + stage * B_BYTES, mb, wk.kx0 + kb * BK, brow, raw(stage));
+                    } else {
+                        mbar_expect_tx(full(stage), STAGE_BYTES);
+                        tma_load_2d(sA + stage * A_BYTES, ma, wk.kx0 + kb * BK, wk.row0, full(stage));
+                        tma_load_2d(sB + stage * B_BYTES, mb, wk.kx0 + kb * BK, brow, full(stage));
+                    }
                     issued |= 1u << stage;
                     last_par = (last_par & ~(1u << stage)) | (phase << stage);
                     if (++stage == STAGES) { stage = 0; phase ^= 1u; }
@@ -439,7 +462,7 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
                 if (!ok) break;
             }
             for (int s = 0; s < STAGES; ++s)        // every issued copy has landed before the CTA exits
-                if (issued & (1u << s)) drain_phase(full(s), (last_par >> s) & 1u, p.err, 0x11u);
+                if (issued & (1u << s)) drain_phase(landed(s), (last_par >> s) & 1u, p.err, 0x11u);
         }
     } else if (warp == 1) {
         if (lane == 0) {
@@ -471,6 +494,47 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
             }
             umma_commit(mma_done);                  // all MMAs finished before the columns are freed
             drain_phase(mma_done, 0, p.err, 0x22u);
+        }
+    } else if (A8 && warp >= 6) {
+        // ---------------------------------------------------------------------- e4m3 -> bf16 (warps 6..13)
+        // Threads i and i + 128 own row i of the stage, 4 of its 8 16-byte chunks each: codes -> fp32 value * the
+        // row's block scale -> bf16, written in the 128-byte-swizzled layout a TMA copy of that bf16 tile would
+        // produce (chunk c of row i at chunk c ^ (i % 8)); then a proxy fence so the tensor core sees the generic
+        // stores, and one arrival per warp on the stage's full barrier.
+        const int i = (threadIdx.x - 192) & (BM - 1), c0 = ((threadIdx.x - 192) >> 7) * 4;
+        int stage = 0;
+        uint32_t phase = 0;
+        for (int w = blockIdx.x; w < total && !*abort_flag; w += gridDim.x) {
+            const Work wk = map_item(p, E, w, nr, KB);
+            const int row = wk.row0 + i;
+            bool ok = true;
+            for (int kb = 0; kb < wk.nkb; ++kb) {
+                if (!wait_phase(raw(stage), phase, p.wait_limit, abort_flag, p.err, 0x40u)) { ok = false; break; }
+                const int col = wk.kx0 + kb * BK;
+                const float sc = row < p.a_rows ? __ldg(p.a_scales + (size_t)row * p.a_nblk + (col >> 7)) : 0.f;
+                const uint8_t* src = smem + (s8 - sbase) + stage * A8_BYTES + i * BK;
+                uint8_t* dst = smem + stage * A_BYTES + i * 128;
+#pragma unroll
+                for (int c = c0; c < c0 + 4; ++c) {
+                    const uint2 q = *reinterpret_cast<const uint2*>(src + 8 * c);
+                    const uint32_t qw[2] = {q.x, q.y};
+                    uint32_t o[4];
+#pragma unroll
+                    for (int hw = 0; hw < 4; ++hw) {
+                        const __nv_fp8x2_storage_t pr = (__nv_fp8x2_storage_t)((qw[hw >> 1] >> (16 * (hw & 1))) & 0xFFFFu);
+                        const __half2_raw hr = __nv_cvt_fp8x2_to_halfraw2(pr, __NV_E4M3);
+                        const float2 fv = __half22float2(*reinterpret_cast<const __half2*>(&hr));
+                        const __nv_bfloat162 bv = __floats2bfloat162_rn(fv.x * sc, fv.y * sc);
+                        o[hw] = *reinterpret_cast<const uint32_t*>(&bv);
+                    }
+                    *reinterpret_cast<uint4*>(dst + ((c ^ (i & 7)) << 4)) = make_uint4(o[0], o[1], o[2], o[3]);
+                }
+                asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+                __syncwarp();
+                if (lane == 0) mbar_arrive(full(stage));
+                if (++stage == STAGES) { stage = 0; phase ^= 1u; }
+            }
+            if (!ok) break;
         }
     } else {
         // ---------------------------------------------------------------------- epilogue (warps 2..5)
@@ -850,6 +914,44 @@ static int make_map(CUtensorMap* m, const void* base, long long rows, long long 
 // (p.sh_rows > 0); otherwise the routed maps are passed twice and never read through the second pair.
 struct SharedOperands { const void* a; const void* b; long long b_rows; };
 
+// 2-D uint8 tensor [rows, cols] (e4m3 codes), box [box_rows, 64 columns] = 64 bytes per row, no swizzle.
+static int make_map_u8(CUtensorMap* m, const void* base, long long rows, long long cols, int box_rows) {
+    auto fn = encode_fn();
+    MOE_REQUIRE(fn, MOE_ERR_CUDA, "cuTensorMapEncodeTiled unavailable from the driver");
+    cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
+    cuuint64_t strides[1] = {(cuuint64_t)cols};
+    cuuint32_t box[2] = {(cuuint32_t)BK, (cuuint32_t)box_rows};
+    cuuint32_t estr[2] = {1, 1};
+    CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims, strides, box, estr,
+                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    MOE_REQUIRE(r == CUDA_SUCCESS, MOE_ERR_CUDA, "cuTensorMapEncodeTiled (u8) failed (%d) rows=%lld cols=%lld", (int)r,
+                rows, cols);
+    return MOE_OK;
+}
+
+// The one-SM kernel with an e4m3 A operand dequantised in its prologue (p.a_scales, p.a_nblk, p.a_rows).
+template <int EPI>
+static int gemm_a8(const void* a8, long long a_rows, const void* b, long long b_rows_total, const Params& p,
+                   cudaStream_t s) {
+    using CF = Wide;
+    static bool attr_set[64];
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64)
+        return set_error(MOE_ERR_CUDA, "grouped_gemm (e4m3): no usable current device");
+    if (!attr_set[dev]) {
+        cudaError_t e = cudaFuncSetAttribute(grouped_gemm_kernel<EPI, CF, true>,
+                                             cudaFuncAttributeMaxDynamicSharedMemorySize, CF::SMEM_BYTES_A8);
+        if (e != cudaSuccess) return set_error(MOE_ERR_CUDA, "grouped_gemm (e4m3) smem attribute: %s", cudaGetErrorString(e));
+        attr_set[dev] = true;
+    }
+    CUtensorMap ma, mb;
+    if (int rc = make_map_u8(&ma, a8, a_rows, p.K, BM)) return rc;
+    if (int rc = make_map(&mb, b, b_rows_total, p.K, CF::BN)) return rc;
+    grouped_gemm_kernel<EPI, CF, true><<<num_sms(), NUM_THREADS_A8, CF::SMEM_BYTES_A8, s>>>(ma, mb, ma, mb, p);
+    return check_launch("grouped_gemm_kernel<up_gate, e4m3 A>");
+}
+
 template <int EPI, class CF>
 static int gemm(const void* a, long long a_rows, const void* b, long long b_rows_total, const Params& p,
                 cudaStream_t s, const SharedOperands& sh = SharedOperands{}) {
@@ -951,6 +1053,22 @@ int ffn_tc_down(const void* act, const int32_t* sched, const void* packed, int E
                                 (long long)h};
     if (tc::use_pair(E, rows)) return tc::gemm_pair<tc::EPI_BF16>(act, rows, b, (long long)E * h, p, s, sh);
     return tc::gemm<tc::EPI_BF16, CF>(act, rows, b, (long long)E * h, p, s, sh);
+}
+
+// Up/gate GEMM + SwiGLU on the FP8 send buffer: A = e4m3 codes [rows, h] with per-row, per-128-column fp32
+// scales, dequantised to bf16 in the kernel's prologue.
+int ffn_tc_up_gate_fp8(const uint8_t* buf8, const float* scales, const int32_t* sched, const void* packed, int E, int h,
+                       int F, int rows, void* act, cudaStream_t s) {
+    const PackedLayout L = packed_layout(E, h, F, 2);
+    unsigned* err = device_error_word();
+    MOE_REQUIRE(err, MOE_ERR_CUDA, "device error word unavailable");
+    tc::Params p{sched, h, L.Fp / 128, 2 * L.Fp, F, F, static_cast<__nv_bfloat16*>(act), nullptr, nullptr, err,
+                 wait_limit(), 0, nullptr};
+    p.a_scales = scales;
+    p.a_nblk = h / 128;
+    p.a_rows = rows;
+    return tc::gemm_a8<tc::EPI_SWIGLU>(buf8, rows, static_cast<const char*>(packed) + L.up_gate_off,
+                                       (long long)E * 2 * L.Fp, p, s);
 }
 
 // d_act [rows, F] = d_eout [rows, h] @ W_down[e] per expert, with W_down^T [E][F][h] (backward packing) as

@@ -31,7 +31,7 @@ class MoELayer:
     STAGES = ("router", "dispatch", "up_gate", "down", "shared_up_gate", "shared_down", "combine")
 
     def __init__(self, *, T, h, E, k, F, gating, cf, R, alpha, w_r, bias, w_gate, w_up, w_down,
-                 shared=None, device="cuda", routing="token", backward=False):
+                 shared=None, device="cuda", routing="token", backward=False, payload="bf16"):
         self.T, self.h, self.E, self.k, self.F = T, h, E, k, F
         self.gating, self.R, self.alpha = gating, R, alpha
         self.C = capacity_slots(cf, k, T, E)
@@ -51,6 +51,9 @@ class MoELayer:
         i32, f32 = torch.int32, torch.float32
         code = moe.dtype_code(dt)
         self.routing = routing
+        if payload not in ("bf16", "fp8") or (payload == "fp8" and (routing != "token" or dt != torch.bfloat16)):
+            raise ValueError("payload: 'bf16', or 'fp8' with token-choice routing in bf16")
+        self.payload = payload
         if routing == "expert_choice":
             # every expert takes C = cf * k * T / E tokens (k: the average number of experts per token)
             self.rows = E * self.C
@@ -82,6 +85,10 @@ class MoELayer:
                           tile_sched=torch.empty(moe.moe_tile_sched_bytes(T, E, k, self.C) // 4, dtype=i32,
                                                  device=dev))
         self.d_ws = moe._bytes_tensor(moe.moe_dispatch_workspace_size(T, E, k, self.C), dev)
+        if payload == "fp8":                         # the FP8 send buffer replaces the bf16 one
+            self.d_out.pop("buf")
+            self.d_out["buf8"] = torch.empty((self.rows, h), dtype=torch.uint8, device=dev)
+            self.d_out["scales"] = torch.empty((self.rows, h // 128), dtype=f32, device=dev)
         self.act = torch.empty((self.rows, F), dtype=dt, device=dev)
         self.eout = torch.empty((self.rows, h), dtype=dt, device=dev)
         if self.shared_packed is not None:
@@ -116,12 +123,20 @@ class MoELayer:
         if self.routing == "expert_choice":
             moe.moe_expert_choice_dispatch(x, self.ec["tokens"], buf=self.d_out["buf"],
                                            tile_sched=self.d_out["tile_sched"], stream=stream)
+        elif self.payload == "fp8":
+            moe.moe_dispatch_fp8(x, r["topk_ids"], self.E, self.C, self.R, out=self.d_out, ws=self.d_ws, stream=stream)
         else:
             moe.moe_dispatch(x, r["topk_ids"], self.E, self.C, self.R, out=self.d_out, ws=self.d_ws, stream=stream)
         mark("dispatch")
         sched = self.d_out["tile_sched"]
         shared_out = None
-        if self.shared_packed is not None and self.dtype == torch.bfloat16:
+        if self.payload == "fp8":
+            moe.moe_expert_up_gate_fp8(self.d_out["buf8"], self.d_out["scales"], sched, self.packed, self.E, self.F,
+                                       act=self.act, stream=stream)
+            mark("up_gate")
+            moe.moe_expert_down(self.act, sched, self.packed, self.E, self.h, eout=self.eout, stream=stream)
+            mark("down")
+        elif self.shared_packed is not None and self.dtype == torch.bfloat16:
             # the shared expert's tiles run inside the routed experts' launches
             moe.moe_expert_up_gate_shared(self.d_out["buf"], sched, self.packed, self.E, self.F, x, self.shared_packed,
                                           act=self.act, act_shared=self.sh_act, stream=stream)
@@ -160,8 +175,8 @@ class MoELayer:
         "expert_dgrad", "expert_wgrad", ["shared_bwd"], "router_bwd", "dispatch_bwd")."""
         if self.packed_bwd is None:
             raise RuntimeError("MoELayer.backward: build the layer with backward=True")
-        if self.routing != "token" or self.dtype != torch.bfloat16:
-            raise NotImplementedError("MoELayer.backward: token-choice routing in bf16")
+        if self.routing != "token" or self.dtype != torch.bfloat16 or self.payload != "bf16":
+            raise NotImplementedError("MoELayer.backward: token-choice routing in bf16 with the bf16 send buffer")
 
         def mark(stage):
             if events is not None:

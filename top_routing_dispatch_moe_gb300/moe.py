@@ -44,6 +44,8 @@ _SIGS = {
     "moe_expert_up_gate": (_I, [_P, _P, _P, _I, _I, _I, _I, _I, _P, _P]),
     "moe_expert_down": (_I, [_P, _P, _P, _I, _I, _I, _I, _I, _P, _P]),
     "moe_expert_up_gate_shared": (_I, [_P, _P, _P, _I, _I, _I, _I, _P, _I, _P, _P, _I, _P, _P]),
+    "moe_dispatch_fp8": (_I, [_P, _P, _I, _I, _I, _I, _I, _I, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _Z, _P]),
+    "moe_expert_up_gate_fp8": (_I, [_P, _P, _P, _P, _I, _I, _I, _I, _P, _P]),
     "moe_combine_backward": (_I, [_P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _P, _P, _P]),
     "moe_router_backward_workspace_size": (_Z, [_I, _I]),
     "moe_router_backward": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _F, _F, _P, _P, _P, _Z, _P]),
@@ -207,6 +209,44 @@ def moe_dispatch(x, topk_ids, E: int, capacity: int = 0, num_ranks: int = 1, *, 
                              _ptr(o["rank_offsets"]), _ptr(o["tile_sched"]), _ptr(ws), ws.numel(), _stream(stream)))
     o["rows"] = rows
     return o
+
+
+def moe_dispatch_fp8(x, topk_ids, E: int, capacity: int = 0, num_ranks: int = 1, *, out=None, ws=None, stream=None):
+    """moe_dispatch with the send buffer in FP8: returns dict(buf8 [rows, h] uint8 e4m3 codes, scales [rows, h/128]
+    fp32, and every index output of moe_dispatch). `out` may hold preallocated tensors under those names."""
+    T, h = x.shape
+    k = topk_ids.shape[1]
+    dev = x.device
+    rows = moe_dispatch_rows(T, E, k, capacity)
+    o = dict(out or {})
+    o.setdefault("buf8", torch.empty((rows, h), dtype=torch.uint8, device=dev))
+    o.setdefault("scales", torch.empty((rows, h // 128), dtype=torch.float32, device=dev))
+    o.setdefault("offsets", torch.empty(E + 1, dtype=torch.int32, device=dev))
+    o.setdefault("kept_counts", torch.empty(E, dtype=torch.int32, device=dev))
+    o.setdefault("dest_row", torch.empty((T, k), dtype=torch.int32, device=dev))
+    o.setdefault("drop_mask", torch.empty((T, k), dtype=torch.uint8, device=dev))
+    o.setdefault("src_token", torch.empty(rows, dtype=torch.int32, device=dev))
+    o.setdefault("src_slot", torch.empty(rows, dtype=torch.int32, device=dev))
+    o.setdefault("rank_counts", torch.empty(num_ranks, dtype=torch.int32, device=dev))
+    o.setdefault("rank_offsets", torch.empty(num_ranks + 1, dtype=torch.int32, device=dev))
+    o.setdefault("tile_sched", torch.empty(moe_tile_sched_bytes(T, E, k, capacity) // 4, dtype=torch.int32,
+                                           device=dev))
+    ws = _bytes_tensor(moe_dispatch_workspace_size(T, E, k, capacity), dev) if ws is None else ws
+    _check(_lib.moe_dispatch_fp8(_ptr(x), _ptr(topk_ids), T, h, E, k, capacity, num_ranks, _ptr(o["buf8"]),
+                                 _ptr(o["scales"]), _ptr(o["offsets"]), _ptr(o["kept_counts"]), _ptr(o["dest_row"]),
+                                 _ptr(o["drop_mask"]), _ptr(o["src_token"]), _ptr(o["src_slot"]), _ptr(o["rank_counts"]),
+                                 _ptr(o["rank_offsets"]), _ptr(o["tile_sched"]), _ptr(ws), ws.numel(), _stream(stream)))
+    o["rows"] = rows
+    return o
+
+
+def moe_expert_up_gate_fp8(buf8, scales, tile_sched, packed_w, E: int, F: int, act=None, stream=None):
+    rows, h = buf8.shape
+    if act is None:
+        act = torch.empty((rows, F), dtype=torch.bfloat16, device=buf8.device)
+    _check(_lib.moe_expert_up_gate_fp8(_ptr(buf8), _ptr(scales), _ptr(tile_sched), _ptr(packed_w), E, h, F, rows,
+                                       _ptr(act), _stream(stream)))
+    return act
 
 
 def moe_dispatch_static(x, topk_ids, E: int, capacity: int = 0, num_ranks: int = 1, *, out=None, stream=None):
