@@ -673,7 +673,8 @@ __device__ __forceinline__ void umma_commit_pair(uint32_t bar) {
                  : "memory");
 }
 
-struct PairWork { int e, arow, row0, row1, n, sh; };   // arow: first row this CTA loads; [row0, row1): rows it stores
+// arow: first row this CTA loads; [row0, row1): rows it stores; K steps 0 .. nkb - 1 from column kx0
+struct PairWork { int e, arow, row0, row1, n, sh, kx0, nkb; };
 
 // Work item w -> (expert, n-tile, pair of 128-row tiles), expert-major, n-tile next, pair fastest; this CTA
 // (rank 0 or 1) takes the first or second tile of the pair. pp: per-expert prefix of pair counts.
@@ -691,19 +692,34 @@ __device__ __forceinline__ PairWork map_pair(const int32_t* sched, const int* pp
     const int t0 = __ldg(prefix + e), mt = __ldg(prefix + e + 1) - t0;
     const bool has = 2 * q + rank < mt;
     const int4 ent = __ldg(reinterpret_cast<const int4*>(sched + sched_tiles_offset(E)) + t0 + 2 * q + (has ? rank : 0));
-    return PairWork{ent.x, ent.y, has ? ent.y : 0, has ? ent.z : 0, n, 0};
+    return PairWork{ent.x, ent.y, has ? ent.y : 0, has ? ent.z : 0, n, 0, 0, 0};
 }
 
 // Merged list of the 2-SM kernel: routed pair items and the shared expert's dense 256-row pairs (n-tile
 // major, pair fastest); a pair whose second tile starts past the shared rows is a phantom for rank 1.
-__device__ __forceinline__ PairWork map_pair_item(const Params& p, const int* pp, int E, int w, int nr, int rank) {
+__device__ __forceinline__ PairWork map_pair_item(const Params& p, const int* pp, int E, int w, int nr, int rank,
+                                                  int KB) {
     int idx;
-    if (!split_item(w, nr, idx)) return map_pair(p.sched, pp, E, p.NT, idx, rank);
+    if (p.wg_E > 0) {                        // weight gradient: (expert, n-tile, pair of m-tiles), K = its segment
+        const int np = (p.wg_MT + 1) / 2, per_e = np * p.NT;
+        const int e = w / per_e, rem = w - e * per_e;
+        const int n = rem / np, q = rem - n * np;
+        const int m = 2 * q + rank;
+        const bool has = m < p.wg_MT;
+        const int k0 = __ldg(p.seg + e), k1 = __ldg(p.seg + e + 1);
+        return PairWork{e, (has ? m : 2 * q) * BM, has ? m * BM : 0, has ? min(m * BM + BM, p.wg_M) : 0, n, 0, k0,
+                        (k1 - k0) / BK};
+    }
+    if (!split_item(w, nr, idx)) {
+        PairWork wk = map_pair(p.sched, pp, E, p.NT, idx, rank);
+        wk.nkb = KB;
+        return wk;
+    }
     const int np = (p.sh_rows + 2 * BM - 1) / (2 * BM);
     const int n = idx / np, q = idx % np;
     const int row0 = 2 * BM * q + BM * rank;
     const bool has = row0 < p.sh_rows;
-    return PairWork{0, has ? row0 : 2 * BM * q, has ? row0 : 0, has ? min(row0 + BM, p.sh_rows) : 0, n, 1};
+    return PairWork{0, has ? row0 : 2 * BM * q, has ? row0 : 0, has ? min(row0 + BM, p.sh_rows) : 0, n, 1, 0, KB};
 }
 
 template <int EPI>
@@ -732,7 +748,7 @@ grouped_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_c
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const uint32_t rank = cluster_rank();
     const bool leader = rank == 0;
-    const int E = __ldg(p.sched + 1);
+    const int E = p.wg_E > 0 ? p.wg_E : __ldg(p.sched + 1);
     if (threadIdx.x == 0) {
         for (int s = 0; s < STAGES; ++s) { mbar_init(full(s), 1); mbar_init(empty(s), 1); }
         for (int a = 0; a < 2; ++a) { mbar_init(tfull(a), 1); mbar_init(tempty(a), 8); }
@@ -744,7 +760,7 @@ grouped_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_c
         prefetch_tmap(&tmB);
         if (p.sh_rows) { prefetch_tmap(&tmA2); prefetch_tmap(&tmB2); }
     }
-    if (warp == 2) {                         // pair prefix: pp[e + 1] = sum over e' <= e of ceil(tiles_e' / 2)
+    if (warp == 2 && p.wg_E == 0) {          // pair prefix: pp[e + 1] = sum over e' <= e of ceil(tiles_e' / 2)
         const int32_t* prefix = p.sched + kSchedHeader;
         int carry = 0;
         if (lane == 0) s_pp[0] = 0;
@@ -768,8 +784,14 @@ grouped_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_c
     const uint32_t peer_abort = map_rank(smem_u32(const_cast<int*>(abort_flag)), rank ^ 1u);
 
     const int NC = gridDim.x >> 1, cid = blockIdx.x >> 1;
-    const int nr = s_pp[E] * p.NT;                                      // routed items
-    const int ns = (p.sh_rows + 2 * BM - 1) / (2 * BM) * p.NT;         // shared-expert items
+    int nr, ns;
+    if (p.wg_E > 0) {                                                   // weight gradient
+        nr = p.wg_E * ((p.wg_MT + 1) / 2) * p.NT;
+        ns = 0;
+    } else {
+        nr = s_pp[E] * p.NT;                                            // routed items
+        ns = (p.sh_rows + 2 * BM - 1) / (2 * BM) * p.NT;                // shared-expert items
+    }
     const int total = nr + ns;
     const int KB = (p.K + BK - 1) / BK;
     int my_rounds = 0;
@@ -780,20 +802,20 @@ grouped_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_c
             int stage = 0;
             uint32_t phase = 0;
             for (int w = cid; w < total && !*abort_flag; w += NC) {
-                const PairWork wk = map_pair_item(p, s_pp, E, w, nr, rank);
+                const PairWork wk = map_pair_item(p, s_pp, E, w, nr, rank, KB);
                 const int brow = wk.e * p.b_rows + wk.n * BN + (int)rank * 128;
                 const CUtensorMap* ma = wk.sh ? &tmA2 : &tmA;
                 const CUtensorMap* mb = wk.sh ? &tmB2 : &tmB;
                 bool ok = true;
-                for (int kb = 0; kb < KB; ++kb) {
+                for (int kb = 0; kb < wk.nkb; ++kb) {
                     if (!wait_phase_pair(empty(stage), phase ^ 1u, p.wait_limit, abort_flag, peer_abort, p.err, 0x40u)) {
                         ok = false;
                         break;
                     }
                     if (leader) mbar_expect_tx(full(stage), 2 * PAIR_STAGE_BYTES);
                     const uint32_t fb = map_rank(full(stage), 0);
-                    tma_load_2d_pair(sA + stage * A_BYTES, ma, kb * BK, wk.arow, fb);
-                    tma_load_2d_pair(sB + stage * B_HALF_BYTES, mb, kb * BK, brow, fb);
+                    tma_load_2d_pair(sA + stage * A_BYTES, ma, wk.kx0 + kb * BK, wk.arow, fb);
+                    tma_load_2d_pair(sB + stage * B_HALF_BYTES, mb, wk.kx0 + kb * BK, brow, fb);
                     ++my_rounds;
                     if (++stage == STAGES) { stage = 0; phase ^= 1u; }
                 }
@@ -814,8 +836,9 @@ grouped_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_c
                     break;
                 tc_fence_after();
                 const uint32_t d_tmem = tmem + (uint32_t)(a * BN);
+                const int nkb = map_pair_item(p, s_pp, E, w, nr, 0, KB).nkb;
                 bool ok = true;
-                for (int kb = 0; kb < KB; ++kb) {
+                for (int kb = 0; kb < nkb; ++kb) {
                     if (!wait_phase_pair(full(stage), phase, p.wait_limit, abort_flag, peer_abort, p.err, 0x51u)) {
                         ok = false;
                         break;
@@ -844,11 +867,22 @@ grouped_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_c
             const uint32_t aph = (iter >> 1) & 1;
             if (!wait_phase_pair(tfull(a), aph, p.wait_limit, abort_flag, peer_abort, p.err, 0x60u)) break;
             tc_fence_after();
-            const PairWork wk = map_pair_item(p, s_pp, E, w, nr, rank);
-            const int row = wk.row0 + lane_base + lane;
-            const bool live = row < wk.row1;
+            const PairWork wk = map_pair_item(p, s_pp, E, w, nr, rank, KB);
+            int row = wk.row0 + lane_base + lane;
+            bool live = row < wk.row1;
+            float* outf = nullptr;
+            if (p.wg_E > 0) {
+                if (p.wg_gu) {                       // de-interleave: this CTA's m-tile is one packed gate/up block
+                    const int b = wk.row0 / BM, f = (b >> 1) * BM + lane_base + lane;
+                    outf = ((b & 1) ? p.out2 : p.out_f32) + ((size_t)wk.e * p.wg_F + (b >> 1) * BM) * p.ldo;
+                    live = live && f < p.wg_F;
+                    row = lane_base + lane;
+                } else {
+                    outf = p.out_f32 + (size_t)wk.e * p.wg_M * p.ldo;
+                }
+            }
             const uint32_t tbase = tmem + (uint32_t)(a * BN) + ((uint32_t)lane_base << 16);
-            store_tile<EPI, BN>(p, wk.sh ? p.sh_out : p.out, tbase, row, live, wk.n);
+            store_tile<EPI, BN>(p, wk.sh ? p.sh_out : p.out, tbase, row, live, wk.n, outf, wk.nkb == 0);
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive_cluster(tempty_leader + 8u * a);
@@ -1015,7 +1049,8 @@ static int gemm_pair(const void* a, long long a_rows, const void* b, long long b
     }
     grouped_gemm_pair_kernel<EPI><<<2 * clusters[dev], NUM_THREADS, PAIR_SMEM_BYTES, s>>>(ma, mb, ma2, mb2, p);
     return check_launch(EPI == EPI_SWIGLU ? "grouped_gemm_pair_kernel<up_gate>"
-                        : EPI == EPI_SWIGLU_BWD ? "grouped_gemm_pair_kernel<swiglu_bwd>" : "grouped_gemm_pair_kernel<bf16>");
+                        : EPI == EPI_SWIGLU_BWD ? "grouped_gemm_pair_kernel<swiglu_bwd>"
+                        : EPI == EPI_F32 ? "grouped_gemm_pair_kernel<f32>" : "grouped_gemm_pair_kernel<bf16>");
 }
 
 // The 2-SM kernel when the average expert has at least four 128-row tiles (an odd tile count costs a
@@ -1121,6 +1156,7 @@ int ffn_tc_weight_grad(const void* At, const void* Bt, long long ktot, const int
                 "weight gradient: K extent %lld", ktot);
     tc::Params p{seg, (int)ktot, cdiv(N, 256), 0, N, N, nullptr, out, nullptr, err, wait_limit(), 0, nullptr, nullptr,
                  E, cdiv(M, tc::BM), M, seg, gu, F, out2};
+    if (cdiv(M, tc::BM) >= 2) return tc::gemm_pair<tc::EPI_F32>(At, M, Bt, N, p, s);   // pairs of m-tiles
     return tc::gemm<tc::EPI_F32, tc::Wide>(At, M, Bt, N, p, s);
 }
 
