@@ -518,11 +518,28 @@ router_finalize(const float* __restrict__ partial_P, const int32_t* __restrict__
         const int e = e0 + tid % min(E - e0, (int)blockDim.x);
         const int s = tid / min(E - e0, (int)blockDim.x);
         const int Se = (int)blockDim.x / min(E - e0, (int)blockDim.x);
-        float ps = 0.f;
+        // 8 independent running sums per thread (8 loads in flight), added in a fixed order at the end
+        float ps[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+        int cs[8] = {0, 0, 0, 0, 0, 0, 0, 0};
+        if (s < Se && e < E) {
+            int b = s;
+            for (; b + 7 * Se < grid; b += 8 * Se) {
+#pragma unroll
+                for (int u = 0; u < 8; ++u) {
+                    ps[u] += partial_P[(size_t)(b + u * Se) * E + e];
+                    cs[u] += partial_C[(size_t)(b + u * Se) * E + e];
+                }
+            }
+            for (; b < grid; b += Se) {
+                ps[0] += partial_P[(size_t)b * E + e];
+                cs[0] += partial_C[(size_t)b * E + e];
+            }
+        }
+        float psum = 0.f;
         int c = 0;
-        if (s < Se && e < E)
-            for (int b = s; b < grid; b += Se) { ps += partial_P[(size_t)b * E + e]; c += partial_C[(size_t)b * E + e]; }
-        s_p[tid] = ps;
+#pragma unroll
+        for (int u = 0; u < 8; ++u) { psum += ps[u]; c += cs[u]; }
+        s_p[tid] = psum;
         s_c[tid] = c;
         __syncthreads();
         const int ew = min(E - e0, (int)blockDim.x);
