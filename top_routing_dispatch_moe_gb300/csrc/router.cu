@@ -589,6 +589,9 @@ router_transpose_kernel(const T* __restrict__ w, int h, int E, T* __restrict__ w
 // ---------------------------------------------------------------------------------------------------
 // Upper bound of the blocks of any router launch (sizes the partial-sum workspace).
 static int router_grid(int T) { return std::max(1, std::min(cdiv(T, kRouterWarps), kRouterMaxBlocks)); }
+// The gating kernel on stored logits: a few tokens per warp, at most two blocks per SM, so that the finalize
+// reduces few per-block partials.
+static int gate_grid(int T) { return std::max(1, std::min(router_grid(T), 2 * num_sms())); }
 // The fused small-E kernel stages the router weight into every block, takes two tokens per warp, and its
 // register budget allows two blocks per SM.
 static int router_small_grid(int T) { return std::max(1, std::min(cdiv(T, 2 * kRouterWarps), 2 * num_sms())); }
@@ -667,7 +670,7 @@ extern "C" int moe_router(const void* x, const void* w_r, const float* bias, int
     MOE_REQUIRE(ws_bytes >= w.bytes && (w.bytes == 0 || ws), MOE_ERR_WORKSPACE,
                 "moe_router: workspace %zu < %zu bytes", ws_bytes, w.bytes);
     cudaStream_t s = static_cast<cudaStream_t>(stream);
-    const int G = !small ? router_grid(T) : dtype == MOE_BF16 ? router_mma_grid(T) : router_small_grid(T);
+    const int G = !small ? gate_grid(T) : dtype == MOE_BF16 ? router_mma_grid(T) : router_small_grid(T);
     GateOut o{topk_ids, gates, logits, w.partial_P, w.partial_C};
     if (T > 0) {
         if (small && dtype == MOE_BF16) {
@@ -753,7 +756,7 @@ extern "C" int moe_router_from_logits(const float* logits, const float* bias, in
     MOE_REQUIRE(ws && ws_bytes >= need, MOE_ERR_WORKSPACE, "moe_router_from_logits: workspace %zu < %zu", ws_bytes,
                 need);
     cudaStream_t s = static_cast<cudaStream_t>(stream);
-    const int G = router_grid(T);
+    const int G = gate_grid(T);              // <= router_grid(T), which sizes the workspace
     char* base = static_cast<char*>(ws);
     GateOut o{topk_ids, gates, nullptr, reinterpret_cast<float*>(base),
               reinterpret_cast<int32_t*>(base + align_up((size_t)G * E * 4, 256))};
