@@ -399,7 +399,7 @@ def run_gpu(args, cfg, C):
 
 
 def want_backward(args, cfg) -> bool:
-    return args.backward and cfg.dtype == "bf16" and cfg.routing == "token" and cfg.payload == "bf16"
+    return args.backward and cfg.dtype == "bf16" and cfg.routing in ("token", "sinkhorn") and cfg.payload == "bf16"
 
 
 def time_backward(args, cfg, layer, x, flush, stream, kept):

@@ -447,7 +447,9 @@ def route_backward(L: np.ndarray, r: dict, d_gates: np.ndarray, gating: str, alp
     (S the sum over the k chosen). aux = alpha E sum_e f_e P_e with P_e = mean_t q[t, e], q = p (softmax modes)
     or s / sum_e s (sigmoid mode), so d aux / d q[t, e] = alpha E f_e / T.
     Softmax modes: dq -> dL by the softmax Jacobian dL = p * (dp - <dp, p>). Sigmoid mode: dq -> ds by the
-    Jacobian of s / sum(s), then dL = ds * s (1 - s)."""
+    Jacobian of s / sum(s), then dL = ds * s (1 - s). The softmax mode with a selection-only bias (Sinkhorn
+    routing: the ids are chosen on L + log c, the gates are p[ids]) is the plain softmax mode here: the
+    selection is held constant, so the bias and the column scalings that produced it carry no gradient."""
     T, E = L.shape
     ids, gates, f = r["ids"], r["gates"], r["f"]
     k = ids.shape[1]
@@ -466,7 +468,7 @@ def route_backward(L: np.ndarray, r: dict, d_gates: np.ndarray, gating: str, alp
         return ds * s * (1.0 - s)
     p = softmax(L)
     dp = np.zeros((T, E))
-    if gating == SOFTMAX:
+    if gating in (SOFTMAX, SOFTMAX_SELBIAS):
         np.add.at(dp, (np.repeat(np.arange(T), k), ids.ravel()), d_gates.ravel())
     elif gating == SOFTMAX_RENORM:
         Sk = p[rows, ids].sum(axis=1, keepdims=True)

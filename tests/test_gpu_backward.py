@@ -223,3 +223,38 @@ def test_layer_backward(name):
     for what, got, want in checks:
         err = cases.rel_l2(got, want)
         assert err <= 2e-2, f"{what}: rel err {err:.3e}"
+
+
+def test_layer_backward_sinkhorn():
+    """Sinkhorn routing: the ids come from L + log c, the gates are softmax(L)[ids]; with the selection held
+    constant the backward is the plain softmax one (the Zipf logit bias gets d_bias). Against the oracle's
+    backward of its own Sinkhorn forward."""
+    import torch
+    cfg = moe_inputs.get_config("mixtral_sinkhorn", T=400, h=256, F=128)
+    inp = cases.router_inputs(cfg, bias=moe_inputs.load_zipf_bias(moe_inputs.get_config("mixtral_zipf")))
+    assert inp["near_ties"] == 0
+    wg, wu, wd = moe_inputs.all_expert_weights(cfg)
+    layer = cases.build_gpu_layer(cfg, inp, wg, wu, wd, backward=True)
+    x = cases.to_device(inp["x"], cfg)
+    layer.forward(x)
+    rng = np.random.default_rng(17)
+    dy = torch.from_numpy(rng.normal(size=(cfg.T, cfg.h)).astype(np.float32)).to("cuda").to(x.dtype)
+    g = layer.backward(x, dy, d_aux=0.7)
+    torch.cuda.synchronize()
+    x64 = moe_inputs.to_f64(inp["x"], cfg.dtype)
+    w_r64 = moe_inputs.to_f64(inp["w_r"], cfg.dtype)
+    wfn = cases.weights_fn_from(cfg, wg, wu, wd)
+    L = O.router_logits(x64, w_r64, inp["bias"], O.SOFTMAX)
+    r = O.route_sinkhorn(L, cfg.k, alpha=cfg.alpha)
+    np.testing.assert_array_equal(layer.r_out["topk_ids"].cpu().numpy(), r["ids"])
+    d = O.dispatch(r["ids"], cfg.E, O.capacity(cfg.cf, cfg.k, cfg.T, cfg.E), cfg.R)
+    buf = O.dispatch_payload(x64, d)
+    eout = O.expert_outputs(buf, d, wfn)
+    fwd = dict(router=r, dispatch=d, buf=buf, eout=eout)
+    ref = O.moe_layer_backward(x64, w_r64, inp["bias"], wfn, fwd, _np(dy), gating=O.SOFTMAX_SELBIAS, alpha=cfg.alpha,
+                               d_aux=0.7)
+    for what, got, want in [("dx", _np(g["dx"]), ref["dx"]), ("dW_r", _np(g["dW_r"]), ref["dW_r"]),
+                            ("d_bias", _np(g["d_bias"]), ref["d_bias"]),
+                            ("dW_down", _np(g["dW_down"]), np.stack([w[2] for w in ref["dW"]]))]:
+        err = cases.rel_l2(got, want)
+        assert err <= 2e-2, f"{what}: rel err {err:.3e}"

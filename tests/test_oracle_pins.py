@@ -657,3 +657,42 @@ def test_fp8_payload_rows_and_pads():
             assert not codes[r].any() and not scales[r].any()
         else:
             assert np.array_equal(codes[r], ct[t]) and np.array_equal(scales[r], st[t])
+
+
+def test_backward_sinkhorn_matches_finite_differences():
+    """Sinkhorn routing (ids chosen on L + log c, gates softmax(L)[ids]) through the layer: the backward in the
+    selection-bias mode against central differences of that forward (the Sinkhorn scalings move with L, but the
+    selection does not move under a 1e-6 step, and the scalings enter only the selection)."""
+    rng = np.random.default_rng(21)
+    T, h, E, k, F = 9, 5, 4, 2, 3
+    x = rng.normal(size=(T, h))
+    w_r = rng.normal(size=(h, E))
+    bias = rng.normal(size=E) * 0.3
+    W = [(rng.normal(size=(F, h)), rng.normal(size=(F, h)), rng.normal(size=(h, F))) for _ in range(E)]
+    dy = rng.normal(size=(T, h))
+    alpha, d_aux = 0.3, 0.7
+
+    def forward(x, w_r, bias):
+        L = O.router_logits(x, w_r, bias, O.SOFTMAX)
+        r = O.route_sinkhorn(L, k, alpha=alpha)
+        d = O.dispatch(r["ids"], E, 0, 1)
+        buf = O.dispatch_payload(x, d)
+        eout = O.expert_outputs(buf, d, lambda e: W[e])
+        y = O.combine(eout, d["dest_row"], r["gates"])
+        return float(np.sum(dy * y) + d_aux * r["aux"]), dict(router=r, dispatch=d, buf=buf, eout=eout)
+
+    _, fwd = forward(x, w_r, bias)
+    g = O.moe_layer_backward(x, w_r, bias, lambda e: W[e], fwd, dy, gating=O.SOFTMAX_SELBIAS, alpha=alpha, d_aux=d_aux)
+    eps = 1e-6
+
+    def bump(a, idx, e):
+        b = a.copy()
+        b[idx] += e
+        return b
+
+    for got, pert in [(g["dx"][2, 3], lambda e: (bump(x, (2, 3), e), w_r, bias)),
+                      (g["dx"][7, 0], lambda e: (bump(x, (7, 0), e), w_r, bias)),
+                      (g["dW_r"][1, 2], lambda e: (x, bump(w_r, (1, 2), e), bias)),
+                      (g["d_bias"][3], lambda e: (x, w_r, bump(bias, 3, e)))]:
+        num = (forward(*pert(eps))[0] - forward(*pert(-eps))[0]) / (2 * eps)
+        assert abs(num - got) <= 1e-6 * max(1.0, abs(num)), (num, got)

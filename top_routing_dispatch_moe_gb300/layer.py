@@ -169,14 +169,15 @@ class MoELayer:
     def backward(self, x, dy, d_aux=1.0, stream=None, events=None):
         """Gradients of <dy, y> + d_aux * aux for the last forward(x): returns dict(dx, dW_r, d_bias, dW_gate,
         dW_up, dW_down[, shared_dW_gate, shared_dW_up, shared_dW_down]); weight gradients fp32, dx in the
-        layer's dtype. Token-choice routing, bf16, and a layer built with backward=True. Order of the calls:
+        layer's dtype. Token-choice or Sinkhorn routing, bf16, and a layer built with backward=True. Order of the calls:
         combine, expert down / up-gate dgrad, expert weight gradients, [shared expert], router, router weight,
         dispatch (+ the router and shared terms of dx). `events` as in forward (stages "combine_bwd",
         "expert_dgrad", "expert_wgrad", ["shared_bwd"], "router_bwd", "dispatch_bwd")."""
         if self.packed_bwd is None:
             raise RuntimeError("MoELayer.backward: build the layer with backward=True")
-        if self.routing != "token" or self.dtype != torch.bfloat16 or self.payload != "bf16":
-            raise NotImplementedError("MoELayer.backward: token-choice routing in bf16 with the bf16 send buffer")
+        if self.routing not in ("token", "sinkhorn") or self.dtype != torch.bfloat16 or self.payload != "bf16":
+            raise NotImplementedError("MoELayer.backward: token-choice or Sinkhorn routing in bf16 with the bf16 "
+                                      "send buffer")
 
         def mark(stage):
             if events is not None:
@@ -242,7 +243,9 @@ class MoELayer:
                                         ws=b["ws_sh"], stream=stream)
             sh_dx = b["sh_dx"]
             mark("shared_bwd")
-        want_bias = self.bias is not None and self.gating in ("softmax", "softmax_renorm")
+        # the bias is part of the logits in the plain softmax modes and under Sinkhorn routing (whose router runs
+        # in the plain softmax mode); the sigmoid mode's bias only selects
+        want_bias = self.bias is not None and (self.gating in ("softmax", "softmax_renorm") or self.routing == "sinkhorn")
         d_logits, d_bias = moe.moe_router_backward(r["logits"], r["topk_ids"], r["gates"], b["d_gates"], r["f"],
                                                    self.gating, self.alpha, d_aux, d_logits=b["d_logits"],
                                                    want_bias_grad=want_bias, ws=b["ws_rb"], stream=stream)
