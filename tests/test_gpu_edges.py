@@ -206,3 +206,31 @@ def test_router_small_expert_counts(E, k, T, h):
     assert cases.rel_max(r["logits"].cpu().numpy(), ref["logits"]) <= 1e-5
     assert cases.rel_max(r["gates"].cpu().numpy(), ref["gates"]) <= 1e-5
     assert cases.rel_max(r["P"].cpu().numpy(), ref["P"]) <= 1e-5
+
+
+@pytest.mark.parametrize("name,E,k", [("page3_cf1.25", 64, 2), ("deepseek_v3", 256, 8), ("qwen3_moe", 128, 8)])
+@pytest.mark.parametrize("T,h", [(1, 256), (100, 1024), (700, 200), (2500, 2048)])
+@pytest.mark.parametrize("want_logits", [True, False])
+def test_router_large_expert_counts(name, E, k, T, h, want_logits):
+    """The bf16 router for E > 32: logits on the tensor cores, split over K into up to 16 partial products
+    when the 128 x 256 output tiles are fewer than the SMs (one token: 4 chunks of 64 columns for h=256;
+    h=200 ends in an 8-column chunk), summed with the bias by the gating kernel. Each workload's gating
+    (softmax for E=64 and 128, sigmoid with selection bias for E=256); the logits output requested or not."""
+    import torch
+    from top_routing_dispatch_moe_gb300 import moe
+    cfg = moe_inputs.get_config(name, T=T, h=h, E=E, k=k, F=128, R=1)
+    inp = cases.router_inputs(cfg)
+    assert inp["near_ties"] == 0
+    x = cases.to_device(inp["x"], cfg)
+    w = cases.to_device(inp["w_r"], cfg)
+    b = None if inp["bias"] is None else torch.from_numpy(np.asarray(inp["bias"], np.float32)).cuda()
+    r = moe.moe_router(x, w, b, k, cfg.gating, cfg.alpha, want_logits=want_logits)
+    torch.cuda.synchronize()
+    assert moe.moe_check_device_error() == moe.MOE_OK, moe.moe_last_error_string()
+    ref = inp["route"]
+    np.testing.assert_array_equal(r["ids"].cpu().numpy(), ref["ids"])
+    np.testing.assert_array_equal(r["counts"].cpu().numpy(), ref["counts"])
+    if want_logits:
+        assert cases.rel_max(r["logits"].cpu().numpy(), ref["logits"]) <= 1e-5
+    assert cases.rel_max(r["gates"].cpu().numpy(), ref["gates"]) <= 1e-5
+    assert cases.rel_max(r["P"].cpu().numpy(), ref["P"]) <= 1e-5

@@ -69,6 +69,11 @@ int ffn_tc_weight_grad(const void* At, const void* Bt, long long ktot, const int
 // Router logits on the tensor cores (bf16 x and transposed router weight, fp32 logits + bias).
 int tc_router_logits(const void* x, const void* w_rT, const float* bias, int T, int h, int E, const int32_t* sched,
                      float* logits, cudaStream_t s);
+// Split-K variant for few output tiles: parts [S][T][E] fp32, part q = x[:, Q] @ w_rT[:, Q]^T over the columns
+// Q = [q kchunk, min(h, (q + 1) kchunk)) (kchunk a multiple of 64, every part non-empty); the caller adds the
+// parts (and the bias) in order.
+int tc_router_logits_split(const void* x, const void* w_rT, int T, int h, int E, int S, int kchunk, float* parts,
+                           cudaStream_t s);
 // Dense tile schedule of `rows` rows (one group), launched on `s`.
 int launch_dense_sched(int rows, int32_t* sched, cudaStream_t s);
 

@@ -216,7 +216,21 @@ struct Params {
     // e4m3 A operand (A8 kernels): value = bf16(fp32(e4m3) * a_scales[row * a_nblk + column / 128]), rows < a_rows
     const float* a_scales;
     int a_nblk, a_rows;
+    // weight-gradient mapping without a segment array (seg == null): part e covers columns
+    // [e * wg_kchunk, min(K, (e + 1) * wg_kchunk)), wg_kchunk a multiple of BK (split-K partial products)
+    int wg_kchunk;
 };
+
+// K range of part / expert e in the weight-gradient mapping.
+__device__ __forceinline__ void wg_krange(const Params& p, int e, int& k0, int& nkb) {
+    if (p.seg) {
+        k0 = __ldg(p.seg + e);
+        nkb = (__ldg(p.seg + e + 1) - k0) / BK;
+    } else {
+        k0 = e * p.wg_kchunk;
+        nkb = max(0, (min(p.K, k0 + p.wg_kchunk) - k0 + BK - 1) / BK);
+    }
+}
 
 // sh: the item belongs to the shared expert; K steps kb0 .. kb0 + nkb of BK columns starting at column kx0
 struct Work { int e, row0, row1, n, sh, kx0, nkb; };
@@ -255,8 +269,9 @@ __device__ __forceinline__ Work map_item(const Params& p, int E, int w, int nr, 
         const int per_e = p.wg_MT * p.NT;
         const int e = w / per_e, rem = w - e * per_e;
         const int n = rem / p.wg_MT, m = rem - n * p.wg_MT;
-        const int k0 = __ldg(p.seg + e), k1 = __ldg(p.seg + e + 1);
-        return Work{e, m * BM, min(m * BM + BM, p.wg_M), n, 0, k0, (k1 - k0) / BK};
+        int k0, nkb;
+        wg_krange(p, e, k0, nkb);
+        return Work{e, m * BM, min(m * BM + BM, p.wg_M), n, 0, k0, nkb};
     }
     if (!split_item(w, nr, idx)) {
         Work wk = map_work(p.sched, E, p.NT, idx);
@@ -421,7 +436,7 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
 
-    const int E = __ldg(p.sched + 1);
+    const int E = p.wg_E > 0 ? p.wg_E : __ldg(p.sched + 1);
     const int KB = (p.K + BK - 1) / BK;
     int nr, ns;
     if (p.wg_E > 0) {                                            // weight gradient: every expert's tiles
@@ -706,9 +721,9 @@ __device__ __forceinline__ PairWork map_pair_item(const Params& p, const int* pp
         const int n = rem / np, q = rem - n * np;
         const int m = 2 * q + rank;
         const bool has = m < p.wg_MT;
-        const int k0 = __ldg(p.seg + e), k1 = __ldg(p.seg + e + 1);
-        return PairWork{e, (has ? m : 2 * q) * BM, has ? m * BM : 0, has ? min(m * BM + BM, p.wg_M) : 0, n, 0, k0,
-                        (k1 - k0) / BK};
+        int k0, nkb;
+        wg_krange(p, e, k0, nkb);
+        return PairWork{e, (has ? m : 2 * q) * BM, has ? m * BM : 0, has ? min(m * BM + BM, p.wg_M) : 0, n, 0, k0, nkb};
     }
     if (!split_item(w, nr, idx)) {
         PairWork wk = map_pair(p.sched, pp, E, p.NT, idx, rank);
@@ -1167,6 +1182,18 @@ int tc_router_logits(const void* x, const void* w_rT, const float* bias, int T, 
     unsigned* err = device_error_word();
     MOE_REQUIRE(err, MOE_ERR_CUDA, "device error word unavailable");
     tc::Params p{sched, h, cdiv(E, tc::Wide::BN), E, E, E, nullptr, logits, bias, err, wait_limit(), 0, nullptr};
+    return tc::gemm<tc::EPI_F32, tc::Wide>(x, T, w_rT, E, p, s);
+}
+
+int tc_router_logits_split(const void* x, const void* w_rT, int T, int h, int E, int S, int kchunk, float* parts,
+                           cudaStream_t s) {
+    unsigned* err = device_error_word();
+    MOE_REQUIRE(err, MOE_ERR_CUDA, "device error word unavailable");
+    MOE_REQUIRE(S >= 1 && kchunk > 0 && kchunk % tc::BK == 0 && (long long)(S - 1) * kchunk < h, MOE_ERR_INVALID_ARG,
+                "tc_router_logits_split: S=%d kchunk=%d h=%d", S, kchunk, h);
+    tc::Params p{nullptr, h, cdiv(E, tc::Wide::BN), 0, E, E, nullptr, parts, nullptr, err, wait_limit(), 0, nullptr,
+                 nullptr, S, cdiv(T, tc::BM), T, nullptr, 0, 0, nullptr};
+    p.wg_kchunk = kchunk;
     return tc::gemm<tc::EPI_F32, tc::Wide>(x, T, w_rT, E, p, s);
 }
 

@@ -476,10 +476,13 @@ router_logits_gemm(const T* __restrict__ x, const T* __restrict__ w, const float
     }
 }
 
+// Gating on stored logits. The logits of token t are sum over q < nparts of logits[q part_stride + t E + e]
+// (split-K partial products, added in part order) + lbias[e] (null: none); when o.logits is set the sums are
+// written there.
 template <int NPL>
 __global__ void __launch_bounds__(kRouterWarps * 32)
-router_gate_kernel(const float* __restrict__ logits, const float* __restrict__ bias, int T_, int E, int k, int gating,
-                   GateOut o) {
+router_gate_kernel(const float* __restrict__ logits, int nparts, size_t part_stride, const float* __restrict__ lbias,
+                   const float* __restrict__ bias, int T_, int E, int k, int gating, GateOut o) {
     extern __shared__ __align__(16) unsigned char smem_raw[];
     float* s_P = reinterpret_cast<float*>(smem_raw);
     int* s_hist = reinterpret_cast<int*>(s_P + kRouterWarps * E);
@@ -495,6 +498,28 @@ router_gate_kernel(const float* __restrict__ logits, const float* __restrict__ b
         for (int i = 0; i < NPL; ++i) {
             int e = lane + 32 * i;
             L[i] = e < E ? logits[(size_t)t * E + e] : -INFINITY;
+        }
+        if (nparts > 1 || lbias) {
+            for (int q = 1; q < nparts; ++q) {
+                const float* lq = logits + q * part_stride + (size_t)t * E;
+#pragma unroll
+                for (int i = 0; i < NPL; ++i) {
+                    int e = lane + 32 * i;
+                    if (e < E) L[i] += lq[e];
+                }
+            }
+#pragma unroll
+            for (int i = 0; i < NPL; ++i) {
+                int e = lane + 32 * i;
+                if (e < E && lbias) L[i] += lbias[e];
+            }
+        }
+        if (o.logits) {
+#pragma unroll
+            for (int i = 0; i < NPL; ++i) {
+                int e = lane + 32 * i;
+                if (e < E) o.logits[(size_t)t * E + e] = L[i];
+            }
         }
         gate_token<NPL>(L, t, E, k, gating, bias, o, Pacc, s_hist);
     }
@@ -617,9 +642,25 @@ static bool use_small_path(int h, int E, int el) {
 // stores 16-byte aligned); otherwise on the CUDA cores.
 static bool use_tc_logits(int E, int dtype, bool small) { return !small && dtype == MOE_BF16 && E % 4 == 0; }
 
-struct RouterWs { float* partial_P; int32_t* partial_C; float* logits; void* w_rT; int32_t* sched; size_t bytes; };
+// Split of the tensor-core logits GEMM's contraction: with fewer 128 x 256 output tiles than SMs, the K range is
+// cut into S chunks of kchunk columns (a multiple of 64, every chunk non-empty), S <= 16, so that about one tile
+// of one chunk lands on each SM. S = 1: no split.
+struct RouterSplit { int S, kchunk; };
+static RouterSplit router_split(int T, int h, int E, bool tc) {
+    if (!tc || T <= 0) return {1, h};
+    const long long tiles = (long long)cdiv(T, 128) * cdiv(E, 256);
+    const int S0 = (int)std::min<long long>(std::min(16, cdiv(h, 64)), num_sms() / tiles);
+    if (S0 < 2) return {1, h};
+    const int kchunk = cdiv(cdiv(h, S0), 64) * 64;
+    return {cdiv(h, kchunk), kchunk};
+}
 
-static RouterWs router_ws_layout(void* ws, int T, int h, int E, int el, bool small, bool need_logits, bool tc) {
+struct RouterWs {
+    float* partial_P; int32_t* partial_C; float* logits; void* w_rT; int32_t* sched; float* parts; size_t bytes;
+};
+
+static RouterWs router_ws_layout(void* ws, int T, int h, int E, int el, bool small, bool need_logits, bool tc,
+                                 int split) {
     RouterWs w{};
     const int G = router_grid(T);
     size_t off = 0;
@@ -634,6 +675,8 @@ static RouterWs router_ws_layout(void* ws, int T, int h, int E, int el, bool sma
         w.w_rT = base + off; off = align_up(off + (size_t)E * h * el, 256);
     }
     if (tc) { w.sched = reinterpret_cast<int32_t*>(base + off); off = align_up(off + sched_words(T, 1) * 4, 256); }
+    w.parts = nullptr;
+    if (split > 1) { w.parts = reinterpret_cast<float*>(base + off); off = align_up(off + (size_t)split * T * E * 4, 256); }
     w.bytes = off;
     return w;
 }
@@ -647,7 +690,8 @@ extern "C" size_t moe_router_workspace_size(int T, int h, int E, int k, int dtyp
     if (T < 0 || h <= 0 || E <= 0) return 0;
     const int el = dtype == MOE_F32 ? 4 : 2;
     const bool small = use_small_path(h, E, el);
-    return router_ws_layout(nullptr, T, h, E, el, small, !small, use_tc_logits(E, dtype, small)).bytes;
+    const bool tc = use_tc_logits(E, dtype, small);
+    return router_ws_layout(nullptr, T, h, E, el, small, !small, tc, router_split(T, h, E, tc).S).bytes;
 }
 
 extern "C" int moe_router(const void* x, const void* w_r, const float* bias, int T, int h, int E, int k, int dtype,
@@ -666,7 +710,8 @@ extern "C" int moe_router(const void* x, const void* w_r, const float* bias, int
     const int el = dtype == MOE_F32 ? 4 : 2;
     const bool small = use_small_path(h, E, el);
     const bool tc = use_tc_logits(E, dtype, small);
-    RouterWs w = router_ws_layout(ws, T, h, E, el, small, !small && logits == nullptr, tc);
+    const RouterSplit sp = router_split(T, h, E, tc);
+    RouterWs w = router_ws_layout(ws, T, h, E, el, small, !small && logits == nullptr && sp.S == 1, tc, sp.S);
     MOE_REQUIRE(ws_bytes >= w.bytes && (w.bytes == 0 || ws), MOE_ERR_WORKSPACE,
                 "moe_router: workspace %zu < %zu bytes", ws_bytes, w.bytes);
     cudaStream_t s = static_cast<cudaStream_t>(stream);
@@ -700,14 +745,18 @@ extern "C" int moe_router(const void* x, const void* w_r, const float* bias, int
 #undef MOE_SMALL_LAUNCH
             if (int rc = check_launch("router_small_kernel")) return rc;
         } else {
-            float* lg = logits ? logits : w.logits;
+            float* lg = sp.S > 1 ? w.parts : logits ? logits : w.logits;
             const float* lbias = bias_in_logits(gating) ? bias : nullptr;
             if (tc) {
                 router_transpose_kernel<__nv_bfloat16><<<dim3(cdiv(E, 32), cdiv(h, 32)), dim3(32, 8), 0, s>>>(
                     static_cast<const __nv_bfloat16*>(w_r), h, E, static_cast<__nv_bfloat16*>(w.w_rT));
                 if (int rc = check_launch("router_transpose_kernel")) return rc;
-                if (int rc = launch_dense_sched(T, w.sched, s)) return rc;
-                if (int rc = tc_router_logits(x, w.w_rT, lbias, T, h, E, w.sched, lg, s)) return rc;
+                if (sp.S > 1) {
+                    if (int rc = tc_router_logits_split(x, w.w_rT, T, h, E, sp.S, sp.kchunk, lg, s)) return rc;
+                } else {
+                    if (int rc = launch_dense_sched(T, w.sched, s)) return rc;
+                    if (int rc = tc_router_logits(x, w.w_rT, lbias, T, h, E, w.sched, lg, s)) return rc;
+                }
             } else {
                 dim3 grid(cdiv(E, 64), cdiv(T, 64));
                 if (dtype == MOE_BF16)
@@ -720,10 +769,13 @@ extern "C" int moe_router(const void* x, const void* w_r, const float* bias, int
             }
             const size_t smem = (size_t)kRouterWarps * E * sizeof(float) + (size_t)E * sizeof(int);
             const int npl = cdiv(E, 32);
-            o.logits = nullptr;
+            // unsplit: the GEMM wrote the final logits (bias included); split: the gate adds the parts and the bias
+            o.logits = sp.S > 1 ? logits : nullptr;
+            const float* gbias = sp.S > 1 ? lbias : nullptr;
+            const size_t pstride = (size_t)T * E;
 #define MOE_GATE_LAUNCH(N)                                                                              \
             cudaFuncSetAttribute(router_gate_kernel<N>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem); \
-            router_gate_kernel<N><<<G, kRouterWarps * 32, smem, s>>>(lg, bias, T, E, k, gating, o);
+            router_gate_kernel<N><<<G, kRouterWarps * 32, smem, s>>>(lg, sp.S, pstride, gbias, bias, T, E, k, gating, o);
             if (npl <= 2) { MOE_GATE_LAUNCH(2) }
             else if (npl <= 4) { MOE_GATE_LAUNCH(4) }
             else if (npl <= 8) { MOE_GATE_LAUNCH(8) }
@@ -765,7 +817,7 @@ extern "C" int moe_router_from_logits(const float* logits, const float* bias, in
         const int npl = cdiv(E, 32);
 #define MOE_GATE_LAUNCH2(N)                                                                             \
         cudaFuncSetAttribute(router_gate_kernel<N>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem); \
-        router_gate_kernel<N><<<G, kRouterWarps * 32, smem, s>>>(logits, bias, T, E, k, gating, o);
+        router_gate_kernel<N><<<G, kRouterWarps * 32, smem, s>>>(logits, 1, 0, nullptr, bias, T, E, k, gating, o);
         if (npl <= 2) { MOE_GATE_LAUNCH2(2) }
         else if (npl <= 4) { MOE_GATE_LAUNCH2(4) }
         else if (npl <= 8) { MOE_GATE_LAUNCH2(8) }
