@@ -273,8 +273,11 @@ def run_gpu(args, cfg, C):
     assert moe.moe_check_device_error() == moe.MOE_OK, moe.moe_last_error_string()
     if cfg.routing == "expert_choice":
         kept = cfg.E * layer.C                        # every expert takes exactly C tokens
+        active = cfg.E
     else:
-        kept = int(layer.d_out["kept_counts"].sum().item())
+        kc = layer.d_out["kept_counts"]
+        kept = int(kc.sum().item())
+        active = int((kc > 0).sum().item())           # experts whose weights the grouped GEMMs read
 
     # ---- device-resident timed region
     events: dict = {}
@@ -362,9 +365,24 @@ def run_gpu(args, cfg, C):
             traffic = tr.get("up_gate_dram_bytes")
     except Exception:
         pass
-    roofline = {"bound": "tensor", "kernel": "up/gate grouped GEMM (SwiGLU epilogue)", "achieved": ug_tflops,
-                "peak": bf16_burst, "unit": "TFLOP/s", "frac": ug_tflops / bf16_burst, "traffic": traffic,
-                "peak_source": f"{peak_src} bf16 burst"}
+    # The up/gate GEMM's algorithmic bytes: the gate and up weights of every expert that received rows (and the
+    # shared expert's), its input rows read once, the activation written once. Below the ridge point (few rows
+    # per expert) the weight stream, not the tensor cores, bounds it; the roofline takes whichever bound is
+    # reached later at the measured peaks.
+    ug_rows = kept + (cfg.T if fused_shared else 0)
+    ug_bytes = ((active + (1 if fused_shared else 0)) * 2.0 * cfg.F * cfg.h + ug_rows * (cfg.h + cfg.F)) * cfg.el
+    ug_gbs = ug_bytes / (ug_ms * 1e-3) / 1e9
+    if ug_bytes / (hbm * 1e9) > ug_flops / (bf16_burst * 1e12):
+        roofline = {"bound": "hbm", "kernel": "up/gate grouped GEMM (SwiGLU epilogue)", "achieved": ug_gbs,
+                    "peak": hbm, "unit": "GB/s", "frac": ug_gbs / hbm, "traffic": traffic,
+                    "peak_source": f"{peak_src} HBM copy", "tensor_tflops": ug_tflops}
+    else:
+        roofline = {"bound": "tensor", "kernel": "up/gate grouped GEMM (SwiGLU epilogue)", "achieved": ug_tflops,
+                    "peak": bf16_burst, "unit": "TFLOP/s", "frac": ug_tflops / bf16_burst, "traffic": traffic,
+                    "peak_source": f"{peak_src} bf16 burst"}
+    roofline["algorithmic_bytes"] = ug_bytes
+    roofline["intensity_flop_per_byte"] = ug_flops / ug_bytes
+    roofline["ridge_flop_per_byte"] = bf16_burst * 1e12 / (hbm * 1e9)
 
     line = {"metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",

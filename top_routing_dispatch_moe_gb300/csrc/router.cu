@@ -30,7 +30,15 @@ struct GateOut {
     float* logits;      // may be null
     float* partial_P;   // [grid][E]
     int32_t* partial_C; // [grid][E]
+    unsigned* ticket;   // the finalize's arrival counter, zeroed by the gating kernel's block 0
 };
+
+// Order-preserving 32-bit key of a selection score: a larger score gives a larger key (-0 and +0 the same);
+// key 0 marks a taken or absent slot (no finite or infinite score maps to it).
+__device__ __forceinline__ unsigned score_key(float v) {
+    const unsigned u = __float_as_uint(v == 0.f ? 0.f : v);
+    return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+}
 
 // The bias enters the logits in the plain and renormalised softmax modes; it is a selection-only term in the
 // sigmoid mode and in the softmax mode with selection bias.
@@ -81,26 +89,33 @@ __device__ __forceinline__ void gate_token(float (&L)[NPL], int t, int E, int k,
         for (int i = 0; i < NPL; ++i) { prob[i] *= inv; Pacc[i] += prob[i]; }
     }
 
-    // k rounds of warp argmax on the selection score
+    // k rounds of warp argmax on the selection score, on order-preserving keys: a warp max reduction finds the
+    // largest key, a warp min reduction the smallest expert index holding it (equal scores: smaller index)
+    unsigned key[NPL];
+#pragma unroll
+    for (int i = 0; i < NPL; ++i) key[i] = live[i] ? score_key(score[i]) : 0u;
     int sel_id[kMaxK];
     float sel_p[kMaxK];
     float psum = 0.f;
 #pragma unroll
     for (int j = 0; j < kMaxK; ++j) {
         if (j < k) {
-            float bv = -INFINITY;
-            int bi = 0x7fffffff;
+            unsigned lm = key[0];
 #pragma unroll
-            for (int i = 0; i < NPL; ++i)
-                if (score[i] > bv) { bv = score[i]; bi = lane + 32 * i; }   // strict: lower index on ties
-            warp_argmax(bv, bi);
+            for (int i = 1; i < NPL; ++i) lm = max(lm, key[i]);
+            const unsigned m = __reduce_max_sync(0xffffffffu, lm);
+            unsigned li = 0xffffffffu;
+#pragma unroll
+            for (int i = NPL - 1; i >= 0; --i)
+                if (key[i] == m) li = (unsigned)(lane + 32 * i);
+            int bi = (int)__reduce_min_sync(0xffffffffu, li);
             if (bi >= E) bi = E - 1;          // only reachable with NaN scores: keeps every index in bounds
             const int owner = bi & 31, slot = bi >> 5;
             float pv = 0.f;
 #pragma unroll
             for (int i = 0; i < NPL; ++i) {
                 if (i == slot) pv = prob[i];
-                if (i == slot && lane == owner) score[i] = -INFINITY;      // taken
+                if (i == slot && lane == owner) key[i] = 0u;               // taken
             }
             pv = __shfl_sync(0xffffffffu, pv, owner);
             sel_id[j] = bi;
@@ -136,6 +151,7 @@ __device__ __forceinline__ void flush_partials(float (&Pacc)[NPL], int E, float*
         o.partial_P[(size_t)blockIdx.x * E + e] = s;
         o.partial_C[(size_t)blockIdx.x * E + e] = s_hist[e];
     }
+    if (blockIdx.x == 0 && threadIdx.x == 0) *o.ticket = 0u;     // the finalize runs after this kernel
 }
 
 // 16 bytes of elements -> fp32 (bf16: the value's bits are the high half of an fp32 word).
@@ -500,7 +516,24 @@ router_gate_kernel(const float* __restrict__ logits, int nparts, size_t part_str
             L[i] = e < E ? logits[(size_t)t * E + e] : -INFINITY;
         }
         if (nparts > 1 || lbias) {
-            for (int q = 1; q < nparts; ++q) {
+            int q = 1;
+            for (; q + 3 < nparts; q += 4) {             // four parts' loads in flight, added in part order
+                float v[4][NPL];
+#pragma unroll
+                for (int u = 0; u < 4; ++u) {
+                    const float* lq = logits + (q + u) * part_stride + (size_t)t * E;
+#pragma unroll
+                    for (int i = 0; i < NPL; ++i) {
+                        int e = lane + 32 * i;
+                        v[u][i] = e < E ? lq[e] : 0.f;
+                    }
+                }
+#pragma unroll
+                for (int u = 0; u < 4; ++u)
+#pragma unroll
+                    for (int i = 0; i < NPL; ++i) L[i] += v[u][i];
+            }
+            for (; q < nparts; ++q) {
                 const float* lq = logits + q * part_stride + (size_t)t * E;
 #pragma unroll
                 for (int i = 0; i < NPL; ++i) {
@@ -527,69 +560,71 @@ router_gate_kernel(const float* __restrict__ logits, int nparts, size_t part_str
     flush_partials<NPL>(Pacc, E, s_P, s_hist, o);
 }
 
-// One block: counts, f, P and aux from the per-block partials. Thread (s, e) of an [S][E] arrangement sums
-// the partials of blocks s, s + S, s + 2S, ... of expert e; the S partial sums of each expert are then added
-// in a fixed tree order, so the result does not depend on timing.
+// Counts, f, P and aux from the per-block partials of `grid` gating blocks. Each block takes chunks of
+// kFinExperts experts (block b: chunks b, b + gridDim.x, ...); thread (s, e) of its [S][chunk] arrangement sums
+// the partials of gating blocks s, s + S, s + 2S, ... of expert e, and the S slice sums of each expert are added
+// in slice order. Every block adds its experts' f_e P_e in expert order; with several blocks, the last one to
+// arrive (counted on `ticket`, which the gating kernel zeroed) adds the blocks' sums in block order. No step
+// depends on timing, so the results are the same on every run.
+constexpr int kFinExperts = 32;
 __global__ void __launch_bounds__(1024)
 router_finalize(const float* __restrict__ partial_P, const int32_t* __restrict__ partial_C, int grid, int T_, int E,
-                int k, float alpha, int32_t* counts, float* f, float* P, float* aux) {
+                int k, float alpha, int32_t* counts, float* f, float* P, float* aux, float* term_part,
+                unsigned* ticket) {
     __shared__ float s_p[1024];
     __shared__ int s_c[1024];
-    __shared__ float s_red[1024];
-    const int S = max(1, (int)blockDim.x / E);          // slices per expert (power of two not required)
-    float term = 0.f;
-    for (int e0 = 0; e0 < E; e0 += blockDim.x) {        // E <= 1024: one pass when E * S <= blockDim
-        const int tid = threadIdx.x;
-        const int e = e0 + tid % min(E - e0, (int)blockDim.x);
-        const int s = tid / min(E - e0, (int)blockDim.x);
-        const int Se = (int)blockDim.x / min(E - e0, (int)blockDim.x);
-        // 8 independent running sums per thread (8 loads in flight), added in a fixed order at the end
-        float ps[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-        int cs[8] = {0, 0, 0, 0, 0, 0, 0, 0};
-        if (s < Se && e < E) {
+    __shared__ float s_t[kFinExperts];
+    const int tid = threadIdx.x;
+    float term = 0.f;                                    // thread 0: this block's sum of f_e P_e
+    for (int e0 = blockIdx.x * kFinExperts; e0 < E; e0 += gridDim.x * kFinExperts) {
+        const int ew = min(kFinExperts, E - e0);
+        const int S = (int)blockDim.x / ew;
+        const int s = tid / ew, e = e0 + tid % ew;
+        float ps[4] = {0.f, 0.f, 0.f, 0.f};
+        int cs[4] = {0, 0, 0, 0};
+        if (s < S) {
             int b = s;
-            for (; b + 7 * Se < grid; b += 8 * Se) {
+            for (; b + 3 * S < grid; b += 4 * S) {       // four partials in flight
 #pragma unroll
-                for (int u = 0; u < 8; ++u) {
-                    ps[u] += partial_P[(size_t)(b + u * Se) * E + e];
-                    cs[u] += partial_C[(size_t)(b + u * Se) * E + e];
+                for (int u = 0; u < 4; ++u) {
+                    ps[u] += partial_P[(size_t)(b + u * S) * E + e];
+                    cs[u] += partial_C[(size_t)(b + u * S) * E + e];
                 }
             }
-            for (; b < grid; b += Se) {
+            for (; b < grid; b += S) {
                 ps[0] += partial_P[(size_t)b * E + e];
                 cs[0] += partial_C[(size_t)b * E + e];
             }
         }
-        float psum = 0.f;
-        int c = 0;
-#pragma unroll
-        for (int u = 0; u < 8; ++u) { psum += ps[u]; c += cs[u]; }
-        s_p[tid] = psum;
-        s_c[tid] = c;
+        s_p[tid] = (ps[0] + ps[1]) + (ps[2] + ps[3]);
+        s_c[tid] = cs[0] + cs[1] + cs[2] + cs[3];
         __syncthreads();
-        const int ew = min(E - e0, (int)blockDim.x);
         if (tid < ew) {
             float tp = 0.f;
             int tc = 0;
-            for (int q = 0; q < Se; ++q) { tp += s_p[q * ew + tid]; tc += s_c[q * ew + tid]; }
+            for (int q = 0; q < S; ++q) { tp += s_p[q * ew + tid]; tc += s_c[q * ew + tid]; }
             const int ee = e0 + tid;
             const float Pe = T_ > 0 ? tp / (float)T_ : 0.f;
             const float fe = T_ > 0 ? (float)tc / ((float)k * (float)T_) : 0.f;
             counts[ee] = tc;
             f[ee] = fe;
             P[ee] = Pe;
-            term += fe * Pe;
+            s_t[tid] = fe * Pe;
         }
         __syncthreads();
+        if (tid == 0)
+            for (int i = 0; i < ew; ++i) term += s_t[i];
+        __syncthreads();                                 // s_p, s_c and s_t are rewritten by the next chunk
     }
-    (void)S;
-    s_red[threadIdx.x] = term;
-    __syncthreads();
-    for (int st = blockDim.x / 2; st > 0; st >>= 1) {
-        if ((int)threadIdx.x < st) s_red[threadIdx.x] += s_red[threadIdx.x + st];
-        __syncthreads();
-    }
-    if (threadIdx.x == 0) aux[0] = alpha * (float)E * s_red[0];
+    if (tid != 0) return;
+    if (gridDim.x == 1) { aux[0] = alpha * (float)E * term; return; }
+    term_part[blockIdx.x] = term;
+    __threadfence();
+    if (atomicAdd(ticket, 1u) != gridDim.x - 1) return;
+    __threadfence();
+    float sum = 0.f;
+    for (unsigned b = 0; b < gridDim.x; ++b) sum += __ldcg(term_part + b);
+    aux[0] = alpha * (float)E * sum;
 }
 
 // W_r [h, E] -> W_rT [E, h]: the K-major operand of the tensor-core logits GEMM. 32 x 32 shared-memory tiles.
@@ -656,8 +691,12 @@ static RouterSplit router_split(int T, int h, int E, bool tc) {
 }
 
 struct RouterWs {
-    float* partial_P; int32_t* partial_C; float* logits; void* w_rT; int32_t* sched; float* parts; size_t bytes;
+    float* partial_P; int32_t* partial_C; float* logits; void* w_rT; int32_t* sched; float* parts;
+    unsigned* ticket; float* term_part; size_t bytes;
 };
+
+// Blocks of the finalize: one per kFinExperts experts when gating blocks zeroed its arrival counter (T > 0).
+static int finalize_grid(int T, int E) { return T > 0 ? cdiv(E, kFinExperts) : 1; }
 
 static RouterWs router_ws_layout(void* ws, int T, int h, int E, int el, bool small, bool need_logits, bool tc,
                                  int split) {
@@ -667,6 +706,8 @@ static RouterWs router_ws_layout(void* ws, int T, int h, int E, int el, bool sma
     char* base = static_cast<char*>(ws);
     w.partial_P = reinterpret_cast<float*>(base + off); off = align_up(off + (size_t)G * E * 4, 256);
     w.partial_C = reinterpret_cast<int32_t*>(base + off); off = align_up(off + (size_t)G * E * 4, 256);
+    w.ticket = reinterpret_cast<unsigned*>(base + off); off = align_up(off + 4, 256);
+    w.term_part = reinterpret_cast<float*>(base + off); off = align_up(off + (size_t)cdiv(E, kFinExperts) * 4, 256);
     w.logits = nullptr;
     if (need_logits) { w.logits = reinterpret_cast<float*>(base + off); off = align_up(off + (size_t)T * E * 4, 256); }
     w.w_rT = nullptr;
@@ -716,7 +757,7 @@ extern "C" int moe_router(const void* x, const void* w_r, const float* bias, int
                 "moe_router: workspace %zu < %zu bytes", ws_bytes, w.bytes);
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     const int G = !small ? gate_grid(T) : dtype == MOE_BF16 ? router_mma_grid(T) : router_small_grid(T);
-    GateOut o{topk_ids, gates, logits, w.partial_P, w.partial_C};
+    GateOut o{topk_ids, gates, logits, w.partial_P, w.partial_C, w.ticket};
     if (T > 0) {
         if (small && dtype == MOE_BF16) {
             const size_t smem = mma_smem_bytes(h, E);
@@ -785,14 +826,14 @@ extern "C" int moe_router(const void* x, const void* w_r, const float* bias, int
             if (int rc = check_launch("router_gate_kernel")) return rc;
         }
     }
-    router_finalize<<<1, 1024, 0, s>>>(w.partial_P, w.partial_C, T > 0 ? G : 0, T, E, k, alpha, counts, f, P, aux);
+    router_finalize<<<finalize_grid(T, E), 1024, 0, s>>>(w.partial_P, w.partial_C, T > 0 ? G : 0, T, E, k, alpha,
+                                                          counts, f, P, aux, w.term_part, w.ticket);
     return check_launch("router_finalize");
 }
 
 extern "C" size_t moe_router_from_logits_workspace_size(int T, int E) {
     if (T < 0 || E <= 0) return 0;
-    const int G = router_grid(T);
-    return 2 * align_up((size_t)G * E * 4, 256);
+    return router_ws_layout(nullptr, T, 8, E, 4, false, false, false, 1).bytes;
 }
 
 extern "C" int moe_router_from_logits(const float* logits, const float* bias, int T, int E, int k, int gating,
@@ -809,9 +850,8 @@ extern "C" int moe_router_from_logits(const float* logits, const float* bias, in
                 need);
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     const int G = gate_grid(T);              // <= router_grid(T), which sizes the workspace
-    char* base = static_cast<char*>(ws);
-    GateOut o{topk_ids, gates, nullptr, reinterpret_cast<float*>(base),
-              reinterpret_cast<int32_t*>(base + align_up((size_t)G * E * 4, 256))};
+    const RouterWs w = router_ws_layout(ws, T, 8, E, 4, false, false, false, 1);
+    GateOut o{topk_ids, gates, nullptr, w.partial_P, w.partial_C, w.ticket};
     if (T > 0) {
         const size_t smem = (size_t)kRouterWarps * E * sizeof(float) + (size_t)E * sizeof(int);
         const int npl = cdiv(E, 32);
@@ -826,6 +866,7 @@ extern "C" int moe_router_from_logits(const float* logits, const float* bias, in
 #undef MOE_GATE_LAUNCH2
         if (int rc = check_launch("router_gate_kernel")) return rc;
     }
-    router_finalize<<<1, 1024, 0, s>>>(o.partial_P, o.partial_C, T > 0 ? G : 0, T, E, k, alpha, counts, f, P, aux);
+    router_finalize<<<finalize_grid(T, E), 1024, 0, s>>>(o.partial_P, o.partial_C, T > 0 ? G : 0, T, E, k, alpha,
+                                                          counts, f, P, aux, w.term_part, w.ticket);
     return check_launch("router_finalize");
 }
