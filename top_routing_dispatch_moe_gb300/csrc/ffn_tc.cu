@@ -115,6 +115,19 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map
         ::"r"(dst), "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(bar)
         : "memory");
 }
+// Tile store shared -> global through the tensor map (rows and columns outside the map's extents are not
+// written); bulk-group completion, so the issuing thread waits on its own groups.
+__device__ __forceinline__ void tma_store_3d(const CUtensorMap* map, uint32_t src, int x, int y, int z) {
+    asm volatile("cp.async.bulk.tensor.3d.global.shared::cta.bulk_group [%0, {%1, %2, %3}], [%4];"
+                 ::"l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(z), "r"(src)
+                 : "memory");
+}
+__device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+__device__ __forceinline__ void bulk_wait_read_all() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
+__device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
+__device__ __forceinline__ void st_shared_v4(uint32_t addr, float a, float b, float c, float d) {
+    asm volatile("st.shared.v4.f32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "f"(a), "f"(b), "f"(c), "f"(d) : "memory");
+}
 __device__ __forceinline__ void prefetch_tmap(const CUtensorMap* map) {
     asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
 }
@@ -284,11 +297,10 @@ __device__ __forceinline__ Work map_item(const Params& p, int E, int w, int nr, 
 }
 
 // Epilogue of one accumulator: this thread's TMEM lane (one output row) -> SwiGLU of the packed gate/up
-// columns into bf16 act, a plain bf16 row, or an fp32 row (+ per-column bias), masked to the valid rows
-// and columns.
+// columns into bf16 act, its backward, or a plain bf16 row, masked to the valid rows and columns.
 template <int EPI, int BN>
 __device__ __forceinline__ void store_tile(const Params& p, __nv_bfloat16* out, uint32_t tbase, int row, bool live,
-                                           int n, float* outf = nullptr, bool zero = false) {
+                                           int n) {
     if constexpr (EPI == EPI_SWIGLU_BWD) {
         // g, u from the accumulator; da = act gradient (0 past F): s = sigmoid(g),
         // d_g = da u s (1 + g (1 - s)), d_u = da g s, written to columns n*256 + c and n*256 + 128 + c.
@@ -340,33 +352,8 @@ __device__ __forceinline__ void store_tile(const Params& p, __nv_bfloat16* out, 
                 }
             }
         }
-    } else if constexpr (EPI == EPI_F32) {
-#pragma unroll 1
-        for (int j = 0; j < BN / 32; ++j) {
-            float v[32];
-            if (zero) {                      // no K steps (an expert without rows): the result is zero
-#pragma unroll
-                for (int i = 0; i < 32; ++i) v[i] = 0.f;
-            } else {
-                tmem_ld32(tbase + 32 * j, v);
-            }
-            const int n0 = n * BN + 32 * j;
-            if (live) {
-                float* dst = (outf ? outf : p.out_f32) + (size_t)row * p.ldo + n0;
-#pragma unroll
-                for (int c = 0; c < 32; c += 4) {
-                    if (n0 + c < p.n_valid) {
-                        float4 o;
-                        o.x = v[c] + (p.bias ? __ldg(p.bias + n0 + c) : 0.f);
-                        o.y = v[c + 1] + (p.bias ? __ldg(p.bias + n0 + c + 1) : 0.f);
-                        o.z = v[c + 2] + (p.bias ? __ldg(p.bias + n0 + c + 2) : 0.f);
-                        o.w = v[c + 3] + (p.bias ? __ldg(p.bias + n0 + c + 3) : 0.f);
-                        *reinterpret_cast<float4*>(dst + c) = o;
-                    }
-                }
-            }
-        }
-    } else {
+    } else {                                 // EPI_BF16
+        static_assert(EPI == EPI_BF16, "the fp32 epilogue stores through TMA (store_tile_f32_tma)");
 #pragma unroll 1
         for (int j = 0; j < BN / 32; ++j) {
             float v[32];
@@ -388,10 +375,53 @@ __device__ __forceinline__ void store_tile(const Params& p, __nv_bfloat16* out, 
     }
 }
 
+// fp32 epilogue through TMA stores, one call per epilogue warp (all 32 lanes): the warp's 32 accumulator rows,
+// 32 columns at a time, are written into its 4 KB staging buffer `stg` (1024-byte aligned) in the 128-byte
+// swizzled layout of a [32 rows][32 fp32] box (16-byte chunk c of row r at chunk c ^ (r % 8): the eight rows of a
+// store phase hit distinct banks), then one lane stores the box at (column, row0, grp) of `map`, whose extents
+// drop the rows and columns past the output. Whole 128-byte lines reach L2, where per-thread row stores would
+// send one 16-byte partial sector per request. `live`: the warp holds at least one valid row (warp-uniform).
+constexpr int EPI_STG_WARP_BYTES = 32 * 32 * 4;
+constexpr int EPI_STG_BYTES = 4 * EPI_STG_WARP_BYTES;
+template <int BN>
+__device__ __forceinline__ void store_tile_f32_tma(const Params& p, const CUtensorMap* map, uint32_t tbase, int n,
+                                                   int row0, int grp, bool zero, bool live, uint32_t stg) {
+    const int lane = threadIdx.x & 31;
+    const uint32_t my_row = stg + (uint32_t)lane * 128u;
+#pragma unroll 1
+    for (int j = 0; j < BN / 32; ++j) {
+        float v[32];
+        if (zero) {                          // no K steps (an expert without rows): the result is zero
+#pragma unroll
+            for (int i = 0; i < 32; ++i) v[i] = 0.f;
+        } else {
+            tmem_ld32(tbase + 32 * j, v);
+        }
+        const int n0 = n * BN + 32 * j;
+        if (!live || n0 >= p.n_valid) continue;
+        if (p.bias) {
+#pragma unroll
+            for (int i = 0; i < 32; ++i) v[i] += n0 + i < p.n_valid ? __ldg(p.bias + n0 + i) : 0.f;
+        }
+        if (lane == 0) bulk_wait_read_all();           // the previous box has left the buffer
+        __syncwarp();
+#pragma unroll
+        for (int c = 0; c < 8; ++c)
+            st_shared_v4(my_row + ((uint32_t)(c ^ (lane & 7)) << 4), v[4 * c], v[4 * c + 1], v[4 * c + 2], v[4 * c + 3]);
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+        __syncwarp();
+        if (lane == 0) {
+            tma_store_3d(map, stg, n0, row0, grp);
+            bulk_commit();
+        }
+    }
+}
+
 template <int EPI, class CF, bool A8 = false>
 __global__ void __launch_bounds__(A8 ? NUM_THREADS_A8 : NUM_THREADS, 1)
 grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
-                    const __grid_constant__ CUtensorMap tmA2, const __grid_constant__ CUtensorMap tmB2, Params p) {
+                    const __grid_constant__ CUtensorMap tmA2, const __grid_constant__ CUtensorMap tmB2,
+                    const __grid_constant__ CUtensorMap tmO, const __grid_constant__ CUtensorMap tmO2, Params p) {
     constexpr int BN = CF::BN, STAGES = CF::STAGES, B_BYTES = CF::B_BYTES, STAGE_BYTES = CF::STAGE_BYTES;
     constexpr uint32_t kIdesc = idesc_bf16<BN>();
     static_assert((EPI != EPI_SWIGLU && EPI != EPI_SWIGLU_BWD) || BN == 256,
@@ -402,6 +432,7 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
     const uint32_t sbase = smem_u32(smem);
     const uint32_t sA = sbase, sB = sbase + STAGES * A_BYTES;
     const uint32_t s8 = sB + STAGES * B_BYTES;                   // A8: e4m3 staging tiles
+    const uint32_t s_out = sbase + STAGES * STAGE_BYTES + 1024;   // fp32 epilogue: per-warp store boxes
     uint64_t* bars = reinterpret_cast<uint64_t*>(smem + STAGES * STAGE_BYTES + (A8 ? STAGES * A8_BYTES : 0));
     const uint32_t bar0 = smem_u32(bars);
     auto full = [&](int s) { return bar0 + 8u * s; };
@@ -561,24 +592,33 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
             if (!wait_phase(tfull(a), aph, p.wait_limit, abort_flag, p.err, 0x30u)) break;
             tc_fence_after();
             const Work wk = map_item(p, E, w, nr, KB);
-            int row = wk.row0 + lane_base + lane;
-            bool live = row < wk.row1;
-            float* outf = nullptr;
-            if (p.wg_E > 0) {
-                if (p.wg_gu) {                       // de-interleave the packed gate/up rows of expert e
-                    const int b = wk.row0 / BM, f = (b >> 1) * BM + lane_base + lane;
-                    outf = ((b & 1) ? p.out2 : p.out_f32) + ((size_t)wk.e * p.wg_F + (b >> 1) * BM) * p.ldo;
-                    row = lane_base + lane;
-                    live = f < p.wg_F;
-                } else {
-                    outf = p.out_f32 + (size_t)wk.e * p.wg_M * p.ldo;
-                }
-            }
             const uint32_t tbase = tmem + (uint32_t)(a * BN) + ((uint32_t)lane_base << 16);
-            store_tile<EPI, BN>(p, wk.sh ? p.sh_out : p.out, tbase, row, live, wk.n, outf, wk.nkb == 0);
+            if constexpr (EPI == EPI_F32) {
+                // output box rows: [T] x E logits (group 0), [parts or experts][M] x N, or the de-interleaved
+                // gate / up matrices [E][F] x N of the packed gate/up rows
+                const CUtensorMap* om = &tmO;
+                int orow = wk.row0 + lane_base, grp = 0, lim = wk.row1;
+                if (p.wg_E > 0) {
+                    grp = wk.e;
+                    if (p.wg_gu) {
+                        const int b = wk.row0 / BM;
+                        om = (b & 1) ? &tmO2 : &tmO;
+                        orow = (b >> 1) * BM + lane_base;
+                        lim = p.wg_F;
+                    }
+                }
+                store_tile_f32_tma<BN>(p, om, tbase, wk.n, orow, grp, wk.nkb == 0, orow < lim,
+                                       s_out + (uint32_t)(warp & 3) * EPI_STG_WARP_BYTES);
+            } else {
+                const int row = wk.row0 + lane_base + lane;
+                store_tile<EPI, BN>(p, wk.sh ? p.sh_out : p.out, tbase, row, row < wk.row1, wk.n);
+            }
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(tempty(a));
+        }
+        if constexpr (EPI == EPI_F32) {
+            if (lane == 0) bulk_wait_all();            // every box stored before the CTA exits
         }
     }
     tc_fence_before();
@@ -605,6 +645,10 @@ constexpr int PAIR_STAGE_BYTES = A_BYTES + B_HALF_BYTES;       // 32 KB per CTA 
 constexpr int PAIR_MAX_E = 1024;
 constexpr int PAIR_SMEM_BYTES = 1024 + PAIR_STAGES * PAIR_STAGE_BYTES + 256 + (PAIR_MAX_E + 1) * 4;
 static_assert(PAIR_SMEM_BYTES <= 227 * 1024, "shared memory per CTA");
+// fp32 epilogue: the store boxes after the barriers and the pair prefix, 1024-byte aligned
+constexpr int PAIR_STG_OFF = (256 + (PAIR_MAX_E + 1) * 4 + 1023) / 1024 * 1024;
+constexpr int PAIR_SMEM_BYTES_F32 = 1024 + PAIR_STAGES * PAIR_STAGE_BYTES + PAIR_STG_OFF + EPI_STG_BYTES;
+static_assert(PAIR_SMEM_BYTES_F32 <= 227 * 1024, "shared memory per CTA (fp32 epilogue)");
 
 __device__ __forceinline__ uint32_t cluster_rank() {
     uint32_t r;
@@ -740,7 +784,8 @@ __device__ __forceinline__ PairWork map_pair_item(const Params& p, const int* pp
 template <int EPI>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
 grouped_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
-                         const __grid_constant__ CUtensorMap tmA2, const __grid_constant__ CUtensorMap tmB2, Params p) {
+                         const __grid_constant__ CUtensorMap tmA2, const __grid_constant__ CUtensorMap tmB2,
+                         const __grid_constant__ CUtensorMap tmO, const __grid_constant__ CUtensorMap tmO2, Params p) {
     constexpr int BN = 256, STAGES = PAIR_STAGES;
     constexpr uint32_t kIdesc = idesc_bf16<BN, 2 * BM>();
     extern __shared__ uint8_t smem_raw[];
@@ -759,6 +804,7 @@ grouped_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_c
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
     volatile int* peer_rounds = reinterpret_cast<volatile int*>(tmem_slot + 2);   // rank 1's copy rounds, in rank 0
     int* s_pp = reinterpret_cast<int*>(smem + STAGES * PAIR_STAGE_BYTES + 256);
+    const uint32_t s_out = sbase + STAGES * PAIR_STAGE_BYTES + PAIR_STG_OFF;   // fp32 epilogue store boxes
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const uint32_t rank = cluster_rank();
@@ -883,24 +929,32 @@ grouped_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_c
             if (!wait_phase_pair(tfull(a), aph, p.wait_limit, abort_flag, peer_abort, p.err, 0x60u)) break;
             tc_fence_after();
             const PairWork wk = map_pair_item(p, s_pp, E, w, nr, rank, KB);
-            int row = wk.row0 + lane_base + lane;
-            bool live = row < wk.row1;
-            float* outf = nullptr;
-            if (p.wg_E > 0) {
-                if (p.wg_gu) {                       // de-interleave: this CTA's m-tile is one packed gate/up block
-                    const int b = wk.row0 / BM, f = (b >> 1) * BM + lane_base + lane;
-                    outf = ((b & 1) ? p.out2 : p.out_f32) + ((size_t)wk.e * p.wg_F + (b >> 1) * BM) * p.ldo;
-                    live = live && f < p.wg_F;
-                    row = lane_base + lane;
-                } else {
-                    outf = p.out_f32 + (size_t)wk.e * p.wg_M * p.ldo;
-                }
-            }
             const uint32_t tbase = tmem + (uint32_t)(a * BN) + ((uint32_t)lane_base << 16);
-            store_tile<EPI, BN>(p, wk.sh ? p.sh_out : p.out, tbase, row, live, wk.n, outf, wk.nkb == 0);
+            if constexpr (EPI == EPI_F32) {
+                // as in the one-SM kernel; a phantom tile (row0 == row1) stores nothing
+                const CUtensorMap* om = &tmO;
+                int orow = wk.row0 + lane_base, grp = 0, lim = wk.row1;
+                if (p.wg_E > 0) {
+                    grp = wk.e;
+                    if (p.wg_gu) {                   // de-interleave: this CTA's m-tile is one packed gate/up block
+                        const int b = wk.row0 / BM;
+                        om = (b & 1) ? &tmO2 : &tmO;
+                        orow = (b >> 1) * BM + lane_base;
+                        lim = wk.row0 + lane_base < wk.row1 ? p.wg_F : 0;
+                    }
+                }
+                store_tile_f32_tma<BN>(p, om, tbase, wk.n, orow, grp, wk.nkb == 0, orow < lim,
+                                       s_out + (uint32_t)(warp & 3) * EPI_STG_WARP_BYTES);
+            } else {
+                const int row = wk.row0 + lane_base + lane;
+                store_tile<EPI, BN>(p, wk.sh ? p.sh_out : p.out, tbase, row, row < wk.row1, wk.n);
+            }
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive_cluster(tempty_leader + 8u * a);
+        }
+        if constexpr (EPI == EPI_F32) {
+            if (lane == 0) bulk_wait_all();            // every box stored before the CTA exits
         }
     }
     cluster_sync_all();                      // every role has left its loop; rank 1's round count is in rank 0
@@ -944,6 +998,44 @@ static PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
 }
 
 // 2-D bf16 tensor [rows, cols] row-major, box [box_rows, 64 columns], 128-byte swizzle, zero fill.
+// fp32 output [groups][rows][cols] with row pitch ldo elements, as [32 rows][32 columns] boxes in the 128-byte
+// swizzled layout of the epilogue's staging buffers.
+static int make_map_out(CUtensorMap* m, float* base, long long groups, long long rows, long long cols, long long ldo) {
+    auto fn = encode_fn();
+    MOE_REQUIRE(fn, MOE_ERR_CUDA, "cuTensorMapEncodeTiled unavailable from the driver");
+    MOE_REQUIRE(base && aligned16(base) && ldo % 4 == 0 && cols <= ldo && groups >= 1 && rows >= 1, MOE_ERR_INVALID_ARG,
+                "fp32 output map: base %p ldo %lld cols %lld", (void*)base, ldo, cols);
+    cuuint64_t dims[3] = {(cuuint64_t)cols, (cuuint64_t)rows, (cuuint64_t)groups};
+    cuuint64_t strides[2] = {(cuuint64_t)ldo * 4, (cuuint64_t)rows * ldo * 4};
+    cuuint32_t box[3] = {32, 32, 1};
+    cuuint32_t estr[3] = {1, 1, 1};
+    CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, base, dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                    CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    MOE_REQUIRE(r == CUDA_SUCCESS, MOE_ERR_CUDA, "cuTensorMapEncodeTiled (fp32 output) failed (%d)", (int)r);
+    return MOE_OK;
+}
+
+// Output maps of an fp32 launch: the weight-gradient groups (experts or split-K parts; the gate and up halves
+// de-interleaved into two maps) or the dense [a_rows] x n_valid logits. Other epilogues take `ma` as a stand-in.
+template <int EPI>
+static int make_out_maps(const Params& p, long long a_rows, const CUtensorMap& ma, CUtensorMap* o1, CUtensorMap* o2) {
+    *o1 = ma;
+    *o2 = ma;
+    if constexpr (EPI == EPI_F32) {
+        if (p.wg_E > 0 && p.wg_gu) {
+            if (int rc = make_map_out(o1, p.out_f32, p.wg_E, p.wg_F, p.n_valid, p.ldo)) return rc;
+            return make_map_out(o2, p.out2, p.wg_E, p.wg_F, p.n_valid, p.ldo);
+        }
+        if (p.wg_E > 0) {
+            if (int rc = make_map_out(o1, p.out_f32, p.wg_E, p.wg_M, p.n_valid, p.ldo)) return rc;
+        } else {
+            if (int rc = make_map_out(o1, p.out_f32, 1, a_rows, p.n_valid, p.ldo)) return rc;
+        }
+        *o2 = *o1;
+    }
+    return MOE_OK;
+}
+
 static int make_map(CUtensorMap* m, const void* base, long long rows, long long cols, int box_rows) {
     auto fn = encode_fn();
     MOE_REQUIRE(fn, MOE_ERR_CUDA, "cuTensorMapEncodeTiled unavailable from the driver");
@@ -997,7 +1089,8 @@ static int gemm_a8(const void* a8, long long a_rows, const void* b, long long b_
     CUtensorMap ma, mb;
     if (int rc = make_map_u8(&ma, a8, a_rows, p.K, BM)) return rc;
     if (int rc = make_map(&mb, b, b_rows_total, p.K, CF::BN)) return rc;
-    grouped_gemm_kernel<EPI, CF, true><<<num_sms(), NUM_THREADS_A8, CF::SMEM_BYTES_A8, s>>>(ma, mb, ma, mb, p);
+    static_assert(EPI != EPI_F32, "the e4m3 operand path has no fp32 epilogue");
+    grouped_gemm_kernel<EPI, CF, true><<<num_sms(), NUM_THREADS_A8, CF::SMEM_BYTES_A8, s>>>(ma, mb, ma, mb, ma, ma, p);
     return check_launch("grouped_gemm_kernel<up_gate, e4m3 A>");
 }
 
@@ -1008,9 +1101,12 @@ static int gemm(const void* a, long long a_rows, const void* b, long long b_rows
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64)
         return set_error(MOE_ERR_CUDA, "grouped_gemm: no usable current device");
+    constexpr int smem_bytes = EPI == EPI_F32 ? 1024 + CF::STAGES * CF::STAGE_BYTES + 1024 + EPI_STG_BYTES
+                                              : CF::SMEM_BYTES;
+    static_assert(smem_bytes <= 227 * 1024, "shared memory per CTA");
     if (!attr_set[dev]) {
         cudaError_t e = cudaFuncSetAttribute(grouped_gemm_kernel<EPI, CF>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             CF::SMEM_BYTES);
+                                             smem_bytes);
         if (e != cudaSuccess) return set_error(MOE_ERR_CUDA, "grouped_gemm smem attribute: %s", cudaGetErrorString(e));
         attr_set[dev] = true;
     }
@@ -1024,7 +1120,9 @@ static int gemm(const void* a, long long a_rows, const void* b, long long b_rows
         if (int rc = make_map(&ma2, sh.a, p.sh_rows, p.K, BM)) return rc;
         if (int rc = make_map(&mb2, sh.b, sh.b_rows, p.K, CF::BN)) return rc;
     }
-    grouped_gemm_kernel<EPI, CF><<<num_sms(), NUM_THREADS, CF::SMEM_BYTES, s>>>(ma, mb, ma2, mb2, p);
+    CUtensorMap mo, mo2;
+    if (int rc = make_out_maps<EPI>(p, a_rows, ma, &mo, &mo2)) return rc;
+    grouped_gemm_kernel<EPI, CF><<<num_sms(), NUM_THREADS, smem_bytes, s>>>(ma, mb, ma2, mb2, mo, mo2, p);
     return check_launch(EPI == EPI_SWIGLU ? "grouped_gemm_kernel<up_gate>"
                         : EPI == EPI_BF16 ? "grouped_gemm_kernel<bf16>"
                         : EPI == EPI_SWIGLU_BWD ? "grouped_gemm_kernel<swiglu_bwd>" : "grouped_gemm_kernel<f32>");
@@ -1038,14 +1136,15 @@ static int gemm_pair(const void* a, long long a_rows, const void* b, long long b
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64)
         return set_error(MOE_ERR_CUDA, "grouped_gemm_pair: no usable current device");
+    constexpr int smem_bytes = EPI == EPI_F32 ? PAIR_SMEM_BYTES_F32 : PAIR_SMEM_BYTES;
     if (!clusters[dev]) {
         cudaError_t e = cudaFuncSetAttribute(grouped_gemm_pair_kernel<EPI>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             PAIR_SMEM_BYTES);
+                                             smem_bytes);
         if (e != cudaSuccess) return set_error(MOE_ERR_CUDA, "grouped_gemm_pair smem attribute: %s", cudaGetErrorString(e));
         cudaLaunchConfig_t cfg = {};
         cfg.gridDim = dim3(2 * (num_sms() / 2));
         cfg.blockDim = dim3(NUM_THREADS);
-        cfg.dynamicSmemBytes = PAIR_SMEM_BYTES;
+        cfg.dynamicSmemBytes = smem_bytes;
         int n = 0;
         e = cudaOccupancyMaxActiveClusters(&n, grouped_gemm_pair_kernel<EPI>, &cfg);
         if (e != cudaSuccess || n <= 0)
@@ -1062,7 +1161,9 @@ static int gemm_pair(const void* a, long long a_rows, const void* b, long long b
         if (int rc = make_map(&ma2, sh.a, p.sh_rows, p.K, BM)) return rc;
         if (int rc = make_map(&mb2, sh.b, sh.b_rows, p.K, 128)) return rc;
     }
-    grouped_gemm_pair_kernel<EPI><<<2 * clusters[dev], NUM_THREADS, PAIR_SMEM_BYTES, s>>>(ma, mb, ma2, mb2, p);
+    CUtensorMap mo, mo2;
+    if (int rc = make_out_maps<EPI>(p, a_rows, ma, &mo, &mo2)) return rc;
+    grouped_gemm_pair_kernel<EPI><<<2 * clusters[dev], NUM_THREADS, smem_bytes, s>>>(ma, mb, ma2, mb2, mo, mo2, p);
     return check_launch(EPI == EPI_SWIGLU ? "grouped_gemm_pair_kernel<up_gate>"
                         : EPI == EPI_SWIGLU_BWD ? "grouped_gemm_pair_kernel<swiglu_bwd>"
                         : EPI == EPI_F32 ? "grouped_gemm_pair_kernel<f32>" : "grouped_gemm_pair_kernel<bf16>");
