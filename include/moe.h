@@ -291,19 +291,25 @@ int moe_router_backward(const float* logits, const int32_t* topk_ids, const floa
                         float* d_bias, void* ws, size_t ws_bytes, void* stream);
 
 /* moe_router_weight_grad: dW_r [h,E] fp32 = x^T d_logits (x [T,h] dtype, d_logits [T,E] fp32), fp32
- *   accumulation: per token slice, then the slices in order. Workspace:
- *   moe_router_weight_grad_workspace_size(T, h, E) bytes. */
+ *   accumulation in a fixed order. bf16 with E >= 64 (E % 8 == 0, h % 8 == 0): on the tensor cores, each fp32
+ *   d_logits value split into three bf16 pieces whose sum is the value to 2^-24 relative, so the products are
+ *   fp32-exact; the K range is split over token blocks and the parts added in order. Otherwise per token
+ *   slice on the CUDA cores, then the slices in order. Workspace: moe_router_weight_grad_workspace_size(T, h, E)
+ *   bytes (enough for either path). */
 size_t moe_router_weight_grad_workspace_size(int T, int h, int E);
 int moe_router_weight_grad(const void* x, const float* d_logits, int T, int h, int E, int dtype, float* dW_r,
                            void* ws, size_t ws_bytes, void* stream);
 
 /* moe_dispatch_backward: through moe_dispatch and the router's x W_r.
  *   dx[t] = dx_extra[t] + sum over kept j of d_buf[dest_row[t,j]] + sum_e d_logits[t,e] * W_r[:, e]
- *   accumulated in fp32 in that order (j ascending, e ascending), rounded once to dtype. dx_extra [T,h] dtype
- *   (e.g. the shared expert's input gradient) and d_logits may be NULL (their terms are then absent; w_r
- *   is only read with d_logits). d_buf [rows,h], dx [T,h], w_r [h,E] dtype. Workspace (with d_logits):
- *   moe_dispatch_backward_workspace_size(h, E, dtype) bytes, 16-byte aligned (W_r transposed). */
-size_t moe_dispatch_backward_workspace_size(int h, int E, int dtype);
+ *   accumulated in fp32 in that order (j ascending), rounded once to dtype. The router term: bf16 with
+ *   E >= 64 (E % 8 == 0): one tensor-core GEMM of the three bf16 pieces of d_logits (as in
+ *   moe_router_weight_grad) with W_r, fp32 [T,h] in the workspace; otherwise e ascending on the CUDA cores.
+ *   dx_extra [T,h] dtype (e.g. the shared expert's input gradient) and d_logits may be NULL (their terms are
+ *   then absent; w_r is only read with d_logits). d_buf [rows,h], dx [T,h], w_r [h,E] dtype (16-byte aligned
+ *   on the tensor-core path). Workspace (with d_logits): moe_dispatch_backward_workspace_size(T, h, E, dtype)
+ *   bytes, 16-byte aligned. */
+size_t moe_dispatch_backward_workspace_size(int T, int h, int E, int dtype);
 int moe_dispatch_backward(const void* d_buf, const int32_t* dest_row, const float* d_logits, const void* w_r,
                           const void* dx_extra, int T, int h, int k, int E, int dtype, void* dx, void* ws,
                           size_t ws_bytes, void* stream);

@@ -25,6 +25,8 @@ CASES = {
     "page3_small": ("page3_cf1.25", dict(T=300, h=256, F=128), None),             # softmax, capacity
     "mixtral_small": ("mixtral_zipf", dict(T=400, h=256, F=128), "zipf"),         # renormalised, logit bias
     "deepseek_small": ("deepseek_v3", dict(T=200, h=256, F=128, E=64, k=6, n_shared=0), None),   # sigmoid + bias
+    # E = 256: the router-weight products on the tensor cores with T = 1000 padded to 1024 and split over K
+    "deepseek_wide": ("deepseek_v3", dict(T=1000, h=1024, F=128, E=256, k=8, n_shared=0), None),
 }
 _cache = {}
 

@@ -7,7 +7,7 @@
 // every output is deterministic.
 #include <math.h>
 #include <algorithm>
-#include "common.cuh"
+#include "ffn.cuh"
 
 namespace moe {
 
@@ -215,6 +215,79 @@ __global__ void column_sum_kernel(const float* __restrict__ partial, int G, int 
 }
 
 // ---------------------------------------------------------------------------------------------------
+// Tensor-core path of the two router-weight products (bf16 x and W_r, E >= 64): d_logits is fp32, so each
+// value v is written as three bf16 pieces v = p0 + p1 + p2 + r (p0 = bf16(v), p1 = bf16(v - p0),
+// p2 = bf16(v - p0 - p1); |r| <= 2^-24 |v|), and the product with a bf16 operand runs as one GEMM over
+// three times the reduction length (bf16 x bf16 products are exact in the fp32 accumulator). The result is
+// the fp32 product up to the accumulation order, as on the CUDA cores.
+// ---------------------------------------------------------------------------------------------------
+__device__ __forceinline__ void split3(float v, __nv_bfloat16 (&q)[3]) {
+    q[0] = __float2bfloat16_rn(v);
+    float r = v - __bfloat162float(q[0]);
+    q[1] = __float2bfloat16_rn(r);
+    r -= __bfloat162float(q[1]);
+    q[2] = __float2bfloat16_rn(r);
+}
+
+// dL [T][E] fp32 -> out [T][3 Ep] bf16: piece q of dL[t][e] at column q Ep + e, zero for e >= E.
+__global__ void split3_rows_kernel(const float* __restrict__ dL, int T_, int E, int Ep, __nv_bfloat16* __restrict__ out) {
+    const long long n = (long long)T_ * Ep;
+    for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < n; i += (long long)gridDim.x * blockDim.x) {
+        const int t = (int)(i / Ep), e = (int)(i - (long long)t * Ep);
+        __nv_bfloat16 q[3];
+        split3(e < E ? dL[(size_t)t * E + e] : 0.f, q);
+        __nv_bfloat16* row = out + (size_t)t * 3 * Ep;
+        row[e] = q[0];
+        row[Ep + e] = q[1];
+        row[2 * Ep + e] = q[2];
+    }
+}
+
+// dL [T][E] fp32 -> out [E][3 Tp] bf16: piece q of dL[t][e] at out[e][q Tp + t], zero for t >= T (32 x 32 tiles).
+__global__ void __launch_bounds__(256)
+split3_cols_kernel(const float* __restrict__ dL, int T_, int E, int Tp, __nv_bfloat16* __restrict__ out) {
+    __shared__ float tile[32][33];
+    const int e0 = blockIdx.x * 32, t0 = blockIdx.y * 32;
+    for (int r = threadIdx.y; r < 32; r += 8) {
+        const int t = t0 + r, e = e0 + threadIdx.x;
+        tile[r][threadIdx.x] = (t < T_ && e < E) ? dL[(size_t)t * E + e] : 0.f;
+    }
+    __syncthreads();
+    for (int r = threadIdx.y; r < 32; r += 8) {
+        const int e = e0 + r, t = t0 + threadIdx.x;
+        if (e < E && t < Tp) {
+            __nv_bfloat16 q[3];
+            split3(tile[threadIdx.x][r], q);
+            __nv_bfloat16* row = out + (size_t)e * 3 * Tp;
+            row[t] = q[0];
+            row[Tp + t] = q[1];
+            row[2 * Tp + t] = q[2];
+        }
+    }
+}
+
+// x [R][C] -> xT [C][ldd]: xT[c][r] = x[r][c] for r < R, zero for R <= r < ldd (64 x 64 tiles).
+template <typename T>
+__global__ void __launch_bounds__(256)
+transpose_pad_kernel(const T* __restrict__ x, int R, int C, int ldd, T* __restrict__ xT) {
+    __shared__ T tile[64][65];
+    const int c0 = blockIdx.x * 64, r0 = blockIdx.y * 64;
+    for (int i = threadIdx.y; i < 64; i += blockDim.y) {
+        const int r = r0 + i, c = c0 + threadIdx.x;
+        tile[i][threadIdx.x] = (r < R && c < C) ? x[(size_t)r * C + c] : T(0.f);
+    }
+    __syncthreads();
+    for (int i = threadIdx.y; i < 64; i += blockDim.y) {
+        const int c = c0 + i, r = r0 + threadIdx.x;
+        if (c < C && r < ldd) xT[(size_t)c * ldd + r] = tile[threadIdx.x][i];
+    }
+}
+
+// The tensor-core path applies to bf16 with E >= 64 experts (E % 8 == 0, h % 8 == 0).
+static bool tc_router_bwd(int h, int E, int dtype) { return dtype == MOE_BF16 && E >= 64 && E % 8 == 0 && h % 8 == 0; }
+static int round64(int v) { return (v + 63) / 64 * 64; }
+
+// ---------------------------------------------------------------------------------------------------
 // router weight gradient: dW_r[d][e] = sum_t x[t][d] dL[t][e]
 // ---------------------------------------------------------------------------------------------------
 // Block (column block of 256 d, token slice s): one thread per column d, experts in groups of 32 whose dL
@@ -278,8 +351,8 @@ wr_transpose_kernel(const T* __restrict__ w, int h, int E, T* __restrict__ wT) {
 template <typename T, int KMAX>
 __global__ void __launch_bounds__(256)
 dispatch_bwd_kernel(const T* __restrict__ d_buf, const int32_t* __restrict__ dest_row, const float* __restrict__ dL,
-                    const T* __restrict__ w_rT, const T* __restrict__ extra, int T_, int h, int k, int E,
-                    T* __restrict__ dx) {
+                    const T* __restrict__ w_rT, const float* __restrict__ rterm, const T* __restrict__ extra, int T_,
+                    int h, int k, int E, T* __restrict__ dx) {
     constexpr int V = Vec16<T>::N;
     const int lane = threadIdx.x & 31;
     const int t = blockIdx.x * 8 + (threadIdx.x >> 5);
@@ -307,7 +380,14 @@ dispatch_bwd_kernel(const T* __restrict__ d_buf, const int32_t* __restrict__ des
                 for (int i = 0; i < V; ++i) acc[i] += v.get(i);
             }
         }
-        if (dlt) {
+        if (rterm) {                         // the router term, summed over e by the tensor cores
+            const float* rt = rterm + (size_t)t * h + d;
+#pragma unroll
+            for (int i = 0; i < V; i += 4) {
+                const float4 v = *reinterpret_cast<const float4*>(rt + i);
+                acc[i] += v.x; acc[i + 1] += v.y; acc[i + 2] += v.z; acc[i + 3] += v.w;
+            }
+        } else if (dlt) {
             for (int e = 0; e < E; ++e) {
                 const float de = __ldg(dlt + e);
                 const Vec16<T> w = ld16(w_rT + (size_t)e * h + d);
@@ -320,6 +400,31 @@ dispatch_bwd_kernel(const T* __restrict__ d_buf, const int32_t* __restrict__ des
         for (int i = 0; i < V; ++i) o.set(i, acc[i]);
         st16(dx + (size_t)t * h + d, o);
     }
+}
+
+// Router weight gradient on the tensor cores: xT [h][Tp] (Tp = T rounded up to 64), the d_logits pieces
+// [E][3 Tp], the split-K parts [S][h][E] (S > 1).
+struct RwgTc { int Tp, S, kchunk; size_t xT_off, dl_off, parts_off, bytes; };
+static RwgTc rwg_tc_layout(int T, int h, int E) {
+    RwgTc L{};
+    L.Tp = round64(std::max(T, 1));
+    tc_splitk_plan(h, E, 3 * L.Tp, &L.S, &L.kchunk);
+    L.xT_off = 0;
+    L.dl_off = align_up((size_t)h * L.Tp * 2, 256);
+    L.parts_off = L.dl_off + align_up((size_t)E * 3 * L.Tp * 2, 256);
+    L.bytes = L.parts_off + (L.S > 1 ? align_up((size_t)L.S * h * E * 4, 256) : 0);
+    return L;
+}
+// Dispatch backward on the tensor cores: the d_logits pieces [T][3 Ep] (Ep = E rounded up to 64), then the
+// router term [T][h] fp32.
+struct DbTc { int Ep; size_t dl_off, rterm_off, bytes; };
+static DbTc db_tc_layout(int T, int h, int E) {
+    DbTc L{};
+    L.Ep = round64(E);
+    L.dl_off = 0;
+    L.rterm_off = align_up((size_t)T * 3 * L.Ep * 2, 256);
+    L.bytes = L.rterm_off + align_up((size_t)T * h * 4, 256);
+    return L;
 }
 
 static int bwd_router_grid(int T) { return std::max(1, std::min(cdiv(T, kBwdWarps), 2 * num_sms())); }
@@ -403,7 +508,8 @@ extern "C" int moe_router_backward(const float* logits, const int32_t* topk_ids,
 
 extern "C" size_t moe_router_weight_grad_workspace_size(int T, int h, int E) {
     if (T < 0 || h <= 0 || E <= 0) return 0;
-    return align_up((size_t)wgrad_slices(std::max(T, 1), h) * h * E * sizeof(float), 256);
+    const size_t simt = align_up((size_t)wgrad_slices(std::max(T, 1), h) * h * E * sizeof(float), 256);
+    return tc_router_bwd(h, E, MOE_BF16) ? std::max(simt, rwg_tc_layout(T, h, E).bytes) : simt;
 }
 
 extern "C" int moe_router_weight_grad(const void* x, const float* d_logits, int T, int h, int E, int dtype, float* dW_r,
@@ -420,6 +526,24 @@ extern "C" int moe_router_weight_grad(const void* x, const float* d_logits, int 
             return set_error(MOE_ERR_CUDA, "moe_router_weight_grad: memset failed");
         return MOE_OK;
     }
+    if (tc_router_bwd(h, E, dtype)) {
+        // dW_r = xT [h][Tp] times the pieces [E][3 Tp] over k < 3 Tp (x's column k mod Tp)
+        const RwgTc L = rwg_tc_layout(T, h, E);
+        char* base = static_cast<char*>(ws);
+        __nv_bfloat16* xT = reinterpret_cast<__nv_bfloat16*>(base + L.xT_off);
+        __nv_bfloat16* dlp = reinterpret_cast<__nv_bfloat16*>(base + L.dl_off);
+        transpose_pad_kernel<__nv_bfloat16><<<dim3(cdiv(h, 64), L.Tp / 64), dim3(64, 4), 0, s>>>(
+            static_cast<const __nv_bfloat16*>(x), T, h, L.Tp, xT);
+        if (int rc = check_launch("transpose_pad_kernel")) return rc;
+        split3_cols_kernel<<<dim3(cdiv(E, 32), L.Tp / 32), dim3(32, 8), 0, s>>>(d_logits, T, E, L.Tp, dlp);
+        if (int rc = check_launch("split3_cols_kernel")) return rc;
+        float* parts = L.S > 1 ? reinterpret_cast<float*>(base + L.parts_off) : dW_r;
+        if (int rc = tc_gemm_f32_splitk(xT, h, L.Tp, L.Tp, dlp, E, 3 * L.Tp, 0, 3 * L.Tp, L.S, L.kchunk, parts, s))
+            return rc;
+        if (L.S == 1) return MOE_OK;
+        column_sum_kernel<<<cdiv(h * E, 256), 256, 0, s>>>(parts, L.S, h * E, dW_r);
+        return check_launch("column_sum_kernel");
+    }
     const int S = wgrad_slices(T, h);
     const int tslice = cdiv(T, S);
     float* part = static_cast<float*>(ws);
@@ -435,8 +559,9 @@ extern "C" int moe_router_weight_grad(const void* x, const float* d_logits, int 
     return check_launch("column_sum_kernel");
 }
 
-extern "C" size_t moe_dispatch_backward_workspace_size(int h, int E, int dtype) {
-    if (h <= 0 || E <= 0) return 0;
+extern "C" size_t moe_dispatch_backward_workspace_size(int T, int h, int E, int dtype) {
+    if (T < 0 || h <= 0 || E <= 0) return 0;
+    if (tc_router_bwd(h, E, dtype)) return db_tc_layout(T, h, E).bytes;
     return align_up((size_t)h * E * (dtype == MOE_F32 ? 4 : 2), 256);
 }
 
@@ -450,15 +575,30 @@ extern "C" int moe_dispatch_backward(const void* d_buf, const int32_t* dest_row,
     MOE_REQUIRE(d_buf && dest_row && dx && (!d_logits || w_r), MOE_ERR_INVALID_ARG, "moe_dispatch_backward: null pointer");
     MOE_REQUIRE(aligned16(d_buf) && aligned16(dx) && aligned16(dx_extra), MOE_ERR_INVALID_ARG,
                 "moe_dispatch_backward: d_buf, dx and dx_extra must be 16-byte aligned");
-    const size_t need = d_logits ? moe_dispatch_backward_workspace_size(h, E, dtype) : 0;
+    const size_t need = d_logits ? moe_dispatch_backward_workspace_size(T, h, E, dtype) : 0;
     MOE_REQUIRE(need == 0 || (ws && ws_bytes >= need && aligned16(ws)), MOE_ERR_WORKSPACE,
                 "moe_dispatch_backward: workspace %zu < %zu", ws_bytes, need);
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     const dim3 tgrid(cdiv(E, 32), cdiv(h, 32)), tblock(32, 8);
     const int grid = cdiv(T, 8);
+    const float* rterm = nullptr;
+    if (d_logits && tc_router_bwd(h, E, dtype)) {
+        // router term [T][h] = pieces [T][3 Ep] times W_r [h][E] over k < 3 Ep (W_r's column k mod Ep)
+        const DbTc L = db_tc_layout(T, h, E);
+        char* base = static_cast<char*>(ws);
+        __nv_bfloat16* dlp = reinterpret_cast<__nv_bfloat16*>(base + L.dl_off);
+        float* rt = reinterpret_cast<float*>(base + L.rterm_off);
+        const long long n = (long long)T * L.Ep;
+        split3_rows_kernel<<<(int)std::min<long long>(cdiv(n, 256), 8LL * num_sms()), 256, 0, s>>>(d_logits, T, E,
+                                                                                                  L.Ep, dlp);
+        if (int rc = check_launch("split3_rows_kernel")) return rc;
+        if (int rc = tc_gemm_f32_splitk(dlp, T, 3 * L.Ep, 0, w_r, h, E, L.Ep, 3 * L.Ep, 1, 3 * L.Ep, rt, s)) return rc;
+        rterm = rt;
+        d_logits = nullptr;
+    }
 #define MOE_DB_LAUNCH(TY, KM)                                                                                   \
     dispatch_bwd_kernel<TY, KM><<<grid, 256, 0, s>>>(static_cast<const TY*>(d_buf), dest_row, d_logits,           \
-        static_cast<const TY*>(ws), static_cast<const TY*>(dx_extra), T, h, k, E, static_cast<TY*>(dx));
+        static_cast<const TY*>(ws), rterm, static_cast<const TY*>(dx_extra), T, h, k, E, static_cast<TY*>(dx));
     if (dtype == MOE_BF16) {
         if (d_logits) {
             wr_transpose_kernel<__nv_bfloat16><<<tgrid, tblock, 0, s>>>(static_cast<const __nv_bfloat16*>(w_r), h, E,

@@ -69,11 +69,16 @@ int ffn_tc_weight_grad(const void* At, const void* Bt, long long ktot, const int
 // Router logits on the tensor cores (bf16 x and transposed router weight, fp32 logits + bias).
 int tc_router_logits(const void* x, const void* w_rT, const float* bias, int T, int h, int E, const int32_t* sched,
                      float* logits, cudaStream_t s);
-// Split-K variant for few output tiles: parts [S][T][E] fp32, part q = x[:, Q] @ w_rT[:, Q]^T over the columns
-// Q = [q kchunk, min(h, (q + 1) kchunk)) (kchunk a multiple of 64, every part non-empty); the caller adds the
-// parts (and the bias) in order.
-int tc_router_logits_split(const void* x, const void* w_rT, int T, int h, int E, int S, int kchunk, float* parts,
-                           cudaStream_t s);
+// parts [S][M][N] fp32 (N % 4 == 0), part q = A[:, k in Q] B[:, k in Q]^T over the reduction indices
+// Q = [q kchunk, min(K, (q + 1) kchunk)) (kchunk a multiple of 64, every part non-empty); A [M][a_cols] and
+// B [N][b_cols] bf16 with contiguous columns (a_cols, b_cols multiples of 8; columns past them read as zero),
+// reduction index k at column k mod a_kmod of A and k mod b_kmod of B (kmod 0: k itself; else a multiple of 64).
+// The caller adds the parts (in order) when S > 1.
+int tc_gemm_f32_splitk(const void* a, int M, int a_cols, int a_kmod, const void* b, int N, int b_cols, int b_kmod, int K,
+                       int S, int kchunk, float* parts, cudaStream_t s);
+// Split of an [M] x [N] x K product: S parts of kchunk columns so that the 128 x 256 output tiles of all parts
+// cover about one per SM (S <= 16; S = 1 when the tiles alone fill the SMs).
+void tc_splitk_plan(int M, int N, int K, int* S, int* kchunk);
 // Dense tile schedule of `rows` rows (one group), launched on `s`.
 int launch_dense_sched(int rows, int32_t* sched, cudaStream_t s);
 

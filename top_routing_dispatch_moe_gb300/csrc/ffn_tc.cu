@@ -232,6 +232,9 @@ struct Params {
     // weight-gradient mapping without a segment array (seg == null): part e covers columns
     // [e * wg_kchunk, min(K, (e + 1) * wg_kchunk)), wg_kchunk a multiple of BK (split-K partial products)
     int wg_kchunk;
+    // one-SM kernel: column extents of the A and B tensor maps (0: K) and the operands' column of reduction
+    // index k, k mod kmod (0: k), for a K range that runs over one operand several times (a multiple of BK)
+    int a_cols, b_cols, a_kmod, b_kmod;
 };
 
 // K range of part / expert e in the weight-gradient mapping.
@@ -497,9 +500,10 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
                         tma_load_2d(s8 + stage * A8_BYTES, ma, wk.kx0 + kb * BK, wk.row0, raw(stage));
                         tma_load_2d(sB + stage * B_BYTES, mb, wk.kx0 + kb * BK, brow, raw(stage));
                     } else {
+                        const int kx = wk.kx0 + kb * BK;
                         mbar_expect_tx(full(stage), STAGE_BYTES);
-                        tma_load_2d(sA + stage * A_BYTES, ma, wk.kx0 + kb * BK, wk.row0, full(stage));
-                        tma_load_2d(sB + stage * B_BYTES, mb, wk.kx0 + kb * BK, brow, full(stage));
+                        tma_load_2d(sA + stage * A_BYTES, ma, p.a_kmod ? kx % p.a_kmod : kx, wk.row0, full(stage));
+                        tma_load_2d(sB + stage * B_BYTES, mb, p.b_kmod ? kx % p.b_kmod : kx, brow, full(stage));
                     }
                     issued |= 1u << stage;
                     last_par = (last_par & ~(1u << stage)) | (phase << stage);
@@ -1112,8 +1116,8 @@ static int gemm(const void* a, long long a_rows, const void* b, long long b_rows
     }
     if (a_rows == 0) { a = sh.a; a_rows = p.sh_rows; b = sh.b; b_rows_total = sh.b_rows; }   // no routed items
     CUtensorMap ma, mb, ma2, mb2;
-    if (int rc = make_map(&ma, a, a_rows, p.K, BM)) return rc;
-    if (int rc = make_map(&mb, b, b_rows_total, p.K, CF::BN)) return rc;
+    if (int rc = make_map(&ma, a, a_rows, p.a_cols ? p.a_cols : p.K, BM)) return rc;
+    if (int rc = make_map(&mb, b, b_rows_total, p.b_cols ? p.b_cols : p.K, CF::BN)) return rc;
     ma2 = ma;
     mb2 = mb;
     if (p.sh_rows > 0) {
@@ -1286,16 +1290,35 @@ int tc_router_logits(const void* x, const void* w_rT, const float* bias, int T, 
     return tc::gemm<tc::EPI_F32, tc::Wide>(x, T, w_rT, E, p, s);
 }
 
-int tc_router_logits_split(const void* x, const void* w_rT, int T, int h, int E, int S, int kchunk, float* parts,
-                           cudaStream_t s) {
+void tc_splitk_plan(int M, int N, int K, int* S, int* kchunk) {
+    const long long tiles = (long long)cdiv(M, tc::BM) * cdiv(N, tc::Wide::BN);
+    const int S0 = (int)std::min<long long>(std::min(16, cdiv(K, tc::BK)), num_sms() / std::max(1LL, tiles));
+    if (S0 < 2) {
+        *S = 1;
+        *kchunk = cdiv(K, tc::BK) * tc::BK;
+        return;
+    }
+    *kchunk = cdiv(cdiv(K, S0), tc::BK) * tc::BK;
+    *S = cdiv(K, *kchunk);
+}
+
+int tc_gemm_f32_splitk(const void* a, int M, int a_cols, int a_kmod, const void* b, int N, int b_cols, int b_kmod, int K,
+                       int S, int kchunk, float* parts, cudaStream_t s) {
     unsigned* err = device_error_word();
     MOE_REQUIRE(err, MOE_ERR_CUDA, "device error word unavailable");
-    MOE_REQUIRE(S >= 1 && kchunk > 0 && kchunk % tc::BK == 0 && (long long)(S - 1) * kchunk < h, MOE_ERR_INVALID_ARG,
-                "tc_router_logits_split: S=%d kchunk=%d h=%d", S, kchunk, h);
-    tc::Params p{nullptr, h, cdiv(E, tc::Wide::BN), 0, E, E, nullptr, parts, nullptr, err, wait_limit(), 0, nullptr,
-                 nullptr, S, cdiv(T, tc::BM), T, nullptr, 0, 0, nullptr};
+    MOE_REQUIRE(M > 0 && N > 0 && N % 4 == 0 && K > 0 && S >= 1 && kchunk > 0 && kchunk % tc::BK == 0 &&
+                    (long long)(S - 1) * kchunk < K && a_cols % 8 == 0 && b_cols % 8 == 0 && a_kmod % tc::BK == 0 &&
+                    b_kmod % tc::BK == 0 && aligned16(a) && aligned16(b) && aligned16(parts),
+                MOE_ERR_INVALID_ARG, "tc_gemm_f32_splitk: M=%d N=%d K=%d S=%d kchunk=%d a_cols=%d b_cols=%d", M, N, K, S,
+                kchunk, a_cols, b_cols);
+    tc::Params p{nullptr, K, cdiv(N, tc::Wide::BN), 0, N, N, nullptr, parts, nullptr, err, wait_limit(), 0, nullptr,
+                 nullptr, S, cdiv(M, tc::BM), M, nullptr, 0, 0, nullptr};
     p.wg_kchunk = kchunk;
-    return tc::gemm<tc::EPI_F32, tc::Wide>(x, T, w_rT, E, p, s);
+    p.a_cols = a_cols;
+    p.b_cols = b_cols;
+    p.a_kmod = a_kmod;
+    p.b_kmod = b_kmod;
+    return tc::gemm<tc::EPI_F32, tc::Wide>(a, M, b, N, p, s);
 }
 
 }  // namespace moe

@@ -683,11 +683,9 @@ static bool use_tc_logits(int E, int dtype, bool small) { return !small && dtype
 struct RouterSplit { int S, kchunk; };
 static RouterSplit router_split(int T, int h, int E, bool tc) {
     if (!tc || T <= 0) return {1, h};
-    const long long tiles = (long long)cdiv(T, 128) * cdiv(E, 256);
-    const int S0 = (int)std::min<long long>(std::min(16, cdiv(h, 64)), num_sms() / tiles);
-    if (S0 < 2) return {1, h};
-    const int kchunk = cdiv(cdiv(h, S0), 64) * 64;
-    return {cdiv(h, kchunk), kchunk};
+    RouterSplit r{1, h};
+    tc_splitk_plan(T, E, h, &r.S, &r.kchunk);
+    return r;
 }
 
 struct RouterWs {
@@ -793,7 +791,7 @@ extern "C" int moe_router(const void* x, const void* w_r, const float* bias, int
                     static_cast<const __nv_bfloat16*>(w_r), h, E, static_cast<__nv_bfloat16*>(w.w_rT));
                 if (int rc = check_launch("router_transpose_kernel")) return rc;
                 if (sp.S > 1) {
-                    if (int rc = tc_router_logits_split(x, w.w_rT, T, h, E, sp.S, sp.kchunk, lg, s)) return rc;
+                    if (int rc = tc_gemm_f32_splitk(x, T, h, 0, w.w_rT, E, h, 0, h, sp.S, sp.kchunk, lg, s)) return rc;
                 } else {
                     if (int rc = launch_dense_sched(T, w.sched, s)) return rc;
                     if (int rc = tc_router_logits(x, w.w_rT, lbias, T, h, E, w.sched, lg, s)) return rc;

@@ -203,8 +203,8 @@ class MoELayer:
                          E, h, F, rows, moe.dtype_code(dt)), dev),
                      ws_rb=moe._bytes_tensor(moe._lib.moe_router_backward_workspace_size(T, E), dev),
                      ws_rw=moe._bytes_tensor(moe._lib.moe_router_weight_grad_workspace_size(T, h, E), dev),
-                     ws_db=moe._bytes_tensor(moe._lib.moe_dispatch_backward_workspace_size(h, E, moe.dtype_code(dt)),
-                                             dev))
+                     ws_db=moe._bytes_tensor(moe._lib.moe_dispatch_backward_workspace_size(T, h, E,
+                                                                                           moe.dtype_code(dt)), dev))
             if self.shared_packed is not None:
                 b.update(sh_d_act=torch.empty((T, F), dtype=dt, device=dev),
                          sh_d_gu=torch.empty((T, moe.gu_cols(F)), dtype=dt, device=dev),

@@ -51,7 +51,7 @@ _SIGS = {
     "moe_router_backward": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _F, _F, _P, _P, _P, _Z, _P]),
     "moe_router_weight_grad_workspace_size": (_Z, [_I, _I, _I]),
     "moe_router_weight_grad": (_I, [_P, _P, _I, _I, _I, _I, _P, _P, _Z, _P]),
-    "moe_dispatch_backward_workspace_size": (_Z, [_I, _I, _I]),
+    "moe_dispatch_backward_workspace_size": (_Z, [_I, _I, _I, _I]),
     "moe_dispatch_backward": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _P, _P, _Z, _P]),
     "moe_packed_weights_backward_bytes": (_Z, [_I, _I, _I, _I]),
     "moe_pack_expert_weights_backward": (_I, [_P, _P, _P, _I, _I, _I, _I, _P, _P]),
@@ -495,7 +495,7 @@ def moe_dispatch_backward(d_buf, dest_row, d_logits, w_r, dx_extra=None, dx=None
     if dx is None:
         dx = torch.empty((T, h), dtype=d_buf.dtype, device=d_buf.device)
     if ws is None and d_logits is not None:
-        ws = _bytes_tensor(_lib.moe_dispatch_backward_workspace_size(h, E, dtype_code(d_buf.dtype)), d_buf.device)
+        ws = _bytes_tensor(_lib.moe_dispatch_backward_workspace_size(T, h, E, dtype_code(d_buf.dtype)), d_buf.device)
     _check(_lib.moe_dispatch_backward(_ptr(d_buf), _ptr(dest_row), _ptr(d_logits), _ptr(w_r), _ptr(dx_extra), T, h, k,
                                       E, dtype_code(d_buf.dtype), _ptr(dx), _ptr(ws),
                                       ws.numel() if ws is not None else 0, _stream(stream)))
