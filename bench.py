@@ -421,18 +421,27 @@ def want_backward(args, cfg) -> bool:
 
 
 def time_backward(args, cfg, layer, x, flush, stream, kept):
-    """Gradients of <dy, y> + aux for one forward of x, timed over K passes with CUDA events per stage."""
+    """Gradients of <dy, y> + aux, timed over K passes with CUDA events per stage, each from the state of a
+    forward(x, save=True) (the forward keeps the experts' pre-activations g and u, so the backward does not
+    recompute the up/gate GEMM); the K saving forwards are timed as well."""
     import torch
     from top_routing_dispatch_moe_gb300 import moe
     dy = torch.randn(x.shape, generator=torch.Generator(device=x.device).manual_seed(5), device=x.device,
                      dtype=torch.float32).to(x.dtype)
-    layer.forward(x)
     for _ in range(max(1, args.warmup)):
+        layer.forward(x, save=True)
         layer.backward(x, dy)
         flush.zero_()
     torch.cuda.synchronize()
     events: dict = {}
+    fwd = []
     for _ in range(args.steps):
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        layer.forward(x, save=True)
+        e1.record(stream)
+        fwd.append((e0, e1))
+        flush.zero_()
         layer.backward(x, dy, events=events)
         flush.zero_()
     torch.cuda.synchronize()
@@ -443,14 +452,17 @@ def time_backward(args, cfg, layer, x, flush, stream, kept):
     st = {b: float(np.mean([events[a][i].elapsed_time(events[b][i]) for i in range(args.steps)]))
           for a, b in zip(order[:-1], order[1:])}
     ms = float(np.mean([events["start"][i].elapsed_time(events[order[-1]][i]) for i in range(args.steps)]))
-    # expert GEMM work: dgrad 10 h F (down 2, up/gate recompute 4, up/gate dgrad 4) + wgrad 6 h F per row
+    fwd_ms = float(np.mean([a.elapsed_time(b) for a, b in fwd]))
+    # expert GEMM work per row: dgrad 6 h F (down 2, up/gate dgrad 4; g and u were saved) + wgrad 6 h F
     rows = kept + (cfg.T if cfg.n_shared else 0)
-    gemm_flops = 16.0 * rows * cfg.h * cfg.F
+    gemm_flops = 12.0 * rows * cfg.h * cfg.F
     gemm_ms = st["expert_dgrad"] + st["expert_wgrad"] + st.get("shared_bwd", 0.0)
     return {"ms_per_step": ms, "tokens_per_s": cfg.T / (ms * 1e-3), "unit": "tokens/s", "stages_ms": st,
+            "forward_save_ms": fwd_ms, "train_step_ms": fwd_ms + ms,
             "expert_gemm_tflops": gemm_flops / (gemm_ms * 1e-3) / 1e12,
             "what": "dx, dW_r, d_bias, every expert's and the shared expert's fp32 weight gradients for "
-                    "<dy, y> + aux; L2 flushed between passes"}
+                    "<dy, y> + aux from a forward that kept the experts' pre-activations (forward_save_ms: that "
+                    "forward); L2 flushed between passes"}
 
 
 def kernel_hash():

@@ -222,6 +222,14 @@ int moe_expert_up_gate_shared(const void* buf, const int32_t* tile_sched, const 
 int moe_expert_down_shared(const void* act, const int32_t* tile_sched, const void* packed_w, int E, int h, int F,
                            int rows, const void* act_shared, int T, const void* packed_shared, void* out_shared,
                            int dtype, void* eout, void* stream);
+/* moe_expert_up_gate_save: moe_expert_up_gate_shared (packed_shared may be NULL: routed experts only, x, T,
+ *   act_shared and gu_shared unused) that also stores the pre-activations for the backward:
+ *     gu [rows, 2*Fp] (Fp = F rounded up to 128; columns in blocks of 256: 128 of g = buf W_gate^T, then the
+ *     u = buf W_up^T of the same f; f >= F zero), gu_shared [T, 2*Fp] likewise for the shared expert,
+ *   both bf16 (rows outside the tiles' kept ranges not written). bf16 only; pointers 16-byte aligned. */
+int moe_expert_up_gate_save(const void* buf, const int32_t* tile_sched, const void* packed_w, int E, int h, int F,
+                            int rows, const void* x, int T, const void* packed_shared, void* act_shared,
+                            void* gu_shared, int dtype, void* act, void* gu, void* stream);
 size_t moe_expert_ffn_workspace_size(int rows, int F, int dtype);
 int moe_expert_ffn(const void* buf, const int32_t* tile_sched, const void* packed_w, int E, int h, int F,
                    int rows, int dtype, void* eout, void* ws, size_t ws_bytes, void* stream);
@@ -336,6 +344,12 @@ int moe_expert_down_backward(const void* d_eout, const int32_t* tile_sched, cons
 int moe_expert_up_gate_backward(const void* buf, const void* d_act, const int32_t* tile_sched, const void* packed_w,
                                 const void* packed_bwd, int E, int h, int F, int rows, int dtype, void* d_gu,
                                 void* d_buf, void* stream);
+/* moe_expert_up_gate_backward_saved: moe_expert_up_gate_backward from the pre-activations gu that
+ *   moe_expert_up_gate_save stored instead of recomputing them: d_gu by the same formulas from the bf16 g and u
+ *   (an elementwise pass over the tiles' kept rows), then d_buf as there. */
+int moe_expert_up_gate_backward_saved(const void* gu, const void* d_act, const int32_t* tile_sched,
+                                      const void* packed_bwd, int E, int h, int F, int rows, int dtype, void* d_gu,
+                                      void* d_buf, void* stream);
 size_t moe_expert_weight_grads_workspace_size(int E, int h, int F, int rows, int dtype);
 int moe_expert_weight_grads(const void* buf, const void* act, const void* d_gu, const void* d_eout,
                             const int32_t* offsets, const int32_t* kept_counts, int E, int h, int F, int rows,

@@ -123,12 +123,15 @@ def test_dispatch_backward(name):
         assert cases.rel_max(_np(dx), ref) <= 1e-5 and cases.rel_max(_np(dx_plain), plain) <= 1e-5
 
 
+@pytest.mark.parametrize("saved", [False, True])
 @pytest.mark.parametrize("sizes", [[0, 1, 127, 129, 300], [0, 257, 1900, 40]])
-def test_expert_backward(sizes):
+def test_expert_backward(sizes, saved):
     """Expert FFN backward per expert against the oracle's SwiGLU backward on the same bf16 operands: d_act,
     the packed d_g / d_u, d_buf and the fp32 weight gradients (zero for an expert without rows). F = 320 leaves a
     zero-padded part of the last 128-column block. The second size list has rows >= 512 E, so the dgrad GEMMs run
-    on the 2-SM kernel; the weight gradients always run on the one-SM kernel."""
+    on the 2-SM kernel; the weight gradients always run on the one-SM kernel. saved: the forward keeps g and u
+    (moe_expert_up_gate_save: act bit-identical to moe_expert_up_gate, g and u within bf16 rounding of the
+    float64 products) and the backward starts from them (moe_expert_up_gate_backward_saved)."""
     import torch
     from top_routing_dispatch_moe_gb300 import moe
     torch.manual_seed(7)
@@ -147,7 +150,11 @@ def test_expert_backward(sizes):
     act = moe.moe_expert_up_gate(buf, sched, packed, E, F)
     d_eout = torch.randn(buf.shape[0], h, device=dev).to(torch.bfloat16)
     d_act = moe.moe_expert_down_backward(d_eout, sched, packed_bwd, E, F)
-    d_gu, d_buf = moe.moe_expert_up_gate_backward(buf, d_act, sched, packed, packed_bwd, E)
+    if saved:
+        act_s, gu_s, _, _ = moe.moe_expert_up_gate_save(buf, sched, packed, E, F)
+        d_gu, d_buf = moe.moe_expert_up_gate_backward_saved(gu_s, d_act, sched, packed_bwd, E, h)
+    else:
+        d_gu, d_buf = moe.moe_expert_up_gate_backward(buf, d_act, sched, packed, packed_bwd, E)
     dWg, dWu, dWd = moe.moe_expert_weight_grads(buf, act, d_gu, d_eout, d["offsets"], d["kept_counts"], E)
     torch.cuda.synchronize()
     assert moe.moe_check_device_error() == moe.MOE_OK, moe.moe_last_error_string()
@@ -158,6 +165,12 @@ def test_expert_backward(sizes):
         if a == b:
             assert not dWg[e].any() and not dWu[e].any() and not dWd[e].any()
             continue
+        if saved:
+            assert torch.equal(act_s[a:b], act[a:b])
+            pre = f64(gu_s[a:b]).reshape(b - a, Fp // 128, 2, 128)
+            for got, w in [(pre[:, :, 0, :].reshape(b - a, Fp), wg[e]), (pre[:, :, 1, :].reshape(b - a, Fp), wu[e])]:
+                assert np.all(got[:, F:] == 0)
+                assert cases.rel_l2(got[:, :F], f64(buf[a:b]) @ f64(w).T) <= 4e-3
         g = O.swiglu_ffn_backward(f64(buf[a:b]), f64(wg[e]), f64(wu[e]), f64(wd[e]), f64(d_eout[a:b]))
         gu = f64(d_gu[a:b]).reshape(b - a, Fp // 128, 2, 128)
         dG = gu[:, :, 0, :].reshape(b - a, Fp)
@@ -177,11 +190,13 @@ LAYER_CASES = {
 }
 
 
+@pytest.mark.parametrize("save", [False, True])
 @pytest.mark.parametrize("name", list(LAYER_CASES))
-def test_layer_backward(name):
+def test_layer_backward(name, save):
     """MoELayer.backward (every backward call in sequence) against the oracle's moe_layer_backward of its own
     float64 forward, for <dy, y> + d_aux * aux: dx, dW_r, d_bias, every expert's and the shared expert's weight
-    gradients. The GPU's intermediates (eout, act, d_act, d_g / d_u, d_buf) are bf16: normwise 2e-2."""
+    gradients. The GPU's intermediates (eout, act, d_act, d_g / d_u, d_buf) are bf16: normwise 2e-2. save: the
+    forward keeps the pre-activations and the backward starts from them (no up/gate recompute)."""
     import torch
     base, over, bias_kind = LAYER_CASES[name]
     cfg = moe_inputs.get_config(base, **over)
@@ -192,7 +207,7 @@ def test_layer_backward(name):
     shared = tuple(a[0] for a in moe_inputs.all_expert_weights(cfg, shared=True)) if cfg.n_shared else None
     layer = cases.build_gpu_layer(cfg, inp, wg, wu, wd, shared, backward=True)
     x = cases.to_device(inp["x"], cfg)
-    layer.forward(x)
+    layer.forward(x, save=save)
     rng = np.random.default_rng(13)
     dy = torch.from_numpy(rng.normal(size=(cfg.T, cfg.h)).astype(np.float32)).to("cuda").to(x.dtype)
     d_aux = 0.7

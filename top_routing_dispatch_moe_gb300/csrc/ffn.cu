@@ -54,6 +54,28 @@ extern "C" int moe_expert_up_gate_shared(const void* buf, const int32_t* tile_sc
                           packed_shared, act_shared);
 }
 
+extern "C" int moe_expert_up_gate_save(const void* buf, const int32_t* tile_sched, const void* packed_w, int E, int h,
+                                       int F, int rows, const void* x, int T, const void* packed_shared,
+                                       void* act_shared, void* gu_shared, int dtype, void* act, void* gu,
+                                       void* stream) {
+    if (int rc = ffn_check("moe_expert_up_gate_save", buf, tile_sched, packed_w, E, h, F, rows, dtype, act)) return rc;
+    MOE_REQUIRE(dtype == MOE_BF16, MOE_ERR_UNSUPPORTED, "moe_expert_up_gate_save: bf16 only");
+    MOE_REQUIRE((rows == 0 || gu) && aligned16(gu), MOE_ERR_INVALID_ARG,
+                "moe_expert_up_gate_save: gu null or not 16-byte aligned");
+    if (packed_shared) {
+        if (int rc = shared_check("moe_expert_up_gate_save", tile_sched, x, T, packed_shared, act_shared, dtype))
+            return rc;
+        MOE_REQUIRE((T == 0 || gu_shared) && aligned16(gu_shared), MOE_ERR_INVALID_ARG,
+                    "moe_expert_up_gate_save: gu_shared null or not 16-byte aligned");
+    } else {
+        T = 0;
+    }
+    if (rows == 0 && T == 0) return MOE_OK;
+    return ffn_tc_up_gate(buf, tile_sched, packed_w, E, h, F, rows, act, static_cast<cudaStream_t>(stream),
+                          T ? x : nullptr, T, T ? packed_shared : nullptr, T ? act_shared : nullptr, gu,
+                          T ? gu_shared : nullptr);
+}
+
 extern "C" int moe_expert_down_shared(const void* act, const int32_t* tile_sched, const void* packed_w, int E, int h,
                                       int F, int rows, const void* act_shared, int T, const void* packed_shared,
                                       void* out_shared, int dtype, void* eout, void* stream) {

@@ -46,9 +46,11 @@ int ffn_simt_down(const void* act, const int32_t* sched, const void* packed, int
 
 // tcgen05 tensor-core path (bf16 operands, fp32 accumulation in tensor memory). With T_sh > 0 the same launch
 // also runs the shared expert (packed_sh, one expert) on its T_sh dense rows: x_sh -> act_sh, act_sh -> out_sh.
+// gu / gu_sh (may be null): also store the pre-activations g and u of the routed / shared rows, [rows][2 Fp] in
+// the packed gate/up column order (the layout of d_gu).
 int ffn_tc_up_gate(const void* buf, const int32_t* sched, const void* packed, int E, int h, int F, int rows, void* act,
                    cudaStream_t s, const void* x_sh = nullptr, int T_sh = 0, const void* packed_sh = nullptr,
-                   void* act_sh = nullptr);
+                   void* act_sh = nullptr, void* gu = nullptr, void* gu_sh = nullptr);
 int ffn_tc_down(const void* act, const int32_t* sched, const void* packed, int E, int h, int F, int rows, void* eout,
                 cudaStream_t s, const void* act_sh = nullptr, int T_sh = 0, const void* packed_sh = nullptr,
                 void* out_sh = nullptr);
@@ -63,6 +65,9 @@ int ffn_tc_down_backward(const void* d_eout, const int32_t* sched, const void* p
 int ffn_tc_up_gate_backward(const void* buf, const void* d_act, const int32_t* sched, const void* packed,
                             const void* packed_bwd, int E, int h, int F, int rows, void* d_gu, void* d_buf,
                             cudaStream_t s);
+// d_buf [rows][h] = d_gu [rows][2 Fp] times the packed gate/up weights (the second step of the up/gate backward).
+int ffn_tc_dbuf(const void* d_gu, const int32_t* sched, const void* packed_bwd, int E, int h, int F, int rows,
+                void* d_buf, cudaStream_t s);
 int ffn_tc_weight_grad(const void* At, const void* Bt, long long ktot, const int32_t* seg, int E, int M, int N, int gu,
                        int F, float* out, float* out2, cudaStream_t s);
 

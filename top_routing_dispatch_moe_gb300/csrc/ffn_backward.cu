@@ -59,6 +59,44 @@ segment_transpose_kernel(const T* __restrict__ src, int C, const int32_t* __rest
         if (c0 + c < C) dst[(size_t)(c0 + c) * ktot + k0 + threadIdx.x] = tile[threadIdx.x][c];
 }
 
+// d_gu from the saved pre-activations, over the live rows of the tile schedule: with g, u of feature f at
+// columns (f / 128) 256 + f % 128 and that + 128 of gu [rows][2 Fp], s = logistic(g) and da = d_act[row][f]
+// (0 for f >= F): d_g = da u s (1 + g (1 - s)), d_u = da g s, written to the same columns of d_gu. Work unit =
+// (tile, 64 column vectors of 8 features); four rows of 64 vector lanes per block pass.
+__global__ void __launch_bounds__(256)
+swiglu_bwd_kernel(const __nv_bfloat16* __restrict__ gu, const __nv_bfloat16* __restrict__ d_act,
+                  const int32_t* __restrict__ sched, int E, int F, int Fp, __nv_bfloat16* __restrict__ d_gu) {
+    const int ntiles = sched[0];
+    const int4* tiles = reinterpret_cast<const int4*>(sched + sched_tiles_offset(E));
+    const int nv = Fp / 8, cch = (nv + 63) / 64;
+    const long long units = (long long)ntiles * cch;
+    const size_t ld = 2 * (size_t)Fp;
+    for (long long w = blockIdx.x; w < units; w += gridDim.x) {
+        const int m = (int)(w / cch), c = (int)(w - (long long)m * cch);
+        const int4 t = tiles[m];
+        const int v = c * 64 + (threadIdx.x & 63);
+        if (v >= nv) continue;
+        const int f = v * 8;
+        const size_t col = (size_t)(f >> 7) * 256 + (f & 127);
+        for (int r = t.y + (threadIdx.x >> 6); r < t.z; r += 4) {
+            const Vec16<__nv_bfloat16> g = ld16(gu + (size_t)r * ld + col), u = ld16(gu + (size_t)r * ld + col + 128);
+            Vec16<__nv_bfloat16> da;
+            if (f < F) da = ld16(d_act + (size_t)r * F + f);
+            else da.v = make_uint4(0, 0, 0, 0);
+            Vec16<__nv_bfloat16> og, ou;
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+                const float gv = g.get(i), uv = u.get(i), a = da.get(i);
+                const float sg = 1.f / (1.f + expf(-gv));
+                og.set(i, a * uv * sg * (1.f + gv * (1.f - sg)));
+                ou.set(i, a * gv * sg);
+            }
+            st16(d_gu + (size_t)r * ld + col, og);
+            st16(d_gu + (size_t)r * ld + col + 128, ou);
+        }
+    }
+}
+
 // Column extent of the transposed operands: every expert's rows rounded up to 64, at most rows + 63 E.
 static long long grads_ktot(int rows, int E) {
     return ((long long)rows + (long long)(kSegAlign - 1) * E + kSegAlign - 1) / kSegAlign * kSegAlign;
@@ -114,6 +152,25 @@ extern "C" int moe_expert_up_gate_backward(const void* buf, const void* d_act, c
                 MOE_ERR_INVALID_ARG, "moe_expert_up_gate_backward: pointers must be 16-byte aligned");
     return ffn_tc_up_gate_backward(buf, d_act, tile_sched, packed_w, packed_bwd, E, h, F, rows, d_gu, d_buf,
                                    static_cast<cudaStream_t>(stream));
+}
+
+extern "C" int moe_expert_up_gate_backward_saved(const void* gu, const void* d_act, const int32_t* tile_sched,
+                                                 const void* packed_bwd, int E, int h, int F, int rows, int dtype,
+                                                 void* d_gu, void* d_buf, void* stream) {
+    if (int rc = bwd_ffn_check("moe_expert_up_gate_backward_saved", E, h, F, rows, dtype)) return rc;
+    if (rows == 0) return MOE_OK;
+    MOE_REQUIRE(gu && d_act && tile_sched && packed_bwd && d_gu && d_buf, MOE_ERR_INVALID_ARG,
+                "moe_expert_up_gate_backward_saved: null pointer");
+    MOE_REQUIRE(aligned16(gu) && aligned16(d_act) && aligned16(tile_sched) && aligned16(packed_bwd) && aligned16(d_gu) &&
+                    aligned16(d_buf),
+                MOE_ERR_INVALID_ARG, "moe_expert_up_gate_backward_saved: pointers must be 16-byte aligned");
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    const int Fp = (F + 127) / 128 * 128;
+    swiglu_bwd_kernel<<<4 * num_sms(), 256, 0, s>>>(static_cast<const __nv_bfloat16*>(gu),
+                                                    static_cast<const __nv_bfloat16*>(d_act), tile_sched, E, F, Fp,
+                                                    static_cast<__nv_bfloat16*>(d_gu));
+    if (int rc = check_launch("swiglu_bwd_kernel")) return rc;
+    return ffn_tc_dbuf(d_gu, tile_sched, packed_bwd, E, h, F, rows, d_buf, s);
 }
 
 extern "C" size_t moe_expert_weight_grads_workspace_size(int E, int h, int F, int rows, int dtype) {

@@ -235,6 +235,10 @@ struct Params {
     // one-SM kernel: column extents of the A and B tensor maps (0: K) and the operands' column of reduction
     // index k, k mod kmod (0: k), for a K range that runs over one operand several times (a multiple of BK)
     int a_cols, b_cols, a_kmod, b_kmod;
+    // EPI_SWIGLU: when set, the pre-activations g and u (bf16) of the routed / shared rows, [rows][NT * 256] in the
+    // packed gate/up column order (block n: 128 columns of g, then the u of the same f)
+    __nv_bfloat16* gu_out;
+    __nv_bfloat16* sh_gu_out;
 };
 
 // K range of part / expert e in the weight-gradient mapping.
@@ -303,7 +307,7 @@ __device__ __forceinline__ Work map_item(const Params& p, int E, int w, int nr, 
 // columns into bf16 act, its backward, or a plain bf16 row, masked to the valid rows and columns.
 template <int EPI, int BN>
 __device__ __forceinline__ void store_tile(const Params& p, __nv_bfloat16* out, uint32_t tbase, int row, bool live,
-                                           int n) {
+                                           int n, __nv_bfloat16* gu = nullptr) {
     if constexpr (EPI == EPI_SWIGLU_BWD) {
         // g, u from the accumulator; da = act gradient (0 past F): s = sigmoid(g),
         // d_g = da u s (1 + g (1 - s)), d_u = da g s, written to columns n*256 + c and n*256 + 128 + c.
@@ -351,6 +355,17 @@ __device__ __forceinline__ void store_tile(const Params& p, __nv_bfloat16* out, 
                             o.set(i, gv / (1.f + expf(-gv)) * u[c + i]);
                         }
                         st16(dst + c, o);
+                    }
+                }
+                if (gu) {                    // saved pre-activations (f >= F: zero weight rows give zero)
+                    __nv_bfloat16* gdst = gu + (size_t)row * (p.NT * 256) + (size_t)n * 256 + 32 * j;
+#pragma unroll
+                    for (int c = 0; c < 32; c += 8) {
+                        Vec16<__nv_bfloat16> og, ou;
+#pragma unroll
+                        for (int i = 0; i < 8; ++i) { og.set(i, g[c + i]); ou.set(i, u[c + i]); }
+                        st16(gdst + c, og);
+                        st16(gdst + 128 + c, ou);
                     }
                 }
             }
@@ -615,7 +630,8 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
                                        s_out + (uint32_t)(warp & 3) * EPI_STG_WARP_BYTES);
             } else {
                 const int row = wk.row0 + lane_base + lane;
-                store_tile<EPI, BN>(p, wk.sh ? p.sh_out : p.out, tbase, row, row < wk.row1, wk.n);
+                store_tile<EPI, BN>(p, wk.sh ? p.sh_out : p.out, tbase, row, row < wk.row1, wk.n,
+                                    wk.sh ? p.sh_gu_out : p.gu_out);
             }
             tc_fence_before();
             __syncwarp();
@@ -951,7 +967,8 @@ grouped_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_c
                                        s_out + (uint32_t)(warp & 3) * EPI_STG_WARP_BYTES);
             } else {
                 const int row = wk.row0 + lane_base + lane;
-                store_tile<EPI, BN>(p, wk.sh ? p.sh_out : p.out, tbase, row, row < wk.row1, wk.n);
+                store_tile<EPI, BN>(p, wk.sh ? p.sh_out : p.out, tbase, row, row < wk.row1, wk.n,
+                                    wk.sh ? p.sh_gu_out : p.gu_out);
             }
             tc_fence_before();
             __syncwarp();
@@ -1180,13 +1197,16 @@ static bool use_pair(int E, long long rows) { return E <= PAIR_MAX_E && rows >= 
 }  // namespace tc
 
 int ffn_tc_up_gate(const void* buf, const int32_t* sched, const void* packed, int E, int h, int F, int rows, void* act,
-                   cudaStream_t s, const void* x_sh, int T_sh, const void* packed_sh, void* act_sh) {
+                   cudaStream_t s, const void* x_sh, int T_sh, const void* packed_sh, void* act_sh, void* gu,
+                   void* gu_sh) {
     const PackedLayout L = packed_layout(E, h, F, 2);
     const PackedLayout Ls = packed_layout(1, h, F, 2);
     unsigned* err = device_error_word();
     MOE_REQUIRE(err, MOE_ERR_CUDA, "device error word unavailable");
     tc::Params p{sched, h, L.Fp / 128, 2 * L.Fp, F, F, static_cast<__nv_bfloat16*>(act), nullptr, nullptr, err,
                  wait_limit(), T_sh, static_cast<__nv_bfloat16*>(act_sh)};
+    p.gu_out = static_cast<__nv_bfloat16*>(gu);
+    p.sh_gu_out = static_cast<__nv_bfloat16*>(gu_sh);
     const char* b = static_cast<const char*>(packed) + L.up_gate_off;
     const tc::SharedOperands sh{x_sh, packed_sh ? static_cast<const char*>(packed_sh) + Ls.up_gate_off : nullptr,
                                 2LL * Ls.Fp};
@@ -1257,6 +1277,15 @@ int ffn_tc_up_gate_backward(const void* buf, const void* d_act, const int32_t* s
                  ? tc::gemm_pair<tc::EPI_SWIGLU_BWD>(buf, rows, b1, (long long)E * 2 * L.Fp, p1, s)
                  : tc::gemm<tc::EPI_SWIGLU_BWD, tc::Wide>(buf, rows, b1, (long long)E * 2 * L.Fp, p1, s);
     if (rc) return rc;
+    return ffn_tc_dbuf(d_gu, sched, packed_bwd, E, h, F, rows, d_buf, s);
+}
+
+int ffn_tc_dbuf(const void* d_gu, const int32_t* sched, const void* packed_bwd, int E, int h, int F, int rows,
+                void* d_buf, cudaStream_t s) {
+    const PackedLayout L = packed_layout(E, h, F, 2);
+    const PackedBwdLayout Lb = packed_bwd_layout(E, h, F, 2);
+    unsigned* err = device_error_word();
+    MOE_REQUIRE(err, MOE_ERR_CUDA, "device error word unavailable");
     tc::Params p2{sched, 2 * L.Fp, cdiv(h, 256), h, h, h, static_cast<__nv_bfloat16*>(d_buf), nullptr, nullptr, err,
                   wait_limit(), 0, nullptr};
     const char* b2 = static_cast<const char*>(packed_bwd) + Lb.gu_t_off;

@@ -26,7 +26,9 @@ class MoELayer:
     Stages (in order): "router", "dispatch", "up_gate", "down", ["shared_up_gate", "shared_down"], "combine". With
     bf16 the shared expert runs inside the "up_gate" and "down" launches; the two shared stages exist for fp32.
     forward(x, events=...) records one CUDA event before the first stage and after each stage when given
-    a dict of lists, so callers can time the stages on the launching stream."""
+    a dict of lists, so callers can time the stages on the launching stream. forward(x, save=True) (a layer built
+    with backward=True, bf16 token-choice or Sinkhorn routing, bf16 payload) also keeps the experts'
+    pre-activations g and u, so that the next backward() needs no recompute of the up/gate GEMM."""
 
     STAGES = ("router", "dispatch", "up_gate", "down", "shared_up_gate", "shared_down", "combine")
 
@@ -96,8 +98,18 @@ class MoELayer:
             self.sh_act = torch.empty((T, F), dtype=dt, device=dev)
             self.sh_out = torch.empty((T, h), dtype=dt, device=dev)
         self.y = torch.empty((T, h), dtype=dt, device=dev)
+        self._saved = False
+        if backward:                                 # pre-activations kept by forward(save=True)
+            self.gu = torch.empty((self.rows, moe.gu_cols(F)), dtype=dt, device=dev)
+            self.sh_gu = (torch.empty((T, moe.gu_cols(F)), dtype=dt, device=dev)
+                          if self.shared_packed is not None else None)
 
-    def forward(self, x, stream=None, events=None, y=None):
+    def forward(self, x, stream=None, events=None, y=None, save=False):
+        if save and (self.packed_bwd is None or self.routing not in ("token", "sinkhorn")
+                     or self.dtype != torch.bfloat16 or self.payload != "bf16"):
+            raise NotImplementedError("MoELayer.forward(save=True): a layer built with backward=True, token-choice or "
+                                      "Sinkhorn routing in bf16 with the bf16 send buffer")
+
         def mark(stage):
             if events is not None:
                 ev = torch.cuda.Event(enable_timing=True)
@@ -138,15 +150,25 @@ class MoELayer:
             mark("down")
         elif self.shared_packed is not None and self.dtype == torch.bfloat16:
             # the shared expert's tiles run inside the routed experts' launches
-            moe.moe_expert_up_gate_shared(self.d_out["buf"], sched, self.packed, self.E, self.F, x, self.shared_packed,
-                                          act=self.act, act_shared=self.sh_act, stream=stream)
+            if save:
+                moe.moe_expert_up_gate_save(self.d_out["buf"], sched, self.packed, self.E, self.F, x=x,
+                                            packed_shared=self.shared_packed, act=self.act, gu=self.gu,
+                                            act_shared=self.sh_act, gu_shared=self.sh_gu, stream=stream)
+            else:
+                moe.moe_expert_up_gate_shared(self.d_out["buf"], sched, self.packed, self.E, self.F, x,
+                                              self.shared_packed, act=self.act, act_shared=self.sh_act, stream=stream)
             mark("up_gate")
             moe.moe_expert_down_shared(self.act, sched, self.packed, self.E, self.h, self.sh_act, self.shared_packed,
                                        eout=self.eout, out_shared=self.sh_out, stream=stream)
             mark("down")
             shared_out = self.sh_out
         else:
-            moe.moe_expert_up_gate(self.d_out["buf"], sched, self.packed, self.E, self.F, act=self.act, stream=stream)
+            if save:
+                moe.moe_expert_up_gate_save(self.d_out["buf"], sched, self.packed, self.E, self.F, act=self.act,
+                                            gu=self.gu, stream=stream)
+            else:
+                moe.moe_expert_up_gate(self.d_out["buf"], sched, self.packed, self.E, self.F, act=self.act,
+                                       stream=stream)
             mark("up_gate")
             moe.moe_expert_down(self.act, sched, self.packed, self.E, self.h, eout=self.eout, stream=stream)
             mark("down")
@@ -164,6 +186,7 @@ class MoELayer:
         else:
             moe.moe_combine(self.eout, self.d_out["dest_row"], r["gates"], shared_out, y=out, stream=stream)
         mark("combine")
+        self._saved = bool(save)
         return out
 
     def backward(self, x, dy, d_aux=1.0, stream=None, events=None):
@@ -225,8 +248,12 @@ class MoELayer:
                                  d_eout=b["d_eout"], d_gates=b["d_gates"], stream=stream)
         mark("combine_bwd")
         moe.moe_expert_down_backward(b["d_eout"], sched, self.packed_bwd, E, F, d_act=b["d_act"], stream=stream)
-        moe.moe_expert_up_gate_backward(d["buf"], b["d_act"], sched, self.packed, self.packed_bwd, E, d_gu=b["d_gu"],
-                                        d_buf=b["d_buf"], stream=stream)
+        if self._saved:                  # g and u kept by forward(save=True)
+            moe.moe_expert_up_gate_backward_saved(self.gu, b["d_act"], sched, self.packed_bwd, E, h, d_gu=b["d_gu"],
+                                                  d_buf=b["d_buf"], stream=stream)
+        else:
+            moe.moe_expert_up_gate_backward(d["buf"], b["d_act"], sched, self.packed, self.packed_bwd, E,
+                                            d_gu=b["d_gu"], d_buf=b["d_buf"], stream=stream)
         mark("expert_dgrad")
         moe.moe_expert_weight_grads(d["buf"], self.act, b["d_gu"], b["d_eout"], d["offsets"], d["kept_counts"], E,
                                     dW_gate=b["dW_gate"], dW_up=b["dW_up"], dW_down=b["dW_down"], ws=b["ws_wg"],
@@ -236,8 +263,13 @@ class MoELayer:
         if self.shared_packed is not None:
             moe.moe_expert_down_backward(dy, self.sh_sched, self.shared_packed_bwd, 1, F, d_act=b["sh_d_act"],
                                          stream=stream)
-            moe.moe_expert_up_gate_backward(x, b["sh_d_act"], self.sh_sched, self.shared_packed, self.shared_packed_bwd,
-                                            1, d_gu=b["sh_d_gu"], d_buf=b["sh_dx"], stream=stream)
+            if self._saved:
+                moe.moe_expert_up_gate_backward_saved(self.sh_gu, b["sh_d_act"], self.sh_sched, self.shared_packed_bwd,
+                                                      1, h, d_gu=b["sh_d_gu"], d_buf=b["sh_dx"], stream=stream)
+            else:
+                moe.moe_expert_up_gate_backward(x, b["sh_d_act"], self.sh_sched, self.shared_packed,
+                                                self.shared_packed_bwd, 1, d_gu=b["sh_d_gu"], d_buf=b["sh_dx"],
+                                                stream=stream)
             moe.moe_expert_weight_grads(x, self.sh_act, b["sh_d_gu"], dy, b["sh_off"], b["sh_kept"], 1,
                                         dW_gate=b["sh_dW_gate"], dW_up=b["sh_dW_up"], dW_down=b["sh_dW_down"],
                                         ws=b["ws_sh"], stream=stream)

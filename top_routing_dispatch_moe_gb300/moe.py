@@ -57,6 +57,8 @@ _SIGS = {
     "moe_pack_expert_weights_backward": (_I, [_P, _P, _P, _I, _I, _I, _I, _P, _P]),
     "moe_expert_down_backward": (_I, [_P, _P, _P, _I, _I, _I, _I, _I, _P, _P]),
     "moe_expert_up_gate_backward": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _P, _P, _P]),
+    "moe_expert_up_gate_save": (_I, [_P, _P, _P, _I, _I, _I, _I, _P, _I, _P, _P, _P, _I, _P, _P, _P]),
+    "moe_expert_up_gate_backward_saved": (_I, [_P, _P, _P, _P, _I, _I, _I, _I, _I, _P, _P, _P]),
     "moe_expert_weight_grads_workspace_size": (_Z, [_I, _I, _I, _I, _I]),
     "moe_expert_weight_grads": (_I, [_P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _P, _P, _P, _P, _Z, _P]),
     "moe_expert_down_shared": (_I, [_P, _P, _P, _I, _I, _I, _I, _P, _I, _P, _P, _I, _P, _P]),
@@ -537,6 +539,36 @@ def moe_expert_up_gate_backward(buf, d_act, tile_sched, packed_w, packed_bwd, E:
     _check(_lib.moe_expert_up_gate_backward(_ptr(buf), _ptr(d_act), _ptr(tile_sched), _ptr(packed_w), _ptr(packed_bwd),
                                             E, h, F, rows, dtype_code(buf.dtype), _ptr(d_gu), _ptr(d_buf),
                                             _stream(stream)))
+    return d_gu, d_buf
+
+
+def moe_expert_up_gate_save(buf, tile_sched, packed_w, E: int, F: int, *, x=None, packed_shared=None, act=None,
+                            gu=None, act_shared=None, gu_shared=None, stream=None):
+    """act and the saved pre-activations gu [rows, gu_cols(F)] (and the shared expert's with packed_shared)."""
+    rows, h = buf.shape
+    dev = buf.device
+    T = x.shape[0] if (x is not None and packed_shared is not None) else 0
+    act = torch.empty((rows, F), dtype=buf.dtype, device=dev) if act is None else act
+    gu = torch.empty((rows, gu_cols(F)), dtype=buf.dtype, device=dev) if gu is None else gu
+    if T:
+        act_shared = torch.empty((T, F), dtype=buf.dtype, device=dev) if act_shared is None else act_shared
+        gu_shared = torch.empty((T, gu_cols(F)), dtype=buf.dtype, device=dev) if gu_shared is None else gu_shared
+    _check(_lib.moe_expert_up_gate_save(_ptr(buf), _ptr(tile_sched), _ptr(packed_w), E, h, F, rows,
+                                        _ptr(x) if T else None, T, _ptr(packed_shared) if T else None,
+                                        _ptr(act_shared) if T else None, _ptr(gu_shared) if T else None,
+                                        dtype_code(buf.dtype), _ptr(act), _ptr(gu), _stream(stream)))
+    return act, gu, act_shared, gu_shared
+
+
+def moe_expert_up_gate_backward_saved(gu, d_act, tile_sched, packed_bwd, E: int, h: int, d_gu=None, d_buf=None,
+                                      stream=None):
+    rows, F = d_act.shape
+    dev = d_act.device
+    d_gu = torch.empty((rows, gu_cols(F)), dtype=d_act.dtype, device=dev) if d_gu is None else d_gu
+    d_buf = torch.empty((rows, h), dtype=d_act.dtype, device=dev) if d_buf is None else d_buf
+    _check(_lib.moe_expert_up_gate_backward_saved(_ptr(gu), _ptr(d_act), _ptr(tile_sched), _ptr(packed_bwd), E, h, F,
+                                                  rows, dtype_code(d_act.dtype), _ptr(d_gu), _ptr(d_buf),
+                                                  _stream(stream)))
     return d_gu, d_buf
 
 
