@@ -259,6 +259,10 @@ int moe_combine(const void* eout, const int32_t* dest_row, const float* gates, c
  * moe_expert_up_gate_fp8: moe_expert_up_gate reading that buffer: each code is dequantised to
  *   bf16(fp32(value) * scale) inside the GEMM (converter warps turn each staged e4m3 tile into the bf16
  *   operand tile in shared memory), so the bf16 buffer never exists in memory. act [rows,F] bf16.
+ * moe_dequant_fp8: the same dequantisation as a pass of its own (the receive side of the FP8 exchange):
+ *   out [rows,h] bf16 = bf16(fp32(value) * scale), bit-identical to the operand moe_expert_up_gate_fp8 builds;
+ *   moe_expert_up_gate on out then gives the same act. h % 128 == 0; buf8 and out 16-byte aligned. On GB300
+ *   this pass plus the bf16 GEMM is the faster of the two routes (the converter warps limit the fused one).
  * ------------------------------------------------------------------------------------------------- */
 int moe_dispatch_fp8(const void* x, const int32_t* topk_ids, int T, int h, int E, int k, int capacity, int num_ranks,
                      uint8_t* buf8, float* scales, int32_t* offsets, int32_t* kept_counts, int32_t* dest_row,
@@ -266,6 +270,7 @@ int moe_dispatch_fp8(const void* x, const int32_t* topk_ids, int T, int h, int E
                      int32_t* rank_offsets, int32_t* tile_sched, void* ws, size_t ws_bytes, void* stream);
 int moe_expert_up_gate_fp8(const uint8_t* buf8, const float* scales, const int32_t* tile_sched, const void* packed_w,
                            int E, int h, int F, int rows, void* act, void* stream);
+int moe_dequant_fp8(const uint8_t* buf8, const float* scales, int rows, int h, void* out, void* stream);
 
 /* ---------------------------------------------------------------------------------------------------
  * Backward of the layer ("专家并行" (formulaic), section "BWD（反向传播）" and the overlap notes: the

@@ -234,3 +234,25 @@ def test_router_large_expert_counts(name, E, k, T, h, want_logits):
         assert cases.rel_max(r["logits"].cpu().numpy(), ref["logits"]) <= 1e-5
     assert cases.rel_max(r["gates"].cpu().numpy(), ref["gates"]) <= 1e-5
     assert cases.rel_max(r["P"].cpu().numpy(), ref["P"]) <= 1e-5
+
+
+def test_router_unsplit_logits_with_bias():
+    """The bf16 tensor-core logits GEMM unsplit (T = 10000, E = 64: 79 output tiles, about one per SM) with the
+    bias added in its fp32 epilogue, whose rows pass through TMA stores (the last tile 16 rows): logits, the
+    indices and the gates against the oracle in the plain softmax mode."""
+    import torch
+    from top_routing_dispatch_moe_gb300 import moe
+    cfg = moe_inputs.get_config("page3_cf1.25", T=10000, h=256, E=64, k=4, F=128, R=1)
+    bias = np.random.default_rng(5).normal(scale=0.1, size=cfg.E)
+    inp = cases.router_inputs(cfg, bias=bias)
+    assert inp["near_ties"] == 0
+    x = cases.to_device(inp["x"], cfg)
+    w = cases.to_device(inp["w_r"], cfg)
+    b = torch.from_numpy(np.asarray(inp["bias"], np.float32)).cuda()
+    r = moe.moe_router(x, w, b, cfg.k, cfg.gating, cfg.alpha)
+    torch.cuda.synchronize()
+    assert moe.moe_check_device_error() == moe.MOE_OK, moe.moe_last_error_string()
+    ref = inp["route"]
+    np.testing.assert_array_equal(r["ids"].cpu().numpy(), ref["ids"])
+    assert cases.rel_max(r["logits"].cpu().numpy(), ref["logits"]) <= 1e-5
+    assert cases.rel_max(r["gates"].cpu().numpy(), ref["gates"]) <= 1e-5

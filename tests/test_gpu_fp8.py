@@ -4,7 +4,8 @@ moe_dispatch_fp8: e4m3 codes and per-token, per-128-column scales bit-exact (the
 round-to-nearest-even on both sides), indices identical to moe_dispatch. moe_expert_up_gate_fp8: its prologue
 turns the staged codes into the bf16 operand tile in shared memory; fed the oracle's dequantised rows as bf16,
 the bf16 GEMM on the same (one-SM) kernel must give bit-identical act, which checks the converter's values and
-its 128-byte swizzle exactly. The layer with the FP8 payload against the oracle's FP8 layer (normwise 2e-2).
+its 128-byte swizzle exactly. moe_dequant_fp8 bit-exact against the oracle's dequantised rows. The layer with the
+FP8 payload (dequantisation pass, then the bf16 GEMM) against the oracle's FP8 layer (normwise 2e-2).
 """
 import numpy as np
 import pytest
@@ -47,6 +48,20 @@ def test_dispatch_fp8_bit_exact(T, h, E, k, C):
     codes, scales = O.dispatch_payload_fp8(x32, disp)
     np.testing.assert_array_equal(d8["buf8"].cpu().numpy(), codes)
     np.testing.assert_array_equal(d8["scales"].cpu().numpy(), scales)
+
+
+@pytest.mark.parametrize("T,h,E,k,C", [(300, 256, 4, 2, 0), (257, 1024, 8, 4, 150)])
+def test_dequant_fp8_matches_oracle(T, h, E, k, C):
+    """moe_dequant_fp8 (the receive side as a pass of its own): bf16(fp32(value) * scale) for every code,
+    bit-identical to the oracle's dequantised rows (pad rows: codes 0, scale 0 -> 0)."""
+    import torch
+    from top_routing_dispatch_moe_gb300 import moe
+    ids, xb, x32 = _problem(T, h, E, k, seed=T + 2 * h)
+    d8 = moe.moe_dispatch_fp8(xb, torch.from_numpy(ids).to("cuda"), E, C, 1)
+    out = moe.moe_dequant_fp8(d8["buf8"], d8["scales"])
+    torch.cuda.synchronize()
+    deq = O.fp8_dequantize_rows(d8["buf8"].cpu().numpy(), d8["scales"].cpu().numpy())
+    np.testing.assert_array_equal(out.float().cpu().numpy(), deq.astype(np.float32))
 
 
 @pytest.mark.parametrize("sizes", [[0, 1, 127, 129, 300], [0, 257, 1900, 40]])

@@ -591,6 +591,49 @@ extern "C" int moe_dispatch_static(const void* x, const int32_t* topk_ids, int T
                         moe::kStaticScratchBytes, stream);
 }
 
+namespace moe {
+// out [rows, h] bf16 = bf16(fp32(e4m3 value of buf8[r, c]) * scales[r, c / 128]): 16 codes per thread pass.
+__global__ void __launch_bounds__(256)
+dequant_fp8_kernel(const uint8_t* __restrict__ buf8, const float* __restrict__ scales, long long rows, int h,
+                   __nv_bfloat16* __restrict__ out) {
+    const int vpr = h / 16, nb = h / 128;
+    const long long n = rows * vpr;
+    for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < n; i += (long long)gridDim.x * blockDim.x) {
+        const long long r = i / vpr;
+        const int c = (int)(i - r * vpr) * 16;
+        const float sc = __ldg(scales + r * nb + (c >> 7));
+        const uint4 q = __ldcs(reinterpret_cast<const uint4*>(buf8 + r * h + c));
+        const uint32_t qw[4] = {q.x, q.y, q.z, q.w};
+        uint32_t o[8];
+#pragma unroll
+        for (int hw = 0; hw < 8; ++hw) {
+            const __nv_fp8x2_storage_t pr = (__nv_fp8x2_storage_t)((qw[hw >> 1] >> (16 * (hw & 1))) & 0xFFFFu);
+            const __half2_raw hr = __nv_cvt_fp8x2_to_halfraw2(pr, __NV_E4M3);
+            const float2 fv = __half22float2(*reinterpret_cast<const __half2*>(&hr));
+            const __nv_bfloat162 bv = __floats2bfloat162_rn(fv.x * sc, fv.y * sc);
+            o[hw] = *reinterpret_cast<const uint32_t*>(&bv);
+        }
+        uint4* dst = reinterpret_cast<uint4*>(out + r * h + c);
+        dst[0] = make_uint4(o[0], o[1], o[2], o[3]);
+        dst[1] = make_uint4(o[4], o[5], o[6], o[7]);
+    }
+}
+}  // namespace moe
+
+extern "C" int moe_dequant_fp8(const uint8_t* buf8, const float* scales, int rows, int h, void* out, void* stream) {
+    MOE_REQUIRE(rows >= 0 && h > 0 && h % 128 == 0, MOE_ERR_INVALID_ARG, "moe_dequant_fp8: rows=%d h=%d (need h%%128==0)",
+                rows, h);
+    if (rows == 0) return MOE_OK;
+    MOE_REQUIRE(buf8 && scales && out, MOE_ERR_INVALID_ARG, "moe_dequant_fp8: null pointer");
+    MOE_REQUIRE(aligned16(buf8) && aligned16(out), MOE_ERR_INVALID_ARG,
+                "moe_dequant_fp8: buf8 and out must be 16-byte aligned");
+    const long long n = (long long)rows * (h / 16);
+    const int grid = (int)std::min<long long>(cdiv(n, 256), 8LL * num_sms());
+    dequant_fp8_kernel<<<grid, 256, 0, static_cast<cudaStream_t>(stream)>>>(buf8, scales, rows, h,
+                                                                            static_cast<__nv_bfloat16*>(out));
+    return check_launch("dequant_fp8_kernel");
+}
+
 extern "C" int moe_dispatch_fp8(const void* x, const int32_t* topk_ids, int T, int h, int E, int k, int capacity,
                                 int num_ranks, uint8_t* buf8, float* scales, int32_t* offsets, int32_t* kept_counts,
                                 int32_t* dest_row, uint8_t* drop_mask, int32_t* src_token, int32_t* src_slot,

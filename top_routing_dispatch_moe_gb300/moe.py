@@ -46,6 +46,7 @@ _SIGS = {
     "moe_expert_up_gate_shared": (_I, [_P, _P, _P, _I, _I, _I, _I, _P, _I, _P, _P, _I, _P, _P]),
     "moe_dispatch_fp8": (_I, [_P, _P, _I, _I, _I, _I, _I, _I, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _Z, _P]),
     "moe_expert_up_gate_fp8": (_I, [_P, _P, _P, _P, _I, _I, _I, _I, _P, _P]),
+    "moe_dequant_fp8": (_I, [_P, _P, _I, _I, _P, _P]),
     "moe_combine_backward": (_I, [_P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _P, _P, _P]),
     "moe_router_backward_workspace_size": (_Z, [_I, _I]),
     "moe_router_backward": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _F, _F, _P, _P, _P, _Z, _P]),
@@ -249,6 +250,13 @@ def moe_expert_up_gate_fp8(buf8, scales, tile_sched, packed_w, E: int, F: int, a
     _check(_lib.moe_expert_up_gate_fp8(_ptr(buf8), _ptr(scales), _ptr(tile_sched), _ptr(packed_w), E, h, F, rows,
                                        _ptr(act), _stream(stream)))
     return act
+
+
+def moe_dequant_fp8(buf8, scales, out=None, stream=None):
+    rows, h = buf8.shape
+    out = torch.empty((rows, h), dtype=torch.bfloat16, device=buf8.device) if out is None else out
+    _check(_lib.moe_dequant_fp8(_ptr(buf8), _ptr(scales), rows, h, _ptr(out), _stream(stream)))
+    return out
 
 
 def moe_dispatch_static(x, topk_ids, E: int, capacity: int = 0, num_ranks: int = 1, *, out=None, stream=None):
