@@ -160,6 +160,59 @@ dispatch_scatter_kernel(const int32_t* __restrict__ ids, int T, int E, int k, in
                [&](int e) { return offsets[e]; }, dest_row, drop_mask, src_token, src_slot);
 }
 
+// One token's FP8 payload, one warp: lanes 0-15 and 16-31 take alternate blocks of 128 columns (8 columns a
+// lane); per block amax over the 16 lanes, scale = amax / 448 (1 for an all-zero block), codes =
+// e4m3(x / scale) to nearest even, saturating; codes and (first lane of the half) the scale go to every kept
+// destination row dj[j] >= 0, j < k.
+__device__ __forceinline__ void fp8_copy_token(const __nv_bfloat16* __restrict__ src, const int (&dj)[16], int k, int h,
+                                               uint8_t* __restrict__ buf8, float* __restrict__ scales, int lane) {
+    const int half = lane >> 4, hl = lane & 15;
+    const int nblk = h / 128;
+    constexpr int U = 2;                          // 2 x 2 blocks of 128 columns per iteration
+    for (int b0 = 0; b0 < nblk; b0 += 2 * U) {
+        Vec16<__nv_bfloat16> v[U];
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+            const int b = b0 + 2 * u + half;
+            if (b < nblk) v[u] = ld16_stream(src + (size_t)b * 128 + hl * 8);
+            else v[u].v = make_uint4(0, 0, 0, 0);
+        }
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+            const int b = b0 + 2 * u + half;
+            float f[8];
+            float amax = 0.f;
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+                f[i] = v[u].get(i);
+                amax = fmaxf(amax, fabsf(f[i]));
+            }
+#pragma unroll
+            for (int off = 8; off > 0; off >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, off));
+            const float sc = amax > 0.f ? amax / 448.f : 1.f;
+            uint32_t w[2];
+#pragma unroll
+            for (int i = 0; i < 2; ++i) {
+                const __nv_fp8x2_storage_t lo = __nv_cvt_float2_to_fp8x2(make_float2(f[4 * i] / sc, f[4 * i + 1] / sc),
+                                                                         __NV_SATFINITE, __NV_E4M3);
+                const __nv_fp8x2_storage_t hi = __nv_cvt_float2_to_fp8x2(make_float2(f[4 * i + 2] / sc,
+                                                                                     f[4 * i + 3] / sc),
+                                                                         __NV_SATFINITE, __NV_E4M3);
+                w[i] = (uint32_t)lo | ((uint32_t)hi << 16);
+            }
+            if (b < nblk) {
+#pragma unroll
+                for (int j = 0; j < 16; ++j)
+                    if (j < k && dj[j] >= 0) {
+                        *reinterpret_cast<uint2*>(buf8 + (size_t)dj[j] * h + (size_t)b * 128 + hl * 8) =
+                            make_uint2(w[0], w[1]);
+                        if (hl == 0) scales[(size_t)dj[j] * nblk + b] = sc;
+                    }
+            }
+        }
+    }
+}
+
 // Scan, scatter and payload copy in one launch, for small count tables (at most kFusedScanEntries
 // entries, chunks of tpc tokens): every block adds up the count table itself (its own chunk base and the
 // per-expert totals, in a fixed order) and derives the same offsets; block 0 also publishes offsets, kept
@@ -190,14 +243,17 @@ inline int fused_tokens_per_chunk(int T, int E, int k, int max_chunks) {
     return tpc * k <= kChunkA ? tpc : 0;
 }
 
-template <typename T>
+// FP8: the payload goes to buf8 / scales as e4m3 codes with per-128-column scales (fp8_copy_token; T is bf16,
+// buf unused); pad rows get codes 0 and scale 0.
+template <typename T, bool FP8 = false>
 __global__ void __launch_bounds__(kChunkA)
 dispatch_fused_kernel(const T* __restrict__ x, const int32_t* __restrict__ ids, int T_, int h, int E, int k, int tpc,
                       int C, int R, const int32_t* __restrict__ chunk_counts, int nchunks, T* __restrict__ buf,
                       int32_t* __restrict__ offsets, int32_t* __restrict__ kept_counts,
                       int32_t* __restrict__ rank_counts, int32_t* __restrict__ rank_offsets,
                       int32_t* __restrict__ sched, int32_t* __restrict__ dest_row, uint8_t* __restrict__ drop_mask,
-                      int32_t* __restrict__ src_token, int32_t* __restrict__ src_slot) {
+                      int32_t* __restrict__ src_token, int32_t* __restrict__ src_slot, uint8_t* __restrict__ buf8 = nullptr,
+                      float* __restrict__ scales = nullptr) {
     extern __shared__ int sm[];
     int* s_wc = sm + fused_wc(E);
     int* s_base = sm + fused_base(E);
@@ -245,6 +301,13 @@ dispatch_fused_kernel(const T* __restrict__ x, const int32_t* __restrict__ ids, 
     const int t0 = blockIdx.x * tpc;
     const int ntok = min(tpc, T_ - t0);
     for (int tl = warp; tl < ntok; tl += kChunkA / 32) {
+        if constexpr (FP8) {
+            int dj[16];
+#pragma unroll
+            for (int j = 0; j < 16; ++j) dj[j] = j < k ? s_dest[tl * k + j] : -1;
+            fp8_copy_token(x + (size_t)(t0 + tl) * h, dj, k, h, buf8, scales, lane);
+            continue;
+        }
         const T* src = x + (size_t)(t0 + tl) * h;
         constexpr int U = 4;
         for (int d0 = lane * V; d0 < h; d0 += U * 32 * V) {
@@ -273,9 +336,15 @@ dispatch_fused_kernel(const T* __restrict__ x, const int32_t* __restrict__ ids, 
             for (; p < npad; p += W) {
                 const long long r = (long long)ee * C + s_kept[ee] + p;
                 if (lane == 0) { src_token[r] = -1; src_slot[r] = -1; }
-                Vec16<T> z;
-                z.v = {};
-                for (int d0 = lane * V; d0 < h; d0 += 32 * V) st16(buf + r * h + d0, z);
+                if constexpr (FP8) {
+                    for (int d0 = lane * 16; d0 < h; d0 += 32 * 16)
+                        *reinterpret_cast<uint4*>(buf8 + r * h + d0) = make_uint4(0, 0, 0, 0);
+                    for (int b = lane; b < h / 128; b += 32) scales[r * (h / 128) + b] = 0.f;
+                } else {
+                    Vec16<T> z;
+                    z.v = {};
+                    for (int d0 = lane * V; d0 < h; d0 += 32 * V) st16(buf + r * h + d0, z);
+                }
             }
             run += npad;
         }
@@ -339,7 +408,7 @@ dispatch_copy_fp8_kernel(const __nv_bfloat16* __restrict__ x, const int32_t* __r
                          int k, uint8_t* __restrict__ buf8, float* __restrict__ scales, int tok_blocks,
                          const int32_t* __restrict__ kept_counts, int E, int C, int32_t* __restrict__ src_token,
                          int32_t* __restrict__ src_slot) {
-    const int lane = threadIdx.x & 31, half = lane >> 4, hl = lane & 15;
+    const int lane = threadIdx.x & 31;
     const int nblk = h / 128;
     if ((int)blockIdx.x < tok_blocks) {
         const int t = blockIdx.x * 8 + (threadIdx.x >> 5);
@@ -348,50 +417,7 @@ dispatch_copy_fp8_kernel(const __nv_bfloat16* __restrict__ x, const int32_t* __r
         int dj[16];
 #pragma unroll
         for (int j = 0; j < 16; ++j) dj[j] = __shfl_sync(0xffffffffu, my, j);
-        const __nv_bfloat16* src = x + (size_t)t * h;
-        constexpr int U = 2;                          // 2 x 2 blocks of 128 columns per iteration
-        for (int b0 = 0; b0 < nblk; b0 += 2 * U) {
-            Vec16<__nv_bfloat16> v[U];
-#pragma unroll
-            for (int u = 0; u < U; ++u) {
-                const int b = b0 + 2 * u + half;
-                if (b < nblk) v[u] = ld16_stream(src + (size_t)b * 128 + hl * 8);
-                else v[u].v = make_uint4(0, 0, 0, 0);
-            }
-#pragma unroll
-            for (int u = 0; u < U; ++u) {
-                const int b = b0 + 2 * u + half;
-                float f[8];
-                float amax = 0.f;
-#pragma unroll
-                for (int i = 0; i < 8; ++i) {
-                    f[i] = v[u].get(i);
-                    amax = fmaxf(amax, fabsf(f[i]));
-                }
-#pragma unroll
-                for (int off = 8; off > 0; off >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, off));
-                const float sc = amax > 0.f ? amax / 448.f : 1.f;
-                uint32_t w[2];
-#pragma unroll
-                for (int i = 0; i < 2; ++i) {
-                    const __nv_fp8x2_storage_t lo = __nv_cvt_float2_to_fp8x2(make_float2(f[4 * i] / sc, f[4 * i + 1] / sc),
-                                                                             __NV_SATFINITE, __NV_E4M3);
-                    const __nv_fp8x2_storage_t hi = __nv_cvt_float2_to_fp8x2(make_float2(f[4 * i + 2] / sc,
-                                                                                         f[4 * i + 3] / sc),
-                                                                             __NV_SATFINITE, __NV_E4M3);
-                    w[i] = (uint32_t)lo | ((uint32_t)hi << 16);
-                }
-                if (b < nblk) {
-#pragma unroll
-                    for (int j = 0; j < 16; ++j)
-                        if (j < k && dj[j] >= 0) {
-                            *reinterpret_cast<uint2*>(buf8 + (size_t)dj[j] * h + (size_t)b * 128 + hl * 8) =
-                                make_uint2(w[0], w[1]);
-                            if (hl == 0) scales[(size_t)dj[j] * nblk + b] = sc;
-                        }
-                }
-            }
-        }
+        fp8_copy_token(x + (size_t)t * h, dj, k, h, buf8, scales, lane);
         return;
     }
     const long long rows = (long long)E * C;
@@ -663,6 +689,19 @@ extern "C" int moe_dispatch_fp8(const void* x, const int32_t* topk_ids, int T, i
     unsigned* err = device_error_word();
     MOE_REQUIRE(err, MOE_ERR_CUDA, "moe_dispatch_fp8: device error word unavailable");
     int32_t* chunk = static_cast<int32_t*>(ws);
+    const int tpc_f = fused_tokens_per_chunk(T, E, k, std::min(kFusedMaxChunks, num_sms()));
+    if (tpc_f > 0) {                              // count, then scan + scatter + quantised copy in one launch
+        const int nchf = cdiv(T, tpc_f);
+        dispatch_count_kernel<<<nchf, kChunkA, E * sizeof(int), s>>>(topk_ids, T, E, k, tpc_f, chunk, err);
+        if (int rc = check_launch("dispatch_count_kernel")) return rc;
+        const size_t smem = (size_t)fused_smem_ints(E) * sizeof(int);
+        cudaFuncSetAttribute(dispatch_fused_kernel<__nv_bfloat16, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)smem);
+        dispatch_fused_kernel<__nv_bfloat16, true><<<nchf, kChunkA, smem, s>>>(static_cast<const __nv_bfloat16*>(x),
+            topk_ids, T, h, E, k, tpc_f, capacity, num_ranks, chunk, nchf, nullptr, offsets, kept_counts, rank_counts,
+            rank_offsets, tile_sched, dest_row, drop_mask, src_token, src_slot, buf8, scales);
+        return check_launch("dispatch_fused_kernel<fp8>");
+    }
     const int nch = num_chunks(T, k);
     if (nch > 0) {
         dispatch_count_kernel<<<nch, kChunkA, E * sizeof(int), s>>>(topk_ids, T, E, k, kChunkA / k, chunk, err);
