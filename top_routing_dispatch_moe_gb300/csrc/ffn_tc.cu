@@ -201,7 +201,9 @@ __host__ __device__ constexpr uint32_t idesc_bf16() {
 // Epilogues: SwiGLU of the packed gate/up tile -> bf16 act; plain bf16 conversion; fp32 (+ per-column bias),
 // used for the router logits and the weight gradients; SwiGLU backward of the packed gate/up tile (reads the
 // act gradient, writes the gate and up pre-activation gradients in the packed column order).
-enum Epi : int { EPI_SWIGLU = 0, EPI_BF16 = 1, EPI_F32 = 2, EPI_SWIGLU_BWD = 3 };
+// EPI_SWIGLU_SAVE: EPI_SWIGLU that also stores the pre-activations (Params::gu_out / sh_gu_out); a separate
+// instantiation, so that the plain forward carries no trace of it.
+enum Epi : int { EPI_SWIGLU = 0, EPI_BF16 = 1, EPI_F32 = 2, EPI_SWIGLU_BWD = 3, EPI_SWIGLU_SAVE = 4 };
 
 struct Params {
     const int32_t* sched;
@@ -235,7 +237,7 @@ struct Params {
     // one-SM kernel: column extents of the A and B tensor maps (0: K) and the operands' column of reduction
     // index k, k mod kmod (0: k), for a K range that runs over one operand several times (a multiple of BK)
     int a_cols, b_cols, a_kmod, b_kmod;
-    // EPI_SWIGLU: when set, the pre-activations g and u (bf16) of the routed / shared rows, [rows][NT * 256] in the
+    // EPI_SWIGLU_SAVE: the pre-activations g and u (bf16) of the routed / shared rows, [rows][NT * 256] in the
     // packed gate/up column order (block n: 128 columns of g, then the u of the same f)
     __nv_bfloat16* gu_out;
     __nv_bfloat16* sh_gu_out;
@@ -336,7 +338,7 @@ __device__ __forceinline__ void store_tile(const Params& p, __nv_bfloat16* out, 
                 }
             }
         }
-    } else if constexpr (EPI == EPI_SWIGLU) {
+    } else if constexpr (EPI == EPI_SWIGLU || EPI == EPI_SWIGLU_SAVE) {
 #pragma unroll 1
         for (int j = 0; j < 4; ++j) {
             float g[32], u[32];
@@ -357,7 +359,7 @@ __device__ __forceinline__ void store_tile(const Params& p, __nv_bfloat16* out, 
                         st16(dst + c, o);
                     }
                 }
-                if (gu) {                    // saved pre-activations (f >= F: zero weight rows give zero)
+                if constexpr (EPI == EPI_SWIGLU_SAVE) {   // pre-activations (f >= F: zero weight rows give zero)
                     __nv_bfloat16* gdst = gu + (size_t)row * (p.NT * 256) + (size_t)n * 256 + 32 * j;
 #pragma unroll
                     for (int c = 0; c < 32; c += 8) {
@@ -442,7 +444,7 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
                     const __grid_constant__ CUtensorMap tmO, const __grid_constant__ CUtensorMap tmO2, Params p) {
     constexpr int BN = CF::BN, STAGES = CF::STAGES, B_BYTES = CF::B_BYTES, STAGE_BYTES = CF::STAGE_BYTES;
     constexpr uint32_t kIdesc = idesc_bf16<BN>();
-    static_assert((EPI != EPI_SWIGLU && EPI != EPI_SWIGLU_BWD) || BN == 256,
+    static_assert((EPI != EPI_SWIGLU && EPI != EPI_SWIGLU_SAVE && EPI != EPI_SWIGLU_BWD) || BN == 256,
                   "the SwiGLU epilogues pair 128 gate with 128 up columns");
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw_addr = smem_u32(smem_raw);
@@ -1145,6 +1147,7 @@ static int gemm(const void* a, long long a_rows, const void* b, long long b_rows
     if (int rc = make_out_maps<EPI>(p, a_rows, ma, &mo, &mo2)) return rc;
     grouped_gemm_kernel<EPI, CF><<<num_sms(), NUM_THREADS, smem_bytes, s>>>(ma, mb, ma2, mb2, mo, mo2, p);
     return check_launch(EPI == EPI_SWIGLU ? "grouped_gemm_kernel<up_gate>"
+                        : EPI == EPI_SWIGLU_SAVE ? "grouped_gemm_kernel<up_gate, save>"
                         : EPI == EPI_BF16 ? "grouped_gemm_kernel<bf16>"
                         : EPI == EPI_SWIGLU_BWD ? "grouped_gemm_kernel<swiglu_bwd>" : "grouped_gemm_kernel<f32>");
 }
@@ -1186,6 +1189,7 @@ static int gemm_pair(const void* a, long long a_rows, const void* b, long long b
     if (int rc = make_out_maps<EPI>(p, a_rows, ma, &mo, &mo2)) return rc;
     grouped_gemm_pair_kernel<EPI><<<2 * clusters[dev], NUM_THREADS, smem_bytes, s>>>(ma, mb, ma2, mb2, mo, mo2, p);
     return check_launch(EPI == EPI_SWIGLU ? "grouped_gemm_pair_kernel<up_gate>"
+                        : EPI == EPI_SWIGLU_SAVE ? "grouped_gemm_pair_kernel<up_gate, save>"
                         : EPI == EPI_SWIGLU_BWD ? "grouped_gemm_pair_kernel<swiglu_bwd>"
                         : EPI == EPI_F32 ? "grouped_gemm_pair_kernel<f32>" : "grouped_gemm_pair_kernel<bf16>");
 }
@@ -1210,6 +1214,11 @@ int ffn_tc_up_gate(const void* buf, const int32_t* sched, const void* packed, in
     const char* b = static_cast<const char*>(packed) + L.up_gate_off;
     const tc::SharedOperands sh{x_sh, packed_sh ? static_cast<const char*>(packed_sh) + Ls.up_gate_off : nullptr,
                                 2LL * Ls.Fp};
+    if (gu || gu_sh) {
+        if (tc::use_pair(E, rows))
+            return tc::gemm_pair<tc::EPI_SWIGLU_SAVE>(buf, rows, b, (long long)E * 2 * L.Fp, p, s, sh);
+        return tc::gemm<tc::EPI_SWIGLU_SAVE, tc::Wide>(buf, rows, b, (long long)E * 2 * L.Fp, p, s, sh);
+    }
     if (tc::use_pair(E, rows)) return tc::gemm_pair<tc::EPI_SWIGLU>(buf, rows, b, (long long)E * 2 * L.Fp, p, s, sh);
     return tc::gemm<tc::EPI_SWIGLU, tc::Wide>(buf, rows, b, (long long)E * 2 * L.Fp, p, s, sh);
 }
