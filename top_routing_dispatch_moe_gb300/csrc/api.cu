@@ -31,6 +31,14 @@ int check_launch(const char* what) {
     return MOE_OK;
 }
 
+int check_launch(cudaError_t launch_result, const char* what) {
+    const int rc = check_launch(what);
+    if (rc != MOE_OK) return rc;
+    if (launch_result != cudaSuccess)
+        return set_error(MOE_ERR_CUDA, "%s: %s", what, cudaGetErrorString(launch_result));
+    return MOE_OK;
+}
+
 static constexpr int kMaxDevices = 64;
 static std::mutex g_mu;
 static int g_sms[kMaxDevices];

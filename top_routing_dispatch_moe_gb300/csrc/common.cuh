@@ -15,6 +15,7 @@ namespace moe {
 // ------------------------------------------------------------------------------------------------
 int set_error(int code, const char* fmt, ...);          // records the message, returns code
 int check_launch(const char* what);                       // MOE_ERR_CUDA if the last launch failed
+int check_launch(cudaError_t launch_result, const char* what);   // the same for a launch that returned a status
 int num_sms();                                            // SM count of the current device (cached)
 unsigned* device_error_word();                            // device address of the error word (current device)
 long long wait_limit();                                   // iteration limit of bounded device waits
@@ -22,6 +23,30 @@ long long wait_limit();                                   // iteration limit of 
 inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 inline size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 inline int cdiv(long long a, long long b) { return (int)((a + b - 1) / b); }
+
+// Programmatic dependent launch: a kernel launched by launch_pdl may start while the previous kernel of its
+// stream still runs (once every block of that kernel has called pdl_trigger, or exited); it must call pdl_wait
+// before it reads anything the previous kernel writes (pdl_wait returns when that kernel has completed and its
+// writes are visible). Both are no-ops for kernels launched without the attribute.
+#ifdef __CUDACC__
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+#endif
+template <typename... KArgs, typename... Args>
+inline cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t s,
+                              Args... args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kernel, static_cast<KArgs>(args)...);
+}
 
 #define MOE_REQUIRE(cond, code, ...) \
     do { if (!(cond)) return ::moe::set_error((code), __VA_ARGS__); } while (0)

@@ -27,6 +27,7 @@ __global__ void __launch_bounds__(kChunkA)
 dispatch_count_kernel(const int32_t* __restrict__ ids, int T, int E, int k, int tpc, int32_t* __restrict__ chunk_counts,
                       unsigned* err) {
     extern __shared__ int s_hist[];
+    pdl_trigger();                            // the fused dispatch may launch now (it waits for these counts)
     for (int e = threadIdx.x; e < E; e += blockDim.x) s_hist[e] = 0;
     __syncthreads();
     const int a = threadIdx.x;
@@ -264,6 +265,15 @@ dispatch_fused_kernel(const T* __restrict__ x, const int32_t* __restrict__ ids, 
     int* s_rb = sm + fused_red(E);
     int* s_rt = s_rb + kChunkA;
     __shared__ int s_tmp[32];
+    {   // this chunk's token rows are known from the start: have L2 fetch them while the count table is summed
+        // and the chunk ranked (16-byte multiples: h % 8 == 0)
+        const int t0p = blockIdx.x * tpc, np = min(tpc, T_ - t0p);
+        const unsigned row_bytes = (unsigned)(h * sizeof(T));
+        for (int i = threadIdx.x; i < np; i += blockDim.x)
+            asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;"
+                         ::"l"(reinterpret_cast<uint64_t>(x + (size_t)(t0p + i) * h)), "r"(row_bytes) : "memory");
+    }
+    pdl_wait();                               // the count table (dispatch_count_kernel) is complete from here on
     {   // count table -> this chunk's base and the per-expert totals: S slices of chunks per expert in
         // parallel, then a tree over the slices (S = largest power of two with S * E <= kChunkA)
         int S = 1;
@@ -500,19 +510,22 @@ extern "C" int moe_dispatch(const void* x, const int32_t* topk_ids, int T, int h
         dispatch_count_kernel<<<nch, kChunkA, E * sizeof(int), s>>>(topk_ids, T, E, k, tpc_f, chunk, err);
         if (int rc = check_launch("dispatch_count_kernel")) return rc;
         const size_t smem = (size_t)fused_smem_ints(E) * sizeof(int);
+        cudaError_t le;
         if (dtype == MOE_BF16) {
             cudaFuncSetAttribute(dispatch_fused_kernel<__nv_bfloat16>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  (int)smem);
-            dispatch_fused_kernel<__nv_bfloat16><<<nch, kChunkA, smem, s>>>(static_cast<const __nv_bfloat16*>(x),
-                topk_ids, T, h, E, k, tpc_f, capacity, num_ranks, chunk, nch, static_cast<__nv_bfloat16*>(buf),
-                offsets, kept_counts, rank_counts, rank_offsets, tile_sched, dest_row, drop_mask, src_token, src_slot);
+            le = launch_pdl(dispatch_fused_kernel<__nv_bfloat16>, dim3(nch), dim3(kChunkA), smem, s,
+                static_cast<const __nv_bfloat16*>(x), topk_ids, T, h, E, k, tpc_f, capacity, num_ranks,
+                (const int32_t*)chunk, nch, static_cast<__nv_bfloat16*>(buf), offsets, kept_counts, rank_counts,
+                rank_offsets, tile_sched, dest_row, drop_mask, src_token, src_slot, (uint8_t*)nullptr, (float*)nullptr);
         } else {
             cudaFuncSetAttribute(dispatch_fused_kernel<float>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-            dispatch_fused_kernel<float><<<nch, kChunkA, smem, s>>>(static_cast<const float*>(x), topk_ids, T, h, E, k,
-                tpc_f, capacity, num_ranks, chunk, nch, static_cast<float*>(buf), offsets, kept_counts, rank_counts,
-                rank_offsets, tile_sched, dest_row, drop_mask, src_token, src_slot);
+            le = launch_pdl(dispatch_fused_kernel<float>, dim3(nch), dim3(kChunkA), smem, s, static_cast<const float*>(x),
+                topk_ids, T, h, E, k, tpc_f, capacity, num_ranks, (const int32_t*)chunk, nch, static_cast<float*>(buf),
+                offsets, kept_counts, rank_counts, rank_offsets, tile_sched, dest_row, drop_mask, src_token, src_slot,
+                (uint8_t*)nullptr, (float*)nullptr);
         }
-        return check_launch("dispatch_fused_kernel");
+        return check_launch(le, "dispatch_fused_kernel");
     }
     // large count tables (or no tokens): count, scan, scatter, then copy and pad fill
     const int nch = num_chunks(T, k);
@@ -697,10 +710,11 @@ extern "C" int moe_dispatch_fp8(const void* x, const int32_t* topk_ids, int T, i
         const size_t smem = (size_t)fused_smem_ints(E) * sizeof(int);
         cudaFuncSetAttribute(dispatch_fused_kernel<__nv_bfloat16, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              (int)smem);
-        dispatch_fused_kernel<__nv_bfloat16, true><<<nchf, kChunkA, smem, s>>>(static_cast<const __nv_bfloat16*>(x),
-            topk_ids, T, h, E, k, tpc_f, capacity, num_ranks, chunk, nchf, nullptr, offsets, kept_counts, rank_counts,
-            rank_offsets, tile_sched, dest_row, drop_mask, src_token, src_slot, buf8, scales);
-        return check_launch("dispatch_fused_kernel<fp8>");
+        const cudaError_t le = launch_pdl(dispatch_fused_kernel<__nv_bfloat16, true>, dim3(nchf), dim3(kChunkA), smem, s,
+            static_cast<const __nv_bfloat16*>(x), topk_ids, T, h, E, k, tpc_f, capacity, num_ranks, (const int32_t*)chunk,
+            nchf, (__nv_bfloat16*)nullptr, offsets, kept_counts, rank_counts, rank_offsets, tile_sched, dest_row,
+            drop_mask, src_token, src_slot, buf8, scales);
+        return check_launch(le, "dispatch_fused_kernel<fp8>");
     }
     const int nch = num_chunks(T, k);
     if (nch > 0) {

@@ -230,6 +230,7 @@ template <typename T, int EMAX, int U>
 __global__ void __launch_bounds__(kRouterWarps * 32, 2)
 router_small_kernel(const T* __restrict__ x, const T* __restrict__ w_r, const float* __restrict__ bias, int T_,
                     int h, int E, int k, int gating, GateOut o) {
+    pdl_trigger();                            // the finalize may launch now (it waits for this kernel's partials)
     extern __shared__ __align__(16) unsigned char smem_raw[];
     T* wT = reinterpret_cast<T*>(smem_raw);                                     // [E][h]
     float* s_P = reinterpret_cast<float*>(smem_raw + (((size_t)E * h * sizeof(T) + 15) & ~(size_t)15));
@@ -332,6 +333,7 @@ template <int NB, int U>   // NB blocks of 8 experts (E <= 8 NB); U chunks of 32
 __global__ void __launch_bounds__(kRouterWarps * 32, 2)
 router_mma_kernel(const __nv_bfloat16* __restrict__ x, const __nv_bfloat16* __restrict__ w_r,
                   const float* __restrict__ bias, int T_, int h, int E, int k, int gating, GateOut o) {
+    pdl_trigger();                            // the finalize may launch now (it waits for this kernel's partials)
     constexpr int EP = 8 * NB;
     extern __shared__ __align__(16) unsigned char smem_raw[];
     const int stride = mma_wt_stride(h);
@@ -499,6 +501,7 @@ template <int NPL>
 __global__ void __launch_bounds__(kRouterWarps * 32)
 router_gate_kernel(const float* __restrict__ logits, int nparts, size_t part_stride, const float* __restrict__ lbias,
                    const float* __restrict__ bias, int T_, int E, int k, int gating, GateOut o) {
+    pdl_trigger();                            // the finalize may launch now (it waits for this kernel's partials)
     extern __shared__ __align__(16) unsigned char smem_raw[];
     float* s_P = reinterpret_cast<float*>(smem_raw);
     int* s_hist = reinterpret_cast<int*>(s_P + kRouterWarps * E);
@@ -571,6 +574,7 @@ __global__ void __launch_bounds__(1024)
 router_finalize(const float* __restrict__ partial_P, const int32_t* __restrict__ partial_C, int grid, int T_, int E,
                 int k, float alpha, int32_t* counts, float* f, float* P, float* aux, float* term_part,
                 unsigned* ticket) {
+    pdl_wait();                               // the gating kernel's partials and its zeroed ticket
     __shared__ float s_p[1024];
     __shared__ int s_c[1024];
     __shared__ float s_t[kFinExperts];
@@ -824,9 +828,10 @@ extern "C" int moe_router(const void* x, const void* w_r, const float* bias, int
             if (int rc = check_launch("router_gate_kernel")) return rc;
         }
     }
-    router_finalize<<<finalize_grid(T, E), 1024, 0, s>>>(w.partial_P, w.partial_C, T > 0 ? G : 0, T, E, k, alpha,
-                                                          counts, f, P, aux, w.term_part, w.ticket);
-    return check_launch("router_finalize");
+    const cudaError_t le = launch_pdl(router_finalize, dim3(finalize_grid(T, E)), dim3(1024), 0, s,
+                                      (const float*)w.partial_P, (const int32_t*)w.partial_C, T > 0 ? G : 0, T, E, k,
+                                      alpha, counts, f, P, aux, w.term_part, w.ticket);
+    return check_launch(le, "router_finalize");
 }
 
 extern "C" size_t moe_router_from_logits_workspace_size(int T, int E) {
@@ -864,7 +869,8 @@ extern "C" int moe_router_from_logits(const float* logits, const float* bias, in
 #undef MOE_GATE_LAUNCH2
         if (int rc = check_launch("router_gate_kernel")) return rc;
     }
-    router_finalize<<<finalize_grid(T, E), 1024, 0, s>>>(o.partial_P, o.partial_C, T > 0 ? G : 0, T, E, k, alpha,
-                                                          counts, f, P, aux, w.term_part, w.ticket);
-    return check_launch("router_finalize");
+    const cudaError_t le = launch_pdl(router_finalize, dim3(finalize_grid(T, E)), dim3(1024), 0, s,
+                                      (const float*)o.partial_P, (const int32_t*)o.partial_C, T > 0 ? G : 0, T, E, k,
+                                      alpha, counts, f, P, aux, w.term_part, w.ticket);
+    return check_launch(le, "router_finalize");
 }
