@@ -338,8 +338,9 @@ int moe_dispatch_backward(const void* d_buf, const int32_t* dest_row, const floa
  *     d_buf [rows,h] = d_g @ W_gate[e] + d_u @ W_up[e]
  *   moe_expert_weight_grads: fp32 [E,F,h] dW_gate = d_g^T buf, dW_up = d_u^T buf, [E,h,F] dW_down = d_eout^T act
  *     over each expert's kept rows [offsets[e], offsets[e] + kept_counts[e]) (zero for an expert without rows),
- *     from buf, act (the forward's), d_gu and d_eout. Workspace: moe_expert_weight_grads_workspace_size()
- *     bytes (each expert's rows transposed into a 64-aligned column segment).
+ *     from buf, act (the forward's), d_gu and d_eout (all pointers 16-byte aligned). Workspace:
+ *     moe_expert_weight_grads_workspace_size() bytes (each expert's rows transposed into a 64-aligned column
+ *     segment).
  *   Rows outside the kept ranges are not read (weight gradients) or not written (d_act, d_gu, d_buf). */
 size_t moe_packed_weights_backward_bytes(int E, int h, int F, int dtype);
 int moe_pack_expert_weights_backward(const void* w_gate, const void* w_up, const void* w_down, int E, int h, int F,

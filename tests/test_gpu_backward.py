@@ -275,3 +275,28 @@ def test_layer_backward_sinkhorn():
                             ("dW_down", _np(g["dW_down"]), np.stack([w[2] for w in ref["dW"]]))]:
         err = cases.rel_l2(got, want)
         assert err <= 2e-2, f"{what}: rel err {err:.3e}"
+
+
+@pytest.mark.parametrize("name", ["page3_small", "deepseek_small"])
+def test_backward_deterministic(name):
+    """Two backward passes over the same saved forward give bit-identical gradients (every reduction runs in a
+    fixed order: no atomics in any accumulation, split-K parts and per-block partials added in order)."""
+    import torch
+    base, over, bias_kind = LAYER_CASES[name]
+    cfg = moe_inputs.get_config(base, **over)
+    inp = cases.router_inputs(cfg)
+    wg, wu, wd = moe_inputs.all_expert_weights(cfg)
+    shared = tuple(a[0] for a in moe_inputs.all_expert_weights(cfg, shared=True)) if cfg.n_shared else None
+    layer = cases.build_gpu_layer(cfg, inp, wg, wu, wd, shared, backward=True)
+    x = cases.to_device(inp["x"], cfg)
+    layer.forward(x, save=True)
+    dy = torch.from_numpy(np.random.default_rng(17).normal(size=(cfg.T, cfg.h)).astype(np.float32)).cuda().to(x.dtype)
+    first = {k: (v.clone() if v is not None else None) for k, v in layer.backward(x, dy, d_aux=0.3).items()}
+    second = layer.backward(x, dy, d_aux=0.3)
+    torch.cuda.synchronize()
+    for k, v in first.items():
+        if v is None:
+            assert second[k] is None
+            continue
+        a, b = (v.view(torch.int16), second[k].view(torch.int16)) if v.dtype == torch.bfloat16 else (v, second[k])
+        assert torch.equal(a, b), k

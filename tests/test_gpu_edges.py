@@ -256,3 +256,20 @@ def test_router_unsplit_logits_with_bias():
     np.testing.assert_array_equal(r["ids"].cpu().numpy(), ref["ids"])
     assert cases.rel_max(r["logits"].cpu().numpy(), ref["logits"]) <= 1e-5
     assert cases.rel_max(r["gates"].cpu().numpy(), ref["gates"]) <= 1e-5
+
+
+def test_router_split_deterministic():
+    """The E = 256 router (K split into partial logits, multi-block finalize with an arrival counter): two calls
+    give bit-identical logits, gates, P and aux."""
+    import torch
+    from top_routing_dispatch_moe_gb300 import moe
+    cfg = moe_inputs.get_config("deepseek_v3", T=2000, h=2048, F=128, R=1)
+    inp = cases.router_inputs(cfg)
+    x = cases.to_device(inp["x"], cfg)
+    w = cases.to_device(inp["w_r"], cfg)
+    b = torch.from_numpy(np.asarray(inp["bias"], np.float32)).cuda()
+    r1 = {k: v.clone() for k, v in moe.moe_router(x, w, b, cfg.k, cfg.gating, cfg.alpha).items()}
+    r2 = moe.moe_router(x, w, b, cfg.k, cfg.gating, cfg.alpha)
+    torch.cuda.synchronize()
+    for key in ("logits", "ids", "gates", "counts", "f", "P", "aux"):
+        assert torch.equal(r1[key], r2[key]), key

@@ -33,14 +33,17 @@ __global__ void seg_offsets_kernel(const int32_t* __restrict__ kept, int E, int3
 }
 
 // dst [C][ktot]: column k of expert e's segment [seg[e], seg[e+1]) holds row offsets[e] + (k - seg[e]) of
-// src [rows][C] while k - seg[e] < kept[e], zero after it. 64 x 64 tiles through shared memory; a 64-column
-// tile of dst lies in one expert's segment (segments are 64-aligned).
-template <typename T>
+// src [rows][C] while k - seg[e] < kept[e], zero after it. bf16, C % 8 == 0. One 64 (k) x 64 (c) tile per block,
+// 16-byte accesses on both sides: the tile is read as rows of 8 16-byte vectors and written as dst rows of 8
+// 16-byte vectors (a warp stores four whole 128-byte lines). In shared memory element (k, c) sits in row k at
+// 16-byte chunk (c / 8) ^ (k / 8): a store phase's eight vectors of one row land in distinct chunks, and the
+// eight k-rows 8 apart that one column read touches land in distinct banks. A 64-column tile of dst lies in
+// one expert's segment (segments are 64-aligned).
 __global__ void __launch_bounds__(256)
-segment_transpose_kernel(const T* __restrict__ src, int C, const int32_t* __restrict__ offsets,
+segment_transpose_kernel(const __nv_bfloat16* __restrict__ src, int C, const int32_t* __restrict__ offsets,
                          const int32_t* __restrict__ kept, const int32_t* __restrict__ seg, int E, long long ktot,
-                         T* __restrict__ dst) {
-    __shared__ T tile[64][65];
+                         __nv_bfloat16* __restrict__ dst) {
+    __shared__ __align__(16) uint16_t tile[64 * 64];
     const int k0 = blockIdx.x * 64;
     if (k0 >= seg[E]) return;                 // the grid covers the largest possible ktot
     int lo = 0, hi = E - 1;                   // last e with seg[e] <= k0
@@ -50,13 +53,29 @@ segment_transpose_kernel(const T* __restrict__ src, int C, const int32_t* __rest
     }
     const int e = lo, local0 = k0 - seg[e], n = kept[e], r0 = offsets[e];
     const int c0 = blockIdx.y * 64;
-    for (int i = threadIdx.y; i < 64; i += blockDim.y) {
-        const int local = local0 + i, c = c0 + threadIdx.x;
-        tile[i][threadIdx.x] = (local < n && c < C) ? src[(size_t)(r0 + local) * C + c] : T(0.f);
+    const int t = threadIdx.x;
+#pragma unroll
+    for (int p = 0; p < 2; ++p) {             // 64 rows x 8 vectors
+        const int k = (t >> 3) + 32 * p, v = t & 7, c = c0 + 8 * v;
+        uint4 val = make_uint4(0, 0, 0, 0);
+        if (local0 + k < n && c < C) val = __ldcs(reinterpret_cast<const uint4*>(src + (size_t)(r0 + local0 + k) * C + c));
+        *reinterpret_cast<uint4*>(tile + k * 64 + 8 * (v ^ (k >> 3))) = val;
     }
     __syncthreads();
-    for (int c = threadIdx.y; c < 64; c += blockDim.y)
-        if (c0 + c < C) dst[(size_t)(c0 + c) * ktot + k0 + threadIdx.x] = tile[threadIdx.x][c];
+#pragma unroll
+    for (int p = 0; p < 2; ++p) {             // 64 dst rows (c) x 8 vectors of 8 k
+        const int cc = (t >> 3) + 32 * p, w = t & 7;
+        if (c0 + cc >= C) continue;
+        uint32_t o[4];
+#pragma unroll
+        for (int j = 0; j < 8; j += 2) {
+            const int ka = 8 * w + j, kb = ka + 1;
+            const uint32_t a = tile[ka * 64 + 8 * ((cc >> 3) ^ (ka >> 3)) + (cc & 7)];
+            const uint32_t b = tile[kb * 64 + 8 * ((cc >> 3) ^ (kb >> 3)) + (cc & 7)];
+            o[j >> 1] = a | (b << 16);
+        }
+        *reinterpret_cast<uint4*>(dst + (size_t)(c0 + cc) * ktot + k0 + 8 * w) = make_uint4(o[0], o[1], o[2], o[3]);
+    }
 }
 
 // d_gu from the saved pre-activations, over the live rows of the tile schedule: with g, u of feature f at
@@ -186,8 +205,9 @@ extern "C" int moe_expert_weight_grads(const void* buf, const void* act, const v
     MOE_REQUIRE(offsets && kept_counts && dW_gate && dW_up && dW_down &&
                     (rows == 0 || (buf && act && d_gu && d_eout)),
                 MOE_ERR_INVALID_ARG, "moe_expert_weight_grads: null pointer");
-    MOE_REQUIRE(aligned16(dW_gate) && aligned16(dW_up) && aligned16(dW_down) && aligned16(ws), MOE_ERR_INVALID_ARG,
-                "moe_expert_weight_grads: pointers must be 16-byte aligned");
+    MOE_REQUIRE(aligned16(dW_gate) && aligned16(dW_up) && aligned16(dW_down) && aligned16(ws) && aligned16(buf) &&
+                    aligned16(act) && aligned16(d_gu) && aligned16(d_eout),
+                MOE_ERR_INVALID_ARG, "moe_expert_weight_grads: pointers must be 16-byte aligned");
     const GradsWs w = grads_ws_layout(ws, E, h, F, rows);
     MOE_REQUIRE(ws && ws_bytes >= w.bytes, MOE_ERR_WORKSPACE, "moe_expert_weight_grads: workspace %zu < %zu", ws_bytes,
                 w.bytes);
@@ -196,12 +216,11 @@ extern "C" int moe_expert_weight_grads(const void* buf, const void* act, const v
     seg_offsets_kernel<<<1, 32, 0, s>>>(kept_counts, E, w.seg);
     if (int rc = check_launch("seg_offsets_kernel")) return rc;
     using B = __nv_bfloat16;
-    const dim3 block(64, 4);
     const int kt = (int)(w.ktot / 64);
     struct { const void* src; int C; void* dst; } tr[4] = {
         {d_eout, h, w.d_eout_t}, {act, F, w.act_t}, {d_gu, 2 * Fp, w.d_gu_t}, {buf, h, w.buf_t}};
     for (auto& t : tr) {
-        segment_transpose_kernel<B><<<dim3(kt, cdiv(t.C, 64)), block, 0, s>>>(
+        segment_transpose_kernel<<<dim3(kt, cdiv(t.C, 64)), 256, 0, s>>>(
             static_cast<const B*>(t.src), t.C, offsets, kept_counts, w.seg, E, w.ktot, static_cast<B*>(t.dst));
         if (int rc = check_launch("segment_transpose_kernel")) return rc;
     }
