@@ -123,7 +123,7 @@ __device__ __forceinline__ void tma_store_3d(const CUtensorMap* map, uint32_t sr
                  : "memory");
 }
 __device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
-__device__ __forceinline__ void bulk_wait_read_all() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
+__device__ __forceinline__ void bulk_wait_read_but1() { asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory"); }
 __device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
 __device__ __forceinline__ void st_shared_v4(uint32_t addr, float a, float b, float c, float d) {
     asm volatile("st.shared.v4.f32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "f"(a), "f"(b), "f"(c), "f"(d) : "memory");
@@ -396,18 +396,22 @@ __device__ __forceinline__ void store_tile(const Params& p, __nv_bfloat16* out, 
 }
 
 // fp32 epilogue through TMA stores, one call per epilogue warp (all 32 lanes): the warp's 32 accumulator rows,
-// 32 columns at a time, are written into its 4 KB staging buffer `stg` (1024-byte aligned) in the 128-byte
-// swizzled layout of a [32 rows][32 fp32] box (16-byte chunk c of row r at chunk c ^ (r % 8): the eight rows of a
-// store phase hit distinct banks), then one lane stores the box at (column, row0, grp) of `map`, whose extents
-// drop the rows and columns past the output. Whole 128-byte lines reach L2, where per-thread row stores would
-// send one 16-byte partial sector per request. `live`: the warp holds at least one valid row (warp-uniform).
-constexpr int EPI_STG_WARP_BYTES = 32 * 32 * 4;
+// 32 columns at a time, are written into one of its two 4 KB staging boxes at `stg` (1024-byte aligned; the
+// warp's n-th box since the kernel began goes to buffer n % 2, `nbox` counting them, so filling one buffer
+// overlaps the store of the other and a buffer is refilled only after the store two boxes back has read it)
+// in the 128-byte swizzled layout of a [32 rows][32 fp32] box (16-byte chunk c of row r at chunk c ^ (r % 8): the
+// eight rows of a store phase hit distinct banks), then one lane stores the box at (column, row0, grp) of `map`,
+// whose extents drop the rows and columns past the output. Whole 128-byte lines reach L2, where per-thread row
+// stores would send one 16-byte partial sector per request. `live`: the warp holds a valid row (warp-uniform).
+constexpr int EPI_BOX_COLS = 32;
+constexpr int EPI_STG_BOX_BYTES = 32 * EPI_BOX_COLS * 4;
+constexpr int EPI_STG_WARP_BYTES = 2 * EPI_STG_BOX_BYTES;
 constexpr int EPI_STG_BYTES = 4 * EPI_STG_WARP_BYTES;
 template <int BN>
 __device__ __forceinline__ void store_tile_f32_tma(const Params& p, const CUtensorMap* map, uint32_t tbase, int n,
-                                                   int row0, int grp, bool zero, bool live, uint32_t stg) {
+                                                   int row0, int grp, bool zero, bool live, uint32_t stg,
+                                                   uint32_t& nbox) {
     const int lane = threadIdx.x & 31;
-    const uint32_t my_row = stg + (uint32_t)lane * 128u;
 #pragma unroll 1
     for (int j = 0; j < BN / 32; ++j) {
         float v[32];
@@ -423,15 +427,17 @@ __device__ __forceinline__ void store_tile_f32_tma(const Params& p, const CUtens
 #pragma unroll
             for (int i = 0; i < 32; ++i) v[i] += n0 + i < p.n_valid ? __ldg(p.bias + n0 + i) : 0.f;
         }
-        if (lane == 0) bulk_wait_read_all();           // the previous box has left the buffer
+        const uint32_t box = stg + (nbox++ & 1u) * EPI_STG_BOX_BYTES;
+        if (lane == 0) bulk_wait_read_but1();          // the box stored from this buffer last time has left it
         __syncwarp();
+        const uint32_t my_row = box + (uint32_t)lane * 128u;
 #pragma unroll
         for (int c = 0; c < 8; ++c)
             st_shared_v4(my_row + ((uint32_t)(c ^ (lane & 7)) << 4), v[4 * c], v[4 * c + 1], v[4 * c + 2], v[4 * c + 3]);
         asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
         __syncwarp();
         if (lane == 0) {
-            tma_store_3d(map, stg, n0, row0, grp);
+            tma_store_3d(map, box, n0, row0, grp);
             bulk_commit();
         }
     }
@@ -607,6 +613,7 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
         // ---------------------------------------------------------------------- epilogue (warps 2..5)
         const int lane_base = 32 * (warp & 3);
         int iter = 0;
+        uint32_t nbox = 0;                       // fp32 epilogue: store boxes issued by this warp
         for (int w = blockIdx.x; w < total; w += gridDim.x, ++iter) {
             const int a = iter & 1;
             const uint32_t aph = (iter >> 1) & 1;
@@ -629,7 +636,7 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
                     }
                 }
                 store_tile_f32_tma<BN>(p, om, tbase, wk.n, orow, grp, wk.nkb == 0, orow < lim,
-                                       s_out + (uint32_t)(warp & 3) * EPI_STG_WARP_BYTES);
+                                       s_out + (uint32_t)(warp & 3) * EPI_STG_WARP_BYTES, nbox);
             } else {
                 const int row = wk.row0 + lane_base + lane;
                 store_tile<EPI, BN>(p, wk.sh ? p.sh_out : p.out, tbase, row, row < wk.row1, wk.n,
@@ -667,8 +674,8 @@ constexpr int PAIR_STAGE_BYTES = A_BYTES + B_HALF_BYTES;       // 32 KB per CTA 
 constexpr int PAIR_MAX_E = 1024;
 constexpr int PAIR_SMEM_BYTES = 1024 + PAIR_STAGES * PAIR_STAGE_BYTES + 256 + (PAIR_MAX_E + 1) * 4;
 static_assert(PAIR_SMEM_BYTES <= 227 * 1024, "shared memory per CTA");
-// fp32 epilogue: the store boxes after the barriers and the pair prefix, 1024-byte aligned
-constexpr int PAIR_STG_OFF = (256 + (PAIR_MAX_E + 1) * 4 + 1023) / 1024 * 1024;
+// fp32 epilogue (weight-gradient mapping only, which has no pair prefix): the store boxes after the barriers
+constexpr int PAIR_STG_OFF = 1024;
 constexpr int PAIR_SMEM_BYTES_F32 = 1024 + PAIR_STAGES * PAIR_STAGE_BYTES + PAIR_STG_OFF + EPI_STG_BYTES;
 static_assert(PAIR_SMEM_BYTES_F32 <= 227 * 1024, "shared memory per CTA (fp32 epilogue)");
 
@@ -843,7 +850,9 @@ grouped_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_c
         prefetch_tmap(&tmB);
         if (p.sh_rows) { prefetch_tmap(&tmA2); prefetch_tmap(&tmB2); }
     }
-    if (warp == 2 && p.wg_E == 0) {          // pair prefix: pp[e + 1] = sum over e' <= e of ceil(tiles_e' / 2)
+    // pair prefix: pp[e + 1] = sum over e' <= e of ceil(tiles_e' / 2) (routed mapping; the fp32 instantiation runs
+    // the weight-gradient mapping only, and its store boxes occupy this region)
+    if (EPI != EPI_F32 && warp == 2 && p.wg_E == 0) {
         const int32_t* prefix = p.sched + kSchedHeader;
         int carry = 0;
         if (lane == 0) s_pp[0] = 0;
@@ -945,6 +954,7 @@ grouped_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_c
         const int lane_base = 32 * (warp & 3);
         const uint32_t tempty_leader = map_rank(tempty(0), 0);
         int iter = 0;
+        uint32_t nbox = 0;                       // fp32 epilogue: store boxes issued by this warp
         for (int w = cid; w < total; w += NC, ++iter) {
             const int a = iter & 1;
             const uint32_t aph = (iter >> 1) & 1;
@@ -966,7 +976,7 @@ grouped_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_c
                     }
                 }
                 store_tile_f32_tma<BN>(p, om, tbase, wk.n, orow, grp, wk.nkb == 0, orow < lim,
-                                       s_out + (uint32_t)(warp & 3) * EPI_STG_WARP_BYTES);
+                                       s_out + (uint32_t)(warp & 3) * EPI_STG_WARP_BYTES, nbox);
             } else {
                 const int row = wk.row0 + lane_base + lane;
                 store_tile<EPI, BN>(p, wk.sh ? p.sh_out : p.out, tbase, row, row < wk.row1, wk.n,
@@ -1030,7 +1040,7 @@ static int make_map_out(CUtensorMap* m, float* base, long long groups, long long
                 "fp32 output map: base %p ldo %lld cols %lld", (void*)base, ldo, cols);
     cuuint64_t dims[3] = {(cuuint64_t)cols, (cuuint64_t)rows, (cuuint64_t)groups};
     cuuint64_t strides[2] = {(cuuint64_t)ldo * 4, (cuuint64_t)rows * ldo * 4};
-    cuuint32_t box[3] = {32, 32, 1};
+    cuuint32_t box[3] = {(cuuint32_t)EPI_BOX_COLS, 32, 1};
     cuuint32_t estr[3] = {1, 1, 1};
     CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, base, dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
                     CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
@@ -1161,6 +1171,8 @@ static int gemm_pair(const void* a, long long a_rows, const void* b, long long b
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64)
         return set_error(MOE_ERR_CUDA, "grouped_gemm_pair: no usable current device");
     constexpr int smem_bytes = EPI == EPI_F32 ? PAIR_SMEM_BYTES_F32 : PAIR_SMEM_BYTES;
+    MOE_REQUIRE(EPI != EPI_F32 || p.wg_E > 0, MOE_ERR_INVALID_ARG,
+                "grouped_gemm_pair: the fp32 epilogue runs the weight-gradient mapping only");
     if (!clusters[dev]) {
         cudaError_t e = cudaFuncSetAttribute(grouped_gemm_pair_kernel<EPI>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                              smem_bytes);
