@@ -143,9 +143,10 @@ def host_inputs(cfg, seed=0):
 # CPU oracle arm (reference arm and cpu_baseline)
 # ---------------------------------------------------------------------------------------------------------
 
-def oracle_step(cfg, inp, w64, sample_tokens):
+def oracle_step(cfg, inp, w64, sample_tokens, keep=None):
     """One bounded oracle step: router + dispatch over all T tokens, FFN + combine for `sample_tokens`.
-    Returns (seconds for router+dispatch, seconds for the sampled FFN)."""
+    Returns (seconds for router+dispatch, seconds for the sampled FFN); `keep` (a dict) receives the routing,
+    the dispatch and the sampled tokens' y."""
     from oracle import moe_oracle as O
     t0 = time.perf_counter()
     x64 = moe_inputs.to_f64(inp["x"], cfg.dtype)
@@ -153,8 +154,10 @@ def oracle_step(cfg, inp, w64, sample_tokens):
     r = O.route(L, cfg.k, cfg.gating, inp["bias"], cfg.alpha)
     d = O.dispatch(r["ids"], cfg.E, O.capacity(cfg.cf, cfg.k, cfg.T, cfg.E), cfg.R)
     t1 = time.perf_counter()
-    O.moe_layer_tokens(sample_tokens, x64, r, d, lambda e: w64[e], shared=w64.get("shared"))
+    y = O.moe_layer_tokens(sample_tokens, x64, r, d, lambda e: w64[e], shared=w64.get("shared"))
     t2 = time.perf_counter()
+    if keep is not None:
+        keep.update(route=r, dispatch=d, y=y, tokens=sample_tokens)
     return t1 - t0, t2 - t1
 
 
@@ -178,15 +181,43 @@ def blas_threads():
     return os.cpu_count() or 1
 
 
-def oracle_throughput(cfg, inp, w64, steps, n_sample, seed=1):
+def oracle_throughput(cfg, inp, w64, steps, n_sample, seed=1, keep=None):
     """Tokens/s of the oracle: T / (router+dispatch time + sampled FFN time scaled to T tokens)."""
     rng = np.random.default_rng(seed)
     vals = []
     for _ in range(steps):
         toks = np.sort(rng.choice(cfg.T, size=n_sample, replace=False))
-        t_rd, t_ffn = oracle_step(cfg, inp, w64, toks)
+        t_rd, t_ffn = oracle_step(cfg, inp, w64, toks, keep)
         vals.append(cfg.T / (t_rd + t_ffn * cfg.T / n_sample))
     return vals
+
+
+def parity_report(cfg, layer, keep):
+    """The GPU layer's output for the bench input against the oracle run of the cpu_baseline leg: router ids over
+    all T tokens (tokens whose top-(k+1) selection scores lie within 1e-6 of each other are near ties, where
+    the fp32 GPU and the float64 oracle may order experts differently), y on the sampled tokens."""
+    from oracle import moe_oracle as O
+    if cfg.routing != "token" or cfg.payload != "bf16":
+        return {"skipped": f"{cfg.routing} routing / {cfg.payload} payload: see the parity tests"}
+    r = keep["route"]
+    ids = layer.r_out["topk_ids"].cpu().numpy()
+    bad = np.nonzero((ids != r["ids"]).any(axis=1))[0]
+    near = O.near_tie_rows(r["gaps"], 1e-6)
+    toks = keep["tokens"]
+    import torch
+    y = layer.y[torch.as_tensor(np.asarray(toks), device=layer.y.device)].float().cpu().numpy().astype(np.float64)
+    y_ref = keep["y"]
+    ok = ~np.isin(toks, bad)
+    d = y[ok] - y_ref[ok]
+    if cfg.dtype == "bf16":
+        kind, tol = "normwise rel l2", 2e-2
+        err = float(np.linalg.norm(d) / max(np.linalg.norm(y_ref[ok]), 1e-300))
+    else:
+        kind, tol = "max abs / max |ref|", 1e-5
+        err = float(np.max(np.abs(d)) / max(np.max(np.abs(y_ref[ok])), 1e-300))
+    return {"tokens_checked": int(len(toks)), "ids_mismatched_tokens": int(bad.size),
+            "near_tie_tokens": int(near.size), "y_err": err, "y_err_kind": kind, "tolerance": tol,
+            "pass": bool(err <= tol and np.isin(bad, near).all())}
 
 
 def run_reference(args, cfg, C):
@@ -309,6 +340,8 @@ def run_gpu(args, cfg, C):
             stage_ms[b].append(events[a][i].elapsed_time(events[b][i]))
         step_ms.append(events["start"][i].elapsed_time(events[order[-1]][i]))
     ms = max_over_ranks(float(np.mean(step_ms)), world, dev)
+    step_stats = {"median": float(np.median(step_ms)), "p10": float(np.percentile(step_ms, 10)),
+                  "p90": float(np.percentile(step_ms, 90))}
     value = world * cfg.T / (ms * 1e-3)
 
     # ---- end-to-end through the public API: every step copies its batch of tokens in from pinned host
@@ -385,7 +418,8 @@ def run_gpu(args, cfg, C):
     roofline["ridge_flop_per_byte"] = bf16_burst * 1e12 / (hbm * 1e9)
 
     line = {"metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
-            "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
+            "warmup": args.warmup, "ms_per_step": ms, "ms_per_step_stats": step_stats, "higher_is_better": True,
+            "scaling": "weak",
             "vs_baseline": None, "dtype": "bf16" if cfg.dtype == "bf16" else "f32", "data": "synthetic",
             "config": {"workload": _workload_desc(cfg, C), "global_batch": cfg.T * world, "tokens_per_gpu": cfg.T,
                        "parallelism": f"replicas x{world}", "l2": "flushed between steps (512 MiB write)",
@@ -405,11 +439,13 @@ def run_gpu(args, cfg, C):
 
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         w64 = decode_weights(cfg, inp)
-        vals = oracle_throughput(cfg, inp, w64, 1, args.baseline_tokens)
+        keep: dict = {}
+        vals = oracle_throughput(cfg, inp, w64, 1, args.baseline_tokens, keep=keep)
         line["cpu_baseline"] = {"value": vals[0], "unit": "tokens/s", "cores": blas_threads(), "kind": "oracle",
                                 "sample": f"oracle router+dispatch over all {cfg.T} tokens, FFN+combine on "
                                           f"{args.baseline_tokens} random tokens (float64 numpy), FFN cost scaled "
                                           f"to {cfg.T} tokens"}
+        line["parity"] = parity_report(cfg, layer, keep)
     if rank == 0:
         print(json.dumps(line), flush=True)
     if world > 1:
