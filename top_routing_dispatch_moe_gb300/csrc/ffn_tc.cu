@@ -122,7 +122,20 @@ __device__ __forceinline__ void tma_store_3d(const CUtensorMap* map, uint32_t sr
                  ::"l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(z), "r"(src)
                  : "memory");
 }
+__device__ __forceinline__ void tma_store_2d(const CUtensorMap* map, uint32_t src, int x, int y) {
+    asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%1, %2}], [%3];"
+                 ::"l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(src)
+                 : "memory");
+}
 __device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+__device__ __forceinline__ void bulk_wait_read_all() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
+__device__ __forceinline__ void st_shared_v4u(uint32_t addr, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
+    asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a), "r"(b), "r"(c), "r"(d) : "memory");
+}
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
+    const __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+    return *reinterpret_cast<const uint32_t*>(&v);
+}
 __device__ __forceinline__ void bulk_wait_read_but1() { asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory"); }
 __device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
 __device__ __forceinline__ void st_shared_v4(uint32_t addr, float a, float b, float c, float d) {
@@ -303,6 +316,46 @@ __device__ __forceinline__ Work map_item(const Params& p, int E, int w, int nr, 
     const int mt = (p.sh_rows + BM - 1) / BM;
     const int n = idx / mt, row0 = (idx % mt) * BM;
     return Work{0, row0, min(row0 + BM, p.sh_rows), n, 1, 0, KB};
+}
+
+// bf16 epilogue through TMA stores (EPI_BF16), for a warp whose 32 rows are all valid (row0 .. row0 + 31): 64
+// columns at a time in a 4 KB staging box `stg` (1024-byte aligned) in the 128-byte swizzled layout of a
+// [32 rows][64 bf16] box (16-byte chunk c of row r at chunk c ^ (r % 8)), stored by one lane at (column, row0) of
+// `map`, whose column extent drops the columns past n_valid. Whole lines reach L2 instead of one 16-byte partial
+// sector per thread and request. Warps with rows past the tile's valid rows keep the per-thread stores (those
+// rows must not be written: they may be the next expert's). The SwiGLU epilogue keeps the per-thread stores:
+// its act rows are half as wide, and the staged path measured no faster there.
+constexpr int EPI_BF16_BOX_BYTES = 32 * 128;
+template <int BN>
+__device__ __forceinline__ void store_tile_bf16_tma(const Params& p, const CUtensorMap* map, uint32_t tbase, int n,
+                                                    int row0, uint32_t stg) {
+    const int lane = threadIdx.x & 31;
+    const uint32_t my_row = stg + (uint32_t)lane * 128u;
+#pragma unroll 1
+    for (int q = 0; q < BN / 64; ++q) {
+        float v0[32], v1[32];
+        tmem_ld32(tbase + 64 * q, v0);
+        tmem_ld32(tbase + 64 * q + 32, v1);
+        const int c0 = n * BN + 64 * q;
+        if (c0 >= p.n_valid) continue;
+        uint32_t w[32];
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+            w[i] = pack_bf16x2(v0[2 * i], v0[2 * i + 1]);
+            w[16 + i] = pack_bf16x2(v1[2 * i], v1[2 * i + 1]);
+        }
+        if (lane == 0) bulk_wait_read_all();          // the previous box has left the buffer
+        __syncwarp();
+#pragma unroll
+        for (int c = 0; c < 8; ++c)
+            st_shared_v4u(my_row + ((uint32_t)(c ^ (lane & 7)) << 4), w[4 * c], w[4 * c + 1], w[4 * c + 2], w[4 * c + 3]);
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+        __syncwarp();
+        if (lane == 0) {
+            tma_store_2d(map, stg, c0, row0);
+            bulk_commit();
+        }
+    }
 }
 
 // Epilogue of one accumulator: this thread's TMEM lane (one output row) -> SwiGLU of the packed gate/up
@@ -637,6 +690,15 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
                 }
                 store_tile_f32_tma<BN>(p, om, tbase, wk.n, orow, grp, wk.nkb == 0, orow < lim,
                                        s_out + (uint32_t)(warp & 3) * EPI_STG_WARP_BYTES, nbox);
+            } else if constexpr (!A8 && EPI == EPI_BF16) {
+                const int row0w = wk.row0 + lane_base;
+                if (row0w + 31 < wk.row1) {              // all 32 rows valid: TMA stores
+                    store_tile_bf16_tma<BN>(p, wk.sh ? &tmO2 : &tmO, tbase, wk.n, row0w,
+                                            s_out + (uint32_t)(warp & 3) * EPI_BF16_BOX_BYTES);
+                } else {
+                    const int row = row0w + lane;
+                    store_tile<EPI, BN>(p, wk.sh ? p.sh_out : p.out, tbase, row, row < wk.row1, wk.n);
+                }
             } else {
                 const int row = wk.row0 + lane_base + lane;
                 store_tile<EPI, BN>(p, wk.sh ? p.sh_out : p.out, tbase, row, row < wk.row1, wk.n,
@@ -646,9 +708,7 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
             __syncwarp();
             if (lane == 0) mbar_arrive(tempty(a));
         }
-        if constexpr (EPI == EPI_F32) {
-            if (lane == 0) bulk_wait_all();            // every box stored before the CTA exits
-        }
+        if (lane == 0) bulk_wait_all();                // every box stored before the CTA exits
     }
     tc_fence_before();
     __syncthreads();
@@ -677,6 +737,10 @@ static_assert(PAIR_SMEM_BYTES <= 227 * 1024, "shared memory per CTA");
 // fp32 epilogue (weight-gradient mapping only, which has no pair prefix): the store boxes after the barriers
 constexpr int PAIR_STG_OFF = 1024;
 constexpr int PAIR_SMEM_BYTES_F32 = 1024 + PAIR_STAGES * PAIR_STAGE_BYTES + PAIR_STG_OFF + EPI_STG_BYTES;
+// bf16 epilogues (routed mapping): one store box per epilogue warp after the barriers and the pair prefix
+constexpr int PAIR_BOX_OFF = (256 + (PAIR_MAX_E + 1) * 4 + 1023) / 1024 * 1024;
+constexpr int PAIR_SMEM_BYTES_BF16 = 1024 + PAIR_STAGES * PAIR_STAGE_BYTES + PAIR_BOX_OFF + 4 * EPI_BF16_BOX_BYTES;
+static_assert(PAIR_SMEM_BYTES_BF16 <= 227 * 1024, "shared memory per CTA (bf16 store boxes)");
 static_assert(PAIR_SMEM_BYTES_F32 <= 227 * 1024, "shared memory per CTA (fp32 epilogue)");
 
 __device__ __forceinline__ uint32_t cluster_rank() {
@@ -834,6 +898,7 @@ grouped_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_c
     volatile int* peer_rounds = reinterpret_cast<volatile int*>(tmem_slot + 2);   // rank 1's copy rounds, in rank 0
     int* s_pp = reinterpret_cast<int*>(smem + STAGES * PAIR_STAGE_BYTES + 256);
     const uint32_t s_out = sbase + STAGES * PAIR_STAGE_BYTES + PAIR_STG_OFF;   // fp32 epilogue store boxes
+    const uint32_t s_box = sbase + STAGES * PAIR_STAGE_BYTES + PAIR_BOX_OFF;   // bf16 epilogue store boxes
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const uint32_t rank = cluster_rank();
@@ -977,6 +1042,15 @@ grouped_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_c
                 }
                 store_tile_f32_tma<BN>(p, om, tbase, wk.n, orow, grp, wk.nkb == 0, orow < lim,
                                        s_out + (uint32_t)(warp & 3) * EPI_STG_WARP_BYTES, nbox);
+            } else if constexpr (EPI == EPI_BF16) {
+                const int row0w = wk.row0 + lane_base;
+                if (row0w + 31 < wk.row1) {              // all 32 rows valid: TMA stores
+                    store_tile_bf16_tma<BN>(p, wk.sh ? &tmO2 : &tmO, tbase, wk.n, row0w,
+                                            s_box + (uint32_t)(warp & 3) * EPI_BF16_BOX_BYTES);
+                } else {
+                    const int row = row0w + lane;
+                    store_tile<EPI, BN>(p, wk.sh ? p.sh_out : p.out, tbase, row, row < wk.row1, wk.n);
+                }
             } else {
                 const int row = wk.row0 + lane_base + lane;
                 store_tile<EPI, BN>(p, wk.sh ? p.sh_out : p.out, tbase, row, row < wk.row1, wk.n,
@@ -986,9 +1060,7 @@ grouped_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_c
             __syncwarp();
             if (lane == 0) mbar_arrive_cluster(tempty_leader + 8u * a);
         }
-        if constexpr (EPI == EPI_F32) {
-            if (lane == 0) bulk_wait_all();            // every box stored before the CTA exits
-        }
+        if (lane == 0) bulk_wait_all();                // every box stored before the CTA exits
     }
     cluster_sync_all();                      // every role has left its loop; rank 1's round count is in rank 0
     if (warp == 0 && lane == 0 && leader) {
@@ -1048,8 +1120,27 @@ static int make_map_out(CUtensorMap* m, float* base, long long groups, long long
     return MOE_OK;
 }
 
+// bf16 output [rows][cols] with row pitch ldo elements, as [32 rows][64 columns] boxes in the 128-byte swizzled
+// layout of the epilogue's staging box.
+static int make_map_bf16_out(CUtensorMap* m, void* base, long long rows, long long cols, long long ldo) {
+    auto fn = encode_fn();
+    MOE_REQUIRE(fn, MOE_ERR_CUDA, "cuTensorMapEncodeTiled unavailable from the driver");
+    MOE_REQUIRE(base && aligned16(base) && ldo % 8 == 0 && cols <= ldo && rows >= 1, MOE_ERR_INVALID_ARG,
+                "bf16 output map: base %p ldo %lld cols %lld rows %lld", base, ldo, cols, rows);
+    cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
+    cuuint64_t strides[1] = {(cuuint64_t)ldo * 2};
+    cuuint32_t box[2] = {64, 32};
+    cuuint32_t estr[2] = {1, 1};
+    CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, base, dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                    CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    MOE_REQUIRE(r == CUDA_SUCCESS, MOE_ERR_CUDA, "cuTensorMapEncodeTiled (bf16 output) failed (%d)", (int)r);
+    return MOE_OK;
+}
+
 // Output maps of an fp32 launch: the weight-gradient groups (experts or split-K parts; the gate and up halves
-// de-interleaved into two maps) or the dense [a_rows] x n_valid logits. Other epilogues take `ma` as a stand-in.
+// de-interleaved into two maps) or the dense [a_rows] x n_valid logits; of a plain bf16 launch: the routed
+// output [a_rows] and the shared expert's [sh_rows], both n_valid wide with pitch ldo. Other epilogues (and
+// absent outputs) take `ma` as a stand-in.
 template <int EPI>
 static int make_out_maps(const Params& p, long long a_rows, const CUtensorMap& ma, CUtensorMap* o1, CUtensorMap* o2) {
     *o1 = ma;
@@ -1065,6 +1156,12 @@ static int make_out_maps(const Params& p, long long a_rows, const CUtensorMap& m
             if (int rc = make_map_out(o1, p.out_f32, 1, a_rows, p.n_valid, p.ldo)) return rc;
         }
         *o2 = *o1;
+    }
+    if constexpr (EPI == EPI_BF16) {
+        if (p.out && a_rows > 0)
+            if (int rc = make_map_bf16_out(o1, p.out, a_rows, p.n_valid, p.ldo)) return rc;
+        if (p.sh_out && p.sh_rows > 0)
+            if (int rc = make_map_bf16_out(o2, p.sh_out, p.sh_rows, p.n_valid, p.ldo)) return rc;
     }
     return MOE_OK;
 }
@@ -1134,7 +1231,9 @@ static int gemm(const void* a, long long a_rows, const void* b, long long b_rows
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64)
         return set_error(MOE_ERR_CUDA, "grouped_gemm: no usable current device");
+    constexpr bool kBox16 = EPI == EPI_BF16;
     constexpr int smem_bytes = EPI == EPI_F32 ? 1024 + CF::STAGES * CF::STAGE_BYTES + 1024 + EPI_STG_BYTES
+                               : kBox16       ? 1024 + CF::STAGES * CF::STAGE_BYTES + 1024 + 4 * EPI_BF16_BOX_BYTES
                                               : CF::SMEM_BYTES;
     static_assert(smem_bytes <= 227 * 1024, "shared memory per CTA");
     if (!attr_set[dev]) {
@@ -1143,6 +1242,7 @@ static int gemm(const void* a, long long a_rows, const void* b, long long b_rows
         if (e != cudaSuccess) return set_error(MOE_ERR_CUDA, "grouped_gemm smem attribute: %s", cudaGetErrorString(e));
         attr_set[dev] = true;
     }
+    const long long routed_rows = a_rows;
     if (a_rows == 0) { a = sh.a; a_rows = p.sh_rows; b = sh.b; b_rows_total = sh.b_rows; }   // no routed items
     CUtensorMap ma, mb, ma2, mb2;
     if (int rc = make_map(&ma, a, a_rows, p.a_cols ? p.a_cols : p.K, BM)) return rc;
@@ -1154,7 +1254,7 @@ static int gemm(const void* a, long long a_rows, const void* b, long long b_rows
         if (int rc = make_map(&mb2, sh.b, sh.b_rows, p.K, CF::BN)) return rc;
     }
     CUtensorMap mo, mo2;
-    if (int rc = make_out_maps<EPI>(p, a_rows, ma, &mo, &mo2)) return rc;
+    if (int rc = make_out_maps<EPI>(p, routed_rows, ma, &mo, &mo2)) return rc;
     grouped_gemm_kernel<EPI, CF><<<num_sms(), NUM_THREADS, smem_bytes, s>>>(ma, mb, ma2, mb2, mo, mo2, p);
     return check_launch(EPI == EPI_SWIGLU ? "grouped_gemm_kernel<up_gate>"
                         : EPI == EPI_SWIGLU_SAVE ? "grouped_gemm_kernel<up_gate, save>"
@@ -1170,7 +1270,8 @@ static int gemm_pair(const void* a, long long a_rows, const void* b, long long b
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64)
         return set_error(MOE_ERR_CUDA, "grouped_gemm_pair: no usable current device");
-    constexpr int smem_bytes = EPI == EPI_F32 ? PAIR_SMEM_BYTES_F32 : PAIR_SMEM_BYTES;
+    constexpr bool kBox16 = EPI == EPI_BF16;
+    constexpr int smem_bytes = EPI == EPI_F32 ? PAIR_SMEM_BYTES_F32 : kBox16 ? PAIR_SMEM_BYTES_BF16 : PAIR_SMEM_BYTES;
     MOE_REQUIRE(EPI != EPI_F32 || p.wg_E > 0, MOE_ERR_INVALID_ARG,
                 "grouped_gemm_pair: the fp32 epilogue runs the weight-gradient mapping only");
     if (!clusters[dev]) {
@@ -1187,6 +1288,7 @@ static int gemm_pair(const void* a, long long a_rows, const void* b, long long b
             return set_error(MOE_ERR_CUDA, "grouped_gemm_pair: no resident cluster of two CTAs (%s)", cudaGetErrorString(e));
         clusters[dev] = std::min(n, num_sms() / 2);
     }
+    const long long routed_rows = a_rows;
     if (a_rows == 0) { a = sh.a; a_rows = p.sh_rows; b = sh.b; b_rows_total = sh.b_rows; }   // no routed items
     CUtensorMap ma, mb, ma2, mb2;
     if (int rc = make_map(&ma, a, a_rows, p.K, BM)) return rc;
@@ -1198,7 +1300,7 @@ static int gemm_pair(const void* a, long long a_rows, const void* b, long long b
         if (int rc = make_map(&mb2, sh.b, sh.b_rows, p.K, 128)) return rc;
     }
     CUtensorMap mo, mo2;
-    if (int rc = make_out_maps<EPI>(p, a_rows, ma, &mo, &mo2)) return rc;
+    if (int rc = make_out_maps<EPI>(p, routed_rows, ma, &mo, &mo2)) return rc;
     grouped_gemm_pair_kernel<EPI><<<2 * clusters[dev], NUM_THREADS, smem_bytes, s>>>(ma, mb, ma2, mb2, mo, mo2, p);
     return check_launch(EPI == EPI_SWIGLU ? "grouped_gemm_pair_kernel<up_gate>"
                         : EPI == EPI_SWIGLU_SAVE ? "grouped_gemm_pair_kernel<up_gate, save>"
