@@ -129,7 +129,8 @@ def test_expert_backward(sizes, saved):
     """Expert FFN backward per expert against the oracle's SwiGLU backward on the same bf16 operands: d_act,
     the packed d_g / d_u, d_buf and the fp32 weight gradients (zero for an expert without rows). F = 320 leaves a
     zero-padded part of the last 128-column block. The second size list has rows >= 512 E, so the dgrad GEMMs run
-    on the 2-SM kernel; the weight gradients always run on the one-SM kernel. saved: the forward keeps g and u
+    on the 2-SM kernel; the weight gradients (M = 2 Fp = 768 and h = 256 output rows per expert) run on the
+    2-SM kernel with its fp32 TMA-store epilogue. saved: the forward keeps g and u
     (moe_expert_up_gate_save: act bit-identical to moe_expert_up_gate, g and u within bf16 rounding of the
     float64 products) and the backward starts from them (moe_expert_up_gate_backward_saved)."""
     import torch
