@@ -84,3 +84,36 @@ def test_host_checks_reject_before_any_cuda_call(lib):
     assert raw.moe_combine(ok, ok, ok, n, 4, 16, 2, 5, ok, n) == lib.MOE_ERR_UNSUPPORTED
     # pack: F % 8
     assert raw.moe_pack_expert_weights(ok, ok, ok, 2, 16, 12, 1, ok, n) == lib.MOE_ERR_INVALID_ARG
+
+
+def test_host_checks_of_the_backward_and_fp8_entry_points(lib):
+    raw = lib.raw_lib()
+    P = ctypes.c_void_p
+    n = None
+    ok, bad = P(0x1000), P(0x1003)
+    # dequantisation pass: h % 128, alignment, nulls; zero rows is a no-op
+    assert raw.moe_dequant_fp8(ok, ok, 4, 100, ok, n) == lib.MOE_ERR_INVALID_ARG
+    assert raw.moe_dequant_fp8(bad, ok, 4, 128, ok, n) == lib.MOE_ERR_INVALID_ARG
+    assert raw.moe_dequant_fp8(n, n, 4, 128, n, n) == lib.MOE_ERR_INVALID_ARG
+    assert raw.moe_dequant_fp8(n, n, 0, 128, n, n) == lib.MOE_OK
+    # the pre-activation-saving forward and the backward from it: bf16 only, pointers checked
+    assert raw.moe_expert_up_gate_save(ok, ok, ok, 4, 16, 16, 8, n, 0, n, n, n, lib.MOE_F32, ok, ok,
+                                       n) == lib.MOE_ERR_UNSUPPORTED
+    assert raw.moe_expert_up_gate_save(ok, ok, ok, 4, 16, 16, 8, n, 0, n, n, n, lib.MOE_BF16, ok, n,
+                                       n) == lib.MOE_ERR_INVALID_ARG
+    assert raw.moe_expert_up_gate_backward_saved(ok, ok, ok, ok, 4, 16, 16, 8, lib.MOE_F32, ok, ok,
+                                                 n) == lib.MOE_ERR_UNSUPPORTED
+    assert raw.moe_expert_up_gate_backward_saved(n, ok, ok, ok, 4, 16, 16, 8, lib.MOE_BF16, ok, ok,
+                                                 n) == lib.MOE_ERR_INVALID_ARG
+    # weight gradients: every operand 16-byte aligned (vector transposes), checked before any launch
+    ws = lib.raw_lib().moe_expert_weight_grads_workspace_size(4, 16, 16, 8, lib.MOE_BF16)
+    assert ws > 0
+    assert raw.moe_expert_weight_grads(bad, ok, ok, ok, ok, ok, 4, 16, 16, 8, lib.MOE_BF16, ok, ok, ok, ok, ws,
+                                       n) == lib.MOE_ERR_INVALID_ARG
+    # dispatch backward: the tensor-core path's workspace holds the d_logits pieces and the fp32 router term
+    T, h, E = 1000, 1024, 256
+    need = lib.raw_lib().moe_dispatch_backward_workspace_size(T, h, E, lib.MOE_BF16)
+    assert need >= T * 3 * E * 2 + T * h * 4
+    assert lib.raw_lib().moe_dispatch_backward_workspace_size(T, h, 8, lib.MOE_BF16) < need
+    # router weight gradient: room for either path
+    assert lib.raw_lib().moe_router_weight_grad_workspace_size(T, h, E) >= h * 1024 * 2 + E * 3 * 1024 * 2
