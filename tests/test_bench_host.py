@@ -1,0 +1,48 @@
+"""Host logic of bench.py on the CPU: the parity report of the cpu_baseline leg (its verdict on an exact
+output, on a perturbed one and on an index mismatch outside the near ties) and the roofline's choice of bound."""
+import types
+
+import numpy as np
+import pytest
+import torch
+
+import bench
+import moe_inputs
+from oracle import moe_oracle as O
+
+
+@pytest.fixture(scope="module")
+def oracle_run():
+    cfg = moe_inputs.get_config("tiny_fp32")
+    inp = bench.host_inputs(cfg)
+    w64 = bench.decode_weights(cfg, inp)
+    keep = {}
+    bench.oracle_step(cfg, inp, w64, np.arange(0, cfg.T, 7), keep)
+    return cfg, keep
+
+
+def _layer(cfg, keep, y_rows):
+    y = torch.zeros((cfg.T, cfg.h), dtype=torch.float32)
+    y[torch.as_tensor(keep["tokens"])] = torch.as_tensor(y_rows, dtype=torch.float32)
+    return types.SimpleNamespace(y=y, r_out={"topk_ids": torch.as_tensor(keep["route"]["ids"].astype(np.int32))})
+
+
+def test_parity_report_verdicts(oracle_run):
+    cfg, keep = oracle_run
+    exact = bench.parity_report(cfg, _layer(cfg, keep, keep["y"]), keep)
+    assert exact["pass"] and exact["ids_mismatched_tokens"] == 0 and exact["y_err"] < 1e-6
+    assert exact["tokens_checked"] == len(keep["tokens"])
+    off = bench.parity_report(cfg, _layer(cfg, keep, keep["y"] * 1.01), keep)
+    assert not off["pass"] and off["y_err"] > 1e-3
+    lay = _layer(cfg, keep, keep["y"])
+    ids = lay.r_out["topk_ids"].clone()
+    t = int(np.setdiff1d(np.arange(cfg.T), O.near_tie_rows(keep["route"]["gaps"], 1e-6))[0])
+    ids[t] = ids[t].flip(0)                 # a swapped pair of ids on a token that is not a near tie
+    lay.r_out["topk_ids"] = ids
+    swapped = bench.parity_report(cfg, lay, keep)
+    assert swapped["ids_mismatched_tokens"] == 1 and not swapped["pass"]
+
+
+def test_parity_report_skips_other_routings():
+    cfg = moe_inputs.get_config("page3_expert_choice")
+    assert "skipped" in bench.parity_report(cfg, None, {})
