@@ -41,3 +41,36 @@ def test_gemm_wait_timeout_reported_and_recoverable(rows):
     g = x.float() @ wg[0].float().T
     ref = g * torch.sigmoid(g) * (x.float() @ wu[0].float().T)
     assert ((act.float() - ref).norm() / ref.norm()).item() < 1e-2
+
+
+def test_dispatch_copy_wait_timeout_reported_and_recoverable():
+    """The fused dispatch's row copy (bulk-copy unit, one issuing thread per block) waits on an mbarrier for
+    each row piece; with the limit at one poll it gives up, waits for the loads already in flight, latches
+    MOE_ERR_TIMEOUT and returns; the next call at the default limit copies every kept row exactly."""
+    import torch
+    from top_routing_dispatch_moe_gb300 import moe
+    torch.manual_seed(5)
+    # one 32 KB token row per block (two 16 KB pieces): each block polls its first piece right after issuing
+    # the two loads, long before a 16 KB copy can have landed
+    T, h, E, k, C = 152, 16384, 8, 2, 48
+    x = torch.randn(T, h, device="cuda").to(torch.bfloat16)
+    ids = torch.stack([torch.randperm(E, device="cuda")[:k] for _ in range(T)]).to(torch.int32)
+    torch.cuda.synchronize()
+    assert moe.moe_check_device_error() == moe.MOE_OK
+    try:
+        moe.moe_set_wait_limit(1)
+        moe.moe_dispatch(x, ids, E, C, 1)
+        rc = moe.moe_check_device_error()
+        msg = moe.moe_last_error_string()
+    finally:
+        moe.moe_set_wait_limit(0)
+    assert rc == moe.MOE_ERR_TIMEOUT, (rc, msg)
+    assert "site 0x110" in msg
+    o = moe.moe_dispatch(x, ids, E, C, 1)
+    torch.cuda.synchronize()
+    assert moe.moe_check_device_error() == moe.MOE_OK
+    dest = o["dest_row"].long()
+    kept = dest >= 0
+    rows = dest[kept]
+    toks = torch.arange(T, device="cuda")[:, None].expand(T, k)[kept]
+    assert torch.equal(o["buf"][rows].view(torch.int16), x[toks].view(torch.int16))

@@ -12,7 +12,9 @@
 // the rank layout and the tile schedule; kernel 3 ranks each assignment inside its chunk (warp match_any
 // + per-warp prefix over the chunk's 32 warps) and writes the indices; kernel 4 copies each token row to
 // its (at most k) destination rows with 16-byte loads and stores, reading x once. In capacity mode a
-// fifth kernel zero-fills the pad rows and marks them -1.
+// fifth kernel zero-fills the pad rows and marks them -1. For small count tables one launch after the
+// count does the scan, the ranking, the copy and the pad fill (dispatch_fused_kernel); its bf16 / fp32 row
+// copy goes through the bulk-copy unit (ring_copy_rows).
 #include <algorithm>
 #include <mutex>
 #include <cuda_fp8.h>
@@ -21,6 +23,85 @@
 namespace moe {
 
 constexpr int kChunkA = 1024;          // assignments per chunk (one thread each)
+
+// Bulk-copy (TMA) unit, untiled: a row piece global -> shared completing on an mbarrier, shared -> global in
+// bulk groups of the issuing thread. Addresses and sizes are multiples of 16 bytes.
+__device__ __forceinline__ uint32_t shared_u32(const void* p) { return (uint32_t)__cvta_generic_to_shared(p); }
+__device__ __forceinline__ void ring_load(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes) : "memory");
+    asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
+                 ::"r"(dst), "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes), "r"(bar) : "memory");
+}
+__device__ __forceinline__ void ring_store(void* dst, uint32_t src, uint32_t bytes) {
+    asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;"
+                 ::"l"(reinterpret_cast<uint64_t>(dst)), "r"(src), "r"(bytes) : "memory");
+}
+// Bounded wait for a stage's load: at most `limit` non-blocking polls 32 ns apart; false when they ran out.
+constexpr long long kRingDrainLimit = 1LL << 24;
+__device__ __forceinline__ bool ring_wait(uint32_t bar, uint32_t parity, long long limit) {
+    for (long long i = 0; i < limit; ++i) {
+        uint32_t ok;
+        asm volatile("{\n\t.reg .pred p;\n\tmbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+                     "selp.u32 %0, 1, 0, p;\n\t}" : "=r"(ok) : "r"(bar), "r"(parity) : "memory");
+        if (ok) return true;
+        __nanosleep(32);
+    }
+    return false;
+}
+
+// One thread copies ntok consecutive rows of row_bytes (a multiple of 16) from src to the destination rows
+// dest[tl * k + j] >= 0 of dst, piece by piece (pieces of at most SB bytes) through a ring of NS >= 2 shared
+// stages: every load in flight at once up to the ring's size, each piece stored to its k destinations as one
+// bulk group, a stage refilled once the group stored out of it has been read. A load that does not arrive
+// within `limit` polls latches a timeout; the loads still in flight are then waited for (up to kRingDrainLimit
+// polls each, whatever `limit` is, so that none lands in shared memory after the block has exited) and the
+// copy stops.
+__device__ void ring_copy_rows(const char* __restrict__ src, uint32_t row_bytes, int ntok, int k,
+                               const int* __restrict__ dest, char* __restrict__ dst, uint32_t ring, uint32_t bars,
+                               int NS, uint32_t SB, long long limit, unsigned* err) {
+    for (int st = 0; st < NS; ++st)
+        asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(bars + 8u * st) : "memory");
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    const int n = ntok * (int)((row_bytes + SB - 1) / SB);      // pieces, in token order
+    // load cursor: next piece's token, byte offset in the row and stage; pieces are loaded in order
+    int lt = 0, lst = 0, loaded = 0;
+    uint32_t loff = 0;
+    auto load_next = [&]() {
+        ring_load(ring + (uint32_t)lst * SB, src + (size_t)lt * row_bytes + loff, min(SB, row_bytes - loff),
+                  bars + 8u * lst);
+        loff += SB;
+        if (loff >= row_bytes) { loff = 0; ++lt; }
+        if (++lst == NS) lst = 0;
+        ++loaded;
+    };
+    while (loaded < min(NS, n)) load_next();
+    // store cursor: piece i (token ct, offset coff) sits in stage cst, its load completing phase parity par
+    int ct = 0, cst = 0;
+    uint32_t coff = 0, par = 0;
+    for (int i = 0; i < n; ++i) {
+        if (!ring_wait(bars + 8u * cst, par, limit)) {
+            latch_device_error(err, kDevErrTimeout, 0x110u);
+            for (int q = i; q < loaded; ++q)
+                ring_wait(bars + 8u * (q % NS), (uint32_t)(q / NS) & 1u, kRingDrainLimit);
+            break;
+        }
+        const uint32_t bytes = min(SB, row_bytes - coff);
+        const uint32_t from = ring + (uint32_t)cst * SB;
+        for (int j = 0; j < k; ++j) {
+            const int d = dest[ct * k + j];
+            if (d >= 0) ring_store(dst + (size_t)d * row_bytes + coff, from, bytes);
+        }
+        asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+        if (i >= 1 && loaded < n) {           // refill the stage of piece i - 1 (loaded == i - 1 + NS)
+            asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory");
+            load_next();
+        }
+        coff += SB;
+        if (coff >= row_bytes) { coff = 0; ++ct; }
+        if (++cst == NS) { cst = 0; par ^= 1u; }
+    }
+    asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
+}
 
 // Chunk c covers tokens [c * tpc, (c + 1) * tpc), i.e. assignments [c * tpc * k, ...): tpc * k <= kChunkA.
 __global__ void __launch_bounds__(kChunkA)
@@ -232,6 +313,12 @@ __host__ __device__ constexpr int fused_tp(int E) { return fused_off(E) + E + 1;
 __host__ __device__ constexpr int fused_dest(int E) { return fused_tp(E) + E + 1; }
 __host__ __device__ constexpr int fused_red(int E) { return fused_dest(E) + kChunkA; }          // 2 x kChunkA
 __host__ __device__ constexpr int fused_smem_ints(int E) { return fused_red(E) + 2 * kChunkA; }
+// Then (bf16 / fp32 payload) the ring of the bulk row copy: kRingMaxStages mbarriers, and the stages from the
+// next 128-byte boundary of the shared window (the launch allocates 128 bytes of slack for that).
+constexpr int kRingMaxStages = 32;
+constexpr uint32_t kRingStageCap = 16384;     // bytes per stage: a row of up to 16 KB is one piece
+__host__ __device__ constexpr int fused_bars_byte(int E) { return (fused_smem_ints(E) * 4 + 7) / 8 * 8; }
+__host__ __device__ constexpr int fused_ring_byte(int E) { return fused_bars_byte(E) + 8 * kRingMaxStages; }
 
 // Tokens per chunk of the fused path (0: the count table would be too large; use the three-launch path).
 // At most max_chunks chunks (the launch uses one chunk per SM so that every block is resident at once; the
@@ -253,8 +340,9 @@ dispatch_fused_kernel(const T* __restrict__ x, const int32_t* __restrict__ ids, 
                       int32_t* __restrict__ offsets, int32_t* __restrict__ kept_counts,
                       int32_t* __restrict__ rank_counts, int32_t* __restrict__ rank_offsets,
                       int32_t* __restrict__ sched, int32_t* __restrict__ dest_row, uint8_t* __restrict__ drop_mask,
-                      int32_t* __restrict__ src_token, int32_t* __restrict__ src_slot, uint8_t* __restrict__ buf8 = nullptr,
-                      float* __restrict__ scales = nullptr) {
+                      int32_t* __restrict__ src_token, int32_t* __restrict__ src_slot, uint8_t* __restrict__ buf8,
+                      float* __restrict__ scales, int ring_stages, uint32_t stage_bytes, long long wait_limit,
+                      unsigned* __restrict__ err) {
     extern __shared__ int sm[];
     int* s_wc = sm + fused_wc(E);
     int* s_base = sm + fused_base(E);
@@ -310,35 +398,27 @@ dispatch_fused_kernel(const T* __restrict__ x, const int32_t* __restrict__ ids, 
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const int t0 = blockIdx.x * tpc;
     const int ntok = min(tpc, T_ - t0);
-    for (int tl = warp; tl < ntok; tl += kChunkA / 32) {
-        if constexpr (FP8) {
+    if constexpr (FP8) {
+        for (int tl = warp; tl < ntok; tl += kChunkA / 32) {
             int dj[16];
 #pragma unroll
             for (int j = 0; j < 16; ++j) dj[j] = j < k ? s_dest[tl * k + j] : -1;
             fp8_copy_token(x + (size_t)(t0 + tl) * h, dj, k, h, buf8, scales, lane);
-            continue;
         }
-        const T* src = x + (size_t)(t0 + tl) * h;
-        constexpr int U = 4;
-        for (int d0 = lane * V; d0 < h; d0 += U * 32 * V) {
-            Vec16<T> v[U];
-#pragma unroll
-            for (int u = 0; u < U; ++u)
-                if (d0 + u * 32 * V < h) v[u] = ld16_stream(src + d0 + u * 32 * V);
-            for (int j = 0; j < k; ++j) {
-                const int dj = s_dest[tl * k + j];
-                if (dj >= 0) {
-#pragma unroll
-                    for (int u = 0; u < U; ++u)
-                        if (d0 + u * 32 * V < h) st16(buf + (size_t)dj * h + d0 + u * 32 * V, v[u]);
-                }
-            }
-        }
+    } else if (threadIdx.x == 0 && ntok > 0) {
+        // the rows move through the bulk-copy unit, issued by this one thread; the other warps fill pad rows
+        const uint32_t bars = shared_u32(sm) + (uint32_t)fused_bars_byte(E);
+        const uint32_t ring = (shared_u32(sm) + (uint32_t)fused_ring_byte(E) + 127u) & ~127u;
+        ring_copy_rows(reinterpret_cast<const char*>(x + (size_t)t0 * h), (uint32_t)(h * sizeof(T)), ntok, k, s_dest,
+                       reinterpret_cast<char*>(buf), ring, bars, ring_stages, stage_bytes, wait_limit, err);
     }
     if (C > 0) {
-        // Pad rows, numbered in expert order, go round-robin to all warps of the grid: pad row number q
-        // (q = pads of earlier experts + p) belongs to warp q mod W.
-        const long long W = (long long)gridDim.x * (kChunkA / 32), g = (long long)blockIdx.x * (kChunkA / 32) + warp;
+        // Pad rows, numbered in expert order, go round-robin to the grid's fill warps (all warps with the FP8
+        // payload, warps 1-31 of each block otherwise): pad row number q (q = pads of earlier experts + p)
+        // belongs to fill warp q mod W.
+        constexpr int FW = FP8 ? kChunkA / 32 : kChunkA / 32 - 1;
+        if (!FP8 && warp == 0) return;
+        const long long W = (long long)gridDim.x * FW, g = (long long)blockIdx.x * FW + (FP8 ? warp : warp - 1);
         long long run = 0;
         for (int ee = 0; ee < E; ++ee) {
             const int npad = C - s_kept[ee];
@@ -451,6 +531,19 @@ __global__ void dense_sched_kernel(int rows, int32_t* sched) {
 }
 
 static int num_chunks(int T, int k) { return T <= 0 ? 0 : cdiv(T, kChunkA / k); }
+
+// Ring of the fused kernel's bulk row copy: stages of min(row bytes, 16 KB), as many as fit (at most 32)
+// beside the kernel's tables in 227 KB of shared memory less 1 KB for its static variables and margin.
+struct RingPlan { int stages; uint32_t stage_bytes; size_t smem; };
+static RingPlan ring_plan(int E, size_t row_bytes) {
+    constexpr size_t kSmemMax = 227 * 1024 - 1024;
+    RingPlan r;
+    r.stage_bytes = (uint32_t)std::min<size_t>(row_bytes, kRingStageCap);
+    const size_t base = (size_t)fused_ring_byte(E) + 128;
+    r.stages = (int)std::min<size_t>(kRingMaxStages, base < kSmemMax ? (kSmemMax - base) / r.stage_bytes : 0);
+    r.smem = base + (size_t)r.stages * r.stage_bytes;
+    return r;
+}
 static int num_fused_chunks(int T, int E, int k) {
     const int tpc = fused_tokens_per_chunk(T, E, k, kFusedMaxChunks);
     return tpc ? cdiv(T, tpc) : 0;
@@ -509,7 +602,10 @@ extern "C" int moe_dispatch(const void* x, const int32_t* topk_ids, int T, int h
         const int nch = cdiv(T, tpc_f);
         dispatch_count_kernel<<<nch, kChunkA, E * sizeof(int), s>>>(topk_ids, T, E, k, tpc_f, chunk, err);
         if (int rc = check_launch("dispatch_count_kernel")) return rc;
-        const size_t smem = (size_t)fused_smem_ints(E) * sizeof(int);
+        const RingPlan rp = ring_plan(E, (size_t)h * (dtype == MOE_BF16 ? 2 : 4));
+        MOE_REQUIRE(rp.stages >= 2, MOE_ERR_INVALID_ARG, "moe_dispatch: no room for the copy ring (E=%d, h=%d)", E, h);
+        const size_t smem = rp.smem;
+        const long long wl = wait_limit();
         cudaError_t le;
         if (dtype == MOE_BF16) {
             cudaFuncSetAttribute(dispatch_fused_kernel<__nv_bfloat16>, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -517,13 +613,14 @@ extern "C" int moe_dispatch(const void* x, const int32_t* topk_ids, int T, int h
             le = launch_pdl(dispatch_fused_kernel<__nv_bfloat16>, dim3(nch), dim3(kChunkA), smem, s,
                 static_cast<const __nv_bfloat16*>(x), topk_ids, T, h, E, k, tpc_f, capacity, num_ranks,
                 (const int32_t*)chunk, nch, static_cast<__nv_bfloat16*>(buf), offsets, kept_counts, rank_counts,
-                rank_offsets, tile_sched, dest_row, drop_mask, src_token, src_slot, (uint8_t*)nullptr, (float*)nullptr);
+                rank_offsets, tile_sched, dest_row, drop_mask, src_token, src_slot, (uint8_t*)nullptr, (float*)nullptr,
+                rp.stages, rp.stage_bytes, wl, err);
         } else {
             cudaFuncSetAttribute(dispatch_fused_kernel<float>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
             le = launch_pdl(dispatch_fused_kernel<float>, dim3(nch), dim3(kChunkA), smem, s, static_cast<const float*>(x),
                 topk_ids, T, h, E, k, tpc_f, capacity, num_ranks, (const int32_t*)chunk, nch, static_cast<float*>(buf),
                 offsets, kept_counts, rank_counts, rank_offsets, tile_sched, dest_row, drop_mask, src_token, src_slot,
-                (uint8_t*)nullptr, (float*)nullptr);
+                (uint8_t*)nullptr, (float*)nullptr, rp.stages, rp.stage_bytes, wl, err);
         }
         return check_launch(le, "dispatch_fused_kernel");
     }
@@ -713,7 +810,7 @@ extern "C" int moe_dispatch_fp8(const void* x, const int32_t* topk_ids, int T, i
         const cudaError_t le = launch_pdl(dispatch_fused_kernel<__nv_bfloat16, true>, dim3(nchf), dim3(kChunkA), smem, s,
             static_cast<const __nv_bfloat16*>(x), topk_ids, T, h, E, k, tpc_f, capacity, num_ranks, (const int32_t*)chunk,
             nchf, (__nv_bfloat16*)nullptr, offsets, kept_counts, rank_counts, rank_offsets, tile_sched, dest_row,
-            drop_mask, src_token, src_slot, buf8, scales);
+            drop_mask, src_token, src_slot, buf8, scales, 0, 0u, 0LL, err);
         return check_launch(le, "dispatch_fused_kernel<fp8>");
     }
     const int nch = num_chunks(T, k);
