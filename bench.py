@@ -318,6 +318,9 @@ def run_gpu(args, cfg, C):
     launches0 = moe.moe_launch_count()
     t_clk0 = time.time()
     t_wall0 = time.perf_counter()
+    # every step follows an L2 flush, the first one too (its launches then queue behind the flush instead of
+    # reaching an idle GPU one by one from the host)
+    flush.zero_()
     for _ in range(args.steps):
         layer.forward(x, events=events)
         flush.zero_()
@@ -475,6 +478,7 @@ def time_backward(args, cfg, layer, x, flush, stream, kept):
     torch.cuda.synchronize()
     events: dict = {}
     fwd = []
+    flush.zero_()                                     # as in the forward timing: a flush before every pass
     for _ in range(args.steps):
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         e0.record(stream)
