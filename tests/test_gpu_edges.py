@@ -273,3 +273,36 @@ def test_router_split_deterministic():
     torch.cuda.synchronize()
     for key in ("logits", "ids", "gates", "counts", "f", "P", "aux"):
         assert torch.equal(r1[key], r2[key]), key
+
+
+@pytest.mark.parametrize("T,h,E,k,C,dtype", [
+    (1000, 16384, 8, 2, 230, "bf16"),       # 32 KB rows: two 16 KB pieces each, the ring wraps; drops and pads
+    (700, 6008, 16, 4, 0, "f32"),           # fp32 rows of 24032 B: pieces of 16384 and 7648 bytes
+    (2000, 4096, 1024, 1, 4, "bf16"),       # the largest count tables: the fewest ring stages, 63 rows a block
+    (300, 8, 4, 2, 0, "f32"),               # 32-byte rows
+])
+def test_dispatch_copy_ring_shapes(T, h, E, k, C, dtype):
+    """The fused dispatch's row copy (bulk-copy unit through a ring of shared stages) on rows split into
+    pieces, uneven last pieces, the smallest ring and the smallest rows: index outputs against the oracle's
+    dispatch, every kept row bitwise its token row, pad rows zero."""
+    import torch
+    from top_routing_dispatch_moe_gb300 import moe
+    rng = np.random.default_rng(T + h)
+    ids = np.stack([rng.permutation(E)[:k] for _ in range(T)]).astype(np.int32)
+    torch.manual_seed(T)
+    x = torch.randn(T, h, device="cuda")
+    if dtype == "bf16":
+        x = x.to(torch.bfloat16)
+    d = moe.moe_dispatch(x, torch.from_numpy(ids).cuda(), E, capacity=C, num_ranks=1)
+    torch.cuda.synchronize()
+    assert moe.moe_check_device_error() == moe.MOE_OK
+    ref = O.dispatch(ids, E, C, 1)
+    for key in ["offsets", "kept_counts", "dest_row", "src_token", "src_slot", "rank_counts", "rank_offsets"]:
+        np.testing.assert_array_equal(d[key].cpu().numpy(), ref[key], err_msg=key)
+    iv = torch.int16 if dtype == "bf16" else torch.int32
+    live = ref["src_token"] >= 0
+    got = d["buf"].view(iv).cpu().numpy()
+    want = x.view(iv).cpu().numpy()[ref["src_token"][live]]
+    np.testing.assert_array_equal(got[live], want)
+    if C:
+        assert np.all(got[~live] == 0)
