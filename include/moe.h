@@ -371,9 +371,9 @@ const char* moe_last_error_string(void);
  * MOE_OK, MOE_ERR_TIMEOUT if a bounded device-side wait ran out since the last check, or MOE_ERR_CUDA. */
 int moe_check_device_error(void* stream);
 /* Sets the iteration limit of the bounded device-side waits (mbarrier polls) of later launches: those of the
- * tensor-core GEMMs and of moe_dispatch's row copy; spins <= 0 restores the default. A small limit makes those waits give up early, which exercises the
- * error path: the kernel drains its copies in flight, frees its tensor memory, latches MOE_ERR_TIMEOUT
- * and returns. */
+ * tensor-core GEMMs and of moe_dispatch's row copy; spins <= 0 restores the default. A small limit makes
+ * those waits give up early, which exercises the error path: the kernel latches MOE_ERR_TIMEOUT, waits
+ * (bounded) for its copies and MMAs in flight, frees its tensor memory and returns. */
 void moe_set_wait_limit(long long spins);
 /* Number of kernels this process has launched through the library (all devices, all threads). */
 unsigned long long moe_launch_count(void);
