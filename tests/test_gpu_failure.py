@@ -1,7 +1,7 @@
-"""Failure detection on the GPU without a fault: the tensor-core GEMM's mbarrier waits are bounded. With the
-limit forced down to one poll the kernel gives up, latches MOE_ERR_TIMEOUT in the library's device error word,
-drains its copies and MMAs, frees its tensor memory and returns; the context stays usable and the next call,
-at the default limit, is correct."""
+"""Failure detection on the GPU without a fault: the mbarrier waits of the tensor-core GEMMs and of the
+dispatch's bulk row copy are bounded. With the limit forced down to one poll the kernel gives up, latches
+MOE_ERR_TIMEOUT in the library's device error word, drains its copies (and MMAs, freeing its tensor memory)
+and returns; the context stays usable and the next call, at the default limit, is correct."""
 import pytest
 
 pytestmark = pytest.mark.gpu
