@@ -13,6 +13,8 @@ _ec = O.expert_choice
 _sk = O.sinkhorn_scaling
 _cbwd, _swbwd, _rbwd = O.combine_backward, O.swiglu_ffn_backward, O.route_backward
 _enc, _q8, _dq8 = O.e4m3_encode, O.fp8_quantize_rows, O.fp8_dequantize_rows
+_logits, _payload, _eout, _selb, _ecl = O.router_logits, O.dispatch_payload, O.expert_outputs, O.route_selbias, \
+    O.expert_choice_layer
 
 
 def mut_renormalise_softmax(L, k, gating, bias=None, alpha=0.01):
@@ -170,6 +172,97 @@ def mut_fp8_dequant_no_scale(codes, scales):
     return _dq8(codes, np.ones_like(scales))
 
 
+def mut_logits_bias_in_sigmoid(x, w_r, bias, gating):
+    # the selection-only bias of sigmoid gating also added to the logits
+    L = np.asarray(x, np.float64) @ np.asarray(w_r, np.float64)
+    return L + np.asarray(bias, np.float64)[None, :] if bias is not None else L
+
+
+def mut_logits_no_bias(x, w_r, bias, gating):
+    # the logit bias of the softmax modes dropped
+    return np.asarray(x, np.float64) @ np.asarray(w_r, np.float64)
+
+
+def mut_softmax_over_tokens(L):
+    z = np.exp(L - L.max(axis=0, keepdims=True))
+    return z / z.sum(axis=0, keepdims=True)
+
+
+def mut_sigmoid_sign(L):
+    return 1.0 / (1.0 + np.exp(L))
+
+
+def mut_silu_sign(z):
+    return z / (1.0 + np.exp(z))
+
+
+def mut_payload_pads_first_token(x, d):
+    buf = _payload(x, d)
+    buf[d["src_token"] < 0] = x[0]
+    return buf
+
+
+def mut_payload_next_token(x, d):
+    buf = np.zeros((d["rows"], x.shape[1]), dtype=x.dtype)
+    live = d["src_token"] >= 0
+    buf[live] = x[(d["src_token"][live] + 1) % x.shape[0]]
+    return buf
+
+
+def mut_eout_next_expert(buf, d, weights):
+    E = len(d["kept_counts"])
+    return _eout(buf, d, lambda e: weights((e + 1) % E))
+
+
+def mut_combine_drops_shared(eout, dest_row, gates, shared_out=None):
+    return _combine(eout, dest_row, gates, None)
+
+
+def mut_ffn_flops_two_matrices(rows, h, F):
+    return 4 * h * F * rows
+
+
+def mut_dispatch_bytes_writes_only(T, kept, h, el):
+    return kept * h * el
+
+
+def mut_selbias_gates_renormalised(L, k, sel_bias, alpha=0.01):
+    r = _selb(L, k, sel_bias, alpha)
+    r["gates"] = r["gates"] / r["gates"].sum(axis=1, keepdims=True)
+    return r
+
+
+def mut_ec_layer_gate_one(x, w_r, weights, C, shared=None):
+    # expert-choice outputs summed with weight 1 instead of the expert's gate for the token
+    out = _ecl(x, w_r, weights, C, shared)
+    ec, eout = out["ec"], out["eout"]
+    y = np.zeros_like(out["y"]) if shared is None else O.swiglu_ffn(np.asarray(x, np.float64), *shared())
+    for e in range(ec["tokens"].shape[0]):
+        y[ec["tokens"][e]] += eout[e * C:(e + 1) * C]
+    return dict(out, y=y)
+
+
+def mut_bf16_truncate(v):
+    b = np.asarray(v, np.float32).view(np.uint32) >> 16
+    return (b.astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+
+
+def mut_e4m3_bias_8(code):
+    s = -1.0 if code & 0x80 else 1.0
+    e, m = (code >> 3) & 0xF, code & 0x7
+    if e == 0xF and m == 0x7:
+        return float("nan")
+    if e == 0:
+        return s * (m / 8.0) * 2.0 ** -7
+    return s * (1.0 + m / 8.0) * 2.0 ** (e - 8)
+
+
+def mut_dispatch_rank_offsets_first(ids, E, C, R):
+    d = _dispatch(ids, E, C, R)
+    d["rank_offsets"] = d["offsets"][:R + 1].copy()
+    return d
+
+
 MUTANTS = [
     ("route", mut_renormalise_softmax), ("route", mut_ascending_order), ("route", mut_bias_in_sigmoid_gates),
     ("route", mut_aux_denominator_T), ("dispatch", mut_drop_latest_first), ("dispatch", mut_dispatch_unstable),
@@ -180,6 +273,14 @@ MUTANTS = [
     ("route_backward", mut_route_backward_no_aux), ("route_backward", mut_route_backward_renorm_as_plain),
     ("combine_backward", mut_combine_backward_no_gate), ("e4m3_encode", mut_e4m3_ties_away),
     ("fp8_quantize_rows", mut_fp8_scale_240), ("fp8_dequantize_rows", mut_fp8_dequant_no_scale),
+    ("router_logits", mut_logits_bias_in_sigmoid), ("router_logits", mut_logits_no_bias),
+    ("softmax", mut_softmax_over_tokens), ("sigmoid", mut_sigmoid_sign), ("silu", mut_silu_sign),
+    ("dispatch_payload", mut_payload_pads_first_token), ("dispatch_payload", mut_payload_next_token),
+    ("expert_outputs", mut_eout_next_expert), ("combine", mut_combine_drops_shared),
+    ("ffn_flops", mut_ffn_flops_two_matrices), ("dispatch_bytes", mut_dispatch_bytes_writes_only),
+    ("route_selbias", mut_selbias_gates_renormalised), ("bf16_round", mut_bf16_truncate),
+    ("e4m3_value", mut_e4m3_bias_8), ("dispatch", mut_dispatch_rank_offsets_first),
+    ("expert_choice_layer", mut_ec_layer_gate_one),
 ]
 
 PINS = [
@@ -198,6 +299,10 @@ PINS = [
     P.test_swiglu_backward_scalar_closed_form, P.test_backward_dropped_pairs_and_pad_rows_get_zero,
     P.test_e4m3_table_closed_form, P.test_e4m3_encode_brute_force_and_ties,
     P.test_fp8_quantize_rows_scale_and_error_bound, P.test_fp8_payload_rows_and_pads,
+    P.test_sigmoid_constant_bias_changes_nothing, P.test_dispatch_payload_rows_and_zero_pads,
+    P.test_bf16_round_against_torch_and_ties, P.test_page3_flops_and_dispatch_bytes, P.test_logit_bias_moves_softmax_selection,
+    P.test_sinkhorn_selection_equals_topk_of_balanced_matrix, P.test_send_layout_is_block_transpose,
+    P.test_expert_choice_layer_against_scalar_loops,
 ]
 
 

@@ -110,6 +110,36 @@ def test_sigmoid_selection_uses_bias_but_gates_do_not():
         assert np.allclose(r["gates"][t], [s[e] / tot for e in sel], rtol=1e-14)
 
 
+def test_sigmoid_constant_bias_changes_nothing():
+    """Under sigmoid gating the bias only ranks experts ([L7] "Load balancing loss", DeepSeek-V3's
+    aux-loss-free bias): a bias equal for all experts keeps every token's order, so through the logits and the
+    routing neither the chosen experts nor the gates may move. Under the softmax modes the same constant is a
+    logit shift, which softmax ignores."""
+    rng = np.random.default_rng(12)
+    x, w_r = rng.standard_normal((30, 6)), rng.standard_normal((6, 8))
+    for gating in (O.SIGMOID_BIAS_RENORM, O.SOFTMAX, O.SOFTMAX_RENORM):
+        r0 = O.route(O.router_logits(x, w_r, np.zeros(8), gating), 3, gating, bias=np.zeros(8))
+        b = np.full(8, 0.7)
+        r1 = O.route(O.router_logits(x, w_r, b, gating), 3, gating, bias=b)
+        assert np.array_equal(r0["ids"], r1["ids"])
+        assert np.allclose(r0["gates"], r1["gates"], rtol=1e-13, atol=0), gating
+
+
+def test_logit_bias_moves_softmax_selection():
+    """In the softmax modes the per-expert bias is part of the logits (the Zipf load skew of the Mixtral-shaped
+    workload is made that way): a bias of +50 on one expert makes it every token's first choice, with a
+    softmax probability within e^-40 of 1."""
+    rng = np.random.default_rng(15)
+    x, w_r = rng.standard_normal((25, 6)), rng.standard_normal((6, 5)) * 0.5
+    b = np.zeros(5)
+    b[2] = 50.0
+    for gating in (O.SOFTMAX, O.SOFTMAX_RENORM):
+        r = O.route(O.router_logits(x, w_r, b, gating), 2, gating)
+        assert np.all(r["ids"][:, 0] == 2)
+        if gating == O.SOFTMAX:
+            assert np.all(np.abs(r["gates"][:, 0] - 1.0) < math.exp(-40))
+
+
 def test_softmax_gate_closed_forms():
     # two experts whose logits differ by ln 3: probabilities 3/4 and 1/4
     L = np.array([[math.log(3.0), 0.0]])
@@ -248,6 +278,29 @@ def test_dispatch_stable_and_bijective():
         assert len(kept) == d["kept_counts"].sum()
         assert np.all(d["src_token"][d["dest_row"][kept[:, 0], kept[:, 1]]] == kept[:, 0])
         assert np.all(d["src_slot"][d["dest_row"][kept[:, 0], kept[:, 1]]] == kept[:, 1])
+
+
+def test_dispatch_payload_rows_and_zero_pads():
+    """Brute force over (t, j): the row dest_row[t, j] of the send buffer is x[t] for every kept pair; every
+    other row (a pad) is zero ([L7] table row "dispatch": unfilled slots are padded)."""
+    rng = np.random.default_rng(13)
+    T, h, E, k = 30, 5, 4, 2
+    x = rng.standard_normal((T, h)) + 3.0                     # no zero entries in real rows
+    ids = np.stack([rng.permutation(E)[:k] for _ in range(T)]).astype(np.int32)
+    for C in (0, 9, 20):
+        d = O.dispatch(ids, E, C, 1)
+        buf = O.dispatch_payload(x, d)
+        used = set()
+        for t in range(T):
+            for j in range(k):
+                r = int(d["dest_row"][t, j])
+                if r >= 0:
+                    assert np.array_equal(buf[r], x[t])
+                    used.add(r)
+        for r in range(buf.shape[0]):
+            if r not in used:
+                assert not buf[r].any()
+        assert len(used) == int(d["kept_counts"].sum())
 
 
 def test_capacity_drops_in_token_order():
@@ -614,6 +667,20 @@ def test_e4m3_encode_brute_force_and_ties():
     assert np.all((m & 1) == 0) and np.all((m == pos[:-1]) | (m == pos[1:]))
     assert np.all(O.e4m3_encode(np.array([449.0, 500.0, 1e30])) == 0x7E)
     assert np.all(O.e4m3_encode(np.array([-449.0, -1e30])) == 0xFE)
+
+
+def test_bf16_round_against_torch_and_ties():
+    """Round to nearest bfloat16, ties to even: against torch's float32 -> bfloat16 conversion on normal,
+    subnormal and large values, and three ties written out by hand (1 + 2^-8 lies midway between 1 and
+    1 + 2^-7, 1 + 3 * 2^-8 midway between 1 + 2^-7 and 1 + 2^-6)."""
+    import torch
+    rng = np.random.default_rng(14)
+    v = np.concatenate([rng.standard_normal(4000), rng.standard_normal(500) * 1e-39, rng.standard_normal(500) * 1e30])
+    v = v.astype(np.float32)
+    want = torch.from_numpy(v).to(torch.bfloat16).to(torch.float64).numpy()
+    assert np.array_equal(O.bf16_round(v), want)
+    ties = np.array([1 + 2.0 ** -8, 1 + 3 * 2.0 ** -8, -(1 + 2.0 ** -8), 1 + 2.0 ** -8 + 2.0 ** -20], np.float32)
+    assert O.bf16_round(ties).tolist() == [1.0, 1 + 2.0 ** -6, -1.0, 1 + 2.0 ** -7]
 
 
 def test_fp8_quantize_rows_scale_and_error_bound():
