@@ -429,7 +429,7 @@ def run_gpu(args, cfg, C):
             "scaling": "weak",
             "vs_baseline": None, "dtype": "bf16" if cfg.dtype == "bf16" else "f32", "data": "synthetic",
             "config": {"workload": _workload_desc(cfg, C), "global_batch": cfg.T * world, "tokens_per_gpu": cfg.T,
-                       "parallelism": f"replicas x{world}", "l2": "flushed between steps (512 MiB write)",
+                       "parallelism": f"replicas x{world}", "l2": "flushed before every step (512 MiB write)",
                        "kept_assignments": kept},
             "roofline": roofline,
             **({"backward": backward} if backward is not None else {}),
