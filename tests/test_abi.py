@@ -117,3 +117,46 @@ def test_host_checks_of_the_backward_and_fp8_entry_points(lib):
     assert lib.raw_lib().moe_dispatch_backward_workspace_size(T, h, 8, lib.MOE_BF16) < need
     # router weight gradient: room for either path
     assert lib.raw_lib().moe_router_weight_grad_workspace_size(T, h, E) >= h * 1024 * 2 + E * 3 * 1024 * 2
+
+
+def _c_kind(t):
+    """Kind of a C type of the header: ptr, void, f32, f64, or i/u plus the width in bits (LP64)."""
+    t = " ".join(t.replace("const", " ").split())
+    if "*" in t:
+        return "ptr"
+    return {"int": "i32", "unsigned": "u32", "size_t": "u64", "long long": "i64", "unsigned long long": "u64",
+            "float": "f32", "double": "f64", "void": "void"}[t]
+
+
+def _ct_kind(c):
+    """The same kind for a ctypes type (ctypes aliases types of equal width, so compare by width and sign)."""
+    if c is None:
+        return "void"
+    if c in (ctypes.c_void_p, ctypes.c_char_p):
+        return "ptr"
+    if c in (ctypes.c_float, ctypes.c_double):
+        return "f%d" % (8 * ctypes.sizeof(c))
+    return ("i" if c(-1).value < 0 else "u") + str(8 * ctypes.sizeof(c))
+
+
+def test_binding_signatures_match_the_header(lib):
+    """Every prototype of include/moe.h against the ctypes signature the binding gives it: the same return
+    kind and the same parameter kinds in the same order (a pointer, int, size_t, float, ...), so that no
+    argument is marshalled with the wrong width."""
+    src = open(os.path.join(ROOT, "include", "moe.h")).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    decls = re.findall(r"([A-Za-z_][A-Za-z0-9_ \*]*?)\b(moe_[a-z0-9_]+)\s*\(([^)]*)\)\s*;", src)
+    assert sorted(n for _, n, _ in decls) == _declared()
+    sigs = {}
+    for name, (res, args) in lib._SIGS.items():
+        sigs[name] = (_ct_kind(res), [_ct_kind(a) for a in args])
+    checked = 0
+    for ret, name, params in decls:
+        ps = [p.strip() for p in params.split(",") if p.strip() and p.strip() != "void"]
+        want = (_c_kind(ret), [_c_kind(re.sub(r"\b[A-Za-z_][A-Za-z0-9_]*$", "", p)) for p in ps])
+        if name in sigs:
+            assert sigs[name] == want, (name, sigs[name], want)
+            checked += 1
+        else:   # declared but bound by hand in the binding: must at least be exported
+            assert hasattr(lib.raw_lib(), name), name
+    assert checked >= 40
