@@ -18,8 +18,8 @@
  *   - Return value: MOE_OK, or an error code with a message retrievable by moe_last_error_string()
  *     (per host thread). Argument checks happen before anything is enqueued, so a call that returns
  *     MOE_ERR_INVALID_ARG / MOE_ERR_UNSUPPORTED / MOE_ERR_WORKSPACE has not touched device memory.
- *     MOE_ERR_CUDA reports a failed launch. Errors detected on the device (a bounded wait that ran out)
- *     are latched in a device word and reported by moe_check_device_error().
+ *     MOE_ERR_CUDA reports a failed launch. Errors detected on the device (a bounded wait that ran out,
+ *     an expert id outside [0, E)) are latched in a device word and reported by moe_check_device_error().
  *   - dtype: MOE_F32 (fp32 in/out, fp32 arithmetic) or MOE_BF16 (bf16 tensors, fp32 accumulation).
  *     Gates, logits, f, P and aux are always fp32.
  *   - Sizes: T >= 0; 1 <= k <= min(E, 16); 1 <= E <= 1024; h % 8 == 0; F % 8 == 0. All tensor pointers
@@ -127,6 +127,10 @@ int moe_sinkhorn_bias(const float* logits, int T, int E, int n_iter, float* sel_
  *   rank_offsets[R+1] int32      first row of each rank block (= offsets[r*E/R])
  *   tile_sched  moe_tile_sched_bytes() bytes, opaque: per-expert MOE_TILE_M-row tiles for the FFN
  *   Deterministic and stable (token order inside every expert block).
+ *   Errors: MOE_ERR_INVALID_ARG if num_ranks does not divide E, rows >= 2^31, capacity < 0, or a pointer
+ *   is null or not 16-byte aligned (x, buf, tile_sched); MOE_ERR_WORKSPACE if ws_bytes <
+ *   moe_dispatch_workspace_size(). An id outside [0, E) is treated as dropped and latched:
+ *   moe_check_device_error() then returns MOE_ERR_INVALID_ARG.
  * ------------------------------------------------------------------------------------------------- */
 size_t moe_dispatch_rows(int T, int E, int k, int capacity);
 size_t moe_tile_sched_bytes(int T, int E, int k, int capacity);
@@ -368,7 +372,8 @@ int moe_expert_weight_grads(const void* buf, const void* act, const void* d_gu, 
 /* Message of the last failing call on this host thread ("" if none). */
 const char* moe_last_error_string(void);
 /* Synchronizes `stream`, then reads and clears the device error word of the current device. Returns
- * MOE_OK, MOE_ERR_TIMEOUT if a bounded device-side wait ran out since the last check, or MOE_ERR_CUDA. */
+ * MOE_OK, MOE_ERR_TIMEOUT if a bounded device-side wait ran out since the last check, MOE_ERR_INVALID_ARG
+ * if a kernel met an expert id outside [0, E), or MOE_ERR_CUDA. */
 int moe_check_device_error(void* stream);
 /* Sets the iteration limit of the bounded device-side waits (mbarrier polls) of later launches: those of the
  * tensor-core GEMMs and of moe_dispatch's row copy; spins <= 0 restores the default. A small limit makes
