@@ -77,6 +77,9 @@ enum moe_gating {
  *                                softmax; sigmoid mode: s_e / sum_e' s_e')
  *   aux      [1]    fp32         alpha * E * sum_e f_e * P_e
  *   Deterministic: the same inputs give bitwise-identical outputs on every call.
+ *   Errors: MOE_ERR_UNSUPPORTED for a dtype or gating value outside the enums; MOE_ERR_INVALID_ARG for
+ *   h % 8 != 0, E or k out of range, a null output, or x / w_r / logits not 16-byte aligned;
+ *   MOE_ERR_WORKSPACE if ws_bytes < moe_router_workspace_size().
  * ------------------------------------------------------------------------------------------------- */
 size_t moe_router_workspace_size(int T, int h, int E, int k, int dtype);
 int moe_router(const void* x, const void* w_r, const float* bias, int T, int h, int E, int k, int dtype,
@@ -204,6 +207,8 @@ int moe_pack_expert_weights(const void* w_gate, const void* w_up, const void* w_
  *   fp32 accumulation in tensor memory; act is stored in bf16); fp32 runs on the CUDA cores.
  *   moe_expert_up_gate and moe_expert_down are the two steps; moe_expert_ffn runs both with act in the
  *   workspace.
+ *   Errors: MOE_ERR_UNSUPPORTED for a dtype outside the enum; MOE_ERR_INVALID_ARG for E, h, F or rows out
+ *   of range (h % 8, F % 8), a null pointer with rows > 0, or a pointer not 16-byte aligned.
  * ------------------------------------------------------------------------------------------------- */
 int moe_expert_up_gate(const void* buf, const int32_t* tile_sched, const void* packed_w, int E, int h, int F,
                        int rows, int dtype, void* act, void* stream);
@@ -247,6 +252,8 @@ int moe_expert_ffn(const void* buf, const int32_t* tile_sched, const void* packe
  *   accumulated in fp32 in ascending j, rounded once to dtype. Dropped pairs add nothing; no residual.
  *   eout [rows,h] dtype; dest_row [T,k] int32; gates [T,k] fp32; shared_out [T,h] dtype or NULL;
  *   y [T,h] dtype. Deterministic (no atomics).
+ *   Errors: MOE_ERR_UNSUPPORTED for a dtype outside the enum; MOE_ERR_INVALID_ARG for h % 8 != 0, k outside
+ *   [1, 16], a null pointer, or eout / shared_out / y not 16-byte aligned.
  * ------------------------------------------------------------------------------------------------- */
 int moe_combine(const void* eout, const int32_t* dest_row, const float* gates, const void* shared_out, int T,
                 int h, int k, int dtype, void* y, void* stream);
