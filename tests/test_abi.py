@@ -84,6 +84,22 @@ def test_host_checks_reject_before_any_cuda_call(lib):
     assert raw.moe_combine(ok, ok, ok, n, 4, 16, 2, 5, ok, n) == lib.MOE_ERR_UNSUPPORTED
     # pack: F % 8
     assert raw.moe_pack_expert_weights(ok, ok, ok, 2, 16, 12, 1, ok, n) == lib.MOE_ERR_INVALID_ARG
+    # dispatch: E out of range, misaligned x, workspace too small
+    args = [ok, ok, 4, 16, 8, 2, 0, 1, 1] + [ok] * 10 + [ok, 1 << 20, n]
+    args[4] = 0
+    assert raw.moe_dispatch(*args) == lib.MOE_ERR_INVALID_ARG
+    args[4], args[0] = 8, bad
+    assert raw.moe_dispatch(*args) == lib.MOE_ERR_INVALID_ARG
+    assert "aligned" in lib.moe_last_error_string()
+    args[0], args[20] = ok, 1
+    assert raw.moe_dispatch(*args) == lib.MOE_ERR_WORKSPACE
+    # combine: k out of range, null eout, misaligned y
+    assert raw.moe_combine(ok, ok, ok, n, 4, 16, 17, 1, ok, n) == lib.MOE_ERR_INVALID_ARG
+    assert raw.moe_combine(n, ok, ok, n, 4, 16, 2, 1, ok, n) == lib.MOE_ERR_INVALID_ARG
+    assert raw.moe_combine(ok, ok, ok, n, 4, 16, 2, 1, bad, n) == lib.MOE_ERR_INVALID_ARG
+    # expert up/gate: dtype, misaligned act
+    assert raw.moe_expert_up_gate(ok, ok, ok, 8, 16, 16, 4, 5, ok, n) == lib.MOE_ERR_UNSUPPORTED
+    assert raw.moe_expert_up_gate(ok, ok, ok, 8, 16, 16, 4, 1, bad, n) == lib.MOE_ERR_INVALID_ARG
 
 
 def test_host_checks_of_the_backward_and_fp8_entry_points(lib):
