@@ -306,3 +306,5 @@ def test_dispatch_copy_ring_shapes(T, h, E, k, C, dtype):
     np.testing.assert_array_equal(got[live], want)
     if C:
         assert np.all(got[~live] == 0)
+    from top_routing_dispatch_moe_gb300.checks import check_dispatch
+    assert check_dispatch(d, ids, E, C, 1, x=x) == []
