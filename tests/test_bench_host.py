@@ -46,3 +46,28 @@ def test_parity_report_verdicts(oracle_run):
 def test_parity_report_skips_other_routings():
     cfg = moe_inputs.get_config("page3_expert_choice")
     assert "skipped" in bench.parity_report(cfg, None, {})
+
+
+def test_reference_arm_json_line_on_cpu():
+    """`bench.py --impl reference` times the oracle on the host cores and prints one JSON line with the bench's
+    keys (impl, metric, value, unit, cpu_baseline of kind oracle, e2e without host-device bytes); a rank other
+    than 0 prints nothing and exits 0."""
+    import json
+    import os
+    import subprocess
+    import sys
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    cmd = [sys.executable, "bench.py", "--impl", "reference", "--steps", "1", "--warmup", "3", "--workload",
+           "tiny_fp32"]
+    env = dict(os.environ, RANK="0")
+    out = subprocess.run(cmd, cwd=root, env=env, capture_output=True, text=True, timeout=600)
+    assert out.returncode == 0, out.stderr[-2000:]
+    line = json.loads(out.stdout.strip().splitlines()[-1])
+    assert line["impl"] == "reference" and line["unit"] == "tokens/s" and line["value"] > 0
+    assert line["higher_is_better"] is True and line["steps"] == 1 and line["warmup"] == 3
+    assert line["cpu_baseline"]["kind"] == "oracle" and line["cpu_baseline"]["value"] == line["value"]
+    assert line["e2e"]["h2d_bytes_per_step"] == 0 and line["e2e"]["d2h_bytes_per_step"] == 0
+    assert line["config"]["workload"].startswith("tiny_fp32")
+    env["RANK"] = "1"
+    out = subprocess.run(cmd, cwd=root, env=env, capture_output=True, text=True, timeout=600)
+    assert out.returncode == 0 and out.stdout.strip() == ""
