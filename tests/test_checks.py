@@ -98,3 +98,57 @@ def test_out_of_range_ids_are_reported():
     ids = ids.copy()
     ids[0, 0] = E
     assert check_dispatch(d, ids, E, C, R) == ["topk_ids outside [0, E)"]
+
+
+def _router_case(gating, seed=3):
+    rng = np.random.default_rng(seed)
+    T, E, k = 50, 8, 3
+    L = rng.standard_normal((T, E))
+    b = rng.standard_normal(E) * 0.3 if gating in (O.SIGMOID_BIAS_RENORM, "softmax_selbias") else None
+    if gating == "softmax_selbias":
+        r = O.route_selbias(L, k, b)
+    else:
+        r = O.route(L, k, gating, b)
+    out = dict(ids=r["ids"].astype(np.int32), gates=r["gates"].astype(np.float32),
+               counts=r["counts"].astype(np.int32), f=r["f"].astype(np.float32), P=r["P"].astype(np.float32),
+               aux=np.array([r["aux"]], np.float32))
+    return out, L.astype(np.float32), b, E
+
+
+@pytest.mark.parametrize("gating", [O.SOFTMAX, O.SOFTMAX_RENORM, O.SIGMOID_BIAS_RENORM, "softmax_selbias"])
+def test_router_checker_accepts_the_oracle_and_names_corruptions(gating):
+    from top_routing_dispatch_moe_gb300.checks import check_router
+    r0, L, b, E = _router_case(gating)
+    assert check_router(r0, E, gating, logits=L, bias=b) == []
+
+    def run(mutate):
+        r = {key: v.copy() for key, v in r0.items()}
+        mutate(r)
+        return " | ".join(check_router(r, E, gating, logits=L, bias=b))
+
+    def dup(r):
+        r["ids"][0, 1] = r["ids"][0, 0]
+    assert "twice" in run(dup)
+
+    def swap(r):
+        r["ids"][1, [0, 1]] = r["ids"][1, [1, 0]]
+    assert "descending" in run(swap)
+
+    def unchosen(r):                                  # replace a choice by the token's lowest-scoring expert
+        sc = L[2] if gating in (O.SOFTMAX, O.SOFTMAX_RENORM) else None
+        if sc is None:
+            sc = (1 / (1 + np.exp(-L[2])) + b) if gating == O.SIGMOID_BIAS_RENORM else L[2] + b
+        r["ids"][2, -1] = int(np.argmin(sc))
+    assert "unchosen" in run(unchosen)
+
+    def counts_off(r):
+        r["counts"][0] += 1
+    assert "histogram" in run(counts_off)
+
+    def aux_off(r):
+        r["aux"][0] *= 1.5
+    assert "aux" in run(aux_off)
+
+    def gate_zero(r):
+        r["gates"][3, 0] = 0.0
+    assert "gate" in run(gate_zero)

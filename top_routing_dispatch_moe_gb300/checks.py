@@ -1,4 +1,5 @@
-"""Host-side checks of moe_dispatch's outputs: a debugging aid standing in for a device race detector.
+"""Host-side checks of moe_router's and moe_dispatch's outputs: a debugging aid standing in for a device race
+detector.
 
 Every index output of a dispatch is checked against the invariants that define it (the v6 MoE page, table
 row "dispatch" and the "Capacity" bullet: group by expert in token order, at most C rows per expert, the
@@ -100,4 +101,65 @@ def check_dispatch(d: dict, topk_ids, E: int, capacity: int, num_ranks: int = 1,
             bad.append("a kept row differs from its token's row")
         if capacity > 0 and np.any(buf[other] != 0):
             bad.append("a pad row is not zero")
+    return bad
+
+
+GATINGS = ("softmax", "softmax_renorm", "sigmoid_bias_renorm", "softmax_selbias")
+
+
+def check_router(r: dict, E: int, gating: str, alpha: float = 0.01, logits=None, bias=None,
+                 tol: float = 1e-5) -> list[str]:
+    """Violations of the router's output invariants by `r` (the dict moe_router returns: ids, gates, counts,
+    f, P, aux); an empty list when every invariant holds. ("Megatron-LM ... (6)", section "Router": top-k with
+    softmax or sigmoid weights; the v6 MoE page, "Load balancing loss": aux = alpha E sum f_i P_i.)
+
+    Checked: ids in [0, E) and distinct within a token; gates positive, at most 1, summing to 1 over the k
+    choices in the renormalised modes; counts the histogram of ids, f = counts / (k T); P a distribution over
+    the experts; aux = alpha E sum f P. With the fp32 `logits` [T, E] (and the selection bias of the sigmoid
+    and selection-bias modes), also: every chosen expert's selection score at least every unchosen one's, the
+    k choices in descending score order (up to `tol`, so near ties pass either way)."""
+    if gating not in GATINGS:
+        return [f"unknown gating {gating!r}"]
+    ids = _host(r["ids"]).astype(np.int64)
+    gates = _host(r["gates"]).astype(np.float64)
+    T, k = ids.shape
+    bad: list[str] = []
+    if ids.size and (ids.min() < 0 or ids.max() >= E):
+        return ["ids outside [0, E)"]
+    if T and np.any(np.sort(ids, axis=1)[:, 1:] == np.sort(ids, axis=1)[:, :-1]):
+        bad.append("a token chose one expert twice")
+    if np.any(gates <= 0) or np.any(gates > 1 + tol):
+        bad.append("a gate outside (0, 1]")
+    if gating in ("softmax_renorm", "sigmoid_bias_renorm") and T:
+        if np.max(np.abs(gates.sum(axis=1) - 1.0)) > tol * k:
+            bad.append("renormalised gates do not sum to 1")
+    counts = _host(r["counts"]).astype(np.int64)
+    if not np.array_equal(counts, np.bincount(ids.ravel(), minlength=E)):
+        bad.append("counts are not the histogram of ids")
+    f, P = _host(r["f"]).astype(np.float64), _host(r["P"]).astype(np.float64)
+    if T and np.max(np.abs(f - counts / float(k * T))) > tol:
+        bad.append("f differs from counts / (k T)")
+    if T and (np.any(P < 0) or abs(P.sum() - 1.0) > tol * E):
+        bad.append("P is not a distribution over the experts")
+    aux = float(_host(r["aux"]).reshape(-1)[0])
+    if T and abs(aux - alpha * E * float(np.sum(f * P))) > tol * max(1.0, abs(aux)):
+        bad.append("aux differs from alpha E sum f P")
+    if logits is not None and T:
+        L = _host(logits).astype(np.float64)
+        b = np.zeros(E) if bias is None else _host(bias).astype(np.float64)
+        if gating == "sigmoid_bias_renorm":
+            score = 1.0 / (1.0 + np.exp(-L)) + b[None, :]
+        elif gating == "softmax_selbias":
+            score = L + b[None, :]
+        else:
+            score = L                                  # the logits already hold a softmax-mode bias
+        chosen = np.take_along_axis(score, ids, axis=1)
+        if k > 1 and np.any(chosen[:, 1:] > chosen[:, :-1] + tol):
+            bad.append("the k choices are not in descending score order")
+        mask = np.ones((T, E), bool)
+        np.put_along_axis(mask, ids, False, axis=1)
+        if E > k:
+            best_other = np.where(mask, score, -np.inf).max(axis=1)
+            if np.any(best_other > chosen.min(axis=1) + tol):
+                bad.append("an unchosen expert scores above a chosen one")
     return bad
