@@ -17,9 +17,10 @@ KEYS = ("offsets", "kept_counts", "dest_row", "drop_mask", "src_token", "src_slo
 
 def _host(a):
     if hasattr(a, "detach"):                          # a torch tensor: bf16 has no numpy type, compare its bits
+        import torch
         a = a.detach().cpu()
-        if str(a.dtype) == "torch.bfloat16":
-            a = a.view(dtype=__import__("torch").int16)
+        if a.dtype == torch.bfloat16:
+            a = a.view(torch.int16)
         a = a.numpy()
     return np.asarray(a)
 
