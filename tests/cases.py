@@ -99,6 +99,16 @@ def from_device(t, cfg):
     return t.detach().cpu().numpy().astype(np.float64)
 
 
+def from_device_rows(t, mask, cfg):
+    """Download the rows of a working-dtype tensor where `mask` (a device bool tensor) is set, as float64 numpy of
+    the full shape with every other row zero (rows a kernel never writes hold whatever the allocator left, and
+    are not converted)."""
+    import torch
+    out = torch.zeros_like(t)
+    out[mask] = t[mask]
+    return from_device(out, cfg)
+
+
 def rel_l2(a, b):
     a = np.asarray(a, np.float64)
     b = np.asarray(b, np.float64)

@@ -60,7 +60,9 @@ def _combine(name):
     cfg, inp, layer, x, dy = _forward(name)
     r, d = layer.r_out, layer.d_out
     d_eout, d_gates = moe.moe_combine_backward(dy, layer.eout, d["src_token"], d["src_slot"], d["dest_row"], r["gates"])
-    ref_eout, ref_gates = O.combine_backward(_np(dy), _np(layer.eout), d["dest_row"].cpu().numpy(), _np(r["gates"]),
+    # pad rows of eout are never written by the GEMMs (and never read by combine): converted as zeros
+    eout64 = cases.from_device_rows(layer.eout, d["src_token"] >= 0, cfg)
+    ref_eout, ref_gates = O.combine_backward(_np(dy), eout64, d["dest_row"].cpu().numpy(), _np(r["gates"]),
                                              layer.rows)
     return cfg, d_eout, d_gates, ref_eout, ref_gates
 

@@ -1,6 +1,10 @@
 """GPU parity of the CUDA path against the oracle, element by element, at sizes the oracle finishes in
 seconds (several 128-row tiles, ragged tails, drop-forcing capacities, empty experts).
 
+The "_pair" cases have at least 4 * 128 * E dispatched rows, the size from which the library runs the grouped
+GEMMs on the 2-SM (cta_group::2) kernel, with experts of odd and even 128-row tile counts (an odd count leaves
+the second CTA of the last pair a phantom tile); every element of their outputs is compared as well.
+
 Indices (ids, counts, offsets, permutation, drop mask, send layout, tile schedule) must match bit-exactly;
 the dispatched payload is a copy and must match bit-exactly too. Floats: router logits, gates, f, P and
 aux within 1e-5 of max|ref| (fp32 arithmetic on both dtypes); expert outputs and y within 1e-5 max-rel
@@ -36,11 +40,21 @@ def _cfg(name):
         "deepseek_small": (g("deepseek_v3", T=700, h=512, F=256), None),
         "qwen3_small": (g("qwen3_moe", T=2000, h=256, F=128), None),
         "tiny_fp32_cf": (g("tiny_fp32", T=300, cf=0.75), None),
+        # 2-SM GEMM path: page-3 routing with capacity (C = 813, rows = 6504), the Zipf-skewed renormalised
+        # routing dropless (rows = 4600; the largest expert has 13 tiles), Qwen3-shaped uniform routing
+        # (rows = 65536 = 4 * 128 * E) and a sigmoid-routed layer with its shared expert in the same launches
+        "page3_pair": (g("page3_cf1.25", T=2600, h=512, F=384), None),
+        "mixtral_pair": (g("mixtral_zipf", T=2300, h=256, F=512), "zipf"),
+        "qwen3_pair": (g("qwen3_moe", T=8192, h=256, F=128), None),
+        "deepseek_pair": (g("deepseek_v3", T=2100, h=512, F=256, E=16, k=4), None),
     }[name]
 
 
 CASE_NAMES = ["tiny_fp32", "page3_small", "page3_small_cf1.0", "page3_small_cf0.5", "mixtral_small",
-              "mixtral_small_cf1.25", "deepseek_small", "qwen3_small", "tiny_fp32_cf"]
+              "mixtral_small_cf1.25", "deepseek_small", "qwen3_small", "tiny_fp32_cf",
+              "page3_pair", "mixtral_pair", "qwen3_pair", "deepseek_pair"]
+PAIR_CASES = [n for n in CASE_NAMES if n.endswith("_pair")]
+PAIR_MIN_ROWS_PER_EXPERT = 4 * 128     # the library's switch to the 2-SM grouped GEMM
 
 _cache = {}
 
@@ -64,7 +78,8 @@ def run_case(name):
     got = {k: v.cpu().numpy() for k, v in layer.r_out.items()}
     got.update({k: v.cpu().numpy() for k, v in layer.d_out.items() if k != "buf"})
     got["buf"] = cases.from_device(layer.d_out["buf"], cfg)
-    got["eout"] = cases.from_device(layer.eout, cfg)
+    # pad rows of eout are never written by the GEMMs: only the dispatched rows are read back
+    got["eout"] = cases.from_device_rows(layer.eout, layer.d_out["src_token"] >= 0, cfg)
     got["act_dtype"] = str(layer.act.dtype)
     got["y"] = cases.from_device(y, cfg)
     got["y_bits"] = y.clone()
@@ -132,9 +147,37 @@ def test_expert_outputs(name):
     cfg, inp, ref, got, *_ = run_case(name)
     d = ref["disp"]
     live = d["src_token"] >= 0
+    assert np.isfinite(got["eout"][live]).all()
     fn, tol = cases.y_tolerance(cfg)
     err = fn(got["eout"][live], ref["eout"][live])
     assert err <= tol, f"expert outputs err {err:.3e} > {tol}"
+
+
+@pytest.mark.parametrize("name", PAIR_CASES)
+def test_pair_cases_reach_the_2sm_gemm(name):
+    """The reduced cases meant for the 2-SM kernel are above its row threshold, and their experts' 128-row
+    tile counts include odd ones (phantom second tiles) as well as even ones."""
+    cfg, inp, ref, got, layer, _ = run_case(name)
+    assert layer.rows >= PAIR_MIN_ROWS_PER_EXPERT * cfg.E
+    tiles = (ref["disp"]["kept_counts"] + 127) // 128
+    assert (tiles % 2 == 1).any() and (tiles[tiles > 0] % 2 == 0).any(), tiles
+
+
+@pytest.mark.parametrize("name", PAIR_CASES)
+def test_pair_cases_every_element(name):
+    """Every dispatched row of eout and every token's y, one row at a time against the oracle: normwise within
+    the bf16 tolerance and no row above 4x it (a wrong tile, a swapped pair half or a phantom tile stored over
+    real rows shows up as whole rows far off)."""
+    cfg, inp, ref, got, *_ = run_case(name)
+    fn, tol = cases.y_tolerance(cfg)
+    live = np.nonzero(ref["disp"]["src_token"] >= 0)[0]
+    for r in live:
+        assert fn(got["eout"][r], ref["eout"][r]) <= 4 * tol, f"eout row {r}"
+    for t in range(cfg.T):
+        if np.linalg.norm(ref["y"][t]) > 0:
+            assert fn(got["y"][t], ref["y"][t]) <= 4 * tol, f"y token {t}"
+        else:
+            assert not got["y"][t].any(), f"y token {t} (every pair dropped) not zero"
 
 
 @pytest.mark.parametrize("name", CASE_NAMES)
