@@ -12,7 +12,12 @@
  * Conventions (every entry point):
  *   - Tensor arguments are DEVICE pointers owned by the caller, row-major with the last dimension
  *     contiguous. The library never allocates memory: calls that need scratch take a caller-provided
- *     device workspace whose size the matching *_workspace_size() function returns.
+ *     device workspace whose size the matching *_workspace_size() function returns. One exception:
+ *     moe_dispatch_static keeps its scratch in a fixed 1 MiB device array of the library's own (held for the
+ *     life of the process and shared by all its calls, so overlapping calls must be serialised by the caller).
+ *   - Per-device state the library caches (the device error word's and that array's addresses, kernel
+ *     attributes) is keyed by the CUDA context it was set up in and set up again in a new context, e.g. after
+ *     cudaDeviceReset; the first call in a new context should come before any stream capture in it.
  *   - `stream` is a cudaStream_t passed as void* (NULL = the legacy default stream). Every call only
  *     enqueues work on that stream; none synchronizes the host.
  *   - Return value: MOE_OK, or an error code with a message retrievable by moe_last_error_string()
@@ -86,6 +91,20 @@ int moe_router(const void* x, const void* w_r, const float* bias, int T, int h, 
                int gating, float alpha, float* logits, int32_t* topk_ids, float* gates, int32_t* counts,
                float* f, float* P, float* aux, void* ws, size_t ws_bytes, void* stream);
 
+/* moe_pack_router_weight / moe_router_packed: moe_router on a router weight repacked once ("Megatron-LM ...
+ *   （六）", section "Router": the same logits GEMM; the packing is this library's operand layout, not the pages').
+ *   moe_pack_router_weight writes `packed` (moe_router_packed_bytes(h, E, dtype) bytes): for bf16 the transpose
+ *   W_r^T [E,h] (the K-major operand of the logits GEMM, which moe_router otherwise builds in its workspace on
+ *   every call), for fp32 a copy of w_r [h,E]. moe_router_packed takes that buffer in place of w_r; every other
+ *   argument, the workspace size and the outputs (bitwise) are those of moe_router. Errors as moe_router;
+ *   moe_pack_router_weight: MOE_ERR_INVALID_ARG for h % 8 != 0, E outside [1, 1024] or a null / misaligned
+ *   pointer. */
+size_t moe_router_packed_bytes(int h, int E, int dtype);
+int moe_pack_router_weight(const void* w_r, int h, int E, int dtype, void* packed, void* stream);
+int moe_router_packed(const void* x, const void* w_packed, const float* bias, int T, int h, int E, int k, int dtype,
+                      int gating, float alpha, float* logits, int32_t* topk_ids, float* gates, int32_t* counts,
+                      float* f, float* P, float* aux, void* ws, size_t ws_bytes, void* stream);
+
 /* moe_router_from_logits: the gating part of moe_router (top-k, gates, counts, f, P, aux) on given fp32
  * logits [T,E] (as moe_router writes them: bias already added in the two plain softmax modes; in the sigmoid
  * and selection-bias modes `bias` is the selection-only term). Workspace: moe_router_from_logits_workspace_size. */
@@ -151,7 +170,8 @@ int moe_dispatch(const void* x, const int32_t* topk_ids, int T, int h, int E, in
  * (1048576-byte) array of the library's own device memory, held by every GPU that loads the library until
  * the process exits. A size whose scratch (moe_dispatch_workspace_size) exceeds 1 MiB is rejected with
  * MOE_ERR_INVALID_ARG before anything is enqueued. The first call on a device (with that device current)
- * looks up the array's device address; make that call before any stream capture on the device. All calls
+ * looks up the array's device address, and so does the first call in a new context of that device (after
+ * cudaDeviceReset); make those calls before any stream capture on the device. All calls
  * share the array and each overwrites it: calls that may overlap on the GPU race and must be serialised by
  * the caller. No call allocates memory. */
 int moe_dispatch_static(const void* x, const int32_t* topk_ids, int T, int h, int E, int k, int capacity,
@@ -257,6 +277,30 @@ int moe_expert_ffn(const void* buf, const int32_t* tile_sched, const void* packe
  * ------------------------------------------------------------------------------------------------- */
 int moe_combine(const void* eout, const int32_t* dest_row, const float* gates, const void* shared_out, int T,
                 int h, int k, int dtype, void* y, void* stream);
+
+/* ---------------------------------------------------------------------------------------------------
+ * moe_expert_down_combine: the down GEMM with the combine in its epilogue (one launch instead of
+ *   moe_expert_down[_shared] followed by moe_combine).
+ *   "v6 长序列和 MoE ...", table row "combine"; "专家并行" (formulaic), section "通信与计算的重叠" (work on
+ *   the outputs that are ready while the rest is still being computed); "Megatron-LM ... （六）" data flow
+ *   (+ shared experts).
+ *   Writes eout [rows,h] (and, when act_shared is not NULL, out_shared [T,h] of the shared expert, whose tiles run in
+ *   the same launch) exactly as moe_expert_down / moe_expert_down_shared, and y [T,h] bit-identical to
+ *   moe_combine(eout, dest_row, gates, out_shared or NULL): the tile that completes a token's 256-column block
+ *   sums that block from the token's rows in ascending j with fp32 fused multiply-adds, rounded once to bf16.
+ *   src_token [rows] int32 (moe_dispatch's; -1 for pads), dest_row / gates [T,k] as for moe_combine.
+ *   arrivals [T * ceil(h/256)] int32, size from moe_combine_arrivals_bytes: per-(token, column block) arrival
+ *   counters; they must be zero before the first call (e.g. one cudaMemsetAsync at allocation) and every call that
+ *   completes leaves them zero again. Two calls that may run at the same time must not share them. After a call
+ *   whose launch was cut short (moe_check_device_error reports MOE_ERR_TIMEOUT) zero them again.
+ *   bf16 only (MOE_ERR_UNSUPPORTED otherwise); tile_sched, packed_w, rows as moe_expert_down; act_shared /
+ *   packed_shared / out_shared all NULL or all set. All pointers 16-byte aligned.
+ * ------------------------------------------------------------------------------------------------- */
+size_t moe_combine_arrivals_bytes(int T, int h);
+int moe_expert_down_combine(const void* act, const int32_t* tile_sched, const void* packed_w, int E, int h, int F,
+                            int rows, const int32_t* src_token, const int32_t* dest_row, const float* gates, int T,
+                            int k, const void* act_shared, const void* packed_shared, int dtype, void* eout,
+                            void* out_shared, void* y, int32_t* arrivals, void* stream);
 
 /* ---------------------------------------------------------------------------------------------------
  * FP8 dispatch payload ("10.5 序列并行与专家并行", section 10.5.7: activations that cross nodes can travel in

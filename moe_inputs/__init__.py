@@ -85,6 +85,15 @@ CONFIGS = {
     # capacity) with F=1536, so that a full ncu capture of the grouped GEMM holds well under 1 GB on the device
     "page3_profile": MoEConfig("page3_profile", T=4096, h=4096, E=8, k=2, F=1536, gating=GATING_SOFTMAX, cf=1.25,
                                R=8, n_shared=0, dtype="bf16", alpha=0.01, bias="none"),
+    # profiling stand-in for the DeepSeek-V3-shaped layer's weight-streaming GEMMs: the same h, F, gating, shared
+    # expert and about the same rows per expert (k T / E = 128), with 32 experts, so that a full ncu capture of the
+    # grouped GEMMs holds ~3 GB of weights on the device (still far more than L2)
+    "deepseek_v3_profile": MoEConfig("deepseek_v3_profile", T=1024, h=7168, E=32, k=4, F=2048,
+                                     gating=GATING_SIGMOID_BIAS_RENORM, cf=0.0, R=8, n_shared=1, dtype="bf16",
+                                     alpha=0.01, bias="normal"),
+    # profiling stand-in for the Qwen3-MoE-shaped layer's router and dispatch: the same T, h, E, k, with F = 128
+    "qwen3_profile": MoEConfig("qwen3_profile", T=16384, h=2048, E=128, k=8, F=128, gating=GATING_SOFTMAX,
+                               cf=0.0, R=8, n_shared=0, dtype="bf16", alpha=0.01, bias="none"),
     # page-3 worked shape with the dispatch send buffer in FP8 (e4m3, one scale per token and 128 columns)
     "page3_fp8": MoEConfig("page3_fp8", T=4096, h=4096, E=8, k=2, F=12288, gating=GATING_SOFTMAX, cf=1.25, R=8,
                            n_shared=0, dtype="bf16", alpha=0.01, bias="none", payload="fp8"),

@@ -128,7 +128,7 @@ def y_tolerance(cfg):
     return (rel_max, 1e-5) if cfg.dtype == "f32" else (rel_l2, 2e-2)
 
 
-def build_gpu_layer(cfg, inp, wg, wu, wd, shared=None, device="cuda", backward=False):
+def build_gpu_layer(cfg, inp, wg, wu, wd, shared=None, device="cuda", backward=False, fuse_combine=False):
     import torch
     from top_routing_dispatch_moe_gb300.layer import MoELayer
     dev = torch.device(device)
@@ -139,7 +139,7 @@ def build_gpu_layer(cfg, inp, wg, wu, wd, shared=None, device="cuda", backward=F
     layer = MoELayer(T=cfg.T, h=cfg.h, E=cfg.E, k=cfg.k, F=cfg.F, gating=cfg.gating, cf=cfg.cf, R=cfg.R,
                      alpha=cfg.alpha, w_r=to_device(inp["w_r"], cfg, dev), bias=b, w_gate=to_device(wg, cfg, dev),
                      w_up=to_device(wu, cfg, dev), w_down=to_device(wd, cfg, dev), shared=sh, device=dev,
-                     routing=cfg.routing, backward=backward, payload=cfg.payload)
+                     routing=cfg.routing, backward=backward, payload=cfg.payload, fuse_combine=fuse_combine)
     return layer
 
 

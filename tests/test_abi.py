@@ -176,3 +176,34 @@ def test_binding_signatures_match_the_header(lib):
         else:   # declared but bound by hand in the binding: must at least be exported
             assert hasattr(lib.raw_lib(), name), name
     assert checked >= 40
+
+
+def test_host_checks_of_the_fused_combine(lib):
+    """moe_expert_down_combine: bf16 only, the shared expert's three pointers all or none, k in range, y aligned;
+    the arrival counters cover every (token, 256-column block)."""
+    raw = lib.raw_lib()
+    P = ctypes.c_void_p
+    n = None
+    ok, bad = P(0x1000), P(0x1003)
+    assert raw.moe_combine_arrivals_bytes(4096, 4096) == 4096 * 16 * 4
+    assert raw.moe_combine_arrivals_bytes(3, 264) % 256 == 0 and raw.moe_combine_arrivals_bytes(3, 264) >= 3 * 2 * 4
+    args = [ok, ok, ok, 8, 256, 128, 64, ok, ok, ok, 32, 2, n, n, lib.MOE_BF16, ok, n, ok, ok, n]
+    bf = list(args)
+    bf[14] = lib.MOE_F32
+    assert raw.moe_expert_down_combine(*bf) == lib.MOE_ERR_UNSUPPORTED
+    half = list(args)
+    half[12] = ok                                    # act_shared without packed_shared / out_shared
+    assert raw.moe_expert_down_combine(*half) == lib.MOE_ERR_INVALID_ARG
+    assert "all NULL or all set" in lib.moe_last_error_string()
+    kk = list(args)
+    kk[11] = 17
+    assert raw.moe_expert_down_combine(*kk) == lib.MOE_ERR_INVALID_ARG
+    yy = list(args)
+    yy[17] = bad
+    assert raw.moe_expert_down_combine(*yy) == lib.MOE_ERR_INVALID_ARG
+    nul = list(args)
+    nul[18] = n                                      # no arrival counters
+    assert raw.moe_expert_down_combine(*nul) == lib.MOE_ERR_INVALID_ARG
+    none = list(args)
+    none[10] = 0                                     # T = 0: nothing to do, nothing launched
+    assert raw.moe_expert_down_combine(*none) == lib.MOE_OK

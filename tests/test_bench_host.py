@@ -71,3 +71,35 @@ def test_reference_arm_json_line_on_cpu():
     env["RANK"] = "1"
     out = subprocess.run(cmd, cwd=root, env=env, capture_output=True, text=True, timeout=600)
     assert out.returncode == 0 and out.stdout.strip() == ""
+
+
+def test_lazy_weights_decode_one_expert_at_a_time():
+    """The further workloads' parity decodes expert weights on demand (the DeepSeek-V3-shaped workload's would
+    not fit in host memory as float64 all at once): the same values as the eager decode, one expert held."""
+    cfg = moe_inputs.get_config("deepseek_v3", T=64, h=64, F=32, E=16, k=4)
+    inp = bench.host_inputs(cfg)
+    eager = bench.decode_weights(cfg, inp)
+    lazy = bench.decode_weights(cfg, inp, lazy=True)
+    for e in [3, 0, 15, 3]:
+        for a, b in zip(lazy[e], eager[e]):
+            np.testing.assert_array_equal(a, b)
+        assert sorted(k for k in lazy if k != "shared") == [e]
+    for a, b in zip(lazy["shared"](), eager["shared"]()):
+        np.testing.assert_array_equal(a, b)
+
+
+def test_stage_metrics_bounds_and_bandwidths():
+    """Per-stage GB/s are the algorithmic bytes over the stage's mean time; the up/gate GEMM's bound is the
+    tensor peak for the page-3 shape and the HBM copy bandwidth for the DeepSeek-V3 shape (about one 128-row tile
+    per expert: fewer flops per weight byte than the ridge point)."""
+    st = {s: [0.01, 0.01] for s in ("router", "dispatch", "up_gate", "down", "combine")}
+    cfg = moe_inputs.get_config("page3_cf1.25")
+    m = bench.stage_metrics(cfg, st, kept=8192, active=8)
+    assert m["roofline"]["bound"] == "tensor" and m["roofline"]["unit"] == "TFLOP/s"
+    assert m["router_gbs"] == pytest.approx((cfg.T * cfg.h + cfg.h * cfg.E) * 2 / 1e-5 / 1e9)
+    assert m["dispatch_gbs"] == pytest.approx((cfg.T + 8192) * cfg.h * 2 / 1e-5 / 1e9)
+    assert m["combine_gbs"] == pytest.approx((8192 + cfg.T) * cfg.h * 2 / 1e-5 / 1e9)
+    ds = moe_inputs.get_config("deepseek_v3")
+    m = bench.stage_metrics(ds, st, kept=ds.k * ds.T, active=148)
+    assert m["roofline"]["bound"] == "hbm" and m["roofline"]["unit"] == "GB/s"
+    assert m["combine_gbs"] == pytest.approx((ds.k * ds.T + 2 * ds.T) * ds.h * 2 / 1e-5 / 1e9)

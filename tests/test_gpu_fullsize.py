@@ -46,15 +46,34 @@ def test_full_size_layer(name):
     shared = None
     if cfg.n_shared:
         shared = tuple(up(np.ascontiguousarray(a[0])[None]) for a in moe_inputs.all_expert_weights(cfg, shared=True))
+    # the separate combine (the configuration bench.py times); the fused one is checked bitwise against it below
+    fused = False
     layer = MoELayer(T=cfg.T, h=cfg.h, E=cfg.E, k=cfg.k, F=cfg.F, gating=cfg.gating, cf=cfg.cf, R=cfg.R,
                      alpha=cfg.alpha, w_r=up(inp["w_r"]),
                      bias=torch.from_numpy(inp["bias"]).to(dev) if inp["bias"] is not None else None,
-                     w_gate=up(wg), w_up=up(wu), w_down=up(wd), shared=shared, device=dev)
+                     w_gate=up(wg), w_up=up(wu), w_down=up(wd), shared=shared, device=dev, fuse_combine=fused)
     del wg, wu, wd, shared
     x = up(inp["x"])
     y = layer.forward(x)
     torch.cuda.synchronize()
     assert moe.moe_check_device_error() == moe.MOE_OK, moe.moe_last_error_string()
+    if cfg.dtype == "bf16":   # the down GEMM with the combine in its epilogue: the same eout and y bits
+        d = layer.d_out
+        arr = moe.moe_combine_arrivals(cfg.T, cfg.h, dev)
+        sh = bool(cfg.n_shared)
+        eout_f, sh_f, y_f = moe.moe_expert_down_combine(
+            layer.act, d["tile_sched"], layer.packed, cfg.E, cfg.h, d["src_token"], d["dest_row"],
+            layer.r_out["gates"], arr, act_shared=layer.sh_act if sh else None,
+            packed_shared=layer.shared_packed if sh else None)
+        torch.cuda.synchronize()
+        assert moe.moe_check_device_error() == moe.MOE_OK, moe.moe_last_error_string()
+        assert torch.equal(y_f.view(torch.int16), y.view(torch.int16)), f"{name}: fused combine differs"
+        live = d["src_token"] >= 0
+        assert torch.equal(eout_f[live].view(torch.int16), layer.eout[live].view(torch.int16))
+        if sh:
+            assert torch.equal(sh_f.view(torch.int16), layer.sh_out.view(torch.int16))
+        assert int(arr.abs().sum().item()) == 0
+        del eout_f, sh_f, y_f, arr
 
     # router: indices exact, floats within 1e-5
     ro = {k: v.cpu().numpy() for k, v in layer.r_out.items()}

@@ -26,10 +26,16 @@ def test_rejects_sizes_beyond_the_static_scratch():
 
 @pytest.mark.gpu
 @pytest.mark.parametrize("T,h,E,k,C,R", [(4096, 512, 8, 2, 1280, 8), (2000, 256, 128, 8, 0, 8),
-                                          (700, 512, 256, 8, 0, 8), (333, 128, 4, 2, 100, 2)])
+                                          (700, 512, 256, 8, 0, 8), (333, 128, 4, 2, 100, 2),
+                                          (262144, 64, 1024, 1, 0, 8)])
 def test_static_dispatch_matches_workspace_dispatch(T, h, E, k, C, R):
     """Two calls in a row with different inputs; each must equal moe_dispatch with a caller workspace
-    (indices and the copied payload bit-exactly)."""
+    (indices and the copied payload bit-exactly). The last size needs exactly the whole 1 MiB array (256 chunks of
+    1024 assignments x 1024 experts x 4 bytes) and takes the separate count / scan / scatter / copy launches, whose
+    scan rewrites the array's last words in place."""
+    from top_routing_dispatch_moe_gb300 import moe as _m
+    if T == 262144:
+        assert _m.raw_lib().moe_dispatch_workspace_size(T, E, k, C) == 1 << 20
     import torch
     from top_routing_dispatch_moe_gb300 import moe
     dev = "cuda"

@@ -4,6 +4,8 @@
 #include <string.h>
 #include <atomic>
 #include <mutex>
+#include <cuda.h>
+#include <cudaTypedefs.h>
 #include "common.cuh"
 
 namespace moe {
@@ -56,14 +58,40 @@ int num_sms() {
     return g_sms[dev];
 }
 
+unsigned long long context_id() {
+    static PFN_cuCtxGetCurrent_v4000 get_current = nullptr;
+    static PFN_cuCtxGetId_v12000 get_id = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &p, 4000, cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            get_current = reinterpret_cast<PFN_cuCtxGetCurrent_v4000>(p);
+        p = nullptr;
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetId", &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            get_id = reinterpret_cast<PFN_cuCtxGetId_v12000>(p);
+    });
+    if (!get_current || !get_id) return 0;
+    CUcontext c = nullptr;
+    if (get_current(&c) != CUDA_SUCCESS || !c) return 0;
+    unsigned long long id = 0;
+    return get_id(c, &id) == CUDA_SUCCESS ? id : 0;
+}
+
+static unsigned long long g_err_ctx[kMaxDevices];
+
 unsigned* device_error_word() {
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
     std::lock_guard<std::mutex> lk(g_mu);
-    if (!g_err_ptr[dev]) {
+    const unsigned long long ctx = context_id();
+    if (!g_err_ptr[dev] || ctx == 0 || g_err_ctx[dev] != ctx) {
         void* p = nullptr;
         if (cudaGetSymbolAddress(&p, g_error_word) != cudaSuccess) return nullptr;
         g_err_ptr[dev] = static_cast<unsigned*>(p);
+        g_err_ctx[dev] = context_id();       // the lookup above made the context current if there was none
     }
     return g_err_ptr[dev];
 }

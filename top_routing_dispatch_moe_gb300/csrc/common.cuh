@@ -18,6 +18,11 @@ int check_launch(const char* what);                       // MOE_ERR_CUDA if the
 int check_launch(cudaError_t launch_result, const char* what);   // the same for a launch that returned a status
 int num_sms();                                            // SM count of the current device (cached)
 unsigned* device_error_word();                            // device address of the error word (current device)
+// Unique id of the calling thread's current CUDA context (0: none, or the driver cannot tell). Per-device caches
+// of device addresses and kernel attributes keep the id they were filled under and are filled again when it
+// changes: after cudaDeviceReset a device gets a new primary context, in which the library's device variables
+// may sit at other addresses and kernel attributes are unset.
+unsigned long long context_id();
 long long wait_limit();                                   // iteration limit of bounded device waits
 
 inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }

@@ -14,7 +14,7 @@
 // its (at most k) destination rows with 16-byte loads and stores, reading x once. In capacity mode a
 // fifth kernel zero-fills the pad rows and marks them -1. For small count tables one launch after the
 // count does the scan, the ranking, the copy and the pad fill (dispatch_fused_kernel); its bf16 / fp32 row
-// copy goes through the bulk-copy unit (ring_copy_rows).
+// copy goes through the bulk-copy unit (ring_start / ring_finish).
 #include <algorithm>
 #include <mutex>
 #include <cuda_fp8.h>
@@ -51,54 +51,67 @@ __device__ __forceinline__ bool ring_wait(uint32_t bar, uint32_t parity, long lo
 
 // One thread copies ntok consecutive rows of row_bytes (a multiple of 16) from src to the destination rows
 // dest[tl * k + j] >= 0 of dst, piece by piece (pieces of at most SB bytes) through a ring of NS >= 2 shared
-// stages: every load in flight at once up to the ring's size, each piece stored to its k destinations as one
-// bulk group, a stage refilled once the group stored out of it has been read. A load that does not arrive
-// within `limit` polls latches a timeout; the loads still in flight are then waited for (up to kRingDrainLimit
-// polls each, whatever `limit` is, so that none lands in shared memory after the block has exited) and the
-// copy stops.
-__device__ void ring_copy_rows(const char* __restrict__ src, uint32_t row_bytes, int ntok, int k,
-                               const int* __restrict__ dest, char* __restrict__ dst, uint32_t ring, uint32_t bars,
-                               int NS, uint32_t SB, long long limit, unsigned* err) {
+// stages. ring_start initialises the stages' mbarriers and puts the first min(NS, pieces) loads in flight;
+// ring_finish then stores every piece to its k destinations as one bulk
+// group as soon as it has landed, refilling a stage once the group stored out of it has been read. A load that
+// does not arrive within `limit` polls latches a timeout; the loads still in flight are then waited for (up to
+// kRingDrainLimit polls each, whatever `limit` is, so that none lands in shared memory after the block has
+// exited) and the copy stops. If one of those drain waits runs out as well, site 0x111 is latched: that load may
+// still land in the shared memory of a block that has exited.
+struct RingCursor {
+    const char* src;
+    uint32_t row_bytes, SB, ring, bars;
+    int NS, n;                 // stages, pieces
+    int lt, lst, loaded;       // next piece to load: token, stage; pieces loaded so far
+    uint32_t loff;             // its byte offset in the row
+};
+
+__device__ __forceinline__ void ring_load_next(RingCursor& c) {
+    ring_load(c.ring + (uint32_t)c.lst * c.SB, c.src + (size_t)c.lt * c.row_bytes + c.loff,
+              min(c.SB, c.row_bytes - c.loff), c.bars + 8u * c.lst);
+    c.loff += c.SB;
+    if (c.loff >= c.row_bytes) { c.loff = 0; ++c.lt; }
+    if (++c.lst == c.NS) c.lst = 0;
+    ++c.loaded;
+}
+
+__device__ RingCursor ring_start(const char* __restrict__ src, uint32_t row_bytes, int ntok, uint32_t ring,
+                                 uint32_t bars, int NS, uint32_t SB) {
+    RingCursor c{src, row_bytes, SB, ring, bars, NS, ntok * (int)((row_bytes + SB - 1) / SB), 0, 0, 0, 0u};
     for (int st = 0; st < NS; ++st)
         asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(bars + 8u * st) : "memory");
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
-    const int n = ntok * (int)((row_bytes + SB - 1) / SB);      // pieces, in token order
-    // load cursor: next piece's token, byte offset in the row and stage; pieces are loaded in order
-    int lt = 0, lst = 0, loaded = 0;
-    uint32_t loff = 0;
-    auto load_next = [&]() {
-        ring_load(ring + (uint32_t)lst * SB, src + (size_t)lt * row_bytes + loff, min(SB, row_bytes - loff),
-                  bars + 8u * lst);
-        loff += SB;
-        if (loff >= row_bytes) { loff = 0; ++lt; }
-        if (++lst == NS) lst = 0;
-        ++loaded;
-    };
-    while (loaded < min(NS, n)) load_next();
+    while (c.loaded < min(NS, c.n)) ring_load_next(c);
+    return c;
+}
+
+__device__ void ring_finish(RingCursor& c, int k, const int* __restrict__ dest, char* __restrict__ dst,
+                            long long limit, unsigned* err) {
     // store cursor: piece i (token ct, offset coff) sits in stage cst, its load completing phase parity par
     int ct = 0, cst = 0;
     uint32_t coff = 0, par = 0;
-    for (int i = 0; i < n; ++i) {
-        if (!ring_wait(bars + 8u * cst, par, limit)) {
+    for (int i = 0; i < c.n; ++i) {
+        if (!ring_wait(c.bars + 8u * cst, par, limit)) {
             latch_device_error(err, kDevErrTimeout, 0x110u);
-            for (int q = i; q < loaded; ++q)
-                ring_wait(bars + 8u * (q % NS), (uint32_t)(q / NS) & 1u, kRingDrainLimit);
+            for (int q = i; q < c.loaded; ++q)
+                if (!ring_wait(c.bars + 8u * (q % c.NS), (uint32_t)(q / c.NS) & 1u, kRingDrainLimit))
+                    latch_device_error(err, kDevErrTimeout, 0x111u);   // a load may still land after the exit
             break;
         }
-        const uint32_t bytes = min(SB, row_bytes - coff);
-        const uint32_t from = ring + (uint32_t)cst * SB;
+        const uint32_t bytes = min(c.SB, c.row_bytes - coff);
+        const uint32_t from = c.ring + (uint32_t)cst * c.SB;
         for (int j = 0; j < k; ++j) {
             const int d = dest[ct * k + j];
-            if (d >= 0) ring_store(dst + (size_t)d * row_bytes + coff, from, bytes);
+            if (d >= 0) ring_store(dst + (size_t)d * c.row_bytes + coff, from, bytes);
         }
         asm volatile("cp.async.bulk.commit_group;" ::: "memory");
-        if (i >= 1 && loaded < n) {           // refill the stage of piece i - 1 (loaded == i - 1 + NS)
+        if (i >= 1 && c.loaded < c.n) {       // refill the stage of piece i - 1 (loaded == i - 1 + NS)
             asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory");
-            load_next();
+            ring_load_next(c);
         }
-        coff += SB;
-        if (coff >= row_bytes) { coff = 0; ++ct; }
-        if (++cst == NS) { cst = 0; par ^= 1u; }
+        coff += c.SB;
+        if (coff >= c.row_bytes) { coff = 0; ++ct; }
+        if (++cst == c.NS) { cst = 0; par ^= 1u; }
     }
     asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
 }
@@ -353,13 +366,15 @@ dispatch_fused_kernel(const T* __restrict__ x, const int32_t* __restrict__ ids, 
     int* s_rb = sm + fused_red(E);
     int* s_rt = s_rb + kChunkA;
     __shared__ int s_tmp[32];
+    const int t0 = blockIdx.x * tpc;
+    const int ntok = min(tpc, T_ - t0);
     {   // this chunk's token rows are known from the start: have L2 fetch them while the count table is summed
-        // and the chunk ranked (16-byte multiples: h % 8 == 0)
-        const int t0p = blockIdx.x * tpc, np = min(tpc, T_ - t0p);
+        // and the chunk ranked (16-byte multiples: h % 8 == 0). (Issuing the ring's bulk loads here instead was
+        // measured: the copy ended no sooner, the issuing thread reached the count table later.)
         const unsigned row_bytes = (unsigned)(h * sizeof(T));
-        for (int i = threadIdx.x; i < np; i += blockDim.x)
+        for (int i = threadIdx.x; i < ntok; i += blockDim.x)
             asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;"
-                         ::"l"(reinterpret_cast<uint64_t>(x + (size_t)(t0p + i) * h)), "r"(row_bytes) : "memory");
+                         ::"l"(reinterpret_cast<uint64_t>(x + (size_t)(t0 + i) * h)), "r"(row_bytes) : "memory");
     }
     pdl_wait();                               // the count table (dispatch_count_kernel) is complete from here on
     {   // count table -> this chunk's base and the per-expert totals: S slices of chunks per expert in
@@ -369,7 +384,18 @@ dispatch_fused_kernel(const T* __restrict__ x, const int32_t* __restrict__ ids, 
         const int tid = threadIdx.x, sl = tid / E, ex = tid - sl * E;
         if (sl < S) {
             int pb = 0, pt = 0;
-            for (int c = sl; c < nchunks; c += S) {
+            int c = sl;
+            for (; c + 3 * S < nchunks; c += 4 * S) {   // four loads in flight
+                int v[4];
+#pragma unroll
+                for (int u = 0; u < 4; ++u) v[u] = __ldg(chunk_counts + (size_t)(c + u * S) * E + ex);
+#pragma unroll
+                for (int u = 0; u < 4; ++u) {
+                    pt += v[u];
+                    pb += c + u * S < (int)blockIdx.x ? v[u] : 0;
+                }
+            }
+            for (; c < nchunks; c += S) {
                 const int v = __ldg(chunk_counts + (size_t)c * E + ex);
                 pt += v;
                 pb += c < (int)blockIdx.x ? v : 0;
@@ -396,8 +422,6 @@ dispatch_fused_kernel(const T* __restrict__ x, const int32_t* __restrict__ ids, 
 
     constexpr int V = Vec16<T>::N;
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    const int t0 = blockIdx.x * tpc;
-    const int ntok = min(tpc, T_ - t0);
     if constexpr (FP8) {
         for (int tl = warp; tl < ntok; tl += kChunkA / 32) {
             int dj[16];
@@ -407,29 +431,34 @@ dispatch_fused_kernel(const T* __restrict__ x, const int32_t* __restrict__ ids, 
         }
     } else if (threadIdx.x == 0 && ntok > 0) {
         // the rows move through the bulk-copy unit, issued by this one thread; the other warps fill pad rows
-        const uint32_t bars = shared_u32(sm) + (uint32_t)fused_bars_byte(E);
-        const uint32_t ring = (shared_u32(sm) + (uint32_t)fused_ring_byte(E) + 127u) & ~127u;
-        ring_copy_rows(reinterpret_cast<const char*>(x + (size_t)t0 * h), (uint32_t)(h * sizeof(T)), ntok, k, s_dest,
-                       reinterpret_cast<char*>(buf), ring, bars, ring_stages, stage_bytes, wait_limit, err);
+        RingCursor rc = ring_start(reinterpret_cast<const char*>(x + (size_t)t0 * h), (uint32_t)(h * sizeof(T)), ntok,
+                                   (shared_u32(sm) + (uint32_t)fused_ring_byte(E) + 127u) & ~127u,
+                                   shared_u32(sm) + (uint32_t)fused_bars_byte(E), ring_stages, stage_bytes);
+        ring_finish(rc, k, s_dest, reinterpret_cast<char*>(buf), wait_limit, err);
     }
     if (C > 0) {
-        // Pad rows, numbered in expert order, go round-robin to the grid's fill warps (all warps with the FP8
-        // payload, warps 1-31 of each block otherwise): pad row number q (q = pads of earlier experts + p)
-        // belongs to fill warp q mod W.
+        // Pad rows, numbered in expert order (q = pads of earlier experts + p), are spread evenly over the blocks
+        // and then over each block's fill warps (all warps with the FP8 payload, warps 1-31 otherwise): row q goes
+        // to fill warp (q mod grid) * FW + (q / grid) mod FW, so that every block fills about the same number.
         constexpr int FW = FP8 ? kChunkA / 32 : kChunkA / 32 - 1;
         if (!FP8 && warp == 0) return;
-        const long long W = (long long)gridDim.x * FW, g = (long long)blockIdx.x * FW + (FP8 ? warp : warp - 1);
-        long long run = 0;
+        const int G = gridDim.x, b = blockIdx.x, fw = FP8 ? warp : warp - 1;
+        const long long step = (long long)G * FW;
+        long long run = 0;                                // pads of earlier experts = rq * G + rr
+        int rq = 0, rr = 0;
         for (int ee = 0; ee < E; ++ee) {
             const int npad = C - s_kept[ee];
-            long long p = ((g - run) % W + W) % W;
-            for (; p < npad; p += W) {
-                const long long r = (long long)ee * C + s_kept[ee] + p;
+            // this warp's first pad row q >= run: q mod G == b (the first such row is in column a = q / G), then
+            // the first of a, a + 1, ... congruent to fw mod FW; after it every G * FW rows
+            const int a = rq + (b < rr ? 1 : 0);
+            const long long q1 = ((long long)a + ((fw - a % FW) % FW + FW) % FW) * G + b;
+            for (long long q = q1; q - run < npad; q += step) {
+                const long long r = (long long)ee * C + s_kept[ee] + (q - run);
                 if (lane == 0) { src_token[r] = -1; src_slot[r] = -1; }
                 if constexpr (FP8) {
                     for (int d0 = lane * 16; d0 < h; d0 += 32 * 16)
                         *reinterpret_cast<uint4*>(buf8 + r * h + d0) = make_uint4(0, 0, 0, 0);
-                    for (int b = lane; b < h / 128; b += 32) scales[r * (h / 128) + b] = 0.f;
+                    for (int sb = lane; sb < h / 128; sb += 32) scales[r * (h / 128) + sb] = 0.f;
                 } else {
                     Vec16<T> z;
                     z.v = {};
@@ -437,6 +466,9 @@ dispatch_fused_kernel(const T* __restrict__ x, const int32_t* __restrict__ ids, 
                 }
             }
             run += npad;
+            rq += npad / G;
+            rr += npad % G;
+            if (rr >= G) { rr -= G; ++rq; }
         }
     }
 }
@@ -684,7 +716,9 @@ extern "C" int moe_dense_tile_sched(int rows, int32_t* tile_sched, void* stream)
 // The array is a file-scope __device__ variable: every GPU that loads the library holds it until the process
 // exits. Its host-side name is only a stand-in for the symbol, never a device address, so the first call on
 // each device, with that device current, looks its address up with cudaGetSymbolAddress and caches it; make
-// that first call on a device before capturing a stream on it. All calls share the one array: calls whose
+// that first call on a device before capturing a stream on it. The cache remembers the context it was filled in
+// and a call in another context (after cudaDeviceReset, say) looks the address up again, so make the first
+// call after a reset before any capture as well. All calls share the one array: calls whose
 // kernels may overlap on the GPU (different streams, no ordering between them) race on it and must be
 // serialised by the caller. Nothing in the array has to start at zero: every call writes each word before it
 // reads it, so the contents left by the previous call do not matter.
@@ -694,6 +728,7 @@ constexpr size_t kStaticScratchBytes = (size_t)1 << 20;     // 1 MiB: ceil(T / (
 static __device__ __align__(256) int32_t g_dispatch_scratch[kStaticScratchBytes / sizeof(int32_t)];
 static std::mutex g_static_mu;
 static void* g_static_ptr[64];
+static unsigned long long g_static_ctx[64];     // the context the address was looked up in, per device
 }  // namespace moe
 
 extern "C" int moe_dispatch_static(const void* x, const int32_t* topk_ids, int T, int h, int E, int k, int capacity,
@@ -713,12 +748,14 @@ extern "C" int moe_dispatch_static(const void* x, const int32_t* topk_ids, int T
     void* scratch = nullptr;
     {
         std::lock_guard<std::mutex> lk(moe::g_static_mu);
-        if (!moe::g_static_ptr[dev]) {
+        const unsigned long long ctx = moe::context_id();
+        if (!moe::g_static_ptr[dev] || ctx == 0 || moe::g_static_ctx[dev] != ctx) {
             void* p = nullptr;
             e = cudaGetSymbolAddress(&p, moe::g_dispatch_scratch);
             MOE_REQUIRE(e == cudaSuccess && p, MOE_ERR_CUDA, "moe_dispatch_static: cudaGetSymbolAddress failed: %s",
                         cudaGetErrorString(e));
             moe::g_static_ptr[dev] = p;
+            moe::g_static_ctx[dev] = moe::context_id();
         }
         scratch = moe::g_static_ptr[dev];
     }

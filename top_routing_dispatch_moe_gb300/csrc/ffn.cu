@@ -87,6 +87,35 @@ extern "C" int moe_expert_down_shared(const void* act, const int32_t* tile_sched
                        packed_shared, out_shared);
 }
 
+extern "C" size_t moe_combine_arrivals_bytes(int T, int h) {
+    if (T < 0 || h <= 0) return 0;
+    return align_up((size_t)T * cdiv(h, 256) * sizeof(int32_t), 256);
+}
+
+extern "C" int moe_expert_down_combine(const void* act, const int32_t* tile_sched, const void* packed_w, int E, int h,
+                                       int F, int rows, const int32_t* src_token, const int32_t* dest_row,
+                                       const float* gates, int T, int k, const void* act_shared,
+                                       const void* packed_shared, int dtype, void* eout, void* out_shared, void* y,
+                                       int32_t* arrivals, void* stream) {
+    const char* fn = "moe_expert_down_combine";
+    if (int rc = ffn_check(fn, act, tile_sched, packed_w, E, h, F, rows, dtype, eout)) return rc;
+    MOE_REQUIRE(dtype == MOE_BF16, MOE_ERR_UNSUPPORTED, "%s: bf16 only (fp32: moe_expert_down, then moe_combine)", fn);
+    MOE_REQUIRE(T >= 0 && k >= 1 && k <= 16 && k <= E, MOE_ERR_INVALID_ARG, "%s: T=%d k=%d E=%d", fn, T, k, E);
+    const bool has_sh = act_shared != nullptr;
+    MOE_REQUIRE(has_sh == (packed_shared != nullptr) && has_sh == (out_shared != nullptr), MOE_ERR_INVALID_ARG,
+                "%s: act_shared, packed_shared and out_shared must be all NULL or all set", fn);
+    if (has_sh) {
+        if (int rc = shared_check(fn, tile_sched, act_shared, T, packed_shared, out_shared, dtype)) return rc;
+    }
+    MOE_REQUIRE(T == 0 || (dest_row && gates && y && arrivals), MOE_ERR_INVALID_ARG, "%s: null pointer", fn);
+    MOE_REQUIRE(rows == 0 || src_token, MOE_ERR_INVALID_ARG, "%s: null src_token", fn);
+    MOE_REQUIRE(aligned16(y), MOE_ERR_INVALID_ARG, "%s: y must be 16-byte aligned", fn);
+    if (T == 0) return MOE_OK;                 // no token: nothing to combine, and no routed row either
+    return ffn_tc_down_combine(act, tile_sched, packed_w, E, h, F, rows, eout, static_cast<cudaStream_t>(stream),
+                               has_sh ? act_shared : nullptr, has_sh ? T : 0, packed_shared, out_shared, src_token,
+                               dest_row, gates, T, k, y, arrivals);
+}
+
 extern "C" int moe_expert_up_gate_fp8(const uint8_t* buf8, const float* scales, const int32_t* tile_sched,
                                       const void* packed_w, int E, int h, int F, int rows, void* act, void* stream) {
     MOE_REQUIRE(E >= 1 && E <= 1024 && h > 0 && h % 128 == 0 && F > 0 && F % 8 == 0 && rows >= 0, MOE_ERR_INVALID_ARG,

@@ -55,6 +55,14 @@ int ffn_tc_down(const void* act, const int32_t* sched, const void* packed, int E
                 cudaStream_t s, const void* act_sh = nullptr, int T_sh = 0, const void* packed_sh = nullptr,
                 void* out_sh = nullptr);
 
+// The down GEMM with the combine fused into its epilogue: eout (and out_sh) as ffn_tc_down, plus
+// y [T][h] = out_sh[t] (when T_sh > 0) + sum over kept j ascending of gates[t][j] eout[dest_row[t][j]], bit-identical
+// to moe_combine. arrivals [T][cdiv(h, 256)] int32: zero on entry, zero again once the launch has completed.
+int ffn_tc_down_combine(const void* act, const int32_t* sched, const void* packed, int E, int h, int F, int rows,
+                        void* eout, cudaStream_t s, const void* act_sh, int T_sh, const void* packed_sh, void* out_sh,
+                        const int32_t* src_token, const int32_t* dest_row, const float* gates, int T, int k, void* y,
+                        int32_t* arrivals);
+
 // Up/gate GEMM on the FP8 send buffer (e4m3 codes + per-row, per-128-column scales), dequantised in the prologue.
 int ffn_tc_up_gate_fp8(const uint8_t* buf8, const float* scales, const int32_t* sched, const void* packed, int E, int h,
                        int F, int rows, void* act, cudaStream_t s);

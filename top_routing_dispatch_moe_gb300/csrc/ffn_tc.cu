@@ -216,7 +216,10 @@ __host__ __device__ constexpr uint32_t idesc_bf16() {
 // act gradient, writes the gate and up pre-activation gradients in the packed column order).
 // EPI_SWIGLU_SAVE: EPI_SWIGLU that also stores the pre-activations (Params::gu_out / sh_gu_out); a separate
 // instantiation, so that the plain forward carries no trace of it.
-enum Epi : int { EPI_SWIGLU = 0, EPI_BF16 = 1, EPI_F32 = 2, EPI_SWIGLU_BWD = 3, EPI_SWIGLU_SAVE = 4 };
+// EPI_BF16_COMBINE: the plain bf16 epilogue of the down GEMM, after which the tile that completes a token's
+// column block also combines it into y (combine_arrive).
+enum Epi : int { EPI_SWIGLU = 0, EPI_BF16 = 1, EPI_F32 = 2, EPI_SWIGLU_BWD = 3, EPI_SWIGLU_SAVE = 4, EPI_BF16_COMBINE = 5 };
+__host__ __device__ constexpr bool plain_bf16(int epi) { return epi == EPI_BF16 || epi == EPI_BF16_COMBINE; }
 
 struct Params {
     const int32_t* sched;
@@ -254,6 +257,16 @@ struct Params {
     // packed gate/up column order (block n: 128 columns of g, then the u of the same f)
     __nv_bfloat16* gu_out;
     __nv_bfloat16* sh_gu_out;
+    // EPI_BF16_COMBINE: the down GEMM of the routed rows (and of the shared expert's T = sh_rows rows, if any) also
+    // combines them. cmb_src [rows]: token of each dispatched row (-1: pad); cmb_dest / cmb_gates [T][k]: the rows
+    // and gates of each token's choices (-1: dropped); cmb_y [T][h] out; cmb_cnt [T][NT]: arrival counters, zero on
+    // entry and zero again when the launch completes.
+    const int32_t* cmb_src;
+    const int32_t* cmb_dest;
+    const float* cmb_gates;
+    __nv_bfloat16* cmb_y;
+    int* cmb_cnt;
+    int cmb_T, cmb_k;
 };
 
 // K range of part / expert e in the weight-gradient mapping.
@@ -425,8 +438,8 @@ __device__ __forceinline__ void store_tile(const Params& p, __nv_bfloat16* out, 
                 }
             }
         }
-    } else {                                 // EPI_BF16
-        static_assert(EPI == EPI_BF16, "the fp32 epilogue stores through TMA (store_tile_f32_tma)");
+    } else {                                 // EPI_BF16, EPI_BF16_COMBINE
+        static_assert(plain_bf16(EPI), "the fp32 epilogue stores through TMA (store_tile_f32_tma)");
 #pragma unroll 1
         for (int j = 0; j < BN / 32; ++j) {
             float v[32];
@@ -493,6 +506,134 @@ __device__ __forceinline__ void store_tile_f32_tma(const Params& p, const CUtens
             tma_store_3d(map, box, n0, row0, grp);
             bulk_commit();
         }
+    }
+}
+
+// ---------------------------------------------------------------------------------------------------
+// Combine fused into the down GEMM's epilogue ("v6 长序列和 MoE", table row "combine": the k expert outputs of a
+// token, weighted by their gates, summed back at its position; "专家并行" (formulaic), section "通信与计算的重叠":
+// start on the outputs that are ready while the rest is still being computed)
+// ---------------------------------------------------------------------------------------------------
+// Column block n (256 columns) of y[t] needs block n of each kept expert row of t, and of t's shared-expert row
+// when the launch has one: need(t) = kept choices (+ 1). Once an epilogue warp's 32 rows of block n are in memory,
+// each row adds one arrival to the counter of (its token, n); the row that brings the count to need(t) makes its
+// warp combine that block: y = shared + sum over kept j, ascending, of gate_j * eout[dest_j], fp32 fused
+// multiply-adds in that fixed order and one rounding to bf16 -- the arithmetic of moe_combine, so the result is
+// bit-identical to it whatever order the tiles finish in. That warp then resets the counter to zero.
+// Ordering: a row's values reach memory (the warp's TMA stores completed and proxy-fenced, or the thread's own
+// stores), a gpu-scope fence, then the relaxed atomic arrival; the last arriver's warp fences before it reads
+// the other rows, through L2 (they were written during this launch).
+__device__ __forceinline__ void fence_proxy_async_global() { asm volatile("fence.proxy.async.global;" ::: "memory"); }
+
+__device__ __forceinline__ int combine_need(const Params& p, int t) {
+    int need = p.sh_rows > 0 ? 1 : 0;
+    const int32_t* d = p.cmb_dest + (size_t)t * p.cmb_k;
+    for (int j = 0; j < p.cmb_k; ++j) need += __ldg(d + j) >= 0 ? 1 : 0;
+    return need;
+}
+
+// Whole warp: block n of y for up to G tokens tt[g] (< 0: none), one 16-byte chunk of 8 columns per lane, every
+// load of the round (shared row and up to KM expert rows per token) in flight before the first use.
+template <int G, int KM>
+__device__ __forceinline__ void combine_tokens(const Params& p, const int (&tt)[G], int n) {
+    const int lane = threadIdx.x & 31, h = p.n_valid, k = p.cmb_k;
+    const int c = n * 256 + lane * 8;
+    if (c >= h) return;
+    int dj[G][KM];
+    float gj[G][KM];
+#pragma unroll
+    for (int g = 0; g < G; ++g)
+#pragma unroll
+        for (int j = 0; j < KM; ++j) {
+            const bool ok = tt[g] >= 0 && j < k;
+            dj[g][j] = ok ? __ldg(p.cmb_dest + (size_t)tt[g] * k + j) : -1;
+            gj[g][j] = ok ? __ldg(p.cmb_gates + (size_t)tt[g] * k + j) : 0.f;
+        }
+    uint4 sv[G], v[G][KM];
+#pragma unroll
+    for (int g = 0; g < G; ++g) {
+        sv[g] = make_uint4(0, 0, 0, 0);
+        if (tt[g] >= 0 && p.sh_rows > 0) sv[g] = __ldcg(reinterpret_cast<const uint4*>(p.sh_out + (size_t)tt[g] * h + c));
+#pragma unroll
+        for (int j = 0; j < KM; ++j)
+            if (dj[g][j] >= 0) v[g][j] = __ldcg(reinterpret_cast<const uint4*>(p.out + (size_t)dj[g][j] * h + c));
+    }
+#pragma unroll
+    for (int g = 0; g < G; ++g) {
+        if (tt[g] < 0) continue;
+        Vec16<__nv_bfloat16> s;
+        s.v = sv[g];
+        float acc[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) acc[i] = p.sh_rows > 0 ? s.get(i) : 0.f;
+#pragma unroll
+        for (int j = 0; j < KM; ++j) {
+            if (dj[g][j] < 0) continue;
+            Vec16<__nv_bfloat16> e;
+            e.v = v[g][j];
+#pragma unroll
+            for (int i = 0; i < 8; ++i) acc[i] = fmaf(gj[g][j], e.get(i), acc[i]);
+        }
+        Vec16<__nv_bfloat16> o;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) o.set(i, acc[i]);
+        st16(p.cmb_y + (size_t)tt[g] * h + c, o);
+    }
+}
+
+// The warp's 32 rows [row0 + lane_base, + 32) of column block n are in memory: one arrival per valid row, then the
+// warp combines every block it completed, G tokens per round.
+template <int G, int KM>
+__device__ __forceinline__ void combine_rounds(const Params& p, unsigned m, int t, int n) {
+    const int lane = threadIdx.x & 31;
+    while (m) {
+        int tt[G];
+#pragma unroll
+        for (int g = 0; g < G; ++g) {
+            tt[g] = -1;
+            if (m) {
+                const int src = __ffs(m) - 1;
+                m &= m - 1;
+                tt[g] = __shfl_sync(0xffffffffu, t, src);
+            }
+        }
+        combine_tokens<G, KM>(p, tt, n);
+#pragma unroll
+        for (int g = 0; g < G; ++g)
+            if (lane == g && tt[g] >= 0) p.cmb_cnt[(size_t)tt[g] * p.NT + n] = 0;
+    }
+}
+
+__device__ __forceinline__ void combine_arrive(const Params& p, int row0, int row1, bool sh, int n, int lane_base) {
+    const int lane = threadIdx.x & 31;
+    const int row = row0 + lane_base + lane;
+    int t = -1;
+    if (row < row1) t = sh ? row : __ldg(p.cmb_src + row);
+    bool last = false;
+    if (t >= 0) {
+        __threadfence();
+        const int old = atomicAdd(p.cmb_cnt + (size_t)t * p.NT + n, 1);
+        last = old == combine_need(p, t) - 1;
+    }
+    __threadfence();
+    const unsigned m = __ballot_sync(0xffffffffu, last);
+    if (!m) return;
+    const int k = p.cmb_k;
+    if (k <= 2) combine_rounds<4, 2>(p, m, t, n);
+    else if (k <= 8) combine_rounds<2, 8>(p, m, t, n);
+    else combine_rounds<1, 16>(p, m, t, n);
+}
+
+// Tokens with no kept choice and no shared expert receive no arrival: y = 0 for them, written by the epilogue
+// warps before their first tile (warp gw of nw).
+__device__ __forceinline__ void combine_zero_dropped(const Params& p, int gw, int nw) {
+    if (p.sh_rows > 0) return;
+    const int lane = threadIdx.x & 31, h = p.n_valid, k = p.cmb_k;
+    for (int t = gw; t < p.cmb_T; t += nw) {
+        const bool kept = lane < k && __ldg(p.cmb_dest + (size_t)t * k + lane) >= 0;
+        if (__any_sync(0xffffffffu, kept)) continue;
+        for (int c = lane * 8; c < h; c += 256)
+            *reinterpret_cast<uint4*>(p.cmb_y + (size_t)t * h + c) = make_uint4(0, 0, 0, 0);
     }
 }
 
@@ -667,6 +808,7 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
         const int lane_base = 32 * (warp & 3);
         int iter = 0;
         uint32_t nbox = 0;                       // fp32 epilogue: store boxes issued by this warp
+        if constexpr (EPI == EPI_BF16_COMBINE) combine_zero_dropped(p, blockIdx.x * 4 + (warp & 3), gridDim.x * 4);
         for (int w = blockIdx.x; w < total; w += gridDim.x, ++iter) {
             const int a = iter & 1;
             const uint32_t aph = (iter >> 1) & 1;
@@ -690,14 +832,25 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
                 }
                 store_tile_f32_tma<BN>(p, om, tbase, wk.n, orow, grp, wk.nkb == 0, orow < lim,
                                        s_out + (uint32_t)(warp & 3) * EPI_STG_WARP_BYTES, nbox);
-            } else if constexpr (!A8 && EPI == EPI_BF16) {
+            } else if constexpr (!A8 && plain_bf16(EPI)) {
                 const int row0w = wk.row0 + lane_base;
-                if (row0w + 31 < wk.row1) {              // all 32 rows valid: TMA stores
+                const bool boxed = row0w + 31 < wk.row1;
+                if (boxed) {                             // all 32 rows valid: TMA stores
                     store_tile_bf16_tma<BN>(p, wk.sh ? &tmO2 : &tmO, tbase, wk.n, row0w,
                                             s_out + (uint32_t)(warp & 3) * EPI_BF16_BOX_BYTES);
                 } else {
                     const int row = row0w + lane;
                     store_tile<EPI, BN>(p, wk.sh ? p.sh_out : p.out, tbase, row, row < wk.row1, wk.n);
+                }
+                if constexpr (EPI == EPI_BF16_COMBINE) {
+                    // the accumulator is read: hand it back first, then make the rows visible and arrive
+                    tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(tempty(a));
+                    if (boxed && lane == 0) { bulk_wait_all(); fence_proxy_async_global(); }
+                    __syncwarp();
+                    combine_arrive(p, wk.row0, wk.row1, wk.sh != 0, wk.n, lane_base);
+                    continue;
                 }
             } else {
                 const int row = wk.row0 + lane_base + lane;
@@ -1020,6 +1173,7 @@ grouped_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_c
         const uint32_t tempty_leader = map_rank(tempty(0), 0);
         int iter = 0;
         uint32_t nbox = 0;                       // fp32 epilogue: store boxes issued by this warp
+        if constexpr (EPI == EPI_BF16_COMBINE) combine_zero_dropped(p, blockIdx.x * 4 + (warp & 3), gridDim.x * 4);
         for (int w = cid; w < total; w += NC, ++iter) {
             const int a = iter & 1;
             const uint32_t aph = (iter >> 1) & 1;
@@ -1042,14 +1196,25 @@ grouped_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_c
                 }
                 store_tile_f32_tma<BN>(p, om, tbase, wk.n, orow, grp, wk.nkb == 0, orow < lim,
                                        s_out + (uint32_t)(warp & 3) * EPI_STG_WARP_BYTES, nbox);
-            } else if constexpr (EPI == EPI_BF16) {
+            } else if constexpr (plain_bf16(EPI)) {
                 const int row0w = wk.row0 + lane_base;
-                if (row0w + 31 < wk.row1) {              // all 32 rows valid: TMA stores
+                const bool boxed = row0w + 31 < wk.row1;
+                if (boxed) {                             // all 32 rows valid: TMA stores
                     store_tile_bf16_tma<BN>(p, wk.sh ? &tmO2 : &tmO, tbase, wk.n, row0w,
                                             s_box + (uint32_t)(warp & 3) * EPI_BF16_BOX_BYTES);
                 } else {
                     const int row = row0w + lane;
                     store_tile<EPI, BN>(p, wk.sh ? p.sh_out : p.out, tbase, row, row < wk.row1, wk.n);
+                }
+                if constexpr (EPI == EPI_BF16_COMBINE) {
+                    // the accumulator is read: hand it back first, then make the rows visible and arrive
+                    tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive_cluster(tempty_leader + 8u * a);
+                    if (boxed && lane == 0) { bulk_wait_all(); fence_proxy_async_global(); }
+                    __syncwarp();
+                    combine_arrive(p, wk.row0, wk.row1, wk.sh != 0, wk.n, lane_base);
+                    continue;
                 }
             } else {
                 const int row = wk.row0 + lane_base + lane;
@@ -1157,7 +1322,7 @@ static int make_out_maps(const Params& p, long long a_rows, const CUtensorMap& m
         }
         *o2 = *o1;
     }
-    if constexpr (EPI == EPI_BF16) {
+    if constexpr (plain_bf16(EPI)) {
         if (p.out && a_rows > 0)
             if (int rc = make_map_bf16_out(o1, p.out, a_rows, p.n_valid, p.ldo)) return rc;
         if (p.sh_out && p.sh_rows > 0)
@@ -1206,15 +1371,16 @@ template <int EPI>
 static int gemm_a8(const void* a8, long long a_rows, const void* b, long long b_rows_total, const Params& p,
                    cudaStream_t s) {
     using CF = Wide;
-    static bool attr_set[64];
+    static unsigned long long attr_ctx[64];  // context in which the attribute was set, per device
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64)
         return set_error(MOE_ERR_CUDA, "grouped_gemm (e4m3): no usable current device");
-    if (!attr_set[dev]) {
+    const unsigned long long ctx = context_id();
+    if (ctx == 0 || attr_ctx[dev] != ctx) {
         cudaError_t e = cudaFuncSetAttribute(grouped_gemm_kernel<EPI, CF, true>,
                                              cudaFuncAttributeMaxDynamicSharedMemorySize, CF::SMEM_BYTES_A8);
         if (e != cudaSuccess) return set_error(MOE_ERR_CUDA, "grouped_gemm (e4m3) smem attribute: %s", cudaGetErrorString(e));
-        attr_set[dev] = true;
+        attr_ctx[dev] = context_id();
     }
     CUtensorMap ma, mb;
     if (int rc = make_map_u8(&ma, a8, a_rows, p.K, BM)) return rc;
@@ -1227,20 +1393,21 @@ static int gemm_a8(const void* a8, long long a_rows, const void* b, long long b_
 template <int EPI, class CF>
 static int gemm(const void* a, long long a_rows, const void* b, long long b_rows_total, const Params& p,
                 cudaStream_t s, const SharedOperands& sh = SharedOperands{}) {
-    static bool attr_set[64];                // the attribute belongs to the kernel in each device's context
+    static unsigned long long attr_ctx[64];  // the attribute belongs to the kernel in each device's context
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64)
         return set_error(MOE_ERR_CUDA, "grouped_gemm: no usable current device");
-    constexpr bool kBox16 = EPI == EPI_BF16;
+    constexpr bool kBox16 = plain_bf16(EPI);
     constexpr int smem_bytes = EPI == EPI_F32 ? 1024 + CF::STAGES * CF::STAGE_BYTES + 1024 + EPI_STG_BYTES
                                : kBox16       ? 1024 + CF::STAGES * CF::STAGE_BYTES + 1024 + 4 * EPI_BF16_BOX_BYTES
                                               : CF::SMEM_BYTES;
     static_assert(smem_bytes <= 227 * 1024, "shared memory per CTA");
-    if (!attr_set[dev]) {
+    const unsigned long long ctx = context_id();
+    if (ctx == 0 || attr_ctx[dev] != ctx) {
         cudaError_t e = cudaFuncSetAttribute(grouped_gemm_kernel<EPI, CF>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                              smem_bytes);
         if (e != cudaSuccess) return set_error(MOE_ERR_CUDA, "grouped_gemm smem attribute: %s", cudaGetErrorString(e));
-        attr_set[dev] = true;
+        attr_ctx[dev] = context_id();
     }
     const long long routed_rows = a_rows;
     if (a_rows == 0) { a = sh.a; a_rows = p.sh_rows; b = sh.b; b_rows_total = sh.b_rows; }   // no routed items
@@ -1259,6 +1426,7 @@ static int gemm(const void* a, long long a_rows, const void* b, long long b_rows
     return check_launch(EPI == EPI_SWIGLU ? "grouped_gemm_kernel<up_gate>"
                         : EPI == EPI_SWIGLU_SAVE ? "grouped_gemm_kernel<up_gate, save>"
                         : EPI == EPI_BF16 ? "grouped_gemm_kernel<bf16>"
+                        : EPI == EPI_BF16_COMBINE ? "grouped_gemm_kernel<bf16, combine>"
                         : EPI == EPI_SWIGLU_BWD ? "grouped_gemm_kernel<swiglu_bwd>" : "grouped_gemm_kernel<f32>");
 }
 
@@ -1267,14 +1435,16 @@ template <int EPI>
 static int gemm_pair(const void* a, long long a_rows, const void* b, long long b_rows_total, const Params& p,
                      cudaStream_t s, const SharedOperands& sh = SharedOperands{}) {
     static int clusters[64];                 // resident pairs per device, 0 = not yet queried
+    static unsigned long long clusters_ctx[64];   // the context they were queried (and the attribute set) in
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64)
         return set_error(MOE_ERR_CUDA, "grouped_gemm_pair: no usable current device");
-    constexpr bool kBox16 = EPI == EPI_BF16;
+    constexpr bool kBox16 = plain_bf16(EPI);
     constexpr int smem_bytes = EPI == EPI_F32 ? PAIR_SMEM_BYTES_F32 : kBox16 ? PAIR_SMEM_BYTES_BF16 : PAIR_SMEM_BYTES;
     MOE_REQUIRE(EPI != EPI_F32 || p.wg_E > 0, MOE_ERR_INVALID_ARG,
                 "grouped_gemm_pair: the fp32 epilogue runs the weight-gradient mapping only");
-    if (!clusters[dev]) {
+    const unsigned long long ctx = context_id();
+    if (!clusters[dev] || ctx == 0 || clusters_ctx[dev] != ctx) {
         cudaError_t e = cudaFuncSetAttribute(grouped_gemm_pair_kernel<EPI>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                              smem_bytes);
         if (e != cudaSuccess) return set_error(MOE_ERR_CUDA, "grouped_gemm_pair smem attribute: %s", cudaGetErrorString(e));
@@ -1287,6 +1457,7 @@ static int gemm_pair(const void* a, long long a_rows, const void* b, long long b
         if (e != cudaSuccess || n <= 0)
             return set_error(MOE_ERR_CUDA, "grouped_gemm_pair: no resident cluster of two CTAs (%s)", cudaGetErrorString(e));
         clusters[dev] = std::min(n, num_sms() / 2);
+        clusters_ctx[dev] = context_id();
     }
     const long long routed_rows = a_rows;
     if (a_rows == 0) { a = sh.a; a_rows = p.sh_rows; b = sh.b; b_rows_total = sh.b_rows; }   // no routed items
@@ -1305,7 +1476,9 @@ static int gemm_pair(const void* a, long long a_rows, const void* b, long long b
     return check_launch(EPI == EPI_SWIGLU ? "grouped_gemm_pair_kernel<up_gate>"
                         : EPI == EPI_SWIGLU_SAVE ? "grouped_gemm_pair_kernel<up_gate, save>"
                         : EPI == EPI_SWIGLU_BWD ? "grouped_gemm_pair_kernel<swiglu_bwd>"
-                        : EPI == EPI_F32 ? "grouped_gemm_pair_kernel<f32>" : "grouped_gemm_pair_kernel<bf16>");
+                        : EPI == EPI_F32 ? "grouped_gemm_pair_kernel<f32>"
+                        : EPI == EPI_BF16_COMBINE ? "grouped_gemm_pair_kernel<bf16, combine>"
+                                                  : "grouped_gemm_pair_kernel<bf16>");
 }
 
 // The 2-SM kernel when the average expert has at least four 128-row tiles (an odd tile count costs a
@@ -1351,6 +1524,34 @@ int ffn_tc_down(const void* act, const int32_t* sched, const void* packed, int E
                                 (long long)h};
     if (tc::use_pair(E, rows)) return tc::gemm_pair<tc::EPI_BF16>(act, rows, b, (long long)E * h, p, s, sh);
     return tc::gemm<tc::EPI_BF16, CF>(act, rows, b, (long long)E * h, p, s, sh);
+}
+
+// The down GEMM with the combine in its epilogue (EPI_BF16_COMBINE): eout and out_sh as ffn_tc_down writes them,
+// and y [T][h] = out_sh[t] (if any) + sum over kept j of gates[t][j] eout[dest_row[t][j]]; arrivals [T][cdiv(h, 256)]
+// int32 must be zero on entry and are zero again when the launch has completed.
+int ffn_tc_down_combine(const void* act, const int32_t* sched, const void* packed, int E, int h, int F, int rows,
+                        void* eout, cudaStream_t s, const void* act_sh, int T_sh, const void* packed_sh, void* out_sh,
+                        const int32_t* src_token, const int32_t* dest_row, const float* gates, int T, int k, void* y,
+                        int32_t* arrivals) {
+    const PackedLayout L = packed_layout(E, h, F, 2);
+    const PackedLayout Ls = packed_layout(1, h, F, 2);
+    unsigned* err = device_error_word();
+    MOE_REQUIRE(err, MOE_ERR_CUDA, "device error word unavailable");
+    using CF = tc::Wide;
+    tc::Params p{sched, F, cdiv(h, CF::BN), h, h, h, static_cast<__nv_bfloat16*>(eout), nullptr, nullptr, err,
+                 wait_limit(), T_sh, static_cast<__nv_bfloat16*>(out_sh)};
+    p.cmb_src = src_token;
+    p.cmb_dest = dest_row;
+    p.cmb_gates = gates;
+    p.cmb_y = static_cast<__nv_bfloat16*>(y);
+    p.cmb_cnt = arrivals;
+    p.cmb_T = T;
+    p.cmb_k = k;
+    const char* b = static_cast<const char*>(packed) + L.down_off;
+    const tc::SharedOperands sh{act_sh, packed_sh ? static_cast<const char*>(packed_sh) + Ls.down_off : nullptr,
+                                (long long)h};
+    if (tc::use_pair(E, rows)) return tc::gemm_pair<tc::EPI_BF16_COMBINE>(act, rows, b, (long long)E * h, p, s, sh);
+    return tc::gemm<tc::EPI_BF16_COMBINE, CF>(act, rows, b, (long long)E * h, p, s, sh);
 }
 
 // Up/gate GEMM + SwiGLU on the FP8 send buffer: A = e4m3 codes [rows, h] with per-row, per-128-column fp32

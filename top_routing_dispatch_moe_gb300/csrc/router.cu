@@ -46,16 +46,55 @@ __host__ __device__ inline bool bias_in_logits(int gating) {
     return gating == MOE_GATING_SOFTMAX || gating == MOE_GATING_SOFTMAX_RENORM;
 }
 
-// Gating of one token whose NPL-per-lane logits are in L (expert of slot i = lane + 32 i).
+// Max / sum over the SEG lanes of this lane's segment (SEG = 32: the warp; 16: its half), a fixed butterfly order.
+// For E <= 16 the lanes 16-31 of a whole-warp gating hold zeros, so the half-warp sums are the same bits.
+template <int SEG>
+__device__ __forceinline__ float seg_max(float v) {
+#pragma unroll
+    for (int o = SEG / 2; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+    return v;
+}
+template <int SEG>
+__device__ __forceinline__ float seg_sum(float v) {
+#pragma unroll
+    for (int o = SEG / 2; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+    return v;
+}
+template <int SEG>
+__device__ __forceinline__ unsigned seg_umax(unsigned v) {
+    if constexpr (SEG == 32) {
+        return __reduce_max_sync(0xffffffffu, v);
+    } else {
+#pragma unroll
+        for (int o = SEG / 2; o > 0; o >>= 1) v = max(v, __shfl_xor_sync(0xffffffffu, v, o));
+        return v;
+    }
+}
+template <int SEG>
+__device__ __forceinline__ unsigned seg_umin(unsigned v) {
+    if constexpr (SEG == 32) {
+        return __reduce_min_sync(0xffffffffu, v);
+    } else {
+#pragma unroll
+        for (int o = SEG / 2; o > 0; o >>= 1) v = min(v, __shfl_xor_sync(0xffffffffu, v, o));
+        return v;
+    }
+}
+
+// Gating of one token whose NPL-per-lane logits are in L (expert of slot i = sl + 32 i, sl the lane's index in its
+// segment of SEG lanes; with SEG = 16 each half-warp gates its own token, NPL = 1 and E <= 16). Every lane of the
+// warp must call it (the reductions are shuffles); a segment with valid = false writes and accumulates nothing.
 // Accumulates the token's router probabilities into Pacc and its choices into the shared histogram.
-template <int NPL>
+template <int NPL, int SEG = 32>
 __device__ __forceinline__ void gate_token(float (&L)[NPL], int t, int E, int k, int gating, const float* bias,
-                                           const GateOut& o, float (&Pacc)[NPL], int* s_hist) {
+                                           const GateOut& o, float (&Pacc)[NPL], int* s_hist, bool valid = true) {
+    static_assert(SEG == 32 || (SEG == 16 && NPL == 1), "half-warp gating holds one expert per lane");
     const int lane = threadIdx.x & 31;
+    const int sl = lane & (SEG - 1), seg0 = lane - sl;
     float score[NPL], prob[NPL];
     bool live[NPL];
 #pragma unroll
-    for (int i = 0; i < NPL; ++i) live[i] = (lane + 32 * i) < E;
+    for (int i = 0; i < NPL; ++i) live[i] = valid && (sl + 32 * i) < E;
 
     if (gating == MOE_GATING_SIGMOID_BIAS_RENORM) {
         float s_sum = 0.f;
@@ -63,30 +102,36 @@ __device__ __forceinline__ void gate_token(float (&L)[NPL], int t, int E, int k,
         for (int i = 0; i < NPL; ++i) {
             float s = live[i] ? 1.f / (1.f + expf(-L[i])) : 0.f;
             prob[i] = s;                                   // sigmoid value, normalised below
-            score[i] = live[i] ? s + (bias ? bias[lane + 32 * i] : 0.f) : -INFINITY;
+            score[i] = live[i] ? s + (bias ? bias[sl + 32 * i] : 0.f) : -INFINITY;
             s_sum += s;
         }
-        s_sum = warp_sum(s_sum);
+        s_sum = seg_sum<SEG>(s_sum);
         float inv = 1.f / s_sum;
+        if (valid) {
 #pragma unroll
-        for (int i = 0; i < NPL; ++i) Pacc[i] += prob[i] * inv;
+            for (int i = 0; i < NPL; ++i) Pacc[i] += prob[i] * inv;
+        }
     } else {
         float m = -INFINITY;
 #pragma unroll
         for (int i = 0; i < NPL; ++i) if (live[i]) m = fmaxf(m, L[i]);
-        m = warp_max(m);
+        m = seg_max<SEG>(m);
         float z = 0.f;
         const bool selbias = gating == MOE_GATING_SOFTMAX_SELBIAS && bias;
 #pragma unroll
         for (int i = 0; i < NPL; ++i) {
             prob[i] = live[i] ? expf(L[i] - m) : 0.f;
             z += prob[i];
-            score[i] = live[i] ? L[i] + (selbias ? bias[lane + 32 * i] : 0.f) : -INFINITY;
+            score[i] = live[i] ? L[i] + (selbias ? bias[sl + 32 * i] : 0.f) : -INFINITY;
         }
-        z = warp_sum(z);
+        z = seg_sum<SEG>(z);
         float inv = 1.f / z;
 #pragma unroll
-        for (int i = 0; i < NPL; ++i) { prob[i] *= inv; Pacc[i] += prob[i]; }
+        for (int i = 0; i < NPL; ++i) prob[i] *= inv;
+        if (valid) {
+#pragma unroll
+            for (int i = 0; i < NPL; ++i) Pacc[i] += prob[i];
+        }
     }
 
     // k rounds of warp argmax on the selection score, on order-preserving keys: a warp max reduction finds the
@@ -103,14 +148,14 @@ __device__ __forceinline__ void gate_token(float (&L)[NPL], int t, int E, int k,
             unsigned lm = key[0];
 #pragma unroll
             for (int i = 1; i < NPL; ++i) lm = max(lm, key[i]);
-            const unsigned m = __reduce_max_sync(0xffffffffu, lm);
+            const unsigned m = seg_umax<SEG>(lm);
             unsigned li = 0xffffffffu;
 #pragma unroll
             for (int i = NPL - 1; i >= 0; --i)
-                if (key[i] == m) li = (unsigned)(lane + 32 * i);
-            int bi = (int)__reduce_min_sync(0xffffffffu, li);
+                if (key[i] == m) li = (unsigned)(sl + 32 * i);
+            int bi = (int)seg_umin<SEG>(li);
             if (bi >= E) bi = E - 1;          // only reachable with NaN scores: keeps every index in bounds
-            const int owner = bi & 31, slot = bi >> 5;
+            const int owner = seg0 + (bi & 31), slot = bi >> 5;
             float pv = 0.f;
 #pragma unroll
             for (int i = 0; i < NPL; ++i) {
@@ -126,7 +171,7 @@ __device__ __forceinline__ void gate_token(float (&L)[NPL], int t, int E, int k,
     const float norm = (gating == MOE_GATING_SOFTMAX || gating == MOE_GATING_SOFTMAX_SELBIAS) ? 1.f : 1.f / psum;
 #pragma unroll
     for (int j = 0; j < kMaxK; ++j) {
-        if (j < k && lane == j) {
+        if (valid && j < k && sl == j) {
             o.ids[(size_t)t * k + j] = sel_id[j];
             o.gates[(size_t)t * k + j] = sel_p[j] * norm;
             atomicAdd(&s_hist[sel_id[j]], 1);
@@ -329,11 +374,21 @@ __device__ __forceinline__ void mma_bf16_16816(float (&d)[4], uint32_t a0, uint3
 // the 8 lanes of a 16-byte load phase (two W rows, four column groups) hit distinct banks.
 __host__ __device__ inline int mma_wt_stride(int h) { return ((h + 31) / 32 * 32 * 2 + 127) / 128 * 64 + 32; }
 
-template <int NB, int U>   // NB blocks of 8 experts (E <= 8 NB); U chunks of 32 columns in flight per warp
+// Token row t of x [T][h] into L2 (nothing for t outside [0, T)); the row is a multiple of 16 bytes.
+__device__ __forceinline__ void prefetch_row_l2(const __nv_bfloat16* x, int T_, int h, int t) {
+    if (t >= 0 && t < T_)
+        asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;"
+                     ::"l"(reinterpret_cast<uint64_t>(x + (size_t)t * h)), "r"((unsigned)(h * 2)) : "memory");
+}
+
+template <int NB, int U>   // NB blocks of 8 experts (E <= 8 NB); 2 x U chunks of 32 columns in flight per warp
 __global__ void __launch_bounds__(kRouterWarps * 32, 2)
 router_mma_kernel(const __nv_bfloat16* __restrict__ x, const __nv_bfloat16* __restrict__ w_r,
-                  const float* __restrict__ bias, int T_, int h, int E, int k, int gating, GateOut o) {
+                  const __nv_bfloat16* __restrict__ w_rT, const float* __restrict__ bias, int T_, int h, int E, int k,
+                  int gating, GateOut o) {
     pdl_trigger();                            // the finalize may launch now (it waits for this kernel's partials)
+    // (an L2 prefetch of the block's first 16 token rows here was measured: the router weight's staging then
+    // queued behind it, and the x loads ended no sooner)
     constexpr int EP = 8 * NB;
     extern __shared__ __align__(16) unsigned char smem_raw[];
     const int stride = mma_wt_stride(h);
@@ -351,7 +406,26 @@ router_mma_kernel(const __nv_bfloat16* __restrict__ x, const __nv_bfloat16* __re
     // keeps 8 vector loads in flight.
     const int d0 = c_begin * 32, d1 = min(h, c_end * 32), dz = c_end * 32;
     const __nv_bfloat16 zero = __float2bfloat16_rn(0.f);
-    if (E == EP) {
+    if (w_rT) {
+        // the packed transpose W_r^T [E][h]: each row's slice is contiguous, copied with 16-byte vectors (d0 and h
+        // are multiples of 8 elements, the shared row stride a multiple of 16 bytes); rows e >= E are zero
+        const int vpr = (d1 - d0) / 8, nvec = EP * vpr;
+        constexpr int B = 8;
+        for (int v0 = lane; v0 < nvec; v0 += 32 * B) {
+            uint4 r[B];
+#pragma unroll
+            for (int b = 0; b < B; ++b) {
+                const int v = v0 + 32 * b, e = v / max(vpr, 1);
+                r[b] = make_uint4(0, 0, 0, 0);
+                if (v < nvec && e < E) r[b] = __ldg(reinterpret_cast<const uint4*>(w_rT + (size_t)e * h + d0) + (v - e * vpr));
+            }
+#pragma unroll
+            for (int b = 0; b < B; ++b) {
+                const int v = v0 + 32 * b, e = v / max(vpr, 1);
+                if (v < nvec) *reinterpret_cast<uint4*>(wT + (size_t)e * stride + d0 + 8 * (v - e * vpr)) = r[b];
+            }
+        }
+    } else if (E == EP) {
         const int nvec = (d1 - d0) * EP / 8;
         const uint4* src = reinterpret_cast<const uint4*>(w_r + (size_t)d0 * EP);
         constexpr int B = 8;
@@ -384,38 +458,50 @@ router_mma_kernel(const __nv_bfloat16* __restrict__ x, const __nv_bfloat16* __re
     float Pacc[1] = {0.f};
     const bool use_bias_in_logits = bias && bias_in_logits(gating);
     const int ntiles = (T_ + kMmaTokens - 1) / kMmaTokens;
+    auto load = [&](uint4 (&xa)[U], uint4 (&xb)[U], const __nv_bfloat16* x0, const __nv_bfloat16* x1, int c0) {
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+            const int d = (c0 + u) * 32 + 8 * t;
+            if (c0 + u < c_end && d < h) {
+                xa[u] = __ldcs(reinterpret_cast<const uint4*>(x0 + d));
+                xb[u] = __ldcs(reinterpret_cast<const uint4*>(x1 + d));
+            } else {
+                xa[u] = make_uint4(0, 0, 0, 0);
+                xb[u] = make_uint4(0, 0, 0, 0);
+            }
+        }
+    };
+    auto compute = [&](float (&acc)[NB][4], const uint4 (&xa)[U], const uint4 (&xb)[U], int c0) {
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+            if (c0 + u < c_end) {
+#pragma unroll
+                for (int nb = 0; nb < NB; ++nb) {
+                    const uint4 wv = *reinterpret_cast<const uint4*>(wT + (size_t)(8 * nb + g) * stride +
+                                                                    (c0 + u) * 32 + 8 * t);
+                    mma_bf16_16816(acc[nb], xa[u].x, xb[u].x, xa[u].y, xb[u].y, wv.x, wv.y);
+                    mma_bf16_16816(acc[nb], xa[u].z, xb[u].z, xa[u].w, xb[u].w, wv.z, wv.w);
+                }
+            }
+        }
+    };
     for (int tile = blockIdx.x; tile < ntiles; tile += gridDim.x) {
         const int tok0 = tile * kMmaTokens;
+        // the next tile of this block goes to L2 while this one is computed (the first one was prefetched at entry)
+        if (threadIdx.x < kMmaTokens && tile + (int)gridDim.x < ntiles) prefetch_row_l2(x, T_, h, tok0 + (int)gridDim.x * kMmaTokens + threadIdx.x);
         const __nv_bfloat16* x0 = x + (size_t)min(tok0 + g, T_ - 1) * h;          // rows past T: any valid row,
         const __nv_bfloat16* x1 = x + (size_t)min(tok0 + g + 8, T_ - 1) * h;      // their logits are not used
         float acc[NB][4];
 #pragma unroll
         for (int nb = 0; nb < NB; ++nb) acc[nb][0] = acc[nb][1] = acc[nb][2] = acc[nb][3] = 0.f;
-        for (int c0 = c_begin; c0 < c_end; c0 += U) {
-            uint4 xa[U], xb[U];
-#pragma unroll
-            for (int u = 0; u < U; ++u) {
-                const int d = (c0 + u) * 32 + 8 * t;
-                if (c0 + u < c_end && d < h) {
-                    xa[u] = __ldcs(reinterpret_cast<const uint4*>(x0 + d));
-                    xb[u] = __ldcs(reinterpret_cast<const uint4*>(x1 + d));
-                } else {
-                    xa[u] = make_uint4(0, 0, 0, 0);
-                    xb[u] = make_uint4(0, 0, 0, 0);
-                }
-            }
-#pragma unroll
-            for (int u = 0; u < U; ++u) {
-                if (c0 + u < c_end) {
-#pragma unroll
-                    for (int nb = 0; nb < NB; ++nb) {
-                        const uint4 wv = *reinterpret_cast<const uint4*>(wT + (size_t)(8 * nb + g) * stride +
-                                                                        (c0 + u) * 32 + 8 * t);
-                        mma_bf16_16816(acc[nb], xa[u].x, xb[u].x, xa[u].y, xb[u].y, wv.x, wv.y);
-                        mma_bf16_16816(acc[nb], xa[u].z, xb[u].z, xa[u].w, xb[u].w, wv.z, wv.w);
-                    }
-                }
-            }
+        // two register buffers of U chunks: the loads of one are in flight while the other is multiplied
+        uint4 a0[U], b0[U], a1[U], b1[U];
+        load(a0, b0, x0, x1, c_begin);
+        for (int c0 = c_begin; c0 < c_end; c0 += 2 * U) {
+            load(a1, b1, x0, x1, c0 + U);
+            compute(acc, a0, b0, c0);
+            load(a0, b0, x0, x1, c0 + 2 * U);
+            compute(acc, a1, b1, c0 + U);
         }
         // D fragment: rows g and g + 8 (tokens), columns 2t, 2t + 1 of each 8-expert block
 #pragma unroll
@@ -427,34 +513,53 @@ router_mma_kernel(const __nv_bfloat16* __restrict__ x, const __nv_bfloat16* __re
             r[(g + 8) * EP + 1] = acc[nb][3];
         }
         __syncthreads();
-        // gating: warp w takes tokens 2w and 2w + 1 of the tile; its lane e sums expert e over the 8 slices
-#pragma unroll
-        for (int j = 2 * warp; j < 2 * warp + 2; ++j) {
+        // gating of the tile's 16 tokens: with E <= 16 warp w gates tokens 2w (lanes 0-15) and 2w + 1 (lanes
+        // 16-31) at once, one expert per lane; otherwise the two one after the other, lane e holding expert e.
+        // Lane e sums expert e's partial logits over the 8 warps' slices in slice order.
+        if constexpr (EP <= 16) {
+            const int j = 2 * warp + (lane >> 4), e = lane & 15;
             const int tok = tok0 + j;
-            if (tok >= T_) break;
+            const bool tv = tok < T_;
             float L[1] = {-INFINITY};
-            if (lane < E) {
+            if (tv && e < E) {
                 float v = 0.f;
 #pragma unroll
-                for (int w = 0; w < kRouterWarps; ++w) v += red[((size_t)w * kMmaTokens + j) * EP + lane];
-                L[0] = v + (use_bias_in_logits ? bias[lane] : 0.f);
-                if (o.logits) o.logits[(size_t)tok * E + lane] = L[0];
+                for (int w = 0; w < kRouterWarps; ++w) v += red[((size_t)w * kMmaTokens + j) * EP + e];
+                L[0] = v + (use_bias_in_logits ? bias[e] : 0.f);
+                if (o.logits) o.logits[(size_t)tok * E + e] = L[0];
             }
-            gate_token<1>(L, tok, E, k, gating, bias, o, Pacc, s_hist);
+            gate_token<1, 16>(L, tv ? tok : 0, E, k, gating, bias, o, Pacc, s_hist, tv);
+        } else {
+#pragma unroll
+            for (int j = 2 * warp; j < 2 * warp + 2; ++j) {
+                const int tok = tok0 + j;
+                if (tok >= T_) break;
+                float L[1] = {-INFINITY};
+                if (lane < E) {
+                    float v = 0.f;
+#pragma unroll
+                    for (int w = 0; w < kRouterWarps; ++w) v += red[((size_t)w * kMmaTokens + j) * EP + lane];
+                    L[0] = v + (use_bias_in_logits ? bias[lane] : 0.f);
+                    if (o.logits) o.logits[(size_t)tok * E + lane] = L[0];
+                }
+                gate_token<1>(L, tok, E, k, gating, bias, o, Pacc, s_hist);
+            }
         }
         __syncthreads();                      // red is rewritten by the next tile
     }
+    if constexpr (EP <= 16) Pacc[0] += __shfl_down_sync(0xffffffffu, Pacc[0], 16);   // expert e: lanes e and e + 16
     flush_partials<1>(Pacc, E, s_P, s_hist, o);
 }
 
 // ---------------------------------------------------------------------------------------------------
 // E > 32: logits GEMM (fp32 accumulation, CUDA cores), then the gating kernel
 // ---------------------------------------------------------------------------------------------------
-// C[T,E] = x[T,h] @ W[h,E] (+ bias in softmax modes). 64x64 tiles, 16-deep K steps, 4x4 per thread.
+// C[T,E] = x[T,h] @ W[h,E] (+ bias in softmax modes). 64x64 tiles, 16-deep K steps, 4x4 per thread. w_kmajor: w is
+// the transpose W^T [E][h] (the packed router weight) instead of W [h][E].
 template <typename T>
 __global__ void __launch_bounds__(256)
 router_logits_gemm(const T* __restrict__ x, const T* __restrict__ w, const float* __restrict__ bias, int T_, int h,
-                   int E, float* __restrict__ out) {
+                   int E, float* __restrict__ out, int w_kmajor) {
     __shared__ float As[16][64 + 4];
     __shared__ float Bs[16][64 + 4];
     const int tx = threadIdx.x & 15, ty = threadIdx.x >> 4;
@@ -467,7 +572,7 @@ router_logits_gemm(const T* __restrict__ x, const T* __restrict__ w, const float
             As[c][r] = (gm < T_ && gk < h) ? to_f32(x[(size_t)gm * h + gk]) : 0.f;
             int kr = i / 64, nc = i % 64;                   // B: k kr, col nc
             int bk = k0 + kr, bn = n0 + nc;
-            Bs[kr][nc] = (bk < h && bn < E) ? to_f32(w[(size_t)bk * E + bn]) : 0.f;
+            Bs[kr][nc] = (bk < h && bn < E) ? to_f32(w_kmajor ? w[(size_t)bn * h + bk] : w[(size_t)bk * E + bn]) : 0.f;
         }
         __syncthreads();
 #pragma unroll
@@ -564,11 +669,11 @@ router_gate_kernel(const float* __restrict__ logits, int nparts, size_t part_str
 }
 
 // Counts, f, P and aux from the per-block partials of `grid` gating blocks. Each block takes chunks of
-// kFinExperts experts (block b: chunks b, b + gridDim.x, ...); thread (s, e) of its [S][chunk] arrangement sums
-// the partials of gating blocks s, s + S, s + 2S, ... of expert e, and the S slice sums of each expert are added
-// in slice order. Every block adds its experts' f_e P_e in expert order; with several blocks, the last one to
-// arrive (counted on `ticket`, which the gating kernel zeroed) adds the blocks' sums in block order. No step
-// depends on timing, so the results are the same on every run.
+// kFinExperts experts (block b: chunks b, b + gridDim.x, ...); thread (s, e) of its [S][chunk] arrangement (S a
+// power of two) sums the partials of gating blocks s, s + S, s + 2S, ... of expert e, and the S slice sums of each
+// expert are added by a pairwise tree over the slices. Every block adds its experts' f_e P_e in expert order; with
+// several blocks, the last one to arrive (counted on `ticket`, which the gating kernel zeroed) adds the blocks'
+// sums in block order. No step depends on timing, so the results are the same on every run.
 constexpr int kFinExperts = 32;
 __global__ void __launch_bounds__(1024)
 router_finalize(const float* __restrict__ partial_P, const int32_t* __restrict__ partial_C, int grid, int T_, int E,
@@ -582,7 +687,8 @@ router_finalize(const float* __restrict__ partial_P, const int32_t* __restrict__
     float term = 0.f;                                    // thread 0: this block's sum of f_e P_e
     for (int e0 = blockIdx.x * kFinExperts; e0 < E; e0 += gridDim.x * kFinExperts) {
         const int ew = min(kFinExperts, E - e0);
-        const int S = (int)blockDim.x / ew;
+        int S = 1;
+        while (2 * S * ew <= (int)blockDim.x) S *= 2;
         const int s = tid / ew, e = e0 + tid % ew;
         float ps[4] = {0.f, 0.f, 0.f, 0.f};
         int cs[4] = {0, 0, 0, 0};
@@ -602,11 +708,14 @@ router_finalize(const float* __restrict__ partial_P, const int32_t* __restrict__
         }
         s_p[tid] = (ps[0] + ps[1]) + (ps[2] + ps[3]);
         s_c[tid] = cs[0] + cs[1] + cs[2] + cs[3];
+        for (int st = S / 2; st > 0; st >>= 1) {         // pairwise tree over the slices, a fixed order
+            __syncthreads();
+            if (s < st) { s_p[tid] += s_p[tid + st * ew]; s_c[tid] += s_c[tid + st * ew]; }
+        }
         __syncthreads();
         if (tid < ew) {
-            float tp = 0.f;
-            int tc = 0;
-            for (int q = 0; q < S; ++q) { tp += s_p[q * ew + tid]; tc += s_c[q * ew + tid]; }
+            const float tp = s_p[tid];
+            const int tc = s_c[tid];
             const int ee = e0 + tid;
             const float Pe = T_ > 0 ? tp / (float)T_ : 0.f;
             const float fe = T_ > 0 ? (float)tc / ((float)k * (float)T_) : 0.f;
@@ -737,18 +846,20 @@ extern "C" size_t moe_router_workspace_size(int T, int h, int E, int k, int dtyp
     return router_ws_layout(nullptr, T, h, E, el, small, !small, tc, router_split(T, h, E, tc).S).bytes;
 }
 
-extern "C" int moe_router(const void* x, const void* w_r, const float* bias, int T, int h, int E, int k, int dtype,
-                          int gating, float alpha, float* logits, int32_t* topk_ids, float* gates, int32_t* counts,
-                          float* f, float* P, float* aux, void* ws, size_t ws_bytes, void* stream) {
+// The router on w_r [h][E], or (bf16, w_r null) on the packed transpose w_rT [E][h] of moe_pack_router_weight,
+// which spares the tensor-core path its per-call transpose and the fused small-E kernel its scattered staging.
+static int router_run(const void* x, const void* w_r, const void* w_rT, const float* bias, int T, int h, int E, int k,
+                      int dtype, int gating, float alpha, float* logits, int32_t* topk_ids, float* gates,
+                      int32_t* counts, float* f, float* P, float* aux, void* ws, size_t ws_bytes, void* stream) {
     MOE_REQUIRE(dtype == MOE_F32 || dtype == MOE_BF16, MOE_ERR_UNSUPPORTED, "moe_router: dtype %d", dtype);
     MOE_REQUIRE(gating >= MOE_GATING_SOFTMAX && gating <= MOE_GATING_SOFTMAX_SELBIAS, MOE_ERR_UNSUPPORTED,
                 "moe_router: gating mode %d", gating);
     MOE_REQUIRE(T >= 0 && h > 0 && h % 8 == 0, MOE_ERR_INVALID_ARG, "moe_router: T=%d h=%d (need T>=0, h%%8==0)", T, h);
     MOE_REQUIRE(E >= 1 && E <= 1024 && k >= 1 && k <= E && k <= kMaxK, MOE_ERR_INVALID_ARG,
                 "moe_router: E=%d k=%d (need 1<=k<=min(E,16), E<=1024)", E, k);
-    MOE_REQUIRE(w_r && counts && f && P && aux && (T == 0 || (x && topk_ids && gates)), MOE_ERR_INVALID_ARG,
+    MOE_REQUIRE((w_r || w_rT) && counts && f && P && aux && (T == 0 || (x && topk_ids && gates)), MOE_ERR_INVALID_ARG,
                 "moe_router: null pointer");
-    MOE_REQUIRE(aligned16(x) && aligned16(w_r) && aligned16(logits), MOE_ERR_INVALID_ARG,
+    MOE_REQUIRE(aligned16(x) && aligned16(w_r) && aligned16(w_rT) && aligned16(logits), MOE_ERR_INVALID_ARG,
                 "moe_router: x, w_r and logits must be 16-byte aligned");
     const int el = dtype == MOE_F32 ? 4 : 2;
     const bool small = use_small_path(h, E, el);
@@ -765,13 +876,14 @@ extern "C" int moe_router(const void* x, const void* w_r, const float* bias, int
             const size_t smem = mma_smem_bytes(h, E);
             const __nv_bfloat16* xb = static_cast<const __nv_bfloat16*>(x);
             const __nv_bfloat16* wb = static_cast<const __nv_bfloat16*>(w_r);
+            const __nv_bfloat16* wtb = static_cast<const __nv_bfloat16*>(w_rT);
 #define MOE_MMA_LAUNCH(NB, UU)                                                                                \
             cudaFuncSetAttribute(router_mma_kernel<NB, UU>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem); \
-            router_mma_kernel<NB, UU><<<G, kRouterWarps * 32, smem, s>>>(xb, wb, bias, T, h, E, k, gating, o);
+            router_mma_kernel<NB, UU><<<G, kRouterWarps * 32, smem, s>>>(xb, wb, wtb, bias, T, h, E, k, gating, o);
             switch (mma_blocks(E)) {
-                case 1: { MOE_MMA_LAUNCH(1, 8) } break;
-                case 2: { MOE_MMA_LAUNCH(2, 8) } break;
-                default: { MOE_MMA_LAUNCH(4, 4) } break;
+                case 1: { MOE_MMA_LAUNCH(1, 4) } break;
+                case 2: { MOE_MMA_LAUNCH(2, 4) } break;
+                default: { MOE_MMA_LAUNCH(4, 2) } break;
             }
 #undef MOE_MMA_LAUNCH
             if (int rc = check_launch("router_mma_kernel")) return rc;
@@ -791,23 +903,27 @@ extern "C" int moe_router(const void* x, const void* w_r, const float* bias, int
             float* lg = sp.S > 1 ? w.parts : logits ? logits : w.logits;
             const float* lbias = bias_in_logits(gating) ? bias : nullptr;
             if (tc) {
-                router_transpose_kernel<__nv_bfloat16><<<dim3(cdiv(E, 32), cdiv(h, 32)), dim3(32, 8), 0, s>>>(
-                    static_cast<const __nv_bfloat16*>(w_r), h, E, static_cast<__nv_bfloat16*>(w.w_rT));
-                if (int rc = check_launch("router_transpose_kernel")) return rc;
+                const void* wt = w_rT;
+                if (!wt) {                           // not packed: transpose into the workspace on every call
+                    router_transpose_kernel<__nv_bfloat16><<<dim3(cdiv(E, 32), cdiv(h, 32)), dim3(32, 8), 0, s>>>(
+                        static_cast<const __nv_bfloat16*>(w_r), h, E, static_cast<__nv_bfloat16*>(w.w_rT));
+                    if (int rc = check_launch("router_transpose_kernel")) return rc;
+                    wt = w.w_rT;
+                }
                 if (sp.S > 1) {
-                    if (int rc = tc_gemm_f32_splitk(x, T, h, 0, w.w_rT, E, h, 0, h, sp.S, sp.kchunk, lg, s)) return rc;
+                    if (int rc = tc_gemm_f32_splitk(x, T, h, 0, wt, E, h, 0, h, sp.S, sp.kchunk, lg, s)) return rc;
                 } else {
                     if (int rc = launch_dense_sched(T, w.sched, s)) return rc;
-                    if (int rc = tc_router_logits(x, w.w_rT, lbias, T, h, E, w.sched, lg, s)) return rc;
+                    if (int rc = tc_router_logits(x, wt, lbias, T, h, E, w.sched, lg, s)) return rc;
                 }
             } else {
                 dim3 grid(cdiv(E, 64), cdiv(T, 64));
                 if (dtype == MOE_BF16)
                     router_logits_gemm<__nv_bfloat16><<<grid, 256, 0, s>>>(static_cast<const __nv_bfloat16*>(x),
-                        static_cast<const __nv_bfloat16*>(w_r), lbias, T, h, E, lg);
+                        static_cast<const __nv_bfloat16*>(w_r ? w_r : w_rT), lbias, T, h, E, lg, w_r ? 0 : 1);
                 else
                     router_logits_gemm<float><<<grid, 256, 0, s>>>(static_cast<const float*>(x),
-                        static_cast<const float*>(w_r), lbias, T, h, E, lg);
+                        static_cast<const float*>(w_r), lbias, T, h, E, lg, 0);
                 if (int rc = check_launch("router_logits_gemm")) return rc;
             }
             const size_t smem = (size_t)kRouterWarps * E * sizeof(float) + (size_t)E * sizeof(int);
@@ -832,6 +948,46 @@ extern "C" int moe_router(const void* x, const void* w_r, const float* bias, int
                                       (const float*)w.partial_P, (const int32_t*)w.partial_C, T > 0 ? G : 0, T, E, k,
                                       alpha, counts, f, P, aux, w.term_part, w.ticket);
     return check_launch(le, "router_finalize");
+}
+
+extern "C" int moe_router(const void* x, const void* w_r, const float* bias, int T, int h, int E, int k, int dtype,
+                          int gating, float alpha, float* logits, int32_t* topk_ids, float* gates, int32_t* counts,
+                          float* f, float* P, float* aux, void* ws, size_t ws_bytes, void* stream) {
+    return router_run(x, w_r, nullptr, bias, T, h, E, k, dtype, gating, alpha, logits, topk_ids, gates, counts, f, P,
+                      aux, ws, ws_bytes, stream);
+}
+
+extern "C" size_t moe_router_packed_bytes(int h, int E, int dtype) {
+    if (h <= 0 || E <= 0) return 0;
+    return align_up((size_t)h * E * (dtype == MOE_F32 ? 4 : 2), 256);
+}
+
+extern "C" int moe_pack_router_weight(const void* w_r, int h, int E, int dtype, void* packed, void* stream) {
+    MOE_REQUIRE(dtype == MOE_F32 || dtype == MOE_BF16, MOE_ERR_UNSUPPORTED, "moe_pack_router_weight: dtype %d", dtype);
+    MOE_REQUIRE(h > 0 && h % 8 == 0 && E >= 1 && E <= 1024, MOE_ERR_INVALID_ARG, "moe_pack_router_weight: h=%d E=%d", h,
+                E);
+    MOE_REQUIRE(w_r && packed && aligned16(w_r) && aligned16(packed), MOE_ERR_INVALID_ARG,
+                "moe_pack_router_weight: null or misaligned pointer");
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (dtype == MOE_F32) {                  // the fp32 kernels read w_r as it is
+        const cudaError_t e = cudaMemcpyAsync(packed, w_r, (size_t)h * E * 4, cudaMemcpyDeviceToDevice, s);
+        MOE_REQUIRE(e == cudaSuccess, MOE_ERR_CUDA, "moe_pack_router_weight: %s", cudaGetErrorString(e));
+        return MOE_OK;
+    }
+    router_transpose_kernel<__nv_bfloat16><<<dim3(cdiv(E, 32), cdiv(h, 32)), dim3(32, 8), 0, s>>>(
+        static_cast<const __nv_bfloat16*>(w_r), h, E, static_cast<__nv_bfloat16*>(packed));
+    return check_launch("router_transpose_kernel");
+}
+
+extern "C" int moe_router_packed(const void* x, const void* w_packed, const float* bias, int T, int h, int E, int k,
+                                 int dtype, int gating, float alpha, float* logits, int32_t* topk_ids, float* gates,
+                                 int32_t* counts, float* f, float* P, float* aux, void* ws, size_t ws_bytes,
+                                 void* stream) {
+    if (dtype == MOE_F32)
+        return router_run(x, w_packed, nullptr, bias, T, h, E, k, dtype, gating, alpha, logits, topk_ids, gates, counts,
+                          f, P, aux, ws, ws_bytes, stream);
+    return router_run(x, nullptr, w_packed, bias, T, h, E, k, dtype, gating, alpha, logits, topk_ids, gates, counts, f,
+                      P, aux, ws, ws_bytes, stream);
 }
 
 extern "C" size_t moe_router_from_logits_workspace_size(int T, int E) {

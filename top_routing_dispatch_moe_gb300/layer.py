@@ -33,7 +33,7 @@ class MoELayer:
     STAGES = ("router", "dispatch", "up_gate", "down", "shared_up_gate", "shared_down", "combine")
 
     def __init__(self, *, T, h, E, k, F, gating, cf, R, alpha, w_r, bias, w_gate, w_up, w_down,
-                 shared=None, device="cuda", routing="token", backward=False, payload="bf16"):
+                 shared=None, device="cuda", routing="token", backward=False, payload="bf16", fuse_combine=False):
         self.T, self.h, self.E, self.k, self.F = T, h, E, k, F
         self.gating, self.R, self.alpha = gating, R, alpha
         self.C = capacity_slots(cf, k, T, E)
@@ -42,6 +42,7 @@ class MoELayer:
         dev = torch.device(device)
         self.device = dev
         self.w_r = w_r
+        self.w_r_packed = moe.moe_pack_router_weight(w_r)    # the router's operand layout, packed once
         self.bias = bias
         self.packed = moe.moe_pack_expert_weights(w_gate, w_up, w_down)
         self.shared_packed = moe.moe_pack_expert_weights(*shared) if shared is not None else None
@@ -99,6 +100,14 @@ class MoELayer:
             self.sh_act = torch.empty((T, F), dtype=dt, device=dev)
             self.sh_out = torch.empty((T, h), dtype=dt, device=dev)
         self.y = torch.empty((T, h), dtype=dt, device=dev)
+        # combine fused into the down GEMM's epilogue (bf16, token-choice or Sinkhorn routing): one launch fewer,
+        # y bit-identical to the separate combine; its arrival counters start at zero and every call leaves them so
+        if fuse_combine and (dt != torch.bfloat16 or routing == "expert_choice"
+                             or (payload == "fp8" and shared is not None)):
+            raise ValueError("fuse_combine: bf16 with token-choice or Sinkhorn routing (and no shared expert with the "
+                             "FP8 payload)")
+        self.fuse_combine = bool(fuse_combine)
+        self.arrivals = moe.moe_combine_arrivals(T, h, dev) if self.fuse_combine else None
         self._saved = False
         if backward:                                 # pre-activations kept by forward(save=True)
             self.gu = torch.empty((self.rows, moe.gu_cols(F)), dtype=dt, device=dev)
@@ -122,7 +131,7 @@ class MoELayer:
         moe.moe_router(x, self.w_r, self.bias, self.k, "softmax" if self.routing == "sinkhorn" else self.gating,
                        self.alpha, logits=r["logits"],
                        topk_ids=r["topk_ids"], gates=r["gates"], counts=r["counts"], f=r["f"], P=r["P"], aux=r["aux"],
-                       ws=self.r_ws, stream=stream)
+                       ws=self.r_ws, stream=stream, w_packed=self.w_r_packed)
         if self.routing == "expert_choice":
             moe.moe_expert_choice_route(r["logits"], self.C, tokens=self.ec["tokens"], gates=self.ec["gates"],
                                         slot=self.ec["slot"], ws=self.ec_ws, stream=stream)
@@ -143,13 +152,14 @@ class MoELayer:
         mark("dispatch")
         sched = self.d_out["tile_sched"]
         shared_out = None
+        out = self.y if y is None else y
         if self.payload == "fp8":
             # dequantise the e4m3 send buffer in a pass of its own, then the bf16 GEMM (on GB300 faster than
             # moe_expert_up_gate_fp8's dequantisation inside the GEMM, with the same act)
             moe.moe_dequant_fp8(self.d_out["buf8"], self.d_out["scales"], out=self.buf_deq, stream=stream)
             moe.moe_expert_up_gate(self.buf_deq, sched, self.packed, self.E, self.F, act=self.act, stream=stream)
             mark("up_gate")
-            moe.moe_expert_down(self.act, sched, self.packed, self.E, self.h, eout=self.eout, stream=stream)
+            self._down(sched, out, stream)
             mark("down")
         elif self.shared_packed is not None and self.dtype == torch.bfloat16:
             # the shared expert's tiles run inside the routed experts' launches
@@ -161,8 +171,7 @@ class MoELayer:
                 moe.moe_expert_up_gate_shared(self.d_out["buf"], sched, self.packed, self.E, self.F, x,
                                               self.shared_packed, act=self.act, act_shared=self.sh_act, stream=stream)
             mark("up_gate")
-            moe.moe_expert_down_shared(self.act, sched, self.packed, self.E, self.h, self.sh_act, self.shared_packed,
-                                       eout=self.eout, out_shared=self.sh_out, stream=stream)
+            self._down(sched, out, stream, shared=True)
             mark("down")
             shared_out = self.sh_out
         else:
@@ -173,7 +182,7 @@ class MoELayer:
                 moe.moe_expert_up_gate(self.d_out["buf"], sched, self.packed, self.E, self.F, act=self.act,
                                        stream=stream)
             mark("up_gate")
-            moe.moe_expert_down(self.act, sched, self.packed, self.E, self.h, eout=self.eout, stream=stream)
+            self._down(sched, out, stream)
             mark("down")
         if self.shared_packed is not None and shared_out is None:
             moe.moe_expert_up_gate(x, self.sh_sched, self.shared_packed, 1, self.F, act=self.sh_act, stream=stream)
@@ -182,15 +191,30 @@ class MoELayer:
                                 stream=stream)
             mark("shared_down")
             shared_out = self.sh_out
-        out = self.y if y is None else y
         if self.routing == "expert_choice":
             moe.moe_expert_choice_combine(self.eout, self.ec["slot"], self.ec["gates"], shared_out, y=out,
                                           stream=stream)
-        else:
+        elif not self.fuse_combine:
             moe.moe_combine(self.eout, self.d_out["dest_row"], r["gates"], shared_out, y=out, stream=stream)
         mark("combine")
         self._saved = bool(save)
         return out
+
+    def _down(self, sched, y, stream, shared=False):
+        """The down GEMM (with the shared expert's tiles in the same launch when `shared`), and with the combine
+        in its epilogue when the layer fuses it (y is then written here)."""
+        if self.fuse_combine:
+            d = self.d_out
+            moe.moe_expert_down_combine(self.act, sched, self.packed, self.E, self.h, d["src_token"], d["dest_row"],
+                                        self.r_out["gates"], self.arrivals,
+                                        act_shared=self.sh_act if shared else None,
+                                        packed_shared=self.shared_packed if shared else None, eout=self.eout,
+                                        out_shared=self.sh_out if shared else None, y=y, stream=stream)
+        elif shared:
+            moe.moe_expert_down_shared(self.act, sched, self.packed, self.E, self.h, self.sh_act, self.shared_packed,
+                                       eout=self.eout, out_shared=self.sh_out, stream=stream)
+        else:
+            moe.moe_expert_down(self.act, sched, self.packed, self.E, self.h, eout=self.eout, stream=stream)
 
     def backward(self, x, dy, d_aux=1.0, stream=None, events=None):
         """Gradients of <dy, y> + d_aux * aux for the last forward(x): returns dict(dx, dW_r, d_bias, dW_gate,

@@ -25,6 +25,9 @@ _P, _I, _Z, _F, _LL = ctypes.c_void_p, ctypes.c_int, ctypes.c_size_t, ctypes.c_f
 _SIGS = {
     "moe_router_workspace_size": (_Z, [_I, _I, _I, _I, _I]),
     "moe_router": (_I, [_P, _P, _P, _I, _I, _I, _I, _I, _I, _F, _P, _P, _P, _P, _P, _P, _P, _P, _Z, _P]),
+    "moe_router_packed_bytes": (_Z, [_I, _I, _I]),
+    "moe_pack_router_weight": (_I, [_P, _I, _I, _I, _P, _P]),
+    "moe_router_packed": (_I, [_P, _P, _P, _I, _I, _I, _I, _I, _I, _F, _P, _P, _P, _P, _P, _P, _P, _P, _Z, _P]),
     "moe_router_from_logits_workspace_size": (_Z, [_I, _I]),
     "moe_router_from_logits": (_I, [_P, _P, _I, _I, _I, _I, _F, _P, _P, _P, _P, _P, _P, _P, _Z, _P]),
     "moe_sinkhorn_workspace_size": (_Z, [_I, _I]),
@@ -66,6 +69,8 @@ _SIGS = {
     "moe_expert_ffn_workspace_size": (_Z, [_I, _I, _I]),
     "moe_expert_ffn": (_I, [_P, _P, _P, _I, _I, _I, _I, _I, _P, _P, _Z, _P]),
     "moe_combine": (_I, [_P, _P, _P, _P, _I, _I, _I, _I, _P, _P]),
+    "moe_combine_arrivals_bytes": (_Z, [_I, _I]),
+    "moe_expert_down_combine": (_I, [_P, _P, _P, _I, _I, _I, _I, _P, _P, _P, _I, _I, _P, _P, _I, _P, _P, _P, _P, _P]),
     "moe_last_error_string": (ctypes.c_char_p, []),
     "moe_check_device_error": (_I, [_P]),
     "moe_set_wait_limit": (None, [_LL]),
@@ -119,9 +124,21 @@ def moe_router_workspace_size(T, h, E, k, dtype) -> int:
     return _lib.moe_router_workspace_size(T, h, E, k, dtype)
 
 
+def moe_pack_router_weight(w_r, packed=None, stream=None):
+    """The router weight repacked once for moe_router_packed (bf16: W_r^T [E, h]; fp32: a copy of w_r)."""
+    h, E = w_r.shape
+    dt = dtype_code(w_r.dtype)
+    if packed is None:
+        packed = _bytes_tensor(_lib.moe_router_packed_bytes(h, E, dt), w_r.device)
+    _check(_lib.moe_pack_router_weight(_ptr(w_r), h, E, dt, _ptr(packed), _stream(stream)))
+    return packed
+
+
 def moe_router(x, w_r, bias, k: int, gating: str | int = "softmax", alpha: float = 0.01, *, logits=None,
                topk_ids=None, gates=None, counts=None, f=None, P=None, aux=None, ws=None, stream=None,
-               want_logits=True):
+               want_logits=True, w_packed=None):
+    """moe_router, or moe_router_packed when `w_packed` (moe_pack_router_weight of w_r) is given; w_r then only
+    supplies the shape."""
     T, h = x.shape
     E = w_r.shape[1]
     dev = x.device
@@ -137,9 +154,10 @@ def moe_router(x, w_r, bias, k: int, gating: str | int = "softmax", alpha: float
     aux = torch.empty(1, dtype=torch.float32, device=dev) if aux is None else aux
     need = moe_router_workspace_size(T, h, E, k, dt)
     ws = _bytes_tensor(need, dev) if ws is None else ws
-    _check(_lib.moe_router(_ptr(x), _ptr(w_r), _ptr(bias), T, h, E, k, dt, g, alpha, _ptr(logits), _ptr(topk_ids),
-                           _ptr(gates), _ptr(counts), _ptr(f), _ptr(P), _ptr(aux), _ptr(ws), ws.numel(),
-                           _stream(stream)))
+    fn = _lib.moe_router if w_packed is None else _lib.moe_router_packed
+    _check(fn(_ptr(x), _ptr(w_r if w_packed is None else w_packed), _ptr(bias), T, h, E, k, dt, g, alpha, _ptr(logits),
+              _ptr(topk_ids), _ptr(gates), _ptr(counts), _ptr(f), _ptr(P), _ptr(aux), _ptr(ws), ws.numel(),
+              _stream(stream)))
     return dict(logits=logits, ids=topk_ids, gates=gates, counts=counts, f=f, P=P, aux=aux)
 
 
@@ -425,6 +443,31 @@ def moe_combine(eout, dest_row, gates, shared_out=None, y=None, stream=None):
     _check(_lib.moe_combine(_ptr(eout), _ptr(dest_row), _ptr(gates), _ptr(shared_out), T, h, k,
                             dtype_code(eout.dtype), _ptr(y), _stream(stream)))
     return y
+
+
+def moe_combine_arrivals(T: int, h: int, device) -> torch.Tensor:
+    """Zeroed arrival counters of moe_expert_down_combine (int32, moe_combine_arrivals_bytes of them)."""
+    return torch.zeros(max(1, _lib.moe_combine_arrivals_bytes(T, h) // 4), dtype=torch.int32, device=device)
+
+
+def moe_expert_down_combine(act, tile_sched, packed_w, E: int, h: int, src_token, dest_row, gates, arrivals,
+                            act_shared=None, packed_shared=None, eout=None, out_shared=None, y=None, stream=None):
+    """Down GEMM (routed and, with act_shared, the shared expert's rows) with the combine in its epilogue (bf16):
+    returns (eout, out_shared or None, y), y bit-identical to moe_combine on those eout / out_shared."""
+    rows, F = act.shape
+    T, k = dest_row.shape
+    dev = act.device
+    if eout is None:
+        eout = torch.empty((rows, h), dtype=act.dtype, device=dev)
+    if act_shared is not None and out_shared is None:
+        out_shared = torch.empty((T, h), dtype=act.dtype, device=dev)
+    if y is None:
+        y = torch.empty((T, h), dtype=act.dtype, device=dev)
+    _check(_lib.moe_expert_down_combine(_ptr(act), _ptr(tile_sched), _ptr(packed_w), E, h, F, rows, _ptr(src_token),
+                                        _ptr(dest_row), _ptr(gates), T, k, _ptr(act_shared), _ptr(packed_shared),
+                                        dtype_code(act.dtype), _ptr(eout), _ptr(out_shared), _ptr(y), _ptr(arrivals),
+                                        _stream(stream)))
+    return eout, out_shared, y
 
 
 # ------------------------------------------------------------------------------------------------ errors
