@@ -102,11 +102,13 @@ class ClockSampler:
             except Exception:
                 self.proc.kill()
 
-    def summary(self):
+    def summary(self, window=None):
+        """Median SM clock, the maximum and the throttle reasons seen in `window` (default: the marked one)."""
+        w0, w1 = window if window is not None else self.window
         sm, mx, reasons = [], [], set()
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        for ts, line in self.lines:
-            if not (self.window[0] <= ts <= self.window[1] + 0.03):
+        for ts, line in list(self.lines):
+            if not (w0 <= ts <= w1 + 0.03):
                 continue
             parts = [p.strip() for p in line.split(",")]
             if len(parts) < 8:
@@ -161,7 +163,30 @@ def oracle_step(cfg, inp, w64, sample_tokens, keep=None):
     return t1 - t0, t2 - t1
 
 
-def decode_weights(cfg, inp):
+class _LazyWeights(dict):
+    """Expert weights decoded to float64 on first use, one expert kept at a time (the DeepSeek-V3-shaped
+    workload's 22.6 GB of bf16 weights would take 90 GB as float64)."""
+
+    def __init__(self, cfg, inp):
+        super().__init__()
+        self.cfg, self.inp = cfg, inp
+        if inp["shared"] is not None:
+            sh = tuple(moe_inputs.to_f64(w, cfg.dtype) for w in inp["shared"])
+            self["shared"] = lambda: sh
+
+    def __missing__(self, e):
+        for key in [k for k in self if k != "shared"]:
+            del self[key]
+        c, i = self.cfg, self.inp
+        w = (moe_inputs.to_f64(i["wg"][e], c.dtype), moe_inputs.to_f64(i["wu"][e], c.dtype),
+             moe_inputs.to_f64(i["wd"][e], c.dtype))
+        self[e] = w
+        return w
+
+
+def decode_weights(cfg, inp, lazy=False):
+    if lazy:
+        return _LazyWeights(cfg, inp)
     w64 = {e: (moe_inputs.to_f64(inp["wg"][e], cfg.dtype), moe_inputs.to_f64(inp["wu"][e], cfg.dtype),
                moe_inputs.to_f64(inp["wd"][e], cfg.dtype)) for e in range(cfg.E)}
     if inp["shared"] is not None:
@@ -259,21 +284,19 @@ def max_over_ranks(v: float, world: int, device) -> float:
     return float(t.item())
 
 
-def run_gpu(args, cfg, C):
+EXTRA_WORKLOADS = ["tiny_fp32", "mixtral_zipf", "deepseek_v3", "qwen3_moe"]
+
+
+def fuses_combine(args, cfg) -> bool:
+    """Whether the layer runs the combine inside the down GEMM's epilogue (bf16, token-choice or Sinkhorn
+    routing, and no shared expert with the FP8 payload), unless --no-fuse-combine."""
+    return (args.fuse_combine and cfg.dtype == "bf16" and cfg.routing != "expert_choice"
+            and not (cfg.payload == "fp8" and cfg.n_shared))
+
+
+def build_layer(cfg, inp, dev, backward, fuse_combine=False):
     import torch
-    import torch.distributed as dist
-    world = int(os.environ.get("WORLD_SIZE", "1"))
-    rank = int(os.environ.get("RANK", "0"))
-    local = int(os.environ.get("LOCAL_RANK", "0"))
-    if world > 1:
-        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
-    torch.cuda.set_device(local)
-    dev = torch.device("cuda", local)
-
-    from top_routing_dispatch_moe_gb300 import moe
     from top_routing_dispatch_moe_gb300.layer import MoELayer
-
-    inp = host_inputs(cfg)
 
     def up(a):
         if cfg.dtype == "bf16":
@@ -286,12 +309,16 @@ def run_gpu(args, cfg, C):
                      w_gate=up(inp["wg"]), w_up=up(inp["wu"]), w_down=up(inp["wd"]),
                      shared=tuple(up(np.ascontiguousarray(w)[None]) for w in inp["shared"])
                      if inp["shared"] is not None else None, device=dev, routing=cfg.routing,
-                     backward=want_backward(args, cfg), payload=cfg.payload)
-    x = up(inp["x"])
-    flush = torch.empty(512 * 2**20, dtype=torch.uint8, device=dev)
-    stream = torch.cuda.current_stream()
+                     backward=backward, payload=cfg.payload, fuse_combine=fuse_combine)
+    return layer, up(inp["x"])
 
-    clk = ClockSampler(_smi_id(local)).start()
+
+def time_forward(args, layer, x, flush, world, dev):
+    """K device-resident layer forwards, each after an L2 flush, with CUDA events around every stage on the
+    launching stream. Returns per-stage times, per-step times, the library's launch count and the clocks."""
+    import torch
+    import torch.distributed as dist
+    from top_routing_dispatch_moe_gb300 import moe
     for _ in range(args.warmup):
         layer.forward(x)
         flush.zero_()
@@ -302,15 +329,6 @@ def run_gpu(args, cfg, C):
         flush.zero_()
         torch.cuda.synchronize()
     assert moe.moe_check_device_error() == moe.MOE_OK, moe.moe_last_error_string()
-    if cfg.routing == "expert_choice":
-        kept = cfg.E * layer.C                        # every expert takes exactly C tokens
-        active = cfg.E
-    else:
-        kc = layer.d_out["kept_counts"]
-        kept = int(kc.sum().item())
-        active = int((kc > 0).sum().item())           # experts whose weights the grouped GEMMs read
-
-    # ---- device-resident timed region
     events: dict = {}
     if world > 1:
         dist.barrier()
@@ -326,14 +344,12 @@ def run_gpu(args, cfg, C):
         flush.zero_()
     torch.cuda.synchronize()
     t_wall = time.perf_counter() - t_wall0
-    clk.mark(t_clk0, time.time())
-    time.sleep(0.05)
-    clk.stop()
+    window = (t_clk0, time.time())
     if world > 1:
         dist.barrier()
     launches = moe.moe_launch_count() - launches0
     assert moe.moe_check_device_error() == moe.MOE_OK, moe.moe_last_error_string()
-
+    from top_routing_dispatch_moe_gb300.layer import MoELayer
     stage_names = [s for s in MoELayer.STAGES if s in events]
     order = ["start"] + stage_names
     stage_ms = {s: [] for s in stage_names}
@@ -343,8 +359,125 @@ def run_gpu(args, cfg, C):
             stage_ms[b].append(events[a][i].elapsed_time(events[b][i]))
         step_ms.append(events["start"][i].elapsed_time(events[order[-1]][i]))
     ms = max_over_ranks(float(np.mean(step_ms)), world, dev)
-    step_stats = {"median": float(np.median(step_ms)), "p10": float(np.percentile(step_ms, 10)),
-                  "p90": float(np.percentile(step_ms, 90))}
+    stats = {"median": float(np.median(step_ms)), "p10": float(np.percentile(step_ms, 10)),
+             "p90": float(np.percentile(step_ms, 90))}
+    return dict(stage_ms=stage_ms, ms=ms, stats=stats, launches=int(launches), wall=t_wall, window=window)
+
+
+def kept_and_active(cfg, layer):
+    if cfg.routing == "expert_choice":
+        return cfg.E * layer.C, cfg.E                 # every expert takes exactly C tokens
+    kc = layer.d_out["kept_counts"]
+    return int(kc.sum().item()), int((kc > 0).sum().item())   # active: experts whose weights the GEMMs read
+
+
+def stage_metrics(cfg, stage_ms, kept, active, fused_combine=False):
+    """Roofline of the dominant kernel (the up/gate grouped GEMM) and the bandwidth of the other stages, from the
+    algorithmic work per unit: router T h el + h E el bytes, dispatch (T + kept) h el, combine (kept + T [+ T
+    shared]) h el, FFN 6 h F flop per kept row (plus the shared expert's T rows). With the combine fused into the
+    down GEMM the "down" stage holds both, and the combine has no bandwidth of its own (null)."""
+    hbm, bf16_burst, bf16_sus, peak_src = _peaks()
+    mean = {s: float(np.mean(v)) for s, v in stage_ms.items()}
+    ug_ms, dn_ms = mean["up_gate"], mean["down"]
+    # with bf16 the shared expert's tiles run inside the up/gate and down launches
+    fused_shared = bool(cfg.n_shared) and "shared_up_gate" not in stage_ms
+    ug_flops = 4.0 * (kept + (cfg.T if fused_shared else 0)) * cfg.h * cfg.F
+    ffn_flops = 6.0 * kept * cfg.h * cfg.F + (6.0 * cfg.T * cfg.h * cfg.F if cfg.n_shared else 0.0)
+    ffn_ms = ug_ms + dn_ms + sum(mean[s] for s in ("shared_up_gate", "shared_down") if s in mean)
+    ug_tflops = ug_flops / (ug_ms * 1e-3) / 1e12
+    if cfg.payload == "fp8":                         # read x once, write one byte per element + a scale per 128
+        disp_bytes = cfg.T * cfg.h * cfg.el + kept * (cfg.h + cfg.h // 128 * 4)
+    else:
+        disp_bytes = (cfg.T + kept) * cfg.h * cfg.el
+    comb_bytes = (kept + cfg.T + (cfg.T if cfg.n_shared else 0)) * cfg.h * cfg.el
+    router_bytes = (cfg.T * cfg.h + cfg.h * cfg.E) * cfg.el
+    gbs = lambda nbytes, stage: nbytes / (mean[stage] * 1e-3) / 1e9   # noqa: E731
+    # The up/gate GEMM's algorithmic bytes: the gate and up weights of every expert that received rows (and the
+    # shared expert's), its input rows read once, the activation written once. Below the ridge point (few rows
+    # per expert) the weight stream, not the tensor cores, bounds it; the roofline takes whichever bound is
+    # reached later at the measured peaks.
+    ug_rows = kept + (cfg.T if fused_shared else 0)
+    ug_bytes = ((active + (1 if fused_shared else 0)) * 2.0 * cfg.F * cfg.h + ug_rows * (cfg.h + cfg.F)) * cfg.el
+    ug_gbs = ug_bytes / (ug_ms * 1e-3) / 1e9
+    if ug_bytes / (hbm * 1e9) > ug_flops / (bf16_burst * 1e12):
+        roofline = {"bound": "hbm", "kernel": "up/gate grouped GEMM (SwiGLU epilogue)", "achieved": ug_gbs,
+                    "peak": hbm, "unit": "GB/s", "frac": ug_gbs / hbm, "traffic": None,
+                    "peak_source": f"{peak_src} HBM copy", "tensor_tflops": ug_tflops}
+    else:
+        roofline = {"bound": "tensor", "kernel": "up/gate grouped GEMM (SwiGLU epilogue)", "achieved": ug_tflops,
+                    "peak": bf16_burst, "unit": "TFLOP/s", "frac": ug_tflops / bf16_burst, "traffic": None,
+                    "peak_source": f"{peak_src} bf16 burst"}
+    if roofline["bound"] == "tensor" and bf16_sus:
+        # the same kernel against the sustained (power-capped, seconds-long loop) bf16 peak: the timed region runs
+        # the GEMMs back to back for the whole run, under the same cap
+        roofline["frac_of_sustained_peak"] = ug_tflops / bf16_sus
+    roofline["algorithmic_bytes"] = ug_bytes
+    roofline["intensity_flop_per_byte"] = ug_flops / ug_bytes
+    roofline["ridge_flop_per_byte"] = bf16_burst * 1e12 / (hbm * 1e9)
+    out = {"stages_ms": mean, "roofline": roofline,
+           "expert_tflops": ffn_flops / (ffn_ms * 1e-3) / 1e12,
+           "grouped_gemm_pct_bf16_peak": 100.0 * ffn_flops / (ffn_ms * 1e-3) / 1e12 / bf16_burst,
+           "router_gbs": gbs(router_bytes, "router"), "router_pct_hbm": 100.0 * gbs(router_bytes, "router") / hbm,
+           "dispatch_gbs": gbs(disp_bytes, "dispatch"), "dispatch_pct_hbm": 100.0 * gbs(disp_bytes, "dispatch") / hbm,
+           "combine_fused_into_down_gemm": bool(fused_combine)}
+    if fused_combine:
+        out.update(combine_gbs=None, combine_pct_hbm=None)
+    else:
+        out.update(combine_gbs=gbs(comb_bytes, "combine"), combine_pct_hbm=100.0 * gbs(comb_bytes, "combine") / hbm)
+    return out
+
+
+def measure_extra_workload(args, name, world, dev, flush, clk, rank):
+    """One more workload of the default run: the forward timed as the headline's is (no backward, no e2e leg),
+    with its stage bandwidths, its roofline and (rank 0, one GPU) its parity against the oracle on a sample."""
+    import torch
+    cfg = moe_inputs.get_config(name)
+    C = 0
+    if cfg.cf:
+        import math
+        C = int(math.ceil(cfg.cf * cfg.k * cfg.T / cfg.E - 1e-9))
+    inp = host_inputs(cfg)
+    layer, x = build_layer(cfg, inp, dev, backward=False, fuse_combine=fuses_combine(args, cfg))
+    t = time_forward(args, layer, x, flush, world, dev)
+    kept, active = kept_and_active(cfg, layer)
+    out = {"workload": _workload_desc(cfg, C), "value": world * cfg.T / (t["ms"] * 1e-3), "unit": "tokens/s",
+           "ms_per_step": t["ms"], "ms_per_step_stats": t["stats"], "kept_assignments": kept,
+           "dtype": "bf16" if cfg.dtype == "bf16" else "f32", "gpu_launches": t["launches"]}
+    out.update(stage_metrics(cfg, t["stage_ms"], kept, active, layer.fuse_combine))
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        keep: dict = {}
+        rng = np.random.default_rng(2)
+        toks = np.sort(rng.choice(cfg.T, size=min(cfg.T, args.parity_tokens), replace=False))
+        oracle_step(cfg, inp, decode_weights(cfg, inp, lazy=True), toks, keep)
+        out["parity"] = parity_report(cfg, layer, keep)
+    time.sleep(0.05)                                  # the sampler's last lines of the timed region
+    out["clocks"] = clk.summary(t["window"])
+    del layer, x
+    torch.cuda.empty_cache()
+    return out
+
+
+def run_gpu(args, cfg, C):
+    import torch
+    import torch.distributed as dist
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+
+    inp = host_inputs(cfg)
+    layer, x = build_layer(cfg, inp, dev, want_backward(args, cfg), fuse_combine=fuses_combine(args, cfg))
+    flush = torch.empty(512 * 2**20, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream()
+
+    clk = ClockSampler(_smi_id(local)).start()
+    # ---- device-resident timed region
+    t = time_forward(args, layer, x, flush, world, dev)
+    stage_ms, ms = t["stage_ms"], t["ms"]
+    kept, active = kept_and_active(cfg, layer)
     value = world * cfg.T / (ms * 1e-3)
 
     # ---- end-to-end through the public API: every step copies its batch of tokens in from pinned host
@@ -376,56 +509,18 @@ def run_gpu(args, cfg, C):
         except Exception as exc:                      # reported in the line; the forward figures stand
             backward = {"error": f"{type(exc).__name__}: {exc}"}
 
-    # ---- roofline of the dominant kernel (the up/gate grouped GEMM) and the bandwidth stages
-    hbm, bf16_burst, bf16_sus, peak_src = _peaks()
-    ug_ms = float(np.mean(stage_ms["up_gate"]))
-    dn_ms = float(np.mean(stage_ms["down"]))
-    # with bf16 the shared expert's tiles run inside the up/gate and down launches
-    fused_shared = bool(cfg.n_shared) and "shared_up_gate" not in stage_ms
-    ug_flops = 4.0 * (kept + (cfg.T if fused_shared else 0)) * cfg.h * cfg.F
-    ffn_flops = 6.0 * kept * cfg.h * cfg.F + (6.0 * cfg.T * cfg.h * cfg.F if cfg.n_shared else 0.0)
-    ffn_ms = ug_ms + dn_ms + sum(float(np.mean(stage_ms[s])) for s in ("shared_up_gate", "shared_down") if s in stage_ms)
-    ug_tflops = ug_flops / (ug_ms * 1e-3) / 1e12
-    if cfg.payload == "fp8":                         # read x once, write one byte per element + a scale per 128
-        disp_bytes = cfg.T * cfg.h * cfg.el + kept * (cfg.h + cfg.h // 128 * 4)
-    else:
-        disp_bytes = (cfg.T + kept) * cfg.h * cfg.el
-    comb_bytes = (kept + cfg.T + (cfg.T if cfg.n_shared else 0)) * cfg.h * cfg.el
-    disp_gbs = disp_bytes / (float(np.mean(stage_ms["dispatch"])) * 1e-3) / 1e9
-    comb_gbs = comb_bytes / (float(np.mean(stage_ms["combine"])) * 1e-3) / 1e9
-    traffic = None
+    m = stage_metrics(cfg, stage_ms, kept, active, layer.fuse_combine)
+    roofline = m.pop("roofline")
     try:
         with open(os.path.join(ROOT, "profiles", "traffic.json")) as fh:
             tr = json.load(fh).get(cfg.name, {})
         if tr.get("kernel_source_hash") == kernel_hash():
-            traffic = tr.get("up_gate_dram_bytes")
+            roofline["traffic"] = tr.get("up_gate_dram_bytes")
     except Exception:
         pass
-    # The up/gate GEMM's algorithmic bytes: the gate and up weights of every expert that received rows (and the
-    # shared expert's), its input rows read once, the activation written once. Below the ridge point (few rows
-    # per expert) the weight stream, not the tensor cores, bounds it; the roofline takes whichever bound is
-    # reached later at the measured peaks.
-    ug_rows = kept + (cfg.T if fused_shared else 0)
-    ug_bytes = ((active + (1 if fused_shared else 0)) * 2.0 * cfg.F * cfg.h + ug_rows * (cfg.h + cfg.F)) * cfg.el
-    ug_gbs = ug_bytes / (ug_ms * 1e-3) / 1e9
-    if ug_bytes / (hbm * 1e9) > ug_flops / (bf16_burst * 1e12):
-        roofline = {"bound": "hbm", "kernel": "up/gate grouped GEMM (SwiGLU epilogue)", "achieved": ug_gbs,
-                    "peak": hbm, "unit": "GB/s", "frac": ug_gbs / hbm, "traffic": traffic,
-                    "peak_source": f"{peak_src} HBM copy", "tensor_tflops": ug_tflops}
-    else:
-        roofline = {"bound": "tensor", "kernel": "up/gate grouped GEMM (SwiGLU epilogue)", "achieved": ug_tflops,
-                    "peak": bf16_burst, "unit": "TFLOP/s", "frac": ug_tflops / bf16_burst, "traffic": traffic,
-                    "peak_source": f"{peak_src} bf16 burst"}
-    if roofline["bound"] == "tensor" and bf16_sus:
-        # the same kernel against the sustained (power-capped, seconds-long loop) bf16 peak: the timed region runs
-        # the GEMMs back to back for the whole run, under the same cap
-        roofline["frac_of_sustained_peak"] = ug_tflops / bf16_sus
-    roofline["algorithmic_bytes"] = ug_bytes
-    roofline["intensity_flop_per_byte"] = ug_flops / ug_bytes
-    roofline["ridge_flop_per_byte"] = bf16_burst * 1e12 / (hbm * 1e9)
 
     line = {"metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
-            "warmup": args.warmup, "ms_per_step": ms, "ms_per_step_stats": step_stats, "higher_is_better": True,
+            "warmup": args.warmup, "ms_per_step": ms, "ms_per_step_stats": t["stats"], "higher_is_better": True,
             "scaling": "weak",
             "vs_baseline": None, "dtype": "bf16" if cfg.dtype == "bf16" else "f32", "data": "synthetic",
             "config": {"workload": _workload_desc(cfg, C), "global_batch": cfg.T * world, "tokens_per_gpu": cfg.T,
@@ -435,14 +530,10 @@ def run_gpu(args, cfg, C):
             **({"backward": backward} if backward is not None else {}),
             "e2e": {"value": world * cfg.T / (e2e * 1e-3), "unit": "tokens/s", "h2d_bytes_per_step": io_bytes,
                     "d2h_bytes_per_step": io_bytes, "ms_per_step": e2e},
-            "gpu_launches": int(launches),
-            "stages_ms": {s: float(np.mean(v)) for s, v in stage_ms.items()},
-            "expert_tflops": ffn_flops / (ffn_ms * 1e-3) / 1e12,
-            "grouped_gemm_pct_bf16_peak": 100.0 * ffn_flops / (ffn_ms * 1e-3) / 1e12 / bf16_burst,
-            "dispatch_gbs": disp_gbs, "dispatch_pct_hbm": 100.0 * disp_gbs / hbm,
-            "combine_gbs": comb_gbs, "combine_pct_hbm": 100.0 * comb_gbs / hbm,
-            "wall_s_timed_region": t_wall}
-    line["clocks"] = clk.summary()
+            "gpu_launches": t["launches"],
+            **m,
+            "wall_s_timed_region": t["wall"]}
+    line["clocks"] = clk.summary(t["window"])
 
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         w64 = decode_weights(cfg, inp)
@@ -453,6 +544,21 @@ def run_gpu(args, cfg, C):
                                           f"{args.baseline_tokens} random tokens (float64 numpy), FFN cost scaled "
                                           f"to {cfg.T} tokens"}
         line["parity"] = parity_report(cfg, layer, keep)
+        del w64
+
+    # ---- the other workloads (forward only), measured the same way after the headline's memory is released
+    extras = [w for w in args.workloads.split(",") if w and w != "none" and w != cfg.name]
+    if extras:
+        del layer, x, x_hosts, y_hosts
+        torch.cuda.empty_cache()
+        line["workloads"] = {}
+        for name in extras:
+            try:
+                line["workloads"][name] = measure_extra_workload(args, name, world, dev, flush, clk, rank)
+            except Exception as exc:                  # reported in the line; the headline figures stand
+                line["workloads"][name] = {"error": f"{type(exc).__name__}: {exc}"}
+                torch.cuda.empty_cache()
+    clk.stop()
     if rank == 0:
         print(json.dumps(line), flush=True)
     if world > 1:
@@ -531,9 +637,19 @@ def main():
     ap.add_argument("--sample-tokens", type=int, default=32, help="oracle tokens per reference-arm step")
     ap.add_argument("--baseline-tokens", type=int, default=128, help="oracle tokens of the cpu_baseline sample")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--workloads", default=None,
+                    help="comma-separated further workloads timed after the headline one (forward only), reported "
+                         "under 'workloads'; default: the other four named configurations when the headline is "
+                         "the page-3 workload, none otherwise; 'none' for none")
+    ap.add_argument("--parity-tokens", type=int, default=32, help="oracle tokens of each further workload's parity")
+    ap.add_argument("--fuse-combine", action=argparse.BooleanOptionalAction, default=False,
+                    help="run the combine in the down GEMM's epilogue (bf16 token-choice / Sinkhorn layers); off by "
+                         "default: on GB300 the separate combine measured faster")
     args = ap.parse_args()
     assert args.warmup >= 3, "at least 3 warm-up steps"
     cfg = moe_inputs.get_config(args.workload)
+    if args.workloads is None:
+        args.workloads = ",".join(EXTRA_WORKLOADS) if args.workload == "page3_cf1.25" else "none"
     C = 0
     if cfg.cf:
         import math
