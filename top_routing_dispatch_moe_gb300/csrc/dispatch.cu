@@ -113,7 +113,9 @@ __device__ void ring_finish(RingCursor& c, int k, const int* __restrict__ dest, 
         if (coff >= c.row_bytes) { coff = 0; ++ct; }
         if (++cst == c.NS) { cst = 0; par ^= 1u; }
     }
-    asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
+    // the stores' sources must have been read before the block's shared memory goes away; their writes complete
+    // on their own, and the kernel's end orders them before any later kernel
+    asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
 }
 
 // Chunk c covers tokens [c * tpc, (c + 1) * tpc), i.e. assignments [c * tpc * k, ...): tpc * k <= kChunkA.

@@ -59,9 +59,11 @@ struct TileCfg {
     static constexpr int SMEM_BYTES_A8 = SMEM_BYTES + STAGES * A8_BYTES;   // + the e4m3 staging tiles
     static_assert(BN % 32 == 0 && BN >= 32 && BN <= 256, "UMMA N for M = 128");
     static_assert(SMEM_BYTES <= 227 * 1024, "shared memory per CTA");
-    static_assert(SMEM_BYTES_A8 <= 227 * 1024, "shared memory per CTA (e4m3 operand)");
 };
 using Wide = TileCfg<256, 4>;
+// fp32-output products at most 128 wide (the router logits of up to 128 experts): half the MMA work per tile of
+// the 256-wide one, which such a product would fill only half of, and six stages of 32 KB
+using Mid = TileCfg<128, 6>;
 constexpr long long kDrainLimit = 1LL << 24;
 
 // ---------------------------------------------------------------------------------------------------
@@ -861,7 +863,7 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
             __syncwarp();
             if (lane == 0) mbar_arrive(tempty(a));
         }
-        if (lane == 0) bulk_wait_all();                // every box stored before the CTA exits
+        if (lane == 0) bulk_wait_read_all();           // every box read out of shared memory before the CTA exits
     }
     tc_fence_before();
     __syncthreads();
@@ -1225,7 +1227,7 @@ grouped_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_c
             __syncwarp();
             if (lane == 0) mbar_arrive_cluster(tempty_leader + 8u * a);
         }
-        if (lane == 0) bulk_wait_all();                // every box stored before the CTA exits
+        if (lane == 0) bulk_wait_read_all();           // every box read out of shared memory before the CTA exits
     }
     cluster_sync_all();                      // every role has left its loop; rank 1's round count is in rank 0
     if (warp == 0 && lane == 0 && leader) {
@@ -1371,6 +1373,7 @@ template <int EPI>
 static int gemm_a8(const void* a8, long long a_rows, const void* b, long long b_rows_total, const Params& p,
                    cudaStream_t s) {
     using CF = Wide;
+    static_assert(CF::SMEM_BYTES_A8 <= 227 * 1024, "shared memory per CTA (e4m3 operand)");
     static unsigned long long attr_ctx[64];  // context in which the attribute was set, per device
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64)
@@ -1639,12 +1642,16 @@ int tc_router_logits(const void* x, const void* w_rT, const float* bias, int T, 
                      float* logits, cudaStream_t s) {
     unsigned* err = device_error_word();
     MOE_REQUIRE(err, MOE_ERR_CUDA, "device error word unavailable");
+    if (E <= tc::Mid::BN) {
+        tc::Params p{sched, h, 1, E, E, E, nullptr, logits, bias, err, wait_limit(), 0, nullptr};
+        return tc::gemm<tc::EPI_F32, tc::Mid>(x, T, w_rT, E, p, s);
+    }
     tc::Params p{sched, h, cdiv(E, tc::Wide::BN), E, E, E, nullptr, logits, bias, err, wait_limit(), 0, nullptr};
     return tc::gemm<tc::EPI_F32, tc::Wide>(x, T, w_rT, E, p, s);
 }
 
 void tc_splitk_plan(int M, int N, int K, int* S, int* kchunk) {
-    const long long tiles = (long long)cdiv(M, tc::BM) * cdiv(N, tc::Wide::BN);
+    const long long tiles = (long long)cdiv(M, tc::BM) * cdiv(N, N <= tc::Mid::BN ? tc::Mid::BN : tc::Wide::BN);
     const int S0 = (int)std::min<long long>(std::min(16, cdiv(K, tc::BK)), num_sms() / std::max(1LL, tiles));
     if (S0 < 2) {
         *S = 1;
@@ -1664,13 +1671,15 @@ int tc_gemm_f32_splitk(const void* a, int M, int a_cols, int a_kmod, const void*
                     b_kmod % tc::BK == 0 && aligned16(a) && aligned16(b) && aligned16(parts),
                 MOE_ERR_INVALID_ARG, "tc_gemm_f32_splitk: M=%d N=%d K=%d S=%d kchunk=%d a_cols=%d b_cols=%d", M, N, K, S,
                 kchunk, a_cols, b_cols);
-    tc::Params p{nullptr, K, cdiv(N, tc::Wide::BN), 0, N, N, nullptr, parts, nullptr, err, wait_limit(), 0, nullptr,
-                 nullptr, S, cdiv(M, tc::BM), M, nullptr, 0, 0, nullptr};
+    const bool mid = N <= tc::Mid::BN;
+    tc::Params p{nullptr, K, mid ? 1 : cdiv(N, tc::Wide::BN), 0, N, N, nullptr, parts, nullptr, err, wait_limit(), 0,
+                 nullptr, nullptr, S, cdiv(M, tc::BM), M, nullptr, 0, 0, nullptr};
     p.wg_kchunk = kchunk;
     p.a_cols = a_cols;
     p.b_cols = b_cols;
     p.a_kmod = a_kmod;
     p.b_kmod = b_kmod;
+    if (mid) return tc::gemm<tc::EPI_F32, tc::Mid>(a, M, b, N, p, s);
     return tc::gemm<tc::EPI_F32, tc::Wide>(a, M, b, N, p, s);
 }
 

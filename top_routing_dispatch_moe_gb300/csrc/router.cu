@@ -674,7 +674,7 @@ router_gate_kernel(const float* __restrict__ logits, int nparts, size_t part_str
 // expert are added by a pairwise tree over the slices. Every block adds its experts' f_e P_e in expert order; with
 // several blocks, the last one to arrive (counted on `ticket`, which the gating kernel zeroed) adds the blocks'
 // sums in block order. No step depends on timing, so the results are the same on every run.
-constexpr int kFinExperts = 32;
+constexpr int kFinExperts = 8;
 __global__ void __launch_bounds__(1024)
 router_finalize(const float* __restrict__ partial_P, const int32_t* __restrict__ partial_C, int grid, int T_, int E,
                 int k, float alpha, int32_t* counts, float* f, float* P, float* aux, float* term_part,
@@ -762,9 +762,16 @@ router_transpose_kernel(const T* __restrict__ w, int h, int E, T* __restrict__ w
 // ---------------------------------------------------------------------------------------------------
 // Upper bound of the blocks of any router launch (sizes the partial-sum workspace).
 static int router_grid(int T) { return std::max(1, std::min(cdiv(T, kRouterWarps), kRouterMaxBlocks)); }
-// The gating kernel on stored logits: a few tokens per warp, at most two blocks per SM, so that the finalize
-// reduces few per-block partials.
-static int gate_grid(int T) { return std::max(1, std::min(router_grid(T), 2 * num_sms())); }
+// The gating kernel on stored logits: a few tokens per warp, as many blocks as are resident at once (its per-token
+// latency chain needs the warps), at most router_grid(T) (the size of the per-block partials in the workspace).
+template <int N>
+static int gate_grid(int T, size_t smem) {
+    int per_sm = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, router_gate_kernel<N>, kRouterWarps * 32, smem) !=
+            cudaSuccess || per_sm < 1)
+        per_sm = 1;
+    return std::max(1, std::min(router_grid(T), per_sm * num_sms()));
+}
 // The fused small-E kernel stages the router weight into every block, takes two tokens per warp, and its
 // register budget allows two blocks per SM.
 static int router_small_grid(int T) { return std::max(1, std::min(cdiv(T, 2 * kRouterWarps), 2 * num_sms())); }
@@ -869,7 +876,7 @@ static int router_run(const void* x, const void* w_r, const void* w_rT, const fl
     MOE_REQUIRE(ws_bytes >= w.bytes && (w.bytes == 0 || ws), MOE_ERR_WORKSPACE,
                 "moe_router: workspace %zu < %zu bytes", ws_bytes, w.bytes);
     cudaStream_t s = static_cast<cudaStream_t>(stream);
-    const int G = !small ? gate_grid(T) : dtype == MOE_BF16 ? router_mma_grid(T) : router_small_grid(T);
+    int G = !small ? 1 : dtype == MOE_BF16 ? router_mma_grid(T) : router_small_grid(T);   // !small: set at launch
     GateOut o{topk_ids, gates, logits, w.partial_P, w.partial_C, w.ticket};
     if (T > 0) {
         if (small && dtype == MOE_BF16) {
@@ -934,6 +941,7 @@ static int router_run(const void* x, const void* w_r, const void* w_rT, const fl
             const size_t pstride = (size_t)T * E;
 #define MOE_GATE_LAUNCH(N)                                                                              \
             cudaFuncSetAttribute(router_gate_kernel<N>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem); \
+            G = gate_grid<N>(T, smem);                                                                         \
             router_gate_kernel<N><<<G, kRouterWarps * 32, smem, s>>>(lg, sp.S, pstride, gbias, bias, T, E, k, gating, o);
             if (npl <= 2) { MOE_GATE_LAUNCH(2) }
             else if (npl <= 4) { MOE_GATE_LAUNCH(4) }
@@ -1008,7 +1016,7 @@ extern "C" int moe_router_from_logits(const float* logits, const float* bias, in
     MOE_REQUIRE(ws && ws_bytes >= need, MOE_ERR_WORKSPACE, "moe_router_from_logits: workspace %zu < %zu", ws_bytes,
                 need);
     cudaStream_t s = static_cast<cudaStream_t>(stream);
-    const int G = gate_grid(T);              // <= router_grid(T), which sizes the workspace
+    int G = 1;                               // set at launch, <= router_grid(T), which sizes the workspace
     const RouterWs w = router_ws_layout(ws, T, 8, E, 4, false, false, false, 1);
     GateOut o{topk_ids, gates, nullptr, w.partial_P, w.partial_C, w.ticket};
     if (T > 0) {
@@ -1016,6 +1024,7 @@ extern "C" int moe_router_from_logits(const float* logits, const float* bias, in
         const int npl = cdiv(E, 32);
 #define MOE_GATE_LAUNCH2(N)                                                                             \
         cudaFuncSetAttribute(router_gate_kernel<N>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem); \
+        G = gate_grid<N>(T, smem);                                                                         \
         router_gate_kernel<N><<<G, kRouterWarps * 32, smem, s>>>(logits, 1, 0, nullptr, bias, T, E, k, gating, o);
         if (npl <= 2) { MOE_GATE_LAUNCH2(2) }
         else if (npl <= 4) { MOE_GATE_LAUNCH2(4) }
