@@ -58,17 +58,17 @@ def test_full_size_layer(name):
     torch.cuda.synchronize()
     assert moe.moe_check_device_error() == moe.MOE_OK, moe.moe_last_error_string()
     if cfg.dtype == "bf16":   # the down GEMM with the combine in its epilogue: the same eout and y bits
-        d = layer.d_out
+        dd = layer.d_out
         arr = moe.moe_combine_arrivals(cfg.T, cfg.h, dev)
         sh = bool(cfg.n_shared)
         eout_f, sh_f, y_f = moe.moe_expert_down_combine(
-            layer.act, d["tile_sched"], layer.packed, cfg.E, cfg.h, d["src_token"], d["dest_row"],
+            layer.act, dd["tile_sched"], layer.packed, cfg.E, cfg.h, dd["src_token"], dd["dest_row"],
             layer.r_out["gates"], arr, act_shared=layer.sh_act if sh else None,
             packed_shared=layer.shared_packed if sh else None)
         torch.cuda.synchronize()
         assert moe.moe_check_device_error() == moe.MOE_OK, moe.moe_last_error_string()
         assert torch.equal(y_f.view(torch.int16), y.view(torch.int16)), f"{name}: fused combine differs"
-        live = d["src_token"] >= 0
+        live = dd["src_token"] >= 0
         assert torch.equal(eout_f[live].view(torch.int16), layer.eout[live].view(torch.int16))
         if sh:
             assert torch.equal(sh_f.view(torch.int16), layer.sh_out.view(torch.int16))

@@ -135,34 +135,40 @@ __device__ __forceinline__ void gate_token(float (&L)[NPL], int t, int E, int k,
     }
 
     // k rounds of warp argmax on the selection score, on order-preserving keys: a warp max reduction finds the
-    // largest key, a warp min reduction the smallest expert index holding it (equal scores: smaller index)
+    // largest key, a warp min reduction the smallest expert index holding it (equal scores: smaller index). Each lane
+    // keeps its own largest remaining key (the lowest slot holding it) and that expert's probability, so a round
+    // rescans the slots of the one lane that gave up its expert only.
     unsigned key[NPL];
 #pragma unroll
     for (int i = 0; i < NPL; ++i) key[i] = live[i] ? score_key(score[i]) : 0u;
+    unsigned lmax = key[0];
+    int lslot = 0;
+    float lprob = prob[0];
+#pragma unroll
+    for (int i = 1; i < NPL; ++i)
+        if (key[i] > lmax) { lmax = key[i]; lslot = i; lprob = prob[i]; }
     int sel_id[kMaxK];
     float sel_p[kMaxK];
     float psum = 0.f;
 #pragma unroll
     for (int j = 0; j < kMaxK; ++j) {
         if (j < k) {
-            unsigned lm = key[0];
-#pragma unroll
-            for (int i = 1; i < NPL; ++i) lm = max(lm, key[i]);
-            const unsigned m = seg_umax<SEG>(lm);
-            unsigned li = 0xffffffffu;
-#pragma unroll
-            for (int i = NPL - 1; i >= 0; --i)
-                if (key[i] == m) li = (unsigned)(sl + 32 * i);
-            int bi = (int)seg_umin<SEG>(li);
+            const unsigned m = seg_umax<SEG>(lmax);
+            int bi = (int)seg_umin<SEG>(lmax == m ? (unsigned)(sl + 32 * lslot) : 0xffffffffu);
             if (bi >= E) bi = E - 1;          // only reachable with NaN scores: keeps every index in bounds
-            const int owner = seg0 + (bi & 31), slot = bi >> 5;
-            float pv = 0.f;
+            const int owner = seg0 + (bi & 31);
+            const float pv = __shfl_sync(0xffffffffu, lprob, owner);
+            if (lane == owner) {               // this lane's expert is taken: its next largest key
 #pragma unroll
-            for (int i = 0; i < NPL; ++i) {
-                if (i == slot) pv = prob[i];
-                if (i == slot && lane == owner) key[i] = 0u;               // taken
+                for (int i = 0; i < NPL; ++i)
+                    if (i == lslot) key[i] = 0u;
+                lmax = key[0];
+                lslot = 0;
+                lprob = prob[0];
+#pragma unroll
+                for (int i = 1; i < NPL; ++i)
+                    if (key[i] > lmax) { lmax = key[i]; lslot = i; lprob = prob[i]; }
             }
-            pv = __shfl_sync(0xffffffffu, pv, owner);
             sel_id[j] = bi;
             sel_p[j] = pv;
             psum += pv;
