@@ -98,7 +98,9 @@ int moe_router(const void* x, const void* w_r, const float* bias, int T, int h, 
  *   every call), for fp32 a copy of w_r [h,E]. moe_router_packed takes that buffer in place of w_r; every other
  *   argument, the workspace size and the outputs (bitwise) are those of moe_router. Errors as moe_router;
  *   moe_pack_router_weight: MOE_ERR_INVALID_ARG for h % 8 != 0, E outside [1, 1024] or a null / misaligned
- *   pointer. */
+ *   pointer. With bf16 and E <= 32 the kernel's blocks wait (bounded, moe_set_wait_limit) for the packed rows'
+ *   bulk copy into shared memory: if the wait runs out, moe_check_device_error() then reports MOE_ERR_TIMEOUT
+ *   (site 0x130) and that call's outputs are not to be used; the context stays usable. */
 size_t moe_router_packed_bytes(int h, int E, int dtype);
 int moe_pack_router_weight(const void* w_r, int h, int E, int dtype, void* packed, void* stream);
 int moe_router_packed(const void* x, const void* w_packed, const float* bias, int T, int h, int E, int k, int dtype,

@@ -1,5 +1,5 @@
-"""Failure detection on the GPU without a fault: the mbarrier waits of the tensor-core GEMMs and of the
-dispatch's bulk row copy are bounded. With the limit forced down to one poll the kernel gives up, latches
+"""Failure detection on the GPU without a fault: the mbarrier waits of the tensor-core GEMMs, of the
+dispatch's bulk row copy and of the router's weight staging are bounded. With the limit forced down to one poll the kernel gives up, latches
 MOE_ERR_TIMEOUT in the library's device error word, drains its copies (and MMAs, freeing its tensor memory)
 and returns; the context stays usable and the next call, at the default limit, is correct."""
 import pytest
@@ -74,3 +74,35 @@ def test_dispatch_copy_wait_timeout_reported_and_recoverable():
     rows = dest[kept]
     toks = torch.arange(T, device="cuda")[:, None].expand(T, k)[kept]
     assert torch.equal(o["buf"][rows].view(torch.int16), x[toks].view(torch.int16))
+
+
+def test_router_weight_wait_timeout_reported_and_recoverable():
+    """The packed-weight router (bf16, E <= 32) has the bulk-copy unit bring the router weight into each block's
+    shared memory and waits for it on an mbarrier; with the limit at one poll the wait gives up before a 128 KB
+    copy can have landed, latches MOE_ERR_TIMEOUT (site 0x130), waits for the copy and returns; the next call at
+    the default limit gives the same outputs as a call before the forced timeout."""
+    import torch
+    from top_routing_dispatch_moe_gb300 import moe
+    torch.manual_seed(7)
+    T, h, E, k = 2048, 4096, 16, 2
+    x = torch.randn(T, h, device="cuda").to(torch.bfloat16)
+    w = (torch.randn(h, E, device="cuda") * 0.05).to(torch.bfloat16)
+    wp = moe.moe_pack_router_weight(w)
+    ref = moe.moe_router(x, w, None, k, "softmax", w_packed=wp)
+    torch.cuda.synchronize()
+    assert moe.moe_check_device_error() == moe.MOE_OK
+    try:
+        moe.moe_set_wait_limit(1)
+        moe.moe_router(x, w, None, k, "softmax", w_packed=wp)
+        rc = moe.moe_check_device_error()
+        msg = moe.moe_last_error_string()
+    finally:
+        moe.moe_set_wait_limit(0)
+    assert rc == moe.MOE_ERR_TIMEOUT, (rc, msg)
+    assert "site 0x130" in msg
+    again = moe.moe_router(x, w, None, k, "softmax", w_packed=wp)
+    torch.cuda.synchronize()
+    assert moe.moe_check_device_error() == moe.MOE_OK
+    for key in ("ids", "gates", "logits", "counts", "P", "aux"):
+        assert torch.equal(again[key], ref[key]), key
+

@@ -276,9 +276,11 @@ __device__ __forceinline__ void stage_router_weight(const T* __restrict__ w_r, i
     }
 }
 
-// U = 16-byte x chunks per token and lane in flight: 4 while the accumulators are small (E <= 8), else 2.
+// U = 16-byte x chunks per token and lane in flight: 4 while the accumulators are small (E <= 8), else 2. Two
+// blocks per SM for EMAX = 8; with 16 or 32 experts the two tokens' packed accumulators alone take 64 or 128
+// registers, so one block per SM keeps them out of local memory.
 template <typename T, int EMAX, int U>
-__global__ void __launch_bounds__(kRouterWarps * 32, 2)
+__global__ void __launch_bounds__(kRouterWarps * 32, EMAX <= 8 ? 2 : 1)
 router_small_kernel(const T* __restrict__ x, const T* __restrict__ w_r, const float* __restrict__ bias, int T_,
                     int h, int E, int k, int gating, GateOut o) {
     pdl_trigger();                            // the finalize may launch now (it waits for this kernel's partials)
@@ -387,11 +389,29 @@ __device__ __forceinline__ void prefetch_row_l2(const __nv_bfloat16* x, int T_, 
                      ::"l"(reinterpret_cast<uint64_t>(x + (size_t)t * h)), "r"((unsigned)(h * 2)) : "memory");
 }
 
+// The packed router weight's rows reach shared memory through the bulk-copy unit, completing on an mbarrier
+// (addresses and sizes multiples of 16 bytes). A wait polls at most `limit` times, 32 ns apart.
+__device__ __forceinline__ void bulk_row_to_shared(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar) {
+    asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
+                 ::"r"(dst), "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes), "r"(bar) : "memory");
+}
+__device__ __forceinline__ bool bar_wait(uint32_t bar, uint32_t parity, long long limit) {
+    for (long long i = 0; i < limit; ++i) {
+        uint32_t ok;
+        asm volatile("{\n\t.reg .pred p;\n\tmbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+                     "selp.u32 %0, 1, 0, p;\n\t}" : "=r"(ok) : "r"(bar), "r"(parity) : "memory");
+        if (ok) return true;
+        __nanosleep(32);
+    }
+    return false;
+}
+constexpr long long kWeightDrainLimit = 1LL << 24;
+
 template <int NB, int U>   // NB blocks of 8 experts (E <= 8 NB); 2 x U chunks of 32 columns in flight per warp
 __global__ void __launch_bounds__(kRouterWarps * 32, 2)
 router_mma_kernel(const __nv_bfloat16* __restrict__ x, const __nv_bfloat16* __restrict__ w_r,
                   const __nv_bfloat16* __restrict__ w_rT, const float* __restrict__ bias, int T_, int h, int E, int k,
-                  int gating, GateOut o) {
+                  int gating, GateOut o, unsigned* err, long long wait_limit) {
     pdl_trigger();                            // the finalize may launch now (it waits for this kernel's partials)
     // (an L2 prefetch of the block's first 16 token rows here was measured: the router weight's staging then
     // queued behind it, and the x loads ended no sooner)
@@ -412,25 +432,17 @@ router_mma_kernel(const __nv_bfloat16* __restrict__ x, const __nv_bfloat16* __re
     // keeps 8 vector loads in flight.
     const int d0 = c_begin * 32, d1 = min(h, c_end * 32), dz = c_end * 32;
     const __nv_bfloat16 zero = __float2bfloat16_rn(0.f);
+    // (packed weight) the mbarrier on which its rows land, after the histogram
+    const uint32_t wbar = (uint32_t)__cvta_generic_to_shared(s_hist + ((E + 1) & ~1));
     if (w_rT) {
-        // the packed transpose W_r^T [E][h]: each row's slice is contiguous, copied with 16-byte vectors (d0 and h
-        // are multiples of 8 elements, the shared row stride a multiple of 16 bytes); rows e >= E are zero
-        const int vpr = (d1 - d0) / 8, nvec = EP * vpr;
-        constexpr int B = 8;
-        for (int v0 = lane; v0 < nvec; v0 += 32 * B) {
-            uint4 r[B];
-#pragma unroll
-            for (int b = 0; b < B; ++b) {
-                const int v = v0 + 32 * b, e = v / max(vpr, 1);
-                r[b] = make_uint4(0, 0, 0, 0);
-                if (v < nvec && e < E) r[b] = __ldg(reinterpret_cast<const uint4*>(w_rT + (size_t)e * h + d0) + (v - e * vpr));
-            }
-#pragma unroll
-            for (int b = 0; b < B; ++b) {
-                const int v = v0 + 32 * b, e = v / max(vpr, 1);
-                if (v < nvec) *reinterpret_cast<uint4*>(wT + (size_t)e * stride + d0 + 8 * (v - e * vpr)) = r[b];
-            }
+        // the packed transpose W_r^T [E][h]: once every thread has its first x loads in flight, thread 0 has the
+        // bulk-copy unit bring each expert's row into its padded shared row (below); rows e >= E are zero
+        if (threadIdx.x == 0) {
+            asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(wbar) : "memory");
+            asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
         }
+        if (warp == 0)
+            for (int f = lane; f < (EP - E) * h; f += 32) wT[(size_t)(E + f / h) * stride + f % h] = zero;
     } else if (E == EP) {
         const int nvec = (d1 - d0) * EP / 8;
         const uint4* src = reinterpret_cast<const uint4*>(w_r + (size_t)d0 * EP);
@@ -503,6 +515,21 @@ router_mma_kernel(const __nv_bfloat16* __restrict__ x, const __nv_bfloat16* __re
         // two register buffers of U chunks: the loads of one are in flight while the other is multiplied
         uint4 a0[U], b0[U], a1[U], b1[U];
         load(a0, b0, x0, x1, c_begin);
+        if (w_rT && tile == (int)blockIdx.x) {
+            if (threadIdx.x == 0) {
+                asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(wbar),
+                             "r"((unsigned)(E * h * 2)) : "memory");
+                for (int e = 0; e < E; ++e)
+                    bulk_row_to_shared((uint32_t)__cvta_generic_to_shared(wT + (size_t)e * stride),
+                                       w_rT + (size_t)e * h, (uint32_t)(h * 2), wbar);
+            }
+            if (!bar_wait(wbar, 0, wait_limit)) {
+                // the weight did not land in time: report it, and wait for the copy before going on (no copy may
+                // land in the shared memory of an exited block); the results of this call are not to be used
+                latch_device_error(err, kDevErrTimeout, 0x130u);
+                if (!bar_wait(wbar, 0, kWeightDrainLimit)) latch_device_error(err, kDevErrTimeout, 0x131u);
+            }
+        }
         for (int c0 = c_begin; c0 < c_end; c0 += 2 * U) {
             load(a1, b1, x0, x1, c0 + U);
             compute(acc, a0, b0, c0);
@@ -675,64 +702,84 @@ router_gate_kernel(const float* __restrict__ logits, int nparts, size_t part_str
 }
 
 // Counts, f, P and aux from the per-block partials of `grid` gating blocks. Each block takes chunks of
-// kFinExperts experts (block b: chunks b, b + gridDim.x, ...); thread (s, e) of its [S][chunk] arrangement (S a
-// power of two) sums the partials of gating blocks s, s + S, s + 2S, ... of expert e, and the S slice sums of each
-// expert are added by a pairwise tree over the slices. Every block adds its experts' f_e P_e in expert order; with
-// several blocks, the last one to arrive (counted on `ticket`, which the gating kernel zeroed) adds the blocks'
-// sums in block order. No step depends on timing, so the results are the same on every run.
+// kFinExperts experts (block b: chunks b, b + gridDim.x, ...). Thread (s, i) of its [kFinSlices][kFinExperts]
+// arrangement sums the partials of gating blocks s, s + kFinSlices, ... of expert e0 + i (four loads in flight;
+// a warp's loads read 8 consecutive experts of 4 rows); the 4 slices of a warp are added by a shuffle tree, then
+// the 32 warps' sums by one warp (eight in warp order per lane, then a shuffle tree). Every block adds its experts' f_e P_e in expert order; with several blocks, the
+// last one to arrive (counted on `ticket`, which the gating kernel zeroed) adds the blocks' sums in block order.
+// No step depends on timing, so the results are the same on every run.
 constexpr int kFinExperts = 8;
-__global__ void __launch_bounds__(1024)
+constexpr int kFinThreads = 1024;
+constexpr int kFinSlices = kFinThreads / kFinExperts;
+__global__ void __launch_bounds__(kFinThreads, 1)
 router_finalize(const float* __restrict__ partial_P, const int32_t* __restrict__ partial_C, int grid, int T_, int E,
                 int k, float alpha, int32_t* counts, float* f, float* P, float* aux, float* term_part,
                 unsigned* ticket) {
     pdl_wait();                               // the gating kernel's partials and its zeroed ticket
-    __shared__ float s_p[1024];
-    __shared__ int s_c[1024];
+    constexpr int NW = kFinThreads / 32;
+    __shared__ float s_p[NW][kFinExperts];
+    __shared__ int s_c[NW][kFinExperts];
     __shared__ float s_t[kFinExperts];
-    const int tid = threadIdx.x;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int sl = tid / kFinExperts, i = tid % kFinExperts;
     float term = 0.f;                                    // thread 0: this block's sum of f_e P_e
     for (int e0 = blockIdx.x * kFinExperts; e0 < E; e0 += gridDim.x * kFinExperts) {
-        const int ew = min(kFinExperts, E - e0);
-        int S = 1;
-        while (2 * S * ew <= (int)blockDim.x) S *= 2;
-        const int s = tid / ew, e = e0 + tid % ew;
+        const int e = e0 + i;
         float ps[4] = {0.f, 0.f, 0.f, 0.f};
         int cs[4] = {0, 0, 0, 0};
-        if (s < S) {
-            int b = s;
-            for (; b + 3 * S < grid; b += 4 * S) {       // four partials in flight
+        if (e < E) {
+            int b = sl;
+            for (; b + 3 * kFinSlices < grid; b += 4 * kFinSlices) {
 #pragma unroll
                 for (int u = 0; u < 4; ++u) {
-                    ps[u] += partial_P[(size_t)(b + u * S) * E + e];
-                    cs[u] += partial_C[(size_t)(b + u * S) * E + e];
+                    ps[u] += partial_P[(size_t)(b + u * kFinSlices) * E + e];
+                    cs[u] += partial_C[(size_t)(b + u * kFinSlices) * E + e];
                 }
             }
-            for (; b < grid; b += S) {
+            for (; b < grid; b += kFinSlices) {
                 ps[0] += partial_P[(size_t)b * E + e];
                 cs[0] += partial_C[(size_t)b * E + e];
             }
         }
-        s_p[tid] = (ps[0] + ps[1]) + (ps[2] + ps[3]);
-        s_c[tid] = cs[0] + cs[1] + cs[2] + cs[3];
-        for (int st = S / 2; st > 0; st >>= 1) {         // pairwise tree over the slices, a fixed order
-            __syncthreads();
-            if (s < st) { s_p[tid] += s_p[tid + st * ew]; s_c[tid] += s_c[tid + st * ew]; }
+        float tp = (ps[0] + ps[1]) + (ps[2] + ps[3]);
+        int tc = cs[0] + cs[1] + cs[2] + cs[3];
+#pragma unroll
+        for (int o = 16; o >= kFinExperts; o >>= 1) {      // the warp's slices of expert i: lanes i, i + 8, ...
+            tp += __shfl_down_sync(0xffffffffu, tp, o);
+            tc += __shfl_down_sync(0xffffffffu, tc, o);
+        }
+        if (lane < kFinExperts) {
+            s_p[warp][lane] = tp;
+            s_c[warp][lane] = tc;
         }
         __syncthreads();
-        if (tid < ew) {
-            const float tp = s_p[tid];
-            const int tc = s_c[tid];
-            const int ee = e0 + tid;
-            const float Pe = T_ > 0 ? tp / (float)T_ : 0.f;
-            const float fe = T_ > 0 ? (float)tc / ((float)k * (float)T_) : 0.f;
-            counts[ee] = tc;
-            f[ee] = fe;
-            P[ee] = Pe;
-            s_t[tid] = fe * Pe;
+        if (warp == 0) {          // lane (q, i): warps 8q .. 8q + 7 of expert i in order, then a shuffle tree over q
+            constexpr int WQ = NW / (32 / kFinExperts);
+            const int q = lane / kFinExperts;
+            float sp = 0.f;
+            int sc = 0;
+#pragma unroll
+            for (int w = 0; w < WQ; ++w) {
+                sp += s_p[q * WQ + w][i];
+                sc += s_c[q * WQ + w][i];
+            }
+#pragma unroll
+            for (int o = 16; o >= kFinExperts; o >>= 1) {
+                sp += __shfl_down_sync(0xffffffffu, sp, o);
+                sc += __shfl_down_sync(0xffffffffu, sc, o);
+            }
+            if (lane < kFinExperts && e < E) {
+                const float Pe = T_ > 0 ? sp / (float)T_ : 0.f;
+                const float fe = T_ > 0 ? (float)sc / ((float)k * (float)T_) : 0.f;
+                counts[e] = sc;
+                f[e] = fe;
+                P[e] = Pe;
+                s_t[lane] = fe * Pe;
+            }
         }
         __syncthreads();
         if (tid == 0)
-            for (int i = 0; i < ew; ++i) term += s_t[i];
+            for (int j = 0; j < min(kFinExperts, E - e0); ++j) term += s_t[j];
         __syncthreads();                                 // s_p, s_c and s_t are rewritten by the next chunk
     }
     if (tid != 0) return;
@@ -778,9 +825,11 @@ static int gate_grid(int T, size_t smem) {
         per_sm = 1;
     return std::max(1, std::min(router_grid(T), per_sm * num_sms()));
 }
-// The fused small-E kernel stages the router weight into every block, takes two tokens per warp, and its
-// register budget allows two blocks per SM.
-static int router_small_grid(int T) { return std::max(1, std::min(cdiv(T, 2 * kRouterWarps), 2 * num_sms())); }
+// The fused small-E kernel stages the router weight into every block and takes two tokens per warp; its register
+// budget allows two blocks per SM for E <= 8, one otherwise.
+static int router_small_grid(int T, int E) {
+    return std::max(1, std::min(cdiv(T, 2 * kRouterWarps), (E <= 8 ? 2 : 1) * num_sms()));
+}
 
 static size_t small_smem_bytes(int h, int E, int el) {
     return align_up((size_t)E * h * el, 16) + (size_t)kRouterWarps * E * sizeof(float) + (size_t)E * sizeof(int);
@@ -792,7 +841,7 @@ static int mma_blocks(int E) { return E <= 8 ? 1 : E <= 16 ? 2 : 4; }
 static size_t mma_smem_bytes(int h, int E) {
     const int EP = 8 * mma_blocks(E);
     return (size_t)EP * mma_wt_stride(h) * 2 + (size_t)kRouterWarps * kMmaTokens * EP * sizeof(float) +
-           (size_t)kRouterWarps * E * sizeof(float) + (size_t)E * sizeof(int);
+           (size_t)kRouterWarps * E * sizeof(float) + (size_t)E * sizeof(int) + 16;   // + the weight's mbarrier
 }
 static int router_mma_grid(int T) { return std::max(1, std::min(cdiv(T, kMmaTokens), 2 * num_sms())); }
 static bool use_small_path(int h, int E, int el) {
@@ -882,17 +931,20 @@ static int router_run(const void* x, const void* w_r, const void* w_rT, const fl
     MOE_REQUIRE(ws_bytes >= w.bytes && (w.bytes == 0 || ws), MOE_ERR_WORKSPACE,
                 "moe_router: workspace %zu < %zu bytes", ws_bytes, w.bytes);
     cudaStream_t s = static_cast<cudaStream_t>(stream);
-    int G = !small ? 1 : dtype == MOE_BF16 ? router_mma_grid(T) : router_small_grid(T);   // !small: set at launch
+    int G = !small ? 1 : dtype == MOE_BF16 ? router_mma_grid(T) : router_small_grid(T, E);   // !small: set at launch
     GateOut o{topk_ids, gates, logits, w.partial_P, w.partial_C, w.ticket};
     if (T > 0) {
         if (small && dtype == MOE_BF16) {
             const size_t smem = mma_smem_bytes(h, E);
+            unsigned* err = device_error_word();
+            MOE_REQUIRE(err, MOE_ERR_CUDA, "moe_router: device error word unavailable");
             const __nv_bfloat16* xb = static_cast<const __nv_bfloat16*>(x);
             const __nv_bfloat16* wb = static_cast<const __nv_bfloat16*>(w_r);
             const __nv_bfloat16* wtb = static_cast<const __nv_bfloat16*>(w_rT);
 #define MOE_MMA_LAUNCH(NB, UU)                                                                                \
             cudaFuncSetAttribute(router_mma_kernel<NB, UU>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem); \
-            router_mma_kernel<NB, UU><<<G, kRouterWarps * 32, smem, s>>>(xb, wb, wtb, bias, T, h, E, k, gating, o);
+            router_mma_kernel<NB, UU><<<G, kRouterWarps * 32, smem, s>>>(xb, wb, wtb, bias, T, h, E, k, gating, o, err, \
+                                                                      wait_limit());
             switch (mma_blocks(E)) {
                 case 1: { MOE_MMA_LAUNCH(1, 4) } break;
                 case 2: { MOE_MMA_LAUNCH(2, 4) } break;
@@ -958,7 +1010,7 @@ static int router_run(const void* x, const void* w_r, const void* w_rT, const fl
             if (int rc = check_launch("router_gate_kernel")) return rc;
         }
     }
-    const cudaError_t le = launch_pdl(router_finalize, dim3(finalize_grid(T, E)), dim3(1024), 0, s,
+    const cudaError_t le = launch_pdl(router_finalize, dim3(finalize_grid(T, E)), dim3(kFinThreads), 0, s,
                                       (const float*)w.partial_P, (const int32_t*)w.partial_C, T > 0 ? G : 0, T, E, k,
                                       alpha, counts, f, P, aux, w.term_part, w.ticket);
     return check_launch(le, "router_finalize");
@@ -1040,7 +1092,7 @@ extern "C" int moe_router_from_logits(const float* logits, const float* bias, in
 #undef MOE_GATE_LAUNCH2
         if (int rc = check_launch("router_gate_kernel")) return rc;
     }
-    const cudaError_t le = launch_pdl(router_finalize, dim3(finalize_grid(T, E)), dim3(1024), 0, s,
+    const cudaError_t le = launch_pdl(router_finalize, dim3(finalize_grid(T, E)), dim3(kFinThreads), 0, s,
                                       (const float*)o.partial_P, (const int32_t*)o.partial_C, T > 0 ? G : 0, T, E, k,
                                       alpha, counts, f, P, aux, w.term_part, w.ticket);
     return check_launch(le, "router_finalize");
