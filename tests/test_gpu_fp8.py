@@ -32,10 +32,12 @@ def _problem(T, h, E, k, seed):
 
 
 @pytest.mark.parametrize("T,h,E,k,C", [(300, 256, 4, 2, 0), (500, 384, 8, 2, 100), (1, 128, 2, 1, 0),
-                                       (257, 1024, 8, 4, 150), (5000, 128, 1024, 8, 0)])
+                                       (257, 1024, 8, 4, 150), (4000, 4096, 8, 2, 1250), (1500, 12288, 8, 2, 450),
+                                       (5000, 128, 1024, 8, 0)])
 def test_dispatch_fp8_bit_exact(T, h, E, k, C):
-    """Small count tables take the fused launch (scan, scatter and quantised copy in one kernel); the last case
-    (E = 1024, T k = 40000) the separate count / scan / scatter / copy launches."""
+    """Small count tables take the fused launch (scan, scatter and quantised copy in one kernel; among them the
+    page-3 width with 27 tokens per block, and 24 KB rows); the last case (E = 1024, T k = 40000) the separate
+    count / scan / scatter / copy launches."""
     import torch
     from top_routing_dispatch_moe_gb300 import moe
     ids, xb, x32 = _problem(T, h, E, k, seed=T + h)
