@@ -147,8 +147,8 @@ __device__ __forceinline__ void gate_token(float (&L)[NPL], int t, int E, int k,
 #pragma unroll
     for (int i = 1; i < NPL; ++i)
         if (key[i] > lmax) { lmax = key[i]; lslot = i; lprob = prob[i]; }
-    int sel_id[kMaxK];
-    float sel_p[kMaxK];
+    int my_id = 0;                         // lane sl keeps choice j = sl (for the writes below)
+    float my_p = 0.f;
     float psum = 0.f;
 #pragma unroll
     for (int j = 0; j < kMaxK; ++j) {
@@ -169,19 +169,18 @@ __device__ __forceinline__ void gate_token(float (&L)[NPL], int t, int E, int k,
                 for (int i = 1; i < NPL; ++i)
                     if (key[i] > lmax) { lmax = key[i]; lslot = i; lprob = prob[i]; }
             }
-            sel_id[j] = bi;
-            sel_p[j] = pv;
+            if (sl == j) {
+                my_id = bi;
+                my_p = pv;
+            }
             psum += pv;
         }
     }
     const float norm = (gating == MOE_GATING_SOFTMAX || gating == MOE_GATING_SOFTMAX_SELBIAS) ? 1.f : 1.f / psum;
-#pragma unroll
-    for (int j = 0; j < kMaxK; ++j) {
-        if (valid && j < k && sl == j) {
-            o.ids[(size_t)t * k + j] = sel_id[j];
-            o.gates[(size_t)t * k + j] = sel_p[j] * norm;
-            atomicAdd(&s_hist[sel_id[j]], 1);
-        }
+    if (valid && sl < k) {                 // the k choices in one store per output (k <= 16 <= SEG)
+        o.ids[(size_t)t * k + sl] = my_id;
+        o.gates[(size_t)t * k + sl] = my_p * norm;
+        atomicAdd(&s_hist[my_id], 1);
     }
 }
 
