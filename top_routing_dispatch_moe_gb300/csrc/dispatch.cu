@@ -386,21 +386,16 @@ dispatch_fused_kernel(const T* __restrict__ x, const int32_t* __restrict__ ids, 
         const int tid = threadIdx.x, sl = tid / E, ex = tid - sl * E;
         if (sl < S) {
             int pb = 0, pt = 0;
-            int c = sl;
-            for (; c + 3 * S < nchunks; c += 4 * S) {   // four loads in flight
+            for (int c = sl; c < nchunks; c += 4 * S) {   // up to four loads in flight, the last round too
                 int v[4];
 #pragma unroll
-                for (int u = 0; u < 4; ++u) v[u] = __ldg(chunk_counts + (size_t)(c + u * S) * E + ex);
+                for (int u = 0; u < 4; ++u)
+                    v[u] = c + u * S < nchunks ? __ldg(chunk_counts + (size_t)(c + u * S) * E + ex) : 0;
 #pragma unroll
                 for (int u = 0; u < 4; ++u) {
                     pt += v[u];
                     pb += c + u * S < (int)blockIdx.x ? v[u] : 0;
                 }
-            }
-            for (; c < nchunks; c += S) {
-                const int v = __ldg(chunk_counts + (size_t)c * E + ex);
-                pt += v;
-                pb += c < (int)blockIdx.x ? v : 0;
             }
             s_rb[tid] = pb;
             s_rt[tid] = pt;
@@ -565,6 +560,9 @@ __global__ void dense_sched_kernel(int rows, int32_t* sched) {
 }
 
 static int num_chunks(int T, int k) { return T <= 0 ? 0 : cdiv(T, kChunkA / k); }
+// Threads of a count block: one per assignment of its chunk, in whole warps (a chunk of the fused path holds
+// far fewer than kChunkA assignments when T is small next to the SM count: 54 at the page-3 shape).
+static int count_threads(int tpc, int k) { return std::max(32, std::min(kChunkA, (tpc * k + 31) / 32 * 32)); }
 
 // Ring of the fused kernel's bulk row copy: stages of min(row bytes, 16 KB), as many as fit (at most 32)
 // beside the kernel's tables in 227 KB of shared memory less 1 KB for its static variables and margin.
@@ -634,7 +632,7 @@ extern "C" int moe_dispatch(const void* x, const int32_t* topk_ids, int T, int h
     const int tpc_f = fused_tokens_per_chunk(T, E, k, std::min(kFusedMaxChunks, num_sms()));
     if (tpc_f > 0) {
         const int nch = cdiv(T, tpc_f);
-        dispatch_count_kernel<<<nch, kChunkA, E * sizeof(int), s>>>(topk_ids, T, E, k, tpc_f, chunk, err);
+        dispatch_count_kernel<<<nch, count_threads(tpc_f, k), E * sizeof(int), s>>>(topk_ids, T, E, k, tpc_f, chunk, err);
         if (int rc = check_launch("dispatch_count_kernel")) return rc;
         const RingPlan rp = ring_plan(E, (size_t)h * (dtype == MOE_BF16 ? 2 : 4));
         MOE_REQUIRE(rp.stages >= 2, MOE_ERR_INVALID_ARG, "moe_dispatch: no room for the copy ring (E=%d, h=%d)", E, h);
@@ -841,7 +839,8 @@ extern "C" int moe_dispatch_fp8(const void* x, const int32_t* topk_ids, int T, i
     const int tpc_f = fused_tokens_per_chunk(T, E, k, std::min(kFusedMaxChunks, num_sms()));
     if (tpc_f > 0) {                              // count, then scan + scatter + quantised copy in one launch
         const int nchf = cdiv(T, tpc_f);
-        dispatch_count_kernel<<<nchf, kChunkA, E * sizeof(int), s>>>(topk_ids, T, E, k, tpc_f, chunk, err);
+        dispatch_count_kernel<<<nchf, count_threads(tpc_f, k), E * sizeof(int), s>>>(topk_ids, T, E, k, tpc_f, chunk,
+                                                                                   err);
         if (int rc = check_launch("dispatch_count_kernel")) return rc;
         const size_t smem = (size_t)fused_smem_ints(E) * sizeof(int);
         cudaFuncSetAttribute(dispatch_fused_kernel<__nv_bfloat16, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
