@@ -320,6 +320,20 @@ class MoELayer:
                        shared_dW_down=b["sh_dW_down"][0])
         return out
 
+    def capture_forward(self, x, stream=None):
+        """The forward of x (device-resident, kept at this address) captured once into a CUDA graph; each
+        `replay()` then runs the layer's launches from the graph instead of from the host, into the same output
+        buffers (`self.y`, `self.r_out`, `self.d_out`, ...). Call `forward` once before (it sets up the kernels'
+        attributes); the graph holds the layer's buffers and x by address, so neither may be freed or moved while
+        it is in use."""
+        import torch
+        s = stream if stream is not None else torch.cuda.Stream(device=self.device)
+        g = torch.cuda.CUDAGraph()
+        torch.cuda.synchronize(self.device)
+        with torch.cuda.graph(g, stream=s):
+            self.forward(x, stream=s)
+        return g
+
     def forward_host_batches(self, x_hosts, y_hosts):
         """Runs the layer over a sequence of batches that live in pinned host memory: x_hosts[i] -> y_hosts[i].
 
