@@ -379,6 +379,7 @@ dispatch_fused_kernel(const T* __restrict__ x, const int32_t* __restrict__ ids, 
                          ::"l"(reinterpret_cast<uint64_t>(x + (size_t)(t0 + i) * h)), "r"(row_bytes) : "memory");
     }
     pdl_wait();                               // the count table (dispatch_count_kernel) is complete from here on
+    pdl_trigger();                            // the grouped GEMM may launch; it waits for this kernel to complete
     {   // count table -> this chunk's base and the per-expert totals: S slices of chunks per expert in
         // parallel, then a tree over the slices (S = largest power of two with S * E <= kChunkA)
         int S = 1;

@@ -688,6 +688,10 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
+    // (launched as a programmatic dependent: everything above overlapped the previous kernel's tail; the tile
+    // schedule and the operands are read only from here on)
+    pdl_wait();
+    pdl_trigger();                           // the next kernel may launch; it waits for this one to complete
 
     const int E = p.wg_E > 0 ? p.wg_E : __ldg(p.sched + 1);
     const int KB = (p.K + BK - 1) / BK;
@@ -1058,7 +1062,6 @@ grouped_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_c
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const uint32_t rank = cluster_rank();
     const bool leader = rank == 0;
-    const int E = p.wg_E > 0 ? p.wg_E : __ldg(p.sched + 1);
     if (threadIdx.x == 0) {
         for (int s = 0; s < STAGES; ++s) { mbar_init(full(s), 1); mbar_init(empty(s), 1); }
         for (int a = 0; a < 2; ++a) { mbar_init(tfull(a), 1); mbar_init(tempty(a), 8); }
@@ -1070,6 +1073,11 @@ grouped_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_c
         prefetch_tmap(&tmB);
         if (p.sh_rows) { prefetch_tmap(&tmA2); prefetch_tmap(&tmB2); }
     }
+    // (launched as a programmatic dependent: the barrier set-up above overlapped the previous kernel's tail; the
+    // tile schedule and the operands are read only from here on)
+    pdl_wait();
+    pdl_trigger();                           // the next kernel may launch; it waits for this one to complete
+    const int E = p.wg_E > 0 ? p.wg_E : __ldg(p.sched + 1);
     // pair prefix: pp[e + 1] = sum over e' <= e of ceil(tiles_e' / 2) (routed mapping; the fp32 instantiation runs
     // the weight-gradient mapping only, and its store boxes occupy this region)
     if (EPI != EPI_F32 && warp == 2 && p.wg_E == 0) {
@@ -1425,7 +1433,9 @@ static int gemm(const void* a, long long a_rows, const void* b, long long b_rows
     }
     CUtensorMap mo, mo2;
     if (int rc = make_out_maps<EPI>(p, routed_rows, ma, &mo, &mo2)) return rc;
-    grouped_gemm_kernel<EPI, CF><<<num_sms(), NUM_THREADS, smem_bytes, s>>>(ma, mb, ma2, mb2, mo, mo2, p);
+    const cudaError_t le = launch_pdl(grouped_gemm_kernel<EPI, CF>, dim3(num_sms()), dim3(NUM_THREADS), smem_bytes, s, ma,
+                                      mb, ma2, mb2, mo, mo2, p);
+    if (le != cudaSuccess) return set_error(MOE_ERR_CUDA, "grouped_gemm_kernel launch: %s", cudaGetErrorString(le));
     return check_launch(EPI == EPI_SWIGLU ? "grouped_gemm_kernel<up_gate>"
                         : EPI == EPI_SWIGLU_SAVE ? "grouped_gemm_kernel<up_gate, save>"
                         : EPI == EPI_BF16 ? "grouped_gemm_kernel<bf16>"
@@ -1475,7 +1485,9 @@ static int gemm_pair(const void* a, long long a_rows, const void* b, long long b
     }
     CUtensorMap mo, mo2;
     if (int rc = make_out_maps<EPI>(p, routed_rows, ma, &mo, &mo2)) return rc;
-    grouped_gemm_pair_kernel<EPI><<<2 * clusters[dev], NUM_THREADS, smem_bytes, s>>>(ma, mb, ma2, mb2, mo, mo2, p);
+    const cudaError_t le = launch_pdl(grouped_gemm_pair_kernel<EPI>, dim3(2 * clusters[dev]), dim3(NUM_THREADS),
+                                      smem_bytes, s, ma, mb, ma2, mb2, mo, mo2, p);
+    if (le != cudaSuccess) return set_error(MOE_ERR_CUDA, "grouped_gemm_pair_kernel launch: %s", cudaGetErrorString(le));
     return check_launch(EPI == EPI_SWIGLU ? "grouped_gemm_pair_kernel<up_gate>"
                         : EPI == EPI_SWIGLU_SAVE ? "grouped_gemm_pair_kernel<up_gate, save>"
                         : EPI == EPI_SWIGLU_BWD ? "grouped_gemm_pair_kernel<swiglu_bwd>"
