@@ -33,6 +33,9 @@ import moe_inputs  # noqa: E402
 
 METRIC = "MoE-layer fwd tokens/s at 1 GB300; grouped-GEMM % bf16 peak; dispatch GB/s"
 
+TIMING_NOTE = ("ms_per_step: K forwards, each after an L2 flush, with CUDA events at each step's start and end; "
+               "stages_ms, roofline and the stage bandwidths: a second pass of K forwards with an event at every "
+               "stage boundary (those events serialise the stages' launches: ms_per_step_instrumented)")
 
 def _workload_desc(cfg, C):
     return (f"{cfg.name}: T={cfg.T} h={cfg.h} E={cfg.E} k={cfg.k} F={cfg.F} gating={cfg.gating} "
@@ -314,8 +317,10 @@ def build_layer(cfg, inp, dev, backward, fuse_combine=False):
 
 
 def time_forward(args, layer, x, flush, world, dev):
-    """K device-resident layer forwards, each after an L2 flush, with CUDA events around every stage on the
-    launching stream. Returns per-stage times, per-step times, the library's launch count and the clocks."""
+    """K device-resident layer forwards, each after an L2 flush, with CUDA events at each step's start and end on
+    the launching stream (the step time); then K more with an event at every stage boundary (the stage times, and
+    from them the up/gate roofline: an event between two launches serialises them, so those steps are longer).
+    Returns both, the library's launch count over the first pass and the clocks of both."""
     import torch
     import torch.distributed as dist
     from top_routing_dispatch_moe_gb300 import moe
@@ -329,7 +334,6 @@ def time_forward(args, layer, x, flush, world, dev):
         flush.zero_()
         torch.cuda.synchronize()
     assert moe.moe_check_device_error() == moe.MOE_OK, moe.moe_last_error_string()
-    events: dict = {}
     if world > 1:
         dist.barrier()
     torch.cuda.synchronize()
@@ -339,29 +343,45 @@ def time_forward(args, layer, x, flush, world, dev):
     # every step follows an L2 flush, the first one too (its launches then queue behind the flush instead of
     # reaching an idle GPU one by one from the host)
     flush.zero_()
+    step_ev = []
+    for _ in range(args.steps):
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        layer.forward(x)
+        e1.record()
+        step_ev.append((e0, e1))
+        flush.zero_()
+    torch.cuda.synchronize()
+    t_wall = time.perf_counter() - t_wall0
+    launches = moe.moe_launch_count() - launches0
+    if world > 1:
+        dist.barrier()
+    # the instrumented pass: the same steps with an event at every stage boundary
+    events: dict = {}
+    flush.zero_()
     for _ in range(args.steps):
         layer.forward(x, events=events)
         flush.zero_()
     torch.cuda.synchronize()
-    t_wall = time.perf_counter() - t_wall0
     window = (t_clk0, time.time())
     if world > 1:
         dist.barrier()
-    launches = moe.moe_launch_count() - launches0
     assert moe.moe_check_device_error() == moe.MOE_OK, moe.moe_last_error_string()
     from top_routing_dispatch_moe_gb300.layer import MoELayer
     stage_names = [s for s in MoELayer.STAGES if s in events]
     order = ["start"] + stage_names
     stage_ms = {s: [] for s in stage_names}
-    step_ms = []
+    inst_ms = []
     for i in range(args.steps):
         for a, b in zip(order[:-1], order[1:]):
             stage_ms[b].append(events[a][i].elapsed_time(events[b][i]))
-        step_ms.append(events["start"][i].elapsed_time(events[order[-1]][i]))
+        inst_ms.append(events["start"][i].elapsed_time(events[order[-1]][i]))
+    step_ms = [a.elapsed_time(b) for a, b in step_ev]
     ms = max_over_ranks(float(np.mean(step_ms)), world, dev)
     stats = {"median": float(np.median(step_ms)), "p10": float(np.percentile(step_ms, 10)),
              "p90": float(np.percentile(step_ms, 90))}
-    return dict(stage_ms=stage_ms, ms=ms, stats=stats, launches=int(launches), wall=t_wall, window=window)
+    return dict(stage_ms=stage_ms, ms=ms, stats=stats, launches=int(launches), wall=t_wall, window=window,
+                ms_instrumented=max_over_ranks(float(np.mean(inst_ms)), world, dev))
 
 
 def kept_and_active(cfg, layer):
@@ -441,8 +461,8 @@ def measure_extra_workload(args, name, world, dev, flush, clk, rank):
     t = time_forward(args, layer, x, flush, world, dev)
     kept, active = kept_and_active(cfg, layer)
     out = {"workload": _workload_desc(cfg, C), "value": world * cfg.T / (t["ms"] * 1e-3), "unit": "tokens/s",
-           "ms_per_step": t["ms"], "ms_per_step_stats": t["stats"], "kept_assignments": kept,
-           "dtype": "bf16" if cfg.dtype == "bf16" else "f32", "gpu_launches": t["launches"]}
+           "ms_per_step": t["ms"], "ms_per_step_stats": t["stats"], "ms_per_step_instrumented": t["ms_instrumented"],
+           "kept_assignments": kept, "dtype": "bf16" if cfg.dtype == "bf16" else "f32", "gpu_launches": t["launches"]}
     out.update(stage_metrics(cfg, t["stage_ms"], kept, active, layer.fuse_combine))
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         keep: dict = {}
@@ -521,7 +541,7 @@ def run_gpu(args, cfg, C):
 
     line = {"metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": ms, "ms_per_step_stats": t["stats"], "higher_is_better": True,
-            "scaling": "weak",
+            "scaling": "weak", "timing": TIMING_NOTE, "ms_per_step_instrumented": t["ms_instrumented"],
             "vs_baseline": None, "dtype": "bf16" if cfg.dtype == "bf16" else "f32", "data": "synthetic",
             "config": {"workload": _workload_desc(cfg, C), "global_batch": cfg.T * world, "tokens_per_gpu": cfg.T,
                        "parallelism": f"replicas x{world}", "l2": "flushed before every step (512 MiB write)",
