@@ -8,9 +8,10 @@
 // The top-k of diag(r) K diag(c) in a row is the top-k of L + log c (a row scaling keeps a row's order), so
 // the result is the selection-only bias log c for MOE_GATING_SOFTMAX_SELBIAS.
 //
-// One launch per iteration (sk_iter_kernel): every block first derives c from the previous iteration's
-// per-block partial column sums (the same fixed-order reduction in every block), then, one warp per token,
-// r_t from c and its own partial column sums of K r. A last one-block kernel writes log c.
+// One launch per iteration (sk_iter_kernel), each a programmatic dependent of the one before: every block first
+// derives c from the previous iteration's per-block partial column sums (the same fixed-order reduction in every
+// block, eight loads in flight per thread), then, one warp per token, r_t from c and its own partial column sums of
+// K r. A last one-block kernel writes log c.
 #include <math.h>
 #include <algorithm>
 #include "common.cuh"
@@ -33,7 +34,13 @@ __device__ __forceinline__ void sk_scalings(const float* __restrict__ partial, i
         const int tid = threadIdx.x, sl = tid / ne, ex = tid - sl * ne;
         float v = 0.f;
         if (sl < S)
-            for (int b = sl; b < G; b += S) v += partial[(size_t)b * E + e0 + ex];
+            for (int b0 = sl; b0 < G; b0 += 8 * S) {       // eight loads in flight, added in block order
+                float w[8];
+#pragma unroll
+                for (int u = 0; u < 8; ++u) w[u] = b0 + u * S < G ? partial[(size_t)(b0 + u * S) * E + e0 + ex] : 0.f;
+#pragma unroll
+                for (int u = 0; u < 8; ++u) v += w[u];
+            }
         s_red[tid] = v;
         for (int st = S / 2; st > 0; st >>= 1) {
             __syncthreads();
@@ -57,6 +64,8 @@ sk_iter_kernel(const float* __restrict__ logits, int T, int E, const float* __re
     float* s_red = sm + E;                               // [kSkThreads]
     float* s_part = s_red + kSkThreads;                  // [kSkWarps][E]
     const int G = gridDim.x;
+    pdl_wait();                              // a programmatic dependent of the previous iteration (or the router)
+    pdl_trigger();                           // the next iteration may launch; it waits for this one to complete
     if (partial_in) sk_scalings(partial_in, G, T, E, s_red, s_c);
     __syncthreads();
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
@@ -135,7 +144,8 @@ extern "C" int moe_sinkhorn_bias(const float* logits, int T, int E, int n_iter, 
         float* pout = part[it & 1];
 #define MOE_SK_LAUNCH(N)                                                                                 \
         cudaFuncSetAttribute(sk_iter_kernel<N>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);    \
-        sk_iter_kernel<N><<<G, kSkThreads, smem, s>>>(logits, T, E, pin, pout);
+        if (cudaError_t le = launch_pdl(sk_iter_kernel<N>, dim3(G), dim3(kSkThreads), smem, s, logits, T, E, pin, pout)) \
+            return set_error(MOE_ERR_CUDA, "sk_iter_kernel: %s", cudaGetErrorString(le));
         if (npl <= 1) { MOE_SK_LAUNCH(1) }
         else if (npl <= 2) { MOE_SK_LAUNCH(2) }
         else if (npl <= 4) { MOE_SK_LAUNCH(4) }
