@@ -8,7 +8,7 @@
 //
 // Kernels:
 //   ec_prob_kernel     softmax over experts per token, written transposed (probT [E][T]) through a shared
-//                      tile so that each expert's column is contiguous for the selection;
+//                      tile so that each expert's column is contiguous for the selection; slot[t][*] = -1;
 //   ec_select_kernel   one block per expert: exact radix select (4 passes of 8 bits over the fp32 score
 //                      bits, which order like the scores since scores are >= 0) finds the C-th largest
 //                      score, then an ordered compaction in token order keeps every larger score and the
@@ -25,10 +25,15 @@ namespace moe {
 constexpr int kEcMaxE = 256;
 
 __global__ void __launch_bounds__(256)
-ec_prob_kernel(const float* __restrict__ logits, int T, int E, float* __restrict__ probT) {
+ec_prob_kernel(const float* __restrict__ logits, int T, int E, float* __restrict__ probT,
+               int32_t* __restrict__ slot) {
     __shared__ float tile[32][kEcMaxE + 1];           // 32 tokens x E experts
+    pdl_wait();                                       // a programmatic dependent: the router's logits from here on
+    pdl_trigger();                                    // the selection may launch; it waits for this kernel
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const int t0 = blockIdx.x * 32;
+    for (int i = threadIdx.x; i < 32 * E; i += blockDim.x)    // slot[t][e] = -1 (not chosen) for these tokens
+        if (t0 + i / E < T) slot[(size_t)t0 * E + i] = -1;
     for (int tl = warp; tl < 32; tl += 8) {
         const int t = t0 + tl;
         if (t >= T) break;
@@ -59,18 +64,36 @@ ec_select_kernel(const float* __restrict__ probT, int T, int E, int C, int32_t* 
     __shared__ int s_tmp[32];
     __shared__ uint32_t s_prefix;
     __shared__ int s_kth;
+    pdl_wait();                                       // a programmatic dependent: probT and slot from here on
     const int e = blockIdx.x;
     const float* col = probT + (size_t)e * T;
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     if (threadIdx.x == 0) { s_prefix = 0u; s_kth = C; }
+    // this thread's scores t = threadIdx.x + i blockDim.x, kept in registers across the passes when they fit
+    constexpr int NV = 8;
+    const bool cached = T <= NV * (int)blockDim.x;
+    uint32_t kc[NV];
+#pragma unroll
+    for (int i = 0; i < NV; ++i) {
+        const int t = threadIdx.x + i * (int)blockDim.x;
+        kc[i] = cached && t < T ? __float_as_uint(col[t]) : 0u;
+    }
     uint32_t mask = 0u;
     for (int shift = 24; shift >= 0; shift -= 8) {
         for (int i = threadIdx.x; i < 256; i += blockDim.x) s_hist[i] = 0;
         __syncthreads();
         const uint32_t prefix = s_prefix;
-        for (int t = threadIdx.x; t < T; t += blockDim.x) {
-            const uint32_t key = __float_as_uint(col[t]);
-            if ((key & mask) == prefix) atomicAdd(&s_hist[(key >> shift) & 255u], 1);
+        if (cached) {
+#pragma unroll
+            for (int i = 0; i < NV; ++i) {
+                const int t = threadIdx.x + i * (int)blockDim.x;
+                if (t < T && (kc[i] & mask) == prefix) atomicAdd(&s_hist[(kc[i] >> shift) & 255u], 1);
+            }
+        } else {
+            for (int t = threadIdx.x; t < T; t += blockDim.x) {
+                const uint32_t key = __float_as_uint(col[t]);
+                if ((key & mask) == prefix) atomicAdd(&s_hist[(key >> shift) & 255u], 1);
+            }
         }
         __syncthreads();
         if (warp == 0) {
@@ -304,12 +327,11 @@ extern "C" int moe_expert_choice_route(const float* logits, int T, int E, int C,
                 need);
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     float* probT = static_cast<float*>(ws);
-    ec_prob_kernel<<<cdiv(T, 32), 256, 0, s>>>(logits, T, E, probT);
-    if (int rc = check_launch("ec_prob_kernel")) return rc;
-    cudaError_t err = cudaMemsetAsync(slot, 0xFF, (size_t)T * E * sizeof(int32_t), s);   // -1: not chosen
-    MOE_REQUIRE(err == cudaSuccess, MOE_ERR_CUDA, "moe_expert_choice_route: %s", cudaGetErrorString(err));
-    ec_select_kernel<<<E, 1024, 0, s>>>(probT, T, E, C, tokens, gates, slot);
-    return check_launch("ec_select_kernel");
+    const cudaError_t lp = launch_pdl(ec_prob_kernel, dim3(cdiv(T, 32)), dim3(256), 0, s, logits, T, E, probT, slot);
+    if (int rc = check_launch(lp, "ec_prob_kernel")) return rc;
+    const cudaError_t ls = launch_pdl(ec_select_kernel, dim3(E), dim3(1024), 0, s, (const float*)probT, T, E, C, tokens,
+                                      gates, slot);
+    return check_launch(ls, "ec_select_kernel");
 }
 
 extern "C" int moe_expert_choice_dispatch(const void* x, const int32_t* tokens, int T, int h, int E, int C, int dtype,
