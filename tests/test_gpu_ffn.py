@@ -127,6 +127,47 @@ def test_grouped_schedule_on_the_pair_kernel():
         assert rel < 1e-2, f"expert {e} ({sizes[e]} rows): rel err {rel:.3e}"
 
 
+@pytest.mark.parametrize("h,F", [(512, 384), (1024, 200)])
+def test_odd_last_tiles_on_the_pair_kernel(h, F):
+    """Every expert ends on a pair whose second tile is absent (a phantom half), its last tile holding 1, 31, 32, 33,
+    40, 100 or 128 valid rows, on the 2-SM kernel. Every act and eout element of every expert against torch in fp32
+    from the same bf16 operands; F = 200 ends the act columns inside the first half of the last 256-column tile."""
+    import torch
+    from top_routing_dispatch_moe_gb300 import moe
+    torch.manual_seed(2)
+    dev = "cuda"
+    sizes = [1, 256 + 31, 512 + 32, 256 + 33, 100, 128, 2560 + 40]
+    E = len(sizes)
+    assert sum(sizes) >= 512 * E and all(-(-n // 128) % 2 == 1 for n in sizes)
+    ids = np.concatenate([np.full(n, e, np.int32) for e, n in enumerate(sizes)])
+    np.random.default_rng(2).shuffle(ids)
+    x = torch.randn(ids.size, h, device=dev).to(torch.bfloat16)
+    d = moe.moe_dispatch(x, torch.from_numpy(ids[:, None]).to(dev), E, 0, 1)
+    wg = (torch.randn(E, F, h, device=dev) / h ** 0.5).to(torch.bfloat16)
+    wu = (torch.randn(E, F, h, device=dev) / h ** 0.5).to(torch.bfloat16)
+    wd = (torch.randn(E, h, F, device=dev) / F ** 0.5).to(torch.bfloat16)
+    packed = moe.moe_pack_expert_weights(wg, wu, wd)
+    rows = d["buf"].shape[0]
+    act = torch.empty(rows, F, dtype=torch.bfloat16, device=dev)
+    eout = torch.empty(rows, h, dtype=torch.bfloat16, device=dev)
+    moe.moe_expert_up_gate(d["buf"], d["tile_sched"], packed, E, F, act)
+    moe.moe_expert_down(act, d["tile_sched"], packed, E, h, eout)
+    torch.cuda.synchronize()
+    assert moe.moe_check_device_error() == moe.MOE_OK, moe.moe_last_error_string()
+    off = d["offsets"].cpu().tolist()
+    for e in range(E):
+        xb = d["buf"][off[e]:off[e + 1]]
+        a_ref = _ref_act(xb, wg[e], wu[e])
+        a_got = act[off[e]:off[e + 1]].float()
+        # act is bf16-rounded (relative 2^-9) from fp32 sums of the same products in another order
+        err = (a_got - a_ref).abs() / (a_ref.abs() + 1e-2 * a_ref.abs().mean())
+        assert err.max().item() < 2e-2, f"act, expert {e} ({sizes[e]} rows): {_blocks(err)}"
+        o_ref = a_got @ wd[e].float().T
+        o_got = eout[off[e]:off[e + 1]].float()
+        err = (o_got - o_ref).abs() / (o_ref.abs() + 1e-2 * o_ref.abs().mean())
+        assert err.max().item() < 2e-2, f"eout, expert {e} ({sizes[e]} rows): {_blocks(err)}"
+
+
 @pytest.mark.parametrize("sizes,T", [
     ([0, 1, 257, 1900], 300),      # 2-SM kernel (rows >= 512 E); 3 shared tiles: a phantom pair half
     ([5, 130, 0, 77], 1000),       # one-SM kernel; ragged last shared tile
