@@ -305,6 +305,82 @@ int moe_expert_down_combine(const void* act, const int32_t* tile_sched, const vo
                             void* out_shared, void* y, int32_t* arrivals, void* stream);
 
 /* ---------------------------------------------------------------------------------------------------
+ * The whole token-choice layer forward in one call ("Megatron-LM ... （六）", section "MoE 层的数据流": router ->
+ * dispatch -> experts as one GroupedGEMM -> combine, plus the shared expert; "v6 长序列和 MoE ...", the worked shape
+ * table of section "NVIDIA 原题").
+ *   moe_layer_forward enqueues moe_router_packed, moe_dispatch, moe_expert_up_gate[_shared],
+ *   moe_expert_down[_shared] and moe_combine on `stream`, the same launches (so the same output bits) as those calls
+ *   made one after the other with the intermediates in the workspace:
+ *     x [T,h] dtype (device)  ->  y [T,h] dtype (device)
+ *   moe_layer_forward_host runs it on n_batches batches that live in page-locked host memory (cudaHostAlloc or
+ *   cudaHostRegister), x_host[i] [T,h] -> y_host[i] [T,h]: one host->device copy of each x and one device->host
+ *   copy of each y (cudaMemcpyAsync), on two streams that the call creates and releases (the first copy waits for
+ *   the work already enqueued on `stream`), so that batch i's copies
+ *   overlap the layer working on its neighbours on `stream` (two device buffers for x and two for y inside the
+ *   workspace; a buffer is refilled only after the layer or the copy that last read it has finished). `stream`
+ *   then waits for the last copy: once `stream` has been synchronised, every y_host[i] is written. Neither call
+ *   waits for the host.
+ *   desc: the layer's sizes, dtype, gating (MOE_GATING_SOFTMAX, _SOFTMAX_RENORM or _SIGMOID_BIAS_RENORM), alpha,
+ *     capacity (0: dropless) and num_ranks as for moe_router / moe_dispatch, and its device-resident parameters:
+ *     w_r_packed (moe_pack_router_weight's output), bias ([E] fp32 or NULL, as for moe_router), packed_w
+ *     (moe_pack_expert_weights for the E routed experts), packed_shared (one shared expert packed with E = 1,
+ *     or NULL for none). The caller owns all of it.
+ *   ws: moe_layer_workspace_size(desc) bytes of device memory (moe_layer_host_workspace_size(desc) for the host
+ *     variant), 16-byte aligned. moe_layer_views_of(desc, ws, &v) gives the device addresses of the intermediates
+ *     inside it (the router's and the dispatch's outputs, act, eout, the shared expert's act and output), as the
+ *     last forward left them.
+ *   Errors: MOE_ERR_INVALID_ARG for a null desc or pointer, n_batches < 0, a host buffer that is not
+ *     page-locked, or what the chained calls reject; MOE_ERR_UNSUPPORTED for MOE_GATING_SOFTMAX_SELBIAS or a
+ *     dtype outside the enum; MOE_ERR_WORKSPACE if ws_bytes is short; MOE_ERR_CUDA. The arguments are checked
+ *     before anything is enqueued; a call that fails later returns the failing step's status with the steps
+ *     before it already enqueued.
+ * ------------------------------------------------------------------------------------------------- */
+typedef struct moe_layer_desc {
+    int T, h, E, k, F;
+    int dtype;                  /* enum moe_dtype */
+    int gating;                 /* enum moe_gating */
+    float alpha;                /* aux-loss coefficient */
+    int capacity;               /* expert capacity C (0: dropless) */
+    int num_ranks;              /* virtual EP ranks of the send layout (divides E) */
+    const void* w_r_packed;     /* moe_pack_router_weight(w_r) */
+    const float* bias;          /* [E] fp32 or NULL */
+    const void* packed_w;       /* moe_pack_expert_weights of the routed experts */
+    const void* packed_shared;  /* the shared expert (E = 1) or NULL */
+} moe_layer_desc;
+
+typedef struct moe_layer_views {
+    float* logits;              /* [T,E] */
+    int32_t* topk_ids;          /* [T,k] */
+    float* gates;               /* [T,k] */
+    int32_t* counts;            /* [E] */
+    float* f;                   /* [E] */
+    float* P;                   /* [E] */
+    float* aux;                 /* [1] */
+    void* buf;                  /* [rows,h] dtype */
+    int32_t* offsets;           /* [E+1] */
+    int32_t* kept_counts;       /* [E] */
+    int32_t* dest_row;          /* [T,k] */
+    uint8_t* drop_mask;         /* [T,k] */
+    int32_t* src_token;         /* [rows] */
+    int32_t* src_slot;          /* [rows] */
+    int32_t* rank_counts;       /* [num_ranks] */
+    int32_t* rank_offsets;      /* [num_ranks+1] */
+    int32_t* tile_sched;        /* moe_tile_sched_bytes() */
+    void* act;                  /* [rows,F] dtype */
+    void* eout;                 /* [rows,h] dtype */
+    void* act_shared;           /* [T,F] dtype, NULL without a shared expert */
+    void* out_shared;           /* [T,h] dtype, NULL without a shared expert */
+    long long rows;             /* moe_dispatch_rows(T, E, k, capacity) */
+} moe_layer_views;
+
+size_t moe_layer_workspace_size(const moe_layer_desc* desc);
+size_t moe_layer_host_workspace_size(const moe_layer_desc* desc);
+int moe_layer_views_of(const moe_layer_desc* desc, void* ws, moe_layer_views* views);
+int moe_layer_forward(const moe_layer_desc* desc, const void* x, void* y, void* ws, size_t ws_bytes, void* stream);
+int moe_layer_forward_host(const moe_layer_desc* desc, int n_batches, const void* const* x_host,
+                           void* const* y_host, void* ws, size_t ws_bytes, void* stream);
+
+/* ---------------------------------------------------------------------------------------------------
  * FP8 dispatch payload ("10.5 序列并行与专家并行", section 10.5.7: activations that cross nodes can travel in
  * a low-precision format such as FP8, halving the bytes with negligible effect on model quality).
  * moe_dispatch_fp8: moe_dispatch with the send buffer in e4m3 (finite-only variant: bias 7, 3 mantissa bits,

@@ -207,3 +207,55 @@ def test_host_checks_of_the_fused_combine(lib):
     none = list(args)
     none[10] = 0                                     # T = 0: nothing to do, nothing launched
     assert raw.moe_expert_down_combine(*none) == lib.MOE_OK
+
+
+def test_layer_structs_match_the_header(lib, tmp_path):
+    """The ctypes mirrors of moe_layer_desc / moe_layer_views have the sizes and field offsets a C compiler gives
+    the header's structs."""
+    import shutil
+    import subprocess
+    cc = shutil.which("gcc") or shutil.which("cc")
+    if cc is None:
+        pytest.skip("no C compiler")
+    desc_f = [f[0] for f in lib.MoELayerDesc._fields_]
+    view_f = [f[0] for f in lib.MoELayerViews._fields_]
+    body = ['printf("%zu %zu\\n", sizeof(moe_layer_desc), sizeof(moe_layer_views));']
+    body += [f'printf("%zu\\n", offsetof(moe_layer_desc, {f}));' for f in desc_f]
+    body += [f'printf("%zu\\n", offsetof(moe_layer_views, {f}));' for f in view_f]
+    src = tmp_path / "layout.c"
+    src.write_text("#include <stdio.h>\n#include <stddef.h>\n#include \"moe.h\"\nint main(void) {\n    "
+                   + "\n    ".join(body) + "\n    return 0;\n}\n")
+    exe = tmp_path / "layout"
+    subprocess.run([cc, "-I", os.path.join(ROOT, "include"), str(src), "-o", str(exe)], check=True)
+    out = [int(v) for v in subprocess.run([str(exe)], capture_output=True, text=True, check=True).stdout.split()]
+    assert out[:2] == [ctypes.sizeof(lib.MoELayerDesc), ctypes.sizeof(lib.MoELayerViews)]
+    got = out[2:]
+    want = [getattr(lib.MoELayerDesc, f).offset for f in desc_f] + [getattr(lib.MoELayerViews, f).offset for f in view_f]
+    assert got == want
+
+
+def test_layer_forward_host_checks(lib):
+    """moe_layer_forward / moe_layer_forward_host reject a bad descriptor, null buffers and a short workspace before
+    anything is enqueued (the fake parameter addresses below are never dereferenced)."""
+    raw = lib.raw_lib()
+    P = ctypes.c_void_p
+    ok = 0x1000
+    d = lib.MoELayerDesc(64, 64, 4, 2, 64, lib.MOE_BF16, 0, 0.01, 0, 1, ok, None, ok, None)
+    assert raw.moe_layer_workspace_size(None) == 0
+    need = raw.moe_layer_workspace_size(ctypes.byref(d))
+    need_host = raw.moe_layer_host_workspace_size(ctypes.byref(d))
+    assert need > 0 and need_host == need + 4 * ((64 * 64 * 2 + 255) // 256 * 256)
+    assert raw.moe_layer_forward(None, P(ok), P(ok), P(ok), need, None) == lib.MOE_ERR_INVALID_ARG
+    assert raw.moe_layer_forward(ctypes.byref(d), None, P(ok), P(ok), need, None) == lib.MOE_ERR_INVALID_ARG
+    assert raw.moe_layer_forward(ctypes.byref(d), P(ok), P(ok), P(ok), need - 1, None) == lib.MOE_ERR_WORKSPACE
+    assert raw.moe_layer_forward(ctypes.byref(d), P(ok), P(ok), P(ok + 8), need, None) == lib.MOE_ERR_INVALID_ARG
+    bad = lib.MoELayerDesc(64, 64, 4, 2, 64, lib.MOE_BF16, 3, 0.01, 0, 1, ok, None, ok, None)   # selection-bias mode
+    assert raw.moe_layer_forward(ctypes.byref(bad), P(ok), P(ok), P(ok), need, None) == lib.MOE_ERR_UNSUPPORTED
+    bad = lib.MoELayerDesc(64, 64, 4, 2, 64, lib.MOE_BF16, 0, 0.01, 0, 3, ok, None, ok, None)   # 3 ranks, E = 4
+    assert raw.moe_layer_forward(ctypes.byref(bad), P(ok), P(ok), P(ok), need, None) == lib.MOE_ERR_INVALID_ARG
+    bad = lib.MoELayerDesc(64, 64, 4, 2, 64, lib.MOE_BF16, 0, 0.01, 0, 1, None, None, ok, None)  # no router weight
+    assert raw.moe_layer_forward(ctypes.byref(bad), P(ok), P(ok), P(ok), need, None) == lib.MOE_ERR_INVALID_ARG
+    arr = (P * 1)(ok)
+    assert raw.moe_layer_forward_host(ctypes.byref(d), -1, arr, arr, P(ok), need_host, None) == lib.MOE_ERR_INVALID_ARG
+    assert raw.moe_layer_forward_host(ctypes.byref(d), 1, arr, arr, P(ok), need_host - 1, None) == lib.MOE_ERR_WORKSPACE
+    assert raw.moe_layer_forward_host(ctypes.byref(d), 1, None, arr, P(ok), need_host, None) == lib.MOE_ERR_INVALID_ARG

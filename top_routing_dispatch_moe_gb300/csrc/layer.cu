@@ -1,0 +1,274 @@
+// The token-choice layer forward as one C call: router -> dispatch -> grouped SwiGLU experts -> combine
+// ("Megatron-LM 分布式训练（六）", section "MoE 层的数据流"; "v6 长序列和 MoE", the worked shape table), and the
+// same over batches in page-locked host memory with the host <-> device copies overlapped with the layer.
+//
+// Host code only: every step is one of the library's own entry points, enqueued on the caller's stream over
+// intermediates laid out in one caller-provided workspace. Nothing here allocates device memory; the host variant
+// creates two copy streams and a few events per call and releases them before it returns (the runtime frees them
+// once the work they order has completed).
+#include <vector>
+#include "common.cuh"
+
+namespace moe {
+namespace {
+
+// Byte offsets of the intermediates inside the workspace, each region 256-byte aligned.
+struct LayerLayout {
+    size_t logits, ids, gates, counts, f, P, aux, router_ws, router_ws_bytes;
+    size_t buf, offsets, kept, dest_row, drop_mask, src_token, src_slot, rank_counts, rank_offsets, sched;
+    size_t disp_ws, disp_ws_bytes;
+    size_t act, eout, sh_sched, sh_act, sh_out;
+    size_t fwd_bytes;        // end of the forward's regions
+    size_t x_dev[2], y_dev[2];
+    size_t host_bytes;       // end of the host variant's regions
+    long long rows;
+};
+
+size_t el_size(int dtype) { return dtype == MOE_BF16 ? 2 : 4; }
+
+LayerLayout layout_of(const moe_layer_desc& d) {
+    LayerLayout L{};
+    size_t o = 0;
+    auto take = [&](size_t bytes) {
+        const size_t at = o;
+        o = align_up(o + bytes, 256);
+        return at;
+    };
+    const size_t T = (size_t)d.T, h = (size_t)d.h, E = (size_t)d.E, k = (size_t)d.k, F = (size_t)d.F;
+    const size_t el = el_size(d.dtype);
+    L.rows = (long long)moe_dispatch_rows(d.T, d.E, d.k, d.capacity);
+    const size_t rows = (size_t)L.rows;
+    L.logits = take(T * E * 4);
+    L.ids = take(T * k * 4);
+    L.gates = take(T * k * 4);
+    L.counts = take(E * 4);
+    L.f = take(E * 4);
+    L.P = take(E * 4);
+    L.aux = take(4);
+    L.router_ws_bytes = moe_router_workspace_size(d.T, d.h, d.E, d.k, d.dtype);
+    L.router_ws = take(L.router_ws_bytes);
+    L.buf = take(rows * h * el);
+    L.offsets = take((E + 1) * 4);
+    L.kept = take(E * 4);
+    L.dest_row = take(T * k * 4);
+    L.drop_mask = take(T * k);
+    L.src_token = take(rows * 4);
+    L.src_slot = take(rows * 4);
+    L.rank_counts = take((size_t)d.num_ranks * 4);
+    L.rank_offsets = take(((size_t)d.num_ranks + 1) * 4);
+    L.sched = take(moe_tile_sched_bytes(d.T, d.E, d.k, d.capacity));
+    L.disp_ws_bytes = moe_dispatch_workspace_size(d.T, d.E, d.k, d.capacity);
+    L.disp_ws = take(L.disp_ws_bytes);
+    L.act = take(rows * F * el);
+    L.eout = take(rows * h * el);
+    if (d.packed_shared) {
+        L.sh_sched = take(moe_tile_sched_bytes(d.T, 1, 1, 0));
+        L.sh_act = take(T * F * el);
+        L.sh_out = take(T * h * el);
+    }
+    L.fwd_bytes = o;
+    for (int b = 0; b < 2; ++b) L.x_dev[b] = take(T * h * el);
+    for (int b = 0; b < 2; ++b) L.y_dev[b] = take(T * h * el);
+    L.host_bytes = o;
+    return L;
+}
+
+int check_desc(const moe_layer_desc* d, const char* who) {
+    MOE_REQUIRE(d, MOE_ERR_INVALID_ARG, "%s: desc is NULL", who);
+    MOE_REQUIRE(d->dtype == MOE_BF16 || d->dtype == MOE_F32, MOE_ERR_UNSUPPORTED, "%s: dtype %d", who, d->dtype);
+    MOE_REQUIRE(d->gating == MOE_GATING_SOFTMAX || d->gating == MOE_GATING_SOFTMAX_RENORM ||
+                    d->gating == MOE_GATING_SIGMOID_BIAS_RENORM,
+                MOE_ERR_UNSUPPORTED, "%s: gating %d (the selection-bias mode takes its bias from moe_sinkhorn_bias)",
+                who, d->gating);
+    MOE_REQUIRE(d->T >= 0 && d->h > 0 && d->h % 8 == 0 && d->F > 0 && d->F % 8 == 0 && d->E >= 1 && d->E <= 1024 &&
+                    d->k >= 1 && d->k <= 16 && d->k <= d->E && d->capacity >= 0 && d->num_ranks >= 1 &&
+                    d->E % d->num_ranks == 0,
+                MOE_ERR_INVALID_ARG, "%s: T=%d h=%d E=%d k=%d F=%d capacity=%d num_ranks=%d", who, d->T, d->h, d->E,
+                d->k, d->F, d->capacity, d->num_ranks);
+    MOE_REQUIRE(d->w_r_packed && aligned16(d->w_r_packed) && d->packed_w && aligned16(d->packed_w) &&
+                    (!d->packed_shared || aligned16(d->packed_shared)) && (!d->bias || aligned16(d->bias)),
+                MOE_ERR_INVALID_ARG, "%s: w_r_packed and packed_w must be non-null, all parameters 16-byte aligned",
+                who);
+    return MOE_OK;
+}
+
+template <class T>
+T* at(void* ws, size_t off) { return reinterpret_cast<T*>(static_cast<char*>(ws) + off); }
+
+moe_layer_views views_at(const moe_layer_desc& d, const LayerLayout& L, void* ws) {
+    moe_layer_views v{};
+    v.logits = at<float>(ws, L.logits);
+    v.topk_ids = at<int32_t>(ws, L.ids);
+    v.gates = at<float>(ws, L.gates);
+    v.counts = at<int32_t>(ws, L.counts);
+    v.f = at<float>(ws, L.f);
+    v.P = at<float>(ws, L.P);
+    v.aux = at<float>(ws, L.aux);
+    v.buf = at<void>(ws, L.buf);
+    v.offsets = at<int32_t>(ws, L.offsets);
+    v.kept_counts = at<int32_t>(ws, L.kept);
+    v.dest_row = at<int32_t>(ws, L.dest_row);
+    v.drop_mask = at<uint8_t>(ws, L.drop_mask);
+    v.src_token = at<int32_t>(ws, L.src_token);
+    v.src_slot = at<int32_t>(ws, L.src_slot);
+    v.rank_counts = at<int32_t>(ws, L.rank_counts);
+    v.rank_offsets = at<int32_t>(ws, L.rank_offsets);
+    v.tile_sched = at<int32_t>(ws, L.sched);
+    v.act = at<void>(ws, L.act);
+    v.eout = at<void>(ws, L.eout);
+    v.act_shared = d.packed_shared ? at<void>(ws, L.sh_act) : nullptr;
+    v.out_shared = d.packed_shared ? at<void>(ws, L.sh_out) : nullptr;
+    v.rows = L.rows;
+    return v;
+}
+
+// The chain on one stream. bf16 with a shared expert runs its tiles inside the routed launches (as
+// moe_expert_up_gate_shared / moe_expert_down_shared); fp32 runs it as a dense group of its own.
+int forward_chain(const moe_layer_desc& d, const LayerLayout& L, const void* x, void* y, void* ws, void* s) {
+    const moe_layer_views v = views_at(d, L, ws);
+    const int rows = (int)L.rows;
+    int rc = moe_router_packed(x, d.w_r_packed, d.bias, d.T, d.h, d.E, d.k, d.dtype, d.gating, d.alpha, v.logits,
+                               v.topk_ids, v.gates, v.counts, v.f, v.P, v.aux, at<void>(ws, L.router_ws),
+                               L.router_ws_bytes, s);
+    if (rc) return rc;
+    rc = moe_dispatch(x, v.topk_ids, d.T, d.h, d.E, d.k, d.capacity, d.num_ranks, d.dtype, v.buf, v.offsets,
+                      v.kept_counts, v.dest_row, v.drop_mask, v.src_token, v.src_slot, v.rank_counts, v.rank_offsets,
+                      v.tile_sched, at<void>(ws, L.disp_ws), L.disp_ws_bytes, s);
+    if (rc) return rc;
+    if (d.packed_shared && d.dtype == MOE_BF16) {
+        rc = moe_expert_up_gate_shared(v.buf, v.tile_sched, d.packed_w, d.E, d.h, d.F, rows, x, d.T, d.packed_shared,
+                                       v.act_shared, d.dtype, v.act, s);
+        if (rc) return rc;
+        rc = moe_expert_down_shared(v.act, v.tile_sched, d.packed_w, d.E, d.h, d.F, rows, v.act_shared, d.T,
+                                    d.packed_shared, v.out_shared, d.dtype, v.eout, s);
+        if (rc) return rc;
+    } else {
+        rc = moe_expert_up_gate(v.buf, v.tile_sched, d.packed_w, d.E, d.h, d.F, rows, d.dtype, v.act, s);
+        if (rc) return rc;
+        rc = moe_expert_down(v.act, v.tile_sched, d.packed_w, d.E, d.h, d.F, rows, d.dtype, v.eout, s);
+        if (rc) return rc;
+        if (d.packed_shared) {
+            int32_t* sh_sched = at<int32_t>(ws, L.sh_sched);
+            rc = moe_dense_tile_sched(d.T, sh_sched, s);
+            if (rc) return rc;
+            rc = moe_expert_up_gate(x, sh_sched, d.packed_shared, 1, d.h, d.F, d.T, d.dtype, v.act_shared, s);
+            if (rc) return rc;
+            rc = moe_expert_down(v.act_shared, sh_sched, d.packed_shared, 1, d.h, d.F, d.T, d.dtype, v.out_shared, s);
+            if (rc) return rc;
+        }
+    }
+    return moe_combine(v.eout, v.dest_row, v.gates, v.out_shared, d.T, d.h, d.k, d.dtype, y, s);
+}
+
+bool page_locked(const void* p) {
+    cudaPointerAttributes a{};
+    if (cudaPointerGetAttributes(&a, p) != cudaSuccess) {
+        cudaGetLastError();                  // clear the sticky-free error of an unknown pointer
+        return false;
+    }
+    return a.type == cudaMemoryTypeHost;
+}
+
+// Releases the copy streams and events of one host-variant call (deferred by the runtime until their work ends).
+struct HostCallObjects {
+    cudaStream_t h2d = nullptr, d2h = nullptr;
+    std::vector<cudaEvent_t> events;
+    ~HostCallObjects() {
+        for (cudaEvent_t e : events) cudaEventDestroy(e);
+        if (h2d) cudaStreamDestroy(h2d);
+        if (d2h) cudaStreamDestroy(d2h);
+    }
+    cudaEvent_t event() {
+        cudaEvent_t e = nullptr;
+        if (cudaEventCreateWithFlags(&e, cudaEventDisableTiming) != cudaSuccess) return nullptr;
+        events.push_back(e);
+        return e;
+    }
+};
+
+}  // namespace
+}  // namespace moe
+
+using namespace moe;
+
+extern "C" size_t moe_layer_workspace_size(const moe_layer_desc* desc) {
+    return desc ? layout_of(*desc).fwd_bytes : 0;
+}
+
+extern "C" size_t moe_layer_host_workspace_size(const moe_layer_desc* desc) {
+    return desc ? layout_of(*desc).host_bytes : 0;
+}
+
+extern "C" int moe_layer_views_of(const moe_layer_desc* desc, void* ws, moe_layer_views* views) {
+    if (int rc = check_desc(desc, "moe_layer_views_of")) return rc;
+    MOE_REQUIRE(ws && aligned16(ws) && views, MOE_ERR_INVALID_ARG, "moe_layer_views_of: null or misaligned ws / views");
+    *views = views_at(*desc, layout_of(*desc), ws);
+    return MOE_OK;
+}
+
+extern "C" int moe_layer_forward(const moe_layer_desc* desc, const void* x, void* y, void* ws, size_t ws_bytes,
+                                 void* stream) {
+    if (int rc = check_desc(desc, "moe_layer_forward")) return rc;
+    const LayerLayout L = layout_of(*desc);
+    MOE_REQUIRE(x && y && ws && aligned16(x) && aligned16(y) && aligned16(ws), MOE_ERR_INVALID_ARG,
+                "moe_layer_forward: x, y and ws must be non-null and 16-byte aligned");
+    MOE_REQUIRE(ws_bytes >= L.fwd_bytes, MOE_ERR_WORKSPACE, "moe_layer_forward: workspace %zu < %zu bytes", ws_bytes,
+                L.fwd_bytes);
+    if (desc->T == 0) return MOE_OK;
+    return forward_chain(*desc, L, x, y, ws, stream);
+}
+
+extern "C" int moe_layer_forward_host(const moe_layer_desc* desc, int n_batches, const void* const* x_host,
+                                      void* const* y_host, void* ws, size_t ws_bytes, void* stream) {
+    if (int rc = check_desc(desc, "moe_layer_forward_host")) return rc;
+    const LayerLayout L = layout_of(*desc);
+    MOE_REQUIRE(n_batches >= 0 && (n_batches == 0 || (x_host && y_host)) && ws && aligned16(ws), MOE_ERR_INVALID_ARG,
+                "moe_layer_forward_host: n_batches=%d, x_host / y_host / ws null or ws misaligned", n_batches);
+    MOE_REQUIRE(ws_bytes >= L.host_bytes, MOE_ERR_WORKSPACE, "moe_layer_forward_host: workspace %zu < %zu bytes",
+                ws_bytes, L.host_bytes);
+    for (int i = 0; i < n_batches; ++i)
+        MOE_REQUIRE(x_host[i] && y_host[i] && page_locked(x_host[i]) && page_locked(y_host[i]), MOE_ERR_INVALID_ARG,
+                    "moe_layer_forward_host: batch %d: x_host and y_host must be page-locked host memory", i);
+    if (n_batches == 0 || desc->T == 0) return MOE_OK;
+    const size_t bytes = (size_t)desc->T * desc->h * el_size(desc->dtype);
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    HostCallObjects o;
+    cudaError_t e = cudaStreamCreateWithFlags(&o.h2d, cudaStreamNonBlocking);
+    if (e == cudaSuccess) e = cudaStreamCreateWithFlags(&o.d2h, cudaStreamNonBlocking);
+    if (e != cudaSuccess) return set_error(MOE_ERR_CUDA, "moe_layer_forward_host: stream: %s", cudaGetErrorString(e));
+    // the first copies start after the work already enqueued on `stream` (which may still use the buffers)
+    cudaEvent_t start = o.event();
+    MOE_REQUIRE(start, MOE_ERR_CUDA, "moe_layer_forward_host: event creation failed");
+    e = cudaEventRecord(start, s);
+    if (e == cudaSuccess) e = cudaStreamWaitEvent(o.h2d, start, 0);
+    if (e != cudaSuccess) return set_error(MOE_ERR_CUDA, "moe_layer_forward_host: start: %s", cudaGetErrorString(e));
+    cudaEvent_t x_free[2] = {nullptr, nullptr};    // the layer has finished reading x buffer b
+    cudaEvent_t y_free[2] = {nullptr, nullptr};    // the copy out of y buffer b has finished
+    for (int i = 0; i < n_batches; ++i) {
+        const int b = i & 1;
+        void* xd = at<void>(ws, L.x_dev[b]);
+        void* yd = at<void>(ws, L.y_dev[b]);
+        cudaEvent_t x_in = o.event(), done = o.event(), out = o.event();
+        MOE_REQUIRE(x_in && done && out, MOE_ERR_CUDA, "moe_layer_forward_host: event creation failed");
+        if (x_free[b]) e = cudaStreamWaitEvent(o.h2d, x_free[b], 0);
+        if (e == cudaSuccess) e = cudaMemcpyAsync(xd, x_host[i], bytes, cudaMemcpyHostToDevice, o.h2d);
+        if (e == cudaSuccess) e = cudaEventRecord(x_in, o.h2d);
+        if (e == cudaSuccess) e = cudaStreamWaitEvent(s, x_in, 0);
+        if (e == cudaSuccess && y_free[b]) e = cudaStreamWaitEvent(s, y_free[b], 0);
+        if (e != cudaSuccess)
+            return set_error(MOE_ERR_CUDA, "moe_layer_forward_host: batch %d copy in: %s", i, cudaGetErrorString(e));
+        if (int rc = forward_chain(*desc, L, xd, yd, ws, stream)) return rc;
+        e = cudaEventRecord(done, s);
+        if (e == cudaSuccess) e = cudaStreamWaitEvent(o.d2h, done, 0);
+        if (e == cudaSuccess) e = cudaMemcpyAsync(y_host[i], yd, bytes, cudaMemcpyDeviceToHost, o.d2h);
+        if (e == cudaSuccess) e = cudaEventRecord(out, o.d2h);
+        if (e != cudaSuccess)
+            return set_error(MOE_ERR_CUDA, "moe_layer_forward_host: batch %d copy out: %s", i, cudaGetErrorString(e));
+        x_free[b] = done;
+        y_free[b] = out;
+    }
+    for (int b = 0; b < 2; ++b)
+        if (y_free[b] && (e = cudaStreamWaitEvent(s, y_free[b], 0)) != cudaSuccess)
+            return set_error(MOE_ERR_CUDA, "moe_layer_forward_host: join: %s", cudaGetErrorString(e));
+    return MOE_OK;
+}

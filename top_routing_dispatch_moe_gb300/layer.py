@@ -334,6 +334,29 @@ class MoELayer:
             self.forward(x, stream=s)
         return g
 
+    def native_desc(self):
+        """The moe_layer_desc of this layer for the one-call C entry points moe_layer_forward and
+        moe_layer_forward_host (token-choice routing with the bf16 or fp32 send buffer and the separate combine,
+        the launches of `forward`): it points at this layer's packed parameters, which must outlive its use."""
+        if self.routing != "token" or self.payload != "bf16" or self.fuse_combine or self.gating == "softmax_selbias":
+            raise NotImplementedError("moe_layer_forward: token-choice routing with the bf16 / fp32 send buffer and the "
+                                      "separate combine")
+        return moe.moe_layer_desc(T=self.T, h=self.h, E=self.E, k=self.k, F=self.F, dtype=self.dtype,
+                                  gating=self.gating, alpha=self.alpha, capacity=self.C, num_ranks=self.R,
+                                  w_r_packed=self.w_r_packed, bias=self.bias, packed_w=self.packed,
+                                  packed_shared=self.shared_packed)
+
+    def forward_host_native(self, x_hosts, y_hosts, ws=None):
+        """forward_host_batches through the C ABI: one moe_layer_forward_host call (the copies and the overlap are
+        the library's). ws: a device byte tensor of moe_layer_host_workspace_size bytes, kept across calls (one is
+        made when None). Returns after the last output has reached host memory."""
+        desc = self.native_desc()
+        if ws is None:
+            ws = moe._bytes_tensor(moe.moe_layer_host_workspace_size(desc), self.device)
+        moe.moe_layer_forward_host(desc, x_hosts, y_hosts, ws)
+        torch.cuda.synchronize(self.device)
+        return y_hosts
+
     def forward_host_batches(self, x_hosts, y_hosts):
         """Runs the layer over a sequence of batches that live in pinned host memory: x_hosts[i] -> y_hosts[i].
 

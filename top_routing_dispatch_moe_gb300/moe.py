@@ -71,6 +71,11 @@ _SIGS = {
     "moe_combine": (_I, [_P, _P, _P, _P, _I, _I, _I, _I, _P, _P]),
     "moe_combine_arrivals_bytes": (_Z, [_I, _I]),
     "moe_expert_down_combine": (_I, [_P, _P, _P, _I, _I, _I, _I, _P, _P, _P, _I, _I, _P, _P, _I, _P, _P, _P, _P, _P]),
+    "moe_layer_workspace_size": (_Z, [_P]),
+    "moe_layer_host_workspace_size": (_Z, [_P]),
+    "moe_layer_views_of": (_I, [_P, _P, _P]),
+    "moe_layer_forward": (_I, [_P, _P, _P, _P, _Z, _P]),
+    "moe_layer_forward_host": (_I, [_P, _I, _P, _P, _P, _Z, _P]),
     "moe_last_error_string": (ctypes.c_char_p, []),
     "moe_check_device_error": (_I, [_P]),
     "moe_set_wait_limit": (None, [_LL]),
@@ -468,6 +473,66 @@ def moe_expert_down_combine(act, tile_sched, packed_w, E: int, h: int, src_token
                                         dtype_code(act.dtype), _ptr(eout), _ptr(out_shared), _ptr(y), _ptr(arrivals),
                                         _stream(stream)))
     return eout, out_shared, y
+
+
+# ------------------------------------------------------------------------------------------------ layer
+
+class MoELayerDesc(ctypes.Structure):
+    """struct moe_layer_desc: the layer's sizes, modes and device-resident parameters."""
+    _fields_ = [("T", _I), ("h", _I), ("E", _I), ("k", _I), ("F", _I), ("dtype", _I), ("gating", _I),
+                ("alpha", _F), ("capacity", _I), ("num_ranks", _I), ("w_r_packed", _P), ("bias", _P),
+                ("packed_w", _P), ("packed_shared", _P)]
+
+
+class MoELayerViews(ctypes.Structure):
+    """struct moe_layer_views: device addresses of the intermediates inside a layer workspace."""
+    _fields_ = [(n, _P) for n in ("logits", "topk_ids", "gates", "counts", "f", "P", "aux", "buf", "offsets",
+                                  "kept_counts", "dest_row", "drop_mask", "src_token", "src_slot", "rank_counts",
+                                  "rank_offsets", "tile_sched", "act", "eout", "act_shared", "out_shared")] + \
+              [("rows", _LL)]
+
+
+def moe_layer_desc(*, T, h, E, k, F, dtype, gating, alpha, capacity, num_ranks, w_r_packed, bias, packed_w,
+                   packed_shared=None) -> MoELayerDesc:
+    """The descriptor of a layer whose parameters are the given device tensors (kept alive by the caller)."""
+    g = GATING[gating] if isinstance(gating, str) else int(gating)
+    d = MoELayerDesc(T, h, E, k, F, dtype_code(dtype) if isinstance(dtype, torch.dtype) else int(dtype), g,
+                     float(alpha), capacity, num_ranks, _ptr(w_r_packed), _ptr(bias), _ptr(packed_w),
+                     _ptr(packed_shared))
+    return d
+
+
+def moe_layer_workspace_size(desc: MoELayerDesc) -> int:
+    return _lib.moe_layer_workspace_size(ctypes.byref(desc))
+
+
+def moe_layer_host_workspace_size(desc: MoELayerDesc) -> int:
+    return _lib.moe_layer_host_workspace_size(ctypes.byref(desc))
+
+
+def moe_layer_views_of(desc: MoELayerDesc, ws) -> MoELayerViews:
+    v = MoELayerViews()
+    _check(_lib.moe_layer_views_of(ctypes.byref(desc), _ptr(ws), ctypes.byref(v)))
+    return v
+
+
+def moe_layer_forward(desc: MoELayerDesc, x, y, ws, stream=None):
+    _check(_lib.moe_layer_forward(ctypes.byref(desc), _ptr(x), _ptr(y), _ptr(ws), ws.numel() * ws.element_size(),
+                                  _stream(stream)))
+    return y
+
+
+def moe_layer_forward_host(desc: MoELayerDesc, x_hosts, y_hosts, ws, stream=None):
+    """x_hosts[i] -> y_hosts[i]: page-locked host tensors of the layer's shape (any dtype of the same bytes).
+    Enqueues everything on the stream and returns; synchronise the stream before reading y_hosts."""
+    n = len(x_hosts)
+    if len(y_hosts) != n:
+        raise MoEError(MOE_ERR_INVALID_ARG, "x_hosts and y_hosts differ in length")
+    xs = (_P * max(n, 1))(*[t.data_ptr() for t in x_hosts])
+    ys = (_P * max(n, 1))(*[t.data_ptr() for t in y_hosts])
+    _check(_lib.moe_layer_forward_host(ctypes.byref(desc), n, xs, ys, _ptr(ws), ws.numel() * ws.element_size(),
+                                       _stream(stream)))
+    return y_hosts
 
 
 # ------------------------------------------------------------------------------------------------ errors
