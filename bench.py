@@ -503,9 +503,9 @@ def run_gpu(args, cfg, C):
 
     # ---- end-to-end through the public API: every step copies its batch of tokens in from pinned host
     # memory and its output back to pinned host memory, overlapped with the neighbouring steps' layer work on
-    # separate streams. Token-choice workloads make one C-ABI call for all K steps (moe_layer_forward_host: the
-    # copies, the chain and the overlap in the library); the other routing modes go through the Python layer's
-    # forward_host_batches. No L2 flush here (the weights already exceed L2), so the time of the whole K-step run
+    # separate streams: one C-ABI call for all K steps (moe_layer_forward_host: the copies, the chain and the
+    # overlap in the library); a layer with the combine fused into the down GEMM goes through the Python layer's
+    # forward_host_batches instead. No L2 flush here (the weights already exceed L2), so the time of the whole K-step run
     # divided by K is the per-step time
     x_np = np.ascontiguousarray(inp["x"]).view(np.int16) if cfg.dtype == "bf16" else np.ascontiguousarray(inp["x"])
     x_hosts = [torch.from_numpy(x_np).pin_memory() for _ in range(2)]

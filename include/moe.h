@@ -305,13 +305,21 @@ int moe_expert_down_combine(const void* act, const int32_t* tile_sched, const vo
                             void* out_shared, void* y, int32_t* arrivals, void* stream);
 
 /* ---------------------------------------------------------------------------------------------------
- * The whole token-choice layer forward in one call ("Megatron-LM ... （六）", section "MoE 层的数据流": router ->
+ * The whole layer forward in one call ("Megatron-LM ... （六）", section "MoE 层的数据流": router ->
  * dispatch -> experts as one GroupedGEMM -> combine, plus the shared expert; "v6 长序列和 MoE ...", the worked shape
  * table of section "NVIDIA 原题").
- *   moe_layer_forward enqueues moe_router_packed, moe_dispatch, moe_expert_up_gate[_shared],
- *   moe_expert_down[_shared] and moe_combine on `stream`, the same launches (so the same output bits) as those calls
- *   made one after the other with the intermediates in the workspace:
+ *   moe_layer_forward enqueues on `stream` the calls of one layer forward, the same launches (so the same output
+ *   bits) as those calls made one after the other with the intermediates in the workspace:
  *     x [T,h] dtype (device)  ->  y [T,h] dtype (device)
+ *   routing MOE_ROUTING_TOKEN: moe_router_packed (gating), moe_dispatch (or moe_dispatch_fp8 + moe_dequant_fp8 with
+ *     payload MOE_PAYLOAD_FP8), moe_expert_up_gate[_shared], moe_expert_down[_shared], moe_combine;
+ *   MOE_ROUTING_SINKHORN: moe_router_packed (softmax mode, for the logits), moe_sinkhorn_bias (sinkhorn_iters, 0 =
+ *     16), moe_router_from_logits (MOE_GATING_SOFTMAX_SELBIAS), then as token routing (`gating` unused);
+ *   MOE_ROUTING_EXPERT_CHOICE: moe_router_packed (gating, for the logits), moe_expert_choice_route /
+ *     _dispatch with C = capacity tokens per expert (1 <= C <= T, E <= 256), the expert FFN,
+ *     moe_expert_choice_combine.
+ *   The shared expert runs inside the routed GEMM launches with bf16 and the dtype payload, otherwise as a dense
+ *   group of T rows after them.
  *   moe_layer_forward_host runs it on n_batches batches that live in page-locked host memory (cudaHostAlloc or
  *   cudaHostRegister), x_host[i] [T,h] -> y_host[i] [T,h]: one host->device copy of each x and one device->host
  *   copy of each y (cudaMemcpyAsync), on two streams that the call creates and releases (the first copy waits for
@@ -321,7 +329,8 @@ int moe_expert_down_combine(const void* act, const int32_t* tile_sched, const vo
  *   then waits for the last copy: once `stream` has been synchronised, every y_host[i] is written. Neither call
  *   waits for the host.
  *   desc: the layer's sizes, dtype, gating (MOE_GATING_SOFTMAX, _SOFTMAX_RENORM or _SIGMOID_BIAS_RENORM), alpha,
- *     capacity (0: dropless) and num_ranks as for moe_router / moe_dispatch, and its device-resident parameters:
+ *     capacity (0: dropless) and num_ranks as for moe_router / moe_dispatch, routing, payload (FP8: bf16, token
+ *     routing, h % 128 == 0), sinkhorn_iters, and its device-resident parameters:
  *     w_r_packed (moe_pack_router_weight's output), bias ([E] fp32 or NULL, as for moe_router), packed_w
  *     (moe_pack_expert_weights for the E routed experts), packed_shared (one shared expert packed with E = 1,
  *     or NULL for none). The caller owns all of it.
@@ -330,11 +339,14 @@ int moe_expert_down_combine(const void* act, const int32_t* tile_sched, const vo
  *     inside it (the router's and the dispatch's outputs, act, eout, the shared expert's act and output), as the
  *     last forward left them.
  *   Errors: MOE_ERR_INVALID_ARG for a null desc or pointer, n_batches < 0, a host buffer that is not
- *     page-locked, or what the chained calls reject; MOE_ERR_UNSUPPORTED for MOE_GATING_SOFTMAX_SELBIAS or a
- *     dtype outside the enum; MOE_ERR_WORKSPACE if ws_bytes is short; MOE_ERR_CUDA. The arguments are checked
+ *     page-locked, or what the chained calls reject; MOE_ERR_UNSUPPORTED for MOE_GATING_SOFTMAX_SELBIAS, a dtype,
+ *     routing or payload outside the enums, or the FP8 payload with fp32 or without token routing; MOE_ERR_WORKSPACE if ws_bytes is short; MOE_ERR_CUDA. The arguments are checked
  *     before anything is enqueued; a call that fails later returns the failing step's status with the steps
  *     before it already enqueued.
  * ------------------------------------------------------------------------------------------------- */
+enum moe_routing { MOE_ROUTING_TOKEN = 0, MOE_ROUTING_EXPERT_CHOICE = 1, MOE_ROUTING_SINKHORN = 2 };
+enum moe_payload { MOE_PAYLOAD_DTYPE = 0, MOE_PAYLOAD_FP8 = 1 };
+
 typedef struct moe_layer_desc {
     int T, h, E, k, F;
     int dtype;                  /* enum moe_dtype */
@@ -346,6 +358,9 @@ typedef struct moe_layer_desc {
     const float* bias;          /* [E] fp32 or NULL */
     const void* packed_w;       /* moe_pack_expert_weights of the routed experts */
     const void* packed_shared;  /* the shared expert (E = 1) or NULL */
+    int routing;                /* enum moe_routing */
+    int payload;                /* enum moe_payload: the send buffer in dtype, or e4m3 with per-128-column scales */
+    int sinkhorn_iters;         /* MOE_ROUTING_SINKHORN: iterations (0: 16) */
 } moe_layer_desc;
 
 typedef struct moe_layer_views {
@@ -370,7 +385,13 @@ typedef struct moe_layer_views {
     void* eout;                 /* [rows,h] dtype */
     void* act_shared;           /* [T,F] dtype, NULL without a shared expert */
     void* out_shared;           /* [T,h] dtype, NULL without a shared expert */
-    long long rows;             /* moe_dispatch_rows(T, E, k, capacity) */
+    long long rows;             /* rows of buf: moe_dispatch_rows(T, E, k, capacity), E * capacity for expert choice */
+    int32_t* ec_tokens;         /* expert choice: [E,C] (else NULL) */
+    float* ec_gates;            /* expert choice: [E,C] */
+    int32_t* ec_slot;           /* expert choice: [T,E] */
+    float* sel_bias;            /* Sinkhorn: [E] log column scalings (else NULL) */
+    uint8_t* buf8;              /* FP8 payload: [rows,h] e4m3 codes (else NULL; buf then holds the dequantised rows) */
+    float* scales;              /* FP8 payload: [rows,h/128] */
 } moe_layer_views;
 
 size_t moe_layer_workspace_size(const moe_layer_desc* desc);

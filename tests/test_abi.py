@@ -255,6 +255,20 @@ def test_layer_forward_host_checks(lib):
     assert raw.moe_layer_forward(ctypes.byref(bad), P(ok), P(ok), P(ok), need, None) == lib.MOE_ERR_INVALID_ARG
     bad = lib.MoELayerDesc(64, 64, 4, 2, 64, lib.MOE_BF16, 0, 0.01, 0, 1, None, None, ok, None)  # no router weight
     assert raw.moe_layer_forward(ctypes.byref(bad), P(ok), P(ok), P(ok), need, None) == lib.MOE_ERR_INVALID_ARG
+    bad = lib.MoELayerDesc(64, 64, 4, 2, 64, lib.MOE_BF16, 0, 0.01, 0, 1, ok, None, ok, None, 5, 0, 0)  # routing 5
+    assert raw.moe_layer_forward(ctypes.byref(bad), P(ok), P(ok), P(ok), need, None) == lib.MOE_ERR_UNSUPPORTED
+    bad = lib.MoELayerDesc(64, 64, 4, 2, 64, lib.MOE_F32, 0, 0.01, 0, 1, ok, None, ok, None, 0, 1, 0)    # fp32 + FP8
+    assert raw.moe_layer_forward(ctypes.byref(bad), P(ok), P(ok), P(ok), need, None) == lib.MOE_ERR_UNSUPPORTED
+    bad = lib.MoELayerDesc(64, 64, 4, 2, 64, lib.MOE_BF16, 0, 0.01, 0, 1, ok, None, ok, None, 0, 1, 0)   # h % 128
+    assert raw.moe_layer_forward(ctypes.byref(bad), P(ok), P(ok), P(ok), need, None) == lib.MOE_ERR_INVALID_ARG
+    bad = lib.MoELayerDesc(64, 64, 4, 2, 64, lib.MOE_BF16, 0, 0.01, 0, 1, ok, None, ok, None, 1, 0, 0)   # EC, C = 0
+    assert raw.moe_layer_forward(ctypes.byref(bad), P(ok), P(ok), P(ok), need, None) == lib.MOE_ERR_INVALID_ARG
+    ec = lib.MoELayerDesc(64, 64, 4, 2, 64, lib.MOE_BF16, 0, 0.01, 16, 1, ok, None, ok, None, 1, 0, 0)   # EC, C = 16
+    sk = lib.MoELayerDesc(64, 64, 4, 2, 64, lib.MOE_BF16, 3, 0.01, 0, 1, ok, None, ok, None, 2, 0, 0)    # Sinkhorn
+    for dd in (ec, sk):
+        n_dd = raw.moe_layer_workspace_size(ctypes.byref(dd))
+        assert n_dd > 0
+        assert raw.moe_layer_forward(ctypes.byref(dd), P(ok), P(ok), P(ok), n_dd - 1, None) == lib.MOE_ERR_WORKSPACE
     arr = (P * 1)(ok)
     assert raw.moe_layer_forward_host(ctypes.byref(d), -1, arr, arr, P(ok), need_host, None) == lib.MOE_ERR_INVALID_ARG
     assert raw.moe_layer_forward_host(ctypes.byref(d), 1, arr, arr, P(ok), need_host - 1, None) == lib.MOE_ERR_WORKSPACE

@@ -1,4 +1,4 @@
-"""moe_layer_forward / moe_layer_forward_host: the whole token-choice layer forward as one C-ABI call.
+"""moe_layer_forward / moe_layer_forward_host: the whole layer forward as one C-ABI call.
 
 The chain is the launches of MoELayer.forward (router, dispatch, grouped up/gate and down GEMMs, combine), so y must
 be bitwise the Python layer's, whose output the parity tests compare with the oracle; the router ids and aux read
@@ -6,7 +6,8 @@ back through moe_layer_views_of must be the layer's too. The host variant runs s
 memory with the copies on its own streams: each batch's y must be bitwise a device forward of that batch. Cases:
 capacity drops on the 2-SM GEMMs (page-3 routing), the one-SM GEMMs, sigmoid gating with a selection bias and the
 shared expert inside the routed launches (DeepSeek-V3-shaped), fp32 on the CUDA cores, with and without a shared
-expert (which fp32 runs as a dense group of its own)."""
+expert (which fp32 runs as a dense group of its own), expert-choice routing, Sinkhorn-balanced routing and the FP8
+send buffer."""
 import numpy as np
 import pytest
 
@@ -19,7 +20,10 @@ CASES = [("page3_cf1.25", dict(T=2048, h=512, F=384)),     # capacity drops, 2-S
          ("page3_cf1.25", dict(T=1024, h=512, F=256)),     # one-SM GEMMs
          ("deepseek_v3", dict(T=512, h=256, F=128)),       # sigmoid + selection bias, shared expert, E = 256, k = 8
          ("tiny_fp32", {}),
-         ("tiny_fp32", dict(n_shared=1))]
+         ("tiny_fp32", dict(n_shared=1)),
+         ("page3_expert_choice", dict(T=1024, h=512, F=256)),
+         ("mixtral_sinkhorn", dict(T=1024, h=512, F=256, bias="none")),
+         ("page3_fp8", dict(T=1024, h=512, F=256))]
 
 
 def _layer(name, over):
@@ -36,7 +40,8 @@ def _layer(name, over):
     layer = MoELayer(T=cfg.T, h=cfg.h, E=cfg.E, k=cfg.k, F=cfg.F, gating=cfg.gating, cf=cfg.cf, R=cfg.R,
                      alpha=cfg.alpha, w_r=up(inp["w_r"]),
                      bias=torch.from_numpy(inp["bias"]).to(dev) if inp["bias"] is not None else None,
-                     w_gate=up(wg), w_up=up(wu), w_down=up(wd), shared=sh, device=dev)
+                     w_gate=up(wg), w_up=up(wu), w_down=up(wd), shared=sh, device=dev, routing=cfg.routing,
+                     payload=cfg.payload)
     return cfg, layer, up(inp["x"])
 
 
@@ -72,11 +77,21 @@ def test_layer_forward_is_the_python_layer_bitwise(name, over):
     ids = _view(ws, v.topk_ids, cfg.T * cfg.k, torch.int32).view(cfg.T, cfg.k)
     assert torch.equal(ids, layer.r_out["topk_ids"])
     assert torch.equal(_view(ws, v.aux, 1, torch.float32), layer.r_out["aux"])
-    dest = _view(ws, v.dest_row, cfg.T * cfg.k, torch.int32).view(cfg.T, cfg.k)
-    assert torch.equal(dest, layer.d_out["dest_row"])
+    if cfg.routing == "expert_choice":
+        assert v.dest_row is None
+        slot = _view(ws, v.ec_slot, cfg.T * cfg.E, torch.int32).view(cfg.T, cfg.E)
+        assert torch.equal(slot, layer.ec["slot"])
+    else:
+        dest = _view(ws, v.dest_row, cfg.T * cfg.k, torch.int32).view(cfg.T, cfg.k)
+        assert torch.equal(dest, layer.d_out["dest_row"])
+    if cfg.routing == "sinkhorn":
+        assert torch.equal(_view(ws, v.sel_bias, cfg.E, torch.float32), layer.sk_bias)
+    if cfg.payload == "fp8":
+        assert torch.equal(_view(ws, v.buf8, layer.rows * cfg.h, torch.uint8).view(layer.rows, cfg.h),
+                           layer.d_out["buf8"])
 
 
-@pytest.mark.parametrize("name,over", [CASES[0], CASES[2], CASES[4]])
+@pytest.mark.parametrize("name,over", [CASES[0], CASES[2], CASES[4], CASES[5], CASES[6], CASES[7]])
 def test_layer_forward_host_batches(name, over):
     import torch
     from top_routing_dispatch_moe_gb300 import moe

@@ -1,6 +1,8 @@
-// The token-choice layer forward as one C call: router -> dispatch -> grouped SwiGLU experts -> combine
-// ("Megatron-LM 分布式训练（六）", section "MoE 层的数据流"; "v6 长序列和 MoE", the worked shape table), and the
-// same over batches in page-locked host memory with the host <-> device copies overlapped with the layer.
+// The layer forward as one C call: router -> dispatch -> grouped SwiGLU experts -> combine ("Megatron-LM
+// 分布式训练（六）", section "MoE 层的数据流"; "v6 长序列和 MoE", the worked shape table), with token-choice,
+// Sinkhorn-balanced or expert-choice routing ("10.5 序列并行与专家并行", section 10.5.6) and the bf16 / fp32 or the
+// FP8 send buffer (section 10.5.7), and the same over batches in page-locked host memory with the host <-> device
+// copies overlapped with the layer.
 //
 // Host code only: every step is one of the library's own entry points, enqueued on the caller's stream over
 // intermediates laid out in one caller-provided workspace. Nothing here allocates device memory; the host variant
@@ -17,6 +19,9 @@ struct LayerLayout {
     size_t logits, ids, gates, counts, f, P, aux, router_ws, router_ws_bytes;
     size_t buf, offsets, kept, dest_row, drop_mask, src_token, src_slot, rank_counts, rank_offsets, sched;
     size_t disp_ws, disp_ws_bytes;
+    size_t ec_tokens, ec_gates, ec_slot, ec_ws, ec_ws_bytes;        // expert choice
+    size_t sel_bias, sk_ws, sk_ws_bytes, rl_ws, rl_ws_bytes;          // Sinkhorn
+    size_t buf8, scales;                                              // FP8 payload
     size_t act, eout, sh_sched, sh_act, sh_out;
     size_t fwd_bytes;        // end of the forward's regions
     size_t x_dev[2], y_dev[2];
@@ -36,7 +41,8 @@ LayerLayout layout_of(const moe_layer_desc& d) {
     };
     const size_t T = (size_t)d.T, h = (size_t)d.h, E = (size_t)d.E, k = (size_t)d.k, F = (size_t)d.F;
     const size_t el = el_size(d.dtype);
-    L.rows = (long long)moe_dispatch_rows(d.T, d.E, d.k, d.capacity);
+    const bool ec = d.routing == MOE_ROUTING_EXPERT_CHOICE;
+    L.rows = ec ? (long long)d.E * d.capacity : (long long)moe_dispatch_rows(d.T, d.E, d.k, d.capacity);
     const size_t rows = (size_t)L.rows;
     L.logits = take(T * E * 4);
     L.ids = take(T * k * 4);
@@ -48,17 +54,37 @@ LayerLayout layout_of(const moe_layer_desc& d) {
     L.router_ws_bytes = moe_router_workspace_size(d.T, d.h, d.E, d.k, d.dtype);
     L.router_ws = take(L.router_ws_bytes);
     L.buf = take(rows * h * el);
-    L.offsets = take((E + 1) * 4);
-    L.kept = take(E * 4);
-    L.dest_row = take(T * k * 4);
-    L.drop_mask = take(T * k);
-    L.src_token = take(rows * 4);
-    L.src_slot = take(rows * 4);
-    L.rank_counts = take((size_t)d.num_ranks * 4);
-    L.rank_offsets = take(((size_t)d.num_ranks + 1) * 4);
-    L.sched = take(moe_tile_sched_bytes(d.T, d.E, d.k, d.capacity));
-    L.disp_ws_bytes = moe_dispatch_workspace_size(d.T, d.E, d.k, d.capacity);
-    L.disp_ws = take(L.disp_ws_bytes);
+    if (ec) {
+        L.ec_tokens = take(E * (size_t)d.capacity * 4);
+        L.ec_gates = take(E * (size_t)d.capacity * 4);
+        L.ec_slot = take(T * E * 4);
+        L.ec_ws_bytes = moe_expert_choice_workspace_size(d.T, d.E);
+        L.ec_ws = take(L.ec_ws_bytes);
+        L.sched = take(moe_tile_sched_bytes(d.T, d.E, 1, d.capacity));
+    } else {
+        L.offsets = take((E + 1) * 4);
+        L.kept = take(E * 4);
+        L.dest_row = take(T * k * 4);
+        L.drop_mask = take(T * k);
+        L.src_token = take(rows * 4);
+        L.src_slot = take(rows * 4);
+        L.rank_counts = take((size_t)d.num_ranks * 4);
+        L.rank_offsets = take(((size_t)d.num_ranks + 1) * 4);
+        L.sched = take(moe_tile_sched_bytes(d.T, d.E, d.k, d.capacity));
+        L.disp_ws_bytes = moe_dispatch_workspace_size(d.T, d.E, d.k, d.capacity);
+        L.disp_ws = take(L.disp_ws_bytes);
+    }
+    if (d.routing == MOE_ROUTING_SINKHORN) {
+        L.sel_bias = take(E * 4);
+        L.sk_ws_bytes = moe_sinkhorn_workspace_size(d.T, d.E);
+        L.sk_ws = take(L.sk_ws_bytes);
+        L.rl_ws_bytes = moe_router_from_logits_workspace_size(d.T, d.E);
+        L.rl_ws = take(L.rl_ws_bytes);
+    }
+    if (d.payload == MOE_PAYLOAD_FP8) {       // the e4m3 send buffer; buf receives its dequantised rows
+        L.buf8 = take(rows * h);
+        L.scales = take(rows * (h / 128) * 4);
+    }
     L.act = take(rows * F * el);
     L.eout = take(rows * h * el);
     if (d.packed_shared) {
@@ -76,10 +102,22 @@ LayerLayout layout_of(const moe_layer_desc& d) {
 int check_desc(const moe_layer_desc* d, const char* who) {
     MOE_REQUIRE(d, MOE_ERR_INVALID_ARG, "%s: desc is NULL", who);
     MOE_REQUIRE(d->dtype == MOE_BF16 || d->dtype == MOE_F32, MOE_ERR_UNSUPPORTED, "%s: dtype %d", who, d->dtype);
-    MOE_REQUIRE(d->gating == MOE_GATING_SOFTMAX || d->gating == MOE_GATING_SOFTMAX_RENORM ||
-                    d->gating == MOE_GATING_SIGMOID_BIAS_RENORM,
-                MOE_ERR_UNSUPPORTED, "%s: gating %d (the selection-bias mode takes its bias from moe_sinkhorn_bias)",
-                who, d->gating);
+    MOE_REQUIRE(d->routing == MOE_ROUTING_TOKEN || d->routing == MOE_ROUTING_EXPERT_CHOICE ||
+                    d->routing == MOE_ROUTING_SINKHORN,
+                MOE_ERR_UNSUPPORTED, "%s: routing %d", who, d->routing);
+    MOE_REQUIRE(d->payload == MOE_PAYLOAD_DTYPE || d->payload == MOE_PAYLOAD_FP8, MOE_ERR_UNSUPPORTED, "%s: payload %d",
+                who, d->payload);
+    MOE_REQUIRE(d->routing == MOE_ROUTING_SINKHORN || d->gating == MOE_GATING_SOFTMAX ||
+                    d->gating == MOE_GATING_SOFTMAX_RENORM || d->gating == MOE_GATING_SIGMOID_BIAS_RENORM,
+                MOE_ERR_UNSUPPORTED, "%s: gating %d (the selection-bias mode is Sinkhorn routing's)", who, d->gating);
+    MOE_REQUIRE(d->payload != MOE_PAYLOAD_FP8 || (d->dtype == MOE_BF16 && d->routing == MOE_ROUTING_TOKEN),
+                MOE_ERR_UNSUPPORTED, "%s: the FP8 payload needs bf16 and token-choice routing", who);
+    MOE_REQUIRE(d->payload != MOE_PAYLOAD_FP8 || d->h % 128 == 0, MOE_ERR_INVALID_ARG,
+                "%s: the FP8 payload needs h %% 128 == 0 (h=%d)", who, d->h);
+    MOE_REQUIRE(d->routing != MOE_ROUTING_EXPERT_CHOICE || (d->capacity >= 1 && d->capacity <= d->T && d->E <= 256),
+                MOE_ERR_INVALID_ARG, "%s: expert choice needs 1 <= capacity <= T and E <= 256 (C=%d T=%d E=%d)", who,
+                d->capacity, d->T, d->E);
+    MOE_REQUIRE(d->sinkhorn_iters >= 0, MOE_ERR_INVALID_ARG, "%s: sinkhorn_iters %d", who, d->sinkhorn_iters);
     MOE_REQUIRE(d->T >= 0 && d->h > 0 && d->h % 8 == 0 && d->F > 0 && d->F % 8 == 0 && d->E >= 1 && d->E <= 1024 &&
                     d->k >= 1 && d->k <= 16 && d->k <= d->E && d->capacity >= 0 && d->num_ranks >= 1 &&
                     d->E % d->num_ranks == 0,
@@ -105,15 +143,26 @@ moe_layer_views views_at(const moe_layer_desc& d, const LayerLayout& L, void* ws
     v.P = at<float>(ws, L.P);
     v.aux = at<float>(ws, L.aux);
     v.buf = at<void>(ws, L.buf);
-    v.offsets = at<int32_t>(ws, L.offsets);
-    v.kept_counts = at<int32_t>(ws, L.kept);
-    v.dest_row = at<int32_t>(ws, L.dest_row);
-    v.drop_mask = at<uint8_t>(ws, L.drop_mask);
-    v.src_token = at<int32_t>(ws, L.src_token);
-    v.src_slot = at<int32_t>(ws, L.src_slot);
-    v.rank_counts = at<int32_t>(ws, L.rank_counts);
-    v.rank_offsets = at<int32_t>(ws, L.rank_offsets);
     v.tile_sched = at<int32_t>(ws, L.sched);
+    if (d.routing == MOE_ROUTING_EXPERT_CHOICE) {
+        v.ec_tokens = at<int32_t>(ws, L.ec_tokens);
+        v.ec_gates = at<float>(ws, L.ec_gates);
+        v.ec_slot = at<int32_t>(ws, L.ec_slot);
+    } else {
+        v.offsets = at<int32_t>(ws, L.offsets);
+        v.kept_counts = at<int32_t>(ws, L.kept);
+        v.dest_row = at<int32_t>(ws, L.dest_row);
+        v.drop_mask = at<uint8_t>(ws, L.drop_mask);
+        v.src_token = at<int32_t>(ws, L.src_token);
+        v.src_slot = at<int32_t>(ws, L.src_slot);
+        v.rank_counts = at<int32_t>(ws, L.rank_counts);
+        v.rank_offsets = at<int32_t>(ws, L.rank_offsets);
+    }
+    if (d.routing == MOE_ROUTING_SINKHORN) v.sel_bias = at<float>(ws, L.sel_bias);
+    if (d.payload == MOE_PAYLOAD_FP8) {
+        v.buf8 = at<uint8_t>(ws, L.buf8);
+        v.scales = at<float>(ws, L.scales);
+    }
     v.act = at<void>(ws, L.act);
     v.eout = at<void>(ws, L.eout);
     v.act_shared = d.packed_shared ? at<void>(ws, L.sh_act) : nullptr;
@@ -122,20 +171,43 @@ moe_layer_views views_at(const moe_layer_desc& d, const LayerLayout& L, void* ws
     return v;
 }
 
-// The chain on one stream. bf16 with a shared expert runs its tiles inside the routed launches (as
-// moe_expert_up_gate_shared / moe_expert_down_shared); fp32 runs it as a dense group of its own.
+// The chain on one stream. With bf16 and the dtype payload a shared expert runs its tiles inside the routed
+// launches (as moe_expert_up_gate_shared / moe_expert_down_shared); otherwise it runs as a dense group of its own.
 int forward_chain(const moe_layer_desc& d, const LayerLayout& L, const void* x, void* y, void* ws, void* s) {
     const moe_layer_views v = views_at(d, L, ws);
     const int rows = (int)L.rows;
-    int rc = moe_router_packed(x, d.w_r_packed, d.bias, d.T, d.h, d.E, d.k, d.dtype, d.gating, d.alpha, v.logits,
-                               v.topk_ids, v.gates, v.counts, v.f, v.P, v.aux, at<void>(ws, L.router_ws),
-                               L.router_ws_bytes, s);
+    const bool ec = d.routing == MOE_ROUTING_EXPERT_CHOICE, sk = d.routing == MOE_ROUTING_SINKHORN;
+    int rc = moe_router_packed(x, d.w_r_packed, d.bias, d.T, d.h, d.E, d.k, d.dtype,
+                               sk ? MOE_GATING_SOFTMAX : d.gating, d.alpha, v.logits, v.topk_ids, v.gates, v.counts,
+                               v.f, v.P, v.aux, at<void>(ws, L.router_ws), L.router_ws_bytes, s);
     if (rc) return rc;
-    rc = moe_dispatch(x, v.topk_ids, d.T, d.h, d.E, d.k, d.capacity, d.num_ranks, d.dtype, v.buf, v.offsets,
-                      v.kept_counts, v.dest_row, v.drop_mask, v.src_token, v.src_slot, v.rank_counts, v.rank_offsets,
-                      v.tile_sched, at<void>(ws, L.disp_ws), L.disp_ws_bytes, s);
+    if (sk) {                                // balanced selection: the Sinkhorn log column scalings as a bias
+        rc = moe_sinkhorn_bias(v.logits, d.T, d.E, d.sinkhorn_iters > 0 ? d.sinkhorn_iters : 16, v.sel_bias,
+                               at<void>(ws, L.sk_ws), L.sk_ws_bytes, s);
+        if (rc) return rc;
+        rc = moe_router_from_logits(v.logits, v.sel_bias, d.T, d.E, d.k, MOE_GATING_SOFTMAX_SELBIAS, d.alpha,
+                                    v.topk_ids, v.gates, v.counts, v.f, v.P, v.aux, at<void>(ws, L.rl_ws),
+                                    L.rl_ws_bytes, s);
+        if (rc) return rc;
+    }
+    if (ec) {
+        rc = moe_expert_choice_route(v.logits, d.T, d.E, d.capacity, v.ec_tokens, v.ec_gates, v.ec_slot,
+                                     at<void>(ws, L.ec_ws), L.ec_ws_bytes, s);
+        if (rc) return rc;
+        rc = moe_expert_choice_dispatch(x, v.ec_tokens, d.T, d.h, d.E, d.capacity, d.dtype, v.buf, v.tile_sched, s);
+    } else if (d.payload == MOE_PAYLOAD_FP8) {
+        rc = moe_dispatch_fp8(x, v.topk_ids, d.T, d.h, d.E, d.k, d.capacity, d.num_ranks, v.buf8, v.scales, v.offsets,
+                              v.kept_counts, v.dest_row, v.drop_mask, v.src_token, v.src_slot, v.rank_counts,
+                              v.rank_offsets, v.tile_sched, at<void>(ws, L.disp_ws), L.disp_ws_bytes, s);
+        if (rc) return rc;
+        rc = moe_dequant_fp8(v.buf8, v.scales, rows, d.h, v.buf, s);   // the receive side, then the bf16 GEMMs
+    } else {
+        rc = moe_dispatch(x, v.topk_ids, d.T, d.h, d.E, d.k, d.capacity, d.num_ranks, d.dtype, v.buf, v.offsets,
+                          v.kept_counts, v.dest_row, v.drop_mask, v.src_token, v.src_slot, v.rank_counts,
+                          v.rank_offsets, v.tile_sched, at<void>(ws, L.disp_ws), L.disp_ws_bytes, s);
+    }
     if (rc) return rc;
-    if (d.packed_shared && d.dtype == MOE_BF16) {
+    if (d.packed_shared && d.dtype == MOE_BF16 && d.payload == MOE_PAYLOAD_DTYPE) {
         rc = moe_expert_up_gate_shared(v.buf, v.tile_sched, d.packed_w, d.E, d.h, d.F, rows, x, d.T, d.packed_shared,
                                        v.act_shared, d.dtype, v.act, s);
         if (rc) return rc;
@@ -157,6 +229,9 @@ int forward_chain(const moe_layer_desc& d, const LayerLayout& L, const void* x, 
             if (rc) return rc;
         }
     }
+    if (ec)
+        return moe_expert_choice_combine(v.eout, v.ec_slot, v.ec_gates, v.out_shared, d.T, d.h, d.E, d.capacity,
+                                         d.dtype, y, s);
     return moe_combine(v.eout, v.dest_row, v.gates, v.out_shared, d.T, d.h, d.k, d.dtype, y, s);
 }
 

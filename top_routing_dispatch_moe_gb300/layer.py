@@ -336,15 +336,15 @@ class MoELayer:
 
     def native_desc(self):
         """The moe_layer_desc of this layer for the one-call C entry points moe_layer_forward and
-        moe_layer_forward_host (token-choice routing with the bf16 or fp32 send buffer and the separate combine,
-        the launches of `forward`): it points at this layer's packed parameters, which must outlive its use."""
-        if self.routing != "token" or self.payload != "bf16" or self.fuse_combine or self.gating == "softmax_selbias":
-            raise NotImplementedError("moe_layer_forward: token-choice routing with the bf16 / fp32 send buffer and the "
-                                      "separate combine")
+        moe_layer_forward_host (every routing mode and send buffer of `forward`, with the separate combine: the
+        same launches): it points at this layer's packed parameters, which must outlive its use."""
+        if self.fuse_combine:
+            raise NotImplementedError("moe_layer_forward runs the separate combine (MoELayer(fuse_combine=False))")
         return moe.moe_layer_desc(T=self.T, h=self.h, E=self.E, k=self.k, F=self.F, dtype=self.dtype,
-                                  gating=self.gating, alpha=self.alpha, capacity=self.C, num_ranks=self.R,
-                                  w_r_packed=self.w_r_packed, bias=self.bias, packed_w=self.packed,
-                                  packed_shared=self.shared_packed)
+                                  gating="softmax" if self.routing == "sinkhorn" else self.gating, alpha=self.alpha,
+                                  capacity=self.C, num_ranks=self.R, w_r_packed=self.w_r_packed, bias=self.bias,
+                                  packed_w=self.packed, packed_shared=self.shared_packed, routing=self.routing,
+                                  payload="fp8" if self.payload == "fp8" else "dtype")
 
     def forward_host_native(self, x_hosts, y_hosts, ws=None):
         """forward_host_batches through the C ABI: one moe_layer_forward_host call (the copies and the overlap are

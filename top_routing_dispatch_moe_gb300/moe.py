@@ -481,7 +481,7 @@ class MoELayerDesc(ctypes.Structure):
     """struct moe_layer_desc: the layer's sizes, modes and device-resident parameters."""
     _fields_ = [("T", _I), ("h", _I), ("E", _I), ("k", _I), ("F", _I), ("dtype", _I), ("gating", _I),
                 ("alpha", _F), ("capacity", _I), ("num_ranks", _I), ("w_r_packed", _P), ("bias", _P),
-                ("packed_w", _P), ("packed_shared", _P)]
+                ("packed_w", _P), ("packed_shared", _P), ("routing", _I), ("payload", _I), ("sinkhorn_iters", _I)]
 
 
 class MoELayerViews(ctypes.Structure):
@@ -489,16 +489,21 @@ class MoELayerViews(ctypes.Structure):
     _fields_ = [(n, _P) for n in ("logits", "topk_ids", "gates", "counts", "f", "P", "aux", "buf", "offsets",
                                   "kept_counts", "dest_row", "drop_mask", "src_token", "src_slot", "rank_counts",
                                   "rank_offsets", "tile_sched", "act", "eout", "act_shared", "out_shared")] + \
-              [("rows", _LL)]
+              [("rows", _LL)] + [(n, _P) for n in ("ec_tokens", "ec_gates", "ec_slot", "sel_bias", "buf8", "scales")]
+
+
+ROUTING = {"token": 0, "expert_choice": 1, "sinkhorn": 2}
+PAYLOAD = {"dtype": 0, "bf16": 0, "f32": 0, "fp8": 1}
 
 
 def moe_layer_desc(*, T, h, E, k, F, dtype, gating, alpha, capacity, num_ranks, w_r_packed, bias, packed_w,
-                   packed_shared=None) -> MoELayerDesc:
+                   packed_shared=None, routing="token", payload="dtype", sinkhorn_iters=0) -> MoELayerDesc:
     """The descriptor of a layer whose parameters are the given device tensors (kept alive by the caller)."""
     g = GATING[gating] if isinstance(gating, str) else int(gating)
     d = MoELayerDesc(T, h, E, k, F, dtype_code(dtype) if isinstance(dtype, torch.dtype) else int(dtype), g,
                      float(alpha), capacity, num_ranks, _ptr(w_r_packed), _ptr(bias), _ptr(packed_w),
-                     _ptr(packed_shared))
+                     _ptr(packed_shared), ROUTING[routing] if isinstance(routing, str) else int(routing),
+                     PAYLOAD[payload] if isinstance(payload, str) else int(payload), int(sinkhorn_iters))
     return d
 
 
