@@ -668,6 +668,9 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
     ap.add_argument("--workload", default="page3_cf1.25", choices=list(moe_inputs.CONFIGS))
+    ap.add_argument("--config", type=int, choices=range(1, len(moe_inputs.CONFIG_ORDER) + 1), default=None,
+                    help="the workload by number, 1.." + str(len(moe_inputs.CONFIG_ORDER)) + " = "
+                         + ", ".join(moe_inputs.CONFIG_ORDER) + " (overrides --workload)")
     ap.add_argument("--backward", action=argparse.BooleanOptionalAction, default=True,
                     help="also time the layer's backward (bf16 token-choice workloads), reported under 'backward'")
     ap.add_argument("--sample-tokens", type=int, default=32, help="oracle tokens per reference-arm step")
@@ -682,6 +685,8 @@ def main():
                     help="run the combine in the down GEMM's epilogue (bf16 token-choice / Sinkhorn layers); off by "
                          "default: on GB300 the separate combine measured faster")
     args = ap.parse_args()
+    if args.config is not None:
+        args.workload = moe_inputs.CONFIG_ORDER[args.config - 1]
     assert args.warmup >= 3, "at least 3 warm-up steps"
     cfg = moe_inputs.get_config(args.workload)
     if args.workloads is None:

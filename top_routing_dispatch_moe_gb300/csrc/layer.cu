@@ -5,10 +5,14 @@
 // copies overlapped with the layer.
 //
 // Host code only: every step is one of the library's own entry points, enqueued on the caller's stream over
-// intermediates laid out in one caller-provided workspace. Nothing here allocates device memory; the host variant
+// intermediates laid out in one caller-provided workspace. Each step, and each batch of the host variant, is an NVTX
+// range ("moe.router", "moe.dispatch", "moe.up_gate", "moe.down", "moe.shared", "moe.combine", "moe.batch"), so that
+// a profiler can attribute the launches (e.g. ncu --nvtx --nvtx-include "moe.up_gate/"); without a profiler attached
+// the ranges cost a branch each. Nothing here allocates device memory; the host variant
 // creates two copy streams and a few events per call and releases them before it returns (the runtime frees them
 // once the work they order has completed).
 #include <vector>
+#include <nvtx3/nvToolsExt.h>
 #include "common.cuh"
 
 namespace moe {
@@ -133,6 +137,12 @@ int check_desc(const moe_layer_desc* d, const char* who) {
 template <class T>
 T* at(void* ws, size_t off) { return reinterpret_cast<T*>(static_cast<char*>(ws) + off); }
 
+// One NVTX range for the lifetime of the object (the enqueueing of one step on the host).
+struct Range {
+    explicit Range(const char* name) { nvtxRangePushA(name); }
+    ~Range() { nvtxRangePop(); }
+};
+
 moe_layer_views views_at(const moe_layer_desc& d, const LayerLayout& L, void* ws) {
     moe_layer_views v{};
     v.logits = at<float>(ws, L.logits);
@@ -177,58 +187,70 @@ int forward_chain(const moe_layer_desc& d, const LayerLayout& L, const void* x, 
     const moe_layer_views v = views_at(d, L, ws);
     const int rows = (int)L.rows;
     const bool ec = d.routing == MOE_ROUTING_EXPERT_CHOICE, sk = d.routing == MOE_ROUTING_SINKHORN;
-    int rc = moe_router_packed(x, d.w_r_packed, d.bias, d.T, d.h, d.E, d.k, d.dtype,
-                               sk ? MOE_GATING_SOFTMAX : d.gating, d.alpha, v.logits, v.topk_ids, v.gates, v.counts,
-                               v.f, v.P, v.aux, at<void>(ws, L.router_ws), L.router_ws_bytes, s);
-    if (rc) return rc;
-    if (sk) {                                // balanced selection: the Sinkhorn log column scalings as a bias
-        rc = moe_sinkhorn_bias(v.logits, d.T, d.E, d.sinkhorn_iters > 0 ? d.sinkhorn_iters : 16, v.sel_bias,
-                               at<void>(ws, L.sk_ws), L.sk_ws_bytes, s);
+    const bool fused_shared = d.packed_shared && d.dtype == MOE_BF16 && d.payload == MOE_PAYLOAD_DTYPE;
+    int rc;
+    {
+        Range r("moe.router");
+        rc = moe_router_packed(x, d.w_r_packed, d.bias, d.T, d.h, d.E, d.k, d.dtype, sk ? MOE_GATING_SOFTMAX : d.gating,
+                               d.alpha, v.logits, v.topk_ids, v.gates, v.counts, v.f, v.P, v.aux,
+                               at<void>(ws, L.router_ws), L.router_ws_bytes, s);
         if (rc) return rc;
-        rc = moe_router_from_logits(v.logits, v.sel_bias, d.T, d.E, d.k, MOE_GATING_SOFTMAX_SELBIAS, d.alpha,
-                                    v.topk_ids, v.gates, v.counts, v.f, v.P, v.aux, at<void>(ws, L.rl_ws),
-                                    L.rl_ws_bytes, s);
-        if (rc) return rc;
-    }
-    if (ec) {
-        rc = moe_expert_choice_route(v.logits, d.T, d.E, d.capacity, v.ec_tokens, v.ec_gates, v.ec_slot,
-                                     at<void>(ws, L.ec_ws), L.ec_ws_bytes, s);
-        if (rc) return rc;
-        rc = moe_expert_choice_dispatch(x, v.ec_tokens, d.T, d.h, d.E, d.capacity, d.dtype, v.buf, v.tile_sched, s);
-    } else if (d.payload == MOE_PAYLOAD_FP8) {
-        rc = moe_dispatch_fp8(x, v.topk_ids, d.T, d.h, d.E, d.k, d.capacity, d.num_ranks, v.buf8, v.scales, v.offsets,
-                              v.kept_counts, v.dest_row, v.drop_mask, v.src_token, v.src_slot, v.rank_counts,
-                              v.rank_offsets, v.tile_sched, at<void>(ws, L.disp_ws), L.disp_ws_bytes, s);
-        if (rc) return rc;
-        rc = moe_dequant_fp8(v.buf8, v.scales, rows, d.h, v.buf, s);   // the receive side, then the bf16 GEMMs
-    } else {
-        rc = moe_dispatch(x, v.topk_ids, d.T, d.h, d.E, d.k, d.capacity, d.num_ranks, d.dtype, v.buf, v.offsets,
-                          v.kept_counts, v.dest_row, v.drop_mask, v.src_token, v.src_slot, v.rank_counts,
-                          v.rank_offsets, v.tile_sched, at<void>(ws, L.disp_ws), L.disp_ws_bytes, s);
-    }
-    if (rc) return rc;
-    if (d.packed_shared && d.dtype == MOE_BF16 && d.payload == MOE_PAYLOAD_DTYPE) {
-        rc = moe_expert_up_gate_shared(v.buf, v.tile_sched, d.packed_w, d.E, d.h, d.F, rows, x, d.T, d.packed_shared,
-                                       v.act_shared, d.dtype, v.act, s);
-        if (rc) return rc;
-        rc = moe_expert_down_shared(v.act, v.tile_sched, d.packed_w, d.E, d.h, d.F, rows, v.act_shared, d.T,
-                                    d.packed_shared, v.out_shared, d.dtype, v.eout, s);
-        if (rc) return rc;
-    } else {
-        rc = moe_expert_up_gate(v.buf, v.tile_sched, d.packed_w, d.E, d.h, d.F, rows, d.dtype, v.act, s);
-        if (rc) return rc;
-        rc = moe_expert_down(v.act, v.tile_sched, d.packed_w, d.E, d.h, d.F, rows, d.dtype, v.eout, s);
-        if (rc) return rc;
-        if (d.packed_shared) {
-            int32_t* sh_sched = at<int32_t>(ws, L.sh_sched);
-            rc = moe_dense_tile_sched(d.T, sh_sched, s);
+        if (sk) {                            // balanced selection: the Sinkhorn log column scalings as a bias
+            rc = moe_sinkhorn_bias(v.logits, d.T, d.E, d.sinkhorn_iters > 0 ? d.sinkhorn_iters : 16, v.sel_bias,
+                                   at<void>(ws, L.sk_ws), L.sk_ws_bytes, s);
             if (rc) return rc;
-            rc = moe_expert_up_gate(x, sh_sched, d.packed_shared, 1, d.h, d.F, d.T, d.dtype, v.act_shared, s);
+            rc = moe_router_from_logits(v.logits, v.sel_bias, d.T, d.E, d.k, MOE_GATING_SOFTMAX_SELBIAS, d.alpha,
+                                        v.topk_ids, v.gates, v.counts, v.f, v.P, v.aux, at<void>(ws, L.rl_ws),
+                                        L.rl_ws_bytes, s);
             if (rc) return rc;
-            rc = moe_expert_down(v.act_shared, sh_sched, d.packed_shared, 1, d.h, d.F, d.T, d.dtype, v.out_shared, s);
+        }
+        if (ec) {
+            rc = moe_expert_choice_route(v.logits, d.T, d.E, d.capacity, v.ec_tokens, v.ec_gates, v.ec_slot,
+                                         at<void>(ws, L.ec_ws), L.ec_ws_bytes, s);
             if (rc) return rc;
         }
     }
+    {
+        Range r("moe.dispatch");
+        if (ec) {
+            rc = moe_expert_choice_dispatch(x, v.ec_tokens, d.T, d.h, d.E, d.capacity, d.dtype, v.buf, v.tile_sched,
+                                            s);
+        } else if (d.payload == MOE_PAYLOAD_FP8) {
+            rc = moe_dispatch_fp8(x, v.topk_ids, d.T, d.h, d.E, d.k, d.capacity, d.num_ranks, v.buf8, v.scales,
+                                  v.offsets, v.kept_counts, v.dest_row, v.drop_mask, v.src_token, v.src_slot,
+                                  v.rank_counts, v.rank_offsets, v.tile_sched, at<void>(ws, L.disp_ws),
+                                  L.disp_ws_bytes, s);
+            if (!rc) rc = moe_dequant_fp8(v.buf8, v.scales, rows, d.h, v.buf, s);   // receive side, then bf16 GEMMs
+        } else {
+            rc = moe_dispatch(x, v.topk_ids, d.T, d.h, d.E, d.k, d.capacity, d.num_ranks, d.dtype, v.buf, v.offsets,
+                              v.kept_counts, v.dest_row, v.drop_mask, v.src_token, v.src_slot, v.rank_counts,
+                              v.rank_offsets, v.tile_sched, at<void>(ws, L.disp_ws), L.disp_ws_bytes, s);
+        }
+        if (rc) return rc;
+    }
+    {
+        Range r("moe.up_gate");
+        rc = fused_shared ? moe_expert_up_gate_shared(v.buf, v.tile_sched, d.packed_w, d.E, d.h, d.F, rows, x, d.T,
+                                                      d.packed_shared, v.act_shared, d.dtype, v.act, s)
+                          : moe_expert_up_gate(v.buf, v.tile_sched, d.packed_w, d.E, d.h, d.F, rows, d.dtype, v.act, s);
+        if (rc) return rc;
+    }
+    {
+        Range r("moe.down");
+        rc = fused_shared ? moe_expert_down_shared(v.act, v.tile_sched, d.packed_w, d.E, d.h, d.F, rows, v.act_shared,
+                                                   d.T, d.packed_shared, v.out_shared, d.dtype, v.eout, s)
+                          : moe_expert_down(v.act, v.tile_sched, d.packed_w, d.E, d.h, d.F, rows, d.dtype, v.eout, s);
+        if (rc) return rc;
+    }
+    if (d.packed_shared && !fused_shared) {  // the shared expert as a dense group of T rows
+        Range r("moe.shared");
+        int32_t* sh_sched = at<int32_t>(ws, L.sh_sched);
+        rc = moe_dense_tile_sched(d.T, sh_sched, s);
+        if (!rc) rc = moe_expert_up_gate(x, sh_sched, d.packed_shared, 1, d.h, d.F, d.T, d.dtype, v.act_shared, s);
+        if (!rc) rc = moe_expert_down(v.act_shared, sh_sched, d.packed_shared, 1, d.h, d.F, d.T, d.dtype, v.out_shared, s);
+        if (rc) return rc;
+    }
+    Range r("moe.combine");
     if (ec)
         return moe_expert_choice_combine(v.eout, v.ec_slot, v.ec_gates, v.out_shared, d.T, d.h, d.E, d.capacity,
                                          d.dtype, y, s);
@@ -332,7 +354,10 @@ extern "C" int moe_layer_forward_host(const moe_layer_desc* desc, int n_batches,
         if (e == cudaSuccess && y_free[b]) e = cudaStreamWaitEvent(s, y_free[b], 0);
         if (e != cudaSuccess)
             return set_error(MOE_ERR_CUDA, "moe_layer_forward_host: batch %d copy in: %s", i, cudaGetErrorString(e));
-        if (int rc = forward_chain(*desc, L, xd, yd, ws, stream)) return rc;
+        {
+            Range r("moe.batch");
+            if (int rc = forward_chain(*desc, L, xd, yd, ws, stream)) return rc;
+        }
         e = cudaEventRecord(done, s);
         if (e == cudaSuccess) e = cudaStreamWaitEvent(o.d2h, done, 0);
         if (e == cudaSuccess) e = cudaMemcpyAsync(y_host[i], yd, bytes, cudaMemcpyDeviceToHost, o.d2h);
