@@ -327,7 +327,8 @@ int moe_expert_down_combine(const void* act, const int32_t* tile_sched, const vo
  *   overlap the layer working on its neighbours on `stream` (two device buffers for x and two for y inside the
  *   workspace; a buffer is refilled only after the layer or the copy that last read it has finished). `stream`
  *   then waits for the last copy: once `stream` has been synchronised, every y_host[i] is written. Neither call
- *   waits for the host.
+ *   waits for the host. moe_layer_forward only launches kernels on `stream` and may be captured into a CUDA graph
+ *   (after one call outside the capture on the device); moe_layer_forward_host creates streams and may not.
  *   desc: the layer's sizes, dtype, gating (MOE_GATING_SOFTMAX, _SOFTMAX_RENORM or _SIGMOID_BIAS_RENORM), alpha,
  *     capacity (0: dropless) and num_ranks as for moe_router / moe_dispatch, routing, payload (FP8: bf16, token
  *     routing, h % 128 == 0), sinkhorn_iters, and its device-resident parameters:

@@ -133,3 +133,27 @@ def test_layer_forward_host_rejects_pageable_buffers():
         moe.moe_layer_forward_host(desc, [x_pageable], [y_pinned], ws)
     assert err.value.code == moe.MOE_ERR_INVALID_ARG
     assert "page-locked" in str(err.value)
+
+
+@pytest.mark.parametrize("name,over", [CASES[0], CASES[2], CASES[6]])
+def test_layer_forward_captures_into_a_cuda_graph(name, over):
+    """moe_layer_forward only enqueues kernels on the caller's stream (no host synchronisation, no allocation), so
+    it can be captured into a CUDA graph: replays give the eager call's bits."""
+    import torch
+    from top_routing_dispatch_moe_gb300 import moe
+    cfg, layer, x = _layer(name, over)
+    desc = layer.native_desc()
+    ws = moe._bytes_tensor(moe.moe_layer_workspace_size(desc), x.device)
+    y_ref = torch.empty_like(x)
+    moe.moe_layer_forward(desc, x, y_ref, ws)           # eager (also sets the kernels' attributes up)
+    torch.cuda.synchronize()
+    y = torch.zeros_like(x)
+    s = torch.cuda.Stream()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=s):
+        moe.moe_layer_forward(desc, x, y, ws, stream=s)
+    for _ in range(2):
+        g.replay()
+    torch.cuda.synchronize()
+    assert moe.moe_check_device_error() == moe.MOE_OK, moe.moe_last_error_string()
+    assert torch.equal(_bits(y), _bits(y_ref))
