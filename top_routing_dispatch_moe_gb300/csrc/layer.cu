@@ -11,6 +11,7 @@
 // the ranges cost a branch each. Nothing here allocates device memory; the host variant
 // creates two copy streams and a few events per call and releases them before it returns (the runtime frees them
 // once the work they order has completed).
+#include <stdio.h>
 #include <vector>
 #include <nvtx3/nvToolsExt.h>
 #include "common.cuh"
@@ -341,34 +342,47 @@ extern "C" int moe_layer_forward_host(const moe_layer_desc* desc, int n_batches,
     if (e != cudaSuccess) return set_error(MOE_ERR_CUDA, "moe_layer_forward_host: start: %s", cudaGetErrorString(e));
     cudaEvent_t x_free[2] = {nullptr, nullptr};    // the layer has finished reading x buffer b
     cudaEvent_t y_free[2] = {nullptr, nullptr};    // the copy out of y buffer b has finished
+    cudaEvent_t last_in = nullptr;                 // the last copy in that was issued
+    // `stream` waits for every copy issued so far, on success and on every error path alike, so that a caller who
+    // synchronises `stream` may then reuse or free the host buffers
+    auto join = [&]() {
+        cudaError_t j = cudaSuccess;
+        for (cudaEvent_t ev : {last_in, y_free[0], y_free[1]})
+            if (ev && j == cudaSuccess) j = cudaStreamWaitEvent(s, ev, 0);
+        return j;
+    };
+    auto fail = [&](int code, int batch, const char* step, cudaError_t err) {
+        join();
+        char inner[512];                     // the failing call's own message (set_error rewrites that buffer)
+        snprintf(inner, sizeof(inner), "%s", err == cudaSuccess ? moe_last_error_string() : cudaGetErrorString(err));
+        return set_error(code, "moe_layer_forward_host: batch %d %s: %s", batch, step, inner);
+    };
     for (int i = 0; i < n_batches; ++i) {
         const int b = i & 1;
         void* xd = at<void>(ws, L.x_dev[b]);
         void* yd = at<void>(ws, L.y_dev[b]);
         cudaEvent_t x_in = o.event(), done = o.event(), out = o.event();
-        MOE_REQUIRE(x_in && done && out, MOE_ERR_CUDA, "moe_layer_forward_host: event creation failed");
+        if (!x_in || !done || !out) return fail(MOE_ERR_CUDA, i, "event creation", cudaErrorMemoryAllocation);
         if (x_free[b]) e = cudaStreamWaitEvent(o.h2d, x_free[b], 0);
         if (e == cudaSuccess) e = cudaMemcpyAsync(xd, x_host[i], bytes, cudaMemcpyHostToDevice, o.h2d);
         if (e == cudaSuccess) e = cudaEventRecord(x_in, o.h2d);
+        if (e == cudaSuccess) last_in = x_in;
         if (e == cudaSuccess) e = cudaStreamWaitEvent(s, x_in, 0);
         if (e == cudaSuccess && y_free[b]) e = cudaStreamWaitEvent(s, y_free[b], 0);
-        if (e != cudaSuccess)
-            return set_error(MOE_ERR_CUDA, "moe_layer_forward_host: batch %d copy in: %s", i, cudaGetErrorString(e));
+        if (e != cudaSuccess) return fail(MOE_ERR_CUDA, i, "copy in", e);
         {
             Range r("moe.batch");
-            if (int rc = forward_chain(*desc, L, xd, yd, ws, stream)) return rc;
+            if (int rc = forward_chain(*desc, L, xd, yd, ws, stream)) return fail(rc, i, "layer", cudaSuccess);
         }
         e = cudaEventRecord(done, s);
         if (e == cudaSuccess) e = cudaStreamWaitEvent(o.d2h, done, 0);
         if (e == cudaSuccess) e = cudaMemcpyAsync(y_host[i], yd, bytes, cudaMemcpyDeviceToHost, o.d2h);
         if (e == cudaSuccess) e = cudaEventRecord(out, o.d2h);
-        if (e != cudaSuccess)
-            return set_error(MOE_ERR_CUDA, "moe_layer_forward_host: batch %d copy out: %s", i, cudaGetErrorString(e));
+        if (e != cudaSuccess) return fail(MOE_ERR_CUDA, i, "copy out", e);
         x_free[b] = done;
         y_free[b] = out;
     }
-    for (int b = 0; b < 2; ++b)
-        if (y_free[b] && (e = cudaStreamWaitEvent(s, y_free[b], 0)) != cudaSuccess)
-            return set_error(MOE_ERR_CUDA, "moe_layer_forward_host: join: %s", cudaGetErrorString(e));
+    if ((e = join()) != cudaSuccess)
+        return set_error(MOE_ERR_CUDA, "moe_layer_forward_host: join: %s", cudaGetErrorString(e));
     return MOE_OK;
 }
