@@ -323,9 +323,9 @@ int moe_expert_down_combine(const void* act, const int32_t* tile_sched, const vo
  *   moe_layer_forward_host runs it on n_batches batches that live in page-locked host memory (cudaHostAlloc or
  *   cudaHostRegister), x_host[i] [T,h] -> y_host[i] [T,h]: one host->device copy of each x and one device->host
  *   copy of each y (cudaMemcpyAsync), on two streams that the call creates and releases (the first copy waits for
- *   the work already enqueued on `stream`), so that batch i's copies
- *   overlap the layer working on its neighbours on `stream` (two device buffers for x and two for y inside the
- *   workspace; a buffer is refilled only after the layer or the copy that last read it has finished). `stream`
+ *   the work already enqueued on `stream`), so that batch i's copies overlap the layer working on its neighbours on
+ *   `stream` (two device buffers for x and two for y inside the workspace; a buffer is refilled only after the
+ *   layer or the copy that last read it has finished). `stream`
  *   then waits for the last copy: once `stream` has been synchronised, every y_host[i] is written. Neither call
  *   waits for the host. moe_layer_forward only launches kernels on `stream` and may be captured into a CUDA graph
  *   (after one call outside the capture on the device); moe_layer_forward_host creates streams and may not.
@@ -341,9 +341,10 @@ int moe_expert_down_combine(const void* act, const int32_t* tile_sched, const vo
  *     last forward left them.
  *   Errors: MOE_ERR_INVALID_ARG for a null desc or pointer, n_batches < 0, a host buffer that is not
  *     page-locked, or what the chained calls reject; MOE_ERR_UNSUPPORTED for MOE_GATING_SOFTMAX_SELBIAS, a dtype,
- *     routing or payload outside the enums, or the FP8 payload with fp32 or without token routing; MOE_ERR_WORKSPACE if ws_bytes is short; MOE_ERR_CUDA. The arguments are checked
- *     before anything is enqueued; a call that fails later returns the failing step's status with the steps
- *     before it already enqueued.
+ *     routing or payload outside the enums, or the FP8 payload with fp32 or without token routing;
+ *     MOE_ERR_WORKSPACE if ws_bytes is short; MOE_ERR_CUDA. The arguments are checked before anything is
+ *     enqueued; a call that fails later returns the failing step's status with the steps before it already
+ *     enqueued (the host variant then still makes `stream` wait for every copy it issued).
  * ------------------------------------------------------------------------------------------------- */
 enum moe_routing { MOE_ROUTING_TOKEN = 0, MOE_ROUTING_EXPERT_CHOICE = 1, MOE_ROUTING_SINKHORN = 2 };
 enum moe_payload { MOE_PAYLOAD_DTYPE = 0, MOE_PAYLOAD_FP8 = 1 };
@@ -373,6 +374,7 @@ typedef struct moe_layer_views {
     float* P;                   /* [E] */
     float* aux;                 /* [1] */
     void* buf;                  /* [rows,h] dtype */
+    /* offsets .. rank_offsets: token and Sinkhorn routing (NULL for expert choice) */
     int32_t* offsets;           /* [E+1] */
     int32_t* kept_counts;       /* [E] */
     int32_t* dest_row;          /* [T,k] */
